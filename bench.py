@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A8 GEMM hot path on one GB300 (or N replicas).
+
+Workload: the Llama-3-8B decode GEMMs with g128 progressive group
+quantization -- M in {1, 8, 32, 64, 128, 256} tokens x the four linear layers
+(qkv 6144x4096, o 4096x4096, gate_up 28672x4096, down 4096x14336).  One step
+runs, for each of the 24 (M, layer) points, the per-token activation
+quantization followed by the W4A8 GEMM with its fp16 epilogue; weights are
+quantized and packed once at load time, outside the timed region.  Inputs are
+seeded synthetic data (random-init weights with outlier input channels,
+N(0,1) activations with outlier channels).
+
+Reported: TOPS = sum 2*M*N*K / step time (whole job over all ranks), the
+per-point roofline fractions, the dominant kernel's roofline against the
+measured HBM peak, an end-to-end figure through the public API with
+host<->device copies, SM clocks sampled during the timed region, and the CPU
+oracle timed on a bounded sample (``cpu_baseline``).
+``--impl reference`` times the CPU oracle alone as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W4A8-g128 GEMM TOPS & % of roofline (HBM / INT8 tensor) on 8B shapes, m=1–4096"
+WORKLOAD = ("Llama-3-8B decode GEMMs g128: M in {1,8,32,64,128,256} x "
+            "{qkv 6144x4096, o 4096x4096, gate_up 28672x4096, down 4096x14336}")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--copies", type=int, default=5, help="packed-weight copies rotated to defeat L2")
+    ap.add_argument("--point-reps", type=int, default=7)
+    ap.add_argument("--cpu-rows", type=int, default=192, help="weight rows in the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", default="qkv,o,gate_up,down")
+    ap.add_argument("--ms", default="1,8,32,64,128,256")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_pci_id(torch, dev: int) -> str | None:
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------- CPU oracle --
+def oracle_sample(layers, Ms, rows: int, seed_base: int = 1):
+    """Inputs of the bounded oracle sample: the first `rows` weight rows of
+    every layer, quantized by the oracle, and the activations of every point."""
+    import oracle
+    from w4a8_quantized_serving_qoq_gb300 import synthetic
+    sample = []
+    for layer in layers:
+        s = synthetic.layer_seed(1, layer)
+        W = synthetic.weights(layer.N, layer.K, s, 0.02, 2)[:rows]
+        wq = oracle.quantize_weights_group(np.ascontiguousarray(W), 128)
+        for M in Ms:
+            X = synthetic.activations(M, layer.K, s, 4)
+            sample.append((layer, M, wq, X))
+    return sample
+
+
+def oracle_pass(sample):
+    """One pass of the oracle over the sample; returns (seconds, ops)."""
+    import oracle
+    ops = 0
+    t0 = time.perf_counter()
+    for layer, M, wq, X in sample:
+        Qx, sx, _ = oracle.quant_act(X)
+        acc = oracle.gemm_i32_group(Qx, wq["q4"], wq["s_g"], wq["z"])
+        oracle.epilogue_f64(acc, sx, wq["s_w"])
+        ops += 2 * M * wq["q4"].shape[0] * layer.K
+    return time.perf_counter() - t0, ops
+
+
+def run_reference(args, layers, Ms):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    rows = 32
+    sample = oracle_sample(layers, Ms, rows)
+    for _ in range(args.warmup):
+        oracle_pass(sample)
+    tot_t, tot_ops = 0.0, 0
+    for _ in range(args.steps):
+        dt, ops = oracle_pass(sample)
+        tot_t += dt
+        tot_ops += ops
+    tops = tot_ops / tot_t / 1e12
+    desc = (f"oracle (plain single-threaded C) on the first {rows} weight rows of each layer, "
+            f"all 24 (M, layer) points: quant_act + int32 GEMM + fp64 epilogue")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": desc},
+        "cpu_baseline": {"value": tops, "unit": "TOPS", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": tops, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ GPU path --
+def main():
+    args = parse_args()
+    from w4a8_quantized_serving_qoq_gb300 import synthetic
+    layer_by_name = {l.name: l for l in synthetic.LLAMA3_8B}
+    layers = [layer_by_name[n] for n in args.layers.split(",")]
+    Ms = [int(m) for m in args.ms.split(",")]
+    if args.impl == "reference":
+        run_reference(args, layers, Ms)
+        return
+
+    import torch
+    import w4a8_quantized_serving_qoq_gb300 as qoq
+    from w4a8_quantized_serving_qoq_gb300 import roofline
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    qoq.load()
+    peaks, peaks_src = load_peaks()
+    bw = peaks["hbm_gbs"] * 1e9
+    p16 = peaks["bf16_tflops"] * 1e12  # fp16 dense tensor rate = bf16 rate
+    stream = torch.cuda.current_stream()
+
+    # ---- load time: quantize + pack weights on the device, make copies ----
+    weights = {}
+    for layer in layers:
+        s = synthetic.layer_seed(1, layer)
+        W = torch.from_numpy(synthetic.weights(layer.N, layer.K, s, 0.02, 2)).to(dev)
+        wq = qoq.qoq_quantize_weights(W, 128)
+        packed = qoq.qoq_pack_weights(wq["q4"], wq["s_g"], wq["z"], 128)
+        copies = [packed] + [packed.clone() for _ in range(args.copies - 1)]
+        weights[layer.name] = (copies, wq["s_w"])
+        del W, wq
+    points = []
+    ws_max = 256
+    for M in Ms:
+        for layer in layers:
+            s = synthetic.layer_seed(1, layer)
+            X = torch.from_numpy(synthetic.activations(M, layer.K, s, 4)).to(dev)
+            Qx = torch.empty((M, layer.K), dtype=torch.int8, device=dev)
+            sx = torch.empty((M,), dtype=torch.float16, device=dev)
+            O = torch.empty((M, layer.N), dtype=torch.float16, device=dev)
+            ws_max = max(ws_max, qoq.qoq_gemm_workspace_bytes(M, layer.N, layer.K, 128))
+            points.append(dict(layer=layer, M=M, X=X, Qx=Qx, sx=sx, O=O))
+    ws = qoq.new_workspace(ws_max, dev)
+    torch.cuda.synchronize()
+
+    def run_point(i, pt, copy_idx):
+        layer = pt["layer"]
+        copies, s_w = weights[layer.name]
+        qoq.qoq_quant_act(pt["X"], pt["Qx"], pt["sx"], None, with_t=False)
+        qoq.qoq_w4a8_gemm(pt["Qx"], pt["sx"], None, copies[copy_idx % len(copies)], s_w, layer.N,
+                          layer.K, 128, O=pt["O"], workspace=ws)
+
+    def step():
+        for i, pt in enumerate(points):
+            run_point(i, pt, i)
+
+    # eager warm-up (sets kernel attributes before capture), then capture one step
+    step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(gpu_pci_id(torch, local_rank))
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_step = ev0.elapsed_time(ev1) / args.steps
+    if dist:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    ops_step = sum(roofline.gemm_ops(p["M"], p["layer"].N, p["layer"].K) for p in points)
+    tops = world * ops_step / (ms_step * 1e-3) / 1e12
+
+    # ---- per-point kernel times (L2 flushed before each launch) ----
+    flush = torch.empty(int(2 * 129e6) // 4 * 4, dtype=torch.uint8, device=dev)
+    pt_rows = []
+    gemm_ms_total, bytes_total = 0.0, 0
+    for i, pt in enumerate(points):
+        layer, M = pt["layer"], pt["M"]
+        copies, s_w = weights[layer.name]
+        tg, tq = [], []
+        for r in range(args.point_reps):
+            flush.fill_(r & 0xFF)
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record(stream)
+            qoq.qoq_quant_act(pt["X"], pt["Qx"], pt["sx"], None, with_t=False)
+            b.record(stream)
+            qoq.qoq_w4a8_gemm(pt["Qx"], pt["sx"], None, copies[r % len(copies)], s_w, layer.N, layer.K,
+                              128, O=pt["O"], workspace=ws)
+            c.record(stream)
+            torch.cuda.synchronize()
+            tq.append(a.elapsed_time(b))
+            tg.append(b.elapsed_time(c))
+        t_g = statistics.median(tg)
+        t_q = statistics.median(tq)
+        nbytes = roofline.w4a8_bytes(M, layer.N, layer.K)
+        nops = roofline.gemm_ops(M, layer.N, layer.K)
+        troof = roofline.roof_time(M, layer.N, layer.K, bw, p16)
+        gemm_ms_total += t_g
+        bytes_total += nbytes
+        pt_rows.append({
+            "layer": layer.name, "M": M, "gemm_us": round(1e3 * t_g, 2), "quant_us": round(1e3 * t_q, 2),
+            "TOPS": round(nops / (t_g * 1e-3) / 1e12, 2), "GBs": round(nbytes / (t_g * 1e-3) / 1e9, 1),
+            "bound": roofline.bound(M, layer.N, layer.K, bw, p16),
+            "roof_frac": round(troof / (t_g * 1e-3), 3),
+        })
+    del flush
+    achieved_gbs = bytes_total / (gemm_ms_total * 1e-3) / 1e9
+    troof_sum = sum(roofline.roof_time(p["M"], p["layer"].N, p["layer"].K, bw, p16) for p in points)
+
+    # ---- end to end through the public API: host buffers, copies timed ----
+    e2e = None
+    if not args.no_e2e:
+        hostX = [p["X"].cpu().pin_memory() for p in points]
+        hostO = [torch.empty(p["O"].shape, dtype=torch.float16).pin_memory() for p in points]
+        h2d = sum(h.numel() * 2 for h in hostX)
+        d2h = sum(h.numel() * 2 for h in hostO)
+        e2e_steps = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            for i, pt in enumerate(points):
+                pt["X"].copy_(hostX[i], non_blocking=True)
+                run_point(i, pt, i)
+                hostO[i].copy_(pt["O"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / e2e_steps
+        e2e = {"value": world * ops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "path": "Python binding -> C ABI per call (no CUDA graph), pinned host buffers"}
+
+    # ---- CPU oracle on a bounded sample ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = oracle_sample(layers, Ms, args.cpu_rows)
+        dt, ops = oracle_pass(sample)
+        cpu = {"value": ops / dt / 1e12, "unit": "TOPS", "cores": 1, "kind": "oracle",
+               "seconds": round(dt, 2),
+               "sample": (f"first {args.cpu_rows} weight rows of each layer at all 24 (M, layer) points; "
+                          f"quant_act + int32 GEMM + fp64 epilogue, plain single-threaded C "
+                          f"({os.cpu_count()} host cores present)")}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "s8 x u4 -> exact i32 (fp16 tensor-core MMA), fp16 out", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "group": 128, "parallelism": f"replicas{world}",
+                   "cuda_graph": True, "l2": f"inputs larger than L2: {args.copies} packed-weight copies "
+                   f"rotated ({sum(len(c) * c[0].numel() for c, _ in weights.values()) / 1e6:.0f} MB)"},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peaks_src, "kernel": "w4a8_gemm_kernel",
+                     "time_weighted_roofline_frac": troof_sum / (gemm_ms_total * 1e-3),
+                     "tensor_peak_tflops": peaks["bf16_tflops"]},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * len(points) * args.steps,
+        "clocks": clk,
+        "points": pt_rows,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

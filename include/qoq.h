@@ -1,0 +1,204 @@
+/*
+ * qoq.h -- C ABI of the GB300 (sm_103a) W4A8 GEMM library (libqoq.so).
+ *
+ * The library computes the hot path of the QoQ / QServe method: a GEMM whose
+ * weights are 4-bit under progressive group quantization and whose
+ * activations are 8-bit per-token, with an fp16 output:
+ *
+ *   O[m,n] = s_x[m] * s_w[n] * sum_k Qx[m,k] * (q4[n,k] - z[n,k/128]) * s_g[n,k/128]
+ *
+ * Page references (web pages on QServe / QoQ):
+ *   [QS-summary] "QServe: W4A8KV4 Quantization and System Co-design for
+ *                Efficient LLM Serving" (papercache.org summary).
+ *   [QS-review]  "QServe：把 W4A8KV4 的理论收益做成实测吞吐的量化—系统协同设计"
+ *                (zenmind.me review).
+ *
+ * Conventions for every entry point:
+ *  - Every tensor pointer is DEVICE memory owned by the caller; the library
+ *    never allocates, frees or synchronizes the device (except
+ *    qoq_workspace_status, which synchronizes the given stream).
+ *  - fp16 tensors are passed as uint16_t IEEE binary16 bit patterns.
+ *  - Matrices are row-major and dense: X, Qx [M][K]; W, q4 [N][K]; O [M][N].
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously.  Calls are stateless and thread-safe
+ *    as long as concurrent GEMMs use distinct workspaces.
+ *  - Arguments are validated before any launch; on a validation error
+ *    nothing is enqueued.  Errors never throw across the ABI.
+ *  - Return value: a qoq_status code.
+ */
+#ifndef QOQ_H_
+#define QOQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qoq_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    QOQ_OK = 0,
+    QOQ_ERR_INVALID_ARG = 1, /* null pointer, non-positive size */
+    QOQ_ERR_UNSUPPORTED = 2, /* N or K not a multiple of 128, group not 0/128 */
+    QOQ_ERR_MISALIGNED = 3,  /* a pointer breaks the alignment stated below */
+    QOQ_ERR_WORKSPACE = 4,   /* workspace smaller than qoq_gemm_workspace_bytes */
+    QOQ_ERR_CUDA = 5,        /* a CUDA launch / runtime call failed */
+    QOQ_ERR_TIMEOUT = 6,     /* a device-side bounded wait expired (status word) */
+    QOQ_ERR_DEVICE = 7       /* packed weights do not match the call or hold illegal codes */
+} qoq_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *qoq_status_string(int status);
+
+/* Library / packed-format version (packed buffers carry it in their header). */
+int qoq_version(void);
+
+/*
+ * qoq_quantize_weights -- progressive group quantization of fp16 weights on
+ * the device ([QS-summary] "渐进式组量化" eq. 4/5 and "保护性量化范围";
+ * [QS-review] 3.1).  One-time, load-time operation.
+ *   group == 128: step 1, per output row n: s_w[n] = fp16(max_k|W[n,k]| / 119)
+ *     (1.0 for an all-zero row), q8 = clamp(rne(W / s_w), -119, 119);
+ *     step 2, per group of 128 k: lo = min(0, min q8), hi = max(0, max q8),
+ *     s_g = max(1, ceil((hi - lo) / 15)), z = clamp(rne(-lo / s_g), 0, 15),
+ *     q4 = clamp(rne(q8 / s_g) + z, 0, 15).  rne = round half to even;
+ *     divisions of floats are IEEE fp32.
+ *   group == 0 (per-channel W4, [QS-summary] "逐通道W4A8 GEMM中的快速反量化"):
+ *     lo/hi = min/max(0, W[n,:]), s_w[n] = fp16((hi - lo) / 15) (1.0 if 0),
+ *     z[n] = clamp(rne(-lo / s_w), 0, 15), q4 = clamp(rne(W / s_w) + z, 0, 15).
+ * W   : fp16 [N][K].              q4 : uint8 [N][K], one code (0..15) per byte.
+ * s_g : uint8 [N][K/128] (group==128; ignored and may be NULL for group==0).
+ * z   : uint8 [N][K/128] (group==128) or [N] (group==0).
+ * s_w : fp16 [N].
+ * Requirements: N, K > 0; K % 128 == 0 for group 128.
+ */
+int qoq_quantize_weights(const uint16_t *W, int N, int K, int group, uint8_t *q4, uint8_t *s_g,
+                         uint8_t *z, uint16_t *s_w, qoq_stream_t stream);
+
+/* Bytes of the packed weight buffer for an N x K matrix (0 if unsupported). */
+size_t qoq_packed_weight_bytes(int N, int K, int group);
+
+/*
+ * qoq_pack_weights -- device-side reorder of integer codes into the GEMM's
+ * compute order ([QS-summary] "计算感知权重重排序"; [QS-review] 3.2: weights are
+ * static, so they are stored once in the order the main loop reads them).
+ * Layout of `packed` (qoq_packed_weight_bytes bytes, 16-byte aligned):
+ *   256-byte header (magic "QOQW", version, N, K, group, block size, count of
+ *   illegal codes), then (N/128) x (K/128) blocks, row-tile major: 8192 bytes
+ *   of 4-bit codes for 128 rows x 128 k, followed (group mode) by 256 bytes
+ *   of (s_g, z) byte pairs per row.  Within a block, 16-byte chunk
+ *   (p*128 + r), p = 0..3, holds row r, k = 32p..32p+31 as four 32-bit words;
+ *   word j covers k = 32p+8j+(0..7) and its byte b holds the code of
+ *   k = 8j+b (low nibble) and k = 8j+b+4 (high nibble).  Per-channel mode
+ *   appends z [N] (padded to 16 bytes).
+ * Codes that break the GEMM's byte-lane bounds (q4 > 15, z > 15, s_g > 17,
+ * or (q4 - z) * s_g outside [-128, 127]) are counted in the header; the GEMM
+ * refuses such a buffer with QOQ_ERR_DEVICE (reported via the status word).
+ * q4 [N][K] (16-byte aligned), s_g/z as in qoq_quantize_weights.
+ * Requirements: N % 128 == 0, K % 128 == 0, group in {0, 128}.
+ */
+int qoq_pack_weights(const uint8_t *q4, const uint8_t *s_g, const uint8_t *z, int N, int K,
+                     int group, void *packed, qoq_stream_t stream);
+
+/* Inverse of qoq_pack_weights (tests and checkpoint inspection). */
+int qoq_unpack_weights(const void *packed, int N, int K, int group, uint8_t *q4, uint8_t *s_g,
+                       uint8_t *z, qoq_stream_t stream);
+
+/*
+ * qoq_quant_act -- per-token symmetric INT8 activation quantization
+ * ([QS-review] 3.2 runtime precision map: every GEMM consumes INT8
+ * activations, quantized by the kernel before it).  Per row m:
+ *   s_x[m] = fp16(max_k |X[m,k]| / 127) (IEEE fp32 division, then round to
+ *   fp16); Qx = clamp(rne(X / s_x), -127, 127); an all-zero scale gives an
+ *   all-zero row; t_x[m] = sum_k Qx[m,k] (the t_X = X·1_k row sum of
+ *   [QS-summary] eq. 13, needed by the per-channel GEMM).  Inputs must be
+ *   finite.
+ * X fp16 [M][K], Qx int8 [M][K] (both 16-byte aligned), s_x fp16 [M],
+ * t_x int32 [M] or NULL.  Requirements: M, K > 0, K % 8 == 0.
+ */
+int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x,
+                  qoq_stream_t stream);
+
+/*
+ * Workspace bytes qoq_w4a8_gemm needs for this shape on the current device
+ * (>= 256: a status word plus, when K is split across CTAs, tile counters
+ * and int32 partial sums).  The workspace must be zero-filled once before
+ * first use (qoq_workspace_init); every call leaves it zero-filled again.
+ */
+size_t qoq_gemm_workspace_bytes(int M, int N, int K, int group);
+
+/* Zero-fill a workspace (enqueued on `stream`). */
+int qoq_workspace_init(void *workspace, size_t bytes, qoq_stream_t stream);
+
+/*
+ * qoq_w4a8_gemm -- the W4A8 GEMM with fused fp16 epilogue.
+ *   group == 128 ([QS-summary] "逐组W4A8 GEMM中的快速反量化"; [QS-review] 3.2):
+ *     acc[m,n] = sum_k Qx[m,k] * (q4[n,k] - z[n,k/128]) * s_g[n,k/128]  (exact int32)
+ *   group == 0 ([QS-summary] eq. 13, zero folded into the epilogue):
+ *     acc[m,n] = sum_k Qx[m,k] * q4[n,k] - z[n] * t_x[m]                 (exact int32)
+ *   O[m,n] = fp16_rn(fp32(acc) * s_x[m] * s_w[n])   (fp32 products, left to right)
+ * Qx int8 [M][K] (16-byte aligned); s_x fp16 [M]; t_x int32 [M] (group 0
+ * only, may be NULL for group 128); packed from qoq_pack_weights for the same
+ * N, K, group (16-byte aligned); s_w fp16 [N]; O fp16 [M][N]; workspace of
+ * ws_bytes >= qoq_gemm_workspace_bytes(M, N, K, group), 16-byte aligned.
+ * Requirements: M > 0, N % 128 == 0, K % 128 == 0, group in {0, 128}.
+ * Device-side failures (a bounded wait expiring, mismatched or illegal packed
+ * weights) do not fault: they set bits in the workspace status word, read by
+ * qoq_workspace_status.
+ */
+int qoq_w4a8_gemm(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const void *packed,
+                  const uint16_t *s_w, int M, int N, int K, int group, uint16_t *O,
+                  void *workspace, size_t ws_bytes, qoq_stream_t stream);
+
+/*
+ * qoq_w4a8_gemm_i32 -- same GEMM, but writes the exact int32 accumulators
+ * acc [M][N] (after the per-channel zero fold, before scaling) instead of O.
+ * Test / debugging entry point; s_x and s_w may be NULL.
+ */
+int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, int M, int N,
+                      int K, int group, int32_t *acc, void *workspace, size_t ws_bytes,
+                      qoq_stream_t stream);
+
+/*
+ * Options for qoq_w4a8_gemm_ex (tests and tuning).  Zero-initialised fields
+ * mean "automatic".
+ *   tokens_per_tile : 16, 32, 64 or 128 (MMA N per CTA), 0 = automatic.
+ *   k_splits        : CTAs sharing one output tile along K, 0 = automatic
+ *                     (clamped to K/128).
+ *   timeout_ns      : bound of every device-side wait, 0 = 2 s.
+ *   debug_flags     : bit 0 = the copy warp withholds the second stage, so
+ *                     the bounded waits expire (timeout path test).
+ *   acc_out         : if non-NULL, int32 accumulators are written here
+ *                     instead of O.
+ */
+typedef struct {
+    int tokens_per_tile;
+    int k_splits;
+    uint64_t timeout_ns;
+    uint32_t debug_flags;
+    int32_t *acc_out;
+} qoq_gemm_options;
+
+/* Workspace bytes for a GEMM run with the given options. */
+size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gemm_options *opt);
+
+int qoq_w4a8_gemm_ex(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x,
+                     const void *packed, const uint16_t *s_w, int M, int N, int K, int group,
+                     uint16_t *O, void *workspace, size_t ws_bytes, const qoq_gemm_options *opt,
+                     qoq_stream_t stream);
+
+/*
+ * qoq_workspace_status -- synchronizes `stream`, copies the workspace status
+ * word to *host_status, clears it on the device, and returns QOQ_OK,
+ * QOQ_ERR_TIMEOUT or QOQ_ERR_DEVICE according to the bits found
+ * (1 = a bounded wait expired, 2 = packed-weight header mismatch/illegal).
+ */
+int qoq_workspace_status(void *workspace, uint32_t *host_status, qoq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QOQ_H_ */

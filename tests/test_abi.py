@@ -1,0 +1,92 @@
+"""Host-only checks of the C ABI: the library loads, exports every function
+include/qoq.h declares, and rejects bad arguments before any launch."""
+import ctypes
+
+import pytest
+
+import w4a8_quantized_serving_qoq_gb300 as qoq
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return qoq.load()
+
+
+def test_exports_every_header_function(lib):
+    names = qoq.header_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in qoq.STATUS_NAMES.items():
+        assert qoq.qoq_status_string(code) == name
+    assert qoq.qoq_status_string(99) == "QOQ_ERR_UNKNOWN"
+    assert qoq.qoq_version() == 1
+
+
+def test_packed_bytes_host_only(lib):
+    # header + N*K/2 codes + (group) 2 bytes per row per group of 128
+    assert qoq.qoq_packed_weight_bytes(256, 512, 128) == 256 + 256 * 512 // 2 + 256 * 4 * 2
+    assert qoq.qoq_packed_weight_bytes(6144, 4096, 128) == 256 + 6144 * 2048 + 6144 * 32 * 2
+    assert qoq.qoq_packed_weight_bytes(128, 128, 0) == 256 + 8192 + 128
+    assert qoq.qoq_packed_weight_bytes(130, 128, 128) == 0
+    assert qoq.qoq_packed_weight_bytes(128, 100, 128) == 0
+    assert qoq.qoq_packed_weight_bytes(128, 128, 64) == 0
+
+
+A = ctypes.c_void_p(0x10000)       # 16-byte aligned fake device address (never dereferenced)
+B = ctypes.c_void_p(0x20008)       # 8-byte aligned, not 16
+NUL = None
+S = ctypes.c_void_p(0)
+
+
+def test_gemm_validation_before_launch(lib):
+    f = lib.qoq_w4a8_gemm
+    ok = (A, A, A, A, A, 16, 256, 512, 128, A, A, 1 << 20, S)
+    # null pointers
+    assert f(NUL, *ok[1:]) == 1
+    assert f(*ok[:3], NUL, *ok[4:]) == 1
+    assert f(*ok[:10], NUL, *ok[11:]) == 1
+    # non-positive sizes
+    assert f(*ok[:5], 0, *ok[6:]) == 1
+    assert f(*ok[:5], 16, -128, *ok[7:]) == 1
+    # unsupported shapes / group
+    assert f(*ok[:5], 16, 200, 512, 128, *ok[9:]) == 2
+    assert f(*ok[:5], 16, 256, 500, 128, *ok[9:]) == 2
+    assert f(*ok[:5], 16, 256, 512, 64, *ok[9:]) == 2
+    # per-channel needs t_x
+    assert f(A, A, NUL, A, A, 16, 256, 512, 0, A, A, 1 << 20, S) == 1
+    # misaligned activations / packed / workspace
+    assert f(B, *ok[1:]) == 3
+    assert f(*ok[:3], B, *ok[4:]) == 3
+    assert f(*ok[:10], B, *ok[11:]) == 3
+    assert f(A, ctypes.c_void_p(0x10001), *ok[2:]) == 3
+
+
+def test_gemm_options_validation(lib):
+    opt = qoq.qoq_gemm_options(48, 0, 0, 0, None)
+    assert lib.qoq_w4a8_gemm_ex(A, A, A, A, A, 16, 256, 512, 128, A, A, 1 << 20,
+                                ctypes.byref(opt), S) == 2
+    opt = qoq.qoq_gemm_options(0, 65, 0, 0, None)
+    assert lib.qoq_w4a8_gemm_ex(A, A, A, A, A, 16, 256, 512, 128, A, A, 1 << 20,
+                                ctypes.byref(opt), S) == 2
+
+
+def test_other_entry_points_validation(lib):
+    assert lib.qoq_quant_act(NUL, 4, 512, A, A, A, S) == 1
+    assert lib.qoq_quant_act(A, 4, 500, A, A, A, S) == 2
+    assert lib.qoq_quant_act(B, 4, 512, A, A, A, S) == 3
+    assert lib.qoq_quant_act(A, 0, 512, A, A, A, S) == 1
+    assert lib.qoq_pack_weights(A, A, A, 256, 512, 128, NUL, S) == 1
+    assert lib.qoq_pack_weights(A, A, A, 250, 512, 128, A, S) == 2
+    assert lib.qoq_pack_weights(B, A, A, 256, 512, 128, A, S) == 3
+    assert lib.qoq_pack_weights(A, NUL, A, 256, 512, 128, A, S) == 1
+    assert lib.qoq_unpack_weights(A, 256, 512, 7, A, A, A, S) == 2
+    assert lib.qoq_quantize_weights(A, 256, 500, 128, A, A, A, A, S) == 2
+    assert lib.qoq_quantize_weights(A, 256, 512, 128, A, NUL, A, A, S) == 1
+    assert lib.qoq_workspace_init(NUL, 256, S) == 1
+    st = ctypes.c_uint32(0)
+    assert lib.qoq_workspace_status(NUL, ctypes.byref(st), S) == 1
+    assert lib.qoq_workspace_status(B, ctypes.byref(st), S) == 3

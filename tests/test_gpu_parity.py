@@ -1,0 +1,265 @@
+"""GPU parity: every step of the CUDA path against the CPU oracle.
+
+Integers (codes, scales, zeros, packed bytes, int32 accumulators) must match
+bit for bit; fp16 outputs must satisfy, per row m,
+    |O_gpu - O_ref| <= 2e-3 * max_n |O_ref[m, :]| + ulp16(|O_ref[m, n]|)
+against the oracle's fp64 epilogue.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import w4a8_quantized_serving_qoq_gb300 as qoq
+from w4a8_quantized_serving_qoq_gb300 import synthetic
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def _np(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def _pack_spec(q4, s_g, z, group):
+    """Independent numpy packer written from the packed-format description in
+    include/qoq.h (no code shared with the CUDA packer)."""
+    N, K = q4.shape
+    G = K // 128
+    blk = 8192 + (256 if group else 0)
+    body = np.zeros((N // 128, G, blk), np.uint8)
+    q = q4.reshape(N // 128, 128, G, 4, 4, 8)  # tile, r, group, p, word j, k-in-word
+    lo = q[..., :4].astype(np.uint8)
+    hi = q[..., 4:].astype(np.uint8)
+    byte = (lo & 15) | ((hi & 15) << 4)             # [..., p, j, b]
+    # chunk (p*128 + r), 16 bytes = words j (4 bytes b each)
+    codes = byte.transpose(0, 2, 3, 1, 4, 5).reshape(N // 128, G, 512 * 16)
+    body[:, :, :8192] = codes
+    if group:
+        meta = np.stack([s_g.reshape(N // 128, 128, G), z.reshape(N // 128, 128, G)], axis=-1)
+        body[:, :, 8192:] = meta.transpose(0, 2, 1, 3).reshape(N // 128, G, 256)
+    out = body.reshape(-1)
+    if not group:
+        zpad = np.zeros((N + 15) // 16 * 16, np.uint8)
+        zpad[:N] = z
+        out = np.concatenate([out, zpad])
+    return out
+
+
+# ------------------------------------------------------------ quantizers --
+@pytest.mark.parametrize("M,K", [(16, 512), (1, 4096), (5, 1024), (129, 256), (300, 14336)])
+def test_quant_act_bit_exact(M, K):
+    X = synthetic.activations(M, K, 100 + M, 4)
+    X[0, : min(K, 8)] = 0
+    if M > 2:
+        X[2] = 0  # all-zero row
+    Qx_r, sx_r, tx_r = oracle.quant_act(X)
+    Qx, sx, tx = qoq.qoq_quant_act(_t(X))
+    assert np.array_equal(_np(Qx), Qx_r)
+    assert np.array_equal(_np(sx).view(np.uint16), sx_r.view(np.uint16))
+    assert np.array_equal(_np(tx), tx_r)
+
+
+def test_quant_act_ties_half_even():
+    row = np.zeros(128, np.float32)
+    row[0] = 127 * 0.125
+    row[1:7] = np.array([2.5, 3.5, -2.5, -0.5, 1.5, 0.5]) * 0.125
+    X = np.stack([row, -row]).astype(np.float16)
+    Qx, sx, tx = qoq.qoq_quant_act(_t(X))
+    q = _np(Qx)
+    assert list(q[0, :7]) == [127, 2, 4, -2, 0, 2, 0]
+    assert list(q[1, :7]) == [-127, -2, -4, 2, 0, -2, 0]
+
+
+@pytest.mark.parametrize("N,K", [(256, 512), (384, 4096), (128, 128)])
+def test_quantize_weights_group_bit_exact(N, K):
+    W = synthetic.weights(N, K, 7 + N, 0.02, 2)
+    W[3] = 0
+    ref = oracle.quantize_weights_group(W, 128)
+    assert ref["n_overflow"] == 0
+    out = qoq.qoq_quantize_weights(_t(W), 128)
+    assert np.array_equal(_np(out["q4"]), ref["q4"])
+    assert np.array_equal(_np(out["s_g"]), ref["s_g"])
+    assert np.array_equal(_np(out["z"]), ref["z"])
+    assert np.array_equal(_np(out["s_w"]).view(np.uint16), ref["s_w"].view(np.uint16))
+
+
+def test_quantize_weights_channel_bit_exact():
+    W = synthetic.weights(256, 1024, 31, 0.02, 2)
+    W[5] = 0
+    ref = oracle.quantize_weights_channel(W)
+    out = qoq.qoq_quantize_weights(_t(W), 0)
+    assert np.array_equal(_np(out["q4"]), ref["q4"])
+    assert np.array_equal(_np(out["z"]), ref["z"])
+    assert np.array_equal(_np(out["s_w"]).view(np.uint16), ref["s_w"].view(np.uint16))
+
+
+# ------------------------------------------------------------------ pack --
+@pytest.mark.parametrize("group", [128, 0])
+def test_pack_matches_spec_and_round_trips(group):
+    N, K = 256, 512
+    q4, s_g, z = synthetic.random_codes(N, K, 5)
+    if not group:
+        z = z[:, 0].copy()
+    packed = qoq.qoq_pack_weights(_t(q4), _t(s_g) if group else None, _t(z), group)
+    p = _np(packed)
+    hdr = p[:256].view(np.uint32)
+    assert hdr[0] == 0x57514F51 and hdr[1] == 1
+    assert hdr[2] == N and hdr[3] == K and hdr[4] == group and hdr[6] == 0
+    assert np.array_equal(p[256:], _pack_spec(q4, s_g, z, group))
+    q4b, sgb, zb = qoq.qoq_unpack_weights(packed, N, K, group)
+    assert np.array_equal(_np(q4b), q4)
+    assert np.array_equal(_np(zb), z)
+    if group:
+        assert np.array_equal(_np(sgb), s_g)
+
+
+def test_pack_counts_illegal_codes():
+    N, K = 128, 256
+    q4, s_g, z = synthetic.random_codes(N, K, 6)
+    q4[0, 0] = 15
+    s_g[0, 0] = 16
+    z[0, 0] = 0  # (15 - 0) * 16 = 240 > 127: illegal
+    q4[1, 1] = 16  # not a 4-bit code
+    packed = qoq.qoq_pack_weights(_t(q4), _t(s_g), _t(z), 128)
+    assert _np(packed)[:256].view(np.uint32)[6] >= 2
+
+
+# ------------------------------------------------------------------ GEMM --
+def _gemm_case(M, N, K, seed, group=128):
+    W = synthetic.weights(N, K, seed, 0.02, 2)
+    X = synthetic.activations(M, K, seed, 4)
+    if group:
+        wq = oracle.quantize_weights_group(W, 128)
+    else:
+        wq = oracle.quantize_weights_channel(W)
+    Qx, sx, tx = oracle.quant_act(X)
+    return wq, Qx, sx, tx
+
+
+def _device_weights(wq, group):
+    packed = qoq.qoq_pack_weights(_t(wq["q4"]), _t(wq["s_g"]) if group else None, _t(wq["z"]), group)
+    return packed, _t(wq["s_w"])
+
+
+def _ref_acc(wq, Qx, tx, group):
+    if group:
+        return oracle.gemm_i32_group(Qx, wq["q4"], wq["s_g"], wq["z"])
+    return oracle.gemm_i32_channel(Qx, tx, wq["q4"], wq["z"])
+
+
+CASES = [(16, 256, 512), (1, 256, 512), (2, 128, 128), (3, 384, 1024), (5, 256, 256),
+         (7, 128, 2048), (33, 256, 640), (64, 128, 384), (127, 256, 512), (129, 128, 256),
+         (200, 256, 1152)]
+
+
+@pytest.mark.parametrize("M,N,K", CASES)
+@pytest.mark.parametrize("group", [128, 0])
+def test_gemm_i32_bit_exact(M, N, K, group):
+    wq, Qx, sx, tx = _gemm_case(M, N, K, 1000 + M + N + K, group)
+    packed, sw = _device_weights(wq, group)
+    acc = qoq.qoq_w4a8_gemm_i32(_t(Qx), _t(tx), packed, N, K, group)
+    assert np.array_equal(_np(acc), _ref_acc(wq, Qx, tx, group))
+
+
+@pytest.mark.parametrize("bt", [16, 32, 64, 128])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_gemm_tiles_and_splits(bt, splits):
+    M, N, K = 37, 256, 896  # ragged token tail; 7 groups
+    wq, Qx, sx, tx = _gemm_case(M, N, K, 77)
+    packed, sw = _device_weights(wq, 128)
+    ref = _ref_acc(wq, Qx, tx, 128)
+    acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    opt = qoq.gemm_options(tokens_per_tile=bt, k_splits=splits, acc_out=acc)
+    qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128, options=opt)
+    assert np.array_equal(_np(acc), ref)
+    O = qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N, K, 128,
+                             options=qoq.gemm_options(tokens_per_tile=bt, k_splits=splits))
+    O_ref = oracle.epilogue_f64(ref, sx, wq["s_w"])
+    assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
+
+
+def test_gemm_exact_at_chunk_extremes():
+    """Largest-magnitude products over whole 1024-k chunks: the fp32
+    accumulation per chunk must still be exact (sums up to 127*128*1024)."""
+    M, N, K = 4, 128, 3072
+    q4 = np.zeros((N, K), np.uint8)
+    s_g = np.full((N, K // 128), 8, np.uint8)
+    z = np.full((N, K // 128), 0, np.uint8)
+    q4[:64] = 15                 # +120
+    s_g[64:] = 16
+    z[64:] = 8
+    q4[64:] = 0                  # (0 - 8) * 16 = -128
+    q4[100, ::3] = 15            # mixed row: (15 - 8) * 16 = 112
+    Qx = np.full((M, K), 127, np.int8)
+    Qx[1] = -127
+    Qx[2, ::2] = -127
+    Qx[3] = np.random.default_rng(1).integers(-127, 128, K).astype(np.int8)
+    packed = qoq.qoq_pack_weights(_t(q4), _t(s_g), _t(z), 128)
+    ref = oracle.gemm_i32_group(Qx, q4, s_g, z)
+    assert abs(int(ref[0, 0])) == 127 * 120 * K
+    for splits in (1, 2):
+        acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+        qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128,
+                             options=qoq.gemm_options(k_splits=splits, acc_out=acc))
+        assert np.array_equal(_np(acc), ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 256, 512), (1, 512, 4096), (77, 256, 1024)])
+@pytest.mark.parametrize("group", [128, 0])
+def test_gemm_fp16_within_tolerance(M, N, K, group):
+    wq, Qx, sx, tx = _gemm_case(M, N, K, 31 + M, group)
+    packed, sw = _device_weights(wq, group)
+    O = qoq.qoq_w4a8_gemm(_t(Qx), _t(sx), _t(tx), packed, sw, N, K, group)
+    O_ref = oracle.epilogue_f64(_ref_acc(wq, Qx, tx, group), sx, wq["s_w"])
+    ok = oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref)
+    assert ok.all(), np.argwhere(~ok)[:5]
+
+
+def test_end_to_end_tiny_workload():
+    """The tiny 16x256x512 workload through every device step (weights
+    quantized on the device, activations quantized on the device)."""
+    (layer,) = synthetic.WORKLOADS[0][1]
+    W, X = synthetic.workload_layer_inputs(0, layer, 16)
+    ref = oracle.reference_forward_group(W, X, 128)
+    wq = qoq.qoq_quantize_weights(_t(W), 128)
+    packed = qoq.qoq_pack_weights(wq["q4"], wq["s_g"], wq["z"], 128)
+    Qx, sx, tx = qoq.qoq_quant_act(_t(X))
+    acc = qoq.qoq_w4a8_gemm_i32(Qx, tx, packed, layer.N, layer.K, 128)
+    O = qoq.qoq_w4a8_gemm(Qx, sx, tx, packed, wq["s_w"], layer.N, layer.K, 128)
+    assert np.array_equal(_np(acc), ref["acc"])
+    assert oracle.o_within_tolerance(_np(O).astype(np.float64), ref["O"]).all()
+
+
+# ----------------------------------------------------------- error paths --
+def test_workspace_too_small_rejected():
+    M, N, K = 8, 256, 4096
+    need = qoq.qoq_gemm_workspace_bytes(M, N, K, 128)
+    assert need > 256  # this shape splits K
+    ws = qoq.new_workspace(256)
+    wq, Qx, sx, tx = _gemm_case(M, N, K, 3)
+    packed, sw = _device_weights(wq, 128)
+    with pytest.raises(qoq.QoqError) as e:
+        qoq.qoq_w4a8_gemm(_t(Qx), _t(sx), None, packed, sw, N, K, 128, workspace=ws)
+    assert e.value.status == 4
+
+
+def test_mismatched_packed_weights_reported_on_device():
+    M, N, K = 8, 256, 512
+    wq, Qx, sx, tx = _gemm_case(M, N, K, 4)
+    packed, sw = _device_weights(wq, 128)
+    ws = qoq.new_workspace(qoq.qoq_gemm_workspace_bytes(M, N - 128, K, 128))
+    O = torch.zeros((M, N - 128), dtype=torch.float16, device=DEV)
+    # packed holds N = 256 rows; calling with N = 128 must be refused on the device
+    qoq.qoq_w4a8_gemm(_t(Qx), _t(sx), None, packed, sw, N - 128, K, 128, O=O, workspace=ws)
+    st, bits = qoq.qoq_workspace_status(ws)
+    assert st == 7 and bits & 2
+    assert float(O.abs().max()) == 0.0  # nothing written
+    st, bits = qoq.qoq_workspace_status(ws)
+    assert st == 0 and bits == 0  # cleared by the read

@@ -1,1 +1,287 @@
-"""GB300-native W4A8 GEMM (QoQ / QServe hot path)."""
+"""GB300-native W4A8 GEMM: the hot path of the QoQ / QServe method.
+
+A thin ctypes binding over ``libqoq.so`` (C ABI declared in
+``include/qoq.h``).  Each function has the name of the C entry point and does
+argument marshalling only: torch tensors provide device memory and the
+current CUDA stream; every step of the computation runs in the library's
+CUDA kernels.  There is no CPU fallback: if the library is missing or fails
+to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import _build
+
+_lock = threading.Lock()
+_lib = None
+
+QOQ_OK = 0
+STATUS_NAMES = {
+    0: "QOQ_OK", 1: "QOQ_ERR_INVALID_ARG", 2: "QOQ_ERR_UNSUPPORTED", 3: "QOQ_ERR_MISALIGNED",
+    4: "QOQ_ERR_WORKSPACE", 5: "QOQ_ERR_CUDA", 6: "QOQ_ERR_TIMEOUT", 7: "QOQ_ERR_DEVICE",
+}
+
+
+class QoqError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        super().__init__(f"{func} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class qoq_gemm_options(ctypes.Structure):
+    _fields_ = [
+        ("tokens_per_tile", ctypes.c_int),
+        ("k_splits", ctypes.c_int),
+        ("timeout_ns", ctypes.c_uint64),
+        ("debug_flags", ctypes.c_uint32),
+        ("acc_out", ctypes.c_void_p),
+    ]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def build(force: bool = False) -> str:
+    """Compile libqoq.so for sm_103a (in-tree)."""
+    return _build.build(force=force)
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/qoq.h."""
+    path = os.path.join(_build.ROOT, "include", "qoq.h")
+    text = open(path).read()
+    return sorted(set(re.findall(r"\b(qoq_[a-z0-9_]+)\s*\(", text)) - {"qoq_gemm_options"})
+
+
+def load():
+    """Load libqoq.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not _build.up_to_date():
+                _build.build()
+            lib = ctypes.CDLL(_build.LIB)
+            P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            sigs = {
+                "qoq_status_string": (ctypes.c_char_p, [I]),
+                "qoq_version": (I, []),
+                "qoq_quantize_weights": (I, [P, I, I, I, P, P, P, P, P]),
+                "qoq_packed_weight_bytes": (S, [I, I, I]),
+                "qoq_pack_weights": (I, [P, P, P, I, I, I, P, P]),
+                "qoq_unpack_weights": (I, [P, I, I, I, P, P, P, P]),
+                "qoq_quant_act": (I, [P, I, I, P, P, P, P]),
+                "qoq_gemm_workspace_bytes": (S, [I, I, I, I]),
+                "qoq_gemm_workspace_bytes_ex": (S, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
+                "qoq_workspace_init": (I, [P, S, P]),
+                "qoq_w4a8_gemm": (I, [P, P, P, P, P, I, I, I, I, P, P, S, P]),
+                "qoq_w4a8_gemm_i32": (I, [P, P, P, I, I, I, I, P, P, S, P]),
+                "qoq_w4a8_gemm_ex": (I, [P, P, P, P, P, I, I, I, I, P, P, S,
+                                         ctypes.POINTER(qoq_gemm_options), P]),
+                "qoq_workspace_status": (I, [P, ctypes.POINTER(ctypes.c_uint32), P]),
+            }
+            for name, (res, args) in sigs.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+# ---------------------------------------------------------------- helpers --
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype, name):
+    torch = _torch()
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    _ = torch
+
+
+def _check(func: str, status: int):
+    if status != QOQ_OK:
+        raise QoqError(func, status)
+
+
+# ------------------------------------------------------------ entry points --
+def qoq_status_string(status: int) -> str:
+    return load().qoq_status_string(int(status)).decode()
+
+
+def qoq_version() -> int:
+    return int(load().qoq_version())
+
+
+def qoq_quantize_weights(W, group: int = 128, stream=None):
+    """fp16 W [N][K] -> dict(q4 [N][K] u8, s_g [N][K/128] u8 or None, z, s_w fp16 [N])."""
+    torch = _torch()
+    _dev(W, torch.float16, "W")
+    N, K = W.shape
+    q4 = torch.empty((N, K), dtype=torch.uint8, device=W.device)
+    s_g = torch.empty((N, K // 128), dtype=torch.uint8, device=W.device) if group else None
+    z = torch.empty((N, K // 128) if group else (N,), dtype=torch.uint8, device=W.device)
+    s_w = torch.empty((N,), dtype=torch.float16, device=W.device)
+    _check("qoq_quantize_weights", load().qoq_quantize_weights(
+        _ptr(W), N, K, group, _ptr(q4), _ptr(s_g), _ptr(z), _ptr(s_w), _stream(stream)))
+    return dict(q4=q4, s_g=s_g, z=z, s_w=s_w)
+
+
+def qoq_packed_weight_bytes(N: int, K: int, group: int = 128) -> int:
+    return int(load().qoq_packed_weight_bytes(N, K, group))
+
+
+def qoq_pack_weights(q4, s_g, z, group: int = 128, packed=None, stream=None):
+    torch = _torch()
+    _dev(q4, torch.uint8, "q4")
+    _dev(s_g, torch.uint8, "s_g")
+    _dev(z, torch.uint8, "z")
+    N, K = q4.shape
+    nbytes = qoq_packed_weight_bytes(N, K, group)
+    if nbytes == 0:
+        raise QoqError("qoq_pack_weights", 2)
+    if packed is None:
+        packed = torch.empty((nbytes,), dtype=torch.uint8, device=q4.device)
+    _dev(packed, torch.uint8, "packed")
+    _check("qoq_pack_weights", load().qoq_pack_weights(
+        _ptr(q4), _ptr(s_g), _ptr(z), N, K, group, _ptr(packed), _stream(stream)))
+    return packed
+
+
+def qoq_unpack_weights(packed, N: int, K: int, group: int = 128, stream=None):
+    torch = _torch()
+    _dev(packed, torch.uint8, "packed")
+    q4 = torch.empty((N, K), dtype=torch.uint8, device=packed.device)
+    s_g = torch.empty((N, K // 128), dtype=torch.uint8, device=packed.device) if group else None
+    z = torch.empty((N, K // 128) if group else (N,), dtype=torch.uint8, device=packed.device)
+    _check("qoq_unpack_weights", load().qoq_unpack_weights(
+        _ptr(packed), N, K, group, _ptr(q4), _ptr(s_g), _ptr(z), _stream(stream)))
+    return q4, s_g, z
+
+
+def qoq_quant_act(X, Qx=None, s_x=None, t_x=None, with_t: bool = True, stream=None):
+    """fp16 X [M][K] -> (Qx int8 [M][K], s_x fp16 [M], t_x int32 [M] or None)."""
+    torch = _torch()
+    _dev(X, torch.float16, "X")
+    M, K = X.shape
+    if Qx is None:
+        Qx = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    if s_x is None:
+        s_x = torch.empty((M,), dtype=torch.float16, device=X.device)
+    if t_x is None and with_t:
+        t_x = torch.empty((M,), dtype=torch.int32, device=X.device)
+    _dev(Qx, torch.int8, "Qx")
+    _dev(s_x, torch.float16, "s_x")
+    _dev(t_x, torch.int32, "t_x")
+    _check("qoq_quant_act", load().qoq_quant_act(
+        _ptr(X), M, K, _ptr(Qx), _ptr(s_x), _ptr(t_x), _stream(stream)))
+    return Qx, s_x, t_x
+
+
+def qoq_gemm_workspace_bytes(M: int, N: int, K: int, group: int = 128, options=None) -> int:
+    if options is None:
+        return int(load().qoq_gemm_workspace_bytes(M, N, K, group))
+    return int(load().qoq_gemm_workspace_bytes_ex(M, N, K, group, ctypes.byref(options)))
+
+
+def qoq_workspace_init(workspace, stream=None):
+    _check("qoq_workspace_init", load().qoq_workspace_init(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def new_workspace(nbytes: int, device="cuda", stream=None):
+    """A zero-filled workspace tensor of at least nbytes (16-byte aligned)."""
+    torch = _torch()
+    ws = torch.empty((max(256, (nbytes + 255) // 256 * 256),), dtype=torch.uint8, device=device)
+    qoq_workspace_init(ws, stream)
+    return ws
+
+
+def qoq_w4a8_gemm(Qx, s_x, t_x, packed, s_w, N: int, K: int, group: int = 128, O=None,
+                  workspace=None, stream=None):
+    torch = _torch()
+    _dev(Qx, torch.int8, "Qx")
+    M = Qx.shape[0]
+    if O is None:
+        O = torch.empty((M, N), dtype=torch.float16, device=Qx.device)
+    if workspace is None:
+        workspace = new_workspace(qoq_gemm_workspace_bytes(M, N, K, group), Qx.device, stream)
+    _check("qoq_w4a8_gemm", load().qoq_w4a8_gemm(
+        _ptr(Qx), _ptr(s_x), _ptr(t_x), _ptr(packed), _ptr(s_w), M, N, K, group, _ptr(O),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return O
+
+
+def qoq_w4a8_gemm_i32(Qx, t_x, packed, N: int, K: int, group: int = 128, acc=None,
+                      workspace=None, stream=None):
+    torch = _torch()
+    _dev(Qx, torch.int8, "Qx")
+    M = Qx.shape[0]
+    if acc is None:
+        acc = torch.empty((M, N), dtype=torch.int32, device=Qx.device)
+    if workspace is None:
+        workspace = new_workspace(qoq_gemm_workspace_bytes(M, N, K, group), Qx.device, stream)
+    _check("qoq_w4a8_gemm_i32", load().qoq_w4a8_gemm_i32(
+        _ptr(Qx), _ptr(t_x), _ptr(packed), M, N, K, group, _ptr(acc), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    return acc
+
+
+def gemm_options(tokens_per_tile=0, k_splits=0, timeout_ns=0, debug_flags=0, acc_out=None):
+    return qoq_gemm_options(tokens_per_tile, k_splits, timeout_ns, debug_flags,
+                            None if acc_out is None else acc_out.data_ptr())
+
+
+def qoq_w4a8_gemm_ex(Qx, s_x, t_x, packed, s_w, N: int, K: int, group: int = 128, O=None,
+                     workspace=None, options=None, stream=None, check: bool = True):
+    torch = _torch()
+    _dev(Qx, torch.int8, "Qx")
+    M = Qx.shape[0]
+    if options is None:
+        options = qoq_gemm_options()
+    if O is None and not options.acc_out:
+        O = torch.empty((M, N), dtype=torch.float16, device=Qx.device)
+    if workspace is None:
+        workspace = new_workspace(qoq_gemm_workspace_bytes(M, N, K, group, options), Qx.device, stream)
+    st = load().qoq_w4a8_gemm_ex(
+        _ptr(Qx), _ptr(s_x), _ptr(t_x), _ptr(packed), _ptr(s_w), M, N, K, group, _ptr(O),
+        _ptr(workspace), workspace.numel(), ctypes.byref(options), _stream(stream))
+    if check:
+        _check("qoq_w4a8_gemm_ex", st)
+        return O
+    return st
+
+
+def qoq_workspace_status(workspace, stream=None):
+    """(status code, raw status bits); synchronizes the stream."""
+    bits = ctypes.c_uint32(0)
+    st = load().qoq_workspace_status(_ptr(workspace), ctypes.byref(bits), _stream(stream))
+    return int(st), int(bits.value)
+
+
+__all__ = [n for n in dir() if n.startswith("qoq_")] + [
+    "QoqError", "build", "load", "library_path", "header_functions", "new_workspace", "gemm_options",
+]

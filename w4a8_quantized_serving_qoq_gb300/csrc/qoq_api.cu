@@ -1,0 +1,213 @@
+// C ABI of libqoq.so: argument validation, workspace planning and launches.
+// Declarations and the full contract of each entry point: include/qoq.h.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/qoq.h"
+#include "qoq_internal.h"
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int num_sms_current_device() {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? QOQ_OK : QOQ_ERR_CUDA; }
+
+int check_gemm_shape(int M, int N, int K, int group) {
+    if (M <= 0 || N <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
+    if (group != 0 && group != 128) return QOQ_ERR_UNSUPPORTED;
+    if (N % 128 != 0 || K % 128 != 0) return QOQ_ERR_UNSUPPORTED;
+    if (N / 128 > 65535) return QOQ_ERR_UNSUPPORTED;
+    return QOQ_OK;
+}
+
+int check_options(const qoq_gemm_options *opt) {
+    if (!opt) return QOQ_OK;
+    const int bt = opt->tokens_per_tile;
+    if (bt != 0 && bt != 16 && bt != 32 && bt != 64 && bt != 128) return QOQ_ERR_UNSUPPORTED;
+    if (opt->k_splits < 0 || opt->k_splits > 64) return QOQ_ERR_UNSUPPORTED;
+    return QOQ_OK;
+}
+
+bool plan_for(int M, int N, int K, const qoq_gemm_options *opt, qoq::GemmPlan *out) {
+    const int sms = num_sms_current_device();
+    if (sms <= 0) return false;
+    *out = qoq::plan_gemm(M, N, K, sms, opt ? opt->tokens_per_tile : 0, opt ? opt->k_splits : 0);
+    return true;
+}
+
+int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const void *packed,
+                const uint16_t *s_w, int M, int N, int K, int group, uint16_t *O, int32_t *acc_out,
+                void *ws, size_t ws_bytes, const qoq_gemm_options *opt, cudaStream_t stream) {
+    int st = check_gemm_shape(M, N, K, group);
+    if (st != QOQ_OK) return st;
+    st = check_options(opt);
+    if (st != QOQ_OK) return st;
+    if (!Qx || !packed || !ws) return QOQ_ERR_INVALID_ARG;
+    if (group == 0 && !t_x) return QOQ_ERR_INVALID_ARG;
+    if (!acc_out && (!O || !s_x || !s_w)) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(Qx, 16) || !aligned(packed, 16) || !aligned(ws, 16)) return QOQ_ERR_MISALIGNED;
+    if ((s_x && !aligned(s_x, 2)) || (s_w && !aligned(s_w, 2)) || (O && !aligned(O, 2)) ||
+        (t_x && !aligned(t_x, 4)) || (acc_out && !aligned(acc_out, 4)))
+        return QOQ_ERR_MISALIGNED;
+    qoq::GemmPlan plan;
+    if (!plan_for(M, N, K, opt, &plan)) return QOQ_ERR_CUDA;
+    if (ws_bytes < plan.ws_bytes) return QOQ_ERR_WORKSPACE;
+    qoq::GemmArgs a;
+    a.Qx = Qx;
+    a.s_x = s_x;
+    a.t_x = t_x;
+    a.packed = packed;
+    a.s_w = s_w;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.group = group;
+    a.O = O;
+    a.acc_out = acc_out;
+    a.ws = ws;
+    a.debug_flags = opt ? opt->debug_flags : 0u;
+    a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+    return cuda_status(qoq::launch_gemm(a, plan, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qoq_status_string(int status) {
+    switch (status) {
+        case QOQ_OK: return "QOQ_OK";
+        case QOQ_ERR_INVALID_ARG: return "QOQ_ERR_INVALID_ARG";
+        case QOQ_ERR_UNSUPPORTED: return "QOQ_ERR_UNSUPPORTED";
+        case QOQ_ERR_MISALIGNED: return "QOQ_ERR_MISALIGNED";
+        case QOQ_ERR_WORKSPACE: return "QOQ_ERR_WORKSPACE";
+        case QOQ_ERR_CUDA: return "QOQ_ERR_CUDA";
+        case QOQ_ERR_TIMEOUT: return "QOQ_ERR_TIMEOUT";
+        case QOQ_ERR_DEVICE: return "QOQ_ERR_DEVICE";
+        default: return "QOQ_ERR_UNKNOWN";
+    }
+}
+
+int qoq_version(void) { return static_cast<int>(qoq::kPackedVersion); }
+
+int qoq_quantize_weights(const uint16_t *W, int N, int K, int group, uint8_t *q4, uint8_t *s_g,
+                         uint8_t *z, uint16_t *s_w, qoq_stream_t stream) {
+    if (N <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
+    if (group != 0 && group != 128) return QOQ_ERR_UNSUPPORTED;
+    if (group == 128 && K % 128 != 0) return QOQ_ERR_UNSUPPORTED;
+    if (!W || !q4 || !z || !s_w || (group && !s_g)) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(W, 2) || !aligned(s_w, 2)) return QOQ_ERR_MISALIGNED;
+    return cuda_status(qoq::launch_quantize_weights(W, N, K, group, q4, s_g, z, s_w,
+                                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t qoq_packed_weight_bytes(int N, int K, int group) {
+    if (N <= 0 || K <= 0 || N % 128 || K % 128 || (group != 0 && group != 128)) return 0;
+    return qoq::packed_bytes(N, K, group);
+}
+
+int qoq_pack_weights(const uint8_t *q4, const uint8_t *s_g, const uint8_t *z, int N, int K,
+                     int group, void *packed, qoq_stream_t stream) {
+    if (N <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
+    if (group != 0 && group != 128) return QOQ_ERR_UNSUPPORTED;
+    if (N % 128 || K % 128 || N / 128 > 65535) return QOQ_ERR_UNSUPPORTED;
+    if (!q4 || !z || !packed || (group && !s_g)) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(q4, 16) || !aligned(packed, 16)) return QOQ_ERR_MISALIGNED;
+    return cuda_status(qoq::launch_pack(q4, s_g, z, N, K, group, packed,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int qoq_unpack_weights(const void *packed, int N, int K, int group, uint8_t *q4, uint8_t *s_g,
+                       uint8_t *z, qoq_stream_t stream) {
+    if (N <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
+    if (group != 0 && group != 128) return QOQ_ERR_UNSUPPORTED;
+    if (N % 128 || K % 128 || N / 128 > 65535) return QOQ_ERR_UNSUPPORTED;
+    if (!q4 || !z || !packed || (group && !s_g)) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(q4, 16) || !aligned(packed, 16)) return QOQ_ERR_MISALIGNED;
+    return cuda_status(qoq::launch_unpack(packed, N, K, group, q4, s_g, z,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x,
+                  qoq_stream_t stream) {
+    if (M <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
+    if (K % 8 != 0) return QOQ_ERR_UNSUPPORTED;
+    if (!X || !Qx || !s_x) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) || (t_x && !aligned(t_x, 4)))
+        return QOQ_ERR_MISALIGNED;
+    return cuda_status(qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gemm_options *opt) {
+    if (check_gemm_shape(M, N, K, group) != QOQ_OK || check_options(opt) != QOQ_OK) return 0;
+    qoq::GemmPlan plan;
+    if (!plan_for(M, N, K, opt, &plan)) return 0;
+    return plan.ws_bytes;
+}
+
+size_t qoq_gemm_workspace_bytes(int M, int N, int K, int group) {
+    return qoq_gemm_workspace_bytes_ex(M, N, K, group, nullptr);
+}
+
+int qoq_workspace_init(void *workspace, size_t bytes, qoq_stream_t stream) {
+    if (!workspace || bytes == 0) return QOQ_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(workspace, 0, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int qoq_w4a8_gemm(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const void *packed,
+                  const uint16_t *s_w, int M, int N, int K, int group, uint16_t *O,
+                  void *workspace, size_t ws_bytes, qoq_stream_t stream) {
+    return gemm_common(Qx, s_x, t_x, packed, s_w, M, N, K, group, O, nullptr, workspace, ws_bytes,
+                       nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, int M, int N,
+                      int K, int group, int32_t *acc, void *workspace, size_t ws_bytes,
+                      qoq_stream_t stream) {
+    if (!acc) return QOQ_ERR_INVALID_ARG;
+    return gemm_common(Qx, nullptr, t_x, packed, nullptr, M, N, K, group, nullptr, acc, workspace,
+                       ws_bytes, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int qoq_w4a8_gemm_ex(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x,
+                     const void *packed, const uint16_t *s_w, int M, int N, int K, int group,
+                     uint16_t *O, void *workspace, size_t ws_bytes, const qoq_gemm_options *opt,
+                     qoq_stream_t stream) {
+    return gemm_common(Qx, s_x, t_x, packed, s_w, M, N, K, group, O, opt ? opt->acc_out : nullptr,
+                       workspace, ws_bytes, opt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int qoq_workspace_status(void *workspace, uint32_t *host_status, qoq_stream_t stream) {
+    if (!workspace || !host_status) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return QOQ_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(v), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return QOQ_ERR_CUDA;
+    *host_status = v;
+    if (v & 1u) return QOQ_ERR_TIMEOUT;
+    if (v & 2u) return QOQ_ERR_DEVICE;
+    return QOQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,514 @@
+// W4A8 GEMM for sm_103a: O[m,n] = s_x[m] * s_w[n] * sum_k Qx[m,k] * w8[n,k],
+// w8 = (q4 - z) * s_g (progressive group quantization, g = 128), or
+// w8 = q4 with the zero folded into the epilogue (per-channel variant).
+//
+// Sources: "QServe: W4A8KV4 Quantization and System Co-design for Efficient
+// LLM Serving" (papercache summary), sections "逐通道W4A8 GEMM中的快速反量化"
+// (eq. 13) and "逐组W4A8 GEMM中的快速反量化"; "QServe：把 W4A8KV4 的理论收益做成
+// 实测吞吐的量化—系统协同设计" (zenmind review), sections 3.2 and 4 (step 3).
+//
+// GB300 design (sm_103a has no tcgen05 INT8 MMA, so the exact integer
+// product runs on the fp16 tensor-core path):
+//  * swap-AB: the MMA's M = 128 weight rows, its N = BT tokens (16..128);
+//  * one warp streams each stage with TMA: one bulk copy of the packed 8 KB
+//    weight block (+ 256 B of group metadata) and one 2D tensor copy of the
+//    INT8 activation tile (128-byte swizzle, rows past M zero-filled);
+//  * 8 converter warps turn codes into fp16 operands in registers with
+//    byte-lane SIMD: one 32-bit multiply-add per 4 weights yields
+//    (q4 - z) * s_g + 128 in each byte (legal because the protective range
+//    keeps every product in [-128, 127]), then byte -> fp16 by exponent
+//    splicing and one fp16x2 subtract; INT8 activations the same way;
+//  * one thread issues tcgen05.mma (kind::f16, fp32 accumulation in TMEM).
+//    Operands are integers with |product| <= 127 * 128, so an fp32 sum over
+//    1024 k (8 stages) stays below 2^24 and is exact; each 1024-k chunk is
+//    drained by the epilogue warps into an int32 running sum kept in TMEM
+//    (two chunk buffers so the MMA never waits on the drain);
+//  * epilogue: int32 result (per-channel: minus z[n] * t_x[m]) scaled by
+//    s_x[m] * s_w[n] in fp32 and rounded to fp16; with a K split, int32
+//    partials are reduced exactly with red.add and the last CTA of a tile
+//    applies the epilogue and re-zeroes its workspace.
+//  * every wait is bounded; on expiry the kernel records kStatusTimeout in the
+//    workspace status word, drains its own copies/MMAs and frees TMEM.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "qoq_device.cuh"
+#include "qoq_internal.h"
+
+namespace qoq {
+namespace {
+
+constexpr int kThreads = 512;          // 16 warps
+constexpr int kConvThreads = 256;      // warps 8..15
+constexpr int kEpiThreads = 128;       // warps 4..7
+constexpr int kChunkStages = 8;        // 8 x 128 k = 1024 k per exact fp32 chunk
+constexpr uint32_t kWRawBytes = 9216;  // 8448 B block slot rounded to 1 KB
+
+template <int BT>
+struct Cfg {
+    static constexpr int kRawStages = BT <= 32 ? 8 : (BT == 64 ? 6 : 3);
+    static constexpr int kOpStages = 2;
+    static constexpr uint32_t kAAtom = 128u * 128u;            // 128 rows x 64 fp16
+    static constexpr uint32_t kBAtom = static_cast<uint32_t>(BT) * 128u;
+    static constexpr uint32_t kOpStageBytes = 2 * kAAtom + 2 * kBAtom;
+    static constexpr uint32_t kQxRawBytes = static_cast<uint32_t>(BT) * 128u;
+    static constexpr uint32_t kRawSlotBytes = kQxRawBytes + kWRawBytes;
+    static constexpr uint32_t kTmemCols = BT <= 16 ? 64 : (BT <= 32 ? 128 : (BT <= 64 ? 256 : 512));
+    static constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 4 + 1;
+    static constexpr uint32_t kMiscBytes = 1024;
+    static constexpr uint32_t kSmemBytes =
+        kOpStages * kOpStageBytes + kRawStages * kRawSlotBytes + kMiscBytes + 1024;
+    static_assert(3 * BT <= static_cast<int>(kTmemCols), "TMEM columns");
+    static_assert(kNumBars * 8 + 64 <= static_cast<int>(kMiscBytes), "barrier area");
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+struct GemmParams {
+    const uint8_t *packed;
+    const uint16_t *s_x;
+    const int32_t *t_x;
+    const uint16_t *s_w;
+    uint16_t *O;
+    int32_t *acc_out;
+    uint32_t *status;
+    uint32_t *counters;
+    int32_t *partials;
+    int M, N, K, group, G, splits;
+    uint32_t debug_flags;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+// Four INT8 / biased bytes -> two fp16x2 words holding the signed values.
+// Input byte b is v + 128 (v in [-128, 127]); 0x64XX is the fp16 1024 + XX.
+__device__ __forceinline__ void biased_bytes_to_f16x4(uint32_t u, uint32_t &lo, uint32_t &hi) {
+    const uint32_t a = __byte_perm(u, 0x64646464u, 0x4140u);
+    const uint32_t b = __byte_perm(u, 0x64646464u, 0x4342u);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
+    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
+    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+    lo = *reinterpret_cast<const uint32_t *>(&ha);
+    hi = *reinterpret_cast<const uint32_t *>(&hb);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+template <int BT>
+__global__ void __launch_bounds__(kThreads, 1)
+    w4a8_gemm_kernel(const __grid_constant__ CUtensorMap qx_map, const GemmParams p) {
+    using C = Cfg<BT>;
+    constexpr int R = C::kRawStages;
+    constexpr int OPS = C::kOpStages;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *op_base = smem;
+    uint8_t *raw_base = smem + OPS * C::kOpStageBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(raw_base + R * C::kRawSlotBytes);
+    uint64_t *raw_full = bars;
+    uint64_t *raw_empty = bars + R;
+    uint64_t *op_full = bars + 2 * R;
+    uint64_t *op_empty = op_full + OPS;
+    uint64_t *chunk_full = op_empty + OPS;
+    uint64_t *chunk_empty = chunk_full + 2;
+    uint64_t *mma_done = chunk_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *hdr_ok = abort_flag + 1;
+    volatile int *is_last = abort_flag + 2;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tok_tile = blockIdx.x, n_tile = blockIdx.y, split = blockIdx.z;
+    const int m0 = tok_tile * BT, n0 = n_tile * kTileN;
+    const int g0 = static_cast<int>((static_cast<long long>(split) * p.G) / p.splits);
+    const int g1 = static_cast<int>((static_cast<long long>(split + 1) * p.G) / p.splits);
+    const int nst = g1 - g0;
+    const int nchunks = (nst + kChunkStages - 1) / kChunkStages;
+    const uint32_t bb = block_bytes(p.group);
+    const uint64_t tmo = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        const PackedHeader *h = reinterpret_cast<const PackedHeader *>(p.packed);
+        const bool ok = h->magic == kPackedMagic && h->version == kPackedVersion && h->N == p.N &&
+                        h->K == p.K && h->group == p.group && h->illegal == 0u;
+        if (!ok) atomicOr(p.status, kStatusBadPacked);
+        *hdr_ok = ok ? 1 : 0;
+        *abort_flag = 0;
+        *is_last = 0;
+        for (int i = 0; i < R; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], kConvThreads);
+        }
+        for (int i = 0; i < OPS; ++i) {
+            mbar_init(&op_full[i], kConvThreads);
+            mbar_init(&op_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&chunk_full[i], 1);
+            mbar_init(&chunk_empty[i], kEpiThreads);
+        }
+        mbar_init(mma_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const bool run = (*hdr_ok != 0) && nst > 0;
+
+    if (run && warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
+            prefetch_tensormap(&qx_map);
+            const uint8_t *wblk = p.packed + kHeaderBytes + (static_cast<size_t>(n_tile) * p.G + g0) * bb;
+            int issued = 0;
+            for (int t = 0; t < nst; ++t) {
+                const int slot = t % R, use = t / R;
+                if (use > 0 && !mbar_wait(&raw_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo))
+                    break;
+                if ((p.debug_flags & kDebugWithholdStage) && t == 1) break;
+                uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
+                mbar_arrive_expect_tx(&raw_full[slot], C::kQxRawBytes + bb);
+                tma_load_2d(dst, &qx_map, (g0 + t) * kTileK, m0, &raw_full[slot], pol_x);
+                tma_load_1d(dst + C::kQxRawBytes, wblk + static_cast<size_t>(t) * bb, bb, &raw_full[slot], pol_w);
+                issued = t + 1;
+            }
+            // Drain: every issued copy must land before the CTA exits.
+            for (int t = (issued > R ? issued - R : 0); t < issued; ++t)
+                mbar_wait(&raw_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
+        }
+    } else if (run && warp == 1) {
+        // ------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(128, BT);
+            for (int t = 0; t < nst; ++t) {
+                const int c = t / kChunkStages;
+                const bool first = (t % kChunkStages) == 0;
+                const bool last = (t % kChunkStages) == kChunkStages - 1 || t == nst - 1;
+                const int cb = c & 1;
+                if (first && c >= 2 &&
+                    !mbar_wait(&chunk_empty[cb], ((c - 2) >> 1) & 1, abort_flag, p.status, tmo))
+                    break;
+                const int os = t % OPS, ouse = t / OPS;
+                if (!mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + static_cast<uint32_t>((1 + cb) * BT);
+                const uint32_t a_base = smem_u32(op_base + os * C::kOpStageBytes);
+                const uint32_t b_base = a_base + 2 * C::kAAtom;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ad = desc_kmajor_sw128(a_base + (kk >> 2) * C::kAAtom + (kk & 3) * 32);
+                    const uint64_t bd = desc_kmajor_sw128(b_base + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
+                    mma_f16(d_tmem, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
+                }
+                mma_commit(&op_empty[os]);
+                if (last) mma_commit(&chunk_full[cb]);
+            }
+            // All issued MMAs must finish before TMEM is released.
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0, nullptr, p.status, tmo);
+        }
+    } else if (run && warp >= 8) {
+        // ---------------------------------------------- converter warps --
+        const int ct = threadIdx.x - (kThreads - kConvThreads);
+        const int wr = ct & 127, wh = ct >> 7;  // weight row, k half (64 k)
+        for (int t = 0; t < nst; ++t) {
+            const int rs = t % R, ruse = t / R, os = t % OPS, ouse = t / OPS;
+            if (!mbar_wait(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo)) break;
+            if (ouse > 0 && !mbar_wait(&op_empty[os], (ouse - 1) & 1, abort_flag, p.status, tmo)) break;
+            const uint32_t raw = smem_u32(raw_base + rs * C::kRawSlotBytes);
+            const uint32_t wraw = raw + C::kQxRawBytes;
+            const uint32_t a_atom = smem_u32(op_base + os * C::kOpStageBytes) + wh * C::kAAtom;
+            const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes) + 2 * C::kAAtom;
+
+            // Weights: row wr, k in [64*wh, 64*wh + 64): 2 raw chunks -> 8 fp16 chunks.
+            uint32_t s = 1, zz = 0;
+            if (p.group) {
+                uint16_t meta;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(meta) : "r"(wraw + kCodeBytes + 2 * wr));
+                s = meta & 0xffu;
+                zz = meta >> 8;
+            }
+            const uint32_t cst = static_cast<uint32_t>(128 - static_cast<int>(zz * s)) * 0x01010101u;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint4 v = ld_shared_v4(wraw + (((wh * 2 + i) * 128 + wr) << 4));
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t lo = w4[j] & 0x0F0F0F0Fu;
+                    const uint32_t hi = (w4[j] >> 4) & 0x0F0F0F0Fu;
+                    const uint32_t ulo = lo * s + cst;  // bytes: (q - z) * s + 128
+                    const uint32_t uhi = hi * s + cst;
+                    uint32_t f0, f1, f2, f3;
+                    biased_bytes_to_f16x4(ulo, f0, f1);
+                    biased_bytes_to_f16x4(uhi, f2, f3);
+                    st_shared_v4(a_atom + sw128_offset(wr, 4 * i + j), f0, f1, f2, f3);
+                }
+            }
+            // Activations: BT rows x 8 raw chunks of 16 int8 -> 2 fp16 chunks each.
+            for (int it = ct; it < BT * 8; it += kConvThreads) {
+                const int r = it % BT, c = it / BT;
+                const uint4 v = ld_shared_v4(raw + sw128_offset(r, c));
+                const uint32_t x4[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                                        v.w ^ 0x80808080u};
+                uint32_t f[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) biased_bytes_to_f16x4(x4[j], f[2 * j], f[2 * j + 1]);
+                const uint32_t b_atom = b_base + (c >> 2) * C::kBAtom;
+                const int cc = 2 * (c & 3);
+                st_shared_v4(b_atom + sw128_offset(r, cc), f[0], f[1], f[2], f[3]);
+                st_shared_v4(b_atom + sw128_offset(r, cc + 1), f[4], f[5], f[6], f[7]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&raw_empty[rs]);
+            mbar_arrive(&op_full[os]);
+        }
+    } else if (run && warp >= 4 && warp < 8) {
+        // ------------------------------------------------ epilogue warps --
+        const int et = threadIdx.x - 128;           // TMEM lane == weight row in tile
+        const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const int n = n0 + et;
+        const bool split_k = p.splits > 1;
+        const float sw = p.s_w ? h2f(p.s_w[n]) : 0.f;
+        int zc = 0;
+        if (p.group == 0) zc = p.packed[packed_z_offset(p.N, p.K) + n];
+        bool ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            const int cb = c & 1;
+            // warp-uniform outcome: the TMEM loads below are warp-collective
+            ok = __all_sync(0xffffffffu, mbar_wait(&chunk_full[cb], (c >> 1) & 1, abort_flag, p.status, tmo));
+            if (!ok) break;
+            tc_fence_after();
+            const bool last = c == nchunks - 1;
+#pragma unroll 1
+            for (int j = 0; j < BT / 16; ++j) {
+                uint32_t f[16], r[16];
+                tmem_ld16(tl + static_cast<uint32_t>((1 + cb) * BT + 16 * j), f);
+                if (c > 0) {
+                    tmem_ld16(tl + static_cast<uint32_t>(16 * j), r);
+                    tmem_wait_ld_regs(r);
+                }
+                tmem_wait_ld_regs(f);
+                uint32_t v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[i])) +
+                                                 (c > 0 ? static_cast<int>(r[i]) : 0));
+                if (!last) {
+                    tmem_st16(tl + static_cast<uint32_t>(16 * j), v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = m0 + 16 * j + i;
+                        if (m >= p.M) break;
+                        const size_t idx = static_cast<size_t>(m) * p.N + n;
+                        if (split_k) {
+                            atomicAdd(p.partials + idx, static_cast<int>(v[i]));
+                        } else {
+                            int acc = static_cast<int>(v[i]);
+                            if (p.group == 0) acc -= zc * p.t_x[m];
+                            if (p.acc_out)
+                                p.acc_out[idx] = acc;
+                            else
+                                p.O[idx] = __half_as_ushort(__float2half_rn(
+                                    __fmul_rn(__fmul_rn(static_cast<float>(acc), h2f(p.s_x[m])), sw)));
+                        }
+                    }
+                }
+            }
+            if (!last) tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&chunk_empty[cb]);
+        }
+        if (split_k) {
+            // Every epilogue thread reaches both named barriers exactly once.
+            // A failed wait anywhere has raised abort_flag before the first
+            // barrier, so the decision below is uniform.
+            if (ok) __threadfence();
+            named_bar_sync(1, kEpiThreads);
+            const int tile = n_tile * gridDim.x + tok_tile;
+            if (et == 0) {
+                int last_cta = 0;
+                if (*abort_flag == 0) {
+                    const unsigned prev = atomicAdd(p.counters + tile, 1u);
+                    last_cta = (prev == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+                }
+                *is_last = last_cta;
+            }
+            named_bar_sync(1, kEpiThreads);
+            if (*is_last) {
+                __threadfence();
+                const int mend = min(p.M, m0 + BT);
+                for (int m = m0; m < mend; ++m) {
+                    const size_t idx = static_cast<size_t>(m) * p.N + n;
+                    int acc = atomicExch(p.partials + idx, 0);
+                    if (p.group == 0) acc -= zc * p.t_x[m];
+                    if (p.acc_out)
+                        p.acc_out[idx] = acc;
+                    else
+                        p.O[idx] = __half_as_ushort(__float2half_rn(
+                            __fmul_rn(__fmul_rn(static_cast<float>(acc), h2f(p.s_x[m])), sw)));
+                }
+                if (et == 0) p.counters[tile] = 0u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+using CUtensorMapEncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                              const cuuint64_t *, const cuuint64_t *,
+                                              const cuuint32_t *, const cuuint32_t *,
+                                              CUtensorMapInterleave, CUtensorMapSwizzle,
+                                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+CUtensorMapEncodeTiledFn get_encode_fn() {
+    static CUtensorMapEncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &qres) == cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CUtensorMapEncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+template <int BT>
+cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
+    using C = Cfg<BT>;
+    static std::mutex mu;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !configured[dev]) {
+            e = cudaFuncSetAttribute(w4a8_gemm_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(C::kSmemBytes));
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
+    CUtensorMapEncodeTiledFn enc = get_encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K)};
+    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(BT)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(a.Qx), dims, strides,
+                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+    GemmParams p;
+    uint8_t *ws = static_cast<uint8_t *>(a.ws);
+    p.packed = static_cast<const uint8_t *>(a.packed);
+    p.s_x = a.s_x;
+    p.t_x = a.t_x;
+    p.s_w = a.s_w;
+    p.O = a.O;
+    p.acc_out = a.acc_out;
+    p.status = reinterpret_cast<uint32_t *>(ws);
+    p.counters = reinterpret_cast<uint32_t *>(ws + plan.counters_offset);
+    p.partials = reinterpret_cast<int32_t *>(ws + plan.partials_offset);
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.group = a.group;
+    p.G = a.K / kTileK;
+    p.splits = plan.splits;
+    p.debug_flags = a.debug_flags;
+    p.timeout_ns = a.timeout_ns;
+    dim3 grid(plan.tok_tiles, plan.n_tiles, plan.splits);
+    w4a8_gemm_kernel<BT><<<grid, kThreads, C::kSmemBytes, stream>>>(map, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+GemmPlan plan_gemm(int M, int N, int K, int num_sms, int force_bt, int force_splits) {
+    GemmPlan pl{};
+    int bt = force_bt;
+    if (bt == 0) bt = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
+    pl.BT = bt;
+    pl.tok_tiles = (M + bt - 1) / bt;
+    pl.n_tiles = N / kTileN;
+    const int G = K / kTileK;
+    const long long tiles = static_cast<long long>(pl.tok_tiles) * pl.n_tiles;
+    int best = 1;
+    if (force_splits > 0) {
+        best = force_splits < G ? force_splits : G;
+    } else if (tiles < num_sms) {
+        // Minimise (waves x stages per CTA), with a fixed per-CTA overhead of
+        // about two stages; ties go to fewer splits.
+        long long best_cost = -1;
+        const int smax = G < 64 ? G : 64;
+        for (int s = 1; s <= smax; ++s) {
+            const long long waves = (tiles * s + num_sms - 1) / num_sms;
+            const long long cost = waves * ((G + s - 1) / s + 2);
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost;
+                best = s;
+            }
+        }
+    }
+    pl.splits = best;
+    pl.counters_offset = kWsStatusBytes;
+    size_t end = kWsStatusBytes;
+    if (pl.splits > 1) {
+        end += (static_cast<size_t>(tiles) * 4 + 255) / 256 * 256;
+        pl.partials_offset = end;
+        end += static_cast<size_t>(M) * static_cast<size_t>(N) * 4;
+    } else {
+        pl.partials_offset = end;
+    }
+    pl.ws_bytes = end;
+    return pl;
+}
+
+cudaError_t launch_gemm(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
+    switch (plan.BT) {
+        case 16: return launch_bt<16>(a, plan, stream);
+        case 32: return launch_bt<32>(a, plan, stream);
+        case 64: return launch_bt<64>(a, plan, stream);
+        case 128: return launch_bt<128>(a, plan, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qoq

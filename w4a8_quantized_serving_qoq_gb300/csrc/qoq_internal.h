@@ -1,0 +1,103 @@
+// Library-internal declarations shared by the CUDA translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qoq {
+
+// ------------------------------------------------------------------------
+// Packed weight format (written by the packer, read by the GEMM).
+// [header: 256 B]
+// [blocks: (N/128) x (K/128) blocks, n-tile major, k-group minor]
+//   each block = 8192 B of 4-bit codes for 128 rows x 128 k, then, in group
+//   mode only, 256 B of metadata: per row r, byte 2r = s_g, byte 2r+1 = z.
+//   Code layout inside a block: 512 chunks of 16 B; chunk (p * 128 + r),
+//   p = 0..3, holds the 32 codes of row r at k = 32p .. 32p + 31 as four
+//   32-bit words; word j covers k = 32p + 8j + (0..7); byte b of a word holds
+//   the code of k = 8j + b in its low nibble and of k = 8j + b + 4 in its high
+//   nibble.
+// [per-channel mode only: z [N] bytes, padded to 16 B]
+// ------------------------------------------------------------------------
+constexpr uint32_t kPackedMagic = 0x57514F51u;  // "QOQW"
+constexpr uint32_t kPackedVersion = 1u;
+constexpr size_t kHeaderBytes = 256;
+constexpr uint32_t kCodeBytes = 8192;           // 128 x 128 x 4 bit
+constexpr uint32_t kMetaBytes = 256;            // 128 rows x (s_g, z)
+constexpr int kTileN = 128;                     // weight rows per tile
+constexpr int kTileK = 128;                     // k per stage = one group
+
+struct PackedHeader {
+    uint32_t magic;
+    uint32_t version;
+    int32_t N;
+    int32_t K;
+    int32_t group;
+    uint32_t block_bytes;
+    uint32_t illegal;     // codes that break the byte-lane bounds (0 when legal)
+    uint32_t reserved[57];
+};
+static_assert(sizeof(PackedHeader) == kHeaderBytes, "header size");
+
+__host__ __device__ inline uint32_t block_bytes(int group) { return group ? kCodeBytes + kMetaBytes : kCodeBytes; }
+
+__host__ __device__ inline size_t packed_bytes(int N, int K, int group) {
+    size_t blocks = static_cast<size_t>(N / kTileN) * static_cast<size_t>(K / kTileK);
+    size_t b = kHeaderBytes + blocks * block_bytes(group);
+    if (group == 0) b += (static_cast<size_t>(N) + 15) / 16 * 16;
+    return b;
+}
+
+__host__ __device__ inline size_t packed_z_offset(int N, int K) {
+    return kHeaderBytes + static_cast<size_t>(N / kTileN) * static_cast<size_t>(K / kTileK) * kCodeBytes;
+}
+
+// Workspace layout: [status word + pad: 256 B][tile counters][int32 partials].
+constexpr size_t kWsStatusBytes = 256;
+
+struct GemmPlan {
+    int BT;          // tokens per tile (MMA N): 16, 32, 64 or 128
+    int tok_tiles;   // ceil(M / BT)
+    int n_tiles;     // N / 128
+    int splits;      // K splits
+    size_t ws_bytes; // workspace needed
+    size_t counters_offset;
+    size_t partials_offset;
+};
+
+// Tile shape and K-split choice for one GEMM.  force_bt / force_splits
+// (0 = automatic) pin the choice for tests.
+GemmPlan plan_gemm(int M, int N, int K, int num_sms, int force_bt = 0, int force_splits = 0);
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
+                             int32_t *t_x, cudaStream_t stream);
+cudaError_t launch_quantize_weights(const uint16_t *W, int N, int K, int group, uint8_t *q4,
+                                    uint8_t *s_g, uint8_t *z, uint16_t *s_w, cudaStream_t stream);
+cudaError_t launch_pack(const uint8_t *q4, const uint8_t *s_g, const uint8_t *z, int N, int K,
+                        int group, void *packed, cudaStream_t stream);
+cudaError_t launch_unpack(const void *packed, int N, int K, int group, uint8_t *q4, uint8_t *s_g,
+                          uint8_t *z, cudaStream_t stream);
+
+struct GemmArgs {
+    const int8_t *Qx;
+    const uint16_t *s_x;
+    const int32_t *t_x;
+    const void *packed;
+    const uint16_t *s_w;
+    int M, N, K, group;
+    uint16_t *O;          // fp16 output, or null when acc_out is set
+    int32_t *acc_out;     // int32 pre-scale accumulators (test/debug mode)
+    void *ws;
+    uint32_t debug_flags;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_gemm(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream);
+
+// Debug flag: the TMA producer withholds the second stage's load, so the
+// consumers' bounded waits expire (exercises the timeout path).
+constexpr uint32_t kDebugWithholdStage = 1u;
+
+}  // namespace qoq

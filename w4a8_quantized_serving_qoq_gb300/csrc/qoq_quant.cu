@@ -1,0 +1,185 @@
+// Quantizers on the device:
+//  * per-token symmetric INT8 activation quantization (the step the QServe
+//    runtime fuses into the kernel before each GEMM; here a standalone,
+//    memory-bound kernel), and
+//  * the offline progressive group weight quantizer (per-channel INT8 in the
+//    protective range [-119, 119], then per-group UINT4 with a UINT8 scale and
+//    a UINT4 zero), plus the per-channel UINT4 variant.
+// Sources: "QServe: W4A8KV4 Quantization and System Co-design for Efficient LLM
+// Serving" (papercache summary), sections "整数量化" (eq. 1), "渐进式组量化"
+// (eq. 4/5) and "保护性量化范围"; "QServe：把 W4A8KV4 的理论收益做成实测吞吐的
+// 量化—系统协同设计" (zenmind review), sections 3.1 and 3.2.
+// Every float that decides an integer code is an IEEE fp32 division rounded
+// to nearest-even (__fdiv_rn), then rounded half-to-even to an integer.
+#include <cuda_fp16.h>
+
+#include "qoq_internal.h"
+
+namespace qoq {
+namespace {
+
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+__device__ __forceinline__ uint16_t f2h_rn(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+__device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+// Round-half-even of a / b for integers, b > 0.
+__device__ __forceinline__ int rne_div(int a, int b) {
+    int q = a / b, r = a - q * b;
+    if (r < 0) { q -= 1; r += b; }
+    if (2 * r > b || (2 * r == b && (q & 1))) q += 1;
+    return q;
+}
+
+template <typename T, typename Op>
+__device__ __forceinline__ T block_reduce(T v, Op op, T *sh) {
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) sh[warp] = v;
+    __syncthreads();
+    v = sh[0];
+    for (int w = 1; w < nw; ++w) v = op(v, sh[w]);
+    return v;
+}
+
+struct MaxOp { __device__ float operator()(float a, float b) const { return fmaxf(a, b); } };
+struct MinOp { __device__ float operator()(float a, float b) const { return fminf(a, b); } };
+struct SumOp { __device__ int operator()(int a, int b) const { return a + b; } };
+
+// One CTA per token row.  s_x = fp16(max|x| / 127); Qx = clamp(rne(x / s_x), -127, 127);
+// an all-zero scale gives an all-zero row; t_x = row sum of Qx.
+__global__ void quant_act_kernel(const uint16_t *__restrict__ X, int K, int8_t *__restrict__ Qx,
+                                 uint16_t *__restrict__ s_x, int32_t *__restrict__ t_x) {
+    __shared__ float shf[32];
+    __shared__ int shi[32];
+    const size_t m = blockIdx.x;
+    const uint4 *row = reinterpret_cast<const uint4 *>(X + m * K);
+    const int nv = K >> 3;
+    float amax = 0.f;
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        uint4 v = __ldg(row + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            amax = fmaxf(amax, fabsf(h2f(static_cast<uint16_t>(w[j] & 0xffffu))));
+            amax = fmaxf(amax, fabsf(h2f(static_cast<uint16_t>(w[j] >> 16))));
+        }
+    }
+    amax = block_reduce(amax, MaxOp(), shf);
+    const uint16_t sbits = f2h_rn(__fdiv_rn(amax, 127.0f));
+    const float sf = h2f(sbits);
+    int tsum = 0;
+    uint2 *qrow = reinterpret_cast<uint2 *>(Qx + m * K);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        uint4 v = __ldg(row + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint16_t hb = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu));
+            int q = 0;
+            if (sf != 0.f) q = clampi(__float2int_rn(__fdiv_rn(h2f(hb), sf)), -127, 127);
+            tsum += q;
+            out[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << ((j & 3) * 8);
+        }
+        qrow[i] = make_uint2(out[0], out[1]);
+    }
+    tsum = block_reduce(tsum, SumOp(), shi);
+    if (threadIdx.x == 0) {
+        s_x[m] = sbits;
+        if (t_x) t_x[m] = tsum;
+    }
+}
+
+// Progressive group quantization of one weight row per CTA.
+__global__ void quantize_group_kernel(const uint16_t *__restrict__ W, int K, int g,
+                                      uint8_t *__restrict__ q4, uint8_t *__restrict__ s_g,
+                                      uint8_t *__restrict__ zp, uint16_t *__restrict__ s_w) {
+    __shared__ float shf[32];
+    const size_t n = blockIdx.x;
+    const uint16_t *row = W + n * K;
+    float amax = 0.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(h2f(row[k])));
+    amax = block_reduce(amax, MaxOp(), shf);
+    uint16_t sbits = f2h_rn(__fdiv_rn(amax, 119.0f));
+    if ((sbits & 0x7fffu) == 0) sbits = 0x3c00u;  // 1.0
+    const float sf = h2f(sbits);
+    if (threadIdx.x == 0) s_w[n] = sbits;
+    const int G = K / g;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int per_lane = g / 32;  // g is a multiple of 32, at most 512
+    for (int gi = warp; gi < G; gi += nw) {
+        int q8[16];
+        int lo = 0, hi = 0;
+        for (int i = 0; i < per_lane; ++i) {
+            const int k = gi * g + i * 32 + lane;
+            q8[i] = clampi(__float2int_rn(__fdiv_rn(h2f(row[k]), sf)), -119, 119);
+            lo = min(lo, q8[i]);
+            hi = max(hi, q8[i]);
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        int s = (hi - lo + 14) / 15;
+        if (s < 1) s = 1;
+        const int z = clampi(rne_div(-lo, s), 0, 15);
+        for (int i = 0; i < per_lane; ++i) {
+            const int k = gi * g + i * 32 + lane;
+            q4[n * K + k] = static_cast<uint8_t>(clampi(rne_div(q8[i], s) + z, 0, 15));
+        }
+        if (lane == 0) {
+            s_g[n * G + gi] = static_cast<uint8_t>(s);
+            zp[n * G + gi] = static_cast<uint8_t>(z);
+        }
+    }
+}
+
+// Per-channel asymmetric UINT4 of one weight row per CTA.
+__global__ void quantize_channel_kernel(const uint16_t *__restrict__ W, int K,
+                                        uint8_t *__restrict__ q4, uint8_t *__restrict__ zp,
+                                        uint16_t *__restrict__ s_w) {
+    __shared__ float shf[32];
+    const size_t n = blockIdx.x;
+    const uint16_t *row = W + n * K;
+    float lo = 0.f, hi = 0.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        const float v = h2f(row[k]);
+        lo = fminf(lo, v);
+        hi = fmaxf(hi, v);
+    }
+    lo = block_reduce(lo, MinOp(), shf);
+    hi = block_reduce(hi, MaxOp(), shf);
+    uint16_t sbits = f2h_rn(__fdiv_rn(__fsub_rn(hi, lo), 15.0f));
+    if ((sbits & 0x7fffu) == 0) sbits = 0x3c00u;
+    const float sf = h2f(sbits);
+    const int z = clampi(__float2int_rn(__fdiv_rn(-lo, sf)), 0, 15);
+    if (threadIdx.x == 0) {
+        s_w[n] = sbits;
+        zp[n] = static_cast<uint8_t>(z);
+    }
+    for (int k = threadIdx.x; k < K; k += blockDim.x)
+        q4[n * K + k] = static_cast<uint8_t>(clampi(__float2int_rn(__fdiv_rn(h2f(row[k]), sf)) + z, 0, 15));
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
+                             int32_t *t_x, cudaStream_t stream) {
+    // Few long rows: one wide CTA per row keeps the per-row latency short.
+    const int threads = (M < 296) ? 1024 : 256;
+    quant_act_kernel<<<M, threads, 0, stream>>>(X, K, Qx, s_x, t_x);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weights(const uint16_t *W, int N, int K, int group, uint8_t *q4,
+                                    uint8_t *s_g, uint8_t *z, uint16_t *s_w, cudaStream_t stream) {
+    if (group > 0)
+        quantize_group_kernel<<<N, 256, 0, stream>>>(W, K, group, q4, s_g, z, s_w);
+    else
+        quantize_channel_kernel<<<N, 256, 0, stream>>>(W, K, q4, z, s_w);
+    return cudaGetLastError();
+}
+
+}  // namespace qoq
