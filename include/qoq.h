@@ -122,10 +122,13 @@ int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, in
                   qoq_stream_t stream);
 
 /*
- * Workspace bytes qoq_w4a8_gemm needs for this shape on the current device
- * (>= 256: a status word plus, when K is split across CTAs, tile counters
- * and int32 partial sums).  The workspace must be zero-filled once before
- * first use (qoq_workspace_init); every call leaves it zero-filled again.
+ * Workspace bytes qoq_w4a8_gemm needs for this shape on the current device:
+ * a 256-byte status word area, one arrival counter per persistent CTA and
+ * one int32 partial-tile slot (tokens-per-tile x 128) per persistent CTA,
+ * used when a CTA's share of the work ends inside an output tile.  The
+ * workspace must be zero-filled once before first use (qoq_workspace_init);
+ * every successful call leaves it zero-filled again (after a
+ * QOQ_ERR_TIMEOUT, re-initialise it).
  */
 size_t qoq_gemm_workspace_bytes(int M, int N, int K, int group);
 
@@ -165,8 +168,10 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  * Options for qoq_w4a8_gemm_ex (tests and tuning).  Zero-initialised fields
  * mean "automatic".
  *   tokens_per_tile : 16, 32, 64 or 128 (MMA N per CTA), 0 = automatic.
- *   k_splits        : CTAs sharing one output tile along K, 0 = automatic
- *                     (clamped to K/128).
+ *   num_ctas        : persistent CTAs that share the work (stream-K: the
+ *                     tiles x K/128 k-stages are cut into num_ctas equal
+ *                     contiguous ranges), 0 = one per SM; clamped to the
+ *                     number of k-stages.
  *   timeout_ns      : bound of every device-side wait, 0 = 2 s.
  *   debug_flags     : bit 0 = the copy warp withholds the second stage, so
  *                     the bounded waits expire (timeout path test).
@@ -175,7 +180,7 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  */
 typedef struct {
     int tokens_per_tile;
-    int k_splits;
+    int num_ctas;
     uint64_t timeout_ns;
     uint32_t debug_flags;
     int32_t *acc_out;

@@ -69,7 +69,7 @@ def test_gemm_options_validation(lib):
     opt = qoq.qoq_gemm_options(48, 0, 0, 0, None)
     assert lib.qoq_w4a8_gemm_ex(A, A, A, A, A, 16, 256, 512, 128, A, A, 1 << 20,
                                 ctypes.byref(opt), S) == 2
-    opt = qoq.qoq_gemm_options(0, 65, 0, 0, None)
+    opt = qoq.qoq_gemm_options(0, -1, 0, 0, None)
     assert lib.qoq_w4a8_gemm_ex(A, A, A, A, A, 16, 256, 512, 128, A, A, 1 << 20,
                                 ctypes.byref(opt), S) == 2
 

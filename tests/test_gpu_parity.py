@@ -169,18 +169,23 @@ def test_gemm_i32_bit_exact(M, N, K, group):
 
 
 @pytest.mark.parametrize("bt", [16, 32, 64, 128])
-@pytest.mark.parametrize("splits", [1, 2, 3, 7])
-def test_gemm_tiles_and_splits(bt, splits):
-    M, N, K = 37, 256, 896  # ragged token tail; 7 groups
+@pytest.mark.parametrize("ctas", [1, 2, 5, 13, 0])
+def test_gemm_tiles_and_stream_k_splits(bt, ctas):
+    """Every tile size, and persistent-CTA counts that cut output tiles at
+    different k-stages (exact int32 reduction of split tiles)."""
+    M, N, K = 37, 256, 1152  # ragged token tail; 9 groups (one chunk boundary)
     wq, Qx, sx, tx = _gemm_case(M, N, K, 77)
     packed, sw = _device_weights(wq, 128)
     ref = _ref_acc(wq, Qx, tx, 128)
     acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
-    opt = qoq.gemm_options(tokens_per_tile=bt, k_splits=splits, acc_out=acc)
-    qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128, options=opt)
-    assert np.array_equal(_np(acc), ref)
+    opt = qoq.gemm_options(tokens_per_tile=bt, num_ctas=ctas, acc_out=acc)
+    ws = qoq.new_workspace(qoq.qoq_gemm_workspace_bytes(M, N, K, 128, opt))
+    for _ in range(2):  # the workspace must come back zeroed
+        acc.fill_(0)
+        qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128, workspace=ws, options=opt)
+        assert np.array_equal(_np(acc), ref)
     O = qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N, K, 128,
-                             options=qoq.gemm_options(tokens_per_tile=bt, k_splits=splits))
+                             options=qoq.gemm_options(tokens_per_tile=bt, num_ctas=ctas))
     O_ref = oracle.epilogue_f64(ref, sx, wq["s_w"])
     assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
 
@@ -204,10 +209,10 @@ def test_gemm_exact_at_chunk_extremes():
     packed = qoq.qoq_pack_weights(_t(q4), _t(s_g), _t(z), 128)
     ref = oracle.gemm_i32_group(Qx, q4, s_g, z)
     assert abs(int(ref[0, 0])) == 127 * 120 * K
-    for splits in (1, 2):
+    for ctas in (1, 7, 0):
         acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
         qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128,
-                             options=qoq.gemm_options(k_splits=splits, acc_out=acc))
+                             options=qoq.gemm_options(num_ctas=ctas, acc_out=acc))
         assert np.array_equal(_np(acc), ref)
 
 
@@ -241,7 +246,7 @@ def test_end_to_end_tiny_workload():
 def test_workspace_too_small_rejected():
     M, N, K = 8, 256, 4096
     need = qoq.qoq_gemm_workspace_bytes(M, N, K, 128)
-    assert need > 256  # this shape splits K
+    assert need > 256  # status area plus counters and partial-tile slots
     ws = qoq.new_workspace(256)
     wq, Qx, sx, tx = _gemm_case(M, N, K, 3)
     packed, sw = _device_weights(wq, 128)
@@ -263,3 +268,22 @@ def test_mismatched_packed_weights_reported_on_device():
     assert float(O.abs().max()) == 0.0  # nothing written
     st, bits = qoq.qoq_workspace_status(ws)
     assert st == 0 and bits == 0  # cleared by the read
+
+
+def test_bounded_wait_timeout_reports_status_and_context_survives():
+    """The copy warp withholds one stage (debug flag), so the consumers'
+    bounded waits expire: the kernel must return, report QOQ_ERR_TIMEOUT
+    through the status word, free its resources, and leave the context
+    usable for a correct GEMM right after."""
+    M, N, K = 16, 256, 1024
+    wq, Qx, sx, tx = _gemm_case(M, N, K, 9)
+    packed, sw = _device_weights(wq, 128)
+    opt = qoq.gemm_options(num_ctas=1, debug_flags=1, timeout_ns=50_000_000)
+    ws = qoq.new_workspace(qoq.qoq_gemm_workspace_bytes(M, N, K, 128, opt))
+    O = torch.zeros((M, N), dtype=torch.float16, device=DEV)
+    qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N, K, 128, O=O, workspace=ws, options=opt)
+    st, bits = qoq.qoq_workspace_status(ws)
+    assert st == 6 and bits & 1
+    qoq.qoq_workspace_init(ws)
+    acc = qoq.qoq_w4a8_gemm_i32(_t(Qx), None, packed, N, K, 128)
+    assert np.array_equal(_np(acc), _ref_acc(wq, Qx, tx, 128))

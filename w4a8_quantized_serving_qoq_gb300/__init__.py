@@ -35,7 +35,7 @@ class QoqError(RuntimeError):
 class qoq_gemm_options(ctypes.Structure):
     _fields_ = [
         ("tokens_per_tile", ctypes.c_int),
-        ("k_splits", ctypes.c_int),
+        ("num_ctas", ctypes.c_int),
         ("timeout_ns", ctypes.c_uint64),
         ("debug_flags", ctypes.c_uint32),
         ("acc_out", ctypes.c_void_p),
@@ -250,8 +250,8 @@ def qoq_w4a8_gemm_i32(Qx, t_x, packed, N: int, K: int, group: int = 128, acc=Non
     return acc
 
 
-def gemm_options(tokens_per_tile=0, k_splits=0, timeout_ns=0, debug_flags=0, acc_out=None):
-    return qoq_gemm_options(tokens_per_tile, k_splits, timeout_ns, debug_flags,
+def gemm_options(tokens_per_tile=0, num_ctas=0, timeout_ns=0, debug_flags=0, acc_out=None):
+    return qoq_gemm_options(tokens_per_tile, num_ctas, timeout_ns, debug_flags,
                             None if acc_out is None else acc_out.data_ptr())
 
 

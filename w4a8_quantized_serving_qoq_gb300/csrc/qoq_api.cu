@@ -41,14 +41,14 @@ int check_options(const qoq_gemm_options *opt) {
     if (!opt) return QOQ_OK;
     const int bt = opt->tokens_per_tile;
     if (bt != 0 && bt != 16 && bt != 32 && bt != 64 && bt != 128) return QOQ_ERR_UNSUPPORTED;
-    if (opt->k_splits < 0 || opt->k_splits > 64) return QOQ_ERR_UNSUPPORTED;
+    if (opt->num_ctas < 0 || opt->num_ctas > 65536) return QOQ_ERR_UNSUPPORTED;
     return QOQ_OK;
 }
 
 bool plan_for(int M, int N, int K, const qoq_gemm_options *opt, qoq::GemmPlan *out) {
     const int sms = num_sms_current_device();
     if (sms <= 0) return false;
-    *out = qoq::plan_gemm(M, N, K, sms, opt ? opt->tokens_per_tile : 0, opt ? opt->k_splits : 0);
+    *out = qoq::plan_gemm(M, N, K, sms, opt ? opt->tokens_per_tile : 0, opt ? opt->num_ctas : 0);
     return true;
 }
 

@@ -42,14 +42,16 @@ namespace {
 
 constexpr int kThreads = 512;          // 16 warps
 constexpr int kConvThreads = 256;      // warps 8..15
-constexpr int kEpiThreads = 128;       // warps 4..7
+constexpr int kConvWarps = kConvThreads / 32;
+constexpr int kEpiWarps = 4;           // warps 4..7
+constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kChunkStages = 8;        // 8 x 128 k = 1024 k per exact fp32 chunk
 constexpr uint32_t kWRawBytes = 9216;  // 8448 B block slot rounded to 1 KB
 
 template <int BT>
 struct Cfg {
-    static constexpr int kRawStages = BT <= 32 ? 8 : (BT == 64 ? 6 : 3);
-    static constexpr int kOpStages = 2;
+    static constexpr int kRawStages = BT <= 32 ? 6 : (BT == 64 ? 4 : 3);
+    static constexpr int kOpStages = BT == 16 ? 4 : (BT == 128 ? 2 : 3);
     static constexpr uint32_t kAAtom = 128u * 128u;            // 128 rows x 64 fp16
     static constexpr uint32_t kBAtom = static_cast<uint32_t>(BT) * 128u;
     static constexpr uint32_t kOpStageBytes = 2 * kAAtom + 2 * kBAtom;
@@ -73,9 +75,12 @@ struct GemmParams {
     uint16_t *O;
     int32_t *acc_out;
     uint32_t *status;
-    uint32_t *counters;
-    int32_t *partials;
-    int M, N, K, group, G, splits;
+    uint32_t *counters;     // [ctas] arrival counters of split tiles
+    int32_t *slots;         // [ctas][BT][128] int32 partial tiles
+    int M, N, K, group, G;
+    int tok_tiles;
+    long long total;        // tiles * G stages
+    int ctas;
     uint32_t debug_flags;
     uint64_t timeout_ns;
 };
@@ -113,6 +118,48 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Persistent stream-K schedule: the tiles x G k-stages of the GEMM are cut
+// into `ctas` contiguous, equal ranges; CTA c owns [c*T/P, (c+1)*T/P).  A
+// range crosses tile boundaries; each piece inside one tile is a segment.
+// Tiles are ordered token-tile fastest, so neighbouring work shares weights.
+struct Segment {
+    int tile, k0, k1;
+};
+
+struct SegmentWalker {
+    long long w, w1;
+    int G;
+    __device__ SegmentWalker(const GemmParams &p, int cta)
+        : w((static_cast<long long>(cta) * p.total) / p.ctas),
+          w1((static_cast<long long>(cta + 1) * p.total) / p.ctas), G(p.G) {}
+    __device__ bool next(Segment &s) {
+        if (w >= w1) return false;
+        const long long t = w / G;
+        s.tile = static_cast<int>(t);
+        s.k0 = static_cast<int>(w - t * G);
+        const long long end = w1 - t * G;
+        s.k1 = end < G ? static_cast<int>(end) : G;
+        w = t * G + s.k1;
+        return true;
+    }
+};
+
+// CTA whose range holds global stage `s`.
+__device__ __forceinline__ int cta_of_stage(long long s, const GemmParams &p) {
+    return static_cast<int>(((s + 1) * p.ctas - 1) / p.total);
+}
+
+template <int BT>
+__device__ __forceinline__ void write_out(const GemmParams &p, int m, int n, int acc, int zc, float sw) {
+    const size_t idx = static_cast<size_t>(m) * p.N + n;
+    if (p.group == 0) acc -= zc * p.t_x[m];
+    if (p.acc_out)
+        p.acc_out[idx] = acc;
+    else
+        p.O[idx] = __half_as_ushort(
+            __float2half_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc), h2f(p.s_x[m])), sw)));
+}
+
 template <int BT>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_gemm_kernel(const __grid_constant__ CUtensorMap qx_map, const GemmParams p) {
@@ -138,12 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *is_last = abort_flag + 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tok_tile = blockIdx.x, n_tile = blockIdx.y, split = blockIdx.z;
-    const int m0 = tok_tile * BT, n0 = n_tile * kTileN;
-    const int g0 = static_cast<int>((static_cast<long long>(split) * p.G) / p.splits);
-    const int g1 = static_cast<int>((static_cast<long long>(split + 1) * p.G) / p.splits);
-    const int nst = g1 - g0;
-    const int nchunks = (nst + kChunkStages - 1) / kChunkStages;
+    const int cta = blockIdx.x;
     const uint32_t bb = block_bytes(p.group);
     const uint64_t tmo = p.timeout_ns;
 
@@ -157,15 +199,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         *is_last = 0;
         for (int i = 0; i < R; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], kConvThreads);
+            mbar_init(&raw_empty[i], kConvWarps);
         }
         for (int i = 0; i < OPS; ++i) {
-            mbar_init(&op_full[i], kConvThreads);
+            mbar_init(&op_full[i], kConvWarps);
             mbar_init(&op_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&chunk_full[i], 1);
-            mbar_init(&chunk_empty[i], kEpiThreads);
+            mbar_init(&chunk_empty[i], kEpiWarps);
         }
         mbar_init(mma_done, 1);
         fence_barrier_init();
@@ -175,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const bool run = (*hdr_ok != 0) && nst > 0;
+    const bool run = (*hdr_ok != 0);
 
     if (run && warp == 0) {
         // ------------------------------------------------ TMA producer --
@@ -183,18 +225,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
             prefetch_tensormap(&qx_map);
-            const uint8_t *wblk = p.packed + kHeaderBytes + (static_cast<size_t>(n_tile) * p.G + g0) * bb;
-            int issued = 0;
-            for (int t = 0; t < nst; ++t) {
-                const int slot = t % R, use = t / R;
-                if (use > 0 && !mbar_wait(&raw_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo))
-                    break;
-                if ((p.debug_flags & kDebugWithholdStage) && t == 1) break;
-                uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
-                mbar_arrive_expect_tx(&raw_full[slot], C::kQxRawBytes + bb);
-                tma_load_2d(dst, &qx_map, (g0 + t) * kTileK, m0, &raw_full[slot], pol_x);
-                tma_load_1d(dst + C::kQxRawBytes, wblk + static_cast<size_t>(t) * bb, bb, &raw_full[slot], pol_w);
-                issued = t + 1;
+            SegmentWalker walk(p, cta);
+            Segment sg;
+            int st = 0, issued = 0;
+            bool stop = false;
+            while (!stop && walk.next(sg)) {
+                const int tok_tile = sg.tile % p.tok_tiles, n_tile = sg.tile / p.tok_tiles;
+                const uint8_t *wblk = p.packed + kHeaderBytes + (static_cast<size_t>(n_tile) * p.G) * bb;
+                for (int k = sg.k0; k < sg.k1; ++k, ++st) {
+                    const int slot = st % R, use = st / R;
+                    if (use > 0 && !mbar_wait(&raw_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo)) {
+                        stop = true;
+                        break;
+                    }
+                    if ((p.debug_flags & kDebugWithholdStage) && st == 1) {
+                        stop = true;
+                        break;
+                    }
+                    uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
+                    mbar_arrive_expect_tx(&raw_full[slot], C::kQxRawBytes + bb);
+                    tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &raw_full[slot], pol_x);
+                    tma_load_1d(dst + C::kQxRawBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[slot],
+                                pol_w);
+                    issued = st + 1;
+                }
             }
             // Drain: every issued copy must land before the CTA exits.
             for (int t = (issued > R ? issued - R : 0); t < issued; ++t)
@@ -204,28 +258,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------- MMA issuer --
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(128, BT);
-            for (int t = 0; t < nst; ++t) {
-                const int c = t / kChunkStages;
-                const bool first = (t % kChunkStages) == 0;
-                const bool last = (t % kChunkStages) == kChunkStages - 1 || t == nst - 1;
-                const int cb = c & 1;
-                if (first && c >= 2 &&
-                    !mbar_wait(&chunk_empty[cb], ((c - 2) >> 1) & 1, abort_flag, p.status, tmo))
-                    break;
-                const int os = t % OPS, ouse = t / OPS;
-                if (!mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + static_cast<uint32_t>((1 + cb) * BT);
-                const uint32_t a_base = smem_u32(op_base + os * C::kOpStageBytes);
-                const uint32_t b_base = a_base + 2 * C::kAAtom;
+            SegmentWalker walk(p, cta);
+            Segment sg;
+            int st = 0, gc = 0;
+            bool stop = false;
+            while (!stop && walk.next(sg)) {
+                const int len = sg.k1 - sg.k0;
+                int cur = 0;
+                for (int i = 0; i < len; ++i, ++st) {
+                    const bool first = (i % kChunkStages) == 0;
+                    const bool last = (i % kChunkStages) == kChunkStages - 1 || i == len - 1;
+                    if (first) {
+                        cur = gc++;
+                        if (cur >= 2 &&
+                            !mbar_wait(&chunk_empty[cur & 1], ((cur - 2) >> 1) & 1, abort_flag, p.status, tmo)) {
+                            stop = true;
+                            break;
+                        }
+                    }
+                    const int os = st % OPS, ouse = st / OPS;
+                    if (!mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + static_cast<uint32_t>((1 + (cur & 1)) * BT);
+                    const uint32_t a_base = smem_u32(op_base + os * C::kOpStageBytes);
+                    const uint32_t b_base = a_base + 2 * C::kAAtom;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = desc_kmajor_sw128(a_base + (kk >> 2) * C::kAAtom + (kk & 3) * 32);
-                    const uint64_t bd = desc_kmajor_sw128(b_base + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
-                    mma_f16(d_tmem, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = desc_kmajor_sw128(a_base + (kk >> 2) * C::kAAtom + (kk & 3) * 32);
+                        const uint64_t bd = desc_kmajor_sw128(b_base + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
+                        mma_f16(d_tmem, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
+                    }
+                    mma_commit(&op_empty[os]);
+                    if (last) mma_commit(&chunk_full[cur & 1]);
                 }
-                mma_commit(&op_empty[os]);
-                if (last) mma_commit(&chunk_full[cb]);
             }
             // All issued MMAs must finish before TMEM is released.
             mma_commit(mma_done);
@@ -235,145 +303,162 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------- converter warps --
         const int ct = threadIdx.x - (kThreads - kConvThreads);
         const int wr = ct & 127, wh = ct >> 7;  // weight row, k half (64 k)
-        for (int t = 0; t < nst; ++t) {
-            const int rs = t % R, ruse = t / R, os = t % OPS, ouse = t / OPS;
-            if (!mbar_wait(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo)) break;
-            if (ouse > 0 && !mbar_wait(&op_empty[os], (ouse - 1) & 1, abort_flag, p.status, tmo)) break;
-            const uint32_t raw = smem_u32(raw_base + rs * C::kRawSlotBytes);
-            const uint32_t wraw = raw + C::kQxRawBytes;
-            const uint32_t a_atom = smem_u32(op_base + os * C::kOpStageBytes) + wh * C::kAAtom;
-            const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes) + 2 * C::kAAtom;
+        SegmentWalker walk(p, cta);
+        Segment sg;
+        int st = 0;
+        bool stop = false;
+        while (!stop && walk.next(sg)) {
+            for (int k = sg.k0; k < sg.k1; ++k, ++st) {
+                const int rs = st % R, ruse = st / R, os = st % OPS, ouse = st / OPS;
+                if (!mbar_wait(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo) ||
+                    (ouse > 0 && !mbar_wait(&op_empty[os], (ouse - 1) & 1, abort_flag, p.status, tmo))) {
+                    stop = true;
+                    break;
+                }
+                const uint32_t raw = smem_u32(raw_base + rs * C::kRawSlotBytes);
+                const uint32_t wraw = raw + C::kQxRawBytes;
+                const uint32_t a_atom = smem_u32(op_base + os * C::kOpStageBytes) + wh * C::kAAtom;
+                const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes) + 2 * C::kAAtom;
 
-            // Weights: row wr, k in [64*wh, 64*wh + 64): 2 raw chunks -> 8 fp16 chunks.
-            uint32_t s = 1, zz = 0;
-            if (p.group) {
-                uint16_t meta;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(meta) : "r"(wraw + kCodeBytes + 2 * wr));
-                s = meta & 0xffu;
-                zz = meta >> 8;
-            }
-            const uint32_t cst = static_cast<uint32_t>(128 - static_cast<int>(zz * s)) * 0x01010101u;
+                // Weights: row wr, k in [64*wh, 64*wh + 64): 2 raw chunks -> 8 fp16 chunks.
+                uint32_t s = 1, zz = 0;
+                if (p.group) {
+                    uint16_t meta;
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(meta) : "r"(wraw + kCodeBytes + 2 * wr));
+                    s = meta & 0xffu;
+                    zz = meta >> 8;
+                }
+                const uint32_t cst = static_cast<uint32_t>(128 - static_cast<int>(zz * s)) * 0x01010101u;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const uint4 v = ld_shared_v4(wraw + (((wh * 2 + i) * 128 + wr) << 4));
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                for (int i = 0; i < 2; ++i) {
+                    const uint4 v = ld_shared_v4(wraw + (((wh * 2 + i) * 128 + wr) << 4));
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t lo = w4[j] & 0x0F0F0F0Fu;
-                    const uint32_t hi = (w4[j] >> 4) & 0x0F0F0F0Fu;
-                    const uint32_t ulo = lo * s + cst;  // bytes: (q - z) * s + 128
-                    const uint32_t uhi = hi * s + cst;
-                    uint32_t f0, f1, f2, f3;
-                    biased_bytes_to_f16x4(ulo, f0, f1);
-                    biased_bytes_to_f16x4(uhi, f2, f3);
-                    st_shared_v4(a_atom + sw128_offset(wr, 4 * i + j), f0, f1, f2, f3);
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t lo = w4[j] & 0x0F0F0F0Fu;
+                        const uint32_t hi = (w4[j] >> 4) & 0x0F0F0F0Fu;
+                        const uint32_t ulo = lo * s + cst;  // bytes: (q - z) * s + 128
+                        const uint32_t uhi = hi * s + cst;
+                        uint32_t f0, f1, f2, f3;
+                        biased_bytes_to_f16x4(ulo, f0, f1);
+                        biased_bytes_to_f16x4(uhi, f2, f3);
+                        st_shared_v4(a_atom + sw128_offset(wr, 4 * i + j), f0, f1, f2, f3);
+                    }
+                }
+                // Activations: BT rows x 8 raw chunks of 16 int8 -> 2 fp16 chunks each.
+#pragma unroll
+                for (int it0 = 0; it0 < BT * 8; it0 += kConvThreads) {
+                    const int it = it0 + ct;
+                    if (BT * 8 % kConvThreads == 0 || it < BT * 8) {
+                        const int r = it % BT, c = it / BT;
+                        const uint4 v = ld_shared_v4(raw + sw128_offset(r, c));
+                        const uint32_t x4[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                                                v.w ^ 0x80808080u};
+                        uint32_t f[8];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) biased_bytes_to_f16x4(x4[j], f[2 * j], f[2 * j + 1]);
+                        const uint32_t b_atom = b_base + (c >> 2) * C::kBAtom;
+                        const int cc = 2 * (c & 3);
+                        st_shared_v4(b_atom + sw128_offset(r, cc), f[0], f[1], f[2], f[3]);
+                        st_shared_v4(b_atom + sw128_offset(r, cc + 1), f[4], f[5], f[6], f[7]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&raw_empty[rs]);
+                    mbar_arrive(&op_full[os]);
                 }
             }
-            // Activations: BT rows x 8 raw chunks of 16 int8 -> 2 fp16 chunks each.
-            for (int it = ct; it < BT * 8; it += kConvThreads) {
-                const int r = it % BT, c = it / BT;
-                const uint4 v = ld_shared_v4(raw + sw128_offset(r, c));
-                const uint32_t x4[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
-                                        v.w ^ 0x80808080u};
-                uint32_t f[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) biased_bytes_to_f16x4(x4[j], f[2 * j], f[2 * j + 1]);
-                const uint32_t b_atom = b_base + (c >> 2) * C::kBAtom;
-                const int cc = 2 * (c & 3);
-                st_shared_v4(b_atom + sw128_offset(r, cc), f[0], f[1], f[2], f[3]);
-                st_shared_v4(b_atom + sw128_offset(r, cc + 1), f[4], f[5], f[6], f[7]);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&raw_empty[rs]);
-            mbar_arrive(&op_full[os]);
         }
     } else if (run && warp >= 4 && warp < 8) {
         // ------------------------------------------------ epilogue warps --
         const int et = threadIdx.x - 128;           // TMEM lane == weight row in tile
         const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        const int n = n0 + et;
-        const bool split_k = p.splits > 1;
-        const float sw = p.s_w ? h2f(p.s_w[n]) : 0.f;
-        int zc = 0;
-        if (p.group == 0) zc = p.packed[packed_z_offset(p.N, p.K) + n];
+        SegmentWalker walk(p, cta);
+        Segment sg;
+        int gc = 0;
         bool ok = true;
-        for (int c = 0; c < nchunks; ++c) {
-            const int cb = c & 1;
-            // warp-uniform outcome: the TMEM loads below are warp-collective
-            ok = __all_sync(0xffffffffu, mbar_wait(&chunk_full[cb], (c >> 1) & 1, abort_flag, p.status, tmo));
-            if (!ok) break;
-            tc_fence_after();
-            const bool last = c == nchunks - 1;
+        while (ok && walk.next(sg)) {
+            const int tok_tile = sg.tile % p.tok_tiles, n_tile = sg.tile / p.tok_tiles;
+            const int m0 = tok_tile * BT, n = n_tile * kTileN + et;
+            const bool split = !(sg.k0 == 0 && sg.k1 == p.G);
+            const float sw = p.s_w ? h2f(p.s_w[n]) : 0.f;
+            const int zc = (p.group == 0) ? p.packed[packed_z_offset(p.N, p.K) + n] : 0;
+            const long long tfirst = static_cast<long long>(sg.tile) * p.G;
+            const int slot_idx = split ? cta_of_stage(tfirst, p) : 0;
+            int32_t *slot = p.slots + static_cast<size_t>(slot_idx) * (BT * kTileN);
+            const int nch = (sg.k1 - sg.k0 + kChunkStages - 1) / kChunkStages;
+            for (int c = 0; c < nch; ++c) {
+                const int cur = gc++;
+                const int cb = cur & 1;
+                // warp-uniform outcome: the TMEM loads below are warp-collective
+                ok = __all_sync(0xffffffffu, mbar_wait(&chunk_full[cb], (cur >> 1) & 1, abort_flag, p.status, tmo));
+                if (!ok) break;
+                tc_fence_after();
+                const bool last = c == nch - 1;
 #pragma unroll 1
-            for (int j = 0; j < BT / 16; ++j) {
-                uint32_t f[16], r[16];
-                tmem_ld16(tl + static_cast<uint32_t>((1 + cb) * BT + 16 * j), f);
-                if (c > 0) {
-                    tmem_ld16(tl + static_cast<uint32_t>(16 * j), r);
-                    tmem_wait_ld_regs(r);
-                }
-                tmem_wait_ld_regs(f);
-                uint32_t v[16];
+                for (int j = 0; j < BT / 16; ++j) {
+                    uint32_t f[16], r[16];
+                    tmem_ld16(tl + static_cast<uint32_t>((1 + cb) * BT + 16 * j), f);
+                    if (c > 0) {
+                        tmem_ld16(tl + static_cast<uint32_t>(16 * j), r);
+                        tmem_wait_ld_regs(r);
+                    }
+                    tmem_wait_ld_regs(f);
+                    uint32_t v[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[i])) +
-                                                 (c > 0 ? static_cast<int>(r[i]) : 0));
-                if (!last) {
-                    tmem_st16(tl + static_cast<uint32_t>(16 * j), v);
-                } else {
+                    for (int i = 0; i < 16; ++i)
+                        v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[i])) +
+                                                     (c > 0 ? static_cast<int>(r[i]) : 0));
+                    if (!last) {
+                        tmem_st16(tl + static_cast<uint32_t>(16 * j), v);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = m0 + 16 * j + i;
-                        if (m >= p.M) break;
-                        const size_t idx = static_cast<size_t>(m) * p.N + n;
-                        if (split_k) {
-                            atomicAdd(p.partials + idx, static_cast<int>(v[i]));
-                        } else {
-                            int acc = static_cast<int>(v[i]);
-                            if (p.group == 0) acc -= zc * p.t_x[m];
-                            if (p.acc_out)
-                                p.acc_out[idx] = acc;
+                        for (int i = 0; i < 16; ++i) {
+                            const int ml = 16 * j + i, m = m0 + ml;
+                            if (m >= p.M) break;
+                            if (split)
+                                atomicAdd(slot + ml * kTileN + et, static_cast<int>(v[i]));
                             else
-                                p.O[idx] = __half_as_ushort(__float2half_rn(
-                                    __fmul_rn(__fmul_rn(static_cast<float>(acc), h2f(p.s_x[m])), sw)));
+                                write_out<BT>(p, m, n, static_cast<int>(v[i]), zc, sw);
                         }
                     }
                 }
+                if (!last) tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&chunk_empty[cb]);
             }
-            if (!last) tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&chunk_empty[cb]);
-        }
-        if (split_k) {
-            // Every epilogue thread reaches both named barriers exactly once.
-            // A failed wait anywhere has raised abort_flag before the first
-            // barrier, so the decision below is uniform.
-            if (ok) __threadfence();
-            named_bar_sync(1, kEpiThreads);
-            const int tile = n_tile * gridDim.x + tok_tile;
-            if (et == 0) {
-                int last_cta = 0;
-                if (*abort_flag == 0) {
-                    const unsigned prev = atomicAdd(p.counters + tile, 1u);
-                    last_cta = (prev == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+            if (split) {
+                // Every epilogue thread reaches both named barriers once per
+                // split segment.  A failed wait anywhere has raised abort_flag
+                // before the first barrier, so the decision below is uniform.
+                if (ok) __threadfence();
+                named_bar_sync(1, kEpiThreads);
+                if (et == 0) {
+                    int last_cta = 0;
+                    if (*abort_flag == 0) {
+                        const long long tlast = tfirst + p.G - 1;
+                        const unsigned expected =
+                            static_cast<unsigned>(cta_of_stage(tlast, p) - slot_idx + 1);
+                        const unsigned prev = atomicAdd(p.counters + slot_idx, 1u);
+                        last_cta = (prev + 1 == expected) ? 1 : 0;
+                    }
+                    *is_last = last_cta;
                 }
-                *is_last = last_cta;
-            }
-            named_bar_sync(1, kEpiThreads);
-            if (*is_last) {
-                __threadfence();
-                const int mend = min(p.M, m0 + BT);
-                for (int m = m0; m < mend; ++m) {
-                    const size_t idx = static_cast<size_t>(m) * p.N + n;
-                    int acc = atomicExch(p.partials + idx, 0);
-                    if (p.group == 0) acc -= zc * p.t_x[m];
-                    if (p.acc_out)
-                        p.acc_out[idx] = acc;
-                    else
-                        p.O[idx] = __half_as_ushort(__float2half_rn(
-                            __fmul_rn(__fmul_rn(static_cast<float>(acc), h2f(p.s_x[m])), sw)));
+                named_bar_sync(1, kEpiThreads);
+                if (*is_last) {
+                    __threadfence();
+                    const int mend = min(p.M - m0, BT);
+                    for (int ml = 0; ml < mend; ++ml) {
+                        const int acc = atomicExch(slot + ml * kTileN + et, 0);
+                        write_out<BT>(p, m0 + ml, n, acc, zc, sw);
+                    }
+                    if (et == 0) p.counters[slot_idx] = 0u;
                 }
-                if (et == 0) p.counters[tile] = 0u;
+                named_bar_sync(1, kEpiThreads);  // is_last is rewritten by the next split segment
+                ok = ok && (*abort_flag == 0);
             }
         }
     }
@@ -445,59 +530,40 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     p.acc_out = a.acc_out;
     p.status = reinterpret_cast<uint32_t *>(ws);
     p.counters = reinterpret_cast<uint32_t *>(ws + plan.counters_offset);
-    p.partials = reinterpret_cast<int32_t *>(ws + plan.partials_offset);
+    p.slots = reinterpret_cast<int32_t *>(ws + plan.slots_offset);
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
     p.group = a.group;
-    p.G = a.K / kTileK;
-    p.splits = plan.splits;
+    p.G = plan.G;
+    p.tok_tiles = plan.tok_tiles;
+    p.total = plan.total;
+    p.ctas = plan.ctas;
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
-    dim3 grid(plan.tok_tiles, plan.n_tiles, plan.splits);
+    dim3 grid(plan.ctas);
     w4a8_gemm_kernel<BT><<<grid, kThreads, C::kSmemBytes, stream>>>(map, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-GemmPlan plan_gemm(int M, int N, int K, int num_sms, int force_bt, int force_splits) {
+GemmPlan plan_gemm(int M, int N, int K, int num_sms, int force_bt, int force_ctas) {
     GemmPlan pl{};
     int bt = force_bt;
     if (bt == 0) bt = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
     pl.BT = bt;
     pl.tok_tiles = (M + bt - 1) / bt;
     pl.n_tiles = N / kTileN;
-    const int G = K / kTileK;
-    const long long tiles = static_cast<long long>(pl.tok_tiles) * pl.n_tiles;
-    int best = 1;
-    if (force_splits > 0) {
-        best = force_splits < G ? force_splits : G;
-    } else if (tiles < num_sms) {
-        // Minimise (waves x stages per CTA), with a fixed per-CTA overhead of
-        // about two stages; ties go to fewer splits.
-        long long best_cost = -1;
-        const int smax = G < 64 ? G : 64;
-        for (int s = 1; s <= smax; ++s) {
-            const long long waves = (tiles * s + num_sms - 1) / num_sms;
-            const long long cost = waves * ((G + s - 1) / s + 2);
-            if (best_cost < 0 || cost < best_cost) {
-                best_cost = cost;
-                best = s;
-            }
-        }
-    }
-    pl.splits = best;
+    pl.G = K / kTileK;
+    pl.tiles = static_cast<long long>(pl.tok_tiles) * pl.n_tiles;
+    pl.total = pl.tiles * pl.G;
+    long long ctas = force_ctas > 0 ? force_ctas : num_sms;
+    if (ctas > pl.total) ctas = pl.total;
+    pl.ctas = static_cast<int>(ctas);
     pl.counters_offset = kWsStatusBytes;
-    size_t end = kWsStatusBytes;
-    if (pl.splits > 1) {
-        end += (static_cast<size_t>(tiles) * 4 + 255) / 256 * 256;
-        pl.partials_offset = end;
-        end += static_cast<size_t>(M) * static_cast<size_t>(N) * 4;
-    } else {
-        pl.partials_offset = end;
-    }
-    pl.ws_bytes = end;
+    pl.slots_offset = kWsStatusBytes + (static_cast<size_t>(pl.ctas) * 4 + 255) / 256 * 256;
+    pl.ws_bytes = pl.slots_offset + static_cast<size_t>(pl.ctas) * bt * kTileN * 4;
     return pl;
 }
 

@@ -53,22 +53,26 @@ __host__ __device__ inline size_t packed_z_offset(int N, int K) {
     return kHeaderBytes + static_cast<size_t>(N / kTileN) * static_cast<size_t>(K / kTileK) * kCodeBytes;
 }
 
-// Workspace layout: [status word + pad: 256 B][tile counters][int32 partials].
+// Workspace layout: [status word + pad: 256 B][ctas arrival counters][ctas x BT x 128
+// int32 partial-tile slots].
 constexpr size_t kWsStatusBytes = 256;
 
 struct GemmPlan {
-    int BT;          // tokens per tile (MMA N): 16, 32, 64 or 128
-    int tok_tiles;   // ceil(M / BT)
-    int n_tiles;     // N / 128
-    int splits;      // K splits
-    size_t ws_bytes; // workspace needed
+    int BT;                // tokens per tile (MMA N): 16, 32, 64 or 128
+    int tok_tiles;         // ceil(M / BT)
+    int n_tiles;           // N / 128
+    int G;                 // K / 128 k-stages per tile
+    long long tiles;       // tok_tiles * n_tiles
+    long long total;       // tiles * G stages of work
+    int ctas;              // persistent CTAs (stream-K ranges)
+    size_t ws_bytes;       // workspace needed
     size_t counters_offset;
-    size_t partials_offset;
+    size_t slots_offset;
 };
 
-// Tile shape and K-split choice for one GEMM.  force_bt / force_splits
+// Tile shape and persistent-CTA count for one GEMM.  force_bt / force_ctas
 // (0 = automatic) pin the choice for tests.
-GemmPlan plan_gemm(int M, int N, int K, int num_sms, int force_bt = 0, int force_splits = 0);
+GemmPlan plan_gemm(int M, int N, int K, int num_sms, int force_bt = 0, int force_ctas = 0);
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
