@@ -68,6 +68,7 @@ int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const
         return QOQ_ERR_MISALIGNED;
     qoq::GemmPlan plan;
     if (!plan_for(M, N, K, opt, &plan)) return QOQ_ERR_CUDA;
+    if (plan.total * (plan.ctas + 1ll) >= (1ll << 32)) return QOQ_ERR_UNSUPPORTED;
     if (ws_bytes < plan.ws_bytes) return QOQ_ERR_WORKSPACE;
     qoq::GemmArgs a;
     a.Qx = Qx;

@@ -41,8 +41,9 @@ namespace qoq {
 namespace {
 
 constexpr int kThreads = 512;          // 16 warps
-constexpr int kConvThreads = 256;      // warps 8..15
+constexpr int kConvThreads = 256;      // warps 8..15: two groups of 4 warps
 constexpr int kConvWarps = kConvThreads / 32;
+constexpr int kConvGroupWarps = kConvWarps / 2;  // one group converts one stage
 constexpr int kEpiWarps = 4;           // warps 4..7
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kChunkStages = 8;        // 8 x 128 k = 1024 k per exact fp32 chunk
@@ -50,19 +51,22 @@ constexpr uint32_t kWRawBytes = 9216;  // 8448 B block slot rounded to 1 KB
 
 template <int BT>
 struct Cfg {
-    static constexpr int kRawStages = BT <= 32 ? 6 : (BT == 64 ? 4 : 3);
-    static constexpr int kOpStages = BT == 16 ? 4 : (BT == 128 ? 2 : 3);
-    static constexpr uint32_t kAAtom = 128u * 128u;            // 128 rows x 64 fp16
-    static constexpr uint32_t kBAtom = static_cast<uint32_t>(BT) * 128u;
-    static constexpr uint32_t kOpStageBytes = 2 * kAAtom + 2 * kBAtom;
+    // TMEM columns: [0, BT) int32 running sum, [BT, 3BT) two fp32 chunk
+    // accumulators, [kA0, kA0 + 64 * kOpStages) fp16 weight operand stages
+    // (128 lanes x 64 columns = 128 rows x 128 k each).
+    static constexpr int kOpStages = BT == 128 ? 2 : 4;
+    static constexpr int kRawStages = BT <= 32 ? 12 : (BT == 64 ? 8 : 6);
+    static constexpr uint32_t kA0 = ((3 * BT + 63) / 64) * 64;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kBAtom = static_cast<uint32_t>(BT) * 128u;  // BT rows x 64 fp16
+    static constexpr uint32_t kOpStageBytes = 2 * kBAtom;
     static constexpr uint32_t kQxRawBytes = static_cast<uint32_t>(BT) * 128u;
     static constexpr uint32_t kRawSlotBytes = kQxRawBytes + kWRawBytes;
-    static constexpr uint32_t kTmemCols = BT <= 16 ? 64 : (BT <= 32 ? 128 : (BT <= 64 ? 256 : 512));
     static constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 4 + 1;
-    static constexpr uint32_t kMiscBytes = 1024;
+    static constexpr uint32_t kMiscBytes = 2048;  // barriers + flags, then s_x / t_x of the current tile
     static constexpr uint32_t kSmemBytes =
         kOpStages * kOpStageBytes + kRawStages * kRawSlotBytes + kMiscBytes + 1024;
-    static_assert(3 * BT <= static_cast<int>(kTmemCols), "TMEM columns");
+    static_assert(kA0 + 64 * kOpStages <= kTmemCols, "TMEM columns");
     static_assert(kNumBars * 8 + 64 <= static_cast<int>(kMiscBytes), "barrier area");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -127,37 +131,45 @@ struct Segment {
 };
 
 struct SegmentWalker {
-    long long w, w1;
-    int G;
+    uint32_t w, w1, G;  // total stages < 2^31 (checked on the host)
+    // ctas * total < 2^32 (checked on the host), so 32-bit arithmetic is exact.
     __device__ SegmentWalker(const GemmParams &p, int cta)
-        : w((static_cast<long long>(cta) * p.total) / p.ctas),
-          w1((static_cast<long long>(cta + 1) * p.total) / p.ctas), G(p.G) {}
+        : w(static_cast<uint32_t>(cta) * static_cast<uint32_t>(p.total) / static_cast<uint32_t>(p.ctas)),
+          w1(static_cast<uint32_t>(cta + 1) * static_cast<uint32_t>(p.total) / static_cast<uint32_t>(p.ctas)),
+          G(static_cast<uint32_t>(p.G)) {}
     __device__ bool next(Segment &s) {
         if (w >= w1) return false;
-        const long long t = w / G;
+        const uint32_t t = w / G;
         s.tile = static_cast<int>(t);
         s.k0 = static_cast<int>(w - t * G);
-        const long long end = w1 - t * G;
-        s.k1 = end < G ? static_cast<int>(end) : G;
-        w = t * G + s.k1;
+        const uint32_t end = w1 - t * G;
+        s.k1 = static_cast<int>(end < G ? end : G);
+        w = t * G + static_cast<uint32_t>(s.k1);
         return true;
     }
 };
 
 // CTA whose range holds global stage `s`.
-__device__ __forceinline__ int cta_of_stage(long long s, const GemmParams &p) {
-    return static_cast<int>(((s + 1) * p.ctas - 1) / p.total);
+__device__ __forceinline__ int cta_of_stage(uint32_t s, const GemmParams &p) {
+    return static_cast<int>(((s + 1) * static_cast<uint32_t>(p.ctas) - 1) / static_cast<uint32_t>(p.total));
 }
 
-template <int BT>
-__device__ __forceinline__ void write_out(const GemmParams &p, int m, int n, int acc, int zc, float sw) {
+// Final output of one accumulator: per-channel zero fold, then either the
+// int32 value (test mode) or fp16(acc * s_x[m] * s_w[n]).
+__device__ __forceinline__ void write_out(const GemmParams &p, int m, int n, int acc, int zc, int tx,
+                                          float sx, float sw) {
     const size_t idx = static_cast<size_t>(m) * p.N + n;
-    if (p.group == 0) acc -= zc * p.t_x[m];
+    acc -= zc * tx;
     if (p.acc_out)
         p.acc_out[idx] = acc;
     else
-        p.O[idx] = __half_as_ushort(
-            __float2half_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc), h2f(p.s_x[m])), sw)));
+        p.O[idx] = __half_as_ushort(__float2half_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc), sx), sw)));
+}
+
+__device__ __forceinline__ int ld_cg_s32(const int32_t *p) {
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 template <int BT>
@@ -183,6 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *hdr_ok = abort_flag + 1;
     volatile int *is_last = abort_flag + 2;
+    float *tile_sx = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 1024);
+    int *tile_tx = reinterpret_cast<int *>(tile_sx + 128);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
@@ -190,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
+        prefetch_tensormap(&qx_map);
         const PackedHeader *h = reinterpret_cast<const PackedHeader *>(p.packed);
         const bool ok = h->magic == kPackedMagic && h->version == kPackedVersion && h->N == p.N &&
                         h->K == p.K && h->group == p.group && h->illegal == 0u;
@@ -199,10 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         *is_last = 0;
         for (int i = 0; i < R; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], kConvWarps);
+            mbar_init(&raw_empty[i], kConvGroupWarps);
         }
         for (int i = 0; i < OPS; ++i) {
-            mbar_init(&op_full[i], kConvWarps);
+            mbar_init(&op_full[i], kConvGroupWarps);
             mbar_init(&op_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -222,9 +237,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (run && warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            const uint64_t pol_w = l2_policy_evict_first();
-            const uint64_t pol_x = l2_policy_evict_last();
-            prefetch_tensormap(&qx_map);
             SegmentWalker walk(p, cta);
             Segment sg;
             int st = 0, issued = 0;
@@ -244,9 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
                     mbar_arrive_expect_tx(&raw_full[slot], C::kQxRawBytes + bb);
-                    tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &raw_full[slot], pol_x);
-                    tma_load_1d(dst + C::kQxRawBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[slot],
-                                pol_w);
+                    tma_load_1d(dst + C::kQxRawBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[slot]);
+                    tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &raw_full[slot]);
                     issued = st + 1;
                 }
             }
@@ -256,12 +267,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (run && warp == 1) {
         // ------------------------------------------------- MMA issuer --
+        // One thread.  A shared-memory read right after a batch of MMAs waits
+        // behind them, so the readiness test of the next operand stage is
+        // issued before this stage's MMAs and consumed after them.
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(128, BT);
             SegmentWalker walk(p, cta);
+            const int my_stages = static_cast<int>(walk.w1 - walk.w);
             Segment sg;
             int st = 0, gc = 0;
-            bool stop = false;
+            bool stop = false, ready = false;
             while (!stop && walk.next(sg)) {
                 const int len = sg.k1 - sg.k0;
                 int cur = 0;
@@ -277,22 +292,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     const int os = st % OPS, ouse = st / OPS;
-                    if (!mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
+                    if (!ready && !mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
                         stop = true;
                         break;
                     }
+                    const int nx = st + 1;
+                    const bool next_ready = nx < my_stages && mbar_test(&op_full[nx % OPS], (nx / OPS) & 1);
                     tc_fence_after();
                     const uint32_t d_tmem = tmem + static_cast<uint32_t>((1 + (cur & 1)) * BT);
-                    const uint32_t a_base = smem_u32(op_base + os * C::kOpStageBytes);
-                    const uint32_t b_base = a_base + 2 * C::kAAtom;
+                    const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u;
+                    const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = desc_kmajor_sw128(a_base + (kk >> 2) * C::kAAtom + (kk & 3) * 32);
                         const uint64_t bd = desc_kmajor_sw128(b_base + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
-                        mma_f16(d_tmem, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
+                        mma_f16_tmem_a(d_tmem, a_tmem + 8u * kk, bd, idesc, (first && kk == 0) ? 0u : 1u);
                     }
                     mma_commit(&op_empty[os]);
                     if (last) mma_commit(&chunk_full[cur & 1]);
+                    ready = next_ready;
                 }
             }
             // All issued MMAs must finish before TMEM is released.
@@ -301,26 +318,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (run && warp >= 8) {
         // ---------------------------------------------- converter warps --
-        const int ct = threadIdx.x - (kThreads - kConvThreads);
-        const int wr = ct & 127, wh = ct >> 7;  // weight row, k half (64 k)
+        // Two groups of four warps take alternate stages, so one group's
+        // waits and fences overlap the other group's arithmetic.  In a group,
+        // warp w converts weight rows 32*(w%4) .. +31 (its TMEM lane quarter)
+        // over the whole 128-k stage.
+        const int cg = (warp - 8) >> 2;
+        const int wr = (warp & 3) * 32 + lane;   // weight row == TMEM lane
+        const uint32_t a_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         SegmentWalker walk(p, cta);
         Segment sg;
         int st = 0;
         bool stop = false;
         while (!stop && walk.next(sg)) {
             for (int k = sg.k0; k < sg.k1; ++k, ++st) {
+                if ((st & 1) != cg) continue;
                 const int rs = st % R, ruse = st / R, os = st % OPS, ouse = st / OPS;
-                if (!mbar_wait(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo) ||
-                    (ouse > 0 && !mbar_wait(&op_empty[os], (ouse - 1) & 1, abort_flag, p.status, tmo))) {
+                if (!mbar_wait_warp(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo) ||
+                    (ouse > 0 && !mbar_wait_warp(&op_empty[os], (ouse - 1) & 1, abort_flag, p.status, tmo))) {
                     stop = true;
                     break;
                 }
+                tc_fence_after();
                 const uint32_t raw = smem_u32(raw_base + rs * C::kRawSlotBytes);
                 const uint32_t wraw = raw + C::kQxRawBytes;
-                const uint32_t a_atom = smem_u32(op_base + os * C::kOpStageBytes) + wh * C::kAAtom;
-                const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes) + 2 * C::kAAtom;
+                const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes);
 
-                // Weights: row wr, k in [64*wh, 64*wh + 64): 2 raw chunks -> 8 fp16 chunks.
+                // Weights: row wr, 4 raw chunks of 32 k -> 128 fp16 -> 64 TMEM
+                // columns of this thread's lane (2 fp16 per column), in two halves.
                 uint32_t s = 1, zz = 0;
                 if (p.group) {
                     uint16_t meta;
@@ -330,26 +354,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t cst = static_cast<uint32_t>(128 - static_cast<int>(zz * s)) * 0x01010101u;
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const uint4 v = ld_shared_v4(wraw + (((wh * 2 + i) * 128 + wr) << 4));
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t a_frag[32];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t lo = w4[j] & 0x0F0F0F0Fu;
-                        const uint32_t hi = (w4[j] >> 4) & 0x0F0F0F0Fu;
-                        const uint32_t ulo = lo * s + cst;  // bytes: (q - z) * s + 128
-                        const uint32_t uhi = hi * s + cst;
-                        uint32_t f0, f1, f2, f3;
-                        biased_bytes_to_f16x4(ulo, f0, f1);
-                        biased_bytes_to_f16x4(uhi, f2, f3);
-                        st_shared_v4(a_atom + sw128_offset(wr, 4 * i + j), f0, f1, f2, f3);
+                    for (int i = 0; i < 2; ++i) {
+                        const uint4 v = ld_shared_v4(wraw + (((h * 2 + i) * 128 + wr) << 4));
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t lo = w4[j] & 0x0F0F0F0Fu;
+                            const uint32_t hi = (w4[j] >> 4) & 0x0F0F0F0Fu;
+                            const uint32_t ulo = lo * s + cst;  // bytes: (q - z) * s + 128
+                            const uint32_t uhi = hi * s + cst;
+                            uint32_t *f = a_frag + 16 * i + 4 * j;
+                            biased_bytes_to_f16x4(ulo, f[0], f[1]);
+                            biased_bytes_to_f16x4(uhi, f[2], f[3]);
+                        }
                     }
+                    tmem_st32(a_lane + C::kA0 + static_cast<uint32_t>(os) * 64u + 32u * h, a_frag);
                 }
                 // Activations: BT rows x 8 raw chunks of 16 int8 -> 2 fp16 chunks each.
+                constexpr int kGroupThreads = 32 * kConvGroupWarps;
 #pragma unroll
-                for (int it0 = 0; it0 < BT * 8; it0 += kConvThreads) {
-                    const int it = it0 + ct;
-                    if (BT * 8 % kConvThreads == 0 || it < BT * 8) {
+                for (int it0 = 0; it0 < BT * 8; it0 += kGroupThreads) {
+                    const int it = it0 + wr;
+                    if (BT * 8 % kGroupThreads == 0 || it < BT * 8) {
                         const int r = it % BT, c = it / BT;
                         const uint4 v = ld_shared_v4(raw + sw128_offset(r, c));
                         const uint32_t x4[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
@@ -364,6 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 fence_proxy_async_smem();
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&raw_empty[rs]);
@@ -378,22 +409,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         SegmentWalker walk(p, cta);
         Segment sg;
         int gc = 0;
+        // All four epilogue warps take every named barrier below the same number
+        // of times: they walk the same segments and leave the walk together,
+        // on a decision read from the shared abort flag after a barrier (any
+        // failed wait has raised it before that barrier).
         bool ok = true;
-        while (ok && walk.next(sg)) {
+        while (walk.next(sg)) {
             const int tok_tile = sg.tile % p.tok_tiles, n_tile = sg.tile / p.tok_tiles;
             const int m0 = tok_tile * BT, n = n_tile * kTileN + et;
             const bool split = !(sg.k0 == 0 && sg.k1 == p.G);
             const float sw = p.s_w ? h2f(p.s_w[n]) : 0.f;
             const int zc = (p.group == 0) ? p.packed[packed_z_offset(p.N, p.K) + n] : 0;
-            const long long tfirst = static_cast<long long>(sg.tile) * p.G;
+            const uint32_t tfirst = static_cast<uint32_t>(sg.tile) * static_cast<uint32_t>(p.G);
             const int slot_idx = split ? cta_of_stage(tfirst, p) : 0;
             int32_t *slot = p.slots + static_cast<size_t>(slot_idx) * (BT * kTileN);
             const int nch = (sg.k1 - sg.k0 + kChunkStages - 1) / kChunkStages;
+            // Stage this tile's per-token scale (and row sums) in shared memory.
+            named_bar_sync(2, kEpiThreads);
+            if (et < BT) {
+                const int m = m0 + et;
+                tile_sx[et] = (m < p.M && p.s_x) ? h2f(p.s_x[m]) : 0.f;
+                tile_tx[et] = (m < p.M && p.group == 0) ? p.t_x[m] : 0;
+            }
+            named_bar_sync(2, kEpiThreads);
             for (int c = 0; c < nch; ++c) {
                 const int cur = gc++;
                 const int cb = cur & 1;
                 // warp-uniform outcome: the TMEM loads below are warp-collective
-                ok = __all_sync(0xffffffffu, mbar_wait(&chunk_full[cb], (cur >> 1) & 1, abort_flag, p.status, tmo));
+                ok = mbar_wait_warp(&chunk_full[cb], (cur >> 1) & 1, abort_flag, p.status, tmo);
                 if (!ok) break;
                 tc_fence_after();
                 const bool last = c == nch - 1;
@@ -421,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (split)
                                 atomicAdd(slot + ml * kTileN + et, static_cast<int>(v[i]));
                             else
-                                write_out<BT>(p, m, n, static_cast<int>(v[i]), zc, sw);
+                                write_out(p, m, n, static_cast<int>(v[i]), zc, tile_tx[ml], tile_sx[ml], sw);
                         }
                     }
                 }
@@ -434,33 +477,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Every epilogue thread reaches both named barriers once per
                 // split segment.  A failed wait anywhere has raised abort_flag
                 // before the first barrier, so the decision below is uniform.
-                if (ok) __threadfence();
+                // One thread publishes the tile's partial sums (the barrier
+                // orders the other threads' red.adds before its fence) and
+                // learns whether this CTA is the tile's last contributor.
                 named_bar_sync(1, kEpiThreads);
                 if (et == 0) {
                     int last_cta = 0;
                     if (*abort_flag == 0) {
-                        const long long tlast = tfirst + p.G - 1;
+                        __threadfence();
+                        const uint32_t tlast = tfirst + static_cast<uint32_t>(p.G) - 1u;
                         const unsigned expected =
                             static_cast<unsigned>(cta_of_stage(tlast, p) - slot_idx + 1);
                         const unsigned prev = atomicAdd(p.counters + slot_idx, 1u);
                         last_cta = (prev + 1 == expected) ? 1 : 0;
+                        if (last_cta) __threadfence();
                     }
                     *is_last = last_cta;
                 }
                 named_bar_sync(1, kEpiThreads);
                 if (*is_last) {
-                    __threadfence();
                     const int mend = min(p.M - m0, BT);
-                    for (int ml = 0; ml < mend; ++ml) {
-                        const int acc = atomicExch(slot + ml * kTileN + et, 0);
-                        write_out<BT>(p, m0 + ml, n, acc, zc, sw);
+                    // Every contributor's red.add landed in L2 before its
+                    // counter increment; read the sums from L2 (16 loads in
+                    // flight), then re-zero the slot for the next call.
+                    for (int ml0 = 0; ml0 < mend; ml0 += 16) {
+                        int acc[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[i] = (ml0 + i < mend) ? ld_cg_s32(slot + (ml0 + i) * kTileN + et) : 0;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (ml0 + i < mend) {
+                                slot[(ml0 + i) * kTileN + et] = 0;
+                                write_out(p, m0 + ml0 + i, n, acc[i], zc, tile_tx[ml0 + i], tile_sx[ml0 + i], sw);
+                            }
+                        }
                     }
                     if (et == 0) p.counters[slot_idx] = 0u;
                 }
-                named_bar_sync(1, kEpiThreads);  // is_last is rewritten by the next split segment
-                ok = ok && (*abort_flag == 0);
             }
+            named_bar_sync(1, kEpiThreads);  // also: is_last is rewritten by the next split segment
+            if (*abort_flag != 0) break;
         }
+        (void)ok;
     }
 
     tc_fence_before();
