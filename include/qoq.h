@@ -195,6 +195,35 @@ int qoq_w4a8_gemm_ex(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x,
                      qoq_stream_t stream);
 
 /*
+ * qoq_w4a8_gemm_noalloc -- the same GEMM (same arguments and results as
+ * qoq_w4a8_gemm) for callers that cannot allocate device memory: for
+ * example a plugin inside another framework's engine that is handed only its
+ * input and output buffers, or a latency-critical path that must not call
+ * cudaMalloc because it can synchronize the device.  The paper has no
+ * counterpart of this entry point.
+ * Its scratch (status word, arrival counters, partial-tile slots) is a fixed
+ * 8 MiB array inside the library, which every GPU that loads the library
+ * keeps until the process exits.  It never calls cudaMalloc, cudaFree or any
+ * allocating routine.
+ *  - Limit: shapes whose scratch need (qoq_gemm_workspace_bytes) exceeds
+ *    8 MiB are rejected with QOQ_ERR_WORKSPACE before any launch; on a
+ *    152-SM GB300 that admits up to 64 tokens (M <= 64).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    outside any stream capture.
+ *  - Every call re-zeroes the part of the array it uses (cudaMemsetAsync on
+ *    `stream`), then launches the GEMM.  All calls share the one array, so
+ *    calls that overlap on the GPU (different streams, no ordering between
+ *    them) race and give wrong results; order them on one stream.
+ *  - Device-side status bits (bounded-wait expiry, packed-weight mismatch)
+ *    are written to the internal array and are not reported by this entry
+ *    point; QOQ_OK means the launch was enqueued.
+ */
+int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x,
+                          const void *packed, const uint16_t *s_w, int M, int N, int K, int group,
+                          uint16_t *O, qoq_stream_t stream);
+
+/*
  * qoq_workspace_status -- synchronizes `stream`, copies the workspace status
  * word to *host_status, clears it on the device, and returns QOQ_OK,
  * QOQ_ERR_TIMEOUT or QOQ_ERR_DEVICE according to the bits found

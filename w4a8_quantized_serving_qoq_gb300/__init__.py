@@ -83,6 +83,7 @@ def load():
                 "qoq_w4a8_gemm_ex": (I, [P, P, P, P, P, I, I, I, I, P, P, S,
                                          ctypes.POINTER(qoq_gemm_options), P]),
                 "qoq_workspace_status": (I, [P, ctypes.POINTER(ctypes.c_uint32), P]),
+                "qoq_w4a8_gemm_noalloc": (I, [P, P, P, P, P, I, I, I, I, P, P]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(lib, name)
@@ -273,6 +274,22 @@ def qoq_w4a8_gemm_ex(Qx, s_x, t_x, packed, s_w, N: int, K: int, group: int = 128
         _check("qoq_w4a8_gemm_ex", st)
         return O
     return st
+
+
+def qoq_w4a8_gemm_noalloc(Qx, s_x, t_x, packed, s_w, N: int, K: int, group: int = 128, O=None,
+                          stream=None):
+    """The GEMM for callers that cannot allocate device memory: the scratch
+    comes from a fixed array inside the library (see include/qoq.h for its
+    size limit and the rule that overlapping calls race)."""
+    torch = _torch()
+    _dev(Qx, torch.int8, "Qx")
+    M = Qx.shape[0]
+    if O is None:
+        O = torch.empty((M, N), dtype=torch.float16, device=Qx.device)
+    _check("qoq_w4a8_gemm_noalloc", load().qoq_w4a8_gemm_noalloc(
+        _ptr(Qx), _ptr(s_x), _ptr(t_x), _ptr(packed), _ptr(s_w), M, N, K, group, _ptr(O),
+        _stream(stream)))
+    return O
 
 
 def qoq_workspace_status(workspace, stream=None):
