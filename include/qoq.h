@@ -87,8 +87,9 @@ size_t qoq_packed_weight_bytes(int N, int K, int group);
  * Layout of `packed` (qoq_packed_weight_bytes bytes, 16-byte aligned):
  *   256-byte header (magic "QOQW", version, N, K, group, block size, count of
  *   illegal codes), then (N/128) x (K/128) blocks, row-tile major: 8192 bytes
- *   of 4-bit codes for 128 rows x 128 k, followed (group mode) by 256 bytes
- *   of (s_g, z) byte pairs per row.  Within a block, 16-byte chunk
+ *   of 4-bit codes for 128 rows x 128 k, followed (group mode) by 512 bytes
+ *   of metadata, 4 per row: s_g, z, and the sum of the row's 128 codes as a
+ *   little-endian uint16.  Within a block, 16-byte chunk
  *   (p*128 + r), p = 0..3, holds row r, k = 32p..32p+31 as four 32-bit words;
  *   word j covers k = 32p+8j+(0..7) and its byte b holds the code of
  *   k = 8j+b (low nibble) and k = 8j+b+4 (high nibble).  Per-channel mode
@@ -177,6 +178,10 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  *                     the bounded waits expire (timeout path test).
  *   acc_out         : if non-NULL, int32 accumulators are written here
  *                     instead of O.
+ *   kernel          : 0 = automatic, 1 = fp16-operand tensor-core path
+ *                     (dequantized weights), 2 = fp8-operand path (4-bit
+ *                     codes and split activations as exact e4m3, group 128
+ *                     only, tokens_per_tile 16 or 32).
  */
 typedef struct {
     int tokens_per_tile;
@@ -184,6 +189,7 @@ typedef struct {
     uint64_t timeout_ns;
     uint32_t debug_flags;
     int32_t *acc_out;
+    int kernel;
 } qoq_gemm_options;
 
 /* Workspace bytes for a GEMM run with the given options. */

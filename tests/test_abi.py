@@ -23,13 +23,13 @@ def test_status_strings(lib):
     for code, name in qoq.STATUS_NAMES.items():
         assert qoq.qoq_status_string(code) == name
     assert qoq.qoq_status_string(99) == "QOQ_ERR_UNKNOWN"
-    assert qoq.qoq_version() == 1
+    assert qoq.qoq_version() == 2
 
 
 def test_packed_bytes_host_only(lib):
-    # header + N*K/2 codes + (group) 2 bytes per row per group of 128
-    assert qoq.qoq_packed_weight_bytes(256, 512, 128) == 256 + 256 * 512 // 2 + 256 * 4 * 2
-    assert qoq.qoq_packed_weight_bytes(6144, 4096, 128) == 256 + 6144 * 2048 + 6144 * 32 * 2
+    # header + N*K/2 codes + (group) 4 bytes per row per group of 128
+    assert qoq.qoq_packed_weight_bytes(256, 512, 128) == 256 + 256 * 512 // 2 + 256 * 4 * 4
+    assert qoq.qoq_packed_weight_bytes(6144, 4096, 128) == 256 + 6144 * 2048 + 6144 * 32 * 4
     assert qoq.qoq_packed_weight_bytes(128, 128, 0) == 256 + 8192 + 128
     assert qoq.qoq_packed_weight_bytes(130, 128, 128) == 0
     assert qoq.qoq_packed_weight_bytes(128, 100, 128) == 0

@@ -32,7 +32,7 @@ def _pack_spec(q4, s_g, z, group):
     include/qoq.h (no code shared with the CUDA packer)."""
     N, K = q4.shape
     G = K // 128
-    blk = 8192 + (256 if group else 0)
+    blk = 8192 + (512 if group else 0)
     body = np.zeros((N // 128, G, blk), np.uint8)
     q = q4.reshape(N // 128, 128, G, 4, 4, 8)  # tile, r, group, p, word j, k-in-word
     lo = q[..., :4].astype(np.uint8)
@@ -42,8 +42,11 @@ def _pack_spec(q4, s_g, z, group):
     codes = byte.transpose(0, 2, 3, 1, 4, 5).reshape(N // 128, G, 512 * 16)
     body[:, :, :8192] = codes
     if group:
-        meta = np.stack([s_g.reshape(N // 128, 128, G), z.reshape(N // 128, 128, G)], axis=-1)
-        body[:, :, 8192:] = meta.transpose(0, 2, 1, 3).reshape(N // 128, G, 256)
+        csum = q4.reshape(N, G, 128).astype(np.int64).sum(axis=2)          # [N][G]
+        meta = np.stack([s_g.reshape(N // 128, 128, G), z.reshape(N // 128, 128, G),
+                         (csum & 0xFF).reshape(N // 128, 128, G), (csum >> 8).reshape(N // 128, 128, G)],
+                        axis=-1).astype(np.uint8)
+        body[:, :, 8192:] = meta.transpose(0, 2, 1, 3).reshape(N // 128, G, 512)
     out = body.reshape(-1)
     if not group:
         zpad = np.zeros((N + 15) // 16 * 16, np.uint8)
@@ -110,7 +113,7 @@ def test_pack_matches_spec_and_round_trips(group):
     packed = qoq.qoq_pack_weights(_t(q4), _t(s_g) if group else None, _t(z), group)
     p = _np(packed)
     hdr = p[:256].view(np.uint32)
-    assert hdr[0] == 0x57514F51 and hdr[1] == 1
+    assert hdr[0] == 0x57514F51 and hdr[1] == 2
     assert hdr[2] == N and hdr[3] == K and hdr[4] == group and hdr[6] == 0
     assert np.array_equal(p[256:], _pack_spec(q4, s_g, z, group))
     q4b, sgb, zb = qoq.qoq_unpack_weights(packed, N, K, group)
@@ -190,6 +193,33 @@ def test_gemm_tiles_and_stream_k_splits(bt, ctas):
     assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
 
 
+FP8_CASES = [(1, 256, 512), (3, 128, 384), (8, 384, 1024), (16, 256, 896), (17, 128, 640), (31, 256, 256),
+             (32, 128, 1152)]
+
+
+@pytest.mark.parametrize("M,N,K", FP8_CASES)
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("ctas", [0, 3])
+def test_both_tensor_core_paths_bit_exact(M, N, K, kernel, ctas):
+    """The fp16-operand path and the fp8-operand path (exact e4m3 codes, per-
+    group drain) give the same int32 accumulators at decode sizes, including
+    odd group counts (a last stage with one group) and split tiles."""
+    wq, Qx, sx, tx = _gemm_case(M, N, K, 4242 + M + K)
+    packed, sw = _device_weights(wq, 128)
+    ref = _ref_acc(wq, Qx, tx, 128)
+    acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    opt = qoq.gemm_options(num_ctas=ctas, acc_out=acc, kernel=kernel)
+    ws = qoq.new_workspace(qoq.qoq_gemm_workspace_bytes(M, N, K, 128, opt))
+    for _ in range(2):
+        acc.fill_(0)
+        qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128, workspace=ws, options=opt)
+        assert np.array_equal(_np(acc), ref)
+    O = qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N, K, 128,
+                             options=qoq.gemm_options(num_ctas=ctas, kernel=kernel))
+    O_ref = oracle.epilogue_f64(ref, sx, wq["s_w"])
+    assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
+
+
 def test_gemm_exact_at_chunk_extremes():
     """Largest-magnitude products over whole 1024-k chunks: the fp32
     accumulation per chunk must still be exact (sums up to 127*128*1024)."""
@@ -210,10 +240,11 @@ def test_gemm_exact_at_chunk_extremes():
     ref = oracle.gemm_i32_group(Qx, q4, s_g, z)
     assert abs(int(ref[0, 0])) == 127 * 120 * K
     for ctas in (1, 7, 0):
-        acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
-        qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128,
-                             options=qoq.gemm_options(num_ctas=ctas, acc_out=acc))
-        assert np.array_equal(_np(acc), ref)
+        for kernel in (1, 2):
+            acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+            qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128,
+                                 options=qoq.gemm_options(num_ctas=ctas, acc_out=acc, kernel=kernel))
+            assert np.array_equal(_np(acc), ref)
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 256, 512), (1, 512, 4096), (77, 256, 1024)])
@@ -270,7 +301,8 @@ def test_mismatched_packed_weights_reported_on_device():
     assert st == 0 and bits == 0  # cleared by the read
 
 
-def test_bounded_wait_timeout_reports_status_and_context_survives():
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_bounded_wait_timeout_reports_status_and_context_survives(kernel):
     """The copy warp withholds one stage (debug flag), so the consumers'
     bounded waits expire: the kernel must return, report QOQ_ERR_TIMEOUT
     through the status word, free its resources, and leave the context
@@ -278,7 +310,7 @@ def test_bounded_wait_timeout_reports_status_and_context_survives():
     M, N, K = 16, 256, 1024
     wq, Qx, sx, tx = _gemm_case(M, N, K, 9)
     packed, sw = _device_weights(wq, 128)
-    opt = qoq.gemm_options(num_ctas=1, debug_flags=1, timeout_ns=50_000_000)
+    opt = qoq.gemm_options(num_ctas=1, debug_flags=1, timeout_ns=50_000_000, kernel=kernel)
     ws = qoq.new_workspace(qoq.qoq_gemm_workspace_bytes(M, N, K, 128, opt))
     O = torch.zeros((M, N), dtype=torch.float16, device=DEV)
     qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N, K, 128, O=O, workspace=ws, options=opt)

@@ -39,6 +39,7 @@ class qoq_gemm_options(ctypes.Structure):
         ("timeout_ns", ctypes.c_uint64),
         ("debug_flags", ctypes.c_uint32),
         ("acc_out", ctypes.c_void_p),
+        ("kernel", ctypes.c_int),
     ]
 
 
@@ -251,9 +252,9 @@ def qoq_w4a8_gemm_i32(Qx, t_x, packed, N: int, K: int, group: int = 128, acc=Non
     return acc
 
 
-def gemm_options(tokens_per_tile=0, num_ctas=0, timeout_ns=0, debug_flags=0, acc_out=None):
+def gemm_options(tokens_per_tile=0, num_ctas=0, timeout_ns=0, debug_flags=0, acc_out=None, kernel=0):
     return qoq_gemm_options(tokens_per_tile, num_ctas, timeout_ns, debug_flags,
-                            None if acc_out is None else acc_out.data_ptr())
+                            None if acc_out is None else acc_out.data_ptr(), kernel)
 
 
 def qoq_w4a8_gemm_ex(Qx, s_x, t_x, packed, s_w, N: int, K: int, group: int = 128, O=None,

@@ -42,13 +42,15 @@ int check_options(const qoq_gemm_options *opt) {
     const int bt = opt->tokens_per_tile;
     if (bt != 0 && bt != 16 && bt != 32 && bt != 64 && bt != 128) return QOQ_ERR_UNSUPPORTED;
     if (opt->num_ctas < 0 || opt->num_ctas > 65536) return QOQ_ERR_UNSUPPORTED;
+    if (opt->kernel < 0 || opt->kernel > 2) return QOQ_ERR_UNSUPPORTED;
     return QOQ_OK;
 }
 
-bool plan_for(int M, int N, int K, const qoq_gemm_options *opt, qoq::GemmPlan *out) {
+bool plan_for(int M, int N, int K, int group, const qoq_gemm_options *opt, qoq::GemmPlan *out) {
     const int sms = num_sms_current_device();
     if (sms <= 0) return false;
-    *out = qoq::plan_gemm(M, N, K, sms, opt ? opt->tokens_per_tile : 0, opt ? opt->num_ctas : 0);
+    *out = qoq::plan_gemm(M, N, K, group, sms, opt ? opt->kernel : 0, opt ? opt->tokens_per_tile : 0,
+                          opt ? opt->num_ctas : 0);
     return true;
 }
 
@@ -67,7 +69,7 @@ int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const
         (t_x && !aligned(t_x, 4)) || (acc_out && !aligned(acc_out, 4)))
         return QOQ_ERR_MISALIGNED;
     qoq::GemmPlan plan;
-    if (!plan_for(M, N, K, opt, &plan)) return QOQ_ERR_CUDA;
+    if (!plan_for(M, N, K, group, opt, &plan)) return QOQ_ERR_CUDA;
     if (plan.total * (plan.ctas + 1ll) >= (1ll << 32)) return QOQ_ERR_UNSUPPORTED;
     if (ws_bytes < plan.ws_bytes) return QOQ_ERR_WORKSPACE;
     qoq::GemmArgs a;
@@ -159,7 +161,7 @@ int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, in
 size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gemm_options *opt) {
     if (check_gemm_shape(M, N, K, group) != QOQ_OK || check_options(opt) != QOQ_OK) return 0;
     qoq::GemmPlan plan;
-    if (!plan_for(M, N, K, opt, &plan)) return 0;
+    if (!plan_for(M, N, K, group, opt, &plan)) return 0;
     return plan.ws_bytes;
 }
 

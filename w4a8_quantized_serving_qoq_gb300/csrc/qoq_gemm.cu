@@ -34,8 +34,7 @@
 
 #include <mutex>
 
-#include "qoq_device.cuh"
-#include "qoq_internal.h"
+#include "qoq_gemm_common.cuh"
 
 namespace qoq {
 namespace {
@@ -47,7 +46,7 @@ constexpr int kConvGroupWarps = kConvWarps / 2;  // one group converts one stage
 constexpr int kEpiWarps = 4;           // warps 4..7
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kChunkStages = 8;        // 8 x 128 k = 1024 k per exact fp32 chunk
-constexpr uint32_t kWRawBytes = 9216;  // 8448 B block slot rounded to 1 KB
+constexpr uint32_t kWRawBytes = 9216;  // 8704 B block slot rounded to 1 KB
 
 template <int BT>
 struct Cfg {
@@ -71,26 +70,6 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-struct GemmParams {
-    const uint8_t *packed;
-    const uint16_t *s_x;
-    const int32_t *t_x;
-    const uint16_t *s_w;
-    uint16_t *O;
-    int32_t *acc_out;
-    uint32_t *status;
-    uint32_t *counters;     // [ctas] arrival counters of split tiles
-    int32_t *slots;         // [ctas][BT][128] int32 partial tiles
-    int M, N, K, group, G;
-    int tok_tiles;
-    long long total;        // tiles * G stages
-    int ctas;
-    uint32_t debug_flags;
-    uint64_t timeout_ns;
-};
-
-__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
-
 // Four INT8 / biased bytes -> two fp16x2 words holding the signed values.
 // Input byte b is v + 128 (v in [-128, 127]); 0x64XX is the fp16 1024 + XX.
 __device__ __forceinline__ void biased_bytes_to_f16x4(uint32_t u, uint32_t &lo, uint32_t &hi) {
@@ -101,75 +80,6 @@ __device__ __forceinline__ void biased_bytes_to_f16x4(uint32_t u, uint32_t &lo, 
     const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
     lo = *reinterpret_cast<const uint32_t *>(&ha);
     hi = *reinterpret_cast<const uint32_t *>(&hb);
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Persistent stream-K schedule: the tiles x G k-stages of the GEMM are cut
-// into `ctas` contiguous, equal ranges; CTA c owns [c*T/P, (c+1)*T/P).  A
-// range crosses tile boundaries; each piece inside one tile is a segment.
-// Tiles are ordered token-tile fastest, so neighbouring work shares weights.
-struct Segment {
-    int tile, k0, k1;
-};
-
-struct SegmentWalker {
-    uint32_t w, w1, G;  // total stages < 2^31 (checked on the host)
-    // ctas * total < 2^32 (checked on the host), so 32-bit arithmetic is exact.
-    __device__ SegmentWalker(const GemmParams &p, int cta)
-        : w(static_cast<uint32_t>(cta) * static_cast<uint32_t>(p.total) / static_cast<uint32_t>(p.ctas)),
-          w1(static_cast<uint32_t>(cta + 1) * static_cast<uint32_t>(p.total) / static_cast<uint32_t>(p.ctas)),
-          G(static_cast<uint32_t>(p.G)) {}
-    __device__ bool next(Segment &s) {
-        if (w >= w1) return false;
-        const uint32_t t = w / G;
-        s.tile = static_cast<int>(t);
-        s.k0 = static_cast<int>(w - t * G);
-        const uint32_t end = w1 - t * G;
-        s.k1 = static_cast<int>(end < G ? end : G);
-        w = t * G + static_cast<uint32_t>(s.k1);
-        return true;
-    }
-};
-
-// CTA whose range holds global stage `s`.
-__device__ __forceinline__ int cta_of_stage(uint32_t s, const GemmParams &p) {
-    return static_cast<int>(((s + 1) * static_cast<uint32_t>(p.ctas) - 1) / static_cast<uint32_t>(p.total));
-}
-
-// Final output of one accumulator: per-channel zero fold, then either the
-// int32 value (test mode) or fp16(acc * s_x[m] * s_w[n]).
-__device__ __forceinline__ void write_out(const GemmParams &p, int m, int n, int acc, int zc, int tx,
-                                          float sx, float sw) {
-    const size_t idx = static_cast<size_t>(m) * p.N + n;
-    acc -= zc * tx;
-    if (p.acc_out)
-        p.acc_out[idx] = acc;
-    else
-        p.O[idx] = __half_as_ushort(__float2half_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc), sx), sw)));
-}
-
-__device__ __forceinline__ int ld_cg_s32(const int32_t *p) {
-    int v;
-    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
 }
 
 template <int BT>
@@ -348,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t s = 1, zz = 0;
                 if (p.group) {
                     uint16_t meta;
-                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(meta) : "r"(wraw + kCodeBytes + 2 * wr));
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(meta) : "r"(wraw + kCodeBytes + 4 * wr));
                     s = meta & 0xffu;
                     zz = meta >> 8;
                 }
@@ -530,26 +440,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-using CUtensorMapEncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                              const cuuint64_t *, const cuuint64_t *,
-                                              const cuuint32_t *, const cuuint32_t *,
-                                              CUtensorMapInterleave, CUtensorMapSwizzle,
-                                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-CUtensorMapEncodeTiledFn get_encode_fn() {
-    static CUtensorMapEncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult qres;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &qres) == cudaSuccess &&
-            qres == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<CUtensorMapEncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
 template <int BT>
 cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
     using C = Cfg<BT>;
@@ -607,10 +497,21 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
 
 }  // namespace
 
-GemmPlan plan_gemm(int M, int N, int K, int num_sms, int force_bt, int force_ctas) {
+GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, int force_bt,
+                   int force_ctas) {
     GemmPlan pl{};
+    // The fp8 path (4 MMAs per 128-k group, per-group exact drain) wins for
+    // decode batches; larger token tiles keep the fp16 path.
+    int path = force_path;
+    if (path == 0) path = (group == 128 && M <= 32) ? kPathF8 : kPathF16;
+    if (group != 128) path = kPathF16;
     int bt = force_bt;
-    if (bt == 0) bt = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
+    if (path == kPathF8) {
+        if (bt != 16 && bt != 32) bt = M <= 16 ? 16 : 32;
+    } else if (bt == 0) {
+        bt = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128));
+    }
+    pl.path = path;
     pl.BT = bt;
     pl.tok_tiles = (M + bt - 1) / bt;
     pl.n_tiles = N / kTileN;
@@ -627,6 +528,7 @@ GemmPlan plan_gemm(int M, int N, int K, int num_sms, int force_bt, int force_cta
 }
 
 cudaError_t launch_gemm(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
+    if (plan.path == kPathF8) return launch_gemm_f8(a, plan, stream);
     switch (plan.BT) {
         case 16: return launch_bt<16>(a, plan, stream);
         case 32: return launch_bt<32>(a, plan, stream);

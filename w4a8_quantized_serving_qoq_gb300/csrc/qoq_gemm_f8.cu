@@ -1,0 +1,523 @@
+// W4A8 GEMM, fp8-operand tensor-core path (decode batches, group = 128).
+//
+// Same result as the fp16-operand path (qoq_gemm.cu):
+//   acc[m,n] = sum_g s_g[n,g] * sum_{k in g} Qx[m,k] * (q4[n,k] - z[n,g]),
+//   O = fp16(acc * s_x[m] * s_w[n]),
+// computed with exact integer arithmetic on the kind::f8f6f4 tensor cores:
+//  * a 4-bit code q placed in a byte is the e4m3 number q * 2^-9, exactly
+//    (e4m3 subnormals continue linearly into the first normal binade), so the
+//    packed codes become the A operand by a nibble -> byte split, without any
+//    multiply;
+//  * an activation is split as u = Qx + 128 = 16*uh + ul with uh, ul in
+//    [0, 15], stored the same way; the two planes are stacked along the MMA's
+//    N dimension (2*BT rows), which costs nothing for N <= 128;
+//  * per 128-k group, D_h = 2^-18 sum q*uh and D_l = 2^-18 sum q*ul are exact in
+//    the fp32 accumulator (|sum| <= 128*15*15 = 28800 units of 2^-18);
+//  * the epilogue turns each group into an integer without a conversion
+//    instruction: 48 + 16*D_h + D_l lies in [32, 64), where fp32 values are
+//    spaced by 2^-18, so its bit pattern minus that of 48 is
+//    P = sum_k q*u = sum_k q*Qx + 128*sum_k q.  Then
+//      acc += s_g * (P - 128*sum_k q - z*t_g[m]),  t_g[m] = sum_{k in g} Qx[m,k].
+//    sum_k q comes with the packed metadata; t_g is summed by the converter
+//    warps while they split the activations.
+// K-stages are 256 wide (two groups per TMA copy), four MMAs (K = 32) per
+// group.  Roles: warp 0 TMA, warp 1 MMA (+ TMEM allocation), warps 4-7
+// convert (one TMEM lane quarter each), warps 8-15 drain (two per lane
+// quarter, one half of the tokens each).  Persistent stream-K schedule, exact
+// int32 reduction of split tiles and bounded waits as in the fp16 path.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "qoq_gemm_common.cuh"
+
+namespace qoq {
+namespace {
+
+constexpr int kF8Threads = 512;
+constexpr int kF8ConvWarps = 4;      // warps 4..7
+constexpr int kF8EpiWarps = 8;       // warps 8..15
+constexpr int kF8EpiThreads = 32 * kF8EpiWarps;
+constexpr int kGroupsPerStage = 2;
+constexpr uint32_t kBlockBytesG = kCodeBytes + kMetaBytes;  // 8704
+
+template <int BT>
+struct F8Cfg {
+    static constexpr int kNmma = 2 * BT;                  // uh plane rows + ul plane rows
+    static constexpr int kRawStages = BT == 16 ? 6 : 5;
+    static constexpr int kOpStages = 4;
+    static constexpr int kAuxStages = 4;
+    static constexpr uint32_t kQxRawBytes = static_cast<uint32_t>(BT) * 128u * kGroupsPerStage;
+    static constexpr uint32_t kWRawBytes = kGroupsPerStage * kBlockBytesG;  // 17408 = 17 KB
+    static constexpr uint32_t kRawSlotBytes = kQxRawBytes + kWRawBytes;
+    static constexpr uint32_t kBGroupBytes = static_cast<uint32_t>(kNmma) * 128u;
+    static constexpr uint32_t kOpStageBytes = kGroupsPerStage * kBGroupBytes;
+    static constexpr uint32_t kAuxMetaBytes = kGroupsPerStage * 128u * 4u;
+    static constexpr uint32_t kAuxStageBytes = kAuxMetaBytes + kGroupsPerStage * BT * 4u;
+    // TMEM: D buffers [2 stage sets][2 groups] x kNmma columns, then A stages of
+    // 64 columns (128 rows x 256 k bytes).
+    static constexpr uint32_t kA0 = 4u * kNmma;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 2 * kAuxStages + 4 + 1;
+    static constexpr uint32_t kMiscBytes = 2048;
+    static constexpr uint32_t kSmemBytes = kOpStages * kOpStageBytes + kRawStages * kRawSlotBytes +
+                                           kAuxStages * kAuxStageBytes + kMiscBytes + 1024;
+    static_assert(kA0 + 64u * kOpStages <= kTmemCols, "TMEM columns");
+    static_assert(kNumBars * 8 + 64 <= 1024, "barrier area");
+    static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(kRawSlotBytes % 1024 == 0 && kOpStageBytes % 1024 == 0, "1 KB aligned slots");
+};
+
+__device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                            int32_t z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+          "r"(smem_u32(bar))
+        : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]);
+
+template <>
+__device__ __forceinline__ void tmem_ld_cols<8>(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "r"(taddr));
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, uint32_t (&r)[16]) {
+    tmem_ld16(taddr, r);
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld_pin(uint32_t (&a)[N], uint32_t (&b)[N]) {
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(a[i]), "+r"(b[i]));
+}
+
+template <int BT>
+__global__ void __launch_bounds__(kF8Threads, 1)
+    w4a8_gemm_f8_kernel(const __grid_constant__ CUtensorMap qx_map, const GemmParams p) {
+    using C = F8Cfg<BT>;
+    constexpr int R = C::kRawStages, OPS = C::kOpStages, AUX = C::kAuxStages;
+    constexpr int HT = BT / 2;  // tokens per drain thread
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint8_t *op_base = smem;                                     // B planes, 1 KB aligned
+    uint8_t *raw_base = op_base + OPS * C::kOpStageBytes;        // [Qx box | 2 weight blocks]
+    uint8_t *aux_base = raw_base + R * C::kRawSlotBytes;         // [meta 2x128x4 | t_g 2xBT]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(aux_base + AUX * C::kAuxStageBytes);
+    uint64_t *raw_full = bars;
+    uint64_t *raw_empty = raw_full + R;
+    uint64_t *op_full = raw_empty + R;
+    uint64_t *op_empty = op_full + OPS;
+    uint64_t *aux_full = op_empty + OPS;
+    uint64_t *aux_empty = aux_full + AUX;
+    uint64_t *d_full = aux_empty + AUX;
+    uint64_t *d_empty = d_full + 2;
+    uint64_t *mma_done = d_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *hdr_ok = abort_flag + 1;
+    volatile int *is_last = abort_flag + 2;
+    float *tile_sx = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 1024);
+    int *tile_tx = reinterpret_cast<int *>(tile_sx + 128);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const uint64_t tmo = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&qx_map);
+        const PackedHeader *h = reinterpret_cast<const PackedHeader *>(p.packed);
+        const bool ok = h->magic == kPackedMagic && h->version == kPackedVersion && h->N == p.N &&
+                        h->K == p.K && h->group == p.group && h->illegal == 0u && p.group == 128;
+        if (!ok) atomicOr(p.status, kStatusBadPacked);
+        *hdr_ok = ok ? 1 : 0;
+        *abort_flag = 0;
+        *is_last = 0;
+        for (int i = 0; i < R; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], kF8ConvWarps);
+        }
+        for (int i = 0; i < OPS; ++i) {
+            mbar_init(&op_full[i], kF8ConvWarps);
+            mbar_init(&op_empty[i], 1);
+        }
+        for (int i = 0; i < AUX; ++i) {
+            mbar_init(&aux_full[i], kF8ConvWarps);
+            mbar_init(&aux_empty[i], kF8EpiWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], kF8EpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const bool run = (*hdr_ok != 0);
+
+    if (run && warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            SegmentWalker walk(p, cta);
+            Segment sg;
+            int st = 0, issued = 0;
+            bool stop = false;
+            while (!stop && walk.next(sg)) {
+                const int tok_tile = sg.tile % p.tok_tiles, n_tile = sg.tile / p.tok_tiles;
+                const uint8_t *wrow = p.packed + kHeaderBytes + static_cast<size_t>(n_tile) * p.G * kBlockBytesG;
+                for (int k = sg.k0; k < sg.k1; k += kGroupsPerStage, ++st) {
+                    const int ng = min(kGroupsPerStage, sg.k1 - k);
+                    const int slot = st % R, use = st / R;
+                    if (use > 0 && !mbar_wait(&raw_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo)) {
+                        stop = true;
+                        break;
+                    }
+                    if ((p.debug_flags & kDebugWithholdStage) && st == 1) {
+                        stop = true;
+                        break;
+                    }
+                    uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
+                    mbar_arrive_expect_tx(&raw_full[slot], C::kQxRawBytes + ng * kBlockBytesG);
+                    tma_load_1d(dst + C::kQxRawBytes, wrow + static_cast<size_t>(k) * kBlockBytesG,
+                                ng * kBlockBytesG, &raw_full[slot]);
+                    tma_load_3d(dst, &qx_map, 0, tok_tile * BT, k, &raw_full[slot]);
+                    issued = st + 1;
+                }
+            }
+            for (int t = (issued > R ? issued - R : 0); t < issued; ++t)
+                mbar_wait(&raw_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
+        }
+    } else if (run && warp == 1) {
+        // ------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(128, C::kNmma);  // e4m3 x e4m3 -> f32 for kind::f8f6f4
+            SegmentWalker walk(p, cta);
+            Segment sg;
+            int st = 0;
+            bool stop = false;
+            while (!stop && walk.next(sg)) {
+                for (int k = sg.k0; k < sg.k1; k += kGroupsPerStage, ++st) {
+                    const int ng = min(kGroupsPerStage, sg.k1 - k);
+                    const int os = st % OPS, ouse = st / OPS;
+                    const int ds = st & 1, duse = st >> 1;
+                    if ((duse > 0 && !mbar_wait(&d_empty[ds], (duse - 1) & 1, abort_flag, p.status, tmo)) ||
+                        !mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
+                        stop = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes);
+                    for (int g = 0; g < ng; ++g) {
+                        const uint32_t d_tmem = tmem + static_cast<uint32_t>((2 * ds + g) * C::kNmma);
+                        const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u + 32u * g;
+                        const uint32_t bg = b_base + g * C::kBGroupBytes;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f8_tmem_a(d_tmem, a_tmem + 8u * kk, desc_kmajor_sw128(bg + 32u * kk), idesc,
+                                          kk ? 1u : 0u);
+                    }
+                    mma_commit(&op_empty[os]);
+                    mma_commit(&d_full[ds]);
+                }
+            }
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0, nullptr, p.status, tmo);
+        }
+    } else if (run && warp >= 4 && warp < 8) {
+        // ---------------------------------------------- converter warps --
+        const int wr = (warp & 3) * 32 + lane;  // weight row == TMEM lane; also the item index
+        const uint32_t a_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        SegmentWalker walk(p, cta);
+        Segment sg;
+        int st = 0;
+        bool stop = false;
+        while (!stop && walk.next(sg)) {
+            for (int k = sg.k0; k < sg.k1; k += kGroupsPerStage, ++st) {
+                const int ng = min(kGroupsPerStage, sg.k1 - k);
+                const int rs = st % R, ruse = st / R, os = st % OPS, ouse = st / OPS, as = st % AUX,
+                          ause = st / AUX;
+                if (!mbar_wait_warp(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo) ||
+                    (ouse > 0 && !mbar_wait_warp(&op_empty[os], (ouse - 1) & 1, abort_flag, p.status, tmo)) ||
+                    (ause > 0 && !mbar_wait_warp(&aux_empty[as], (ause - 1) & 1, abort_flag, p.status, tmo))) {
+                    stop = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t raw = smem_u32(raw_base + rs * C::kRawSlotBytes);
+                const uint32_t wraw = raw + C::kQxRawBytes;
+                const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes);
+                uint8_t *aux = aux_base + as * C::kAuxStageBytes;
+                uint32_t *aux_meta = reinterpret_cast<uint32_t *>(aux);
+                int *aux_tg = reinterpret_cast<int *>(aux + C::kAuxMetaBytes);
+
+                // Weights: row wr, 128 k per group -> 128 code bytes (e4m3 q * 2^-9)
+                // -> 32 TMEM columns of this lane per group.
+                for (int g = 0; g < ng; ++g) {
+                    const uint32_t blk = wraw + g * kBlockBytesG;
+                    uint32_t a_frag[32];
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp) {
+                        const uint4 v = ld_shared_v4(blk + ((pp * 128 + wr) << 4));
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            a_frag[8 * pp + 2 * j] = w4[j] & 0x0F0F0F0Fu;             // k = 8j .. 8j+3
+                            a_frag[8 * pp + 2 * j + 1] = (w4[j] >> 4) & 0x0F0F0F0Fu;  // k = 8j+4 .. 8j+7
+                        }
+                    }
+                    tmem_st32(a_lane + C::kA0 + static_cast<uint32_t>(os) * 64u + 32u * g, a_frag);
+                    uint32_t meta;
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(meta) : "r"(blk + kCodeBytes + 4 * wr));
+                    aux_meta[g * 128 + wr] = meta;
+                }
+                // Activations: items (group, token, 16-byte chunk); eight consecutive
+                // lanes take the eight chunks of one token row.
+                constexpr int kItems = kGroupsPerStage * BT * 8;
+#pragma unroll
+                for (int it0 = 0; it0 < kItems; it0 += 128) {
+                    const int it = it0 + wr;
+                    const int g = it / (8 * BT), r = (it / 8) % BT, c = it % 8;
+                    int part = 0;
+                    if (g < ng) {
+                        const uint4 v = ld_shared_v4(raw + (g * BT + r) * 128 + ((c ^ (r & 7)) << 4));
+                        const uint32_t x4[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            part = __dp4a(static_cast<int>(x4[j]), 0x01010101, part);  // signed byte sum
+                            const uint32_t u = x4[j] ^ 0x80808080u;                   // Qx + 128
+                            hi[j] = (u >> 4) & 0x0F0F0F0Fu;
+                            lo[j] = u & 0x0F0F0F0Fu;
+                        }
+                        const uint32_t bg = b_base + g * C::kBGroupBytes;
+                        st_shared_v4(bg + sw128_offset(r, c), hi[0], hi[1], hi[2], hi[3]);
+                        st_shared_v4(bg + sw128_offset(BT + r, c), lo[0], lo[1], lo[2], lo[3]);
+                    }
+                    part += __shfl_xor_sync(0xffffffffu, part, 1);
+                    part += __shfl_xor_sync(0xffffffffu, part, 2);
+                    part += __shfl_xor_sync(0xffffffffu, part, 4);
+                    if (c == 0 && g < ng) aux_tg[g * BT + r] = part;
+                }
+                fence_proxy_async_smem();
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&raw_empty[rs]);
+                    mbar_arrive(&op_full[os]);
+                    mbar_arrive(&aux_full[as]);
+                }
+            }
+        }
+    } else if (run && warp >= 8) {
+        // ------------------------------------------------- drain warps --
+        const int ew = warp - 8;
+        const int et = threadIdx.x - 256;          // 0..255 among the drain threads
+        const int row = (ew & 3) * 32 + lane;      // weight row == TMEM lane
+        const int hs = ew >> 2;                    // token half
+        const uint32_t tl = tmem + (static_cast<uint32_t>((ew & 3) * 32) << 16);
+        const int bits48 = 0x42400000;             // fp32 48.0
+        SegmentWalker walk(p, cta);
+        Segment sg;
+        int st = 0;
+        while (walk.next(sg)) {
+            const int tok_tile = sg.tile % p.tok_tiles, n_tile = sg.tile / p.tok_tiles;
+            const int m0 = tok_tile * BT, n = n_tile * kTileN + row;
+            const bool split = !(sg.k0 == 0 && sg.k1 == p.G);
+            const float sw = p.s_w ? h2f(p.s_w[n]) : 0.f;
+            const uint32_t tfirst = static_cast<uint32_t>(sg.tile) * static_cast<uint32_t>(p.G);
+            const int slot_idx = split ? cta_of_stage(tfirst, p) : 0;
+            int32_t *slot = p.slots + static_cast<size_t>(slot_idx) * (BT * kTileN);
+            named_bar_sync(2, kF8EpiThreads);
+            if (et < BT) {
+                const int m = m0 + et;
+                tile_sx[et] = (m < p.M && p.s_x) ? h2f(p.s_x[m]) : 0.f;
+                tile_tx[et] = 0;
+            }
+            named_bar_sync(2, kF8EpiThreads);
+            int acc[HT];
+#pragma unroll
+            for (int i = 0; i < HT; ++i) acc[i] = 0;
+            bool ok = true;
+            for (int k = sg.k0; k < sg.k1 && ok; k += kGroupsPerStage, ++st) {
+                const int ng = min(kGroupsPerStage, sg.k1 - k);
+                const int ds = st & 1, duse = st >> 1, as = st % AUX, ause = st / AUX;
+                ok = mbar_wait_warp(&aux_full[as], ause & 1, abort_flag, p.status, tmo) &&
+                     mbar_wait_warp(&d_full[ds], duse & 1, abort_flag, p.status, tmo);
+                if (!ok) break;
+                tc_fence_after();
+                const uint8_t *aux = aux_base + as * C::kAuxStageBytes;
+                const uint32_t *aux_meta = reinterpret_cast<const uint32_t *>(aux);
+                const int *aux_tg = reinterpret_cast<const int *>(aux + C::kAuxMetaBytes);
+                for (int g = 0; g < ng; ++g) {
+                    uint32_t dh[HT], dl[HT];
+                    const uint32_t dcol = static_cast<uint32_t>((2 * ds + g) * C::kNmma + hs * HT);
+                    tmem_ld_cols<HT>(tl + dcol, dh);
+                    tmem_ld_cols<HT>(tl + dcol + BT, dl);
+                    tmem_wait_ld_pin<HT>(dh, dl);
+                    const uint32_t meta = aux_meta[g * 128 + row];
+                    const int s = static_cast<int>(meta & 0xffu), z = static_cast<int>((meta >> 8) & 0xffu);
+                    const int base = bits48 + 128 * static_cast<int>(meta >> 16);
+#pragma unroll
+                    for (int i = 0; i < HT; ++i) {
+                        const float y = __fmaf_rn(__uint_as_float(dh[i]), 16.0f,
+                                                  __fadd_rn(__uint_as_float(dl[i]), 48.0f));
+                        const int corr = z * aux_tg[g * BT + hs * HT + i] + base;
+                        acc[i] += s * (__float_as_int(y) - corr);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&d_empty[ds]);
+                    mbar_arrive(&aux_empty[as]);
+                }
+            }
+            if (ok) {
+#pragma unroll
+                for (int i = 0; i < HT; ++i) {
+                    const int ml = hs * HT + i, m = m0 + ml;
+                    if (m < p.M) {
+                        if (split)
+                            atomicAdd(slot + ml * kTileN + row, acc[i]);
+                        else
+                            write_out(p, m, n, acc[i], 0, 0, tile_sx[ml], sw);
+                    }
+                }
+            }
+            if (split) {
+                named_bar_sync(1, kF8EpiThreads);
+                if (et == 0) {
+                    int last_cta = 0;
+                    if (*abort_flag == 0) {
+                        __threadfence();
+                        const uint32_t tlast = tfirst + static_cast<uint32_t>(p.G) - 1u;
+                        const unsigned expected = static_cast<unsigned>(cta_of_stage(tlast, p) - slot_idx + 1);
+                        const unsigned prev = atomicAdd(p.counters + slot_idx, 1u);
+                        last_cta = (prev + 1 == expected) ? 1 : 0;
+                        if (last_cta) __threadfence();
+                    }
+                    *is_last = last_cta;
+                }
+                named_bar_sync(1, kF8EpiThreads);
+                if (*is_last) {
+                    int v[HT];
+#pragma unroll
+                    for (int i = 0; i < HT; ++i) {
+                        const int ml = hs * HT + i;
+                        v[i] = (m0 + ml < p.M) ? ld_cg_s32(slot + ml * kTileN + row) : 0;
+                    }
+#pragma unroll
+                    for (int i = 0; i < HT; ++i) {
+                        const int ml = hs * HT + i;
+                        if (m0 + ml < p.M) {
+                            slot[ml * kTileN + row] = 0;
+                            write_out(p, m0 + ml, n, v[i], 0, 0, tile_sx[ml], sw);
+                        }
+                    }
+                    if (et == 0) p.counters[slot_idx] = 0u;
+                }
+            }
+            named_bar_sync(1, kF8EpiThreads);
+            if (*abort_flag != 0) break;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int BT>
+cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
+    using C = F8Cfg<BT>;
+    static std::mutex mu;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !configured[dev]) {
+            e = cudaFuncSetAttribute(w4a8_gemm_f8_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(C::kSmemBytes));
+            if (e != cudaSuccess) return e;
+            configured[dev] = true;
+        }
+    }
+    CUtensorMapEncodeTiledFn enc = get_encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    // Qx [M][K] viewed as [K/128][M][128]: one box = 2 groups x BT rows x 128 k.
+    CUtensorMap map;
+    const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(a.M), static_cast<cuuint64_t>(a.K / 128)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.K), 128u};
+    const cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(BT), static_cast<cuuint32_t>(kGroupsPerStage)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<int8_t *>(a.Qx), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    GemmParams p;
+    uint8_t *ws = static_cast<uint8_t *>(a.ws);
+    p.packed = static_cast<const uint8_t *>(a.packed);
+    p.s_x = a.s_x;
+    p.t_x = a.t_x;
+    p.s_w = a.s_w;
+    p.O = a.O;
+    p.acc_out = a.acc_out;
+    p.status = reinterpret_cast<uint32_t *>(ws);
+    p.counters = reinterpret_cast<uint32_t *>(ws + plan.counters_offset);
+    p.slots = reinterpret_cast<int32_t *>(ws + plan.slots_offset);
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.group = a.group;
+    p.G = plan.G;
+    p.tok_tiles = plan.tok_tiles;
+    p.total = plan.total;
+    p.ctas = plan.ctas;
+    p.debug_flags = a.debug_flags;
+    p.timeout_ns = a.timeout_ns;
+    w4a8_gemm_f8_kernel<BT><<<dim3(plan.ctas), kF8Threads, C::kSmemBytes, stream>>>(map, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_f8(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
+    if (a.group != 128) return cudaErrorInvalidValue;
+    switch (plan.BT) {
+        case 16: return launch_f8_bt<16>(a, plan, stream);
+        case 32: return launch_f8_bt<32>(a, plan, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qoq

@@ -12,7 +12,8 @@ namespace qoq {
 // [header: 256 B]
 // [blocks: (N/128) x (K/128) blocks, n-tile major, k-group minor]
 //   each block = 8192 B of 4-bit codes for 128 rows x 128 k, then, in group
-//   mode only, 256 B of metadata: per row r, byte 2r = s_g, byte 2r+1 = z.
+//   mode only, 512 B of metadata: per row r, byte 4r = s_g, byte 4r+1 = z,
+//   bytes 4r+2..4r+3 = sum of the row's 128 codes (little-endian uint16).
 //   Code layout inside a block: 512 chunks of 16 B; chunk (p * 128 + r),
 //   p = 0..3, holds the 32 codes of row r at k = 32p .. 32p + 31 as four
 //   32-bit words; word j covers k = 32p + 8j + (0..7); byte b of a word holds
@@ -21,10 +22,10 @@ namespace qoq {
 // [per-channel mode only: z [N] bytes, padded to 16 B]
 // ------------------------------------------------------------------------
 constexpr uint32_t kPackedMagic = 0x57514F51u;  // "QOQW"
-constexpr uint32_t kPackedVersion = 1u;
+constexpr uint32_t kPackedVersion = 2u;
 constexpr size_t kHeaderBytes = 256;
 constexpr uint32_t kCodeBytes = 8192;           // 128 x 128 x 4 bit
-constexpr uint32_t kMetaBytes = 256;            // 128 rows x (s_g, z)
+constexpr uint32_t kMetaBytes = 512;            // 128 rows x (s_g, z, code sum)
 constexpr int kTileN = 128;                     // weight rows per tile
 constexpr int kTileK = 128;                     // k per stage = one group
 
@@ -57,8 +58,14 @@ __host__ __device__ inline size_t packed_z_offset(int N, int K) {
 // int32 partial-tile slots].
 constexpr size_t kWsStatusBytes = 256;
 
+enum GemmPath : int {
+    kPathF16 = 1,          // weights dequantized to exact fp16, kind::f16 MMA
+    kPathF8 = 2,           // raw 4-bit codes and split activations as exact e4m3, kind::f8f6f4 MMA
+};
+
 struct GemmPlan {
-    int BT;                // tokens per tile (MMA N): 16, 32, 64 or 128
+    int path;              // GemmPath
+    int BT;                // tokens per tile: 16, 32, 64 or 128
     int tok_tiles;         // ceil(M / BT)
     int n_tiles;           // N / 128
     int G;                 // K / 128 k-stages per tile
@@ -70,9 +77,10 @@ struct GemmPlan {
     size_t slots_offset;
 };
 
-// Tile shape and persistent-CTA count for one GEMM.  force_bt / force_ctas
-// (0 = automatic) pin the choice for tests.
-GemmPlan plan_gemm(int M, int N, int K, int num_sms, int force_bt = 0, int force_ctas = 0);
+// Kernel path, tile shape and persistent-CTA count for one GEMM.
+// force_path / force_bt / force_ctas (0 = automatic) pin the choice for tests.
+GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path = 0, int force_bt = 0,
+                   int force_ctas = 0);
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
@@ -99,6 +107,7 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream);
+cudaError_t launch_gemm_f8(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream);
 
 // Debug flag: the TMA producer withholds the second stage's load, so the
 // consumers' bounded waits expire (exercises the timeout path).

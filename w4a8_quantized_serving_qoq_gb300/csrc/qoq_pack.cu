@@ -56,8 +56,21 @@ __global__ void pack_kernel(const uint8_t *__restrict__ q4, const uint8_t *__res
     if (c < 128) {
         if (group) {
             illegal += (s > 17) + (z > 15);
-            blk[kCodeBytes + 2 * r] = static_cast<uint8_t>(s);
-            blk[kCodeBytes + 2 * r + 1] = static_cast<uint8_t>(z);
+            // sum of the row's 128 codes in this group (used by the fp8 path)
+            const uint4 *row = reinterpret_cast<const uint4 *>(q4 + static_cast<size_t>(n) * K + kg * kTileK);
+            uint32_t sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint4 v = row[i];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    sum += ((w[j] & 0xffu) + ((w[j] >> 8) & 0xffu) + ((w[j] >> 16) & 0xffu) + (w[j] >> 24)) & 0xffffu;
+            }
+            blk[kCodeBytes + 4 * r] = static_cast<uint8_t>(s);
+            blk[kCodeBytes + 4 * r + 1] = static_cast<uint8_t>(z);
+            blk[kCodeBytes + 4 * r + 2] = static_cast<uint8_t>(sum & 0xffu);
+            blk[kCodeBytes + 4 * r + 3] = static_cast<uint8_t>(sum >> 8);
         } else if (kg == 0) {
             const int zc = zp[n];
             illegal += (zc > 15);
@@ -102,8 +115,8 @@ __global__ void unpack_kernel(const uint8_t *__restrict__ packed, int N, int K, 
     dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
     if (c < 128) {
         if (group) {
-            s_g[static_cast<size_t>(n) * G + kg] = blk[kCodeBytes + 2 * r];
-            zp[static_cast<size_t>(n) * G + kg] = blk[kCodeBytes + 2 * r + 1];
+            s_g[static_cast<size_t>(n) * G + kg] = blk[kCodeBytes + 4 * r];
+            zp[static_cast<size_t>(n) * G + kg] = blk[kCodeBytes + 4 * r + 1];
         } else if (kg == 0) {
             zp[n] = packed[packed_z_offset(N, K) + n];
         }
