@@ -123,13 +123,39 @@ int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, in
                   qoq_stream_t stream);
 
 /*
+ * Bytes of the activation operand that the GEMM's fp8-operand path reads
+ * (0 for an invalid shape; requires K % 128 == 0).  Layout, for M tokens:
+ *   [u_hi plane: M x K bytes][u_lo plane: M x K bytes][t_g: (K/128) x Mp int32]
+ * with u = Qx + 128 = 16*u_hi + u_lo (u_hi, u_lo in [0, 15]),
+ * t_g[g][m] = sum of Qx[m, k] over the 128 k of group g, and Mp = M rounded
+ * up to a multiple of 4.  It is the INT8 activation of qoq_quant_act in the
+ * order and encoding the kernel consumes (the activation-side counterpart of
+ * the compute-aware weight reordering of [QS-summary] "计算感知权重重排序").
+ */
+size_t qoq_act_operand_bytes(int M, int K);
+
+/*
+ * qoq_quant_act_ex -- qoq_quant_act, and, when act_operand is not NULL, also
+ * the fp8-path activation operand described above (qoq_act_operand_bytes(M,
+ * K) bytes, 16-byte aligned, written completely; requires K % 128 == 0).
+ * Pass it to the GEMM with qoq_gemm_options.act_operand; without it, a GEMM
+ * that takes the fp8 path builds the operand itself in its workspace with
+ * one extra kernel launch.  Same results in both cases.
+ */
+int qoq_quant_act_ex(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x,
+                     void *act_operand, qoq_stream_t stream);
+
+/*
  * Workspace bytes qoq_w4a8_gemm needs for this shape on the current device:
  * a 256-byte status word area, one arrival counter per persistent CTA and
  * one int32 partial-tile slot (tokens-per-tile x 128) per persistent CTA,
- * used when a CTA's share of the work ends inside an output tile.  The
- * workspace must be zero-filled once before first use (qoq_workspace_init);
- * every successful call leaves it zero-filled again (after a
- * QOQ_ERR_TIMEOUT, re-initialise it).
+ * used when a CTA's share of the work ends inside an output tile; for shapes
+ * that take the fp8-operand path, followed by scratch for the activation
+ * operand (qoq_act_operand_bytes).  The workspace must be zero-filled once
+ * before first use (qoq_workspace_init); every successful call leaves the
+ * status word, counters and slots zero-filled again (after a
+ * QOQ_ERR_TIMEOUT, re-initialise it); the activation scratch needs no
+ * initialisation.
  */
 size_t qoq_gemm_workspace_bytes(int M, int N, int K, int group);
 
@@ -182,6 +208,10 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  *                     (dequantized weights), 2 = fp8-operand path (4-bit
  *                     codes and split activations as exact e4m3, group 128
  *                     only, tokens_per_tile 16 or 32).
+ *   act_operand     : the activation operand written by qoq_quant_act_ex for
+ *                     the same Qx (16-byte aligned), read by the fp8 path
+ *                     instead of building it; ignored by the fp16 path.
+ *                     NULL = build it in the workspace.
  */
 typedef struct {
     int tokens_per_tile;
@@ -190,10 +220,20 @@ typedef struct {
     uint32_t debug_flags;
     int32_t *acc_out;
     int kernel;
+    const void *act_operand;
 } qoq_gemm_options;
 
 /* Workspace bytes for a GEMM run with the given options. */
 size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gemm_options *opt);
+
+/*
+ * The tensor-core path a GEMM of this shape and options takes on the current
+ * device: 1 = fp16-operand path, 2 = fp8-operand path (the one that reads
+ * qoq_gemm_options.act_operand), or minus a qoq_status for invalid
+ * arguments.  Lets a caller produce the activation operand only when it is
+ * used.
+ */
+int qoq_gemm_path(int M, int N, int K, int group, const qoq_gemm_options *opt);
 
 int qoq_w4a8_gemm_ex(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x,
                      const void *packed, const uint16_t *s_w, int M, int N, int K, int group,

@@ -47,15 +47,21 @@ def _check_point(workload, name, M, group=128, check_quantizer=False):
     N, K = layer.N, layer.K
     packed = qoq.qoq_pack_weights(_t(wq["q4"]), _t(wq["s_g"]) if group else None, _t(wq["z"]), group)
     sw = _t(wq["s_w"])
-    # device activation quantizer, bit-exact at full size
-    Qx_d, sx_d, tx_d = qoq.qoq_quant_act(_t(X))
+    # device activation quantizer (with the fp8-path activation operand, as
+    # the benchmark calls it), bit-exact at full size
+    Qx_d, sx_d, tx_d, act_d = qoq.qoq_quant_act_ex(_t(X))
     torch.cuda.synchronize()
     assert np.array_equal(Qx_d.cpu().numpy(), Qx)
     assert np.array_equal(sx_d.cpu().numpy().view(np.uint16), sx.view(np.uint16))
     assert np.array_equal(tx_d.cpu().numpy(), tx)
-    acc = qoq.qoq_w4a8_gemm_i32(Qx_d, tx_d, packed, N, K, group)
-    O = qoq.qoq_w4a8_gemm(Qx_d, sx_d, tx_d, packed, sw, N, K, group)
+    acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    qoq.qoq_w4a8_gemm_ex(Qx_d, None, tx_d, packed, None, N, K, group,
+                         options=qoq.gemm_options(acc_out=acc, act_operand=act_d))
+    O = qoq.qoq_w4a8_gemm_ex(Qx_d, sx_d, tx_d, packed, sw, N, K, group,
+                             options=qoq.gemm_options(act_operand=act_d))
+    O_plain = qoq.qoq_w4a8_gemm(Qx_d, sx_d, tx_d, packed, sw, N, K, group)
     torch.cuda.synchronize()
+    assert torch.equal(O, O_plain)  # operand from the quantizer == operand built by the GEMM
     acc = acc.cpu().numpy()
     O = O.cpu().numpy().astype(np.float64)
 

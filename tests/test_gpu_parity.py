@@ -69,6 +69,41 @@ def test_quant_act_bit_exact(M, K):
     assert np.array_equal(_np(tx), tx_r)
 
 
+def _act_operand_spec(Qx):
+    """The fp8-path activation operand written out from its description in
+    include/qoq.h: u = Qx + 128 split into high/low nibble planes, then the
+    per-128-k-group sums of Qx as [K/128][Mp] int32 (Mp = M rounded up to 4)."""
+    M, K = Qx.shape
+    u = Qx.astype(np.int64) + 128
+    hi = (u // 16).astype(np.uint8)
+    lo = (u % 16).astype(np.uint8)
+    Mp = (M + 3) // 4 * 4
+    tg = np.zeros((K // 128, Mp), np.int32)
+    tg[:, :M] = Qx.astype(np.int64).reshape(M, K // 128, 128).sum(axis=2).T
+    return hi, lo, tg
+
+
+@pytest.mark.parametrize("M,K", [(1, 128), (3, 512), (16, 4096), (17, 1152), (300, 14336)])
+def test_quant_act_ex_act_operand_bit_exact(M, K):
+    X = synthetic.activations(M, K, 300 + M, 4)
+    if M > 2:
+        X[1] = 0
+    Qx_r, sx_r, tx_r = oracle.quant_act(X)
+    nbytes = qoq.qoq_act_operand_bytes(M, K)
+    Mp = (M + 3) // 4 * 4
+    assert nbytes == 2 * M * K + (K // 128) * Mp * 4
+    Qx, sx, tx, act = qoq.qoq_quant_act_ex(_t(X))
+    assert np.array_equal(_np(Qx), Qx_r)
+    assert np.array_equal(_np(sx).view(np.uint16), sx_r.view(np.uint16))
+    assert np.array_equal(_np(tx), tx_r)
+    a = _np(act)
+    hi, lo, tg = _act_operand_spec(Qx_r)
+    assert np.array_equal(a[: M * K].reshape(M, K), hi)
+    assert np.array_equal(a[M * K: 2 * M * K].reshape(M, K), lo)
+    got_tg = a[2 * M * K:].view(np.int32).reshape(K // 128, Mp)
+    assert np.array_equal(got_tg[:, :M], tg[:, :M])
+
+
 def test_quant_act_ties_half_even():
     row = np.zeros(128, np.float32)
     row[0] = 127 * 0.125
@@ -217,6 +252,32 @@ def test_both_tensor_core_paths_bit_exact(M, N, K, kernel, ctas):
     O = qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N, K, 128,
                              options=qoq.gemm_options(num_ctas=ctas, kernel=kernel))
     O_ref = oracle.epilogue_f64(ref, sx, wq["s_w"])
+    assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
+
+
+@pytest.mark.parametrize("M,N,K", FP8_CASES)
+def test_fp8_path_with_quantizer_act_operand(M, N, K):
+    """The activation operand written by qoq_quant_act_ex, handed to the GEMM,
+    gives the oracle's accumulators and the same fp16 output as the GEMM
+    building the operand itself."""
+    W = synthetic.weights(N, K, 5150 + M, 0.02, 2)
+    X = synthetic.activations(M, K, 5151 + M, 4)
+    wq = oracle.quantize_weights_group(W, 128)
+    Qx_r, sx_r, _ = oracle.quant_act(X)
+    packed, sw = _device_weights(wq, 128)
+    ref = _ref_acc(wq, Qx_r, None, 128)
+    Qx, sx, _, act = qoq.qoq_quant_act_ex(_t(X), with_t=False)
+    acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    for ctas in (0, 3):
+        acc.fill_(0)
+        qoq.qoq_w4a8_gemm_ex(Qx, None, None, packed, None, N, K, 128,
+                             options=qoq.gemm_options(num_ctas=ctas, acc_out=acc, kernel=2, act_operand=act))
+        assert np.array_equal(_np(acc), ref)
+    O = qoq.qoq_w4a8_gemm_ex(Qx, sx, None, packed, sw, N, K, 128,
+                             options=qoq.gemm_options(kernel=2, act_operand=act))
+    O_self = qoq.qoq_w4a8_gemm_ex(Qx, sx, None, packed, sw, N, K, 128, options=qoq.gemm_options(kernel=2))
+    assert torch.equal(O, O_self)
+    O_ref = oracle.epilogue_f64(ref, sx_r, wq["s_w"])
     assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
 
 

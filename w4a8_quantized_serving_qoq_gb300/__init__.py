@@ -40,6 +40,7 @@ class qoq_gemm_options(ctypes.Structure):
         ("debug_flags", ctypes.c_uint32),
         ("acc_out", ctypes.c_void_p),
         ("kernel", ctypes.c_int),
+        ("act_operand", ctypes.c_void_p),
     ]
 
 
@@ -76,8 +77,11 @@ def load():
                 "qoq_pack_weights": (I, [P, P, P, I, I, I, P, P]),
                 "qoq_unpack_weights": (I, [P, I, I, I, P, P, P, P]),
                 "qoq_quant_act": (I, [P, I, I, P, P, P, P]),
+                "qoq_act_operand_bytes": (S, [I, I]),
+                "qoq_quant_act_ex": (I, [P, I, I, P, P, P, P, P]),
                 "qoq_gemm_workspace_bytes": (S, [I, I, I, I]),
                 "qoq_gemm_workspace_bytes_ex": (S, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
+                "qoq_gemm_path": (I, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
                 "qoq_workspace_init": (I, [P, S, P]),
                 "qoq_w4a8_gemm": (I, [P, P, P, P, P, I, I, I, I, P, P, S, P]),
                 "qoq_w4a8_gemm_i32": (I, [P, P, P, I, I, I, I, P, P, S, P]),
@@ -203,10 +207,49 @@ def qoq_quant_act(X, Qx=None, s_x=None, t_x=None, with_t: bool = True, stream=No
     return Qx, s_x, t_x
 
 
+def qoq_act_operand_bytes(M: int, K: int) -> int:
+    return int(load().qoq_act_operand_bytes(M, K))
+
+
+def qoq_quant_act_ex(X, Qx=None, s_x=None, t_x=None, act=None, with_t: bool = True,
+                     with_act: bool = True, stream=None):
+    """qoq_quant_act plus the fp8-path activation operand (uint8 tensor of
+    qoq_act_operand_bytes(M, K) bytes) -> (Qx, s_x, t_x, act)."""
+    torch = _torch()
+    _dev(X, torch.float16, "X")
+    M, K = X.shape
+    if Qx is None:
+        Qx = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    if s_x is None:
+        s_x = torch.empty((M,), dtype=torch.float16, device=X.device)
+    if t_x is None and with_t:
+        t_x = torch.empty((M,), dtype=torch.int32, device=X.device)
+    if act is None and with_act:
+        nbytes = qoq_act_operand_bytes(M, K)
+        if nbytes == 0:
+            raise QoqError("qoq_quant_act_ex", 2)
+        act = torch.empty((nbytes,), dtype=torch.uint8, device=X.device)
+    _dev(Qx, torch.int8, "Qx")
+    _dev(s_x, torch.float16, "s_x")
+    _dev(t_x, torch.int32, "t_x")
+    _dev(act, torch.uint8, "act")
+    _check("qoq_quant_act_ex", load().qoq_quant_act_ex(
+        _ptr(X), M, K, _ptr(Qx), _ptr(s_x), _ptr(t_x), _ptr(act), _stream(stream)))
+    return Qx, s_x, t_x, act
+
+
 def qoq_gemm_workspace_bytes(M: int, N: int, K: int, group: int = 128, options=None) -> int:
     if options is None:
         return int(load().qoq_gemm_workspace_bytes(M, N, K, group))
     return int(load().qoq_gemm_workspace_bytes_ex(M, N, K, group, ctypes.byref(options)))
+
+
+def qoq_gemm_path(M: int, N: int, K: int, group: int = 128, options=None) -> int:
+    """1 = fp16-operand path, 2 = fp8-operand path (reads the activation operand)."""
+    st = int(load().qoq_gemm_path(M, N, K, group, None if options is None else ctypes.byref(options)))
+    if st < 0:
+        raise QoqError("qoq_gemm_path", -st)
+    return st
 
 
 def qoq_workspace_init(workspace, stream=None):
@@ -252,9 +295,11 @@ def qoq_w4a8_gemm_i32(Qx, t_x, packed, N: int, K: int, group: int = 128, acc=Non
     return acc
 
 
-def gemm_options(tokens_per_tile=0, num_ctas=0, timeout_ns=0, debug_flags=0, acc_out=None, kernel=0):
+def gemm_options(tokens_per_tile=0, num_ctas=0, timeout_ns=0, debug_flags=0, acc_out=None, kernel=0,
+                 act_operand=None):
     return qoq_gemm_options(tokens_per_tile, num_ctas, timeout_ns, debug_flags,
-                            None if acc_out is None else acc_out.data_ptr(), kernel)
+                            None if acc_out is None else acc_out.data_ptr(), kernel,
+                            None if act_operand is None else act_operand.data_ptr())
 
 
 def qoq_w4a8_gemm_ex(Qx, s_x, t_x, packed, s_w, N: int, K: int, group: int = 128, O=None,

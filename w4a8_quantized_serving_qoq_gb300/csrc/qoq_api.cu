@@ -57,6 +57,8 @@ bool plan_for(int M, int N, int K, int group, const qoq_gemm_options *opt, qoq::
 int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const void *packed,
                 const uint16_t *s_w, int M, int N, int K, int group, uint16_t *O, int32_t *acc_out,
                 void *ws, size_t ws_bytes, const qoq_gemm_options *opt, cudaStream_t stream) {
+    const void *act = opt ? opt->act_operand : nullptr;
+    if (act && !aligned(act, 16)) return QOQ_ERR_MISALIGNED;
     int st = check_gemm_shape(M, N, K, group);
     if (st != QOQ_OK) return st;
     st = check_options(opt);
@@ -82,6 +84,7 @@ int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const
     a.N = N;
     a.K = K;
     a.group = group;
+    a.act = plan.path == qoq::kPathF8 ? act : nullptr;
     a.O = O;
     a.acc_out = acc_out;
     a.ws = ws;
@@ -155,7 +158,25 @@ int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, in
     if (!X || !Qx || !s_x) return QOQ_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) || (t_x && !aligned(t_x, 4)))
         return QOQ_ERR_MISALIGNED;
-    return cuda_status(qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, reinterpret_cast<cudaStream_t>(stream)));
+    return cuda_status(
+        qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, nullptr, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t qoq_act_operand_bytes(int M, int K) {
+    if (M <= 0 || K <= 0 || K % 128 != 0) return 0;
+    return qoq::act_operand_bytes(M, K);
+}
+
+int qoq_quant_act_ex(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x,
+                     void *act_operand, qoq_stream_t stream) {
+    if (M <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
+    if (K % 8 != 0 || (act_operand && K % 128 != 0)) return QOQ_ERR_UNSUPPORTED;
+    if (!X || !Qx || !s_x) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) || (t_x && !aligned(t_x, 4)) ||
+        (act_operand && !aligned(act_operand, 16)))
+        return QOQ_ERR_MISALIGNED;
+    return cuda_status(
+        qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, act_operand, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gemm_options *opt) {
@@ -167,6 +188,16 @@ size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gem
 
 size_t qoq_gemm_workspace_bytes(int M, int N, int K, int group) {
     return qoq_gemm_workspace_bytes_ex(M, N, K, group, nullptr);
+}
+
+int qoq_gemm_path(int M, int N, int K, int group, const qoq_gemm_options *opt) {
+    int st = check_gemm_shape(M, N, K, group);
+    if (st != QOQ_OK) return -st;
+    st = check_options(opt);
+    if (st != QOQ_OK) return -st;
+    qoq::GemmPlan plan;
+    if (!plan_for(M, N, K, group, opt, &plan)) return -QOQ_ERR_CUDA;
+    return plan.path;
 }
 
 int qoq_workspace_init(void *workspace, size_t bytes, qoq_stream_t stream) {

@@ -523,7 +523,13 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
     pl.ctas = static_cast<int>(ctas);
     pl.counters_offset = kWsStatusBytes;
     pl.slots_offset = kWsStatusBytes + (static_cast<size_t>(pl.ctas) * 4 + 255) / 256 * 256;
-    pl.ws_bytes = pl.slots_offset + static_cast<size_t>(pl.ctas) * bt * kTileN * 4;
+    pl.zero_bytes = pl.slots_offset + static_cast<size_t>(pl.ctas) * bt * kTileN * 4;
+    pl.act_offset = 0;
+    pl.ws_bytes = pl.zero_bytes;
+    if (path == kPathF8) {
+        pl.act_offset = (pl.zero_bytes + 255) / 256 * 256;
+        pl.ws_bytes = pl.act_offset + act_operand_bytes(M, K);
+    }
     return pl;
 }
 

@@ -10,7 +10,11 @@
 //    multiply;
 //  * an activation is split as u = Qx + 128 = 16*uh + ul with uh, ul in
 //    [0, 15], stored the same way; the two planes are stacked along the MMA's
-//    N dimension (2*BT rows), which costs nothing for N <= 128;
+//    N dimension (2*BT rows), which costs nothing for N <= 128.  The planes
+//    and the per-group activation sums t_g come precomputed (the activation
+//    operand written by the activation quantizer, or by a preparation kernel
+//    launched before this one), so TMA lands the B operand directly in its
+//    swizzled shared-memory layout;
 //  * per 128-k group, D_h = 2^-18 sum q*uh and D_l = 2^-18 sum q*ul are exact in
 //    the fp32 accumulator (|sum| <= 128*15*15 = 28800 units of 2^-18);
 //  * the epilogue turns each group into an integer without a conversion
@@ -18,13 +22,17 @@
 //    spaced by 2^-18, so its bit pattern minus that of 48 is
 //    P = sum_k q*u = sum_k q*Qx + 128*sum_k q.  Then
 //      acc += s_g * (P - 128*sum_k q - z*t_g[m]),  t_g[m] = sum_{k in g} Qx[m,k].
-//    sum_k q comes with the packed metadata; t_g is summed by the converter
-//    warps while they split the activations.
-// K-stages are 256 wide (two groups per TMA copy), four MMAs (K = 32) per
-// group.  Roles: warp 0 TMA, warp 1 MMA (+ TMEM allocation), warps 4-7
-// convert (one TMEM lane quarter each), warps 8-15 drain (two per lane
-// quarter, one half of the tokens each).  Persistent stream-K schedule, exact
-// int32 reduction of split tiles and bounded waits as in the fp16 path.
+//    sum_k q comes with the packed metadata.
+// K-stages are 256 wide (two groups per TMA transaction), four MMAs (K = 32)
+// per group.  Roles (20 warps): warp 0 TMA, warps 1 and 2 issue the MMAs of
+// alternate stages (warp 1 also allocates TMEM), warps 4-7 and 16-19 two
+// converter groups that take alternate stages (one
+// TMEM lane quarter per warp: codes -> bytes -> TMEM), warps 8-15 drain (two
+// per lane quarter, one half of the tokens each).  A drained stage also
+// proves its MMAs complete, so the drain's release of a stage's metadata
+// slot is what frees the matching TMEM operand slot too.  Persistent
+// stream-K schedule, exact int32 reduction of split tiles and bounded waits
+// as in the fp16 path.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -35,8 +43,8 @@
 namespace qoq {
 namespace {
 
-constexpr int kF8Threads = 512;
-constexpr int kF8ConvWarps = 4;      // warps 4..7
+constexpr int kF8Threads = 640;
+constexpr int kF8ConvWarps = 4;      // per converter group: warps 4..7 and 16..19
 constexpr int kF8EpiWarps = 8;       // warps 8..15
 constexpr int kF8EpiThreads = 32 * kF8EpiWarps;
 constexpr int kGroupsPerStage = 2;
@@ -45,28 +53,31 @@ constexpr uint32_t kBlockBytesG = kCodeBytes + kMetaBytes;  // 8704
 template <int BT>
 struct F8Cfg {
     static constexpr int kNmma = 2 * BT;                  // uh plane rows + ul plane rows
-    static constexpr int kRawStages = BT == 16 ? 6 : 5;
-    static constexpr int kOpStages = 4;
-    static constexpr int kAuxStages = 4;
-    static constexpr uint32_t kQxRawBytes = static_cast<uint32_t>(BT) * 128u * kGroupsPerStage;
-    static constexpr uint32_t kWRawBytes = kGroupsPerStage * kBlockBytesG;  // 17408 = 17 KB
-    static constexpr uint32_t kRawSlotBytes = kQxRawBytes + kWRawBytes;
-    static constexpr uint32_t kBGroupBytes = static_cast<uint32_t>(kNmma) * 128u;
-    static constexpr uint32_t kOpStageBytes = kGroupsPerStage * kBGroupBytes;
+    static constexpr int kRawStages = 6;
+    static constexpr int kOpStages = 4;                   // TMEM A slots == metadata slots
+    static constexpr int kAuxStages = kOpStages;
+    // Raw slot: [B planes, group 0 | group 1][t_g 2 x BT][weight blocks 2 x 8704].
+    static constexpr uint32_t kPlaneGroupBytes = static_cast<uint32_t>(kNmma) * 128u;
+    static constexpr uint32_t kTgOff = kGroupsPerStage * kPlaneGroupBytes;
+    static constexpr uint32_t kTgBytes = kGroupsPerStage * static_cast<uint32_t>(BT) * 4u;
+    static constexpr uint32_t kWOff = kTgOff + kTgBytes;
+    static constexpr uint32_t kRawSlotBytes = (kWOff + kGroupsPerStage * kBlockBytesG + 1023u) / 1024u * 1024u;
     static constexpr uint32_t kAuxMetaBytes = kGroupsPerStage * 128u * 4u;
-    static constexpr uint32_t kAuxStageBytes = kAuxMetaBytes + kGroupsPerStage * BT * 4u;
-    // TMEM: D buffers [2 stage sets][2 groups] x kNmma columns, then A stages of
+    static constexpr uint32_t kAuxStageBytes = kAuxMetaBytes + kTgBytes;
+    // TMEM: D buffers [2 stage sets][2 groups] x kNmma columns, then A slots of
     // 64 columns (128 rows x 256 k bytes).
     static constexpr uint32_t kA0 = 4u * kNmma;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 2 * kAuxStages + 4 + 1;
+    static constexpr int kNumBars = 2 * kRawStages + kOpStages + 2 * kAuxStages + 4 + 1;
     static constexpr uint32_t kMiscBytes = 2048;
-    static constexpr uint32_t kSmemBytes = kOpStages * kOpStageBytes + kRawStages * kRawSlotBytes +
-                                           kAuxStages * kAuxStageBytes + kMiscBytes + 1024;
+    static constexpr uint32_t kSmemBytes =
+        kRawStages * kRawSlotBytes + kAuxStages * kAuxStageBytes + kMiscBytes + 1024;
     static_assert(kA0 + 64u * kOpStages <= kTmemCols, "TMEM columns");
     static_assert(kNumBars * 8 + 64 <= 1024, "barrier area");
     static_assert(kSmemBytes <= 232448, "shared memory");
-    static_assert(kRawSlotBytes % 1024 == 0 && kOpStageBytes % 1024 == 0, "1 KB aligned slots");
+    static_assert(kPlaneGroupBytes % 1024 == 0 && kRawSlotBytes % 1024 == 0, "1 KB aligned swizzled tiles");
+    static_assert(kWOff % 16 == 0 && kTgOff % 16 == 0, "16-byte aligned bulk copies");
+    static_assert((kAuxStages * kAuxStageBytes) % 8 == 0, "barrier alignment");
 };
 
 __device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -113,22 +124,21 @@ __device__ __forceinline__ void tmem_wait_ld_pin(uint32_t (&a)[N], uint32_t (&b)
 
 template <int BT>
 __global__ void __launch_bounds__(kF8Threads, 1)
-    w4a8_gemm_f8_kernel(const __grid_constant__ CUtensorMap qx_map, const GemmParams p) {
+    w4a8_gemm_f8_kernel(const __grid_constant__ CUtensorMap plane_map, const __grid_constant__ CUtensorMap tg_map,
+                        const GemmParams p) {
     using C = F8Cfg<BT>;
     constexpr int R = C::kRawStages, OPS = C::kOpStages, AUX = C::kAuxStages;
     constexpr int HT = BT / 2;  // tokens per drain thread
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *op_base = smem;                                     // B planes, 1 KB aligned
-    uint8_t *raw_base = op_base + OPS * C::kOpStageBytes;        // [Qx box | 2 weight blocks]
+    uint8_t *raw_base = smem;                                    // [B planes | t_g | 2 weight blocks]
     uint8_t *aux_base = raw_base + R * C::kRawSlotBytes;         // [meta 2x128x4 | t_g 2xBT]
     uint64_t *bars = reinterpret_cast<uint64_t *>(aux_base + AUX * C::kAuxStageBytes);
     uint64_t *raw_full = bars;
     uint64_t *raw_empty = raw_full + R;
     uint64_t *op_full = raw_empty + R;
-    uint64_t *op_empty = op_full + OPS;
-    uint64_t *aux_full = op_empty + OPS;
+    uint64_t *aux_full = op_full + OPS;
     uint64_t *aux_empty = aux_full + AUX;
     uint64_t *d_full = aux_empty + AUX;
     uint64_t *d_empty = d_full + 2;
@@ -145,7 +155,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
-        prefetch_tensormap(&qx_map);
+        prefetch_tensormap(&plane_map);
+        prefetch_tensormap(&tg_map);
         const PackedHeader *h = reinterpret_cast<const PackedHeader *>(p.packed);
         const bool ok = h->magic == kPackedMagic && h->version == kPackedVersion && h->N == p.N &&
                         h->K == p.K && h->group == p.group && h->illegal == 0u && p.group == 128;
@@ -155,12 +166,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         *is_last = 0;
         for (int i = 0; i < R; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], kF8ConvWarps);
+            mbar_init(&raw_empty[i], kF8ConvWarps + 1);  // one converter group + the MMA commit
         }
-        for (int i = 0; i < OPS; ++i) {
-            mbar_init(&op_full[i], kF8ConvWarps);
-            mbar_init(&op_empty[i], 1);
-        }
+        for (int i = 0; i < OPS; ++i) mbar_init(&op_full[i], kF8ConvWarps);
         for (int i = 0; i < AUX; ++i) {
             mbar_init(&aux_full[i], kF8ConvWarps);
             mbar_init(&aux_empty[i], kF8EpiWarps);
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             mbar_init(&d_full[i], 1);
             mbar_init(&d_empty[i], kF8EpiWarps);
         }
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 2);  // one commit per issuing thread
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
@@ -188,6 +196,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             bool stop = false;
             while (!stop && walk.next(sg)) {
                 const int tok_tile = sg.tile % p.tok_tiles, n_tile = sg.tile / p.tok_tiles;
+                const int m0 = tok_tile * BT;
                 const uint8_t *wrow = p.packed + kHeaderBytes + static_cast<size_t>(n_tile) * p.G * kBlockBytesG;
                 for (int k = sg.k0; k < sg.k1; k += kGroupsPerStage, ++st) {
                     const int ng = min(kGroupsPerStage, sg.k1 - k);
@@ -201,28 +210,39 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                         break;
                     }
                     uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
-                    mbar_arrive_expect_tx(&raw_full[slot], C::kQxRawBytes + ng * kBlockBytesG);
-                    tma_load_1d(dst + C::kQxRawBytes, wrow + static_cast<size_t>(k) * kBlockBytesG,
-                                ng * kBlockBytesG, &raw_full[slot]);
-                    tma_load_3d(dst, &qx_map, 0, tok_tile * BT, k, &raw_full[slot]);
+                    mbar_arrive_expect_tx(&raw_full[slot], ng * (kBlockBytesG + C::kPlaneGroupBytes) + C::kTgBytes);
+                    tma_load_1d(dst + C::kWOff, wrow + static_cast<size_t>(k) * kBlockBytesG, ng * kBlockBytesG,
+                                &raw_full[slot]);
+                    for (int g = 0; g < ng; ++g)
+                        tma_load_3d(dst + g * C::kPlaneGroupBytes, &plane_map, (k + g) * kTileK, m0, 0,
+                                    &raw_full[slot]);
+                    tma_load_2d(dst + C::kTgOff, &tg_map, m0, k, &raw_full[slot]);
                     issued = st + 1;
                 }
             }
             for (int t = (issued > R ? issued - R : 0); t < issued; ++t)
                 mbar_wait(&raw_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
         }
-    } else if (run && warp == 1) {
-        // ------------------------------------------------- MMA issuer --
+    } else if (run && (warp == 1 || warp == 2)) {
+        // ------------------------------------------------ MMA issuers --
+        // Two issuing threads take alternate stages (warp 1 even, warp 2
+        // odd; stage parity is also the D set).  A barrier wait issued after
+        // a thread's own MMAs queues behind them, so with one issuer every
+        // wait left the tensor pipe idle; with two, one thread waits while
+        // the other's MMAs execute.  tcgen05.commit tracks the MMAs of the
+        // committing thread, which are exactly those of its own stages.
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(128, C::kNmma);  // e4m3 x e4m3 -> f32 for kind::f8f6f4
+            const int par = warp - 1;
             SegmentWalker walk(p, cta);
             Segment sg;
             int st = 0;
             bool stop = false;
             while (!stop && walk.next(sg)) {
                 for (int k = sg.k0; k < sg.k1; k += kGroupsPerStage, ++st) {
+                    if ((st & 1) != par) continue;
                     const int ng = min(kGroupsPerStage, sg.k1 - k);
-                    const int os = st % OPS, ouse = st / OPS;
+                    const int rs = st % R, os = st % OPS, ouse = st / OPS;
                     const int ds = st & 1, duse = st >> 1;
                     if ((duse > 0 && !mbar_wait(&d_empty[ds], (duse - 1) & 1, abort_flag, p.status, tmo)) ||
                         !mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
@@ -230,26 +250,30 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes);
+                    const uint32_t b_base = smem_u32(raw_base + rs * C::kRawSlotBytes);
                     for (int g = 0; g < ng; ++g) {
                         const uint32_t d_tmem = tmem + static_cast<uint32_t>((2 * ds + g) * C::kNmma);
                         const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u + 32u * g;
-                        const uint32_t bg = b_base + g * C::kBGroupBytes;
+                        const uint32_t bg = b_base + g * C::kPlaneGroupBytes;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             mma_f8_tmem_a(d_tmem, a_tmem + 8u * kk, desc_kmajor_sw128(bg + 32u * kk), idesc,
                                           kk ? 1u : 0u);
                     }
-                    mma_commit(&op_empty[os]);
+                    mma_commit(&raw_empty[rs]);
                     mma_commit(&d_full[ds]);
                 }
             }
+            // All of this thread's MMAs must finish before TMEM is released.
             mma_commit(mma_done);
             mbar_wait(mma_done, 0, nullptr, p.status, tmo);
         }
-    } else if (run && warp >= 4 && warp < 8) {
+    } else if (run && ((warp >= 4 && warp < 8) || warp >= 16)) {
         // ---------------------------------------------- converter warps --
-        const int wr = (warp & 3) * 32 + lane;  // weight row == TMEM lane; also the item index
+        // Group 0 (warps 4-7) takes even stages, group 1 (warps 16-19) odd
+        // ones, so one group's waits overlap the other's conversion.
+        const int cg = warp >= 16 ? 1 : 0;
+        const int wr = (warp & 3) * 32 + lane;  // weight row == TMEM lane
         const uint32_t a_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         SegmentWalker walk(p, cta);
         Segment sg;
@@ -257,22 +281,21 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         bool stop = false;
         while (!stop && walk.next(sg)) {
             for (int k = sg.k0; k < sg.k1; k += kGroupsPerStage, ++st) {
+                if ((st & 1) != cg) continue;
                 const int ng = min(kGroupsPerStage, sg.k1 - k);
-                const int rs = st % R, ruse = st / R, os = st % OPS, ouse = st / OPS, as = st % AUX,
-                          ause = st / AUX;
+                const int rs = st % R, ruse = st / R, os = st % OPS, as = st % AUX, ause = st / AUX;
+                // aux_empty of this slot means the drain finished stage st - AUX,
+                // whose MMAs therefore completed: TMEM A slot os is free as well.
                 if (!mbar_wait_warp(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo) ||
-                    (ouse > 0 && !mbar_wait_warp(&op_empty[os], (ouse - 1) & 1, abort_flag, p.status, tmo)) ||
                     (ause > 0 && !mbar_wait_warp(&aux_empty[as], (ause - 1) & 1, abort_flag, p.status, tmo))) {
                     stop = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t raw = smem_u32(raw_base + rs * C::kRawSlotBytes);
-                const uint32_t wraw = raw + C::kQxRawBytes;
-                const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes);
+                const uint8_t *raw = raw_base + rs * C::kRawSlotBytes;
+                const uint32_t wraw = smem_u32(raw) + C::kWOff;
                 uint8_t *aux = aux_base + as * C::kAuxStageBytes;
                 uint32_t *aux_meta = reinterpret_cast<uint32_t *>(aux);
-                int *aux_tg = reinterpret_cast<int *>(aux + C::kAuxMetaBytes);
 
                 // Weights: row wr, 128 k per group -> 128 code bytes (e4m3 q * 2^-9)
                 // -> 32 TMEM columns of this lane per group.
@@ -294,35 +317,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(meta) : "r"(blk + kCodeBytes + 4 * wr));
                     aux_meta[g * 128 + wr] = meta;
                 }
-                // Activations: items (group, token, 16-byte chunk); eight consecutive
-                // lanes take the eight chunks of one token row.
-                constexpr int kItems = kGroupsPerStage * BT * 8;
-#pragma unroll
-                for (int it0 = 0; it0 < kItems; it0 += 128) {
-                    const int it = it0 + wr;
-                    const int g = it / (8 * BT), r = (it / 8) % BT, c = it % 8;
-                    int part = 0;
-                    if (g < ng) {
-                        const uint4 v = ld_shared_v4(raw + (g * BT + r) * 128 + ((c ^ (r & 7)) << 4));
-                        const uint32_t x4[4] = {v.x, v.y, v.z, v.w};
-                        uint32_t hi[4], lo[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            part = __dp4a(static_cast<int>(x4[j]), 0x01010101, part);  // signed byte sum
-                            const uint32_t u = x4[j] ^ 0x80808080u;                   // Qx + 128
-                            hi[j] = (u >> 4) & 0x0F0F0F0Fu;
-                            lo[j] = u & 0x0F0F0F0Fu;
-                        }
-                        const uint32_t bg = b_base + g * C::kBGroupBytes;
-                        st_shared_v4(bg + sw128_offset(r, c), hi[0], hi[1], hi[2], hi[3]);
-                        st_shared_v4(bg + sw128_offset(BT + r, c), lo[0], lo[1], lo[2], lo[3]);
-                    }
-                    part += __shfl_xor_sync(0xffffffffu, part, 1);
-                    part += __shfl_xor_sync(0xffffffffu, part, 2);
-                    part += __shfl_xor_sync(0xffffffffu, part, 4);
-                    if (c == 0 && g < ng) aux_tg[g * BT + r] = part;
+                // Per-group activation sums for the drain: [2 groups][BT] int32.
+                if ((warp & 3) == 0) {
+                    const int *src = reinterpret_cast<const int *>(raw + C::kTgOff);
+                    int *dstg = reinterpret_cast<int *>(aux + C::kAuxMetaBytes);
+                    for (int i = lane; i < kGroupsPerStage * BT; i += 32) dstg[i] = src[i];
                 }
-                fence_proxy_async_smem();
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 }
             }
         }
-    } else if (run && warp >= 8) {
+    } else if (run && warp >= 8 && warp < 16) {
         // ------------------------------------------------- drain warps --
         const int ew = warp - 8;
         const int et = threadIdx.x - 256;          // 0..255 among the drain threads
@@ -474,18 +474,41 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
     }
     CUtensorMapEncodeTiledFn enc = get_encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    // Qx [M][K] viewed as [K/128][M][128]: one box = 2 groups x BT rows x 128 k.
-    CUtensorMap map;
-    const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(a.M), static_cast<cuuint64_t>(a.K / 128)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.K), 128u};
-    const cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(BT), static_cast<cuuint32_t>(kGroupsPerStage)};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<int8_t *>(a.Qx), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    GemmParams p;
     uint8_t *ws = static_cast<uint8_t *>(a.ws);
+    const uint8_t *act = static_cast<const uint8_t *>(a.act);
+    if (!act) {
+        // No precomputed operand: build it from Qx in the workspace first.
+        uint8_t *scratch = ws + plan.act_offset;
+        e = launch_act_operand(a.Qx, a.M, a.K, scratch, stream);
+        if (e != cudaSuccess) return e;
+        act = scratch;
+    }
+    // B planes [2][M][K] bytes: one box = one group = {128 k, BT tokens, 2 planes}.
+    CUtensorMap plane_map, tg_map;
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.M), 2u};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.K),
+                                       static_cast<cuuint64_t>(a.M) * static_cast<cuuint64_t>(a.K)};
+        const cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(BT), 2u};
+        const cuuint32_t estr[3] = {1u, 1u, 1u};
+        CUresult cr = enc(&plane_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(act), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    // t_g [K/128][Mp] int32: one box = {BT tokens, 2 groups}; tokens past M read as 0.
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.M), static_cast<cuuint64_t>(plan.G)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(act_tg_pitch(a.M)) * 4u};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(BT), static_cast<cuuint32_t>(kGroupsPerStage)};
+        const cuuint32_t estr[2] = {1u, 1u};
+        CUresult cr = enc(&tg_map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2,
+                          const_cast<uint8_t *>(act + act_planes_bytes(a.M, a.K)), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    GemmParams p;
     p.packed = static_cast<const uint8_t *>(a.packed);
     p.s_x = a.s_x;
     p.t_x = a.t_x;
@@ -505,7 +528,7 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
     p.ctas = plan.ctas;
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
-    w4a8_gemm_f8_kernel<BT><<<dim3(plan.ctas), kF8Threads, C::kSmemBytes, stream>>>(map, p);
+    w4a8_gemm_f8_kernel<BT><<<dim3(plan.ctas), kF8Threads, C::kSmemBytes, stream>>>(plane_map, tg_map, p);
     return cudaGetLastError();
 }
 

@@ -72,8 +72,9 @@ extern "C" int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, cons
     if (plan.ws_bytes > kNoAllocScratchBytes) return QOQ_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // The array keeps whatever the previous call left; the GEMM needs its
-    // status word, counters and partial slots to start at zero.
-    if (cudaMemsetAsync(scratch, 0, plan.ws_bytes, s) != cudaSuccess) return QOQ_ERR_CUDA;
+    // status word, counters and partial slots to start at zero (the fp8
+    // path's activation scratch after them is fully overwritten each call).
+    if (cudaMemsetAsync(scratch, 0, plan.zero_bytes, s) != cudaSuccess) return QOQ_ERR_CUDA;
     qoq::GemmArgs a;
     a.Qx = Qx;
     a.s_x = s_x;
@@ -84,6 +85,7 @@ extern "C" int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, cons
     a.N = N;
     a.K = K;
     a.group = group;
+    a.act = nullptr;
     a.O = O;
     a.acc_out = nullptr;
     a.ws = scratch;

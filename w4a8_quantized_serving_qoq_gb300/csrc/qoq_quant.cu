@@ -47,48 +47,144 @@ struct MaxOp { __device__ float operator()(float a, float b) const { return fmax
 struct MinOp { __device__ float operator()(float a, float b) const { return fminf(a, b); } };
 struct SumOp { __device__ int operator()(int a, int b) const { return a + b; } };
 
+// Quantize eight fp16 values (one 16-byte load) with scale sf; returns the
+// eight INT8 codes as two words and adds them to *sum.
+__device__ __forceinline__ uint2 quant8(const uint4 v, float sf, int *sum) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint16_t hb = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu));
+        int q = 0;
+        if (sf != 0.f) q = clampi(__float2int_rn(__fdiv_rn(h2f(hb), sf)), -127, 127);
+        *sum += q;
+        out[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << ((j & 3) * 8);
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+__device__ __forceinline__ float amax8(const uint4 v, float amax) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        amax = fmaxf(amax, fabsf(h2f(static_cast<uint16_t>(w[j] & 0xffffu))));
+        amax = fmaxf(amax, fabsf(h2f(static_cast<uint16_t>(w[j] >> 16))));
+    }
+    return amax;
+}
+
+// Activation-operand bytes of eight INT8 codes (two words): u = Qx + 128
+// (flip of the sign bit), then its high and low nibble planes.
+__device__ __forceinline__ void split_u(uint2 q, uint2 &hi, uint2 &lo) {
+    const uint32_t u0 = q.x ^ 0x80808080u, u1 = q.y ^ 0x80808080u;
+    hi = make_uint2((u0 >> 4) & 0x0F0F0F0Fu, (u1 >> 4) & 0x0F0F0F0Fu);
+    lo = make_uint2(u0 & 0x0F0F0F0Fu, u1 & 0x0F0F0F0Fu);
+}
+
+constexpr int kActCache = 4;  // 16-byte items per thread kept in registers between the passes
+
 // One CTA per token row.  s_x = fp16(max|x| / 127); Qx = clamp(rne(x / s_x), -127, 127);
-// an all-zero scale gives an all-zero row; t_x = row sum of Qx.
-__global__ void quant_act_kernel(const uint16_t *__restrict__ X, int K, int8_t *__restrict__ Qx,
-                                 uint16_t *__restrict__ s_x, int32_t *__restrict__ t_x) {
+// an all-zero scale gives an all-zero row; t_x = row sum of Qx.  With
+// kAct, also the fp8-path activation operand (planes of u = Qx + 128 and the
+// per-group sums t_g).  The trip count of every loop is uniform across the
+// CTA (blockDim.x is a multiple of 32), so the half-warp shuffles that sum
+// one 128-k group (16 items of 8) always run with every lane present.
+template <bool kAct>
+__global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, int8_t *__restrict__ Qx,
+                                 uint16_t *__restrict__ s_x, int32_t *__restrict__ t_x,
+                                 uint8_t *__restrict__ act) {
     __shared__ float shf[32];
     __shared__ int shi[32];
     const size_t m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(X + m * K);
-    const int nv = K >> 3;
+    const int nv = K >> 3, bd = blockDim.x, tid = threadIdx.x;
+    uint4 cache[kActCache];
     float amax = 0.f;
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-        uint4 v = __ldg(row + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            amax = fmaxf(amax, fabsf(h2f(static_cast<uint16_t>(w[j] & 0xffffu))));
-            amax = fmaxf(amax, fabsf(h2f(static_cast<uint16_t>(w[j] >> 16))));
-        }
+    for (int j = 0; j < kActCache; ++j) {
+        const int i = tid + j * bd;
+        cache[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < nv) cache[j] = __ldg(row + i);
+        amax = amax8(cache[j], amax);
     }
+    for (int i = tid + kActCache * bd; i < nv; i += bd) amax = amax8(__ldg(row + i), amax);
     amax = block_reduce(amax, MaxOp(), shf);
     const uint16_t sbits = f2h_rn(__fdiv_rn(amax, 127.0f));
     const float sf = h2f(sbits);
-    int tsum = 0;
+
     uint2 *qrow = reinterpret_cast<uint2 *>(Qx + m * K);
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-        uint4 v = __ldg(row + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[2] = {0u, 0u};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint16_t hb = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu));
-            int q = 0;
-            if (sf != 0.f) q = clampi(__float2int_rn(__fdiv_rn(h2f(hb), sf)), -127, 127);
-            tsum += q;
-            out[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << ((j & 3) * 8);
+    uint2 *hrow = nullptr, *lrow = nullptr;
+    int32_t *tg = nullptr;
+    const int pitch = act_tg_pitch(M);
+    if (kAct) {
+        hrow = reinterpret_cast<uint2 *>(act + m * K);
+        lrow = reinterpret_cast<uint2 *>(act + static_cast<size_t>(M) * K + m * K);
+        tg = reinterpret_cast<int32_t *>(act + act_planes_bytes(M, K));
+    }
+    int tsum = 0;
+    auto emit = [&](int i, const uint4 v) {
+        int part = 0;
+        uint2 q = make_uint2(0u, 0u);
+        if (i < nv) {
+            q = quant8(v, sf, &part);
+            qrow[i] = q;
         }
-        qrow[i] = make_uint2(out[0], out[1]);
+        tsum += part;
+        if (kAct) {
+            if (i < nv) {
+                uint2 hi, lo;
+                split_u(q, hi, lo);
+                hrow[i] = hi;
+                lrow[i] = lo;
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if ((tid & 15) == 0 && i < nv) tg[static_cast<size_t>(i >> 4) * pitch + m] = part;
+        }
+    };
+#pragma unroll
+    for (int j = 0; j < kActCache; ++j)
+        if (j * bd < nv) emit(tid + j * bd, cache[j]);
+    for (int base = kActCache * bd; base < nv; base += bd) {
+        const int i = base + tid;
+        emit(i, i < nv ? __ldg(row + i) : make_uint4(0u, 0u, 0u, 0u));
     }
     tsum = block_reduce(tsum, SumOp(), shi);
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         s_x[m] = sbits;
         if (t_x) t_x[m] = tsum;
+    }
+}
+
+// fp8-path activation operand from INT8 activations: one CTA per token row,
+// one 16-byte item (16 codes) per thread and step; eight items form a group.
+__global__ void act_operand_kernel(const int8_t *__restrict__ Qx, int M, int K, uint8_t *__restrict__ act) {
+    const size_t m = blockIdx.x;
+    const int nv = K >> 4, pitch = act_tg_pitch(M);
+    const uint4 *row = reinterpret_cast<const uint4 *>(Qx + m * K);
+    uint4 *hrow = reinterpret_cast<uint4 *>(act + m * K);
+    uint4 *lrow = reinterpret_cast<uint4 *>(act + static_cast<size_t>(M) * K + m * K);
+    int32_t *tg = reinterpret_cast<int32_t *>(act + act_planes_bytes(M, K));
+    for (int base = 0; base < nv; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        int part = 0;
+        if (i < nv) {
+            const uint4 v = __ldg(row + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                part = __dp4a(static_cast<int>(w[j]), 0x01010101, part);
+                const uint32_t u = w[j] ^ 0x80808080u;
+                hi[j] = (u >> 4) & 0x0F0F0F0Fu;
+                lo[j] = u & 0x0F0F0F0Fu;
+            }
+            hrow[i] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            lrow[i] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if ((threadIdx.x & 7) == 0 && i < nv) tg[static_cast<size_t>(i >> 3) * pitch + m] = part;
     }
 }
 
@@ -166,10 +262,18 @@ __global__ void quantize_channel_kernel(const uint16_t *__restrict__ W, int K,
 }  // namespace
 
 cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
-                             int32_t *t_x, cudaStream_t stream) {
+                             int32_t *t_x, void *act_operand, cudaStream_t stream) {
     // Few long rows: one wide CTA per row keeps the per-row latency short.
     const int threads = (M < 296) ? 1024 : 256;
-    quant_act_kernel<<<M, threads, 0, stream>>>(X, K, Qx, s_x, t_x);
+    if (act_operand)
+        quant_act_kernel<true><<<M, threads, 0, stream>>>(X, M, K, Qx, s_x, t_x, static_cast<uint8_t *>(act_operand));
+    else
+        quant_act_kernel<false><<<M, threads, 0, stream>>>(X, M, K, Qx, s_x, t_x, nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_act_operand(const int8_t *Qx, int M, int K, void *act_operand, cudaStream_t stream) {
+    act_operand_kernel<<<M, 256, 0, stream>>>(Qx, M, K, static_cast<uint8_t *>(act_operand));
     return cudaGetLastError();
 }
 
