@@ -242,19 +242,17 @@ def main():
             sx = torch.empty((M,), dtype=torch.float16, device=dev)
             O = torch.empty((M, layer.N), dtype=torch.float16, device=dev)
             ws_max = max(ws_max, qoq.qoq_gemm_workspace_bytes(M, layer.N, layer.K, 128))
-            # decode sizes take the fp8-operand path: the quantizer also writes
-            # the activation operand that path reads
-            act = None
-            if qoq.qoq_gemm_path(M, layer.N, layer.K, 128) == 2:
-                act = torch.empty((qoq.qoq_act_operand_bytes(M, layer.K),), dtype=torch.uint8, device=dev)
-            points.append(dict(layer=layer, M=M, X=X, Qx=Qx, sx=sx, O=O, act=act,
+            # the quantizer also writes the activation operand the GEMM's path
+            # reads (fp8 planes for decode sizes, an fp16 copy above)
+            kind = qoq.qoq_gemm_path(M, layer.N, layer.K, 128)
+            act = torch.empty((qoq.qoq_act_operand_bytes(M, layer.K, kind),), dtype=torch.uint8, device=dev)
+            points.append(dict(layer=layer, M=M, X=X, Qx=Qx, sx=sx, O=O, act=act, kind=kind,
                                opt=qoq.gemm_options(act_operand=act)))
     ws = qoq.new_workspace(ws_max, dev)
     torch.cuda.synchronize()
 
     def quant_point(pt):
-        qoq.qoq_quant_act_ex(pt["X"], pt["Qx"], pt["sx"], None, pt["act"], with_t=False,
-                             with_act=pt["act"] is not None)
+        qoq.qoq_quant_act_ex(pt["X"], pt["Qx"], pt["sx"], None, pt["act"], kind=pt["kind"], with_t=False)
 
     def gemm_point(pt, copy_idx):
         layer = pt["layer"]
@@ -395,7 +393,7 @@ def main():
                    f"rotated ({sum(len(c) * c[0].numel() for c, _ in weights.values()) / 1e6:.0f} MB)"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
-                     "peak_source": peaks_src, "kernel": "w4a8_gemm (fp8-operand kernel for M <= 32, fp16-operand above)",
+                     "peak_source": peaks_src, "kernel": "w4a8_gemm (fp8-operand kernel for M <= 32, fp16-operand kernel above)",
                      "time_weighted_roofline_frac": troof_sum / (gemm_ms_total * 1e-3),
                      "tensor_peak_tflops": peaks["bf16_tflops"]},
         "cpu_baseline": cpu,

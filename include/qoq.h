@@ -123,35 +123,44 @@ int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, in
                   qoq_stream_t stream);
 
 /*
- * Bytes of the activation operand that the GEMM's fp8-operand path reads
- * (0 for an invalid shape; requires K % 128 == 0).  Layout, for M tokens:
- *   [u_hi plane: M x K bytes][u_lo plane: M x K bytes][t_g: (K/128) x Mp int32]
- * with u = Qx + 128 = 16*u_hi + u_lo (u_hi, u_lo in [0, 15]),
- * t_g[g][m] = sum of Qx[m, k] over the 128 k of group g, and Mp = M rounded
- * up to a multiple of 4.  It is the INT8 activation of qoq_quant_act in the
- * order and encoding the kernel consumes (the activation-side counterpart of
- * the compute-aware weight reordering of [QS-summary] "计算感知权重重排序").
+ * Bytes of an activation operand (0 for an invalid shape or kind; requires
+ * K % 128 == 0).  An activation operand is the INT8 activation of
+ * qoq_quant_act in the order and encoding one GEMM path's tensor cores
+ * consume (the activation-side counterpart of the compute-aware weight
+ * reordering of [QS-summary] "计算感知权重重排序"); the GEMM lands it in shared
+ * memory with TMA, without conversion work.  Two kinds, numbered like the
+ * path that reads them (qoq_gemm_path):
+ *   kind 1, fp16-operand path: Qx as fp16, [M][K] (int8 values are exact in
+ *     fp16), 2*M*K bytes.
+ *   kind 2, fp8-operand path:
+ *     [u_hi plane: M x K bytes][u_lo plane: M x K bytes][t_g: (K/128) x Mp int32]
+ *     with u = Qx + 128 = 16*u_hi + u_lo (u_hi, u_lo in [0, 15]),
+ *     t_g[g][m] = sum of Qx[m, k] over the 128 k of group g, and Mp = M
+ *     rounded up to a multiple of 4.
  */
-size_t qoq_act_operand_bytes(int M, int K);
+size_t qoq_act_operand_bytes(int M, int K, int kind);
 
 /*
  * qoq_quant_act_ex -- qoq_quant_act, and, when act_operand is not NULL, also
- * the fp8-path activation operand described above (qoq_act_operand_bytes(M,
- * K) bytes, 16-byte aligned, written completely; requires K % 128 == 0).
- * Pass it to the GEMM with qoq_gemm_options.act_operand; without it, a GEMM
- * that takes the fp8 path builds the operand itself in its workspace with
- * one extra kernel launch.  Same results in both cases.
+ * the activation operand of the given kind (qoq_act_operand_bytes(M, K,
+ * kind) bytes, 16-byte aligned, written completely; requires K % 128 == 0).
+ * Pass it to the GEMM with qoq_gemm_options.act_operand, for a GEMM whose
+ * qoq_gemm_path equals `kind`; without it, the GEMM builds the operand itself
+ * in its workspace with one extra kernel launch.  Same results in both cases.
+ * kind is ignored when act_operand is NULL; otherwise it must be 1 or 2
+ * (QOQ_ERR_INVALID_ARG).
  */
 int qoq_quant_act_ex(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x,
-                     void *act_operand, qoq_stream_t stream);
+                     int kind, void *act_operand, qoq_stream_t stream);
 
 /*
  * Workspace bytes qoq_w4a8_gemm needs for this shape on the current device:
  * a 256-byte status word area, one arrival counter per persistent CTA and
  * one int32 partial-tile slot (tokens-per-tile x 128) per persistent CTA,
- * used when a CTA's share of the work ends inside an output tile; for shapes
- * that take the fp8-operand path, followed by scratch for the activation
- * operand (qoq_act_operand_bytes).  The workspace must be zero-filled once
+ * used when a CTA's share of the work ends inside an output tile; then
+ * scratch for the activation operand of the GEMM's path
+ * (qoq_act_operand_bytes), used when the caller passes none.  The workspace
+ * must be zero-filled once
  * before first use (qoq_workspace_init); every successful call leaves the
  * status word, counters and slots zero-filled again (after a
  * QOQ_ERR_TIMEOUT, re-initialise it); the activation scratch needs no
@@ -171,7 +180,8 @@ int qoq_workspace_init(void *workspace, size_t bytes, qoq_stream_t stream);
  *   O[m,n] = fp16_rn(fp32(acc) * s_x[m] * s_w[n])   (fp32 products, left to right)
  * Qx int8 [M][K] (16-byte aligned); s_x fp16 [M]; t_x int32 [M] (group 0
  * only, may be NULL for group 128); packed from qoq_pack_weights for the same
- * N, K, group (16-byte aligned); s_w fp16 [N]; O fp16 [M][N]; workspace of
+ * N, K, group (16-byte aligned); s_w fp16 [N]; O fp16 [M][N] (16-byte aligned: the
+ * output tiles are written by tensor bulk copies); workspace of
  * ws_bytes >= qoq_gemm_workspace_bytes(M, N, K, group), 16-byte aligned.
  * Requirements: M > 0, N % 128 == 0, K % 128 == 0, group in {0, 128}.
  * Device-side failures (a bounded wait expiring, mismatched or illegal packed
@@ -209,9 +219,9 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  *                     codes and split activations as exact e4m3, group 128
  *                     only, tokens_per_tile 16 or 32).
  *   act_operand     : the activation operand written by qoq_quant_act_ex for
- *                     the same Qx (16-byte aligned), read by the fp8 path
- *                     instead of building it; ignored by the fp16 path.
- *                     NULL = build it in the workspace.
+ *                     the same Qx (16-byte aligned), of the kind equal to
+ *                     this GEMM's qoq_gemm_path; the GEMM reads it instead
+ *                     of building it.  NULL = build it in the workspace.
  */
 typedef struct {
     int tokens_per_tile;
@@ -228,10 +238,9 @@ size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gem
 
 /*
  * The tensor-core path a GEMM of this shape and options takes on the current
- * device: 1 = fp16-operand path, 2 = fp8-operand path (the one that reads
- * qoq_gemm_options.act_operand), or minus a qoq_status for invalid
- * arguments.  Lets a caller produce the activation operand only when it is
- * used.
+ * device: 1 = fp16-operand path, 2 = fp8-operand path, or minus a qoq_status
+ * for invalid arguments.  It is also the kind of activation operand the GEMM
+ * reads (qoq_quant_act_ex).
  */
 int qoq_gemm_path(int M, int N, int K, int group, const qoq_gemm_options *opt);
 

@@ -63,6 +63,9 @@ def test_gemm_validation_before_launch(lib):
     assert f(*ok[:3], B, *ok[4:]) == 3
     assert f(*ok[:10], B, *ok[11:]) == 3
     assert f(A, ctypes.c_void_p(0x10001), *ok[2:]) == 3
+    # the fp16 output is written by tensor bulk copies: 16-byte aligned
+    assert f(*ok[:9], ctypes.c_void_p(0x10008), *ok[10:]) == 3
+    assert lib.qoq_w4a8_gemm_noalloc(A, A, NUL, A, A, 16, 256, 512, 128, ctypes.c_void_p(0x10008), S) == 3
 
 
 def test_gemm_options_validation(lib):
@@ -72,6 +75,22 @@ def test_gemm_options_validation(lib):
     opt = qoq.qoq_gemm_options(0, -1, 0, 0, None)
     assert lib.qoq_w4a8_gemm_ex(A, A, A, A, A, 16, 256, 512, 128, A, A, 1 << 20,
                                 ctypes.byref(opt), S) == 2
+
+
+def test_act_operand_entry_points_validation(lib):
+    # sizes of both operand kinds; invalid shapes / kinds give 0
+    assert lib.qoq_act_operand_bytes(5, 256, 1) == 2 * 5 * 256
+    assert lib.qoq_act_operand_bytes(5, 256, 2) == 2 * 5 * 256 + 2 * 8 * 4
+    assert lib.qoq_act_operand_bytes(5, 200, 1) == 0
+    assert lib.qoq_act_operand_bytes(5, 256, 3) == 0
+    assert lib.qoq_act_operand_bytes(0, 256, 1) == 0
+    # quant_act_ex: bad kind with an operand, K not a multiple of 128, misaligned operand
+    assert lib.qoq_quant_act_ex(A, 4, 512, A, A, A, 0, A, S) == 1
+    assert lib.qoq_quant_act_ex(A, 4, 520, A, A, A, 1, A, S) == 2
+    assert lib.qoq_quant_act_ex(A, 4, 512, A, A, A, 2, B, S) == 3
+    # the path query validates like the GEMM
+    assert lib.qoq_gemm_path(16, 200, 512, 128, None) == -2
+    assert lib.qoq_gemm_path(0, 256, 512, 128, None) == -1
 
 
 def test_other_entry_points_validation(lib):

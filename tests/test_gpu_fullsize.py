@@ -49,7 +49,7 @@ def _check_point(workload, name, M, group=128, check_quantizer=False):
     sw = _t(wq["s_w"])
     # device activation quantizer (with the fp8-path activation operand, as
     # the benchmark calls it), bit-exact at full size
-    Qx_d, sx_d, tx_d, act_d = qoq.qoq_quant_act_ex(_t(X))
+    Qx_d, sx_d, tx_d, act_d = qoq.qoq_quant_act_ex(_t(X), kind=qoq.qoq_gemm_path(M, N, K, group))
     torch.cuda.synchronize()
     assert np.array_equal(Qx_d.cpu().numpy(), Qx)
     assert np.array_equal(sx_d.cpu().numpy().view(np.uint16), sx.view(np.uint16))

@@ -84,19 +84,23 @@ def _act_operand_spec(Qx):
 
 
 @pytest.mark.parametrize("M,K", [(1, 128), (3, 512), (16, 4096), (17, 1152), (300, 14336)])
-def test_quant_act_ex_act_operand_bit_exact(M, K):
+@pytest.mark.parametrize("kind", [1, 2])
+def test_quant_act_ex_act_operand_bit_exact(M, K, kind):
     X = synthetic.activations(M, K, 300 + M, 4)
     if M > 2:
         X[1] = 0
     Qx_r, sx_r, tx_r = oracle.quant_act(X)
-    nbytes = qoq.qoq_act_operand_bytes(M, K)
+    nbytes = qoq.qoq_act_operand_bytes(M, K, kind)
     Mp = (M + 3) // 4 * 4
-    assert nbytes == 2 * M * K + (K // 128) * Mp * 4
-    Qx, sx, tx, act = qoq.qoq_quant_act_ex(_t(X))
+    assert nbytes == (2 * M * K if kind == 1 else 2 * M * K + (K // 128) * Mp * 4)
+    Qx, sx, tx, act = qoq.qoq_quant_act_ex(_t(X), kind=kind)
     assert np.array_equal(_np(Qx), Qx_r)
     assert np.array_equal(_np(sx).view(np.uint16), sx_r.view(np.uint16))
     assert np.array_equal(_np(tx), tx_r)
     a = _np(act)
+    if kind == 1:  # the same integers as fp16
+        assert np.array_equal(a.view(np.float16).reshape(M, K).astype(np.float64), Qx_r.astype(np.float64))
+        return
     hi, lo, tg = _act_operand_spec(Qx_r)
     assert np.array_equal(a[: M * K].reshape(M, K), hi)
     assert np.array_equal(a[M * K: 2 * M * K].reshape(M, K), lo)
@@ -266,7 +270,7 @@ def test_fp8_path_with_quantizer_act_operand(M, N, K):
     Qx_r, sx_r, _ = oracle.quant_act(X)
     packed, sw = _device_weights(wq, 128)
     ref = _ref_acc(wq, Qx_r, None, 128)
-    Qx, sx, _, act = qoq.qoq_quant_act_ex(_t(X), with_t=False)
+    Qx, sx, _, act = qoq.qoq_quant_act_ex(_t(X), kind=2, with_t=False)
     acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
     for ctas in (0, 3):
         acc.fill_(0)
@@ -276,6 +280,32 @@ def test_fp8_path_with_quantizer_act_operand(M, N, K):
     O = qoq.qoq_w4a8_gemm_ex(Qx, sx, None, packed, sw, N, K, 128,
                              options=qoq.gemm_options(kernel=2, act_operand=act))
     O_self = qoq.qoq_w4a8_gemm_ex(Qx, sx, None, packed, sw, N, K, 128, options=qoq.gemm_options(kernel=2))
+    assert torch.equal(O, O_self)
+    O_ref = oracle.epilogue_f64(ref, sx_r, wq["s_w"])
+    assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
+
+
+@pytest.mark.parametrize("M,N,K", [(33, 256, 640), (64, 128, 1152), (129, 256, 384), (200, 128, 2304)])
+@pytest.mark.parametrize("group", [128, 0])
+def test_fp16_path_with_quantizer_act_operand(M, N, K, group):
+    """The fp16 activation operand written by qoq_quant_act_ex, handed to the
+    fp16-operand GEMM, gives the oracle's accumulators and the same output as
+    the GEMM building the operand itself (every tile size)."""
+    W = synthetic.weights(N, K, 6150 + M, 0.02, 2)
+    X = synthetic.activations(M, K, 6151 + M, 4)
+    wq = oracle.quantize_weights_group(W, 128) if group else oracle.quantize_weights_channel(W)
+    Qx_r, sx_r, tx_r = oracle.quant_act(X)
+    packed, sw = _device_weights(wq, group)
+    ref = _ref_acc(wq, Qx_r, tx_r, group)
+    Qx, sx, tx, act = qoq.qoq_quant_act_ex(_t(X), kind=1)
+    acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    for bt in (16, 32, 64, 128):
+        acc.fill_(0)
+        qoq.qoq_w4a8_gemm_ex(Qx, None, tx, packed, None, N, K, group,
+                             options=qoq.gemm_options(tokens_per_tile=bt, acc_out=acc, kernel=1, act_operand=act))
+        assert np.array_equal(_np(acc), ref)
+    O = qoq.qoq_w4a8_gemm_ex(Qx, sx, tx, packed, sw, N, K, group, options=qoq.gemm_options(kernel=1, act_operand=act))
+    O_self = qoq.qoq_w4a8_gemm_ex(Qx, sx, tx, packed, sw, N, K, group, options=qoq.gemm_options(kernel=1))
     assert torch.equal(O, O_self)
     O_ref = oracle.epilogue_f64(ref, sx_r, wq["s_w"])
     assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()

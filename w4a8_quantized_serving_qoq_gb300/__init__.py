@@ -77,8 +77,8 @@ def load():
                 "qoq_pack_weights": (I, [P, P, P, I, I, I, P, P]),
                 "qoq_unpack_weights": (I, [P, I, I, I, P, P, P, P]),
                 "qoq_quant_act": (I, [P, I, I, P, P, P, P]),
-                "qoq_act_operand_bytes": (S, [I, I]),
-                "qoq_quant_act_ex": (I, [P, I, I, P, P, P, P, P]),
+                "qoq_act_operand_bytes": (S, [I, I, I]),
+                "qoq_quant_act_ex": (I, [P, I, I, P, P, P, I, P, P]),
                 "qoq_gemm_workspace_bytes": (S, [I, I, I, I]),
                 "qoq_gemm_workspace_bytes_ex": (S, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
                 "qoq_gemm_path": (I, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
@@ -207,14 +207,15 @@ def qoq_quant_act(X, Qx=None, s_x=None, t_x=None, with_t: bool = True, stream=No
     return Qx, s_x, t_x
 
 
-def qoq_act_operand_bytes(M: int, K: int) -> int:
-    return int(load().qoq_act_operand_bytes(M, K))
+def qoq_act_operand_bytes(M: int, K: int, kind: int) -> int:
+    return int(load().qoq_act_operand_bytes(M, K, kind))
 
 
-def qoq_quant_act_ex(X, Qx=None, s_x=None, t_x=None, act=None, with_t: bool = True,
+def qoq_quant_act_ex(X, Qx=None, s_x=None, t_x=None, act=None, kind: int = 2, with_t: bool = True,
                      with_act: bool = True, stream=None):
-    """qoq_quant_act plus the fp8-path activation operand (uint8 tensor of
-    qoq_act_operand_bytes(M, K) bytes) -> (Qx, s_x, t_x, act)."""
+    """qoq_quant_act plus the activation operand of `kind` (1: fp16 copy of
+    Qx for the fp16-operand path, 2: fp8-path planes and group sums), a uint8
+    tensor of qoq_act_operand_bytes(M, K, kind) bytes -> (Qx, s_x, t_x, act)."""
     torch = _torch()
     _dev(X, torch.float16, "X")
     M, K = X.shape
@@ -225,7 +226,7 @@ def qoq_quant_act_ex(X, Qx=None, s_x=None, t_x=None, act=None, with_t: bool = Tr
     if t_x is None and with_t:
         t_x = torch.empty((M,), dtype=torch.int32, device=X.device)
     if act is None and with_act:
-        nbytes = qoq_act_operand_bytes(M, K)
+        nbytes = qoq_act_operand_bytes(M, K, kind)
         if nbytes == 0:
             raise QoqError("qoq_quant_act_ex", 2)
         act = torch.empty((nbytes,), dtype=torch.uint8, device=X.device)
@@ -234,7 +235,7 @@ def qoq_quant_act_ex(X, Qx=None, s_x=None, t_x=None, act=None, with_t: bool = Tr
     _dev(t_x, torch.int32, "t_x")
     _dev(act, torch.uint8, "act")
     _check("qoq_quant_act_ex", load().qoq_quant_act_ex(
-        _ptr(X), M, K, _ptr(Qx), _ptr(s_x), _ptr(t_x), _ptr(act), _stream(stream)))
+        _ptr(X), M, K, _ptr(Qx), _ptr(s_x), _ptr(t_x), int(kind), _ptr(act), _stream(stream)))
     return Qx, s_x, t_x, act
 
 

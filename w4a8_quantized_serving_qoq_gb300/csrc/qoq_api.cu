@@ -67,7 +67,7 @@ int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const
     if (group == 0 && !t_x) return QOQ_ERR_INVALID_ARG;
     if (!acc_out && (!O || !s_x || !s_w)) return QOQ_ERR_INVALID_ARG;
     if (!aligned(Qx, 16) || !aligned(packed, 16) || !aligned(ws, 16)) return QOQ_ERR_MISALIGNED;
-    if ((s_x && !aligned(s_x, 2)) || (s_w && !aligned(s_w, 2)) || (O && !aligned(O, 2)) ||
+    if ((s_x && !aligned(s_x, 2)) || (s_w && !aligned(s_w, 2)) || (O && !aligned(O, 16)) ||
         (t_x && !aligned(t_x, 4)) || (acc_out && !aligned(acc_out, 4)))
         return QOQ_ERR_MISALIGNED;
     qoq::GemmPlan plan;
@@ -84,7 +84,7 @@ int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const
     a.N = N;
     a.K = K;
     a.group = group;
-    a.act = plan.path == qoq::kPathF8 ? act : nullptr;
+    a.act = act;
     a.O = O;
     a.acc_out = acc_out;
     a.ws = ws;
@@ -159,24 +159,26 @@ int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, in
     if (!aligned(X, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) || (t_x && !aligned(t_x, 4)))
         return QOQ_ERR_MISALIGNED;
     return cuda_status(
-        qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, nullptr, reinterpret_cast<cudaStream_t>(stream)));
+        qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, 0, nullptr, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-size_t qoq_act_operand_bytes(int M, int K) {
-    if (M <= 0 || K <= 0 || K % 128 != 0) return 0;
-    return qoq::act_operand_bytes(M, K);
+size_t qoq_act_operand_bytes(int M, int K, int kind) {
+    if (M <= 0 || K <= 0 || K % 128 != 0 || (kind != 1 && kind != 2)) return 0;
+    return qoq::act_operand_bytes(M, K, kind);
 }
 
 int qoq_quant_act_ex(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x,
-                     void *act_operand, qoq_stream_t stream) {
+                     int kind, void *act_operand, qoq_stream_t stream) {
     if (M <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
+    if (act_operand && kind != 1 && kind != 2) return QOQ_ERR_INVALID_ARG;
     if (K % 8 != 0 || (act_operand && K % 128 != 0)) return QOQ_ERR_UNSUPPORTED;
     if (!X || !Qx || !s_x) return QOQ_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) || (t_x && !aligned(t_x, 4)) ||
         (act_operand && !aligned(act_operand, 16)))
         return QOQ_ERR_MISALIGNED;
     return cuda_status(
-        qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, act_operand, reinterpret_cast<cudaStream_t>(stream)));
+        qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, act_operand ? kind : 0, act_operand,
+                              reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gemm_options *opt) {

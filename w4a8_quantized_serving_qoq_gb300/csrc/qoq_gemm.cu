@@ -11,22 +11,27 @@
 // product runs on the fp16 tensor-core path):
 //  * swap-AB: the MMA's M = 128 weight rows, its N = BT tokens (16..128);
 //  * one warp streams each stage with TMA: one bulk copy of the packed 8 KB
-//    weight block (+ 256 B of group metadata) and one 2D tensor copy of the
-//    INT8 activation tile (128-byte swizzle, rows past M zero-filled);
-//  * 8 converter warps turn codes into fp16 operands in registers with
-//    byte-lane SIMD: one 32-bit multiply-add per 4 weights yields
+//    weight block (+ 512 B of group metadata) and two 2D tensor copies of the
+//    activation operand (Qx as exact fp16, written by the activation
+//    quantizer or by a preparation kernel) straight into the MMA's B layout
+//    (128-byte swizzle, rows past M zero-filled);
+//  * 8 converter warps turn weight codes into fp16 operands in registers
+//    with byte-lane SIMD: one 32-bit multiply-add per 4 weights yields
 //    (q4 - z) * s_g + 128 in each byte (legal because the protective range
 //    keeps every product in [-128, 127]), then byte -> fp16 by exponent
-//    splicing and one fp16x2 subtract; INT8 activations the same way;
-//  * one thread issues tcgen05.mma (kind::f16, fp32 accumulation in TMEM).
-//    Operands are integers with |product| <= 127 * 128, so an fp32 sum over
-//    1024 k (8 stages) stays below 2^24 and is exact; each 1024-k chunk is
-//    drained by the epilogue warps into an int32 running sum kept in TMEM
-//    (two chunk buffers so the MMA never waits on the drain);
+//    splicing and one fp16x2 subtract, stored to TMEM as the A operand;
+//  * two threads issue tcgen05.mma on alternate stages (kind::f16, fp32
+//    accumulation in TMEM).  Operands are integers with |product| <= 127 *
+//    128, so an fp32 sum over 1024 k (8 stages) stays below 2^24 and is exact
+//    in any order; each 1024-k chunk is drained by the epilogue warps into an
+//    int32 running sum kept in TMEM, which also hand the chunk buffer back
+//    zeroed (two chunk buffers so the MMAs never wait on the drain);
 //  * epilogue: int32 result (per-channel: minus z[n] * t_x[m]) scaled by
-//    s_x[m] * s_w[n] in fp32 and rounded to fp16; with a K split, int32
-//    partials are reduced exactly with red.add and the last CTA of a tile
-//    applies the epilogue and re-zeroes its workspace.
+//    s_x[m] * s_w[n] in fp32 and rounded to fp16, staged in shared memory 16
+//    tokens at a time and written by a tensor bulk store; with a K split, the
+//    int32 partials of 16 tokens (8 KB, contiguous in the tile's workspace
+//    slot) go out as one bulk reduce-add, and the last CTA of a tile applies
+//    the epilogue and re-zeroes the slot with bulk copies of a zero block.
 //  * every wait is bounded; on expiry the kernel records kStatusTimeout in the
 //    workspace status word, drains its own copies/MMAs and frees TMEM.
 #include <cuda.h>
@@ -54,18 +59,25 @@ struct Cfg {
     // accumulators, [kA0, kA0 + 64 * kOpStages) fp16 weight operand stages
     // (128 lanes x 64 columns = 128 rows x 128 k each).
     static constexpr int kOpStages = BT == 128 ? 2 : 4;
-    static constexpr int kRawStages = BT <= 32 ? 12 : (BT == 64 ? 8 : 6);
+    static constexpr int kRawStages = BT == 16 ? 12 : (BT == 32 ? 10 : (BT == 64 ? 7 : 4));
     static constexpr uint32_t kA0 = ((3 * BT + 63) / 64) * 64;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kBAtom = static_cast<uint32_t>(BT) * 128u;  // BT rows x 64 fp16
-    static constexpr uint32_t kOpStageBytes = 2 * kBAtom;
-    static constexpr uint32_t kQxRawBytes = static_cast<uint32_t>(BT) * 128u;
-    static constexpr uint32_t kRawSlotBytes = kQxRawBytes + kWRawBytes;
+    // Raw slot: [B operand: two 128-byte-swizzled atoms of BT rows x 64 fp16
+    // (k 0..63, k 64..127), landed by TMA from the fp16 activation operand]
+    // [packed weight block (+ group metadata)].
+    static constexpr uint32_t kBAtom = static_cast<uint32_t>(BT) * 128u;
+    static constexpr uint32_t kBBytes = 2 * kBAtom;
+    static constexpr uint32_t kRawSlotBytes = kBBytes + kWRawBytes;
     static constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 4 + 1;
+    // Epilogue staging: two 8 KB buffers (16 tokens x 128 rows, int32 partials
+    // or fp16 outputs) written by the epilogue threads and sent out by one
+    // bulk copy each, then an 8 KB block of zeros that re-zeroes partial slots.
+    static constexpr uint32_t kStgBytes = 8192;
+    static constexpr uint32_t kStgRegion = 3 * kStgBytes;
     static constexpr uint32_t kMiscBytes = 2048;  // barriers + flags, then s_x / t_x of the current tile
-    static constexpr uint32_t kSmemBytes =
-        kOpStages * kOpStageBytes + kRawStages * kRawSlotBytes + kMiscBytes + 1024;
+    static constexpr uint32_t kSmemBytes = kRawStages * kRawSlotBytes + kStgRegion + kMiscBytes + 1024;
     static_assert(kA0 + 64 * kOpStages <= kTmemCols, "TMEM columns");
+    static_assert(kRawSlotBytes % 1024 == 0 && kBAtom % 1024 == 0, "1 KB aligned swizzled atoms");
     static_assert(kNumBars * 8 + 64 <= static_cast<int>(kMiscBytes), "barrier area");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -84,16 +96,17 @@ __device__ __forceinline__ void biased_bytes_to_f16x4(uint32_t u, uint32_t &lo, 
 
 template <int BT>
 __global__ void __launch_bounds__(kThreads, 1)
-    w4a8_gemm_kernel(const __grid_constant__ CUtensorMap qx_map, const GemmParams p) {
+    w4a8_gemm_kernel(const __grid_constant__ CUtensorMap qx_map, const __grid_constant__ CUtensorMap o_map,
+                     const GemmParams p) {
     using C = Cfg<BT>;
     constexpr int R = C::kRawStages;
     constexpr int OPS = C::kOpStages;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *op_base = smem;
-    uint8_t *raw_base = smem + OPS * C::kOpStageBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(raw_base + R * C::kRawSlotBytes);
+    uint8_t *raw_base = smem;
+    uint8_t *stg_base = raw_base + R * C::kRawSlotBytes;        // 2 staging buffers, then the zero block
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stg_base + C::kStgRegion);
     uint64_t *raw_full = bars;
     uint64_t *raw_empty = bars + R;
     uint64_t *op_full = bars + 2 * R;
@@ -124,19 +137,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         *is_last = 0;
         for (int i = 0; i < R; ++i) {
             mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], kConvGroupWarps);
+            mbar_init(&raw_empty[i], kConvGroupWarps + 1);  // converter group + the MMA commit (B operand)
         }
         for (int i = 0; i < OPS; ++i) {
             mbar_init(&op_full[i], kConvGroupWarps);
             mbar_init(&op_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&chunk_full[i], 1);
-            mbar_init(&chunk_empty[i], kEpiWarps);
+            mbar_init(&chunk_full[i], 2);           // one commit per issuing thread
+            mbar_init(&chunk_empty[i], kEpiWarps);  // phase 0: zeroed at start
         }
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 2);
         fence_barrier_init();
     }
+    // The zero block is read by bulk copies (async proxy).
+    for (int i = threadIdx.x; i < static_cast<int>(C::kStgBytes / 16); i += kThreads)
+        st_shared_v4(smem_u32(stg_base + 2 * C::kStgBytes) + 16u * i, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -165,9 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
-                    mbar_arrive_expect_tx(&raw_full[slot], C::kQxRawBytes + bb);
-                    tma_load_1d(dst + C::kQxRawBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[slot]);
+                    mbar_arrive_expect_tx(&raw_full[slot], C::kBBytes + bb);
+                    tma_load_1d(dst + C::kBBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[slot]);
                     tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &raw_full[slot]);
+                    tma_load_2d(dst + C::kBAtom, &qx_map, k * kTileK + 64, tok_tile * BT, &raw_full[slot]);
                     issued = st + 1;
                 }
             }
@@ -175,54 +193,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = (issued > R ? issued - R : 0); t < issued; ++t)
                 mbar_wait(&raw_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
         }
-    } else if (run && warp == 1) {
-        // ------------------------------------------------- MMA issuer --
-        // One thread.  A shared-memory read right after a batch of MMAs waits
-        // behind them, so the readiness test of the next operand stage is
-        // issued before this stage's MMAs and consumed after them.
+    } else if (run && (warp == 1 || warp == 2)) {
+        // ------------------------------------------------ MMA issuers --
+        // Two threads take alternate stages (warp 1 even, warp 2 odd): a
+        // barrier wait issued after a thread's own MMAs queues behind them,
+        // so with one issuer every wait idled the tensor pipe.  Their MMAs
+        // into a chunk buffer have no mutual order, so none of them clears
+        // the accumulator: the epilogue hands out every chunk buffer zeroed,
+        // and each issuer commits to chunk_full at every chunk end (the
+        // barrier counts both).  The fp32 partial sums are exact integers,
+        // so the order of the MMAs does not change the result.
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(128, BT);
+            const int par = warp - 1;
             SegmentWalker walk(p, cta);
-            const int my_stages = static_cast<int>(walk.w1 - walk.w);
             Segment sg;
             int st = 0, gc = 0;
-            bool stop = false, ready = false;
+            bool stop = false;
             while (!stop && walk.next(sg)) {
                 const int len = sg.k1 - sg.k0;
                 int cur = 0;
+                bool own_in_chunk = false;
                 for (int i = 0; i < len; ++i, ++st) {
                     const bool first = (i % kChunkStages) == 0;
                     const bool last = (i % kChunkStages) == kChunkStages - 1 || i == len - 1;
                     if (first) {
                         cur = gc++;
-                        if (cur >= 2 &&
-                            !mbar_wait(&chunk_empty[cur & 1], ((cur - 2) >> 1) & 1, abort_flag, p.status, tmo)) {
+                        own_in_chunk = false;
+                    }
+                    if ((st & 1) == par) {
+                        if (!own_in_chunk) {
+                            own_in_chunk = true;
+                            if (!mbar_wait(&chunk_empty[cur & 1], (cur >> 1) & 1, abort_flag, p.status, tmo)) {
+                                stop = true;
+                                break;
+                            }
+                        }
+                        const int os = st % OPS, ouse = st / OPS;
+                        if (!mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
                             stop = true;
                             break;
                         }
-                    }
-                    const int os = st % OPS, ouse = st / OPS;
-                    if (!ready && !mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
-                        stop = true;
-                        break;
-                    }
-                    const int nx = st + 1;
-                    const bool next_ready = nx < my_stages && mbar_test(&op_full[nx % OPS], (nx / OPS) & 1);
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem + static_cast<uint32_t>((1 + (cur & 1)) * BT);
-                    const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u;
-                    const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes);
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem + static_cast<uint32_t>((1 + (cur & 1)) * BT);
+                        const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u;
+                        const uint32_t b_base = smem_u32(raw_base + (st % R) * C::kRawSlotBytes);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t bd = desc_kmajor_sw128(b_base + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
-                        mma_f16_tmem_a(d_tmem, a_tmem + 8u * kk, bd, idesc, (first && kk == 0) ? 0u : 1u);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t bd = desc_kmajor_sw128(b_base + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
+                            mma_f16_tmem_a(d_tmem, a_tmem + 8u * kk, bd, idesc, 1u);
+                        }
+                        mma_commit(&op_empty[os]);
+                        mma_commit(&raw_empty[st % R]);
                     }
-                    mma_commit(&op_empty[os]);
                     if (last) mma_commit(&chunk_full[cur & 1]);
-                    ready = next_ready;
                 }
             }
-            // All issued MMAs must finish before TMEM is released.
+            // All of this thread's MMAs must finish before TMEM is released.
             mma_commit(mma_done);
             mbar_wait(mma_done, 0, nullptr, p.status, tmo);
         }
@@ -249,9 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t raw = smem_u32(raw_base + rs * C::kRawSlotBytes);
-                const uint32_t wraw = raw + C::kQxRawBytes;
-                const uint32_t b_base = smem_u32(op_base + os * C::kOpStageBytes);
+                const uint32_t wraw = smem_u32(raw_base + rs * C::kRawSlotBytes) + C::kBBytes;
 
                 // Weights: row wr, 4 raw chunks of 32 k -> 128 fp16 -> 64 TMEM
                 // columns of this thread's lane (2 fp16 per column), in two halves.
@@ -283,26 +308,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_st32(a_lane + C::kA0 + static_cast<uint32_t>(os) * 64u + 32u * h, a_frag);
                 }
-                // Activations: BT rows x 8 raw chunks of 16 int8 -> 2 fp16 chunks each.
-                constexpr int kGroupThreads = 32 * kConvGroupWarps;
-#pragma unroll
-                for (int it0 = 0; it0 < BT * 8; it0 += kGroupThreads) {
-                    const int it = it0 + wr;
-                    if (BT * 8 % kGroupThreads == 0 || it < BT * 8) {
-                        const int r = it % BT, c = it / BT;
-                        const uint4 v = ld_shared_v4(raw + sw128_offset(r, c));
-                        const uint32_t x4[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
-                                                v.w ^ 0x80808080u};
-                        uint32_t f[8];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) biased_bytes_to_f16x4(x4[j], f[2 * j], f[2 * j + 1]);
-                        const uint32_t b_atom = b_base + (c >> 2) * C::kBAtom;
-                        const int cc = 2 * (c & 3);
-                        st_shared_v4(b_atom + sw128_offset(r, cc), f[0], f[1], f[2], f[3]);
-                        st_shared_v4(b_atom + sw128_offset(r, cc + 1), f[4], f[5], f[6], f[7]);
-                    }
-                }
-                fence_proxy_async_smem();
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -319,6 +324,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         SegmentWalker walk(p, cta);
         Segment sg;
         int gc = 0;
+        int stg_use = 0;  // staging buffers used so far (buffer stg_use & 1 is next)
+        {
+            // Both chunk buffers start zeroed (the MMAs only accumulate).
+            uint32_t zero16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) zero16[i] = 0u;
+            for (int j = 0; j < 2 * BT / 16; ++j) tmem_st16(tl + static_cast<uint32_t>(BT + 16 * j), zero16);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&chunk_empty[0]);
+                mbar_arrive(&chunk_empty[1]);
+            }
+        }
         // All four epilogue warps take every named barrier below the same number
         // of times: they walk the same segments and leave the walk together,
         // on a decision read from the shared abort flag after a barrier (any
@@ -345,9 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < nch; ++c) {
                 const int cur = gc++;
                 const int cb = cur & 1;
-                // warp-uniform outcome: the TMEM loads below are warp-collective
+                // warp-uniform outcome (the TMEM loads below are warp-collective).
+                // A failed wait does not leave the loop: every epilogue warp
+                // must take the same named barriers; the abort flag, read by
+                // the issuing thread after each barrier, stops all output.
                 ok = mbar_wait_warp(&chunk_full[cb], (cur >> 1) & 1, abort_flag, p.status, tmo);
-                if (!ok) break;
                 tc_fence_after();
                 const bool last = c == nch - 1;
 #pragma unroll 1
@@ -359,6 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_wait_ld_regs(r);
                     }
                     tmem_wait_ld_regs(f);
+                    {
+                        // hand the chunk buffer back zeroed
+                        uint32_t zero16[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) zero16[i] = 0u;
+                        tmem_st16(tl + static_cast<uint32_t>((1 + cb) * BT + 16 * j), zero16);
+                    }
                     uint32_t v[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -366,19 +395,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      (c > 0 ? static_cast<int>(r[i]) : 0));
                     if (!last) {
                         tmem_st16(tl + static_cast<uint32_t>(16 * j), v);
-                    } else {
+                    } else if (!split && p.acc_out) {
+                        // int32 test output: one store per element
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int ml = 16 * j + i, m = m0 + ml;
-                            if (m >= p.M) break;
-                            if (split)
-                                atomicAdd(slot + ml * kTileN + et, static_cast<int>(v[i]));
-                            else
-                                write_out(p, m, n, static_cast<int>(v[i]), zc, tile_tx[ml], tile_sx[ml], sw);
+                        for (int i = 0; i < 16; ++i)
+                            if (ok && m0 + 16 * j + i < p.M)
+                                write_out(p, m0 + 16 * j + i, n, static_cast<int>(v[i]), zc, tile_tx[16 * j + i],
+                                          tile_sx[16 * j + i], sw);
+                    } else {
+                        // Stage the block of 16 tokens x 128 rows, then one bulk
+                        // copy: int32 partials reduced into the tile's slot (rows
+                        // 16j.. of a slot are contiguous), or fp16 outputs stored
+                        // to O (rows past M are clipped by the copy).
+                        if (et == 0) bulk_wait_read<1>();  // the buffer's previous copy has read it
+                        named_bar_sync(3, kEpiThreads);
+                        const uint32_t buf = smem_u32(stg_base) + (stg_use & 1) * C::kStgBytes;
+                        if (split) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) st_shared_b32(buf + 4u * (i * kTileN + et), v[i]);
+                        } else {
+                            uint32_t sxv[16], txv[16];
+                            ld_shared_x16(smem_u32(tile_sx + 16 * j), sxv);
+                            ld_shared_x16(smem_u32(tile_tx + 16 * j), txv);
+                            uint16_t o[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                o[i] = out_fp16(static_cast<int>(v[i]), zc, static_cast<int>(txv[i]),
+                                                __uint_as_float(sxv[i]), sw);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) st_shared_u16(buf + 2u * (i * kTileN + et), o[i]);
                         }
+                        fence_proxy_async_smem();
+                        named_bar_sync(3, kEpiThreads);
+                        if (et == 0 && *abort_flag == 0) {
+                            const uint8_t *src = stg_base + (stg_use & 1) * C::kStgBytes;
+                            if (split)
+                                bulk_reduce_add_s32(slot + 16 * j * kTileN, src, C::kStgBytes);
+                            else
+                                tma_store_2d(&o_map, src, n_tile * kTileN, m0 + 16 * j);
+                            bulk_commit();
+                        }
+                        ++stg_use;
                     }
                 }
-                if (!last) tmem_wait_st();
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&chunk_empty[cb]);
@@ -387,13 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Every epilogue thread reaches both named barriers once per
                 // split segment.  A failed wait anywhere has raised abort_flag
                 // before the first barrier, so the decision below is uniform.
-                // One thread publishes the tile's partial sums (the barrier
-                // orders the other threads' red.adds before its fence) and
-                // learns whether this CTA is the tile's last contributor.
+                // One thread issued this tile's partial reductions; it waits for
+                // them to complete, publishes them with a fence and the arrival
+                // counter, and learns whether this CTA is the last contributor.
                 named_bar_sync(1, kEpiThreads);
                 if (et == 0) {
                     int last_cta = 0;
                     if (*abort_flag == 0) {
+                        bulk_wait<0>();
                         __threadfence();
                         const uint32_t tlast = tfirst + static_cast<uint32_t>(p.G) - 1u;
                         const unsigned expected =
@@ -407,28 +468,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(1, kEpiThreads);
                 if (*is_last) {
                     const int mend = min(p.M - m0, BT);
-                    // Every contributor's red.add landed in L2 before its
+                    // Every contributor's reduction landed in L2 before its
                     // counter increment; read the sums from L2 (16 loads in
-                    // flight), then re-zero the slot for the next call.
+                    // flight), write the outputs through the staging buffers,
+                    // then re-zero the slot for the next call.
                     for (int ml0 = 0; ml0 < mend; ml0 += 16) {
                         int acc[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             acc[i] = (ml0 + i < mend) ? ld_cg_s32(slot + (ml0 + i) * kTileN + et) : 0;
+                        if (p.acc_out) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (ml0 + i < mend) {
-                                slot[(ml0 + i) * kTileN + et] = 0;
-                                write_out(p, m0 + ml0 + i, n, acc[i], zc, tile_tx[ml0 + i], tile_sx[ml0 + i], sw);
-                            }
+                            for (int i = 0; i < 16; ++i)
+                                if (ml0 + i < mend)
+                                    write_out(p, m0 + ml0 + i, n, acc[i], zc, tile_tx[ml0 + i], tile_sx[ml0 + i], sw);
+                            continue;
                         }
+                        if (et == 0) bulk_wait_read<1>();
+                        named_bar_sync(3, kEpiThreads);
+                        const uint32_t buf = smem_u32(stg_base) + (stg_use & 1) * C::kStgBytes;
+                        uint32_t sxv[16], txv[16];
+                        ld_shared_x16(smem_u32(tile_sx + ml0), sxv);
+                        ld_shared_x16(smem_u32(tile_tx + ml0), txv);
+                        uint16_t o[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            o[i] = out_fp16(acc[i], zc, static_cast<int>(txv[i]), __uint_as_float(sxv[i]), sw);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) st_shared_u16(buf + 2u * (i * kTileN + et), o[i]);
+                        fence_proxy_async_smem();
+                        named_bar_sync(3, kEpiThreads);
+                        if (et == 0 && *abort_flag == 0) {
+                            tma_store_2d(&o_map, stg_base + (stg_use & 1) * C::kStgBytes, n_tile * kTileN, m0 + ml0);
+                            bulk_commit();
+                        }
+                        ++stg_use;
                     }
-                    if (et == 0) p.counters[slot_idx] = 0u;
+                    // All slot reads above have completed (their values were
+                    // used before this barrier); zero the whole slot.
+                    named_bar_sync(3, kEpiThreads);
+                    if (et == 0) {
+                        for (int j = 0; j < BT / 16; ++j)
+                            bulk_store(slot + 16 * j * kTileN, stg_base + 2 * C::kStgBytes, C::kStgBytes);
+                        bulk_commit();
+                        p.counters[slot_idx] = 0u;
+                    }
                 }
             }
             named_bar_sync(1, kEpiThreads);  // also: is_last is rewritten by the next split segment
             if (*abort_flag != 0) break;
         }
+        // Bulk copies read shared memory until they complete: wait before exit.
+        if (et == 0) bulk_wait<0>();
         (void)ok;
     }
 
@@ -459,15 +550,37 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     }
     CUtensorMapEncodeTiledFn enc = get_encode_fn();
     if (!enc) return cudaErrorNotSupported;
+    uint8_t *ws0 = static_cast<uint8_t *>(a.ws);
+    const void *act = a.act;
+    if (!act) {
+        // No precomputed operand: build the fp16 copy of Qx in the workspace first.
+        void *scratch = ws0 + plan.act_offset;
+        e = launch_act_operand(a.Qx, a.M, a.K, kPathF16, scratch, stream);
+        if (e != cudaSuccess) return e;
+        act = scratch;
+    }
+    // fp16 activation operand [M][K]: one box = 64 k (128 bytes) x BT tokens.
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K)};
-    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(BT)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K) * 2u};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(BT)};
     const cuuint32_t estr[2] = {1u, 1u};
-    CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(a.Qx), dims, strides,
-                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(act), dims, strides, box,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // fp16 output O [M][N]: one store box = 128 rows of a tile x 16 tokens.
+    // (Unused in the int32 test mode.)
+    CUtensorMap o_map{};
+    if (a.O) {
+        const cuuint64_t odims[2] = {static_cast<cuuint64_t>(a.N), static_cast<cuuint64_t>(a.M)};
+        const cuuint64_t ostrides[1] = {static_cast<cuuint64_t>(a.N) * 2u};
+        const cuuint32_t obox[2] = {static_cast<cuuint32_t>(kTileN), 16u};
+        cr = enc(&o_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.O, odims, ostrides, obox, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
 
     GemmParams p;
     uint8_t *ws = static_cast<uint8_t *>(a.ws);
@@ -491,7 +604,7 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
     dim3 grid(plan.ctas);
-    w4a8_gemm_kernel<BT><<<grid, kThreads, C::kSmemBytes, stream>>>(map, p);
+    w4a8_gemm_kernel<BT><<<grid, kThreads, C::kSmemBytes, stream>>>(map, o_map, p);
     return cudaGetLastError();
 }
 
@@ -524,12 +637,8 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
     pl.counters_offset = kWsStatusBytes;
     pl.slots_offset = kWsStatusBytes + (static_cast<size_t>(pl.ctas) * 4 + 255) / 256 * 256;
     pl.zero_bytes = pl.slots_offset + static_cast<size_t>(pl.ctas) * bt * kTileN * 4;
-    pl.act_offset = 0;
-    pl.ws_bytes = pl.zero_bytes;
-    if (path == kPathF8) {
-        pl.act_offset = (pl.zero_bytes + 255) / 256 * 256;
-        pl.ws_bytes = pl.act_offset + act_operand_bytes(M, K);
-    }
+    pl.act_offset = (pl.zero_bytes + 255) / 256 * 256;
+    pl.ws_bytes = pl.act_offset + act_operand_bytes(M, K, path);
     return pl;
 }
 

@@ -97,6 +97,42 @@ __device__ __forceinline__ void write_out(const GemmParams &p, int m, int n, int
         p.O[idx] = __half_as_ushort(__float2half_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc), sx), sw)));
 }
 
+// Staging stores: no memory clobber, so a run of them pipelines; the
+// proxy fence and barrier that follow them are volatile asm too and stay after.
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v));
+}
+
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v));
+}
+
+// Sixteen consecutive 32-bit shared-memory words (16-byte aligned) into registers.
+__device__ __forceinline__ void ld_shared_x16(uint32_t addr, uint32_t (&r)[16]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r[4 * q]), "=r"(r[4 * q + 1]), "=r"(r[4 * q + 2]), "=r"(r[4 * q + 3])
+                     : "r"(addr + 16u * q));
+}
+
+// fp16 output of one accumulator (per-channel zero fold, then the two scales).
+__device__ __forceinline__ uint16_t out_fp16(int acc, int zc, int tx, float sx, float sw) {
+    return __half_as_ushort(__float2half_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc - zc * tx), sx), sw)));
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ int ld_shared_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ int ld_cg_s32(const int32_t *p) {
     int v;
     asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

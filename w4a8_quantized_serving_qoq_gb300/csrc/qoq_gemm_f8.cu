@@ -64,15 +64,20 @@ struct F8Cfg {
     static constexpr uint32_t kRawSlotBytes = (kWOff + kGroupsPerStage * kBlockBytesG + 1023u) / 1024u * 1024u;
     static constexpr uint32_t kAuxMetaBytes = kGroupsPerStage * 128u * 4u;
     static constexpr uint32_t kAuxStageBytes = kAuxMetaBytes + kTgBytes;
-    // TMEM: D buffers [2 stage sets][2 groups] x kNmma columns, then A slots of
-    // 64 columns (128 rows x 256 k bytes).
-    static constexpr uint32_t kA0 = 4u * kNmma;
+    // TMEM: D buffers [kDSets stage sets][2 groups] x kNmma columns, then A
+    // slots of 64 columns (128 rows x 256 k bytes).  With as many D sets as
+    // metadata slots (BT = 16), the converter's wait for the drain of stage
+    // s - 4 already frees the D set of stage s, so the MMA issuers wait on
+    // op_full alone; BT = 32 has room for two sets and waits on d_empty too.
+    static constexpr int kDSets = BT == 16 ? 4 : 2;
+    static constexpr uint32_t kA0 = static_cast<uint32_t>(kDSets) * 2u * kNmma;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kNumBars = 2 * kRawStages + kOpStages + 2 * kAuxStages + 4 + 1;
+    static constexpr int kNumBars = 2 * kRawStages + kOpStages + 2 * kAuxStages + 2 * kDSets + 1;
     static constexpr uint32_t kMiscBytes = 2048;
     static constexpr uint32_t kSmemBytes =
         kRawStages * kRawSlotBytes + kAuxStages * kAuxStageBytes + kMiscBytes + 1024;
     static_assert(kA0 + 64u * kOpStages <= kTmemCols, "TMEM columns");
+    static_assert(kDSets == 2 || kDSets == kAuxStages, "D sets: double buffered, or one per metadata slot");
     static_assert(kNumBars * 8 + 64 <= 1024, "barrier area");
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(kPlaneGroupBytes % 1024 == 0 && kRawSlotBytes % 1024 == 0, "1 KB aligned swizzled tiles");
@@ -127,7 +132,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     w4a8_gemm_f8_kernel(const __grid_constant__ CUtensorMap plane_map, const __grid_constant__ CUtensorMap tg_map,
                         const GemmParams p) {
     using C = F8Cfg<BT>;
-    constexpr int R = C::kRawStages, OPS = C::kOpStages, AUX = C::kAuxStages;
+    constexpr int R = C::kRawStages, OPS = C::kOpStages, AUX = C::kAuxStages, DS = C::kDSets;
     constexpr int HT = BT / 2;  // tokens per drain thread
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
@@ -141,8 +146,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     uint64_t *aux_full = op_full + OPS;
     uint64_t *aux_empty = aux_full + AUX;
     uint64_t *d_full = aux_empty + AUX;
-    uint64_t *d_empty = d_full + 2;
-    uint64_t *mma_done = d_empty + 2;
+    uint64_t *d_empty = d_full + DS;
+    uint64_t *mma_done = d_empty + DS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *hdr_ok = abort_flag + 1;
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             mbar_init(&aux_full[i], kF8ConvWarps);
             mbar_init(&aux_empty[i], kF8EpiWarps);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < DS; ++i) {
             mbar_init(&d_full[i], 1);
             mbar_init(&d_empty[i], kF8EpiWarps);
         }
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     } else if (run && (warp == 1 || warp == 2)) {
         // ------------------------------------------------ MMA issuers --
         // Two issuing threads take alternate stages (warp 1 even, warp 2
-        // odd; stage parity is also the D set).  A barrier wait issued after
+        // odd).  A barrier wait issued after
         // a thread's own MMAs queues behind them, so with one issuer every
         // wait left the tensor pipe idle; with two, one thread waits while
         // the other's MMAs execute.  tcgen05.commit tracks the MMAs of the
@@ -243,8 +248,9 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     if ((st & 1) != par) continue;
                     const int ng = min(kGroupsPerStage, sg.k1 - k);
                     const int rs = st % R, os = st % OPS, ouse = st / OPS;
-                    const int ds = st & 1, duse = st >> 1;
-                    if ((duse > 0 && !mbar_wait(&d_empty[ds], (duse - 1) & 1, abort_flag, p.status, tmo)) ||
+                    const int ds = st % DS, duse = st / DS;
+                    if ((DS < AUX && duse > 0 &&
+                         !mbar_wait(&d_empty[ds], (duse - 1) & 1, abort_flag, p.status, tmo)) ||
                         !mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
                         stop = true;
                         break;
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             bool ok = true;
             for (int k = sg.k0; k < sg.k1 && ok; k += kGroupsPerStage, ++st) {
                 const int ng = min(kGroupsPerStage, sg.k1 - k);
-                const int ds = st & 1, duse = st >> 1, as = st % AUX, ause = st / AUX;
+                const int ds = st % DS, duse = st / DS, as = st % AUX, ause = st / AUX;
                 ok = mbar_wait_warp(&aux_full[as], ause & 1, abort_flag, p.status, tmo) &&
                      mbar_wait_warp(&d_full[ds], duse & 1, abort_flag, p.status, tmo);
                 if (!ok) break;
@@ -479,7 +485,7 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
     if (!act) {
         // No precomputed operand: build it from Qx in the workspace first.
         uint8_t *scratch = ws + plan.act_offset;
-        e = launch_act_operand(a.Qx, a.M, a.K, scratch, stream);
+        e = launch_act_operand(a.Qx, a.M, a.K, kPathF8, scratch, stream);
         if (e != cudaSuccess) return e;
         act = scratch;
     }

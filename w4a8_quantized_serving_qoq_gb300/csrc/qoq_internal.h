@@ -55,18 +55,24 @@ __host__ __device__ inline size_t packed_z_offset(int N, int K) {
 }
 
 // Workspace layout: [status word + pad: 256 B][ctas arrival counters][ctas x BT x 128
-// int32 partial-tile slots][fp8 path only: activation operand scratch].
+// int32 partial-tile slots][activation operand scratch].
 constexpr size_t kWsStatusBytes = 256;
 
-// Activation operand of the fp8 path (written by quant_act_ex or by the
-// GEMM's own preparation kernel, read by TMA):
-//   [u_hi plane: M x K bytes][u_lo plane: M x K bytes][t_g: (K/128) x Mp int32]
-// u = Qx + 128 = 16 * u_hi + u_lo; each plane byte is its own e4m3 encoding
-// of value * 2^-9.  t_g[g][m] = sum of Qx[m, k] over the 128 k of group g.
-// Mp = M rounded up to 4 keeps every t_g row 16-byte aligned for TMA.
+// Activation operands: the INT8 activation in the order and encoding a GEMM
+// path's tensor cores consume, written by quant_act_ex (or by a preparation
+// kernel the GEMM launches itself) and landed in shared memory by TMA.
+//  kind 1 (fp16-operand path): Qx as fp16, [M][K] (every int8 value is an
+//    exact fp16 number).
+//  kind 2 (fp8-operand path):
+//    [u_hi plane: M x K bytes][u_lo plane: M x K bytes][t_g: (K/128) x Mp int32]
+//    u = Qx + 128 = 16 * u_hi + u_lo; each plane byte is its own e4m3 encoding
+//    of value * 2^-9.  t_g[g][m] = sum of Qx[m, k] over the 128 k of group g.
+//    Mp = M rounded up to 4 keeps every t_g row 16-byte aligned for TMA.
+// The kind equals the GemmPath value of the path that reads it.
 __host__ __device__ inline int act_tg_pitch(int M) { return (M + 3) & ~3; }
 __host__ __device__ inline size_t act_planes_bytes(int M, int K) { return 2 * static_cast<size_t>(M) * K; }
-__host__ __device__ inline size_t act_operand_bytes(int M, int K) {
+__host__ __device__ inline size_t act_operand_bytes(int M, int K, int kind) {
+    if (kind == 1) return 2 * static_cast<size_t>(M) * K;
     return act_planes_bytes(M, K) + static_cast<size_t>(K / kTileK) * act_tg_pitch(M) * 4;
 }
 
@@ -87,7 +93,7 @@ struct GemmPlan {
     size_t ws_bytes;       // workspace needed
     size_t counters_offset;
     size_t slots_offset;
-    size_t act_offset;     // fp8 path: activation operand scratch (0 if none)
+    size_t act_offset;     // activation operand scratch (used when the caller passes none)
     size_t zero_bytes;     // leading workspace bytes that must be zero before a launch
 };
 
@@ -98,9 +104,10 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path =
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
-                             int32_t *t_x, void *act_operand, cudaStream_t stream);
-// fp8-path activation operand from already quantized activations.
-cudaError_t launch_act_operand(const int8_t *Qx, int M, int K, void *act_operand, cudaStream_t stream);
+                             int32_t *t_x, int act_kind, void *act_operand, cudaStream_t stream);
+// Activation operand of the given kind from already quantized activations.
+cudaError_t launch_act_operand(const int8_t *Qx, int M, int K, int act_kind, void *act_operand,
+                               cudaStream_t stream);
 cudaError_t launch_quantize_weights(const uint16_t *W, int N, int K, int group, uint8_t *q4,
                                     uint8_t *s_g, uint8_t *z, uint16_t *s_w, cudaStream_t stream);
 cudaError_t launch_pack(const uint8_t *q4, const uint8_t *s_g, const uint8_t *z, int N, int K,
@@ -115,7 +122,7 @@ struct GemmArgs {
     const void *packed;
     const uint16_t *s_w;
     int M, N, K, group;
-    const void *act;      // fp8 path: activation operand (act_operand_bytes layout)
+    const void *act;      // activation operand of the plan's kind, or null (built in the workspace)
     uint16_t *O;          // fp16 output, or null when acc_out is set
     int32_t *acc_out;     // int32 pre-scale accumulators (test/debug mode)
     void *ws;

@@ -61,7 +61,7 @@ extern "C" int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, cons
     if (N % 128 != 0 || K % 128 != 0 || N / 128 > 65535) return QOQ_ERR_UNSUPPORTED;
     if (!Qx || !s_x || !packed || !s_w || !O || (group == 0 && !t_x)) return QOQ_ERR_INVALID_ARG;
     if (!is_aligned(Qx, 16) || !is_aligned(packed, 16) || !is_aligned(s_x, 2) || !is_aligned(s_w, 2) ||
-        !is_aligned(O, 2) || (t_x && !is_aligned(t_x, 4)))
+        !is_aligned(O, 16) || (t_x && !is_aligned(t_x, 4)))
         return QOQ_ERR_MISALIGNED;
     void *scratch = nullptr;
     int sms = 0;
@@ -72,8 +72,8 @@ extern "C" int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, cons
     if (plan.ws_bytes > kNoAllocScratchBytes) return QOQ_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // The array keeps whatever the previous call left; the GEMM needs its
-    // status word, counters and partial slots to start at zero (the fp8
-    // path's activation scratch after them is fully overwritten each call).
+    // status word, counters and partial slots to start at zero (the
+    // activation-operand scratch after them is fully overwritten each call).
     if (cudaMemsetAsync(scratch, 0, plan.zero_bytes, s) != cudaSuccess) return QOQ_ERR_CUDA;
     qoq::GemmArgs a;
     a.Qx = Qx;

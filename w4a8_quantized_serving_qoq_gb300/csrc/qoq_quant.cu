@@ -73,7 +73,7 @@ __device__ __forceinline__ float amax8(const uint4 v, float amax) {
     return amax;
 }
 
-// Activation-operand bytes of eight INT8 codes (two words): u = Qx + 128
+// fp8-path operand bytes of eight INT8 codes (two words): u = Qx + 128
 // (flip of the sign bit), then its high and low nibble planes.
 __device__ __forceinline__ void split_u(uint2 q, uint2 &hi, uint2 &lo) {
     const uint32_t u0 = q.x ^ 0x80808080u, u1 = q.y ^ 0x80808080u;
@@ -81,15 +81,26 @@ __device__ __forceinline__ void split_u(uint2 q, uint2 &hi, uint2 &lo) {
     lo = make_uint2(u0 & 0x0F0F0F0Fu, u1 & 0x0F0F0F0Fu);
 }
 
+// fp16-path operand of four INT8 codes (one word): the same integers as
+// fp16 (exact), two fp16x2 words.
+__device__ __forceinline__ uint2 int8x4_to_f16x4(uint32_t w) {
+    uint32_t h[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+        h[b] = __half_as_ushort(__int2half_rn(static_cast<int>(static_cast<int8_t>((w >> (8 * b)) & 0xffu))));
+    return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
 constexpr int kActCache = 4;  // 16-byte items per thread kept in registers between the passes
 
 // One CTA per token row.  s_x = fp16(max|x| / 127); Qx = clamp(rne(x / s_x), -127, 127);
-// an all-zero scale gives an all-zero row; t_x = row sum of Qx.  With
-// kAct, also the fp8-path activation operand (planes of u = Qx + 128 and the
-// per-group sums t_g).  The trip count of every loop is uniform across the
-// CTA (blockDim.x is a multiple of 32), so the half-warp shuffles that sum
-// one 128-k group (16 items of 8) always run with every lane present.
-template <bool kAct>
+// an all-zero scale gives an all-zero row; t_x = row sum of Qx.  kAct
+// selects an activation operand written alongside: 0 none, 1 the fp16 copy
+// of Qx, 2 the fp8-path planes of u = Qx + 128 and the per-group sums t_g.
+// The trip count of every loop is uniform across the CTA (blockDim.x is a
+// multiple of 32), so the half-warp shuffles that sum one 128-k group (16
+// items of 8) always run with every lane present.
+template <int kAct>
 __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, int8_t *__restrict__ Qx,
                                  uint16_t *__restrict__ s_x, int32_t *__restrict__ t_x,
                                  uint8_t *__restrict__ act) {
@@ -114,9 +125,11 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
 
     uint2 *qrow = reinterpret_cast<uint2 *>(Qx + m * K);
     uint2 *hrow = nullptr, *lrow = nullptr;
+    uint4 *frow = nullptr;
     int32_t *tg = nullptr;
     const int pitch = act_tg_pitch(M);
-    if (kAct) {
+    if (kAct == 1) frow = reinterpret_cast<uint4 *>(act + 2 * m * K);
+    if (kAct == 2) {
         hrow = reinterpret_cast<uint2 *>(act + m * K);
         lrow = reinterpret_cast<uint2 *>(act + static_cast<size_t>(M) * K + m * K);
         tg = reinterpret_cast<int32_t *>(act + act_planes_bytes(M, K));
@@ -130,7 +143,11 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
             qrow[i] = q;
         }
         tsum += part;
-        if (kAct) {
+        if (kAct == 1 && i < nv) {
+            const uint2 a = int8x4_to_f16x4(q.x), b = int8x4_to_f16x4(q.y);
+            frow[i] = make_uint4(a.x, a.y, b.x, b.y);
+        }
+        if (kAct == 2) {
             if (i < nv) {
                 uint2 hi, lo;
                 split_u(q, hi, lo);
@@ -153,6 +170,19 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
     if (tid == 0) {
         s_x[m] = sbits;
         if (t_x) t_x[m] = tsum;
+    }
+}
+
+// fp16-path activation operand from INT8 activations: 8 codes per thread
+// and step, grid-stride over the whole matrix.
+__global__ void act_operand_f16_kernel(const int8_t *__restrict__ Qx, size_t n8, uint8_t *__restrict__ act) {
+    const uint2 *src = reinterpret_cast<const uint2 *>(Qx);
+    uint4 *dst = reinterpret_cast<uint4 *>(act);
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        const uint2 q = __ldg(src + i);
+        const uint2 a = int8x4_to_f16x4(q.x), b = int8x4_to_f16x4(q.y);
+        dst[i] = make_uint4(a.x, a.y, b.x, b.y);
     }
 }
 
@@ -262,18 +292,30 @@ __global__ void quantize_channel_kernel(const uint16_t *__restrict__ W, int K,
 }  // namespace
 
 cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
-                             int32_t *t_x, void *act_operand, cudaStream_t stream) {
+                             int32_t *t_x, int act_kind, void *act_operand, cudaStream_t stream) {
     // Few long rows: one wide CTA per row keeps the per-row latency short.
     const int threads = (M < 296) ? 1024 : 256;
-    if (act_operand)
-        quant_act_kernel<true><<<M, threads, 0, stream>>>(X, M, K, Qx, s_x, t_x, static_cast<uint8_t *>(act_operand));
+    uint8_t *act = static_cast<uint8_t *>(act_operand);
+    if (!act) act_kind = 0;
+    if (act_kind == 1)
+        quant_act_kernel<1><<<M, threads, 0, stream>>>(X, M, K, Qx, s_x, t_x, act);
+    else if (act_kind == 2)
+        quant_act_kernel<2><<<M, threads, 0, stream>>>(X, M, K, Qx, s_x, t_x, act);
     else
-        quant_act_kernel<false><<<M, threads, 0, stream>>>(X, M, K, Qx, s_x, t_x, nullptr);
+        quant_act_kernel<0><<<M, threads, 0, stream>>>(X, M, K, Qx, s_x, t_x, nullptr);
     return cudaGetLastError();
 }
 
-cudaError_t launch_act_operand(const int8_t *Qx, int M, int K, void *act_operand, cudaStream_t stream) {
-    act_operand_kernel<<<M, 256, 0, stream>>>(Qx, M, K, static_cast<uint8_t *>(act_operand));
+cudaError_t launch_act_operand(const int8_t *Qx, int M, int K, int act_kind, void *act_operand,
+                               cudaStream_t stream) {
+    uint8_t *act = static_cast<uint8_t *>(act_operand);
+    if (act_kind == 1) {
+        const size_t n8 = static_cast<size_t>(M) * K / 8;
+        const size_t blocks = (n8 + 255) / 256;
+        act_operand_f16_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(Qx, n8, act);
+    } else {
+        act_operand_kernel<<<M, 256, 0, stream>>>(Qx, M, K, act);
+    }
     return cudaGetLastError();
 }
 
