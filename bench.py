@@ -247,12 +247,13 @@ def main():
             kind = qoq.qoq_gemm_path(M, layer.N, layer.K, 128)
             act = torch.empty((qoq.qoq_act_operand_bytes(M, layer.K, kind),), dtype=torch.uint8, device=dev)
             points.append(dict(layer=layer, M=M, X=X, Qx=Qx, sx=sx, O=O, act=act, kind=kind,
-                               opt=qoq.gemm_options(act_operand=act)))
+                               opt=qoq.gemm_options(act_operand=act, flags=qoq.QOQ_LAUNCH_OVERLAP)))
     ws = qoq.new_workspace(ws_max, dev)
     torch.cuda.synchronize()
 
     def quant_point(pt):
-        qoq.qoq_quant_act_ex(pt["X"], pt["Qx"], pt["sx"], None, pt["act"], kind=pt["kind"], with_t=False)
+        qoq.qoq_quant_act_ex(pt["X"], pt["Qx"], pt["sx"], None, pt["act"], kind=pt["kind"], with_t=False,
+                             flags=qoq.QOQ_LAUNCH_OVERLAP)
 
     def gemm_point(pt, copy_idx):
         layer = pt["layer"]

@@ -123,6 +123,20 @@ int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, in
                   qoq_stream_t stream);
 
 /*
+ * Launch flag (qoq_quant_act_ex flags, qoq_gemm_options.flags):
+ * QOQ_LAUNCH_OVERLAP launches the kernel as a programmatic dependent of the
+ * kernel that precedes it in the stream (CUDA programmatic dependent
+ * launch), so its launch and setup overlap that kernel's end.  The kernel
+ * waits for the preceding kernel to complete before it reads its
+ * activations, scales, workspace or output, and before it writes anything.
+ * The GEMM also reads its packed weights and weight scales before that wait,
+ * so with this flag they must not be written by a kernel that may still be
+ * running (weights are static in serving).  Also valid inside CUDA graph
+ * capture.
+ */
+#define QOQ_LAUNCH_OVERLAP 1u
+
+/*
  * Bytes of an activation operand (0 for an invalid shape or kind; requires
  * K % 128 == 0).  An activation operand is the INT8 activation of
  * qoq_quant_act in the order and encoding one GEMM path's tensor cores
@@ -148,10 +162,11 @@ size_t qoq_act_operand_bytes(int M, int K, int kind);
  * qoq_gemm_path equals `kind`; without it, the GEMM builds the operand itself
  * in its workspace with one extra kernel launch.  Same results in both cases.
  * kind is ignored when act_operand is NULL; otherwise it must be 1 or 2
- * (QOQ_ERR_INVALID_ARG).
+ * (QOQ_ERR_INVALID_ARG).  flags: 0 or QOQ_LAUNCH_OVERLAP (other bits:
+ * QOQ_ERR_UNSUPPORTED).
  */
 int qoq_quant_act_ex(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x,
-                     int kind, void *act_operand, qoq_stream_t stream);
+                     int kind, void *act_operand, uint32_t flags, qoq_stream_t stream);
 
 /*
  * Workspace bytes qoq_w4a8_gemm needs for this shape on the current device:
@@ -222,6 +237,8 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  *                     the same Qx (16-byte aligned), of the kind equal to
  *                     this GEMM's qoq_gemm_path; the GEMM reads it instead
  *                     of building it.  NULL = build it in the workspace.
+ *   flags           : 0 or QOQ_LAUNCH_OVERLAP (see above; other bits:
+ *                     QOQ_ERR_UNSUPPORTED).
  */
 typedef struct {
     int tokens_per_tile;
@@ -231,6 +248,7 @@ typedef struct {
     int32_t *acc_out;
     int kernel;
     const void *act_operand;
+    uint32_t flags;
 } qoq_gemm_options;
 
 /* Workspace bytes for a GEMM run with the given options. */

@@ -85,9 +85,14 @@ def test_act_operand_entry_points_validation(lib):
     assert lib.qoq_act_operand_bytes(5, 256, 3) == 0
     assert lib.qoq_act_operand_bytes(0, 256, 1) == 0
     # quant_act_ex: bad kind with an operand, K not a multiple of 128, misaligned operand
-    assert lib.qoq_quant_act_ex(A, 4, 512, A, A, A, 0, A, S) == 1
-    assert lib.qoq_quant_act_ex(A, 4, 520, A, A, A, 1, A, S) == 2
-    assert lib.qoq_quant_act_ex(A, 4, 512, A, A, A, 2, B, S) == 3
+    assert lib.qoq_quant_act_ex(A, 4, 512, A, A, A, 0, A, 0, S) == 1
+    assert lib.qoq_quant_act_ex(A, 4, 520, A, A, A, 1, A, 0, S) == 2
+    assert lib.qoq_quant_act_ex(A, 4, 512, A, A, A, 2, B, 0, S) == 3
+    # unknown launch flags
+    assert lib.qoq_quant_act_ex(A, 4, 512, A, A, A, 2, A, 2, S) == 2
+    opt = qoq.qoq_gemm_options()
+    opt.flags = 4
+    assert lib.qoq_w4a8_gemm_ex(A, A, A, A, A, 16, 256, 512, 128, A, A, 1 << 20, ctypes.byref(opt), S) == 2
     # the path query validates like the GEMM
     assert lib.qoq_gemm_path(16, 200, 512, 128, None) == -2
     assert lib.qoq_gemm_path(0, 256, 512, 128, None) == -1

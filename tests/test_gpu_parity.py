@@ -392,6 +392,59 @@ def test_mismatched_packed_weights_reported_on_device():
     assert st == 0 and bits == 0  # cleared by the read
 
 
+def _overlap_chain(points, bufs, ws, use_flags):
+    flags = qoq.QOQ_LAUNCH_OVERLAP if use_flags else 0
+    for pt in points:
+        M, N, K = pt["M"], pt["N"], pt["K"]
+        Qx = bufs["Qx"][: M * K].view(M, K)
+        sx = bufs["sx"][:M]
+        kind = qoq.qoq_gemm_path(M, N, K, 128)
+        act = bufs["act"][: qoq.qoq_act_operand_bytes(M, K, kind)]
+        qoq.qoq_quant_act_ex(pt["X"], Qx, sx, None, act, kind=kind, with_t=False, flags=flags)
+        qoq.qoq_w4a8_gemm_ex(Qx, sx, None, pt["packed"], pt["sw"], N, K, 128, O=pt["O"], workspace=ws,
+                             options=qoq.gemm_options(act_operand=act, flags=flags))
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_overlapped_launch_chain_with_shared_buffers(graph):
+    """Programmatic dependent launch: quantizer and GEMM of consecutive
+    (M, layer) points share the activation, operand, scale and workspace
+    buffers, so a kernel that touched them before its predecessor finished
+    would corrupt an earlier point; every point must still equal the oracle,
+    launched eagerly and replayed from a CUDA graph."""
+    shapes = [(8, 256, 512), (48, 384, 1024), (1, 128, 640), (40, 256, 512), (16, 384, 1024), (130, 128, 384)]
+    points = []
+    for i, (M, N, K) in enumerate(shapes):
+        W = synthetic.weights(N, K, 7100 + i, 0.02, 2)
+        X = synthetic.activations(M, K, 7200 + i, 4)
+        wq = oracle.quantize_weights_group(W, 128)
+        Qx_r, sx_r, _ = oracle.quant_act(X)
+        ref = oracle.epilogue_f64(_ref_acc(wq, Qx_r, None, 128), sx_r, wq["s_w"])
+        packed, sw = _device_weights(wq, 128)
+        points.append(dict(M=M, N=N, K=K, X=_t(X), packed=packed, sw=sw, ref=ref,
+                           O=torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)))
+    maxMK = max(M * K for M, _, K in shapes)
+    bufs = dict(Qx=torch.empty(maxMK, dtype=torch.int8, device=DEV),
+                sx=torch.empty(max(M for M, _, _ in shapes), dtype=torch.float16, device=DEV),
+                act=torch.empty(max(qoq.qoq_act_operand_bytes(M, K, k) for M, _, K in shapes for k in (1, 2)),
+                                dtype=torch.uint8, device=DEV))
+    ws = qoq.new_workspace(max(qoq.qoq_gemm_workspace_bytes(M, N, K, 128) for M, N, K in shapes))
+    _overlap_chain(points, bufs, ws, True)  # eager first (sets kernel attributes before any capture)
+    torch.cuda.synchronize()
+    if graph:
+        for pt in points:
+            pt["O"].fill_(float("nan"))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            _overlap_chain(points, bufs, ws, True)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+    for pt in points:
+        assert oracle.o_within_tolerance(_np(pt["O"]).astype(np.float64), pt["ref"]).all()
+    assert qoq.qoq_workspace_status(ws)[0] == qoq.QOQ_OK
+
+
 @pytest.mark.parametrize("kernel", [1, 2])
 def test_bounded_wait_timeout_reports_status_and_context_survives(kernel):
     """The copy warp withholds one stage (debug flag), so the consumers'

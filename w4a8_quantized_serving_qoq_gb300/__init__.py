@@ -20,6 +20,7 @@ _lock = threading.Lock()
 _lib = None
 
 QOQ_OK = 0
+QOQ_LAUNCH_OVERLAP = 1  # programmatic dependent launch (include/qoq.h)
 STATUS_NAMES = {
     0: "QOQ_OK", 1: "QOQ_ERR_INVALID_ARG", 2: "QOQ_ERR_UNSUPPORTED", 3: "QOQ_ERR_MISALIGNED",
     4: "QOQ_ERR_WORKSPACE", 5: "QOQ_ERR_CUDA", 6: "QOQ_ERR_TIMEOUT", 7: "QOQ_ERR_DEVICE",
@@ -41,6 +42,7 @@ class qoq_gemm_options(ctypes.Structure):
         ("acc_out", ctypes.c_void_p),
         ("kernel", ctypes.c_int),
         ("act_operand", ctypes.c_void_p),
+        ("flags", ctypes.c_uint32),
     ]
 
 
@@ -78,7 +80,7 @@ def load():
                 "qoq_unpack_weights": (I, [P, I, I, I, P, P, P, P]),
                 "qoq_quant_act": (I, [P, I, I, P, P, P, P]),
                 "qoq_act_operand_bytes": (S, [I, I, I]),
-                "qoq_quant_act_ex": (I, [P, I, I, P, P, P, I, P, P]),
+                "qoq_quant_act_ex": (I, [P, I, I, P, P, P, I, P, ctypes.c_uint32, P]),
                 "qoq_gemm_workspace_bytes": (S, [I, I, I, I]),
                 "qoq_gemm_workspace_bytes_ex": (S, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
                 "qoq_gemm_path": (I, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
@@ -212,7 +214,7 @@ def qoq_act_operand_bytes(M: int, K: int, kind: int) -> int:
 
 
 def qoq_quant_act_ex(X, Qx=None, s_x=None, t_x=None, act=None, kind: int = 2, with_t: bool = True,
-                     with_act: bool = True, stream=None):
+                     with_act: bool = True, flags: int = 0, stream=None):
     """qoq_quant_act plus the activation operand of `kind` (1: fp16 copy of
     Qx for the fp16-operand path, 2: fp8-path planes and group sums), a uint8
     tensor of qoq_act_operand_bytes(M, K, kind) bytes -> (Qx, s_x, t_x, act)."""
@@ -235,7 +237,7 @@ def qoq_quant_act_ex(X, Qx=None, s_x=None, t_x=None, act=None, kind: int = 2, wi
     _dev(t_x, torch.int32, "t_x")
     _dev(act, torch.uint8, "act")
     _check("qoq_quant_act_ex", load().qoq_quant_act_ex(
-        _ptr(X), M, K, _ptr(Qx), _ptr(s_x), _ptr(t_x), int(kind), _ptr(act), _stream(stream)))
+        _ptr(X), M, K, _ptr(Qx), _ptr(s_x), _ptr(t_x), int(kind), _ptr(act), int(flags), _stream(stream)))
     return Qx, s_x, t_x, act
 
 
@@ -297,10 +299,10 @@ def qoq_w4a8_gemm_i32(Qx, t_x, packed, N: int, K: int, group: int = 128, acc=Non
 
 
 def gemm_options(tokens_per_tile=0, num_ctas=0, timeout_ns=0, debug_flags=0, acc_out=None, kernel=0,
-                 act_operand=None):
+                 act_operand=None, flags=0):
     return qoq_gemm_options(tokens_per_tile, num_ctas, timeout_ns, debug_flags,
                             None if acc_out is None else acc_out.data_ptr(), kernel,
-                            None if act_operand is None else act_operand.data_ptr())
+                            None if act_operand is None else act_operand.data_ptr(), flags)
 
 
 def qoq_w4a8_gemm_ex(Qx, s_x, t_x, packed, s_w, N: int, K: int, group: int = 128, O=None,
@@ -348,4 +350,5 @@ def qoq_workspace_status(workspace, stream=None):
 
 __all__ = [n for n in dir() if n.startswith("qoq_")] + [
     "QoqError", "build", "load", "library_path", "header_functions", "new_workspace", "gemm_options",
+    "QOQ_LAUNCH_OVERLAP",
 ]

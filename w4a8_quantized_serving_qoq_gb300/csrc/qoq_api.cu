@@ -43,6 +43,7 @@ int check_options(const qoq_gemm_options *opt) {
     if (bt != 0 && bt != 16 && bt != 32 && bt != 64 && bt != 128) return QOQ_ERR_UNSUPPORTED;
     if (opt->num_ctas < 0 || opt->num_ctas > 65536) return QOQ_ERR_UNSUPPORTED;
     if (opt->kernel < 0 || opt->kernel > 2) return QOQ_ERR_UNSUPPORTED;
+    if (opt->flags & ~QOQ_LAUNCH_OVERLAP) return QOQ_ERR_UNSUPPORTED;
     return QOQ_OK;
 }
 
@@ -90,6 +91,7 @@ int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const
     a.ws = ws;
     a.debug_flags = opt ? opt->debug_flags : 0u;
     a.timeout_ns = (opt && opt->timeout_ns) ? opt->timeout_ns : kDefaultTimeoutNs;
+    a.pdl = opt && (opt->flags & QOQ_LAUNCH_OVERLAP) != 0;
     return cuda_status(qoq::launch_gemm(a, plan, stream));
 }
 
@@ -159,7 +161,7 @@ int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, in
     if (!aligned(X, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) || (t_x && !aligned(t_x, 4)))
         return QOQ_ERR_MISALIGNED;
     return cuda_status(
-        qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, 0, nullptr, reinterpret_cast<cudaStream_t>(stream)));
+        qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, 0, nullptr, false, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t qoq_act_operand_bytes(int M, int K, int kind) {
@@ -168,8 +170,9 @@ size_t qoq_act_operand_bytes(int M, int K, int kind) {
 }
 
 int qoq_quant_act_ex(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x,
-                     int kind, void *act_operand, qoq_stream_t stream) {
+                     int kind, void *act_operand, uint32_t flags, qoq_stream_t stream) {
     if (M <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
+    if (flags & ~QOQ_LAUNCH_OVERLAP) return QOQ_ERR_UNSUPPORTED;
     if (act_operand && kind != 1 && kind != 2) return QOQ_ERR_INVALID_ARG;
     if (K % 8 != 0 || (act_operand && K % 128 != 0)) return QOQ_ERR_UNSUPPORTED;
     if (!X || !Qx || !s_x) return QOQ_ERR_INVALID_ARG;
@@ -178,7 +181,7 @@ int qoq_quant_act_ex(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
         return QOQ_ERR_MISALIGNED;
     return cuda_status(
         qoq::launch_quant_act(X, M, K, Qx, s_x, t_x, act_operand ? kind : 0, act_operand,
-                              reinterpret_cast<cudaStream_t>(stream)));
+                              (flags & QOQ_LAUNCH_OVERLAP) != 0, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gemm_options *opt) {

@@ -117,6 +117,13 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait blocks until the grids this
+// one depends on have completed and their memory is visible (it returns at
+// once for a grid launched without that dependency); griddep_launch_dependents
+// lets the next grid in the stream start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Shared -> global bulk operations (bulk-group completion; the issuing thread
 // waits with bulk_wait_read before reusing the source, with bulk_wait before
 // relying on the global writes).

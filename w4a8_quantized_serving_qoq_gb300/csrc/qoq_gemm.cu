@@ -127,11 +127,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
+        griddep_launch_dependents();
         prefetch_tensormap(&qx_map);
         const PackedHeader *h = reinterpret_cast<const PackedHeader *>(p.packed);
         const bool ok = h->magic == kPackedMagic && h->version == kPackedVersion && h->N == p.N &&
                         h->K == p.K && h->group == p.group && h->illegal == 0u;
-        if (!ok) atomicOr(p.status, kStatusBadPacked);
         *hdr_ok = ok ? 1 : 0;
         *abort_flag = 0;
         *is_last = 0;
@@ -160,10 +160,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const bool run = (*hdr_ok != 0);
+    if (!run && threadIdx.x == 0) {
+        griddep_wait();  // the status word may still be in use by the preceding kernel
+        atomicOr(p.status, kStatusBadPacked);
+    }
 
     if (run && warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
+            // Before the dependency wait (programmatic dependent launch): the
+            // weight blocks of the first R stages, which no preceding kernel
+            // writes.  Each stage's barrier is armed for all its bytes; its
+            // activation copies follow after the wait.
+            const bool withhold = (p.debug_flags & kDebugWithholdStage) != 0;
+            const int pre_max = withhold ? 1 : R;
+            int pre = 0;
+            {
+                SegmentWalker w0(p, cta);
+                Segment s0;
+                while (pre < pre_max && w0.next(s0)) {
+                    const int n_tile = s0.tile / p.tok_tiles;
+                    const uint8_t *wblk = p.packed + kHeaderBytes + (static_cast<size_t>(n_tile) * p.G) * bb;
+                    for (int k = s0.k0; k < s0.k1 && pre < pre_max; ++k, ++pre) {
+                        uint8_t *dst = raw_base + pre * C::kRawSlotBytes;
+                        mbar_arrive_expect_tx(&raw_full[pre], C::kBBytes + bb);
+                        tma_load_1d(dst + C::kBBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[pre]);
+                    }
+                }
+            }
+            griddep_wait();
             SegmentWalker walk(p, cta);
             Segment sg;
             int st = 0, issued = 0;
@@ -177,13 +202,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         stop = true;
                         break;
                     }
-                    if ((p.debug_flags & kDebugWithholdStage) && st == 1) {
+                    if (withhold && st == 1) {
                         stop = true;
                         break;
                     }
                     uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
-                    mbar_arrive_expect_tx(&raw_full[slot], C::kBBytes + bb);
-                    tma_load_1d(dst + C::kBBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[slot]);
+                    if (st >= pre) {
+                        mbar_arrive_expect_tx(&raw_full[slot], C::kBBytes + bb);
+                        tma_load_1d(dst + C::kBBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[slot]);
+                    }
                     tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &raw_full[slot]);
                     tma_load_2d(dst + C::kBAtom, &qx_map, k * kTileK + 64, tok_tile * BT, &raw_full[slot]);
                     issued = st + 1;
@@ -319,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (run && warp >= 4 && warp < 8) {
         // ------------------------------------------------ epilogue warps --
+        griddep_wait();  // scales, workspace and output may belong to the preceding kernel
         const int et = threadIdx.x - 128;           // TMEM lane == weight row in tile
         const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         SegmentWalker walk(p, cta);
@@ -604,8 +632,7 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
     dim3 grid(plan.ctas);
-    w4a8_gemm_kernel<BT><<<grid, kThreads, C::kSmemBytes, stream>>>(map, o_map, p);
-    return cudaGetLastError();
+    return launch_kernel(w4a8_gemm_kernel<BT>, grid, dim3(kThreads), C::kSmemBytes, stream, a.pdl, map, o_map, p);
 }
 
 }  // namespace

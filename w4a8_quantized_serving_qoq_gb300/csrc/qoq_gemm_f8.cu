@@ -160,12 +160,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     const uint64_t tmo = p.timeout_ns;
 
     if (threadIdx.x == 0) {
+        griddep_launch_dependents();
         prefetch_tensormap(&plane_map);
         prefetch_tensormap(&tg_map);
         const PackedHeader *h = reinterpret_cast<const PackedHeader *>(p.packed);
         const bool ok = h->magic == kPackedMagic && h->version == kPackedVersion && h->N == p.N &&
                         h->K == p.K && h->group == p.group && h->illegal == 0u && p.group == 128;
-        if (!ok) atomicOr(p.status, kStatusBadPacked);
         *hdr_ok = ok ? 1 : 0;
         *abort_flag = 0;
         *is_last = 0;
@@ -191,10 +191,37 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const bool run = (*hdr_ok != 0);
+    if (!run && threadIdx.x == 0) {
+        griddep_wait();  // the status word may still be in use by the preceding kernel
+        atomicOr(p.status, kStatusBadPacked);
+    }
 
     if (run && warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
+            // Before the dependency wait (programmatic dependent launch): the
+            // weight blocks of the first R stages, which no preceding kernel
+            // writes.  Each stage's barrier is armed for all its bytes; the
+            // activation operand copies follow after the wait.
+            const bool withhold = (p.debug_flags & kDebugWithholdStage) != 0;
+            const int pre_max = withhold ? 1 : R;
+            int pre = 0;
+            {
+                SegmentWalker w0(p, cta);
+                Segment s0;
+                while (pre < pre_max && w0.next(s0)) {
+                    const int n_tile = s0.tile / p.tok_tiles;
+                    const uint8_t *wrow = p.packed + kHeaderBytes + static_cast<size_t>(n_tile) * p.G * kBlockBytesG;
+                    for (int k = s0.k0; k < s0.k1 && pre < pre_max; k += kGroupsPerStage, ++pre) {
+                        const int ng = min(kGroupsPerStage, s0.k1 - k);
+                        uint8_t *dst = raw_base + pre * C::kRawSlotBytes;
+                        mbar_arrive_expect_tx(&raw_full[pre], ng * (kBlockBytesG + C::kPlaneGroupBytes) + C::kTgBytes);
+                        tma_load_1d(dst + C::kWOff, wrow + static_cast<size_t>(k) * kBlockBytesG, ng * kBlockBytesG,
+                                    &raw_full[pre]);
+                    }
+                }
+            }
+            griddep_wait();
             SegmentWalker walk(p, cta);
             Segment sg;
             int st = 0, issued = 0;
@@ -210,14 +237,16 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                         stop = true;
                         break;
                     }
-                    if ((p.debug_flags & kDebugWithholdStage) && st == 1) {
+                    if (withhold && st == 1) {
                         stop = true;
                         break;
                     }
                     uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
-                    mbar_arrive_expect_tx(&raw_full[slot], ng * (kBlockBytesG + C::kPlaneGroupBytes) + C::kTgBytes);
-                    tma_load_1d(dst + C::kWOff, wrow + static_cast<size_t>(k) * kBlockBytesG, ng * kBlockBytesG,
-                                &raw_full[slot]);
+                    if (st >= pre) {
+                        mbar_arrive_expect_tx(&raw_full[slot], ng * (kBlockBytesG + C::kPlaneGroupBytes) + C::kTgBytes);
+                        tma_load_1d(dst + C::kWOff, wrow + static_cast<size_t>(k) * kBlockBytesG, ng * kBlockBytesG,
+                                    &raw_full[slot]);
+                    }
                     for (int g = 0; g < ng; ++g)
                         tma_load_3d(dst + g * C::kPlaneGroupBytes, &plane_map, (k + g) * kTileK, m0, 0,
                                     &raw_full[slot]);
@@ -341,6 +370,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
     } else if (run && warp >= 8 && warp < 16) {
         // ------------------------------------------------- drain warps --
+        griddep_wait();  // scales, workspace and output may belong to the preceding kernel
         const int ew = warp - 8;
         const int et = threadIdx.x - 256;          // 0..255 among the drain threads
         const int row = (ew & 3) * 32 + lane;      // weight row == TMEM lane
@@ -534,8 +564,8 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
     p.ctas = plan.ctas;
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
-    w4a8_gemm_f8_kernel<BT><<<dim3(plan.ctas), kF8Threads, C::kSmemBytes, stream>>>(plane_map, tg_map, p);
-    return cudaGetLastError();
+    return launch_kernel(w4a8_gemm_f8_kernel<BT>, dim3(plan.ctas), dim3(kF8Threads), C::kSmemBytes, stream, a.pdl,
+                         plane_map, tg_map, p);
 }
 
 }  // namespace

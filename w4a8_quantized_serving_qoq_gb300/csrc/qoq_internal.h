@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 namespace qoq {
@@ -104,7 +105,7 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path =
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
-                             int32_t *t_x, int act_kind, void *act_operand, cudaStream_t stream);
+                             int32_t *t_x, int act_kind, void *act_operand, bool pdl, cudaStream_t stream);
 // Activation operand of the given kind from already quantized activations.
 cudaError_t launch_act_operand(const int8_t *Qx, int M, int K, int act_kind, void *act_operand,
                                cudaStream_t stream);
@@ -128,6 +129,7 @@ struct GemmArgs {
     void *ws;
     uint32_t debug_flags;
     uint64_t timeout_ns;
+    bool pdl;             // launch as a programmatic dependent of the preceding kernel
 };
 
 cudaError_t launch_gemm(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream);
@@ -136,5 +138,24 @@ cudaError_t launch_gemm_f8(const GemmArgs &a, const GemmPlan &plan, cudaStream_t
 // Debug flag: the TMA producer withholds the second stage's load, so the
 // consumers' bounded waits expire (exercises the timeout path).
 constexpr uint32_t kDebugWithholdStage = 1u;
+
+// Launch, optionally as a programmatic dependent of the preceding kernel in
+// the stream (the kernel itself calls griddepcontrol.wait before it touches
+// memory that kernel may still be writing).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          bool pdl, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1u : 0u;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace qoq

@@ -91,5 +91,6 @@ extern "C" int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, cons
     a.ws = scratch;
     a.debug_flags = 0;
     a.timeout_ns = 2000000000ull;
+    a.pdl = false;
     return qoq::launch_gemm(a, plan, s) == cudaSuccess ? QOQ_OK : QOQ_ERR_CUDA;
 }

@@ -14,6 +14,7 @@
 #include <cuda_fp16.h>
 
 #include "qoq_internal.h"
+#include "qoq_device.cuh"
 
 namespace qoq {
 namespace {
@@ -106,6 +107,10 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
                                  uint8_t *__restrict__ act) {
     __shared__ float shf[32];
     __shared__ int shi[32];
+    // Under programmatic dependent launch: let the next kernel start
+    // launching, then wait for the previous one before reading X or writing.
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_wait();
     const size_t m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(X + m * K);
     const int nv = K >> 3, bd = blockDim.x, tid = threadIdx.x;
@@ -292,18 +297,17 @@ __global__ void quantize_channel_kernel(const uint16_t *__restrict__ W, int K,
 }  // namespace
 
 cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
-                             int32_t *t_x, int act_kind, void *act_operand, cudaStream_t stream) {
+                             int32_t *t_x, int act_kind, void *act_operand, bool pdl, cudaStream_t stream) {
     // Few long rows: one wide CTA per row keeps the per-row latency short.
-    const int threads = (M < 296) ? 1024 : 256;
+    const dim3 grid(M), block((M < 296) ? 1024 : 256);
     uint8_t *act = static_cast<uint8_t *>(act_operand);
     if (!act) act_kind = 0;
     if (act_kind == 1)
-        quant_act_kernel<1><<<M, threads, 0, stream>>>(X, M, K, Qx, s_x, t_x, act);
-    else if (act_kind == 2)
-        quant_act_kernel<2><<<M, threads, 0, stream>>>(X, M, K, Qx, s_x, t_x, act);
-    else
-        quant_act_kernel<0><<<M, threads, 0, stream>>>(X, M, K, Qx, s_x, t_x, nullptr);
-    return cudaGetLastError();
+        return launch_kernel(quant_act_kernel<1>, grid, block, 0, stream, pdl, X, M, K, Qx, s_x, t_x, act);
+    if (act_kind == 2)
+        return launch_kernel(quant_act_kernel<2>, grid, block, 0, stream, pdl, X, M, K, Qx, s_x, t_x, act);
+    return launch_kernel(quant_act_kernel<0>, grid, block, 0, stream, pdl, X, M, K, Qx, s_x, t_x,
+                         static_cast<uint8_t *>(nullptr));
 }
 
 cudaError_t launch_act_operand(const int8_t *Qx, int M, int K, int act_kind, void *act_operand,
