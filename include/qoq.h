@@ -226,7 +226,10 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  *                     number of k-stages.
  *   timeout_ns      : bound of every device-side wait, 0 = 2 s.
  *   debug_flags     : bit 0 = the copy warp withholds the second stage, so
- *                     the bounded waits expire (timeout path test).
+ *                     the bounded waits expire (timeout path test); bit 1 =
+ *                     a split tile's last contributor never finishes it
+ *                     directly, every contributor publishes its partial
+ *                     (tests the fix-up by the last arriver).
  *   acc_out         : if non-NULL, int32 accumulators are written here
  *                     instead of O.
  *   kernel          : 0 = automatic, 1 = fp16-operand tensor-core path

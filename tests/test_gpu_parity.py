@@ -212,24 +212,29 @@ def test_gemm_i32_bit_exact(M, N, K, group):
 
 @pytest.mark.parametrize("bt", [16, 32, 64, 128])
 @pytest.mark.parametrize("ctas", [1, 2, 5, 13, 0])
-def test_gemm_tiles_and_stream_k_splits(bt, ctas):
+@pytest.mark.parametrize("publish", [0, 2])
+def test_gemm_tiles_and_stream_k_splits(bt, ctas, publish):
     """Every tile size, and persistent-CTA counts that cut output tiles at
-    different k-stages (exact int32 reduction of split tiles)."""
+    different k-stages (exact int32 reduction of split tiles), with the last
+    contributor finishing a tile directly or (debug bit 1) every contributor
+    publishing its partial for a fix-up by the last arriver."""
     M, N, K = 37, 256, 1152  # ragged token tail; 9 groups (one chunk boundary)
     wq, Qx, sx, tx = _gemm_case(M, N, K, 77)
     packed, sw = _device_weights(wq, 128)
     ref = _ref_acc(wq, Qx, tx, 128)
     acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
-    opt = qoq.gemm_options(tokens_per_tile=bt, num_ctas=ctas, acc_out=acc)
+    opt = qoq.gemm_options(tokens_per_tile=bt, num_ctas=ctas, acc_out=acc, debug_flags=publish)
     ws = qoq.new_workspace(qoq.qoq_gemm_workspace_bytes(M, N, K, 128, opt))
     for _ in range(2):  # the workspace must come back zeroed
         acc.fill_(0)
         qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128, workspace=ws, options=opt)
         assert np.array_equal(_np(acc), ref)
-    O = qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N, K, 128,
-                             options=qoq.gemm_options(tokens_per_tile=bt, num_ctas=ctas))
     O_ref = oracle.epilogue_f64(ref, sx, wq["s_w"])
-    assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
+    for _ in range(2):
+        O = qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N, K, 128, workspace=ws,
+                                 options=qoq.gemm_options(tokens_per_tile=bt, num_ctas=ctas, debug_flags=publish))
+        assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
+    assert qoq.qoq_workspace_status(ws)[0] == qoq.QOQ_OK
 
 
 FP8_CASES = [(1, 256, 512), (3, 128, 384), (8, 384, 1024), (16, 256, 896), (17, 128, 640), (31, 256, 256),

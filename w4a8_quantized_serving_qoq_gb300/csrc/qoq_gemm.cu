@@ -55,12 +55,14 @@ constexpr uint32_t kWRawBytes = 9216;  // 8704 B block slot rounded to 1 KB
 
 template <int BT>
 struct Cfg {
-    // TMEM columns: [0, BT) int32 running sum, [BT, 3BT) two fp32 chunk
-    // accumulators, [kA0, kA0 + 64 * kOpStages) fp16 weight operand stages
-    // (128 lanes x 64 columns = 128 rows x 128 k each).
+    // TMEM columns: [0, BT) int32 running sum, then two fp32 chunk
+    // accumulators of BT columns from kChunk0, then kOpStages fp16 weight
+    // operand slots of 64 columns (128 lanes x 64 columns = 128 rows x 128 k
+    // each) from kA0.
     static constexpr int kOpStages = BT == 128 ? 2 : 4;
     static constexpr int kRawStages = BT == 16 ? 12 : (BT == 32 ? 10 : (BT == 64 ? 7 : 4));
-    static constexpr uint32_t kA0 = ((3 * BT + 63) / 64) * 64;
+    static constexpr uint32_t kChunk0 = static_cast<uint32_t>(BT);
+    static constexpr uint32_t kA0 = ((kChunk0 + 2 * BT + 63) / 64) * 64;
     static constexpr uint32_t kTmemCols = 512;
     // Raw slot: [B operand: two 128-byte-swizzled atoms of BT rows x 64 fp16
     // (k 0..63, k 64..127), landed by TMA from the fp16 activation operand]
@@ -68,12 +70,14 @@ struct Cfg {
     static constexpr uint32_t kBAtom = static_cast<uint32_t>(BT) * 128u;
     static constexpr uint32_t kBBytes = 2 * kBAtom;
     static constexpr uint32_t kRawSlotBytes = kBBytes + kWRawBytes;
-    static constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 4 + 1;
-    // Epilogue staging: two 8 KB buffers (16 tokens x 128 rows, int32 partials
-    // or fp16 outputs) written by the epilogue threads and sent out by one
-    // bulk copy each, then an 8 KB block of zeros that re-zeroes partial slots.
+    static constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 4 + 1 + 2;
+    // Epilogue staging: two 8 KB buffers (16 tokens x 128 rows of int32
+    // partials or fp16 outputs, written by the epilogue threads and sent out
+    // by one bulk copy each; during a split-tile fix-up they receive slot rows
+    // by bulk loads), an 8 KB block of zeros that re-zeroes partial slots,
+    // and two 4 KB fp16 output buffers for the fix-up.
     static constexpr uint32_t kStgBytes = 8192;
-    static constexpr uint32_t kStgRegion = 3 * kStgBytes;
+    static constexpr uint32_t kStgRegion = 4 * kStgBytes;
     static constexpr uint32_t kMiscBytes = 2048;  // barriers + flags, then s_x / t_x of the current tile
     static constexpr uint32_t kSmemBytes = kRawStages * kRawSlotBytes + kStgRegion + kMiscBytes + 1024;
     static_assert(kA0 + 64 * kOpStages <= kTmemCols, "TMEM columns");
@@ -114,10 +118,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *chunk_full = op_empty + OPS;
     uint64_t *chunk_empty = chunk_full + 2;
     uint64_t *mma_done = chunk_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *fix_bar = mma_done + 1;  // [2]: slot rows landed in staging buffer 0 / 1
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fix_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *hdr_ok = abort_flag + 1;
     volatile int *is_last = abort_flag + 2;
+    volatile int *fin_flag = abort_flag + 3;
     float *tile_sx = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 1024);
     int *tile_tx = reinterpret_cast<int *>(tile_sx + 128);
 
@@ -148,6 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&chunk_empty[i], kEpiWarps);  // phase 0: zeroed at start
         }
         mbar_init(mma_done, 2);
+        mbar_init(&fix_bar[0], 1);
+        mbar_init(&fix_bar[1], 1);
         fence_barrier_init();
     }
     // The zero block is read by bulk copies (async proxy).
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t d_tmem = tmem + static_cast<uint32_t>((1 + (cur & 1)) * BT);
+                        const uint32_t d_tmem = tmem + C::kChunk0 + static_cast<uint32_t>((cur & 1) * BT);
                         const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u;
                         const uint32_t b_base = smem_u32(raw_base + (st % R) * C::kRawSlotBytes);
 #pragma unroll
@@ -353,12 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         Segment sg;
         int gc = 0;
         int stg_use = 0;  // staging buffers used so far (buffer stg_use & 1 is next)
+        uint32_t fix_n0 = 0, fix_n1 = 0;  // fix-up loads consumed per staging buffer (mbarrier phases)
         {
             // Both chunk buffers start zeroed (the MMAs only accumulate).
             uint32_t zero16[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) zero16[i] = 0u;
-            for (int j = 0; j < 2 * BT / 16; ++j) tmem_st16(tl + static_cast<uint32_t>(BT + 16 * j), zero16);
+            for (int j = 0; j < 2 * BT / 16; ++j) tmem_st16(tl + C::kChunk0 + static_cast<uint32_t>(16 * j), zero16);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -390,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_tx[et] = (m < p.M && p.group == 0) ? p.t_x[m] : 0;
             }
             named_bar_sync(2, kEpiThreads);
+            bool fin_seg = false;  // this CTA finishes the split tile directly
             for (int c = 0; c < nch; ++c) {
                 const int cur = gc++;
                 const int cb = cur & 1;
@@ -400,10 +410,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait_warp(&chunk_full[cb], (cur >> 1) & 1, abort_flag, p.status, tmo);
                 tc_fence_after();
                 const bool last = c == nch - 1;
+                // Split tile: if every other contributor has already published
+                // its partial, this CTA is the last one and finishes the tile
+                // itself, keeping its own partial in the TMEM running sum.
+                bool fin = false;
+                if (last && split) {
+                    named_bar_sync(3, kEpiThreads);
+                    if (et == 0) {
+                        int f = 0;
+                        if (*abort_flag == 0 && !(p.debug_flags & kDebugAlwaysPublish)) {
+                            const uint32_t others = static_cast<uint32_t>(
+                                cta_of_stage(tfirst + static_cast<uint32_t>(p.G) - 1u, p) - slot_idx);
+                            f = (ld_acquire_gpu_u32(p.counters + slot_idx) == others) ? 1 : 0;
+                        }
+                        *fin_flag = f;
+                    }
+                    named_bar_sync(3, kEpiThreads);
+                    fin = *fin_flag != 0;
+                }
 #pragma unroll 1
                 for (int j = 0; j < BT / 16; ++j) {
                     uint32_t f[16], r[16];
-                    tmem_ld16(tl + static_cast<uint32_t>((1 + cb) * BT + 16 * j), f);
+                    tmem_ld16(tl + C::kChunk0 + static_cast<uint32_t>(cb * BT + 16 * j), f);
                     if (c > 0) {
                         tmem_ld16(tl + static_cast<uint32_t>(16 * j), r);
                         tmem_wait_ld_regs(r);
@@ -414,14 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t zero16[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) zero16[i] = 0u;
-                        tmem_st16(tl + static_cast<uint32_t>((1 + cb) * BT + 16 * j), zero16);
+                        tmem_st16(tl + C::kChunk0 + static_cast<uint32_t>(cb * BT + 16 * j), zero16);
                     }
                     uint32_t v[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[i])) +
                                                      (c > 0 ? static_cast<int>(r[i]) : 0));
-                    if (!last) {
+                    if (!last || fin) {
                         tmem_st16(tl + static_cast<uint32_t>(16 * j), v);
                     } else if (!split && p.acc_out) {
                         // int32 test output: one store per element
@@ -470,77 +498,107 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&chunk_empty[cb]);
+                if (last) fin_seg = fin;
             }
             if (split) {
-                // Every epilogue thread reaches both named barriers once per
-                // split segment.  A failed wait anywhere has raised abort_flag
-                // before the first barrier, so the decision below is uniform.
-                // One thread issued this tile's partial reductions; it waits for
-                // them to complete, publishes them with a fence and the arrival
-                // counter, and learns whether this CTA is the last contributor.
-                named_bar_sync(1, kEpiThreads);
-                if (et == 0) {
-                    int last_cta = 0;
-                    if (*abort_flag == 0) {
-                        bulk_wait<0>();
-                        __threadfence();
-                        const uint32_t tlast = tfirst + static_cast<uint32_t>(p.G) - 1u;
-                        const unsigned expected =
-                            static_cast<unsigned>(cta_of_stage(tlast, p) - slot_idx + 1);
-                        const unsigned prev = atomicAdd(p.counters + slot_idx, 1u);
-                        last_cta = (prev + 1 == expected) ? 1 : 0;
-                        if (last_cta) __threadfence();
+                bool do_fix = fin_seg;
+                if (!fin_seg) {
+                    // Every epilogue thread reaches both named barriers once per
+                    // split segment.  A failed wait anywhere has raised abort_flag
+                    // before the first barrier, so the decision below is uniform.
+                    // One thread issued this tile's partial reductions; it waits
+                    // for them to complete, publishes them with a fence and the
+                    // arrival counter, and learns whether this CTA is the last.
+                    named_bar_sync(1, kEpiThreads);
+                    if (et == 0) {
+                        int last_cta = 0;
+                        if (*abort_flag == 0) {
+                            bulk_wait<0>();
+                            __threadfence();
+                            const uint32_t tlast = tfirst + static_cast<uint32_t>(p.G) - 1u;
+                            const unsigned expected =
+                                static_cast<unsigned>(cta_of_stage(tlast, p) - slot_idx + 1);
+                            const unsigned prev = atomicAdd(p.counters + slot_idx, 1u);
+                            last_cta = (prev + 1 == expected) ? 1 : 0;
+                            if (last_cta) __threadfence();
+                        }
+                        *is_last = last_cta;
                     }
-                    *is_last = last_cta;
+                    named_bar_sync(1, kEpiThreads);
+                    do_fix = *is_last != 0;
                 }
-                named_bar_sync(1, kEpiThreads);
-                if (*is_last) {
-                    const int mend = min(p.M - m0, BT);
-                    // Every contributor's reduction landed in L2 before its
-                    // counter increment; read the sums from L2 (16 loads in
-                    // flight), write the outputs through the staging buffers,
-                    // then re-zero the slot for the next call.
-                    for (int ml0 = 0; ml0 < mend; ml0 += 16) {
+                if (do_fix) {
+                    // Fix-up: out = (own partial, kept in TMEM when finishing
+                    // directly) + the slot's sums.  Slot rows of 16 tokens (8 KB)
+                    // come in by bulk loads, two in flight through the staging
+                    // buffers; each block's rows are then re-zeroed and its fp16
+                    // outputs leave through the two fix-up output buffers.
+                    constexpr int nb = BT / 16;
+                    if (et == 0) {
+                        bulk_wait_read<0>();        // staging buffers no longer read by earlier copies
+                        fence_proxy_async_global();  // the counter acquire orders the loads below
+                        for (int q = 0; q < (nb < 2 ? nb : 2); ++q) {
+                            mbar_arrive_expect_tx(&fix_bar[q], C::kStgBytes);
+                            tma_load_1d(stg_base + q * C::kStgBytes, slot + 16 * q * kTileN, C::kStgBytes, &fix_bar[q]);
+                        }
+                    }
+#pragma unroll 1
+                    for (int j = 0; j < nb; ++j) {
+                        const int q = j & 1;
+                        // The loads always complete (they read the workspace), so
+                        // this wait ignores the abort flag: none is left in flight.
+                        mbar_wait_warp(&fix_bar[q], (q ? fix_n1 : fix_n0) & 1u, nullptr, p.status, tmo);
+                        if (q) ++fix_n1; else ++fix_n0;
+                        const uint32_t sbuf = smem_u32(stg_base) + q * C::kStgBytes;
                         int acc[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[i] = (ml0 + i < mend) ? ld_cg_s32(slot + (ml0 + i) * kTileN + et) : 0;
+                        for (int i = 0; i < 16; ++i) acc[i] = ld_shared_s32(sbuf + 4u * (i * kTileN + et));
+                        if (fin_seg) {
+                            uint32_t r[16];
+                            tmem_ld16(tl + static_cast<uint32_t>(16 * j), r);
+                            tmem_wait_ld_regs(r);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[i] += static_cast<int>(r[i]);
+                        }
+                        if (et == 0) bulk_wait_read<1>();  // output buffer q: its store from block j-2 has read it
+                        named_bar_sync(3, kEpiThreads);     // ... and every thread has read staging buffer q
+                        if (et == 0) {
+                            if (*abort_flag == 0) {
+                                bulk_store(slot + 16 * j * kTileN, stg_base + 2 * C::kStgBytes, C::kStgBytes);
+                                bulk_commit();
+                            }
+                            if (j + 2 < nb) {
+                                mbar_arrive_expect_tx(&fix_bar[q], C::kStgBytes);
+                                tma_load_1d(stg_base + q * C::kStgBytes, slot + 16 * (j + 2) * kTileN, C::kStgBytes,
+                                            &fix_bar[q]);
+                            }
+                        }
                         if (p.acc_out) {
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
-                                if (ml0 + i < mend)
-                                    write_out(p, m0 + ml0 + i, n, acc[i], zc, tile_tx[ml0 + i], tile_sx[ml0 + i], sw);
+                                if (*abort_flag == 0 && m0 + 16 * j + i < p.M)
+                                    write_out(p, m0 + 16 * j + i, n, acc[i], zc, tile_tx[16 * j + i], tile_sx[16 * j + i], sw);
                             continue;
                         }
-                        if (et == 0) bulk_wait_read<1>();
-                        named_bar_sync(3, kEpiThreads);
-                        const uint32_t buf = smem_u32(stg_base) + (stg_use & 1) * C::kStgBytes;
+                        const uint32_t obuf = smem_u32(stg_base) + 3 * C::kStgBytes + q * (C::kStgBytes / 2);
                         uint32_t sxv[16], txv[16];
-                        ld_shared_x16(smem_u32(tile_sx + ml0), sxv);
-                        ld_shared_x16(smem_u32(tile_tx + ml0), txv);
+                        ld_shared_x16(smem_u32(tile_sx + 16 * j), sxv);
+                        ld_shared_x16(smem_u32(tile_tx + 16 * j), txv);
                         uint16_t o[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             o[i] = out_fp16(acc[i], zc, static_cast<int>(txv[i]), __uint_as_float(sxv[i]), sw);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) st_shared_u16(buf + 2u * (i * kTileN + et), o[i]);
+                        for (int i = 0; i < 16; ++i) st_shared_u16(obuf + 2u * (i * kTileN + et), o[i]);
                         fence_proxy_async_smem();
                         named_bar_sync(3, kEpiThreads);
                         if (et == 0 && *abort_flag == 0) {
-                            tma_store_2d(&o_map, stg_base + (stg_use & 1) * C::kStgBytes, n_tile * kTileN, m0 + ml0);
+                            tma_store_2d(&o_map, stg_base + 3 * C::kStgBytes + q * (C::kStgBytes / 2), n_tile * kTileN,
+                                         m0 + 16 * j);
                             bulk_commit();
                         }
-                        ++stg_use;
                     }
-                    // All slot reads above have completed (their values were
-                    // used before this barrier); zero the whole slot.
-                    named_bar_sync(3, kEpiThreads);
-                    if (et == 0) {
-                        for (int j = 0; j < BT / 16; ++j)
-                            bulk_store(slot + 16 * j * kTileN, stg_base + 2 * C::kStgBytes, C::kStgBytes);
-                        bulk_commit();
-                        p.counters[slot_idx] = 0u;
-                    }
+                    if (et == 0 && *abort_flag == 0) p.counters[slot_idx] = 0u;
                 }
             }
             named_bar_sync(1, kEpiThreads);  // also: is_last is rewritten by the next split segment

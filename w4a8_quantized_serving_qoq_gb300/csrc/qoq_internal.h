@@ -138,6 +138,10 @@ cudaError_t launch_gemm_f8(const GemmArgs &a, const GemmPlan &plan, cudaStream_t
 // Debug flag: the TMA producer withholds the second stage's load, so the
 // consumers' bounded waits expire (exercises the timeout path).
 constexpr uint32_t kDebugWithholdStage = 1u;
+// Debug flag: a split tile's last contributor never finishes it directly;
+// every contributor publishes its partial (exercises the fix-up by the last
+// arriver).
+constexpr uint32_t kDebugAlwaysPublish = 2u;
 
 // Launch, optionally as a programmatic dependent of the preceding kernel in
 // the stream (the kernel itself calls griddepcontrol.wait before it touches
