@@ -244,24 +244,28 @@ FP8_CASES = [(1, 256, 512), (3, 128, 384), (8, 384, 1024), (16, 256, 896), (17, 
 @pytest.mark.parametrize("M,N,K", FP8_CASES)
 @pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("ctas", [0, 3])
-def test_both_tensor_core_paths_bit_exact(M, N, K, kernel, ctas):
+@pytest.mark.parametrize("publish", [0, 2])
+def test_both_tensor_core_paths_bit_exact(M, N, K, kernel, ctas, publish):
     """The fp16-operand path and the fp8-operand path (exact e4m3 codes, per-
     group drain) give the same int32 accumulators at decode sizes, including
-    odd group counts (a last stage with one group) and split tiles."""
+    odd group counts (a last stage with one group) and split tiles, finished
+    directly or (debug bit 1) through published partials."""
     wq, Qx, sx, tx = _gemm_case(M, N, K, 4242 + M + K)
     packed, sw = _device_weights(wq, 128)
     ref = _ref_acc(wq, Qx, tx, 128)
     acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
-    opt = qoq.gemm_options(num_ctas=ctas, acc_out=acc, kernel=kernel)
+    opt = qoq.gemm_options(num_ctas=ctas, acc_out=acc, kernel=kernel, debug_flags=publish)
     ws = qoq.new_workspace(qoq.qoq_gemm_workspace_bytes(M, N, K, 128, opt))
     for _ in range(2):
         acc.fill_(0)
         qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128, workspace=ws, options=opt)
         assert np.array_equal(_np(acc), ref)
-    O = qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N, K, 128,
-                             options=qoq.gemm_options(num_ctas=ctas, kernel=kernel))
     O_ref = oracle.epilogue_f64(ref, sx, wq["s_w"])
-    assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
+    for _ in range(2):
+        O = qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N, K, 128, workspace=ws,
+                                 options=qoq.gemm_options(num_ctas=ctas, kernel=kernel, debug_flags=publish))
+        assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
+    assert qoq.qoq_workspace_status(ws)[0] == qoq.QOQ_OK
 
 
 @pytest.mark.parametrize("M,N,K", FP8_CASES)

@@ -31,8 +31,10 @@
 // per lane quarter, one half of the tokens each).  A drained stage also
 // proves its MMAs complete, so the drain's release of a stage's metadata
 // slot is what frees the matching TMEM operand slot too.  Persistent
-// stream-K schedule, exact int32 reduction of split tiles and bounded waits
-// as in the fp16 path.
+// stream-K schedule, bounded waits, and tile outputs as in the fp16 path:
+// fp16 tiles by tensor bulk stores; a split tile's partial published by one
+// bulk reduce-add, finished by the last contributor (directly, when every
+// other partial is already published) from one bulk load of the slot.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -53,7 +55,7 @@ constexpr uint32_t kBlockBytesG = kCodeBytes + kMetaBytes;  // 8704
 template <int BT>
 struct F8Cfg {
     static constexpr int kNmma = 2 * BT;                  // uh plane rows + ul plane rows
-    static constexpr int kRawStages = 6;
+    static constexpr int kRawStages = BT == 16 ? 6 : 5;
     static constexpr int kOpStages = 4;                   // TMEM A slots == metadata slots
     static constexpr int kAuxStages = kOpStages;
     // Raw slot: [B planes, group 0 | group 1][t_g 2 x BT][weight blocks 2 x 8704].
@@ -72,10 +74,17 @@ struct F8Cfg {
     static constexpr int kDSets = BT == 16 ? 4 : 2;
     static constexpr uint32_t kA0 = static_cast<uint32_t>(kDSets) * 2u * kNmma;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kNumBars = 2 * kRawStages + kOpStages + 2 * kAuxStages + 2 * kDSets + 1;
+    static constexpr int kNumBars = 2 * kRawStages + kOpStages + 2 * kAuxStages + 2 * kDSets + 1 + 1;
+    // Tile output staging: int32 [BT][128] (a split tile's partials, or the
+    // slot read back for the fix-up), an 8 KB zero block that re-zeroes
+    // slots, and fp16 [BT][128] outputs; all moved by bulk copies.
+    static constexpr uint32_t kStgI32Bytes = static_cast<uint32_t>(BT) * kTileN * 4u;
+    static constexpr uint32_t kZeroBytes = 8192;
+    static constexpr uint32_t kOutBytes = static_cast<uint32_t>(BT) * kTileN * 2u;
+    static constexpr uint32_t kEpiRegion = kStgI32Bytes + kZeroBytes + kOutBytes;
     static constexpr uint32_t kMiscBytes = 2048;
     static constexpr uint32_t kSmemBytes =
-        kRawStages * kRawSlotBytes + kAuxStages * kAuxStageBytes + kMiscBytes + 1024;
+        kRawStages * kRawSlotBytes + kAuxStages * kAuxStageBytes + kEpiRegion + kMiscBytes + 1024;
     static_assert(kA0 + 64u * kOpStages <= kTmemCols, "TMEM columns");
     static_assert(kDSets == 2 || kDSets == kAuxStages, "D sets: double buffered, or one per metadata slot");
     static_assert(kNumBars * 8 + 64 <= 1024, "barrier area");
@@ -130,7 +139,7 @@ __device__ __forceinline__ void tmem_wait_ld_pin(uint32_t (&a)[N], uint32_t (&b)
 template <int BT>
 __global__ void __launch_bounds__(kF8Threads, 1)
     w4a8_gemm_f8_kernel(const __grid_constant__ CUtensorMap plane_map, const __grid_constant__ CUtensorMap tg_map,
-                        const GemmParams p) {
+                        const __grid_constant__ CUtensorMap o_map, const GemmParams p) {
     using C = F8Cfg<BT>;
     constexpr int R = C::kRawStages, OPS = C::kOpStages, AUX = C::kAuxStages, DS = C::kDSets;
     constexpr int HT = BT / 2;  // tokens per drain thread
@@ -139,7 +148,8 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *raw_base = smem;                                    // [B planes | t_g | 2 weight blocks]
     uint8_t *aux_base = raw_base + R * C::kRawSlotBytes;         // [meta 2x128x4 | t_g 2xBT]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(aux_base + AUX * C::kAuxStageBytes);
+    uint8_t *epi_base = aux_base + AUX * C::kAuxStageBytes;      // [int32 BTx128 | zeros 8 KB | fp16 BTx128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(epi_base + C::kEpiRegion);
     uint64_t *raw_full = bars;
     uint64_t *raw_empty = raw_full + R;
     uint64_t *op_full = raw_empty + R;
@@ -148,10 +158,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     uint64_t *d_full = aux_empty + AUX;
     uint64_t *d_empty = d_full + DS;
     uint64_t *mma_done = d_empty + DS;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *fix_bar = mma_done + 1;  // slot rows landed in the int32 staging (fix-up)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fix_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *hdr_ok = abort_flag + 1;
     volatile int *is_last = abort_flag + 2;
+    volatile int *fin_flag = abort_flag + 3;
     float *tile_sx = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 1024);
     int *tile_tx = reinterpret_cast<int *>(tile_sx + 128);
 
@@ -183,8 +195,13 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             mbar_init(&d_empty[i], kF8EpiWarps);
         }
         mbar_init(mma_done, 2);  // one commit per issuing thread
+        mbar_init(fix_bar, 1);
         fence_barrier_init();
     }
+    // The zero block is read by bulk copies (async proxy).
+    for (int i = threadIdx.x; i < static_cast<int>(C::kZeroBytes / 16); i += kF8Threads)
+        st_shared_v4(smem_u32(epi_base + C::kStgI32Bytes) + 16u * i, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
     if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -377,6 +394,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         const int hs = ew >> 2;                    // token half
         const uint32_t tl = tmem + (static_cast<uint32_t>((ew & 3) * 32) << 16);
         const int bits48 = 0x42400000;             // fp32 48.0
+        uint32_t fix_n = 0;                        // fix-up loads consumed (fix_bar phases)
         SegmentWalker walk(p, cta);
         Segment sg;
         int st = 0;
@@ -409,21 +427,46 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 const uint8_t *aux = aux_base + as * C::kAuxStageBytes;
                 const uint32_t *aux_meta = reinterpret_cast<const uint32_t *>(aux);
                 const int *aux_tg = reinterpret_cast<const int *>(aux + C::kAuxMetaBytes);
-                for (int g = 0; g < ng; ++g) {
-                    uint32_t dh[HT], dl[HT];
-                    const uint32_t dcol = static_cast<uint32_t>((2 * ds + g) * C::kNmma + hs * HT);
-                    tmem_ld_cols<HT>(tl + dcol, dh);
-                    tmem_ld_cols<HT>(tl + dcol + BT, dl);
-                    tmem_wait_ld_pin<HT>(dh, dl);
+                auto group_sum = [&](int g, const uint32_t (&dh)[HT], const uint32_t (&dl)[HT]) {
                     const uint32_t meta = aux_meta[g * 128 + row];
                     const int s = static_cast<int>(meta & 0xffu), z = static_cast<int>((meta >> 8) & 0xffu);
                     const int base = bits48 + 128 * static_cast<int>(meta >> 16);
+                    uint32_t tg[HT];
+                    const uint32_t tga = smem_u32(aux_tg + g * BT + hs * HT);
+#pragma unroll
+                    for (int q = 0; q < HT / 4; ++q)
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(tg[4 * q]), "=r"(tg[4 * q + 1]), "=r"(tg[4 * q + 2]), "=r"(tg[4 * q + 3])
+                                     : "r"(tga + 16u * q));
 #pragma unroll
                     for (int i = 0; i < HT; ++i) {
                         const float y = __fmaf_rn(__uint_as_float(dh[i]), 16.0f,
                                                   __fadd_rn(__uint_as_float(dl[i]), 48.0f));
-                        const int corr = z * aux_tg[g * BT + hs * HT + i] + base;
+                        const int corr = z * static_cast<int>(tg[i]) + base;
                         acc[i] += s * (__float_as_int(y) - corr);
+                    }
+                };
+                const uint32_t dcol = static_cast<uint32_t>(2 * ds * C::kNmma + hs * HT);
+                if constexpr (HT <= 8) {
+                    // Both groups' accumulators in one TMEM round trip.
+                    uint32_t dh0[HT], dl0[HT], dh1[HT], dl1[HT];
+                    tmem_ld_cols<HT>(tl + dcol, dh0);
+                    tmem_ld_cols<HT>(tl + dcol + BT, dl0);
+                    if (ng > 1) {
+                        tmem_ld_cols<HT>(tl + dcol + C::kNmma, dh1);
+                        tmem_ld_cols<HT>(tl + dcol + C::kNmma + BT, dl1);
+                    }
+                    tmem_wait_ld_pin<HT>(dh0, dl0);
+                    tmem_wait_ld_pin<HT>(dh1, dl1);
+                    group_sum(0, dh0, dl0);
+                    if (ng > 1) group_sum(1, dh1, dl1);
+                } else {
+                    for (int g = 0; g < ng; ++g) {
+                        uint32_t dh[HT], dl[HT];
+                        tmem_ld_cols<HT>(tl + dcol + g * C::kNmma, dh);
+                        tmem_ld_cols<HT>(tl + dcol + g * C::kNmma + BT, dl);
+                        tmem_wait_ld_pin<HT>(dh, dl);
+                        group_sum(g, dh, dl);
                     }
                 }
                 tc_fence_before();
@@ -433,54 +476,127 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     mbar_arrive(&aux_empty[as]);
                 }
             }
-            if (ok) {
+            // ---- tile output.  Every drain thread takes the same named
+            // barriers below; the abort flag, read by the issuing thread,
+            // stops all global writes after a failed wait.
+            const uint32_t stg = smem_u32(epi_base);                                   // int32 [BT][128]
+            const uint8_t *zero_blk = epi_base + C::kStgI32Bytes;
+            const uint32_t outb = smem_u32(epi_base + C::kStgI32Bytes + C::kZeroBytes);  // fp16 [BT][128]
+            auto store_outputs = [&](const int (&val)[HT]) {
+                // fp16 tile through the staging buffer, 16 tokens per tensor store
+                if (et == 0) bulk_wait_read<0>();
+                named_bar_sync(3, kF8EpiThreads);
 #pragma unroll
                 for (int i = 0; i < HT; ++i) {
-                    const int ml = hs * HT + i, m = m0 + ml;
-                    if (m < p.M) {
-                        if (split)
-                            atomicAdd(slot + ml * kTileN + row, acc[i]);
-                        else
-                            write_out(p, m, n, acc[i], 0, 0, tile_sx[ml], sw);
-                    }
+                    const int ml = hs * HT + i;
+                    st_shared_u16(outb + 2u * (ml * kTileN + row), out_fp16(val[i], 0, 0, tile_sx[ml], sw));
                 }
-            }
-            if (split) {
-                named_bar_sync(1, kF8EpiThreads);
+                fence_proxy_async_smem();
+                named_bar_sync(3, kF8EpiThreads);
+                if (et == 0 && *abort_flag == 0) {
+                    for (int b = 0; b < BT / 16; ++b)
+                        tma_store_2d(&o_map, epi_base + C::kStgI32Bytes + C::kZeroBytes + b * 16 * kTileN * 2,
+                                     n_tile * kTileN, m0 + 16 * b);
+                    bulk_commit();
+                }
+            };
+            if (!split) {
+                if (p.acc_out) {
+#pragma unroll
+                    for (int i = 0; i < HT; ++i) {
+                        const int ml = hs * HT + i, m = m0 + ml;
+                        if (ok && m < p.M) write_out(p, m, n, acc[i], 0, 0, tile_sx[ml], sw);
+                    }
+                } else {
+                    store_outputs(acc);
+                }
+            } else {
+                // If every other contributor has published its partial, this
+                // CTA is the last one and finishes the tile with its own
+                // partial still in registers.
+                named_bar_sync(3, kF8EpiThreads);
                 if (et == 0) {
-                    int last_cta = 0;
-                    if (*abort_flag == 0) {
-                        __threadfence();
-                        const uint32_t tlast = tfirst + static_cast<uint32_t>(p.G) - 1u;
-                        const unsigned expected = static_cast<unsigned>(cta_of_stage(tlast, p) - slot_idx + 1);
-                        const unsigned prev = atomicAdd(p.counters + slot_idx, 1u);
-                        last_cta = (prev + 1 == expected) ? 1 : 0;
-                        if (last_cta) __threadfence();
+                    int f = 0;
+                    if (*abort_flag == 0 && !(p.debug_flags & kDebugAlwaysPublish)) {
+                        const uint32_t others = static_cast<uint32_t>(
+                            cta_of_stage(tfirst + static_cast<uint32_t>(p.G) - 1u, p) - slot_idx);
+                        f = (ld_acquire_gpu_u32(p.counters + slot_idx) == others) ? 1 : 0;
                     }
-                    *is_last = last_cta;
+                    *fin_flag = f;
                 }
-                named_bar_sync(1, kF8EpiThreads);
-                if (*is_last) {
-                    int v[HT];
+                named_bar_sync(3, kF8EpiThreads);
+                const bool fin = *fin_flag != 0;
+                bool do_fix = fin;
+                if (!fin) {
+                    // Publish: the [BT][128] int32 partial (contiguous in the
+                    // slot) as one bulk reduce-add; when it has completed, a
+                    // fence and the arrival counter; the last arriver fixes up.
+                    if (et == 0) bulk_wait_read<0>();
+                    named_bar_sync(3, kF8EpiThreads);
 #pragma unroll
-                    for (int i = 0; i < HT; ++i) {
-                        const int ml = hs * HT + i;
-                        v[i] = (m0 + ml < p.M) ? ld_cg_s32(slot + ml * kTileN + row) : 0;
-                    }
-#pragma unroll
-                    for (int i = 0; i < HT; ++i) {
-                        const int ml = hs * HT + i;
-                        if (m0 + ml < p.M) {
-                            slot[ml * kTileN + row] = 0;
-                            write_out(p, m0 + ml, n, v[i], 0, 0, tile_sx[ml], sw);
+                    for (int i = 0; i < HT; ++i)
+                        st_shared_b32(stg + 4u * ((hs * HT + i) * kTileN + row), static_cast<uint32_t>(acc[i]));
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, kF8EpiThreads);
+                    if (et == 0) {
+                        int last_cta = 0;
+                        if (*abort_flag == 0) {
+                            bulk_reduce_add_s32(slot, epi_base, C::kStgI32Bytes);
+                            bulk_commit();
+                            bulk_wait<0>();
+                            __threadfence();
+                            const uint32_t tlast = tfirst + static_cast<uint32_t>(p.G) - 1u;
+                            const unsigned expected =
+                                static_cast<unsigned>(cta_of_stage(tlast, p) - slot_idx + 1);
+                            const unsigned prev = atomicAdd(p.counters + slot_idx, 1u);
+                            last_cta = (prev + 1 == expected) ? 1 : 0;
+                            if (last_cta) __threadfence();
                         }
+                        *is_last = last_cta;
                     }
-                    if (et == 0) p.counters[slot_idx] = 0u;
+                    named_bar_sync(1, kF8EpiThreads);
+                    do_fix = *is_last != 0;
+                }
+                if (do_fix) {
+                    // Fix-up: the slot's sums (one bulk load) plus, when finishing
+                    // directly, this CTA's own partial; then fp16 outputs, the
+                    // slot re-zeroed and the counter reset.
+                    if (et == 0) {
+                        bulk_wait_read<0>();         // the staging buffers are no longer read
+                        fence_proxy_async_global();  // the counter acquire orders the load below
+                        mbar_arrive_expect_tx(fix_bar, C::kStgI32Bytes);
+                        tma_load_1d(epi_base, slot, C::kStgI32Bytes, fix_bar);
+                    }
+                    // The load always completes (it reads the workspace), so this
+                    // wait ignores the abort flag: it is never left in flight.
+                    mbar_wait_warp(fix_bar, fix_n & 1u, nullptr, p.status, tmo);
+                    ++fix_n;
+                    int tot[HT];
+#pragma unroll
+                    for (int i = 0; i < HT; ++i)
+                        tot[i] = ld_shared_s32(stg + 4u * ((hs * HT + i) * kTileN + row)) + (fin ? acc[i] : 0);
+                    if (p.acc_out) {
+#pragma unroll
+                        for (int i = 0; i < HT; ++i) {
+                            const int ml = hs * HT + i;
+                            if (*abort_flag == 0 && m0 + ml < p.M) write_out(p, m0 + ml, n, tot[i], 0, 0, tile_sx[ml], sw);
+                        }
+                    } else {
+                        store_outputs(tot);
+                    }
+                    if (et == 0 && *abort_flag == 0) {
+                        for (uint32_t b = 0; b < C::kStgI32Bytes; b += C::kZeroBytes)
+                            bulk_store(reinterpret_cast<uint8_t *>(slot) + b, zero_blk, C::kZeroBytes);
+                        bulk_commit();
+                        p.counters[slot_idx] = 0u;
+                    }
                 }
             }
             named_bar_sync(1, kF8EpiThreads);
             if (*abort_flag != 0) break;
         }
+        // Bulk copies read shared memory until they complete: wait before exit.
+        if (et == 0) bulk_wait<0>();
     }
 
     tc_fence_before();
@@ -544,6 +660,18 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
+    // fp16 output O [M][N]: one store box = 128 rows of a tile x 16 tokens (unused in the int32 test mode).
+    CUtensorMap o_map{};
+    if (a.O) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.N), static_cast<cuuint64_t>(a.M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.N) * 2u};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), 16u};
+        const cuuint32_t estr[2] = {1u, 1u};
+        CUresult cr = enc(&o_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.O, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     GemmParams p;
     p.packed = static_cast<const uint8_t *>(a.packed);
     p.s_x = a.s_x;
@@ -565,7 +693,7 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
     return launch_kernel(w4a8_gemm_f8_kernel<BT>, dim3(plan.ctas), dim3(kF8Threads), C::kSmemBytes, stream, a.pdl,
-                         plane_map, tg_map, p);
+                         plane_map, tg_map, o_map, p);
 }
 
 }  // namespace

@@ -171,7 +171,7 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
         const int i = base + tid;
         emit(i, i < nv ? __ldg(row + i) : make_uint4(0u, 0u, 0u, 0u));
     }
-    tsum = block_reduce(tsum, SumOp(), shi);
+    if (t_x) tsum = block_reduce(tsum, SumOp(), shi);  // t_x is uniform across the CTA
     if (tid == 0) {
         s_x[m] = sbits;
         if (t_x) t_x[m] = tsum;
@@ -298,8 +298,13 @@ __global__ void quantize_channel_kernel(const uint16_t *__restrict__ W, int K,
 
 cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
                              int32_t *t_x, int act_kind, void *act_operand, bool pdl, cudaStream_t stream) {
-    // Few long rows: one wide CTA per row keeps the per-row latency short.
-    const dim3 grid(M), block((M < 296) ? 1024 : 256);
+    // One CTA per row; about two 16-byte items per thread keeps the per-row
+    // latency short (few rows) without idle warps; many rows: 256 threads.
+    const int nv = K / 8;
+    int threads = (nv / 2 + 31) / 32 * 32;
+    threads = threads < 128 ? 128 : (threads > 1024 ? 1024 : threads);
+    if (M >= 296) threads = 256;
+    const dim3 grid(M), block(threads);
     uint8_t *act = static_cast<uint8_t *>(act_operand);
     if (!act) act_kind = 0;
     if (act_kind == 1)
