@@ -20,6 +20,7 @@ oracle timed on a bounded sample (``cpu_baseline``).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -54,6 +55,31 @@ def parse_args():
     ap.add_argument("--layers", default="qkv,o,gate_up,down")
     ap.add_argument("--ms", default="1,8,32,64,128,256")
     return ap.parse_args()
+
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+GEMM_SOURCES = ("qoq_gemm.cu", "qoq_gemm_f8.cu", "qoq_gemm_common.cuh", "qoq_device.cuh", "qoq_internal.h")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "w4a8_gemm_traffic_llama3_8b_decode_step.md")
+
+
+def gemm_traffic():
+    """DRAM bytes of one step's GEMM launches from the committed ncu summary,
+    or None when the GEMM kernel sources changed since that capture."""
+    try:
+        vals = {}
+        for line in open(TRAFFIC_SUMMARY):
+            if ":" in line and not line.startswith(("|", "#", " ")):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        h = hashlib.sha256()
+        for f in GEMM_SOURCES:
+            with open(os.path.join(ROOT, "w4a8_quantized_serving_qoq_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+        if h.hexdigest()[:16] != vals.get("gemm_source_digest"):
+            return None
+        return int(vals["dram_bytes_per_step"]), int(vals["algorithmic_bytes_per_step"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def load_peaks():
@@ -338,6 +364,7 @@ def main():
         })
     del flush
     achieved_gbs = bytes_total / (gemm_ms_total * 1e-3) / 1e9
+    traffic = gemm_traffic()
     troof_sum = sum(roofline.roof_time(p["M"], p["layer"].N, p["layer"].K, bw, p16) for p in points)
 
     # ---- end to end through the public API: host buffers, copies timed ----
@@ -393,7 +420,10 @@ def main():
                    "cuda_graph": True, "l2": f"inputs larger than L2: {args.copies} packed-weight copies "
                    f"rotated ({sum(len(c) * c[0].numel() for c, _ in weights.values()) / 1e6:.0f} MB)"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved_gbs / peaks["hbm_gbs"],
+                     "traffic": traffic[0] if traffic else None,
+                     "traffic_scope": "DRAM read+write bytes of the step's 24 GEMM launches (ncu, cold cache)",
+                     "algorithmic_bytes_per_step": traffic[1] if traffic else None,
                      "peak_source": peaks_src, "kernel": "w4a8_gemm (fp8-operand kernel for M <= 32, fp16-operand kernel above)",
                      "time_weighted_roofline_frac": troof_sum / (gemm_ms_total * 1e-3),
                      "tensor_peak_tflops": peaks["bf16_tflops"]},
