@@ -418,11 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     named_bar_sync(3, kEpiThreads);
                     if (et == 0) {
                         int f = 0;
-                        if (*abort_flag == 0 && !(p.debug_flags & kDebugAlwaysPublish)) {
-                            const uint32_t others = static_cast<uint32_t>(
-                                cta_of_stage(tfirst + static_cast<uint32_t>(p.G) - 1u, p) - slot_idx);
-                            f = (ld_acquire_gpu_u32(p.counters + slot_idx) == others) ? 1 : 0;
-                        }
+                        if (*abort_flag == 0 && !(p.debug_flags & kDebugAlwaysPublish))
+                            f = finish_directly(p, cta, slot_idx, tfirst, abort_flag) ? 1 : 0;
                         *fin_flag = f;
                     }
                     named_bar_sync(3, kEpiThreads);

@@ -85,6 +85,32 @@ __device__ __forceinline__ int cta_of_stage(uint32_t s, const GemmParams &p) {
     return static_cast<int>(((s + 1) * static_cast<uint32_t>(p.ctas) - 1) / static_cast<uint32_t>(p.total));
 }
 
+// Split-tile completion, decided by one thread: true when every other
+// contributor of the tile has published its partial (arrival counter ==
+// number of other contributors), so this CTA can finish the tile with its own
+// partial still on chip.  The contributor that owns the tile's first k-stage
+// processes its part at the end of its range, about when contributors whose
+// whole range lies in the tile finish theirs, so it waits for them, bounded
+// (then it publishes instead).  No wait cycle exists: a CTA publishes the
+// partial of its first segment (processed at the start of its range) before
+// it can wait at the end, and only first-stage owners wait.
+constexpr uint64_t kFinishWaitNs = 10000;
+
+__device__ __forceinline__ bool finish_directly(const GemmParams &p, int cta, int slot_idx, uint32_t tfirst,
+                                                volatile int *abort_flag) {
+    const uint32_t others =
+        static_cast<uint32_t>(cta_of_stage(tfirst + static_cast<uint32_t>(p.G) - 1u, p) - slot_idx);
+    if (ld_acquire_gpu_u32(p.counters + slot_idx) == others) return true;
+    if (cta != slot_idx) return false;
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kFinishWaitNs) {
+        __nanosleep(256);
+        if (*abort_flag) return false;
+        if (ld_acquire_gpu_u32(p.counters + slot_idx) == others) return true;
+    }
+    return false;
+}
+
 // Final output of one accumulator: per-channel zero fold, then either the
 // int32 value (test mode) or fp16(acc * s_x[m] * s_w[n]).
 __device__ __forceinline__ void write_out(const GemmParams &p, int m, int n, int acc, int zc, int tx,
