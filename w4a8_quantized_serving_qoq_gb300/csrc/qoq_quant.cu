@@ -32,15 +32,18 @@ __device__ __forceinline__ int rne_div(int a, int b) {
     return q;
 }
 
+// Block-wide reduction (blockDim.x a multiple of 32, at most 1024): warp
+// shuffles, one partial per warp in shared memory, then every warp reduces
+// the partials with shuffles again (identity for the missing lanes).
 template <typename T, typename Op>
-__device__ __forceinline__ T block_reduce(T v, Op op, T *sh) {
+__device__ __forceinline__ T block_reduce(T v, Op op, T *sh, T identity) {
     for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     __syncthreads();
     if (lane == 0) sh[warp] = v;
     __syncthreads();
-    v = sh[0];
-    for (int w = 1; w < nw; ++w) v = op(v, sh[w]);
+    v = lane < nw ? sh[lane] : identity;
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
 
@@ -50,14 +53,27 @@ struct SumOp { __device__ int operator()(int a, int b) const { return a + b; } }
 
 // Quantize eight fp16 values (one 16-byte load) with scale sf; returns the
 // eight INT8 codes as two words and adds them to *sum.
-__device__ __forceinline__ uint2 quant8(const uint4 v, float sf, int *sum) {
+// rne(x / s) with the quotient rounded to fp32 first, as the definition
+// states, without a division per element: inv = RN(1/s) and t = RN(x * inv)
+// differ from x/s by at most 127.1 * 2^-23 < 1.6e-5, and RN(x/s) by at most
+// half an ulp of 127 (3.9e-6) more.  So t and RN(x/s) round to the same
+// integer unless t lies within 3e-5 of a half-integer; there the IEEE
+// division decides.  (|x / s| <= 127.1 because s is max|x| / 127 rounded to
+// fp16.)
+__device__ __forceinline__ int quant_one(float x, float sf, float inv) {
+    const float t = __fmul_rn(x, inv);
+    if (fabsf(__fsub_rn(__fsub_rn(t, floorf(t)), 0.5f)) < 3.0e-5f) return __float2int_rn(__fdiv_rn(x, sf));
+    return __float2int_rn(t);
+}
+
+__device__ __forceinline__ uint2 quant8(const uint4 v, float sf, float inv, int *sum) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t out[2] = {0u, 0u};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const uint16_t hb = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu));
         int q = 0;
-        if (sf != 0.f) q = clampi(__float2int_rn(__fdiv_rn(h2f(hb), sf)), -127, 127);
+        if (sf != 0.f) q = clampi(quant_one(h2f(hb), sf, inv), -127, 127);
         *sum += q;
         out[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << ((j & 3) * 8);
     }
@@ -124,9 +140,10 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
         amax = amax8(cache[j], amax);
     }
     for (int i = tid + kActCache * bd; i < nv; i += bd) amax = amax8(__ldg(row + i), amax);
-    amax = block_reduce(amax, MaxOp(), shf);
+    amax = block_reduce(amax, MaxOp(), shf, 0.f);
     const uint16_t sbits = f2h_rn(__fdiv_rn(amax, 127.0f));
     const float sf = h2f(sbits);
+    const float inv = sf != 0.f ? __frcp_rn(sf) : 0.f;
 
     uint2 *qrow = reinterpret_cast<uint2 *>(Qx + m * K);
     uint2 *hrow = nullptr, *lrow = nullptr;
@@ -144,7 +161,7 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
         int part = 0;
         uint2 q = make_uint2(0u, 0u);
         if (i < nv) {
-            q = quant8(v, sf, &part);
+            q = quant8(v, sf, inv, &part);
             qrow[i] = q;
         }
         tsum += part;
@@ -171,7 +188,7 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
         const int i = base + tid;
         emit(i, i < nv ? __ldg(row + i) : make_uint4(0u, 0u, 0u, 0u));
     }
-    if (t_x) tsum = block_reduce(tsum, SumOp(), shi);  // t_x is uniform across the CTA
+    if (t_x) tsum = block_reduce(tsum, SumOp(), shi, 0);  // t_x is uniform across the CTA
     if (tid == 0) {
         s_x[m] = sbits;
         if (t_x) t_x[m] = tsum;
@@ -232,7 +249,7 @@ __global__ void quantize_group_kernel(const uint16_t *__restrict__ W, int K, int
     const uint16_t *row = W + n * K;
     float amax = 0.f;
     for (int k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(h2f(row[k])));
-    amax = block_reduce(amax, MaxOp(), shf);
+    amax = block_reduce(amax, MaxOp(), shf, 0.f);
     uint16_t sbits = f2h_rn(__fdiv_rn(amax, 119.0f));
     if ((sbits & 0x7fffu) == 0) sbits = 0x3c00u;  // 1.0
     const float sf = h2f(sbits);
@@ -280,8 +297,8 @@ __global__ void quantize_channel_kernel(const uint16_t *__restrict__ W, int K,
         lo = fminf(lo, v);
         hi = fmaxf(hi, v);
     }
-    lo = block_reduce(lo, MinOp(), shf);
-    hi = block_reduce(hi, MaxOp(), shf);
+    lo = block_reduce(lo, MinOp(), shf, 0.f);
+    hi = block_reduce(hi, MaxOp(), shf, 0.f);
     uint16_t sbits = f2h_rn(__fdiv_rn(__fsub_rn(hi, lo), 15.0f));
     if ((sbits & 0x7fffu) == 0) sbits = 0x3c00u;
     const float sf = h2f(sbits);
