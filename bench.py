@@ -47,8 +47,11 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--copies", type=int, default=5, help="packed-weight copies rotated to defeat L2")
-    ap.add_argument("--point-reps", type=int, default=7)
+    ap.add_argument("--copies", type=int, default=0,
+                    help="packed-weight copies per layer rotated to defeat L2 (0: enough that one layer's "
+                         "copies exceed twice the L2 size, at least 5)")
+    ap.add_argument("--point-reps", type=int, default=24,
+                    help="launches per CUDA graph when timing each point's kernels alone")
     ap.add_argument("--cpu-rows", type=int, default=192, help="weight rows in the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -248,6 +251,7 @@ def main():
     p16 = peaks["bf16_tflops"] * 1e12  # fp16 dense tensor rate = bf16 rate
     stream = torch.cuda.current_stream()
 
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2**20)
     # ---- load time: quantize + pack weights on the device, make copies ----
     weights = {}
     for layer in layers:
@@ -255,7 +259,8 @@ def main():
         W = torch.from_numpy(synthetic.weights(layer.N, layer.K, s, 0.02, 2)).to(dev)
         wq = qoq.qoq_quantize_weights(W, 128)
         packed = qoq.qoq_pack_weights(wq["q4"], wq["s_g"], wq["z"], 128)
-        copies = [packed] + [packed.clone() for _ in range(args.copies - 1)]
+        ncopy = args.copies or max(5, -(-2 * l2_bytes // packed.numel()) + 1)
+        copies = [packed] + [packed.clone() for _ in range(ncopy - 1)]
         weights[layer.name] = (copies, wq["s_w"])
         del W, wq
     points = []
@@ -330,27 +335,37 @@ def main():
     ops_step = sum(roofline.gemm_ops(p["M"], p["layer"].N, p["layer"].K) for p in points)
     tops = world * ops_step / (ms_step * 1e-3) / 1e12
 
-    # ---- per-point kernel times (L2 flushed before each launch) ----
-    flush = torch.empty(int(2 * 129e6) // 4 * 4, dtype=torch.uint8, device=dev)
+    # ---- per-point kernel times: each point's quantizer and GEMM alone, each
+    # launched R times back to back in a CUDA graph (launch overlap as in the
+    # step); the GEMMs rotate over the layer's weight copies, which together
+    # exceed twice the L2 size, so every launch reads its weights from HBM ----
+    def graph_us(fn, reps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for r in range(reps):
+                fn(r)
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3 / reps)
+        del g
+        return statistics.median(ts)
+
     pt_rows = []
     gemm_ms_total, bytes_total = 0.0, 0
     for i, pt in enumerate(points):
         layer, M = pt["layer"], pt["M"]
         copies, s_w = weights[layer.name]
-        tg, tq = [], []
-        for r in range(args.point_reps):
-            flush.fill_(r & 0xFF)
-            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-            a.record(stream)
-            quant_point(pt)
-            b.record(stream)
-            gemm_point(pt, r)
-            c.record(stream)
-            torch.cuda.synchronize()
-            tq.append(a.elapsed_time(b))
-            tg.append(b.elapsed_time(c))
-        t_g = statistics.median(tg)
-        t_q = statistics.median(tq)
+        reps = max(args.point_reps, len(copies))
+        t_q = 1e-3 * graph_us(lambda r: quant_point(pt), reps)
+        t_g = 1e-3 * graph_us(lambda r: gemm_point(pt, r), reps)
         nbytes = roofline.w4a8_bytes(M, layer.N, layer.K)
         nops = roofline.gemm_ops(M, layer.N, layer.K)
         troof = roofline.roof_time(M, layer.N, layer.K, bw, p16)
@@ -362,7 +377,6 @@ def main():
             "bound": roofline.bound(M, layer.N, layer.K, bw, p16),
             "roof_frac": round(troof / (t_g * 1e-3), 3),
         })
-    del flush
     achieved_gbs = bytes_total / (gemm_ms_total * 1e-3) / 1e9
     traffic = gemm_traffic()
     troof_sum = sum(roofline.roof_time(p["M"], p["layer"].N, p["layer"].K, bw, p16) for p in points)
@@ -417,8 +431,9 @@ def main():
         "scaling": "weak", "vs_baseline": None,
         "dtype": "s8 x u4 -> exact i32 (e4m3 / fp16 tensor-core MMA), fp16 out", "data": "synthetic",
         "config": {"workload": WORKLOAD, "group": 128, "parallelism": f"replicas{world}",
-                   "cuda_graph": True, "l2": f"inputs larger than L2: {args.copies} packed-weight copies "
-                   f"rotated ({sum(len(c) * c[0].numel() for c, _ in weights.values()) / 1e6:.0f} MB)"},
+                   "cuda_graph": True, "l2": "inputs larger than L2: packed-weight copies rotated, "
+                   + ", ".join(f"{k} x{len(c)}" for k, (c, _) in weights.items())
+                   + f" ({sum(len(c) * c[0].numel() for c, _ in weights.values()) / 1e6:.0f} MB)"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved_gbs / peaks["hbm_gbs"],
                      "traffic": traffic[0] if traffic else None,

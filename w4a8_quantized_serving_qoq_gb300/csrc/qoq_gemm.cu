@@ -305,16 +305,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = sg.k0; k < sg.k1; ++k, ++st) {
                 if ((st & 1) != cg) continue;
                 const int rs = st % R, ruse = st / R, os = st % OPS, ouse = st / OPS;
-                if (!mbar_wait_warp(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo) ||
-                    (ouse > 0 && !mbar_wait_warp(&op_empty[os], (ouse - 1) & 1, abort_flag, p.status, tmo))) {
+                if (!mbar_wait_warp(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo)) {
                     stop = true;
                     break;
                 }
-                tc_fence_after();
                 const uint32_t wraw = smem_u32(raw_base + rs * C::kRawSlotBytes) + C::kBBytes;
 
                 // Weights: row wr, 4 raw chunks of 32 k -> 128 fp16 -> 64 TMEM
-                // columns of this thread's lane (2 fp16 per column), in two halves.
+                // columns of this thread's lane (2 fp16 per column).  The whole
+                // stage is converted into registers before the wait for its
+                // operand slot, so only the TMEM store follows the MMAs that
+                // free the slot.
                 uint32_t s = 1, zz = 0;
                 if (p.group) {
                     uint16_t meta;
@@ -323,9 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     zz = meta >> 8;
                 }
                 const uint32_t cst = static_cast<uint32_t>(128 - static_cast<int>(zz * s)) * 0x01010101u;
+                uint32_t a_frag[2][32];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    uint32_t a_frag[32];
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
                         const uint4 v = ld_shared_v4(wraw + (((h * 2 + i) * 128 + wr) << 4));
@@ -336,20 +337,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t hi = (w4[j] >> 4) & 0x0F0F0F0Fu;
                             const uint32_t ulo = lo * s + cst;  // bytes: (q - z) * s + 128
                             const uint32_t uhi = hi * s + cst;
-                            uint32_t *f = a_frag + 16 * i + 4 * j;
+                            uint32_t *f = a_frag[h] + 16 * i + 4 * j;
                             biased_bytes_to_f16x4(ulo, f[0], f[1]);
                             biased_bytes_to_f16x4(uhi, f[2], f[3]);
                         }
                     }
-                    tmem_st32(a_lane + C::kA0 + static_cast<uint32_t>(os) * 64u + 32u * h, a_frag);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[rs]);  // this warp is done reading the raw slot
+                if (ouse > 0 && !mbar_wait_warp(&op_empty[os], (ouse - 1) & 1, abort_flag, p.status, tmo)) {
+                    stop = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_dst = a_lane + C::kA0 + static_cast<uint32_t>(os) * 64u;
+                tmem_st32(a_dst, a_frag[0]);
+                tmem_st32(a_dst + 32u, a_frag[1]);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&raw_empty[rs]);
-                    mbar_arrive(&op_full[os]);
-                }
+                if (lane == 0) mbar_arrive(&op_full[os]);
             }
         }
     } else if (run && warp >= 4 && warp < 8) {
