@@ -125,10 +125,16 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
     __shared__ int shi[32];
     // Under programmatic dependent launch: let the next kernel start
     // launching, then wait for the previous one before reading X or writing.
-    if (threadIdx.x == 0) griddep_launch_dependents();
-    griddep_wait();
+    // The row is prefetched into L2 first (the row is 16-byte aligned and a
+    // multiple of 16 bytes, K % 8 == 0): the wait covers the previous
+    // kernel's writes, and L2 holds the current data of every line.
     const size_t m = blockIdx.x;
     const uint4 *row = reinterpret_cast<const uint4 *>(X + m * K);
+    if (threadIdx.x == 0) {
+        griddep_launch_dependents();
+        prefetch_l2_bulk(row, static_cast<uint32_t>(K) * 2u);
+    }
+    griddep_wait();
     const int nv = K >> 3, bd = blockDim.x, tid = threadIdx.x;
     uint4 cache[kActCache];
     float amax = 0.f;
