@@ -70,7 +70,7 @@ struct Cfg {
     static constexpr uint32_t kBAtom = static_cast<uint32_t>(BT) * 128u;
     static constexpr uint32_t kBBytes = 2 * kBAtom;
     static constexpr uint32_t kRawSlotBytes = kBBytes + kWRawBytes;
-    static constexpr int kNumBars = 2 * kRawStages + 2 * kOpStages + 4 + 1 + 2;
+    static constexpr int kNumBars = 3 * kRawStages + 2 * kOpStages + 4 + 1 + 2;
     // Epilogue staging: two 8 KB buffers (16 tokens x 128 rows of int32
     // partials or fp16 outputs, written by the epilogue threads and sent out
     // by one bulk copy each; during a split-tile fix-up they receive slot rows
@@ -82,7 +82,7 @@ struct Cfg {
     static constexpr uint32_t kSmemBytes = kRawStages * kRawSlotBytes + kStgRegion + kMiscBytes + 1024;
     static_assert(kA0 + 64 * kOpStages <= kTmemCols, "TMEM columns");
     static_assert(kRawSlotBytes % 1024 == 0 && kBAtom % 1024 == 0, "1 KB aligned swizzled atoms");
-    static_assert(kNumBars * 8 + 64 <= static_cast<int>(kMiscBytes), "barrier area");
+    static_assert(kNumBars * 8 + 64 <= 1024, "barrier area (the tile scales start at +1024)");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *chunk_empty = chunk_full + 2;
     uint64_t *mma_done = chunk_empty + 2;
     uint64_t *fix_bar = mma_done + 1;  // [2]: slot rows landed in staging buffer 0 / 1
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fix_bar + 2);
+    uint64_t *act_full = fix_bar + 2;  // [R]: the B operand of a raw slot landed (raw_full: its weights)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(act_full + R);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *hdr_ok = abort_flag + 1;
     volatile int *is_last = abort_flag + 2;
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < R; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], kConvGroupWarps + 1);  // converter group + the MMA commit (B operand)
+            mbar_init(&act_full[i], 1);
         }
         for (int i = 0; i < OPS; ++i) {
             mbar_init(&op_full[i], kConvGroupWarps);
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint8_t *wblk = p.packed + kHeaderBytes + (static_cast<size_t>(n_tile) * p.G) * bb;
                     for (int k = s0.k0; k < s0.k1 && pre < pre_max; ++k, ++pre) {
                         uint8_t *dst = raw_base + pre * C::kRawSlotBytes;
-                        mbar_arrive_expect_tx(&raw_full[pre], C::kBBytes + bb);
+                        mbar_arrive_expect_tx(&raw_full[pre], bb);
                         tma_load_1d(dst + C::kBBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[pre]);
                     }
                 }
@@ -216,17 +218,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
                     if (st >= pre) {
-                        mbar_arrive_expect_tx(&raw_full[slot], C::kBBytes + bb);
+                        mbar_arrive_expect_tx(&raw_full[slot], bb);
                         tma_load_1d(dst + C::kBBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[slot]);
                     }
-                    tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &raw_full[slot]);
-                    tma_load_2d(dst + C::kBAtom, &qx_map, k * kTileK + 64, tok_tile * BT, &raw_full[slot]);
+                    mbar_arrive_expect_tx(&act_full[slot], C::kBBytes);
+                    tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &act_full[slot]);
+                    tma_load_2d(dst + C::kBAtom, &qx_map, k * kTileK + 64, tok_tile * BT, &act_full[slot]);
                     issued = st + 1;
                 }
             }
             // Drain: every issued copy must land before the CTA exits.
-            for (int t = (issued > R ? issued - R : 0); t < issued; ++t)
+            for (int t = (issued > R ? issued - R : 0); t < issued; ++t) {
                 mbar_wait(&raw_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
+                mbar_wait(&act_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
+            }
+            // Weight blocks issued before the dependency wait for stages the
+            // walk never reached (it stopped early) must land as well.
+            for (int t = issued; t < pre; ++t) mbar_wait(&raw_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
         }
     } else if (run && (warp == 1 || warp == 2)) {
         // ------------------------------------------------ MMA issuers --
@@ -355,6 +363,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st32(a_dst + 32u, a_frag[1]);
                 tmem_wait_st();
                 tc_fence_before();
+                // The B operand of this stage, copied after the dependency
+                // wait, must have landed before the MMAs (ordered after
+                // op_full) read it; the weights were converted without it.
+                if (!mbar_wait_warp(&act_full[rs], ruse & 1, abort_flag, p.status, tmo)) {
+                    stop = true;
+                    break;
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&op_full[os]);
             }

@@ -74,7 +74,7 @@ struct F8Cfg {
     static constexpr int kDSets = BT == 16 ? 4 : 2;
     static constexpr uint32_t kA0 = static_cast<uint32_t>(kDSets) * 2u * kNmma;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kNumBars = 2 * kRawStages + kOpStages + 2 * kAuxStages + 2 * kDSets + 1 + 1;
+    static constexpr int kNumBars = 3 * kRawStages + kOpStages + 2 * kAuxStages + 2 * kDSets + 1 + 1;
     // Tile output staging: int32 [BT][128] (a split tile's partials, or the
     // slot read back for the fix-up), an 8 KB zero block that re-zeroes
     // slots, and fp16 [BT][128] outputs; all moved by bulk copies.
@@ -150,9 +150,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     uint8_t *aux_base = raw_base + R * C::kRawSlotBytes;         // [meta 2x128x4 | t_g 2xBT]
     uint8_t *epi_base = aux_base + AUX * C::kAuxStageBytes;      // [int32 BTx128 | zeros 8 KB | fp16 BTx128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(epi_base + C::kEpiRegion);
-    uint64_t *raw_full = bars;
+    uint64_t *raw_full = bars;           // weight blocks of a raw slot landed
     uint64_t *raw_empty = raw_full + R;
-    uint64_t *op_full = raw_empty + R;
+    uint64_t *act_full = raw_empty + R;  // activation planes and t_g of a raw slot landed
+    uint64_t *op_full = act_full + R;
     uint64_t *aux_full = op_full + OPS;
     uint64_t *aux_empty = aux_full + AUX;
     uint64_t *d_full = aux_empty + AUX;
@@ -184,6 +185,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         for (int i = 0; i < R; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], kF8ConvWarps + 1);  // one converter group + the MMA commit
+            mbar_init(&act_full[i], 1);
         }
         for (int i = 0; i < OPS; ++i) mbar_init(&op_full[i], kF8ConvWarps);
         for (int i = 0; i < AUX; ++i) {
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     for (int k = s0.k0; k < s0.k1 && pre < pre_max; k += kGroupsPerStage, ++pre) {
                         const int ng = min(kGroupsPerStage, s0.k1 - k);
                         uint8_t *dst = raw_base + pre * C::kRawSlotBytes;
-                        mbar_arrive_expect_tx(&raw_full[pre], ng * (kBlockBytesG + C::kPlaneGroupBytes) + C::kTgBytes);
+                        mbar_arrive_expect_tx(&raw_full[pre], ng * kBlockBytesG);
                         tma_load_1d(dst + C::kWOff, wrow + static_cast<size_t>(k) * kBlockBytesG, ng * kBlockBytesG,
                                     &raw_full[pre]);
                     }
@@ -260,19 +262,25 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     }
                     uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
                     if (st >= pre) {
-                        mbar_arrive_expect_tx(&raw_full[slot], ng * (kBlockBytesG + C::kPlaneGroupBytes) + C::kTgBytes);
+                        mbar_arrive_expect_tx(&raw_full[slot], ng * kBlockBytesG);
                         tma_load_1d(dst + C::kWOff, wrow + static_cast<size_t>(k) * kBlockBytesG, ng * kBlockBytesG,
                                     &raw_full[slot]);
                     }
+                    mbar_arrive_expect_tx(&act_full[slot], ng * C::kPlaneGroupBytes + C::kTgBytes);
                     for (int g = 0; g < ng; ++g)
                         tma_load_3d(dst + g * C::kPlaneGroupBytes, &plane_map, (k + g) * kTileK, m0, 0,
-                                    &raw_full[slot]);
-                    tma_load_2d(dst + C::kTgOff, &tg_map, m0, k, &raw_full[slot]);
+                                    &act_full[slot]);
+                    tma_load_2d(dst + C::kTgOff, &tg_map, m0, k, &act_full[slot]);
                     issued = st + 1;
                 }
             }
-            for (int t = (issued > R ? issued - R : 0); t < issued; ++t)
+            for (int t = (issued > R ? issued - R : 0); t < issued; ++t) {
                 mbar_wait(&raw_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
+                mbar_wait(&act_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
+            }
+            // Weight blocks issued before the dependency wait for stages the
+            // walk never reached (it stopped early) must land as well.
+            for (int t = issued; t < pre; ++t) mbar_wait(&raw_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
         }
     } else if (run && (warp == 1 || warp == 2)) {
         // ------------------------------------------------ MMA issuers --
@@ -368,6 +376,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     uint32_t meta;
                     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(meta) : "r"(blk + kCodeBytes + 4 * wr));
                     aux_meta[g * 128 + wr] = meta;
+                }
+                // The activation planes and sums of this stage, copied after the
+                // dependency wait, must have landed before the sums are copied
+                // and the MMAs (ordered after op_full) read the planes; the
+                // weights above were converted without waiting for them.
+                if (!mbar_wait_warp(&act_full[rs], ruse & 1, abort_flag, p.status, tmo)) {
+                    tmem_wait_st();
+                    stop = true;
+                    break;
                 }
                 // Per-group activation sums for the drain: [2 groups][BT] int32.
                 if ((warp & 3) == 0) {
