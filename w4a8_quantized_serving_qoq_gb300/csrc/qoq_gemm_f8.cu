@@ -74,14 +74,17 @@ struct F8Cfg {
     static constexpr int kDSets = BT == 16 ? 4 : 2;
     static constexpr uint32_t kA0 = static_cast<uint32_t>(kDSets) * 2u * kNmma;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kNumBars = 3 * kRawStages + kOpStages + 2 * kAuxStages + 2 * kDSets + 1 + 1;
+    static constexpr int kNumBars = 3 * kRawStages + kOpStages + 2 * kAuxStages + 2 * kDSets + 1 + 1 + 1;
     // Tile output staging: int32 [BT][128] (a split tile's partials, or the
     // slot read back for the fix-up), an 8 KB zero block that re-zeroes
     // slots, and fp16 [BT][128] outputs; all moved by bulk copies.
     static constexpr uint32_t kStgI32Bytes = static_cast<uint32_t>(BT) * kTileN * 4u;
     static constexpr uint32_t kZeroBytes = 8192;
     static constexpr uint32_t kOutBytes = static_cast<uint32_t>(BT) * kTileN * 2u;
-    static constexpr uint32_t kEpiRegion = kStgI32Bytes + kZeroBytes + kOutBytes;
+    // ... and an int32 [BT][128] buffer into which the prefetch warp loads
+    // the slot of the split tile this CTA finishes.
+    static constexpr uint32_t kPreOff = kStgI32Bytes + kZeroBytes + kOutBytes;
+    static constexpr uint32_t kEpiRegion = kPreOff + kStgI32Bytes;
     static constexpr uint32_t kMiscBytes = 2048;
     static constexpr uint32_t kSmemBytes =
         kRawStages * kRawSlotBytes + kAuxStages * kAuxStageBytes + kEpiRegion + kMiscBytes + 1024;
@@ -160,11 +163,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     uint64_t *d_empty = d_full + DS;
     uint64_t *mma_done = d_empty + DS;
     uint64_t *fix_bar = mma_done + 1;  // slot rows landed in the int32 staging (fix-up)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fix_bar + 1);
+    uint64_t *pre_bar = fix_bar + 1;   // slot rows landed in the prefetch buffer
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pre_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *hdr_ok = abort_flag + 1;
     volatile int *is_last = abort_flag + 2;
     volatile int *fin_flag = abort_flag + 3;
+    // 0: open; 1: the prefetch warp has loaded (or is loading) the finished
+    // tile's slot; 2: the drain has decided without it.  Changed by atomicCAS.
+    int *pre_state = const_cast<int *>(abort_flag + 4);
     float *tile_sx = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(bars) + 1024);
     int *tile_tx = reinterpret_cast<int *>(tile_sx + 128);
 
@@ -182,6 +189,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         *hdr_ok = ok ? 1 : 0;
         *abort_flag = 0;
         *is_last = 0;
+        *pre_state = 0;
         for (int i = 0; i < R; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], kF8ConvWarps + 1);  // one converter group + the MMA commit
@@ -198,6 +206,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
         mbar_init(mma_done, 2);  // one commit per issuing thread
         mbar_init(fix_bar, 1);
+        mbar_init(pre_bar, 1);
         fence_barrier_init();
     }
     // The zero block is read by bulk copies (async proxy).
@@ -327,6 +336,46 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             // All of this thread's MMAs must finish before TMEM is released.
             mma_commit(mma_done);
             mbar_wait(mma_done, 0, nullptr, p.status, tmo);
+        }
+    } else if (run && warp == 3) {
+        // --------------------------------------------- slot prefetch warp --
+        // The split tile this CTA finishes (its range's last segment, when the
+        // tile's first k-stage lies in this range) needs the other
+        // contributors' sums from the tile's slot.  They publish them at the
+        // start of their own ranges, usually long before this CTA reaches the
+        // tile's end, so this warp polls the arrival counter and, once it is
+        // complete, loads the slot into the prefetch buffer: the drain then
+        // finishes the tile with neither a counter read nor a load on its
+        // path.  pre_state (compare-and-swap) makes either this load or the
+        // drain's own decision happen, never both.
+        if (lane == 0 && !(p.debug_flags & kDebugAlwaysPublish)) {
+            SegmentWalker w(p, cta);
+            Segment sg, last{0, 0, 0};
+            while (w.next(sg)) last = sg;
+            const bool split = last.k1 > last.k0 && !(last.k0 == 0 && last.k1 == p.G);
+            const uint32_t tfirst = static_cast<uint32_t>(last.tile) * static_cast<uint32_t>(p.G);
+            if (split && cta_of_stage(tfirst, p) == cta) {
+                griddep_wait();  // the workspace belongs to the preceding kernel until it completes
+                const uint32_t others = static_cast<uint32_t>(
+                    cta_of_stage(tfirst + static_cast<uint32_t>(p.G) - 1u, p) - cta);
+                const uint64_t t0 = globaltimer_ns();
+                bool ready = false;
+                while (*abort_flag == 0 && abort_flag[4] == 0 && globaltimer_ns() - t0 < tmo) {
+                    if (ld_acquire_gpu_u32(p.counters + cta) == others) {
+                        ready = true;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+                if (ready && atomicCAS(pre_state, 0, 1) == 0) {
+                    const int32_t *slot = p.slots + static_cast<size_t>(cta) * (BT * kTileN);
+                    fence_proxy_async_global();  // the counter acquire orders the load below
+                    mbar_arrive_expect_tx(pre_bar, C::kStgI32Bytes);
+                    tma_load_1d(epi_base + C::kPreOff, slot, C::kStgI32Bytes, pre_bar);
+                    // Never left in flight at exit (the load reads the workspace).
+                    mbar_wait(pre_bar, 0u, nullptr, p.status, tmo);
+                }
+            }
         }
     } else if (run && ((warp >= 4 && warp < 8) || warp >= 16)) {
         // ---------------------------------------------- converter warps --
@@ -534,12 +583,21 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 named_bar_sync(3, kF8EpiThreads);
                 if (et == 0) {
                     int f = 0;
-                    if (*abort_flag == 0 && !(p.debug_flags & kDebugAlwaysPublish))
-                        f = finish_directly(p, cta, slot_idx, tfirst, abort_flag) ? 1 : 0;
+                    if (*abort_flag == 0 && !(p.debug_flags & kDebugAlwaysPublish)) {
+                        // The tile's first k-stage is in this range only for the
+                        // range's last segment.  If the prefetch warp already
+                        // found every other partial published, its buffer holds
+                        // the slot (f = 2); otherwise the claim stops it.
+                        if (slot_idx == cta && atomicCAS(pre_state, 0, 2) == 1)
+                            f = 2;
+                        else
+                            f = finish_directly(p, cta, slot_idx, tfirst, abort_flag) ? 1 : 0;
+                    }
                     *fin_flag = f;
                 }
                 named_bar_sync(3, kF8EpiThreads);
-                const bool fin = *fin_flag != 0;
+                const int fmode = *fin_flag;
+                const bool fin = fmode != 0;
                 bool do_fix = fin;
                 if (!fin) {
                     // Publish: the [BT][128] int32 partial (contiguous in the
@@ -575,20 +633,27 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     // Fix-up: the slot's sums (one bulk load) plus, when finishing
                     // directly, this CTA's own partial; then fp16 outputs, the
                     // slot re-zeroed and the counter reset.
-                    if (et == 0) {
-                        bulk_wait_read<0>();         // the staging buffers are no longer read
-                        fence_proxy_async_global();  // the counter acquire orders the load below
-                        mbar_arrive_expect_tx(fix_bar, C::kStgI32Bytes);
-                        tma_load_1d(epi_base, slot, C::kStgI32Bytes, fix_bar);
+                    uint32_t src = stg;
+                    if (fmode == 2) {
+                        // Loaded by the prefetch warp (the load always completes).
+                        mbar_wait_warp(pre_bar, 0u, nullptr, p.status, tmo);
+                        src = smem_u32(epi_base + C::kPreOff);
+                    } else {
+                        if (et == 0) {
+                            bulk_wait_read<0>();         // the staging buffers are no longer read
+                            fence_proxy_async_global();  // the counter acquire orders the load below
+                            mbar_arrive_expect_tx(fix_bar, C::kStgI32Bytes);
+                            tma_load_1d(epi_base, slot, C::kStgI32Bytes, fix_bar);
+                        }
+                        // The load always completes (it reads the workspace), so this
+                        // wait ignores the abort flag: it is never left in flight.
+                        mbar_wait_warp(fix_bar, fix_n & 1u, nullptr, p.status, tmo);
+                        ++fix_n;
                     }
-                    // The load always completes (it reads the workspace), so this
-                    // wait ignores the abort flag: it is never left in flight.
-                    mbar_wait_warp(fix_bar, fix_n & 1u, nullptr, p.status, tmo);
-                    ++fix_n;
                     int tot[HT];
 #pragma unroll
                     for (int i = 0; i < HT; ++i)
-                        tot[i] = ld_shared_s32(stg + 4u * ((hs * HT + i) * kTileN + row)) + (fin ? acc[i] : 0);
+                        tot[i] = ld_shared_s32(src + 4u * ((hs * HT + i) * kTileN + row)) + (fin ? acc[i] : 0);
                     if (p.acc_out) {
 #pragma unroll
                         for (int i = 0; i < HT; ++i) {
