@@ -10,11 +10,13 @@
 // GB300 design (sm_103a has no tcgen05 INT8 MMA, so the exact integer
 // product runs on the fp16 tensor-core path):
 //  * swap-AB: the MMA's M = 128 weight rows, its N = BT tokens (16..128);
-//  * one warp streams each stage with TMA: one bulk copy of the packed 8 KB
-//    weight block (+ 512 B of group metadata) and two 2D tensor copies of the
+//  * two warps stream the stages with TMA into two rings: warp 0 one bulk
+//    copy of the packed 8 KB weight block (+ 512 B of group metadata) per
+//    stage into a deep weight ring, without waiting for the preceding
+//    kernel; warp 3, after that wait, two 2D tensor copies of the
 //    activation operand (Qx as exact fp16, written by the activation
 //    quantizer or by a preparation kernel) straight into the MMA's B layout
-//    (128-byte swizzle, rows past M zero-filled);
+//    (128-byte swizzle, rows past M zero-filled) in a shorter ring;
 //  * 8 converter warps turn weight codes into fp16 operands in registers
 //    with byte-lane SIMD: one 32-bit multiply-add per 4 weights yields
 //    (q4 - z) * s_g + 128 in each byte (legal because the protective range
@@ -60,17 +62,21 @@ struct Cfg {
     // operand slots of 64 columns (128 lanes x 64 columns = 128 rows x 128 k
     // each) from kA0.
     static constexpr int kOpStages = BT == 128 ? 2 : 4;
-    static constexpr int kRawStages = BT == 16 ? 12 : (BT == 32 ? 10 : (BT == 64 ? 7 : 4));
+    // Two rings of TMA stages: packed weight blocks (kWStages slots of
+    // kWRawBytes, released by the converters once read into registers) and
+    // the B operand (kBStages slots, released by the MMAs' commit).  The
+    // weight ring runs far ahead of the MMAs to cover HBM latency; the
+    // activation operand comes from L2.
+    static constexpr int kWStages = BT == 128 ? 10 : (BT == 64 ? 12 : 14);
+    static constexpr int kBStages = BT == 16 ? 8 : (BT == 32 ? 6 : (BT == 64 ? 4 : 3));
     static constexpr uint32_t kChunk0 = static_cast<uint32_t>(BT);
     static constexpr uint32_t kA0 = ((kChunk0 + 2 * BT + 63) / 64) * 64;
     static constexpr uint32_t kTmemCols = 512;
-    // Raw slot: [B operand: two 128-byte-swizzled atoms of BT rows x 64 fp16
-    // (k 0..63, k 64..127), landed by TMA from the fp16 activation operand]
-    // [packed weight block (+ group metadata)].
+    // B slot: two 128-byte-swizzled atoms of BT rows x 64 fp16 (k 0..63,
+    // k 64..127), landed by TMA from the fp16 activation operand.
     static constexpr uint32_t kBAtom = static_cast<uint32_t>(BT) * 128u;
     static constexpr uint32_t kBBytes = 2 * kBAtom;
-    static constexpr uint32_t kRawSlotBytes = kBBytes + kWRawBytes;
-    static constexpr int kNumBars = 3 * kRawStages + 2 * kOpStages + 4 + 1 + 2;
+    static constexpr int kNumBars = 2 * kWStages + 2 * kBStages + 2 * kOpStages + 4 + 1 + 2;
     // Epilogue staging: two 8 KB buffers (16 tokens x 128 rows of int32
     // partials or fp16 outputs, written by the epilogue threads and sent out
     // by one bulk copy each; during a split-tile fix-up they receive slot rows
@@ -79,9 +85,10 @@ struct Cfg {
     static constexpr uint32_t kStgBytes = 8192;
     static constexpr uint32_t kStgRegion = 4 * kStgBytes;
     static constexpr uint32_t kMiscBytes = 2048;  // barriers + flags, then s_x / t_x of the current tile
-    static constexpr uint32_t kSmemBytes = kRawStages * kRawSlotBytes + kStgRegion + kMiscBytes + 1024;
+    static constexpr uint32_t kSmemBytes =
+        kBStages * kBBytes + kWStages * kWRawBytes + kStgRegion + kMiscBytes + 1024;
     static_assert(kA0 + 64 * kOpStages <= kTmemCols, "TMEM columns");
-    static_assert(kRawSlotBytes % 1024 == 0 && kBAtom % 1024 == 0, "1 KB aligned swizzled atoms");
+    static_assert(kWRawBytes % 1024 == 0 && kBAtom % 1024 == 0, "1 KB aligned swizzled atoms");
     static_assert(kNumBars * 8 + 64 <= 1024, "barrier area (the tile scales start at +1024)");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -103,24 +110,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     w4a8_gemm_kernel(const __grid_constant__ CUtensorMap qx_map, const __grid_constant__ CUtensorMap o_map,
                      const GemmParams p) {
     using C = Cfg<BT>;
-    constexpr int R = C::kRawStages;
+    constexpr int RW = C::kWStages;
+    constexpr int RB = C::kBStages;
     constexpr int OPS = C::kOpStages;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *raw_base = smem;
-    uint8_t *stg_base = raw_base + R * C::kRawSlotBytes;        // 2 staging buffers, then the zero block
+    uint8_t *b_base = smem;                                      // B operand ring
+    uint8_t *w_base = b_base + RB * C::kBBytes;                  // weight ring
+    uint8_t *stg_base = w_base + RW * kWRawBytes;                // 2 staging buffers, then the zero block
     uint64_t *bars = reinterpret_cast<uint64_t *>(stg_base + C::kStgRegion);
-    uint64_t *raw_full = bars;
-    uint64_t *raw_empty = bars + R;
-    uint64_t *op_full = bars + 2 * R;
+    uint64_t *w_full = bars;
+    uint64_t *w_empty = w_full + RW;
+    uint64_t *b_full = w_empty + RW;
+    uint64_t *b_empty = b_full + RB;
+    uint64_t *op_full = b_empty + RB;
     uint64_t *op_empty = op_full + OPS;
     uint64_t *chunk_full = op_empty + OPS;
     uint64_t *chunk_empty = chunk_full + 2;
     uint64_t *mma_done = chunk_empty + 2;
     uint64_t *fix_bar = mma_done + 1;  // [2]: slot rows landed in staging buffer 0 / 1
-    uint64_t *act_full = fix_bar + 2;  // [R]: the B operand of a raw slot landed (raw_full: its weights)
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(act_full + R);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fix_bar + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *hdr_ok = abort_flag + 1;
     volatile int *is_last = abort_flag + 2;
@@ -142,10 +152,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         *hdr_ok = ok ? 1 : 0;
         *abort_flag = 0;
         *is_last = 0;
-        for (int i = 0; i < R; ++i) {
-            mbar_init(&raw_full[i], 1);
-            mbar_init(&raw_empty[i], kConvGroupWarps + 1);  // converter group + the MMA commit (B operand)
-            mbar_init(&act_full[i], 1);
+        for (int i = 0; i < RW; ++i) {
+            mbar_init(&w_full[i], 1);
+            mbar_init(&w_empty[i], kConvGroupWarps);  // the converter group of the stage
+        }
+        for (int i = 0; i < RB; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);  // the MMA commit of the stage
         }
         for (int i = 0; i < OPS; ++i) {
             mbar_init(&op_full[i], kConvGroupWarps);
@@ -176,65 +189,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (run && warp == 0) {
-        // ------------------------------------------------ TMA producer --
+        // ------------------------------------------- weight TMA producer --
+        // Weight blocks are never written by a preceding kernel, so this
+        // producer does not wait for the launch dependency: under launch
+        // overlap its first RW stages stream in while the preceding kernel
+        // finishes.
         if (lane == 0) {
-            // Before the dependency wait (programmatic dependent launch): the
-            // weight blocks of the first R stages, which no preceding kernel
-            // writes.  Each stage's barrier is armed for all its bytes; its
-            // activation copies follow after the wait.
             const bool withhold = (p.debug_flags & kDebugWithholdStage) != 0;
-            const int pre_max = withhold ? 1 : R;
-            int pre = 0;
-            {
-                SegmentWalker w0(p, cta);
-                Segment s0;
-                while (pre < pre_max && w0.next(s0)) {
-                    const int n_tile = s0.tile / p.tok_tiles;
-                    const uint8_t *wblk = p.packed + kHeaderBytes + (static_cast<size_t>(n_tile) * p.G) * bb;
-                    for (int k = s0.k0; k < s0.k1 && pre < pre_max; ++k, ++pre) {
-                        uint8_t *dst = raw_base + pre * C::kRawSlotBytes;
-                        mbar_arrive_expect_tx(&raw_full[pre], bb);
-                        tma_load_1d(dst + C::kBBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[pre]);
-                    }
-                }
-            }
-            griddep_wait();
             SegmentWalker walk(p, cta);
             Segment sg;
             int st = 0, issued = 0;
             bool stop = false;
             while (!stop && walk.next(sg)) {
-                const int tok_tile = sg.tile % p.tok_tiles, n_tile = sg.tile / p.tok_tiles;
+                const int n_tile = sg.tile / p.tok_tiles;
                 const uint8_t *wblk = p.packed + kHeaderBytes + (static_cast<size_t>(n_tile) * p.G) * bb;
                 for (int k = sg.k0; k < sg.k1; ++k, ++st) {
-                    const int slot = st % R, use = st / R;
-                    if (use > 0 && !mbar_wait(&raw_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo)) {
-                        stop = true;
-                        break;
-                    }
+                    const int slot = st % RW, use = st / RW;
                     if (withhold && st == 1) {
                         stop = true;
                         break;
                     }
-                    uint8_t *dst = raw_base + slot * C::kRawSlotBytes;
-                    if (st >= pre) {
-                        mbar_arrive_expect_tx(&raw_full[slot], bb);
-                        tma_load_1d(dst + C::kBBytes, wblk + static_cast<size_t>(k) * bb, bb, &raw_full[slot]);
+                    if (use > 0 && !mbar_wait(&w_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo)) {
+                        stop = true;
+                        break;
                     }
-                    mbar_arrive_expect_tx(&act_full[slot], C::kBBytes);
-                    tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &act_full[slot]);
-                    tma_load_2d(dst + C::kBAtom, &qx_map, k * kTileK + 64, tok_tile * BT, &act_full[slot]);
+                    mbar_arrive_expect_tx(&w_full[slot], bb);
+                    tma_load_1d(w_base + slot * kWRawBytes, wblk + static_cast<size_t>(k) * bb, bb, &w_full[slot]);
                     issued = st + 1;
                 }
             }
             // Drain: every issued copy must land before the CTA exits.
-            for (int t = (issued > R ? issued - R : 0); t < issued; ++t) {
-                mbar_wait(&raw_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
-                mbar_wait(&act_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
+            for (int t = (issued > RW ? issued - RW : 0); t < issued; ++t)
+                mbar_wait(&w_full[t % RW], (t / RW) & 1, nullptr, p.status, tmo);
+        }
+    } else if (run && warp == 3) {
+        // ------------------------------------- activation TMA producer --
+        if (lane == 0) {
+            griddep_wait();  // the activation operand may be written by the preceding kernel
+            SegmentWalker walk(p, cta);
+            Segment sg;
+            int st = 0, issued = 0;
+            bool stop = false;
+            while (!stop && walk.next(sg)) {
+                const int tok_tile = sg.tile % p.tok_tiles;
+                for (int k = sg.k0; k < sg.k1; ++k, ++st) {
+                    const int slot = st % RB, use = st / RB;
+                    if (use > 0 && !mbar_wait(&b_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo)) {
+                        stop = true;
+                        break;
+                    }
+                    uint8_t *dst = b_base + slot * C::kBBytes;
+                    mbar_arrive_expect_tx(&b_full[slot], C::kBBytes);
+                    tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &b_full[slot]);
+                    tma_load_2d(dst + C::kBAtom, &qx_map, k * kTileK + 64, tok_tile * BT, &b_full[slot]);
+                    issued = st + 1;
+                }
             }
-            // Weight blocks issued before the dependency wait for stages the
-            // walk never reached (it stopped early) must land as well.
-            for (int t = issued; t < pre; ++t) mbar_wait(&raw_full[t % R], (t / R) & 1, nullptr, p.status, tmo);
+            for (int t = (issued > RB ? issued - RB : 0); t < issued; ++t)
+                mbar_wait(&b_full[t % RB], (t / RB) & 1, nullptr, p.status, tmo);
         }
     } else if (run && (warp == 1 || warp == 2)) {
         // ------------------------------------------------ MMA issuers --
@@ -280,14 +292,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         const uint32_t d_tmem = tmem + C::kChunk0 + static_cast<uint32_t>((cur & 1) * BT);
                         const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u;
-                        const uint32_t b_base = smem_u32(raw_base + (st % R) * C::kRawSlotBytes);
+                        const uint32_t b_slot = smem_u32(b_base + (st % RB) * C::kBBytes);
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t bd = desc_kmajor_sw128(b_base + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
+                            const uint64_t bd = desc_kmajor_sw128(b_slot + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
                             mma_f16_tmem_a(d_tmem, a_tmem + 8u * kk, bd, idesc, 1u);
                         }
                         mma_commit(&op_empty[os]);
-                        mma_commit(&raw_empty[st % R]);
+                        mma_commit(&b_empty[st % RB]);
                     }
                     if (last) mma_commit(&chunk_full[cur & 1]);
                 }
@@ -312,12 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (!stop && walk.next(sg)) {
             for (int k = sg.k0; k < sg.k1; ++k, ++st) {
                 if ((st & 1) != cg) continue;
-                const int rs = st % R, ruse = st / R, os = st % OPS, ouse = st / OPS;
-                if (!mbar_wait_warp(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo)) {
+                const int ws = st % RW, wuse = st / RW, bs = st % RB, buse = st / RB;
+                const int os = st % OPS, ouse = st / OPS;
+                if (!mbar_wait_warp(&w_full[ws], wuse & 1, abort_flag, p.status, tmo)) {
                     stop = true;
                     break;
                 }
-                const uint32_t wraw = smem_u32(raw_base + rs * C::kRawSlotBytes) + C::kBBytes;
+                const uint32_t wraw = smem_u32(w_base + ws * kWRawBytes);
 
                 // Weights: row wr, 4 raw chunks of 32 k -> 128 fp16 -> 64 TMEM
                 // columns of this thread's lane (2 fp16 per column).  The whole
@@ -352,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_empty[rs]);  // this warp is done reading the raw slot
+                if (lane == 0) mbar_arrive(&w_empty[ws]);  // this warp is done reading the weight slot
                 if (ouse > 0 && !mbar_wait_warp(&op_empty[os], (ouse - 1) & 1, abort_flag, p.status, tmo)) {
                     stop = true;
                     break;
@@ -366,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The B operand of this stage, copied after the dependency
                 // wait, must have landed before the MMAs (ordered after
                 // op_full) read it; the weights were converted without it.
-                if (!mbar_wait_warp(&act_full[rs], ruse & 1, abort_flag, p.status, tmo)) {
+                if (!mbar_wait_warp(&b_full[bs], buse & 1, abort_flag, p.status, tmo)) {
                     stop = true;
                     break;
                 }
