@@ -88,6 +88,10 @@ struct Cfg {
     static constexpr uint32_t kSmemBytes =
         kBStages * kBBytes + kWStages * kWRawBytes + kStgRegion + kMiscBytes + 1024;
     static_assert(kA0 + 64 * kOpStages <= kTmemCols, "TMEM columns");
+    // The converter groups and the MMA issuers alternate stages; with even
+    // depths every weight slot and operand slot is waited on by one group (or
+    // one issuer) in stage order, which keeps their parity waits exact.
+    static_assert(kWStages % 2 == 0 && kOpStages % 2 == 0, "even weight-ring and operand-slot depths");
     static_assert(kWRawBytes % 1024 == 0 && kBAtom % 1024 == 0, "1 KB aligned swizzled atoms");
     static_assert(kNumBars * 8 + 64 <= 1024, "barrier area (the tile scales start at +1024)");
     static_assert(kSmemBytes <= 232448, "shared memory");
@@ -379,7 +383,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The B operand of this stage, copied after the dependency
                 // wait, must have landed before the MMAs (ordered after
                 // op_full) read it; the weights were converted without it.
-                if (!mbar_wait_warp(&b_full[bs], buse & 1, abort_flag, p.status, tmo)) {
+                // A parity wait is exact only once the slot's previous phase
+                // has completed: with an odd ring depth the previous use of
+                // this B slot belongs to the other converter group, which
+                // this one may have overtaken, so first wait for that use's
+                // MMA commit (it follows the previous b_full phase).  With an
+                // even depth the same group waited for it and this returns
+                // at once.
+                if ((buse > 0 && !mbar_wait_warp(&b_empty[bs], (buse - 1) & 1, abort_flag, p.status, tmo)) ||
+                    !mbar_wait_warp(&b_full[bs], buse & 1, abort_flag, p.status, tmo)) {
                     stop = true;
                     break;
                 }

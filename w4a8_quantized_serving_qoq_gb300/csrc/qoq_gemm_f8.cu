@@ -395,7 +395,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 const int rs = st % R, ruse = st / R, os = st % OPS, as = st % AUX, ause = st / AUX;
                 // aux_empty of this slot means the drain finished stage st - AUX,
                 // whose MMAs therefore completed: TMEM A slot os is free as well.
-                if (!mbar_wait_warp(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo) ||
+                // A parity wait is exact only once the slot's previous phase has
+                // completed; with an odd ring depth the previous use of this raw
+                // slot belongs to the other converter group, so first wait for
+                // its release (raw_empty, which follows both of its fill phases).
+                if ((ruse > 0 && !mbar_wait_warp(&raw_empty[rs], (ruse - 1) & 1, abort_flag, p.status, tmo)) ||
+                    !mbar_wait_warp(&raw_full[rs], ruse & 1, abort_flag, p.status, tmo) ||
                     (ause > 0 && !mbar_wait_warp(&aux_empty[as], (ause - 1) & 1, abort_flag, p.status, tmo))) {
                     stop = true;
                     break;
