@@ -238,7 +238,10 @@ def test_gemm_tiles_and_stream_k_splits(bt, ctas, publish):
 
 
 FP8_CASES = [(1, 256, 512), (3, 128, 384), (8, 384, 1024), (16, 256, 896), (17, 128, 640), (31, 256, 256),
-             (32, 128, 1152)]
+             (32, 128, 1152),
+             # several 32-token tiles (the planner's choice for M <= 64 when a
+             # launch has few k-stages per CTA), ragged last tile
+             (48, 256, 512), (64, 128, 384), (100, 128, 640)]
 
 
 @pytest.mark.parametrize("M,N,K", FP8_CASES)

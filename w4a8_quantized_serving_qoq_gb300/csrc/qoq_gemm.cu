@@ -748,6 +748,23 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
     if (path == 0) path = (group == 128 && M <= 32) ? kPathF8 : kPathF16;
     if (group != 128) path = kPathF16;
     int bt = force_bt;
+    if (force_path == 0 && force_bt == 0 && M > 32 && num_sms > 0) {
+        // Few k-stages per CTA at the natural tile (64 tokens up to M = 64,
+        // else 128): half-width token tiles double the work units, which
+        // balances the stream-K ranges and halves each split tile's fix-up;
+        // measured faster up to 12 stages per CTA (Llama-3-8B qkv and o at
+        // M = 64 and 128), slower from 13.5 (o at M = 256).
+        const long long nat = M <= 64 ? 64 : 128;
+        const long long stages = (M + nat - 1) / nat * (N / kTileN) * static_cast<long long>(K / kTileK);
+        if (stages <= 12LL * num_sms) {
+            if (M <= 64 && group == 128) {
+                path = kPathF8;
+                bt = 32;
+            } else if (M > 64) {
+                bt = 64;
+            }
+        }
+    }
     if (path == kPathF8) {
         if (bt != 16 && bt != 32) bt = M <= 16 ? 16 : 32;
     } else if (bt == 0) {
