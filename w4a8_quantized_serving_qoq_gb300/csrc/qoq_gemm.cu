@@ -778,6 +778,19 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
     pl.tiles = static_cast<long long>(pl.tok_tiles) * pl.n_tiles;
     pl.total = pl.tiles * pl.G;
     long long ctas = force_ctas > 0 ? force_ctas : num_sms;
+    if (force_ctas <= 0 && num_sms > 16) {
+        if (pl.tiles <= num_sms && pl.tiles * 5 >= static_cast<long long>(num_sms) * 3) {
+            // The tiles fill at least 60 % of one wave: one whole tile per CTA
+            // (no split tiles, no fix-ups) beats stream-K over every SM.
+            ctas = pl.tiles;
+        } else if (M <= 32) {
+            // Decode sizes: leave 8 SMs free so that the first CTAs of the
+            // kernel launched behind this one (typically the next layer's
+            // activation quantizer, one CTA per token) start at once
+            // instead of waiting for this GEMM's CTAs to leave.
+            ctas = num_sms - 8;
+        }
+    }
     if (ctas > pl.total) ctas = pl.total;
     pl.ctas = static_cast<int>(ctas);
     pl.counters_offset = kWsStatusBytes;
