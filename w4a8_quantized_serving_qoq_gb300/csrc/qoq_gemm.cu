@@ -25,9 +25,10 @@
 //  * two threads issue tcgen05.mma on alternate stages (kind::f16, fp32
 //    accumulation in TMEM).  Operands are integers with |product| <= 127 *
 //    128, so an fp32 sum over 1024 k (8 stages) stays below 2^24 and is exact
-//    in any order; each 1024-k chunk is drained by the epilogue warps into an
-//    int32 running sum kept in TMEM, which also hand the chunk buffer back
-//    zeroed (two chunk buffers so the MMAs never wait on the drain);
+//    in any order; each 1024-k chunk is drained by the epilogue warps into
+//    int32 sums held in their registers (one weight row per thread, all BT
+//    tokens), which also hand the chunk buffer back zeroed at once (two chunk
+//    buffers so the MMAs never wait on the drain);
 //  * epilogue: int32 result (per-channel: minus z[n] * t_x[m]) scaled by
 //    s_x[m] * s_w[n] in fp32 and rounded to fp16, staged in shared memory 16
 //    tokens at a time and written by a tensor bulk store; with a K split, the
@@ -57,11 +58,11 @@ constexpr uint32_t kWRawBytes = 9216;  // 8704 B block slot rounded to 1 KB
 
 template <int BT>
 struct Cfg {
-    // TMEM columns: [0, BT) int32 running sum, then two fp32 chunk
-    // accumulators of BT columns from kChunk0, then kOpStages fp16 weight
-    // operand slots of 64 columns (128 lanes x 64 columns = 128 rows x 128 k
-    // each) from kA0.
-    static constexpr int kOpStages = BT == 128 ? 2 : 4;
+    // TMEM columns: two fp32 chunk accumulators of BT columns from kChunk0
+    // (the int32 sums live in the epilogue threads' registers), then
+    // kOpStages fp16 weight operand slots of 64 columns (128 lanes x 64
+    // columns = 128 rows x 128 k each) from kA0.
+    static constexpr int kOpStages = 4;
     // Two rings of TMA stages: packed weight blocks (kWStages slots of
     // kWRawBytes, released by the converters once read into registers) and
     // the B operand (kBStages slots, released by the MMAs' commit).  The
@@ -69,9 +70,17 @@ struct Cfg {
     // activation operand comes from L2.
     static constexpr int kWStages = BT == 128 ? 10 : (BT == 64 ? 12 : 14);
     static constexpr int kBStages = BT == 16 ? 8 : (BT == 32 ? 6 : (BT == 64 ? 4 : 3));
-    static constexpr uint32_t kChunk0 = static_cast<uint32_t>(BT);
+    static constexpr uint32_t kChunk0 = 0;
     static constexpr uint32_t kA0 = ((kChunk0 + 2 * BT + 63) / 64) * 64;
     static constexpr uint32_t kTmemCols = 512;
+    // Registers per thread by warpgroup for BT >= 64 (the epilogue holds BT
+    // int32 sums per thread): warps 0-3 (TMA producers, MMA issuers) give up
+    // registers to warps 4-7 (epilogue); the converters keep the launch
+    // allocation.  128 x 80 + 128 x 176 + 256 x 128 = 512 x 128, the launch
+    // allocation, which the host checks before the first launch.
+    static constexpr bool kRegSplit = BT >= 64;
+    static constexpr uint32_t kRegLow = 80, kRegEpi = 176, kRegLaunch = 128;
+    static_assert(128 * kRegLow + 128 * kRegEpi + 256 * kRegLaunch == 512 * kRegLaunch, "register split");
     // B slot: two 128-byte-swizzled atoms of BT rows x 64 fp16 (k 0..63,
     // k 64..127), landed by TMA from the fp16 activation operand.
     static constexpr uint32_t kBAtom = static_cast<uint32_t>(BT) * 128u;
@@ -97,6 +106,19 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
+// int32 test output of one block of 16 tokens for this thread's weight row:
+// the values were stored to this thread's own slots (token i at 4*(i*128+et))
+// of the buffer at buf; one rolled loop keeps the epilogue's code small.
+__device__ __forceinline__ void write_block_i32(const GemmParams &p, uint32_t buf, int m0j, int n, int zc,
+                                             const float *sx16, const int *tx16, float sw, bool live) {
+    const int et = static_cast<int>(threadIdx.x) - 128;
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) {
+        const int m = m0j + i;
+        if (live && m < p.M) write_out(p, m, n, ld_shared_s32(buf + 4u * (i * kTileN + et)), zc, tx16[i], sx16[i], sw);
+    }
+}
+
 // Four INT8 / biased bytes -> two fp16x2 words holding the signed values.
 // Input byte b is v + 128 (v in [-128, 127]); 0x64XX is the fp16 1024 + XX.
 __device__ __forceinline__ void biased_bytes_to_f16x4(uint32_t u, uint32_t &lo, uint32_t &hi) {
@@ -109,7 +131,9 @@ __device__ __forceinline__ void biased_bytes_to_f16x4(uint32_t u, uint32_t &lo, 
     hi = *reinterpret_cast<const uint32_t *>(&hb);
 }
 
-template <int BT>
+// kAccOut: the int32 test output (GemmParams::acc_out) instead of fp16 O.  A
+// separate instantiation, so that the fp16 kernel carries no code for it.
+template <int BT, bool kAccOut>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_gemm_kernel(const __grid_constant__ CUtensorMap qx_map, const __grid_constant__ CUtensorMap o_map,
                      const GemmParams p) {
@@ -192,127 +216,391 @@ __global__ void __launch_bounds__(kThreads, 1)
         atomicOr(p.status, kStatusBadPacked);
     }
 
-    if (run && warp == 0) {
-        // ------------------------------------------- weight TMA producer --
-        // Weight blocks are never written by a preceding kernel, so this
-        // producer does not wait for the launch dependency: under launch
-        // overlap its first RW stages stream in while the preceding kernel
-        // finishes.
-        if (lane == 0) {
-            const bool withhold = (p.debug_flags & kDebugWithholdStage) != 0;
-            SegmentWalker walk(p, cta);
-            Segment sg;
-            int st = 0, issued = 0;
-            bool stop = false;
-            while (!stop && walk.next(sg)) {
-                const int n_tile = sg.tile / p.tok_tiles;
-                const uint8_t *wblk = p.packed + kHeaderBytes + (static_cast<size_t>(n_tile) * p.G) * bb;
-                for (int k = sg.k0; k < sg.k1; ++k, ++st) {
-                    const int slot = st % RW, use = st / RW;
-                    if (withhold && st == 1) {
-                        stop = true;
-                        break;
-                    }
-                    if (use > 0 && !mbar_wait(&w_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo)) {
-                        stop = true;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&w_full[slot], bb);
-                    tma_load_1d(w_base + slot * kWRawBytes, wblk + static_cast<size_t>(k) * bb, bb, &w_full[slot]);
-                    issued = st + 1;
-                }
-            }
-            // Drain: every issued copy must land before the CTA exits.
-            for (int t = (issued > RW ? issued - RW : 0); t < issued; ++t)
-                mbar_wait(&w_full[t % RW], (t / RW) & 1, nullptr, p.status, tmo);
-        }
-    } else if (run && warp == 3) {
-        // ------------------------------------- activation TMA producer --
-        if (lane == 0) {
-            griddep_wait();  // the activation operand may be written by the preceding kernel
-            SegmentWalker walk(p, cta);
-            Segment sg;
-            int st = 0, issued = 0;
-            bool stop = false;
-            while (!stop && walk.next(sg)) {
-                const int tok_tile = sg.tile % p.tok_tiles;
-                for (int k = sg.k0; k < sg.k1; ++k, ++st) {
-                    const int slot = st % RB, use = st / RB;
-                    if (use > 0 && !mbar_wait(&b_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo)) {
-                        stop = true;
-                        break;
-                    }
-                    uint8_t *dst = b_base + slot * C::kBBytes;
-                    mbar_arrive_expect_tx(&b_full[slot], C::kBBytes);
-                    tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &b_full[slot]);
-                    tma_load_2d(dst + C::kBAtom, &qx_map, k * kTileK + 64, tok_tile * BT, &b_full[slot]);
-                    issued = st + 1;
-                }
-            }
-            for (int t = (issued > RB ? issued - RB : 0); t < issued; ++t)
-                mbar_wait(&b_full[t % RB], (t / RB) & 1, nullptr, p.status, tmo);
-        }
-    } else if (run && (warp == 1 || warp == 2)) {
-        // ------------------------------------------------ MMA issuers --
-        // Two threads take alternate stages (warp 1 even, warp 2 odd): a
-        // barrier wait issued after a thread's own MMAs queues behind them,
-        // so with one issuer every wait idled the tensor pipe.  Their MMAs
-        // into a chunk buffer have no mutual order, so none of them clears
-        // the accumulator: the epilogue hands out every chunk buffer zeroed,
-        // and each issuer commits to chunk_full at every chunk end (the
-        // barrier counts both).  The fp32 partial sums are exact integers,
-        // so the order of the MMAs does not change the result.
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16_f32(128, BT);
-            const int par = warp - 1;
-            SegmentWalker walk(p, cta);
-            Segment sg;
-            int st = 0, gc = 0;
-            bool stop = false;
-            while (!stop && walk.next(sg)) {
-                const int len = sg.k1 - sg.k0;
-                int cur = 0;
-                bool own_in_chunk = false;
-                for (int i = 0; i < len; ++i, ++st) {
-                    const bool first = (i % kChunkStages) == 0;
-                    const bool last = (i % kChunkStages) == kChunkStages - 1 || i == len - 1;
-                    if (first) {
-                        cur = gc++;
-                        own_in_chunk = false;
-                    }
-                    if ((st & 1) == par) {
-                        if (!own_in_chunk) {
-                            own_in_chunk = true;
-                            if (!mbar_wait(&chunk_empty[cur & 1], (cur >> 1) & 1, abort_flag, p.status, tmo)) {
-                                stop = true;
-                                break;
-                            }
-                        }
-                        const int os = st % OPS, ouse = st / OPS;
-                        if (!mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
+    if (warp < 4) {
+        // warpgroup 0: weight producer (warp 0), MMA issuers (1, 2), activation producer (3)
+        if constexpr (C::kRegSplit) setmaxnreg_dec<C::kRegLow>();
+        if (run && warp == 0) {
+            // ------------------------------------------- weight TMA producer --
+            // Weight blocks are never written by a preceding kernel, so this
+            // producer does not wait for the launch dependency: under launch
+            // overlap its first RW stages stream in while the preceding kernel
+            // finishes.
+            if (lane == 0) {
+                const bool withhold = (p.debug_flags & kDebugWithholdStage) != 0;
+                SegmentWalker walk(p, cta);
+                Segment sg;
+                int st = 0, issued = 0;
+                bool stop = false;
+                while (!stop && walk.next(sg)) {
+                    const int n_tile = sg.tile / p.tok_tiles;
+                    const uint8_t *wblk = p.packed + kHeaderBytes + (static_cast<size_t>(n_tile) * p.G) * bb;
+                    for (int k = sg.k0; k < sg.k1; ++k, ++st) {
+                        const int slot = st % RW, use = st / RW;
+                        if (withhold && st == 1) {
                             stop = true;
                             break;
                         }
-                        tc_fence_after();
-                        const uint32_t d_tmem = tmem + C::kChunk0 + static_cast<uint32_t>((cur & 1) * BT);
-                        const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u;
-                        const uint32_t b_slot = smem_u32(b_base + (st % RB) * C::kBBytes);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t bd = desc_kmajor_sw128(b_slot + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
-                            mma_f16_tmem_a(d_tmem, a_tmem + 8u * kk, bd, idesc, 1u);
+                        if (use > 0 && !mbar_wait(&w_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo)) {
+                            stop = true;
+                            break;
                         }
-                        mma_commit(&op_empty[os]);
-                        mma_commit(&b_empty[st % RB]);
+                        mbar_arrive_expect_tx(&w_full[slot], bb);
+                        tma_load_1d(w_base + slot * kWRawBytes, wblk + static_cast<size_t>(k) * bb, bb, &w_full[slot]);
+                        issued = st + 1;
                     }
-                    if (last) mma_commit(&chunk_full[cur & 1]);
+                }
+                // Drain: every issued copy must land before the CTA exits.
+                for (int t = (issued > RW ? issued - RW : 0); t < issued; ++t)
+                    mbar_wait(&w_full[t % RW], (t / RW) & 1, nullptr, p.status, tmo);
+            }
+        } else if (run && warp == 3) {
+            // ------------------------------------- activation TMA producer --
+            if (lane == 0) {
+                griddep_wait();  // the activation operand may be written by the preceding kernel
+                SegmentWalker walk(p, cta);
+                Segment sg;
+                int st = 0, issued = 0;
+                bool stop = false;
+                while (!stop && walk.next(sg)) {
+                    const int tok_tile = sg.tile % p.tok_tiles;
+                    for (int k = sg.k0; k < sg.k1; ++k, ++st) {
+                        const int slot = st % RB, use = st / RB;
+                        if (use > 0 && !mbar_wait(&b_empty[slot], (use - 1) & 1, abort_flag, p.status, tmo)) {
+                            stop = true;
+                            break;
+                        }
+                        uint8_t *dst = b_base + slot * C::kBBytes;
+                        mbar_arrive_expect_tx(&b_full[slot], C::kBBytes);
+                        tma_load_2d(dst, &qx_map, k * kTileK, tok_tile * BT, &b_full[slot]);
+                        tma_load_2d(dst + C::kBAtom, &qx_map, k * kTileK + 64, tok_tile * BT, &b_full[slot]);
+                        issued = st + 1;
+                    }
+                }
+                for (int t = (issued > RB ? issued - RB : 0); t < issued; ++t)
+                    mbar_wait(&b_full[t % RB], (t / RB) & 1, nullptr, p.status, tmo);
+            }
+        } else if (run && (warp == 1 || warp == 2)) {
+            // ------------------------------------------------ MMA issuers --
+            // Two threads take alternate stages (warp 1 even, warp 2 odd): a
+            // barrier wait issued after a thread's own MMAs queues behind them,
+            // so with one issuer every wait idled the tensor pipe.  Their MMAs
+            // into a chunk buffer have no mutual order, so none of them clears
+            // the accumulator: the epilogue hands out every chunk buffer zeroed,
+            // and each issuer commits to chunk_full at every chunk end (the
+            // barrier counts both).  The fp32 partial sums are exact integers,
+            // so the order of the MMAs does not change the result.
+            if (lane == 0) {
+                constexpr uint32_t idesc = idesc_f16_f32(128, BT);
+                const int par = warp - 1;
+                SegmentWalker walk(p, cta);
+                Segment sg;
+                int st = 0, gc = 0;
+                bool stop = false;
+                while (!stop && walk.next(sg)) {
+                    const int len = sg.k1 - sg.k0;
+                    int cur = 0;
+                    bool own_in_chunk = false;
+                    for (int i = 0; i < len; ++i, ++st) {
+                        const bool first = (i % kChunkStages) == 0;
+                        const bool last = (i % kChunkStages) == kChunkStages - 1 || i == len - 1;
+                        if (first) {
+                            cur = gc++;
+                            own_in_chunk = false;
+                        }
+                        if ((st & 1) == par) {
+                            if (!own_in_chunk) {
+                                own_in_chunk = true;
+                                if (!mbar_wait(&chunk_empty[cur & 1], (cur >> 1) & 1, abort_flag, p.status, tmo)) {
+                                    stop = true;
+                                    break;
+                                }
+                            }
+                            const int os = st % OPS, ouse = st / OPS;
+                            if (!mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
+                                stop = true;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t d_tmem = tmem + C::kChunk0 + static_cast<uint32_t>((cur & 1) * BT);
+                            const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u;
+                            const uint32_t b_slot = smem_u32(b_base + (st % RB) * C::kBBytes);
+    #pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t bd = desc_kmajor_sw128(b_slot + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
+                                mma_f16_tmem_a(d_tmem, a_tmem + 8u * kk, bd, idesc, 1u);
+                            }
+                            mma_commit(&op_empty[os]);
+                            mma_commit(&b_empty[st % RB]);
+                        }
+                        if (last) mma_commit(&chunk_full[cur & 1]);
+                    }
+                }
+                // All of this thread's MMAs must finish before TMEM is released.
+                mma_commit(mma_done);
+                mbar_wait(mma_done, 0, nullptr, p.status, tmo);
+            }
+        }
+    } else if (warp < 8) {
+        // warpgroup 1: epilogue
+        if constexpr (C::kRegSplit) setmaxnreg_inc<C::kRegEpi>();
+        if (run) {
+            // ------------------------------------------------ epilogue warps --
+            // Each thread owns one weight row of the tile (its TMEM lane) and keeps
+            // that row's int32 sums for all BT tokens of the segment in registers:
+            // a drained chunk is added into them and its buffer goes back to the
+            // MMAs at once (zeroed); the tile's output then leaves from registers.
+            griddep_wait();  // scales, workspace and output may belong to the preceding kernel
+            const int et = threadIdx.x - 128;           // TMEM lane == weight row in tile
+            const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            constexpr int NB = BT / 16;                 // blocks of 16 tokens
+            SegmentWalker walk(p, cta);
+            Segment sg;
+            int gc = 0;
+            int stg_use = 0;  // staging buffers used so far (buffer stg_use & 1 is next)
+            uint32_t fix_n0 = 0, fix_n1 = 0;  // fix-up loads consumed per staging buffer (mbarrier phases)
+            uint32_t zero16[16];
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) zero16[i] = 0u;
+            {
+                // Both chunk buffers start zeroed (the MMAs only accumulate).
+                for (int j = 0; j < 2 * NB; ++j) tmem_st16(tl + C::kChunk0 + static_cast<uint32_t>(16 * j), zero16);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&chunk_empty[0]);
+                    mbar_arrive(&chunk_empty[1]);
                 }
             }
-            // All of this thread's MMAs must finish before TMEM is released.
-            mma_commit(mma_done);
-            mbar_wait(mma_done, 0, nullptr, p.status, tmo);
+            // All four epilogue warps take every named barrier below the same number
+            // of times: they walk the same segments and leave the walk together,
+            // on a decision read from the shared abort flag after a barrier (any
+            // failed wait has raised it before that barrier).
+            bool ok = true;
+            while (walk.next(sg)) {
+                const int tok_tile = sg.tile % p.tok_tiles, n_tile = sg.tile / p.tok_tiles;
+                const int m0 = tok_tile * BT, n = n_tile * kTileN + et;
+                const bool split = !(sg.k0 == 0 && sg.k1 == p.G);
+                const float sw = p.s_w ? h2f(p.s_w[n]) : 0.f;
+                const int zc = (p.group == 0) ? p.packed[packed_z_offset(p.N, p.K) + n] : 0;
+                const uint32_t tfirst = static_cast<uint32_t>(sg.tile) * static_cast<uint32_t>(p.G);
+                const int slot_idx = split ? cta_of_stage(tfirst, p) : 0;
+                int32_t *slot = p.slots + static_cast<size_t>(slot_idx) * (BT * kTileN);
+                const int nch = (sg.k1 - sg.k0 + kChunkStages - 1) / kChunkStages;
+                // Stage this tile's per-token scale (and row sums) in shared memory.
+                named_bar_sync(2, kEpiThreads);
+                if (et < BT) {
+                    const int m = m0 + et;
+                    tile_sx[et] = (m < p.M && p.s_x) ? h2f(p.s_x[m]) : 0.f;
+                    tile_tx[et] = (m < p.M && p.group == 0) ? p.t_x[m] : 0;
+                }
+                named_bar_sync(2, kEpiThreads);
+                int acc[BT];
+    #pragma unroll
+                for (int i = 0; i < BT; ++i) acc[i] = 0;
+                for (int c = 0; c < nch; ++c) {
+                    const int cur = gc++;
+                    const int cb = cur & 1;
+                    // A failed wait does not leave the loop: every epilogue warp
+                    // must take the same named barriers; the abort flag, read by
+                    // the issuing thread after each barrier, stops all output.
+                    ok = mbar_wait_warp(&chunk_full[cb], (cur >> 1) & 1, abort_flag, p.status, tmo);
+                    tc_fence_after();
+                    const uint32_t cbase = tl + C::kChunk0 + static_cast<uint32_t>(cb * BT);
+    #pragma unroll
+                    for (int j = 0; j < NB; j += 2) {
+                        // two 16-column loads in flight, then the zeros back
+                        uint32_t f0[16], f1[16];
+                        tmem_ld16(cbase + static_cast<uint32_t>(16 * j), f0);
+                        if (j + 1 < NB) tmem_ld16(cbase + static_cast<uint32_t>(16 * j + 16), f1);
+                        tmem_wait_ld_regs(f0);
+                        if (j + 1 < NB) tmem_wait_ld_regs(f1);
+                        tmem_st16(cbase + static_cast<uint32_t>(16 * j), zero16);
+                        if (j + 1 < NB) tmem_st16(cbase + static_cast<uint32_t>(16 * j + 16), zero16);
+    #pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            acc[16 * j + i] += __float2int_rn(__uint_as_float(f0[i]));
+                            if (j + 1 < NB) acc[16 * j + 16 + i] += __float2int_rn(__uint_as_float(f1[i]));
+                        }
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&chunk_empty[cb]);
+                }
+                if (!split) {
+                    if constexpr (kAccOut) {
+                        // int32 test output: per block of 16 tokens, this thread's
+                        // values go through its own slots of the fix-up output
+                        // buffers (unused in this mode) into one rolled loop.
+                        const uint32_t ibuf = smem_u32(stg_base) + 3 * C::kStgBytes;
+    #pragma unroll
+                        for (int j = 0; j < NB; ++j) {
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                st_shared_b32(ibuf + 4u * (i * kTileN + et), static_cast<uint32_t>(acc[16 * j + i]));
+                            write_block_i32(p, ibuf, m0 + 16 * j, n, zc, tile_sx + 16 * j, tile_tx + 16 * j, sw, ok);
+                        }
+                    } else {
+                        // fp16 outputs: blocks of 16 tokens x 128 rows staged, then
+                        // one tensor store each (rows past M are clipped by the copy).
+    #pragma unroll
+                        for (int j = 0; j < NB; ++j) {
+                            if (et == 0) bulk_wait_read<1>();  // the buffer's previous copy has read it
+                            named_bar_sync(3, kEpiThreads);
+                            const uint32_t buf = smem_u32(stg_base) + (stg_use & 1) * C::kStgBytes;
+                            uint32_t sxv[16], txv[16];
+                            ld_shared_x16(smem_u32(tile_sx + 16 * j), sxv);
+                            ld_shared_x16(smem_u32(tile_tx + 16 * j), txv);
+                            uint16_t o[16];
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                o[i] = out_fp16(acc[16 * j + i], zc, static_cast<int>(txv[i]), __uint_as_float(sxv[i]), sw);
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i) st_shared_u16(buf + 2u * (i * kTileN + et), o[i]);
+                            fence_proxy_async_smem();
+                            named_bar_sync(3, kEpiThreads);
+                            if (et == 0 && *abort_flag == 0) {
+                                tma_store_2d(&o_map, stg_base + (stg_use & 1) * C::kStgBytes, n_tile * kTileN, m0 + 16 * j);
+                                bulk_commit();
+                            }
+                            ++stg_use;
+                        }
+                    }
+                } else {
+                    // Split tile: if every other contributor has already published
+                    // its partial, this CTA is the last one and finishes the tile
+                    // with its own partial still in registers.
+                    named_bar_sync(3, kEpiThreads);
+                    if (et == 0) {
+                        int f = 0;
+                        if (*abort_flag == 0 && !(p.debug_flags & kDebugAlwaysPublish))
+                            f = finish_directly(p, cta, slot_idx, tfirst, abort_flag) ? 1 : 0;
+                        *fin_flag = f;
+                    }
+                    named_bar_sync(3, kEpiThreads);
+                    const bool fin_seg = *fin_flag != 0;
+                    bool do_fix = fin_seg;
+                    if (!fin_seg) {
+                        // Publish: each block of 16 tokens (8 KB, rows 16j.. of the
+                        // slot are contiguous) goes out as one bulk reduce-add.
+    #pragma unroll
+                        for (int j = 0; j < NB; ++j) {
+                            if (et == 0) bulk_wait_read<1>();
+                            named_bar_sync(3, kEpiThreads);
+                            const uint32_t buf = smem_u32(stg_base) + (stg_use & 1) * C::kStgBytes;
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                st_shared_b32(buf + 4u * (i * kTileN + et), static_cast<uint32_t>(acc[16 * j + i]));
+                            fence_proxy_async_smem();
+                            named_bar_sync(3, kEpiThreads);
+                            if (et == 0 && *abort_flag == 0) {
+                                bulk_reduce_add_s32(slot + 16 * j * kTileN, stg_base + (stg_use & 1) * C::kStgBytes,
+                                                    C::kStgBytes);
+                                bulk_commit();
+                            }
+                            ++stg_use;
+                        }
+                        // Every epilogue thread reaches both named barriers once per
+                        // publish.  A failed wait anywhere has raised abort_flag
+                        // before the first barrier, so the decision below is uniform.
+                        // One thread issued this tile's partial reductions; it waits
+                        // for them to complete, publishes them with a fence and the
+                        // arrival counter, and learns whether this CTA is the last.
+                        named_bar_sync(1, kEpiThreads);
+                        if (et == 0) {
+                            int last_cta = 0;
+                            if (*abort_flag == 0) {
+                                bulk_wait<0>();
+                                __threadfence();
+                                const uint32_t tlast = tfirst + static_cast<uint32_t>(p.G) - 1u;
+                                const unsigned expected =
+                                    static_cast<unsigned>(cta_of_stage(tlast, p) - slot_idx + 1);
+                                const unsigned prev = atomicAdd(p.counters + slot_idx, 1u);
+                                last_cta = (prev + 1 == expected) ? 1 : 0;
+                                if (last_cta) __threadfence();
+                            }
+                            *is_last = last_cta;
+                        }
+                        named_bar_sync(1, kEpiThreads);
+                        do_fix = *is_last != 0;
+                    }
+                    if (do_fix) {
+                        // Fix-up: out = (own partial, when finishing directly) + the
+                        // slot's sums.  Slot rows of 16 tokens (8 KB) come in by bulk
+                        // loads, two in flight through the staging buffers; each
+                        // block's rows are then re-zeroed and its fp16 outputs leave
+                        // through the two fix-up output buffers.
+                        if (et == 0) {
+                            bulk_wait_read<0>();        // staging buffers no longer read by earlier copies
+                            fence_proxy_async_global();  // the counter acquire orders the loads below
+                            for (int q = 0; q < (NB < 2 ? NB : 2); ++q) {
+                                mbar_arrive_expect_tx(&fix_bar[q], C::kStgBytes);
+                                tma_load_1d(stg_base + q * C::kStgBytes, slot + 16 * q * kTileN, C::kStgBytes, &fix_bar[q]);
+                            }
+                        }
+    #pragma unroll
+                        for (int j = 0; j < NB; ++j) {
+                            const int q = j & 1;
+                            // The loads always complete (they read the workspace), so
+                            // this wait ignores the abort flag: none is left in flight.
+                            mbar_wait_warp(&fix_bar[q], (q ? fix_n1 : fix_n0) & 1u, nullptr, p.status, tmo);
+                            if (q) ++fix_n1; else ++fix_n0;
+                            const uint32_t sbuf = smem_u32(stg_base) + q * C::kStgBytes;
+                            int tot[16];
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                tot[i] = ld_shared_s32(sbuf + 4u * (i * kTileN + et)) + (fin_seg ? acc[16 * j + i] : 0);
+                            if (et == 0) bulk_wait_read<1>();  // output buffer q: its store from block j-2 has read it
+                            named_bar_sync(3, kEpiThreads);     // ... and every thread has read staging buffer q
+                            if (et == 0) {
+                                if (*abort_flag == 0) {
+                                    bulk_store(slot + 16 * j * kTileN, stg_base + 2 * C::kStgBytes, C::kStgBytes);
+                                    bulk_commit();
+                                }
+                                if (j + 2 < NB) {
+                                    mbar_arrive_expect_tx(&fix_bar[q], C::kStgBytes);
+                                    tma_load_1d(stg_base + q * C::kStgBytes, slot + 16 * (j + 2) * kTileN, C::kStgBytes,
+                                                &fix_bar[q]);
+                                }
+                            }
+                            if constexpr (kAccOut) {
+                                const uint32_t ibuf = smem_u32(stg_base) + 3 * C::kStgBytes;
+    #pragma unroll
+                                for (int i = 0; i < 16; ++i) st_shared_b32(ibuf + 4u * (i * kTileN + et), static_cast<uint32_t>(tot[i]));
+                                write_block_i32(p, ibuf, m0 + 16 * j, n, zc, tile_sx + 16 * j, tile_tx + 16 * j, sw,
+                                                *abort_flag == 0);
+                                continue;
+                            }
+                            const uint32_t obuf = smem_u32(stg_base) + 3 * C::kStgBytes + q * (C::kStgBytes / 2);
+                            uint32_t sxv[16], txv[16];
+                            ld_shared_x16(smem_u32(tile_sx + 16 * j), sxv);
+                            ld_shared_x16(smem_u32(tile_tx + 16 * j), txv);
+                            uint16_t o[16];
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                o[i] = out_fp16(tot[i], zc, static_cast<int>(txv[i]), __uint_as_float(sxv[i]), sw);
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i) st_shared_u16(obuf + 2u * (i * kTileN + et), o[i]);
+                            fence_proxy_async_smem();
+                            named_bar_sync(3, kEpiThreads);
+                            if (et == 0 && *abort_flag == 0) {
+                                tma_store_2d(&o_map, stg_base + 3 * C::kStgBytes + q * (C::kStgBytes / 2), n_tile * kTileN,
+                                             m0 + 16 * j);
+                                bulk_commit();
+                            }
+                        }
+                        if (et == 0 && *abort_flag == 0) p.counters[slot_idx] = 0u;
+                    }
+                }
+                named_bar_sync(1, kEpiThreads);  // also: is_last is rewritten by the next split segment
+                if (*abort_flag != 0) break;
+            }
+            // Bulk copies read shared memory until they complete: wait before exit.
+            if (et == 0) bulk_wait<0>();
+            (void)ok;
         }
-    } else if (run && warp >= 8) {
+    } else if (run) {
         // ---------------------------------------------- converter warps --
         // Two groups of four warps take alternate stages, so one group's
         // waits and fences overlap the other group's arithmetic.  In a group,
@@ -399,258 +687,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&op_full[os]);
             }
         }
-    } else if (run && warp >= 4 && warp < 8) {
-        // ------------------------------------------------ epilogue warps --
-        griddep_wait();  // scales, workspace and output may belong to the preceding kernel
-        const int et = threadIdx.x - 128;           // TMEM lane == weight row in tile
-        const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        SegmentWalker walk(p, cta);
-        Segment sg;
-        int gc = 0;
-        int stg_use = 0;  // staging buffers used so far (buffer stg_use & 1 is next)
-        uint32_t fix_n0 = 0, fix_n1 = 0;  // fix-up loads consumed per staging buffer (mbarrier phases)
-        {
-            // Both chunk buffers start zeroed (the MMAs only accumulate).
-            uint32_t zero16[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) zero16[i] = 0u;
-            for (int j = 0; j < 2 * BT / 16; ++j) tmem_st16(tl + C::kChunk0 + static_cast<uint32_t>(16 * j), zero16);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&chunk_empty[0]);
-                mbar_arrive(&chunk_empty[1]);
-            }
-        }
-        // All four epilogue warps take every named barrier below the same number
-        // of times: they walk the same segments and leave the walk together,
-        // on a decision read from the shared abort flag after a barrier (any
-        // failed wait has raised it before that barrier).
-        bool ok = true;
-        while (walk.next(sg)) {
-            const int tok_tile = sg.tile % p.tok_tiles, n_tile = sg.tile / p.tok_tiles;
-            const int m0 = tok_tile * BT, n = n_tile * kTileN + et;
-            const bool split = !(sg.k0 == 0 && sg.k1 == p.G);
-            const float sw = p.s_w ? h2f(p.s_w[n]) : 0.f;
-            const int zc = (p.group == 0) ? p.packed[packed_z_offset(p.N, p.K) + n] : 0;
-            const uint32_t tfirst = static_cast<uint32_t>(sg.tile) * static_cast<uint32_t>(p.G);
-            const int slot_idx = split ? cta_of_stage(tfirst, p) : 0;
-            int32_t *slot = p.slots + static_cast<size_t>(slot_idx) * (BT * kTileN);
-            const int nch = (sg.k1 - sg.k0 + kChunkStages - 1) / kChunkStages;
-            // Stage this tile's per-token scale (and row sums) in shared memory.
-            named_bar_sync(2, kEpiThreads);
-            if (et < BT) {
-                const int m = m0 + et;
-                tile_sx[et] = (m < p.M && p.s_x) ? h2f(p.s_x[m]) : 0.f;
-                tile_tx[et] = (m < p.M && p.group == 0) ? p.t_x[m] : 0;
-            }
-            named_bar_sync(2, kEpiThreads);
-            bool fin_seg = false;  // this CTA finishes the split tile directly
-            for (int c = 0; c < nch; ++c) {
-                const int cur = gc++;
-                const int cb = cur & 1;
-                // warp-uniform outcome (the TMEM loads below are warp-collective).
-                // A failed wait does not leave the loop: every epilogue warp
-                // must take the same named barriers; the abort flag, read by
-                // the issuing thread after each barrier, stops all output.
-                ok = mbar_wait_warp(&chunk_full[cb], (cur >> 1) & 1, abort_flag, p.status, tmo);
-                tc_fence_after();
-                const bool last = c == nch - 1;
-                // Split tile: if every other contributor has already published
-                // its partial, this CTA is the last one and finishes the tile
-                // itself, keeping its own partial in the TMEM running sum.
-                bool fin = false;
-                if (last && split) {
-                    named_bar_sync(3, kEpiThreads);
-                    if (et == 0) {
-                        int f = 0;
-                        if (*abort_flag == 0 && !(p.debug_flags & kDebugAlwaysPublish))
-                            f = finish_directly(p, cta, slot_idx, tfirst, abort_flag) ? 1 : 0;
-                        *fin_flag = f;
-                    }
-                    named_bar_sync(3, kEpiThreads);
-                    fin = *fin_flag != 0;
-                }
-#pragma unroll 1
-                for (int j = 0; j < BT / 16; ++j) {
-                    uint32_t f[16], r[16];
-                    tmem_ld16(tl + C::kChunk0 + static_cast<uint32_t>(cb * BT + 16 * j), f);
-                    if (c > 0) {
-                        tmem_ld16(tl + static_cast<uint32_t>(16 * j), r);
-                        tmem_wait_ld_regs(r);
-                    }
-                    tmem_wait_ld_regs(f);
-                    {
-                        // hand the chunk buffer back zeroed
-                        uint32_t zero16[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) zero16[i] = 0u;
-                        tmem_st16(tl + C::kChunk0 + static_cast<uint32_t>(cb * BT + 16 * j), zero16);
-                    }
-                    uint32_t v[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(f[i])) +
-                                                     (c > 0 ? static_cast<int>(r[i]) : 0));
-                    if (!last || fin) {
-                        tmem_st16(tl + static_cast<uint32_t>(16 * j), v);
-                    } else if (!split && p.acc_out) {
-                        // int32 test output: one store per element
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (ok && m0 + 16 * j + i < p.M)
-                                write_out(p, m0 + 16 * j + i, n, static_cast<int>(v[i]), zc, tile_tx[16 * j + i],
-                                          tile_sx[16 * j + i], sw);
-                    } else {
-                        // Stage the block of 16 tokens x 128 rows, then one bulk
-                        // copy: int32 partials reduced into the tile's slot (rows
-                        // 16j.. of a slot are contiguous), or fp16 outputs stored
-                        // to O (rows past M are clipped by the copy).
-                        if (et == 0) bulk_wait_read<1>();  // the buffer's previous copy has read it
-                        named_bar_sync(3, kEpiThreads);
-                        const uint32_t buf = smem_u32(stg_base) + (stg_use & 1) * C::kStgBytes;
-                        if (split) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) st_shared_b32(buf + 4u * (i * kTileN + et), v[i]);
-                        } else {
-                            uint32_t sxv[16], txv[16];
-                            ld_shared_x16(smem_u32(tile_sx + 16 * j), sxv);
-                            ld_shared_x16(smem_u32(tile_tx + 16 * j), txv);
-                            uint16_t o[16];
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                o[i] = out_fp16(static_cast<int>(v[i]), zc, static_cast<int>(txv[i]),
-                                                __uint_as_float(sxv[i]), sw);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) st_shared_u16(buf + 2u * (i * kTileN + et), o[i]);
-                        }
-                        fence_proxy_async_smem();
-                        named_bar_sync(3, kEpiThreads);
-                        if (et == 0 && *abort_flag == 0) {
-                            const uint8_t *src = stg_base + (stg_use & 1) * C::kStgBytes;
-                            if (split)
-                                bulk_reduce_add_s32(slot + 16 * j * kTileN, src, C::kStgBytes);
-                            else
-                                tma_store_2d(&o_map, src, n_tile * kTileN, m0 + 16 * j);
-                            bulk_commit();
-                        }
-                        ++stg_use;
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&chunk_empty[cb]);
-                if (last) fin_seg = fin;
-            }
-            if (split) {
-                bool do_fix = fin_seg;
-                if (!fin_seg) {
-                    // Every epilogue thread reaches both named barriers once per
-                    // split segment.  A failed wait anywhere has raised abort_flag
-                    // before the first barrier, so the decision below is uniform.
-                    // One thread issued this tile's partial reductions; it waits
-                    // for them to complete, publishes them with a fence and the
-                    // arrival counter, and learns whether this CTA is the last.
-                    named_bar_sync(1, kEpiThreads);
-                    if (et == 0) {
-                        int last_cta = 0;
-                        if (*abort_flag == 0) {
-                            bulk_wait<0>();
-                            __threadfence();
-                            const uint32_t tlast = tfirst + static_cast<uint32_t>(p.G) - 1u;
-                            const unsigned expected =
-                                static_cast<unsigned>(cta_of_stage(tlast, p) - slot_idx + 1);
-                            const unsigned prev = atomicAdd(p.counters + slot_idx, 1u);
-                            last_cta = (prev + 1 == expected) ? 1 : 0;
-                            if (last_cta) __threadfence();
-                        }
-                        *is_last = last_cta;
-                    }
-                    named_bar_sync(1, kEpiThreads);
-                    do_fix = *is_last != 0;
-                }
-                if (do_fix) {
-                    // Fix-up: out = (own partial, kept in TMEM when finishing
-                    // directly) + the slot's sums.  Slot rows of 16 tokens (8 KB)
-                    // come in by bulk loads, two in flight through the staging
-                    // buffers; each block's rows are then re-zeroed and its fp16
-                    // outputs leave through the two fix-up output buffers.
-                    constexpr int nb = BT / 16;
-                    if (et == 0) {
-                        bulk_wait_read<0>();        // staging buffers no longer read by earlier copies
-                        fence_proxy_async_global();  // the counter acquire orders the loads below
-                        for (int q = 0; q < (nb < 2 ? nb : 2); ++q) {
-                            mbar_arrive_expect_tx(&fix_bar[q], C::kStgBytes);
-                            tma_load_1d(stg_base + q * C::kStgBytes, slot + 16 * q * kTileN, C::kStgBytes, &fix_bar[q]);
-                        }
-                    }
-#pragma unroll 1
-                    for (int j = 0; j < nb; ++j) {
-                        const int q = j & 1;
-                        // The loads always complete (they read the workspace), so
-                        // this wait ignores the abort flag: none is left in flight.
-                        mbar_wait_warp(&fix_bar[q], (q ? fix_n1 : fix_n0) & 1u, nullptr, p.status, tmo);
-                        if (q) ++fix_n1; else ++fix_n0;
-                        const uint32_t sbuf = smem_u32(stg_base) + q * C::kStgBytes;
-                        int acc[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] = ld_shared_s32(sbuf + 4u * (i * kTileN + et));
-                        if (fin_seg) {
-                            uint32_t r[16];
-                            tmem_ld16(tl + static_cast<uint32_t>(16 * j), r);
-                            tmem_wait_ld_regs(r);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[i] += static_cast<int>(r[i]);
-                        }
-                        if (et == 0) bulk_wait_read<1>();  // output buffer q: its store from block j-2 has read it
-                        named_bar_sync(3, kEpiThreads);     // ... and every thread has read staging buffer q
-                        if (et == 0) {
-                            if (*abort_flag == 0) {
-                                bulk_store(slot + 16 * j * kTileN, stg_base + 2 * C::kStgBytes, C::kStgBytes);
-                                bulk_commit();
-                            }
-                            if (j + 2 < nb) {
-                                mbar_arrive_expect_tx(&fix_bar[q], C::kStgBytes);
-                                tma_load_1d(stg_base + q * C::kStgBytes, slot + 16 * (j + 2) * kTileN, C::kStgBytes,
-                                            &fix_bar[q]);
-                            }
-                        }
-                        if (p.acc_out) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (*abort_flag == 0 && m0 + 16 * j + i < p.M)
-                                    write_out(p, m0 + 16 * j + i, n, acc[i], zc, tile_tx[16 * j + i], tile_sx[16 * j + i], sw);
-                            continue;
-                        }
-                        const uint32_t obuf = smem_u32(stg_base) + 3 * C::kStgBytes + q * (C::kStgBytes / 2);
-                        uint32_t sxv[16], txv[16];
-                        ld_shared_x16(smem_u32(tile_sx + 16 * j), sxv);
-                        ld_shared_x16(smem_u32(tile_tx + 16 * j), txv);
-                        uint16_t o[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            o[i] = out_fp16(acc[i], zc, static_cast<int>(txv[i]), __uint_as_float(sxv[i]), sw);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) st_shared_u16(obuf + 2u * (i * kTileN + et), o[i]);
-                        fence_proxy_async_smem();
-                        named_bar_sync(3, kEpiThreads);
-                        if (et == 0 && *abort_flag == 0) {
-                            tma_store_2d(&o_map, stg_base + 3 * C::kStgBytes + q * (C::kStgBytes / 2), n_tile * kTileN,
-                                         m0 + 16 * j);
-                            bulk_commit();
-                        }
-                    }
-                    if (et == 0 && *abort_flag == 0) p.counters[slot_idx] = 0u;
-                }
-            }
-            named_bar_sync(1, kEpiThreads);  // also: is_last is rewritten by the next split segment
-            if (*abort_flag != 0) break;
-        }
-        // Bulk copies read shared memory until they complete: wait before exit.
-        if (et == 0) bulk_wait<0>();
-        (void)ok;
     }
 
     tc_fence_before();
@@ -672,9 +708,20 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(w4a8_gemm_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(C::kSmemBytes));
-            if (e != cudaSuccess) return e;
+            for (auto kern : {w4a8_gemm_kernel<BT, false>, w4a8_gemm_kernel<BT, true>}) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+                if (e != cudaSuccess) return e;
+                if (C::kRegSplit) {
+                    // The warpgroup register split adds up to the launch
+                    // allocation only at this per-thread count; any other would
+                    // leave the epilogue's increase waiting, so refuse to launch.
+                    cudaFuncAttributes fa;
+                    e = cudaFuncGetAttributes(&fa, kern);
+                    if (e != cudaSuccess) return e;
+                    if (fa.numRegs != static_cast<int>(C::kRegLaunch)) return cudaErrorInvalidConfiguration;
+                }
+            }
             configured[dev] = true;
         }
     }
@@ -734,7 +781,9 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
     dim3 grid(plan.ctas);
-    return launch_kernel(w4a8_gemm_kernel<BT>, grid, dim3(kThreads), C::kSmemBytes, stream, a.pdl, map, o_map, p);
+    if (a.acc_out)
+        return launch_kernel(w4a8_gemm_kernel<BT, true>, grid, dim3(kThreads), C::kSmemBytes, stream, a.pdl, map, o_map, p);
+    return launch_kernel(w4a8_gemm_kernel<BT, false>, grid, dim3(kThreads), C::kSmemBytes, stream, a.pdl, map, o_map, p);
 }
 
 }  // namespace
