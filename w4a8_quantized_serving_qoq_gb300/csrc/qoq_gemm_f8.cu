@@ -139,7 +139,9 @@ __device__ __forceinline__ void tmem_wait_ld_pin(uint32_t (&a)[N], uint32_t (&b)
     for (int i = 0; i < N; ++i) asm volatile("" : "+r"(a[i]), "+r"(b[i]));
 }
 
-template <int BT>
+// kAccOut: the int32 test output (GemmParams::acc_out) instead of fp16 O.  A
+// separate instantiation, so that the fp16-output kernel carries no code for it.
+template <int BT, bool kAccOut>
 __global__ void __launch_bounds__(kF8Threads, 1)
     w4a8_gemm_f8_kernel(const __grid_constant__ CUtensorMap plane_map, const __grid_constant__ CUtensorMap tg_map,
                         const __grid_constant__ CUtensorMap o_map, const GemmParams p) {
@@ -572,7 +574,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 }
             };
             if (!split) {
-                if (p.acc_out) {
+                if constexpr (kAccOut) {
 #pragma unroll
                     for (int i = 0; i < HT; ++i) {
                         const int ml = hs * HT + i, m = m0 + ml;
@@ -659,7 +661,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 #pragma unroll
                     for (int i = 0; i < HT; ++i)
                         tot[i] = ld_shared_s32(src + 4u * ((hs * HT + i) * kTileN + row)) + (fin ? acc[i] : 0);
-                    if (p.acc_out) {
+                    if constexpr (kAccOut) {
 #pragma unroll
                         for (int i = 0; i < HT; ++i) {
                             const int ml = hs * HT + i;
@@ -702,9 +704,11 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
     {
         std::lock_guard<std::mutex> lock(mu);
         if (dev < 64 && !configured[dev]) {
-            e = cudaFuncSetAttribute(w4a8_gemm_f8_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(C::kSmemBytes));
-            if (e != cudaSuccess) return e;
+            for (auto kern : {w4a8_gemm_f8_kernel<BT, false>, w4a8_gemm_f8_kernel<BT, true>}) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+                if (e != cudaSuccess) return e;
+            }
             configured[dev] = true;
         }
     }
@@ -776,8 +780,11 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
     p.ctas = plan.ctas;
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
-    return launch_kernel(w4a8_gemm_f8_kernel<BT>, dim3(plan.ctas), dim3(kF8Threads), C::kSmemBytes, stream, a.pdl,
-                         plane_map, tg_map, o_map, p);
+    if (a.acc_out)
+        return launch_kernel(w4a8_gemm_f8_kernel<BT, true>, dim3(plan.ctas), dim3(kF8Threads), C::kSmemBytes, stream,
+                             a.pdl, plane_map, tg_map, o_map, p);
+    return launch_kernel(w4a8_gemm_f8_kernel<BT, false>, dim3(plan.ctas), dim3(kF8Threads), C::kSmemBytes, stream,
+                         a.pdl, plane_map, tg_map, o_map, p);
 }
 
 }  // namespace
