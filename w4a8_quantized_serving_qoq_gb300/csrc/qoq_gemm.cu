@@ -801,11 +801,11 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
         // Few k-stages per CTA at the natural tile (64 tokens up to M = 64,
         // else 128): half-width token tiles double the work units, which
         // balances the stream-K ranges and halves each split tile's fix-up;
-        // measured faster up to 12 stages per CTA (Llama-3-8B qkv and o at
-        // M = 64 and 128), slower from 13.5 (o at M = 256).
+        // measured faster up to 13.5 stages per CTA (Llama-3-8B qkv and o at
+        // M = 64 and 128, o at M = 256), slower from 20 (qkv at M = 256).
         const long long nat = M <= 64 ? 64 : 128;
         const long long stages = (M + nat - 1) / nat * (N / kTileN) * static_cast<long long>(K / kTileK);
-        if (stages <= 12LL * num_sms) {
+        if (stages <= 16LL * num_sms) {
             if (M <= 64 && group == 128) {
                 path = kPathF8;
                 bt = 32;
