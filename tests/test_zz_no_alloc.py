@@ -53,9 +53,15 @@ def test_noalloc_matches_workspace_entry_point_twice(M, N, K):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = qoq.load()
-    M, N, K = 256, 4096, 4096  # 128-token tiles need more partial-slot scratch than 8 MiB
+    # many weight tiles keep 128-token tiles, whose partial slots need more than 8 MiB of scratch
+    M, N, K = 256, 16384, 4096
     assert qoq.qoq_gemm_workspace_bytes(M, N, K, 128) > (8 << 20)
-    Qx, sx, packed, sw = _case(M, N, K, 7)
+    # any valid packed weights and activations: the call must be refused before running
+    q4, sg, z = synthetic.random_codes(N, K, 7)
+    packed = qoq.qoq_pack_weights(_t(q4), _t(sg), _t(z), 128)
+    Qx = torch.zeros((M, K), dtype=torch.int8, device="cuda")
+    sx = torch.ones((M,), dtype=torch.float16, device="cuda")
+    sw = torch.ones((N,), dtype=torch.float16, device="cuda")
     O = torch.empty((M, N), dtype=torch.float16, device="cuda")
     st = lib.qoq_w4a8_gemm_noalloc(
         ctypes.c_void_p(Qx.data_ptr()), ctypes.c_void_p(sx.data_ptr()), None,
