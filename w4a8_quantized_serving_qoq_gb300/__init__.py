@@ -65,6 +65,9 @@ def header_functions() -> list[str]:
 def load():
     """Load libqoq.so (building it first if it is missing or stale)."""
     global _lib
+    lib = _lib
+    if lib is not None:  # fast path: every entry point calls this
+        return lib
     with _lock:
         if _lib is None:
             if not _build.up_to_date():
@@ -101,20 +104,43 @@ def load():
 
 
 # ---------------------------------------------------------------- helpers --
+_torch_mod = None
+_raw_stream = None
+
+
 def _torch():
-    import torch
-    return torch
+    global _torch_mod
+    if _torch_mod is None:
+        import torch
+        _torch_mod = torch
+    return _torch_mod
 
 
-def _stream(stream):
+def _stream(stream, device=None):
+    """cudaStream_t of `stream`, else of the current stream of `device` (a
+    torch.device or index; None: the current device)."""
+    global _raw_stream
+    if stream is not None:
+        return stream.cuda_stream
     torch = _torch()
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is None:
+        # The raw handle of the current stream, as torch's own generated code
+        # reads it; the public call builds a Stream object each time.
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+    if _raw_stream:
+        if device is None:
+            index = torch.cuda.current_device()
+        else:
+            index = device.index if isinstance(device, torch.device) else int(device)
+            if index is None:
+                index = torch.cuda.current_device()
+        return _raw_stream(index)
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device address of a tensor as an int (the prototypes declare c_void_p)."""
+    return None if t is None else t.data_ptr()
 
 
 def _dev(t, dtype, name):
