@@ -390,30 +390,44 @@ def main():
         d2h = sum(h.numel() * 2 for h in hostO)
         e2e_steps = max(3, min(args.steps, 10))
 
-        # Transfers overlap the compute, as in a serving loop: every input
-        # goes up on a copy-in stream (one event per point, which the point's
-        # quantizer waits for), every output comes down on a copy-out stream
-        # once its GEMM is done, and the step ends when all outputs are on
-        # the host.  A step overwrites inputs and outputs only after the
+        # Transfers overlap the compute, as in a serving loop: the inputs go
+        # up on a copy-in stream and the outputs come down on a copy-out
+        # stream, in groups of consecutive points (up to about 2 MB of output
+        # each, so large outputs go down while later points compute): a
+        # group's compute waits for its inputs' event, its outputs are copied
+        # once its last GEMM is done, and the step ends when all outputs are
+        # on the host.  A step overwrites inputs and outputs only after the
         # previous step's readers of them have finished.
         copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev_in = [torch.cuda.Event() for _ in points]
-        ev_done = [torch.cuda.Event() for _ in points]
+        groups, cur, cur_bytes = [], [], 0
+        for i, pt in enumerate(points):
+            cur.append(i)
+            cur_bytes += pt["O"].numel() * 2
+            if cur_bytes >= 2 << 20:
+                groups.append(cur)
+                cur, cur_bytes = [], 0
+        if cur:
+            groups.append(cur)
+        ev_in = [torch.cuda.Event() for _ in groups]
+        ev_done = [torch.cuda.Event() for _ in groups]
 
         def e2e_step():
             copy_in.wait_stream(stream)
             with torch.cuda.stream(copy_in):
-                for i, pt in enumerate(points):
-                    pt["X"].copy_(hostX[i], non_blocking=True)
-                    ev_in[i].record(copy_in)
+                for gi, grp in enumerate(groups):
+                    for i in grp:
+                        points[i]["X"].copy_(hostX[i], non_blocking=True)
+                    ev_in[gi].record(copy_in)
             stream.wait_stream(copy_out)
-            for i, pt in enumerate(points):
-                stream.wait_event(ev_in[i])
-                run_point(i, pt, i)
-                ev_done[i].record(stream)
-                copy_out.wait_event(ev_done[i])
+            for gi, grp in enumerate(groups):
+                stream.wait_event(ev_in[gi])
+                for i in grp:
+                    run_point(i, points[i], i)
+                ev_done[gi].record(stream)
+                copy_out.wait_event(ev_done[gi])
                 with torch.cuda.stream(copy_out):
-                    hostO[i].copy_(pt["O"], non_blocking=True)
+                    for i in grp:
+                        hostO[i].copy_(points[i]["O"], non_blocking=True)
             stream.wait_stream(copy_out)
 
         for _ in range(2):
