@@ -154,6 +154,23 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest of every rank's value (replicas are timed by the slowest
+    one); the value itself when there is no process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tops(ops_per_replica_step: float, world: int, ms_step: float) -> float:
+    """Whole-job throughput: each of the `world` replicas runs the whole step,
+    so the job does world x its operations in the slowest replica's time."""
+    return world * ops_per_replica_step / (ms_step * 1e-3) / 1e12
+
+
 def gpu_pci_id(torch, dev: int) -> str | None:
     try:
         p = torch.cuda.get_device_properties(dev)
@@ -327,13 +344,9 @@ def main():
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    ms_step = ev0.elapsed_time(ev1) / args.steps
-    if dist:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dist, dev)
     ops_step = sum(roofline.gemm_ops(p["M"], p["layer"].N, p["layer"].K) for p in points)
-    tops = world * ops_step / (ms_step * 1e-3) / 1e12
+    tops = whole_job_tops(ops_step, world, ms_step)
 
     # ---- per-point kernel times: each point's quantizer and GEMM alone, each
     # launched R times back to back in a CUDA graph (launch overlap as in the
@@ -433,14 +446,18 @@ def main():
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(e2e_steps):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / e2e_steps
-        e2e = {"value": world * ops_step / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+        if dist:
+            dist.barrier()
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, dist, dev)
+        e2e = {"value": whole_job_tops(ops_step, world, e2e_ms), "unit": "TOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "path": "Python binding -> C ABI per call (no CUDA graph), pinned host buffers, host<->device copies on two side streams overlapping the compute"}
 
