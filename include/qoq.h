@@ -265,6 +265,33 @@ size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gem
  */
 int qoq_gemm_path(int M, int N, int K, int group, const qoq_gemm_options *opt);
 
+/*
+ * The launch plan a GEMM of this shape and options gets on a GPU with
+ * num_sms streaming multiprocessors, computed on the host by the library's
+ * planner without a GPU (the GEMM entry points plan for the current device):
+ *   path            : 1 = fp16-operand path, 2 = fp8-operand path (as
+ *                     qoq_gemm_path);
+ *   tokens_per_tile : tokens of one output tile (the MMA's N);
+ *   num_ctas        : persistent CTAs (stream-K ranges);
+ *   tiles           : output tiles (token tiles x N/128 weight tiles);
+ *   k_stages        : tiles x K/128, the k-stages of work the CTAs share;
+ *   workspace_bytes : as qoq_gemm_workspace_bytes_ex on such a GPU.
+ * Returns QOQ_OK; QOQ_ERR_INVALID_ARG for a NULL out, num_sms <= 0 or
+ * non-positive sizes; QOQ_ERR_UNSUPPORTED for an unsupported shape, group or
+ * option value.  *out is written only on QOQ_OK.
+ */
+typedef struct {
+    int path;
+    int tokens_per_tile;
+    int num_ctas;
+    long long tiles;
+    long long k_stages;
+    size_t workspace_bytes;
+} qoq_gemm_plan_info;
+
+int qoq_gemm_plan(int M, int N, int K, int group, int num_sms, const qoq_gemm_options *opt,
+                  qoq_gemm_plan_info *out);
+
 int qoq_w4a8_gemm_ex(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x,
                      const void *packed, const uint16_t *s_w, int M, int N, int K, int group,
                      uint16_t *O, void *workspace, size_t ws_bytes, const qoq_gemm_options *opt,

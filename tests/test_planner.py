@@ -1,0 +1,86 @@
+"""The GEMM launch planner (qoq_gemm_plan, host only): which tensor-core path,
+tile size and CTA count each Llama-3-8B decode shape gets on a 152-SM GB300,
+the option overrides, the workspace layout and argument errors."""
+import pytest
+
+import w4a8_quantized_serving_qoq_gb300 as qoq
+
+SMS = 152
+QKV, O, GATE_UP, DOWN = (6144, 4096), (4096, 4096), (28672, 4096), (4096, 14336)
+
+
+def _plan(M, NK, group=128, **opt):
+    N, K = NK
+    options = qoq.gemm_options(**opt) if opt else None
+    return qoq.qoq_gemm_plan(M, N, K, group, SMS, options)
+
+
+@pytest.mark.parametrize("M", [1, 8, 16, 32])
+@pytest.mark.parametrize("NK", [QKV, O, GATE_UP, DOWN])
+def test_decode_sizes_take_the_fp8_path_and_leave_8_sms(M, NK):
+    p = _plan(M, NK)
+    assert p["path"] == 2
+    assert p["tokens_per_tile"] == (16 if M <= 16 else 32)
+    assert p["num_ctas"] == SMS - 8
+    assert p["tiles"] == (NK[0] // 128)
+    assert p["k_stages"] == p["tiles"] * (NK[1] // 128)
+
+
+def test_per_channel_weights_always_take_the_fp16_path():
+    for M in (1, 32, 64, 256):
+        assert _plan(M, GATE_UP, group=0)["path"] == 1
+
+
+def test_half_width_tiles_when_a_launch_has_few_stages():
+    # qkv at M = 64: 48 x 32 = 1536 stages at 64 tokens <= 16 x 152 -> 32-token fp8 tiles,
+    # and 2 x 48 = 96 tiles fill 60 % of a wave -> one whole tile per CTA
+    p = _plan(64, QKV)
+    assert (p["path"], p["tokens_per_tile"], p["tiles"], p["num_ctas"]) == (2, 32, 96, 96)
+    # o at M = 128: 32 x 32 = 1024 stages at 128 tokens -> 64-token fp16 tiles, stream-K over every SM
+    p = _plan(128, O)
+    assert (p["path"], p["tokens_per_tile"], p["tiles"], p["num_ctas"]) == (1, 64, 64, SMS)
+
+
+def test_natural_tiles_for_long_launches():
+    p = _plan(64, GATE_UP)  # 224 x 32 stages: no halving
+    assert (p["path"], p["tokens_per_tile"], p["num_ctas"]) == (1, 64, SMS)
+    p = _plan(256, GATE_UP)
+    assert (p["path"], p["tokens_per_tile"], p["tiles"], p["k_stages"]) == (1, 128, 448, 448 * 32)
+    p = _plan(256, QKV)  # 96 tiles of 128 tokens: one whole tile per CTA
+    assert (p["tokens_per_tile"], p["tiles"], p["num_ctas"]) == (128, 96, 96)
+
+
+def test_options_override_the_plan():
+    assert _plan(256, GATE_UP, tokens_per_tile=64)["tokens_per_tile"] == 64
+    p = _plan(256, GATE_UP, kernel=2)
+    assert (p["path"], p["tokens_per_tile"]) == (2, 32)
+    assert _plan(256, GATE_UP, num_ctas=7)["num_ctas"] == 7
+    assert _plan(1, O, num_ctas=5000)["num_ctas"] == 32 * 32  # clamped to the k-stages
+
+
+def _aligned(x, a=256):
+    return (x + a - 1) // a * a
+
+
+@pytest.mark.parametrize("M,NK", [(1, QKV), (64, QKV), (128, O), (256, GATE_UP), (8, DOWN)])
+def test_workspace_layout(M, NK):
+    """[256-byte status][CTA counters][CTAs x tile x 128 int32 slots][activation operand]."""
+    N, K = NK
+    p = _plan(M, NK)
+    slots = 256 + _aligned(p["num_ctas"] * 4)
+    act = 2 * M * K if p["path"] == 1 else 2 * M * K + (K // 128) * ((M + 3) // 4 * 4) * 4
+    expect = _aligned(slots + p["num_ctas"] * p["tokens_per_tile"] * 128 * 4) + act
+    assert p["workspace_bytes"] == expect
+
+
+def test_argument_errors():
+    lib = qoq.load()
+    info = qoq.qoq_gemm_plan_info()
+    byref = qoq.ctypes.byref
+    assert lib.qoq_gemm_plan(16, 256, 512, 128, 0, None, byref(info)) == 1      # no SMs
+    assert lib.qoq_gemm_plan(16, 256, 512, 128, SMS, None, None) == 1           # no output
+    assert lib.qoq_gemm_plan(0, 256, 512, 128, SMS, None, byref(info)) == 1     # M = 0
+    assert lib.qoq_gemm_plan(16, 200, 512, 128, SMS, None, byref(info)) == 2    # N % 128
+    assert lib.qoq_gemm_plan(16, 256, 512, 64, SMS, None, byref(info)) == 2     # group
+    opt = qoq.gemm_options(tokens_per_tile=48)
+    assert lib.qoq_gemm_plan(16, 256, 512, 128, SMS, byref(opt), byref(info)) == 2

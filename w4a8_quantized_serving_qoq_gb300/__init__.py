@@ -62,6 +62,17 @@ def header_functions() -> list[str]:
     return sorted(set(re.findall(r"\b(qoq_[a-z0-9_]+)\s*\(", text)) - {"qoq_gemm_options"})
 
 
+class qoq_gemm_plan_info(ctypes.Structure):
+    _fields_ = [
+        ("path", ctypes.c_int),
+        ("tokens_per_tile", ctypes.c_int),
+        ("num_ctas", ctypes.c_int),
+        ("tiles", ctypes.c_longlong),
+        ("k_stages", ctypes.c_longlong),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
 def load():
     """Load libqoq.so (building it first if it is missing or stale)."""
     global _lib
@@ -87,6 +98,8 @@ def load():
                 "qoq_gemm_workspace_bytes": (S, [I, I, I, I]),
                 "qoq_gemm_workspace_bytes_ex": (S, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
                 "qoq_gemm_path": (I, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
+                "qoq_gemm_plan": (I, [I, I, I, I, I, ctypes.POINTER(qoq_gemm_options),
+                                      ctypes.POINTER(qoq_gemm_plan_info)]),
                 "qoq_workspace_init": (I, [P, S, P]),
                 "qoq_w4a8_gemm": (I, [P, P, P, P, P, I, I, I, I, P, P, S, P]),
                 "qoq_w4a8_gemm_i32": (I, [P, P, P, I, I, I, I, P, P, S, P]),
@@ -279,6 +292,15 @@ def qoq_gemm_path(M: int, N: int, K: int, group: int = 128, options=None) -> int
     if st < 0:
         raise QoqError("qoq_gemm_path", -st)
     return st
+
+
+def qoq_gemm_plan(M: int, N: int, K: int, group: int = 128, num_sms: int = 152, options=None) -> dict:
+    """The launch plan on a GPU with num_sms SMs (host only, no GPU needed)."""
+    info = qoq_gemm_plan_info()
+    _check("qoq_gemm_plan", load().qoq_gemm_plan(M, N, K, group, num_sms,
+                                                 None if options is None else ctypes.byref(options),
+                                                 ctypes.byref(info)))
+    return {f: getattr(info, f) for f, _ in qoq_gemm_plan_info._fields_}
 
 
 def qoq_workspace_init(workspace, stream=None):

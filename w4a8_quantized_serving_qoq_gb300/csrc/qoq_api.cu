@@ -205,6 +205,24 @@ int qoq_gemm_path(int M, int N, int K, int group, const qoq_gemm_options *opt) {
     return plan.path;
 }
 
+int qoq_gemm_plan(int M, int N, int K, int group, int num_sms, const qoq_gemm_options *opt,
+                  qoq_gemm_plan_info *out) {
+    if (!out || num_sms <= 0) return QOQ_ERR_INVALID_ARG;
+    int st = check_gemm_shape(M, N, K, group);
+    if (st != QOQ_OK) return st;
+    st = check_options(opt);
+    if (st != QOQ_OK) return st;
+    const qoq::GemmPlan plan = qoq::plan_gemm(M, N, K, group, num_sms, opt ? opt->kernel : 0,
+                                              opt ? opt->tokens_per_tile : 0, opt ? opt->num_ctas : 0);
+    out->path = plan.path;
+    out->tokens_per_tile = plan.BT;
+    out->num_ctas = plan.ctas;
+    out->tiles = plan.tiles;
+    out->k_stages = plan.total;
+    out->workspace_bytes = plan.ws_bytes;
+    return QOQ_OK;
+}
+
 int qoq_workspace_init(void *workspace, size_t bytes, qoq_stream_t stream) {
     if (!workspace || bytes == 0) return QOQ_ERR_INVALID_ARG;
     return cuda_status(cudaMemsetAsync(workspace, 0, bytes, reinterpret_cast<cudaStream_t>(stream)));
