@@ -1,20 +1,30 @@
 #!/usr/bin/env python
 """Benchmark of the W4A8 GEMM hot path on one GB300 (or N replicas).
 
-Workload: the Llama-3-8B decode GEMMs with g128 progressive group
-quantization -- M in {1, 8, 32, 64, 128, 256} tokens x the four linear layers
-(qkv 6144x4096, o 4096x4096, gate_up 28672x4096, down 4096x14336).  One step
-runs, for each of the 24 (M, layer) points, the per-token activation
-quantization followed by the W4A8 GEMM with its fp16 epilogue; weights are
-quantized and packed once at load time, outside the timed region.  Inputs are
-seeded synthetic data (random-init weights with outlier input channels,
-N(0,1) activations with outlier channels).
+Headline workload: the Llama-3-8B linear layers with g128 progressive group
+quantization over the whole token range of the metric -- the decode batches
+M in {1, 8, 32, 64, 128, 256} and the prefill batch M = 4096 (4 sequences x
+1024 tokens), each x the four layers (qkv 6144x4096, o 4096x4096, gate_up
+28672x4096, down 4096x14336): 28 points.  One step runs, for every point,
+the per-token activation quantization followed by the W4A8 GEMM with its
+fp16 epilogue; weights are quantized and packed once at load time, outside
+the timed region.  Inputs are seeded synthetic data (random-init weights
+with outlier input channels, N(0,1) activations with outlier channels), one
+seed per (workload, layer) as the input recipe states.
 
-Reported: TOPS = sum 2*M*N*K / step time (whole job over all ranks), the
-per-point roofline fractions, the dominant kernel's roofline against the
-measured HBM peak, an end-to-end figure through the public API with
-host<->device copies, SM clocks sampled during the timed region, and the CPU
-oracle timed on a bounded sample (``cpu_baseline``).
+Two further workloads are timed point by point as separate blocks (they are
+not part of the headline step): the Qwen1.5-72B-shaped FFN GEMMs (gate_up
+59136x8192, down 8192x29568 at M in {64, 1024}) and the per-channel W4A8
+variant on Llama-3-8B gate_up over M = 1 .. 4096.
+
+Reported: TOPS = sum 2*M*N*K / step time (whole job over all ranks); per
+point the GEMM's time alone (a CUDA graph of back-to-back launches rotating
+over weight copies larger than L2), its bound (max of the HBM time of the
+4-bit weight + 8-bit activation bytes and the tensor time of the MACs at the
+fp16/bf16 dense peak) and its roofline fraction; the dominant kernel's
+roofline; an end-to-end figure through the public API with host<->device
+copies; SM clocks sampled over a loaded window that ends with the timed
+region; and the CPU oracle timed on a bounded sample (``cpu_baseline``).
 ``--impl reference`` times the CPU oracle alone as the reference arm.
 """
 from __future__ import annotations
@@ -36,12 +46,18 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "W4A8-g128 GEMM TOPS & % of roofline (HBM / INT8 tensor) on 8B shapes, m=1–4096"
-WORKLOAD = ("Llama-3-8B decode GEMMs g128: M in {1,8,32,64,128,256} x "
+WORKLOAD = ("Llama-3-8B GEMMs g128, decode M in {1,8,32,64,128,256} + prefill M=4096 x "
             "{qkv 6144x4096, o 4096x4096, gate_up 28672x4096, down 4096x14336}")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+BLOCKS = {
+    "qwen72b": (3, "Qwen1.5-72B-shaped FFN GEMMs g128: {gate_up 59136x8192, down 8192x29568} x M in {64,1024}"),
+    "per_channel": (4, "Llama-3-8B gate_up 28672x4096, per-channel W4A8 (zero folded via t_x), M = 1..4096"),
+}
+GEMM_SOURCES = ("qoq_gemm.cu", "qoq_gemm_f8.cu", "qoq_gemm_common.cuh", "qoq_device.cuh", "qoq_internal.h")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "w4a8_gemm_traffic_llama3_8b_step.md")
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -49,38 +65,77 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--copies", type=int, default=0,
                     help="packed-weight copies per layer rotated to defeat L2 (0: enough that one layer's "
-                         "copies exceed twice the L2 size, at least 5)")
+                         "copies exceed twice the L2 size, at least 3)")
     ap.add_argument("--point-reps", type=int, default=24,
                     help="launches per CUDA graph when timing each point's kernels alone")
-    ap.add_argument("--cpu-rows", type=int, default=192, help="weight rows in the oracle sample")
+    ap.add_argument("--soak-s", type=float, default=1.0,
+                    help="seconds of untimed step replays right before the timed region, with the clock "
+                         "sampler running (the timed region itself is shorter than one sampling interval)")
+    ap.add_argument("--cpu-rows", type=int, default=64, help="weight rows per layer in the oracle sample")
+    ap.add_argument("--cpu-prefill-tokens", type=int, default=1024,
+                    help="tokens of the prefill batch in the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-points", action="store_true", help="skip the per-point timings (and the blocks)")
+    ap.add_argument("--blocks", default="qwen72b,per_channel",
+                    help="comma list of extra workloads timed point by point ('' for none)")
     ap.add_argument("--layers", default="qkv,o,gate_up,down")
-    ap.add_argument("--ms", default="1,8,32,64,128,256")
-    return ap.parse_args()
+    ap.add_argument("--ms", default="1,8,32,64,128,256,4096",
+                    help="token counts of the headline step (4096 = the prefill workload)")
+    return ap.parse_args(argv)
 
 
-ROOT = os.path.dirname(os.path.abspath(__file__))
-GEMM_SOURCES = ("qoq_gemm.cu", "qoq_gemm_f8.cu", "qoq_gemm_common.cuh", "qoq_device.cuh", "qoq_internal.h")
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "w4a8_gemm_traffic_llama3_8b_decode_step.md")
+# ----------------------------------------------------------- workloads --
+def headline_points(layer_names, Ms):
+    """(workload id, layer, M) of the headline step, M-major like a serving
+    loop that runs every layer at one batch size before the next."""
+    from w4a8_quantized_serving_qoq_gb300 import synthetic
+    by = {l.name: l for l in synthetic.LLAMA3_8B}
+    pts = []
+    for M in Ms:
+        wid = 2 if M == synthetic.PREFILL_M else 1
+        for n in layer_names:
+            pts.append((wid, by[n], M))
+    return pts
+
+
+def block_points(name):
+    from w4a8_quantized_serving_qoq_gb300 import synthetic
+    wid, _ = BLOCKS[name]
+    _, layers, Ms, _, _, _, _ = synthetic.WORKLOADS[wid]
+    return [(wid, layer, M) for layer in layers for M in Ms]
+
+
+def group_of(wid):
+    from w4a8_quantized_serving_qoq_gb300 import synthetic
+    return synthetic.WORKLOADS[wid][6]
+
+
+def gemm_source_digest():
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "w4a8_quantized_serving_qoq_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def gemm_traffic():
-    """DRAM bytes of one step's GEMM launches from the committed ncu summary,
-    or None when the GEMM kernel sources changed since that capture."""
+    """DRAM bytes per GEMM launch of the headline step from the committed ncu
+    summary, keyed (workload, layer, M), or None when the GEMM kernel sources
+    changed since that capture."""
     try:
-        vals = {}
+        vals, per = {}, {}
         for line in open(TRAFFIC_SUMMARY):
-            if ":" in line and not line.startswith(("|", "#", " ")):
+            if line.startswith("traffic:"):
+                _, key, dram = line.split()
+                w, l, m = key.split("/")
+                per[(int(w), l, int(m))] = int(dram)
+            elif ":" in line and not line.startswith(("|", "#", " ")):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-        h = hashlib.sha256()
-        for f in GEMM_SOURCES:
-            with open(os.path.join(ROOT, "w4a8_quantized_serving_qoq_gb300", "csrc", f), "rb") as fh:
-                h.update(fh.read())
-        if h.hexdigest()[:16] != vals.get("gemm_source_digest"):
+        if gemm_source_digest() != vals.get("gemm_source_digest"):
             return None
-        return int(vals["dram_bytes_per_step"]), int(vals["algorithmic_bytes_per_step"])
+        return per or None
     except (OSError, KeyError, ValueError):
         return None
 
@@ -97,14 +152,14 @@ def load_peaks():
 
 # --------------------------------------------------------------- clocks --
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_id: str | None):
         self.gpu_id = gpu_id
         self.proc = None
-        self.lines: list[str] = []
+        self.lines: list[tuple[float, str]] = []
         self.thread = None
 
     def start(self):
@@ -121,9 +176,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def stop(self, window=None):
+        """Summary of the samples taken while the GPU was loaded (host times
+        within `window` = (t0, t1), when given)."""
         if self.proc is None:
             return None
         time.sleep(0.25)
@@ -134,24 +191,31 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
-                                 parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return summarize_clocks(self.lines, window)
+
+
+def summarize_clocks(lines, window=None):
+    sm, smax, power, reasons = [], [], [], set()
+    for t, ln in lines:
+        if window and not (window[0] <= t <= window[1] + 0.25):
+            continue
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            sm.append(float(parts[2]))
+            smax.append(float(parts[3]))
+            power.append(float(parts[4]))
+        except ValueError:
+            continue
+        for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                             parts[6:10]):
+            if val.lower().startswith("active"):
+                reasons.add(name)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+            "power_w_max": max(power), "reasons": sorted(reasons)}
 
 
 def max_over_ranks(value: float, dist=None, device=None) -> float:
@@ -179,20 +243,55 @@ def gpu_pci_id(torch, dev: int) -> str | None:
         return None
 
 
+def roofline_summary(rows, bw, p16):
+    """Roofline of a set of per-point GEMM timings (rows carry layer N, K, M
+    and gemm_us): per bound class the achieved rate against its peak, the
+    dominant class (most GEMM time) and the time-weighted fraction
+    sum(roof time) / sum(measured time)."""
+    from w4a8_quantized_serving_qoq_gb300 import roofline
+    cls = {}
+    troof = tsum = 0.0
+    for r in rows:
+        t = r["gemm_us"] * 1e-6
+        M, N, K = r["M"], r["N"], r["K"]
+        c = cls.setdefault(r["bound"], {"time_s": 0.0, "bytes": 0, "flops": 0, "roof_s": 0.0, "points": 0})
+        c["time_s"] += t
+        c["bytes"] += roofline.w4a8_bytes(M, N, K)
+        c["flops"] += roofline.gemm_ops(M, N, K)
+        c["roof_s"] += roofline.roof_time(M, N, K, bw, p16)
+        c["points"] += 1
+        troof += roofline.roof_time(M, N, K, bw, p16)
+        tsum += t
+    out = {}
+    for b, c in cls.items():
+        if b == "hbm":
+            ach, peak, unit = c["bytes"] / c["time_s"] / 1e9, bw / 1e9, "GB/s"
+        else:
+            ach, peak, unit = c["flops"] / c["time_s"] / 1e12, p16 / 1e12, "TFLOP/s"
+        out[b] = {"achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak, "points": c["points"],
+                  "gemm_time_us": 1e6 * c["time_s"], "time_weighted_roofline_frac": c["roof_s"] / c["time_s"]}
+    dom = max(cls, key=lambda b: cls[b]["time_s"]) if cls else None
+    return out, dom, (troof / tsum if tsum else None)
+
+
 # ----------------------------------------------------------- CPU oracle --
-def oracle_sample(layers, Ms, rows: int, seed_base: int = 1):
-    """Inputs of the bounded oracle sample: the first `rows` weight rows of
-    every layer, quantized by the oracle, and the activations of every point."""
+def oracle_sample(points, rows: int, max_tokens: int):
+    """Inputs of a bounded oracle sample: the first `rows` weight rows of each
+    point's layer, quantized by the oracle, and the first min(M, max_tokens)
+    tokens of each point's activations."""
     import oracle
     from w4a8_quantized_serving_qoq_gb300 import synthetic
-    sample = []
-    for layer in layers:
-        s = synthetic.layer_seed(1, layer)
-        W = synthetic.weights(layer.N, layer.K, s, 0.02, 2)[:rows]
-        wq = oracle.quantize_weights_group(np.ascontiguousarray(W), 128)
-        for M in Ms:
-            X = synthetic.activations(M, layer.K, s, 4)
-            sample.append((layer, M, wq, X))
+    wcache, sample = {}, []
+    for wid, layer, M in points:
+        _, _, _, sigma, wo, xo, group = synthetic.WORKLOADS[wid]
+        s = synthetic.layer_seed(wid, layer)
+        if (wid, layer.name) not in wcache:
+            W = synthetic.weights(layer.N, layer.K, s, sigma, wo, rows=rows)
+            wcache[(wid, layer.name)] = (oracle.quantize_weights_group(W, 128) if group
+                                         else oracle.quantize_weights_channel(W))
+        m = min(M, max_tokens)
+        X = synthetic.activations(M, layer.K, s, xo)[:m]
+        sample.append((layer, m, group, wcache[(wid, layer.name)], np.ascontiguousarray(X)))
     return sample
 
 
@@ -201,20 +300,29 @@ def oracle_pass(sample):
     import oracle
     ops = 0
     t0 = time.perf_counter()
-    for layer, M, wq, X in sample:
-        Qx, sx, _ = oracle.quant_act(X)
-        acc = oracle.gemm_i32_group(Qx, wq["q4"], wq["s_g"], wq["z"])
+    for layer, M, group, wq, X in sample:
+        Qx, sx, tx = oracle.quant_act(X)
+        if group:
+            acc = oracle.gemm_i32_group(Qx, wq["q4"], wq["s_g"], wq["z"])
+        else:
+            acc = oracle.gemm_i32_channel(Qx, tx, wq["q4"], wq["z"])
         oracle.epilogue_f64(acc, sx, wq["s_w"])
         ops += 2 * M * wq["q4"].shape[0] * layer.K
     return time.perf_counter() - t0, ops
 
 
-def run_reference(args, layers, Ms):
+def sample_desc(rows, tokens, npts):
+    return (f"first {rows} weight rows of each layer and the first {tokens} tokens of the prefill batch "
+            f"(all tokens of the decode batches), all {npts} (M, layer) points: quant_act + int32 GEMM + "
+            f"fp64 epilogue, plain single-threaded C")
+
+
+def run_reference(args, points):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    rows = 32
-    sample = oracle_sample(layers, Ms, rows)
+    rows, tokens = 8, 256
+    sample = oracle_sample(points, rows, tokens)
     for _ in range(args.warmup):
         oracle_pass(sample)
     tot_t, tot_ops = 0.0, 0
@@ -223,8 +331,7 @@ def run_reference(args, layers, Ms):
         tot_t += dt
         tot_ops += ops
     tops = tot_ops / tot_t / 1e12
-    desc = (f"oracle (plain single-threaded C) on the first {rows} weight rows of each layer, "
-            f"all 24 (M, layer) points: quant_act + int32 GEMM + fp64 epilogue")
+    desc = sample_desc(rows, tokens, len(points))
     line = {
         "impl": "reference", "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
@@ -237,14 +344,13 @@ def run_reference(args, layers, Ms):
 
 
 # ------------------------------------------------------------ GPU path --
-def main():
-    args = parse_args()
+def main(argv=None):
+    args = parse_args(argv)
     from w4a8_quantized_serving_qoq_gb300 import synthetic
-    layer_by_name = {l.name: l for l in synthetic.LLAMA3_8B}
-    layers = [layer_by_name[n] for n in args.layers.split(",")]
-    Ms = [int(m) for m in args.ms.split(",")]
+    Ms = [int(m) for m in args.ms.split(",") if m]
+    points = headline_points(args.layers.split(","), Ms)
     if args.impl == "reference":
-        run_reference(args, layers, Ms)
+        run_reference(args, points)
         return
 
     import torch
@@ -267,55 +373,66 @@ def main():
     bw = peaks["hbm_gbs"] * 1e9
     p16 = peaks["bf16_tflops"] * 1e12  # fp16 dense tensor rate = bf16 rate
     stream = torch.cuda.current_stream()
-
+    blocks = [b for b in args.blocks.split(",") if b] if not args.no_points else []
     l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2**20)
+
     # ---- load time: quantize + pack weights on the device, make copies ----
     weights = {}
-    for layer in layers:
-        s = synthetic.layer_seed(1, layer)
-        W = torch.from_numpy(synthetic.weights(layer.N, layer.K, s, 0.02, 2)).to(dev)
-        wq = qoq.qoq_quantize_weights(W, 128)
-        packed = qoq.qoq_pack_weights(wq["q4"], wq["s_g"], wq["z"], 128)
-        ncopy = args.copies or max(5, -(-2 * l2_bytes // packed.numel()) + 1)
+
+    def load_weights(wid, layer):
+        key = (wid, layer.name)
+        if key in weights:
+            return weights[key]
+        _, _, _, sigma, wo, _, group = synthetic.WORKLOADS[wid]
+        W = torch.from_numpy(synthetic.weights(layer.N, layer.K, synthetic.layer_seed(wid, layer), sigma, wo)).to(dev)
+        wq = qoq.qoq_quantize_weights(W, group)
+        packed = qoq.qoq_pack_weights(wq["q4"], wq["s_g"], wq["z"], group)
+        ncopy = args.copies or max(3, -(-2 * l2_bytes // packed.numel()) + 1)
         copies = [packed] + [packed.clone() for _ in range(ncopy - 1)]
-        weights[layer.name] = (copies, wq["s_w"])
+        weights[key] = (copies, wq["s_w"])
         del W, wq
-    points = []
-    ws_max = 256
-    for M in Ms:
-        for layer in layers:
-            s = synthetic.layer_seed(1, layer)
-            X = torch.from_numpy(synthetic.activations(M, layer.K, s, 4)).to(dev)
-            Qx = torch.empty((M, layer.K), dtype=torch.int8, device=dev)
-            sx = torch.empty((M,), dtype=torch.float16, device=dev)
-            O = torch.empty((M, layer.N), dtype=torch.float16, device=dev)
-            ws_max = max(ws_max, qoq.qoq_gemm_workspace_bytes(M, layer.N, layer.K, 128))
-            # the quantizer also writes the activation operand the GEMM's path
-            # reads (fp8 planes for decode sizes, an fp16 copy above)
-            kind = qoq.qoq_gemm_path(M, layer.N, layer.K, 128)
-            act = torch.empty((qoq.qoq_act_operand_bytes(M, layer.K, kind),), dtype=torch.uint8, device=dev)
-            points.append(dict(layer=layer, M=M, X=X, Qx=Qx, sx=sx, O=O, act=act, kind=kind,
-                               opt=qoq.gemm_options(act_operand=act, flags=qoq.QOQ_LAUNCH_OVERLAP)))
+        return weights[key]
+
+    def make_point(wid, layer, M):
+        group = group_of(wid)
+        _, _, _, _, _, xo, _ = synthetic.WORKLOADS[wid]
+        load_weights(wid, layer)
+        X = torch.from_numpy(synthetic.activations(M, layer.K, synthetic.layer_seed(wid, layer), xo)).to(dev)
+        kind = qoq.qoq_gemm_path(M, layer.N, layer.K, group)
+        plan = qoq.qoq_gemm_plan(M, layer.N, layer.K, group, torch.cuda.get_device_properties(dev).multi_processor_count)
+        pt = dict(wid=wid, layer=layer, M=M, group=group, X=X, kind=kind, plan=plan,
+                  Qx=torch.empty((M, layer.K), dtype=torch.int8, device=dev),
+                  sx=torch.empty((M,), dtype=torch.float16, device=dev),
+                  tx=torch.empty((M,), dtype=torch.int32, device=dev) if group == 0 else None,
+                  O=torch.empty((M, layer.N), dtype=torch.float16, device=dev),
+                  # the quantizer also writes the activation operand the GEMM's
+                  # path reads (fp8 planes for decode sizes, an fp16 copy above)
+                  act=torch.empty((qoq.qoq_act_operand_bytes(M, layer.K, kind),), dtype=torch.uint8, device=dev))
+        pt["opt"] = qoq.gemm_options(act_operand=pt["act"], flags=qoq.QOQ_LAUNCH_OVERLAP)
+        return pt
+
+    pts = [make_point(*p) for p in points]
+    ws_max = max([256] + [qoq.qoq_gemm_workspace_bytes(p["M"], p["layer"].N, p["layer"].K, p["group"]) for p in pts])
     ws = qoq.new_workspace(ws_max, dev)
     torch.cuda.synchronize()
 
     def quant_point(pt):
-        qoq.qoq_quant_act_ex(pt["X"], pt["Qx"], pt["sx"], None, pt["act"], kind=pt["kind"], with_t=False,
-                             flags=qoq.QOQ_LAUNCH_OVERLAP)
+        qoq.qoq_quant_act_ex(pt["X"], pt["Qx"], pt["sx"], pt["tx"], pt["act"], kind=pt["kind"],
+                             with_t=pt["group"] == 0, flags=qoq.QOQ_LAUNCH_OVERLAP)
 
     def gemm_point(pt, copy_idx):
         layer = pt["layer"]
-        copies, s_w = weights[layer.name]
-        qoq.qoq_w4a8_gemm_ex(pt["Qx"], pt["sx"], None, copies[copy_idx % len(copies)], s_w, layer.N,
-                             layer.K, 128, O=pt["O"], workspace=ws, options=pt["opt"])
+        copies, s_w = weights[(pt["wid"], layer.name)]
+        qoq.qoq_w4a8_gemm_ex(pt["Qx"], pt["sx"], pt["tx"], copies[copy_idx % len(copies)], s_w, layer.N,
+                             layer.K, pt["group"], O=pt["O"], workspace=ws, options=pt["opt"])
 
-    def run_point(i, pt, copy_idx):
+    def run_point(pt, copy_idx):
         quant_point(pt)
         gemm_point(pt, copy_idx)
 
     def step():
-        for i, pt in enumerate(points):
-            run_point(i, pt, i)
+        for i, pt in enumerate(pts):
+            run_point(pt, i)
 
     # eager warm-up (sets kernel attributes before capture), then capture one step
     step()
@@ -324,13 +441,21 @@ def main():
     with torch.cuda.graph(graph):
         step()
     torch.cuda.synchronize()
+    t0 = time.perf_counter()
     for _ in range(max(3, args.warmup)):
         graph.replay()
     torch.cuda.synchronize()
+    est_ms = 1e3 * (time.perf_counter() - t0) / max(3, args.warmup)
 
+    # Clocks: the timed region (K steps) is shorter than one 200 ms sampling
+    # interval, so the sampler runs over a loaded window of untimed replays
+    # of the same step that ends with the timed region.
     clocks = ClockSampler(gpu_pci_id(torch, local_rank))
     clocks.start()
     time.sleep(0.3)
+    w0 = time.time()
+    for _ in range(int(args.soak_s * 1e3 / max(est_ms, 1e-3))):
+        graph.replay()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -341,12 +466,17 @@ def main():
         graph.replay()
     ev1.record(stream)
     torch.cuda.synchronize()
+    w1 = time.time()
     if dist:
         dist.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(window=(w0, w1))
+    if clk:
+        clk["window_s"] = round(w1 - w0, 2)
+        clk["window"] = "untimed replays of the step, then the timed region"
     ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, dist, dev)
-    ops_step = sum(roofline.gemm_ops(p["M"], p["layer"].N, p["layer"].K) for p in points)
+    ops_step = sum(roofline.gemm_ops(p["M"], p["layer"].N, p["layer"].K) for p in pts)
     tops = whole_job_tops(ops_step, world, ms_step)
+    del graph
 
     # ---- per-point kernel times: each point's quantizer and GEMM alone, each
     # launched R times back to back in a CUDA graph (launch overlap as in the
@@ -371,34 +501,41 @@ def main():
         del g
         return statistics.median(ts)
 
-    pt_rows = []
-    gemm_ms_total, bytes_total = 0.0, 0
-    for i, pt in enumerate(points):
-        layer, M = pt["layer"], pt["M"]
-        copies, s_w = weights[layer.name]
-        reps = max(args.point_reps, len(copies))
-        t_q = 1e-3 * graph_us(lambda r: quant_point(pt), reps)
-        t_g = 1e-3 * graph_us(lambda r: gemm_point(pt, r), reps)
-        nbytes = roofline.w4a8_bytes(M, layer.N, layer.K)
-        nops = roofline.gemm_ops(M, layer.N, layer.K)
-        troof = roofline.roof_time(M, layer.N, layer.K, bw, p16)
-        gemm_ms_total += t_g
-        bytes_total += nbytes
-        pt_rows.append({
-            "layer": layer.name, "M": M, "gemm_us": round(1e3 * t_g, 2), "quant_us": round(1e3 * t_q, 2),
-            "TOPS": round(nops / (t_g * 1e-3) / 1e12, 2), "GBs": round(nbytes / (t_g * 1e-3) / 1e9, 1),
-            "bound": roofline.bound(M, layer.N, layer.K, bw, p16),
-            "roof_frac": round(troof / (t_g * 1e-3), 3),
-        })
-    achieved_gbs = bytes_total / (gemm_ms_total * 1e-3) / 1e9
-    traffic = gemm_traffic()
-    troof_sum = sum(roofline.roof_time(p["M"], p["layer"].N, p["layer"].K, bw, p16) for p in points)
+    def time_points(plist):
+        rows = []
+        for pt in plist:
+            layer, M = pt["layer"], pt["M"]
+            copies, _ = weights[(pt["wid"], layer.name)]
+            reps = max(args.point_reps, len(copies))
+            if M * layer.N * layer.K >= 2 ** 36:  # long launches: fewer per graph
+                reps = max(8, len(copies))
+            run_point(pt, 0)  # eager once (kernel attributes) before capture
+            torch.cuda.synchronize()
+            t_q = graph_us(lambda r: quant_point(pt), reps)
+            t_g = graph_us(lambda r: gemm_point(pt, r), reps)
+            nbytes = roofline.w4a8_bytes(M, layer.N, layer.K)
+            nops = roofline.gemm_ops(M, layer.N, layer.K)
+            troof = roofline.roof_time(M, layer.N, layer.K, bw, p16)
+            rows.append({
+                "workload": pt["wid"], "layer": layer.name, "N": layer.N, "K": layer.K, "M": M,
+                "group": pt["group"], "path": pt["plan"]["path"], "tokens_per_tile": pt["plan"]["tokens_per_tile"],
+                "ctas": pt["plan"]["num_ctas"], "gemm_us": round(t_g, 2), "quant_us": round(t_q, 2),
+                "TOPS": round(nops / (t_g * 1e-6) / 1e12, 2), "GBs": round(nbytes / (t_g * 1e-6) / 1e9, 1),
+                "bound": roofline.bound(M, layer.N, layer.K, bw, p16),
+                "roof_frac": round(troof / (t_g * 1e-6), 3),
+            })
+        return rows
+
+    pt_rows, by_bound, dom, twf = [], {}, None, None
+    if not args.no_points:
+        pt_rows = time_points(pts)
+        by_bound, dom, twf = roofline_summary(pt_rows, bw, p16)
 
     # ---- end to end through the public API: host buffers, copies timed ----
     e2e = None
     if not args.no_e2e:
-        hostX = [p["X"].cpu().pin_memory() for p in points]
-        hostO = [torch.empty(p["O"].shape, dtype=torch.float16).pin_memory() for p in points]
+        hostX = [p["X"].cpu().pin_memory() for p in pts]
+        hostO = [torch.empty(p["O"].shape, dtype=torch.float16).pin_memory() for p in pts]
         h2d = sum(h.numel() * 2 for h in hostX)
         d2h = sum(h.numel() * 2 for h in hostO)
         e2e_steps = max(3, min(args.steps, 10))
@@ -413,7 +550,7 @@ def main():
         # previous step's readers of them have finished.
         copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         groups, cur, cur_bytes = [], [], 0
-        for i, pt in enumerate(points):
+        for i, pt in enumerate(pts):
             cur.append(i)
             cur_bytes += pt["O"].numel() * 2
             if cur_bytes >= 2 << 20:
@@ -429,18 +566,18 @@ def main():
             with torch.cuda.stream(copy_in):
                 for gi, grp in enumerate(groups):
                     for i in grp:
-                        points[i]["X"].copy_(hostX[i], non_blocking=True)
+                        pts[i]["X"].copy_(hostX[i], non_blocking=True)
                     ev_in[gi].record(copy_in)
             stream.wait_stream(copy_out)
             for gi, grp in enumerate(groups):
                 stream.wait_event(ev_in[gi])
                 for i in grp:
-                    run_point(i, points[i], i)
+                    run_point(pts[i], i)
                 ev_done[gi].record(stream)
                 copy_out.wait_event(ev_done[gi])
                 with torch.cuda.stream(copy_out):
                     for i in grp:
-                        hostO[i].copy_(points[i]["O"], non_blocking=True)
+                        hostO[i].copy_(pts[i]["O"], non_blocking=True)
             stream.wait_stream(copy_out)
 
         for _ in range(2):
@@ -460,22 +597,65 @@ def main():
         e2e = {"value": whole_job_tops(ops_step, world, e2e_ms), "unit": "TOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "path": "Python binding -> C ABI per call (no CUDA graph), pinned host buffers, host<->device copies on two side streams overlapping the compute"}
+        del hostX, hostO
+
+    # ---- further workloads, point by point ----
+    block_out = {}
+    for bname in blocks:
+        wid, desc = BLOCKS[bname]
+        bpts = [make_point(*p) for p in block_points(bname)]
+        need = max(qoq.qoq_gemm_workspace_bytes(p["M"], p["layer"].N, p["layer"].K, p["group"]) for p in bpts)
+        if need > ws.numel():
+            ws = qoq.new_workspace(need, dev)
+        torch.cuda.synchronize()
+        rows = time_points(bpts)
+        bb, bdom, btwf = roofline_summary(rows, bw, p16)
+        block_out[bname] = {"workload": desc, "tops_gemm_only": sum(roofline.gemm_ops(r["M"], r["N"], r["K"]) for r in rows)
+                            / (sum(r["gemm_us"] for r in rows) * 1e-6) / 1e12,
+                            "time_weighted_roofline_frac": btwf, "by_bound": bb, "dominant_bound": bdom,
+                            "points": rows}
+        for p in bpts:
+            del p["X"], p["Qx"], p["O"], p["act"]
+        for k in [k for k in weights if k[0] == wid]:
+            del weights[k]
+        torch.cuda.empty_cache()
 
     # ---- CPU oracle on a bounded sample ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = oracle_sample(layers, Ms, args.cpu_rows)
+        sample = oracle_sample(points, args.cpu_rows, args.cpu_prefill_tokens)
         dt, ops = oracle_pass(sample)
         cpu = {"value": ops / dt / 1e12, "unit": "TOPS", "cores": 1, "kind": "oracle",
                "seconds": round(dt, 2),
-               "sample": (f"first {args.cpu_rows} weight rows of each layer at all 24 (M, layer) points; "
-                          f"quant_act + int32 GEMM + fp64 epilogue, plain single-threaded C "
-                          f"({os.cpu_count()} host cores present)")}
+               "sample": sample_desc(args.cpu_rows, args.cpu_prefill_tokens, len(points))
+               + f" ({os.cpu_count()} host cores present)"}
 
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
+
+    # the dominant kernel's roofline: the bound class with the most GEMM time
+    roof = None
+    if dom:
+        d = by_bound[dom]
+        traffic = gemm_traffic()
+        dom_rows = [r for r in pt_rows if r["bound"] == dom]
+        tr = None
+        if traffic and all((r["workload"], r["layer"], r["M"]) in traffic for r in dom_rows):
+            tr = sum(traffic[(r["workload"], r["layer"], r["M"])] for r in dom_rows) / len(dom_rows)
+        kern = sorted({("fp8-operand" if r["path"] == 2 else "fp16-operand") for r in dom_rows})
+        roof = {"bound": "hbm" if dom == "hbm" else "tensor", "achieved": d["achieved"], "peak": d["peak"],
+                "unit": d["unit"], "frac": d["frac"], "traffic": tr,
+                "traffic_scope": "mean DRAM read+write bytes per GEMM launch of this bound class (ncu, cold cache)",
+                "algorithmic_bytes_per_launch": sum(roofline.w4a8_bytes(r["M"], r["N"], r["K"]) for r in dom_rows)
+                / len(dom_rows),
+                "kernel": " + ".join(f"w4a8_gemm {k} kernel" for k in kern)
+                + f" on the {d['points']} {dom}-bound points ({', '.join(sorted({str(r['M']) for r in dom_rows}, key=int))} tokens)",
+                "peak_source": f"{peaks_src} ({'HBM copy' if dom == 'hbm' else 'cuBLAS bf16 dense, burst; fp16 rate = bf16 rate'})",
+                "time_weighted_roofline_frac": twf,
+                "by_bound": by_bound,
+                "tensor_peak_tflops": peaks["bf16_tflops"], "tensor_peak_sustained_tflops": peaks["bf16_tflops_sustained"]}
     line = {
         "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -483,21 +663,15 @@ def main():
         "dtype": "s8 x u4 -> exact i32 (e4m3 / fp16 tensor-core MMA), fp16 out", "data": "synthetic",
         "config": {"workload": WORKLOAD, "group": 128, "parallelism": f"replicas{world}",
                    "cuda_graph": True, "l2": "inputs larger than L2: packed-weight copies rotated, "
-                   + ", ".join(f"{k} x{len(c)}" for k, (c, _) in weights.items())
+                   + ", ".join(f"{k[1]}@w{k[0]} x{len(c)}" for k, (c, _) in weights.items())
                    + f" ({sum(len(c) * c[0].numel() for c, _ in weights.values()) / 1e6:.0f} MB)"},
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved_gbs / peaks["hbm_gbs"],
-                     "traffic": traffic[0] if traffic else None,
-                     "traffic_scope": "DRAM read+write bytes of the step's 24 GEMM launches (ncu, cold cache)",
-                     "algorithmic_bytes_per_step": traffic[1] if traffic else None,
-                     "peak_source": peaks_src, "kernel": "w4a8_gemm (fp8-operand kernel for M <= 32, fp16-operand kernel above)",
-                     "time_weighted_roofline_frac": troof_sum / (gemm_ms_total * 1e-3),
-                     "tensor_peak_tflops": peaks["bf16_tflops"]},
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * len(points) * args.steps,
+        "gpu_launches": 2 * len(pts) * args.steps,
         "clocks": clk,
         "points": pt_rows,
+        "blocks": block_out,
     }
     print(json.dumps(line), flush=True)
     if dist:

@@ -16,7 +16,8 @@
  * Conventions for every entry point:
  *  - Every tensor pointer is DEVICE memory owned by the caller; the library
  *    never allocates, frees or synchronizes the device (except
- *    qoq_workspace_status, which synchronizes the given stream).
+ *    qoq_workspace_status and qoq_noalloc_status, which synchronize the
+ *    given stream).
  *  - fp16 tensors are passed as uint16_t IEEE binary16 bit patterns.
  *  - Matrices are row-major and dense: X, Qx [M][K]; W, q4 [N][K]; O [M][N].
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
@@ -308,9 +309,12 @@ int qoq_w4a8_gemm_ex(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x,
  * 8 MiB array inside the library, which every GPU that loads the library
  * keeps until the process exits.  It never calls cudaMalloc, cudaFree or any
  * allocating routine.
- *  - Limit: shapes whose scratch need (qoq_gemm_workspace_bytes) exceeds
- *    8 MiB are rejected with QOQ_ERR_WORKSPACE before any launch; on a
- *    152-SM GB300 that admits up to 64 tokens (M <= 64).
+ *  - Limit: a call needs qoq_gemm_workspace_bytes(M, N, K, group) <= 8 MiB;
+ *    larger shapes are rejected with QOQ_ERR_WORKSPACE before any launch.
+ *    The need depends on the whole shape, not on M alone: on a 152-SM GB300
+ *    every Llama-3-8B linear layer fits up to M = 64 (qkv and o also at M = 128,
+ *    whose planner picks half-width tiles), while Qwen1.5-72B down
+ *    (N = 8192, K = 29568) at M = 64 needs about 8.8 MB and is rejected.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    outside any stream capture.
@@ -319,12 +323,26 @@ int qoq_w4a8_gemm_ex(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x,
  *    calls that overlap on the GPU (different streams, no ordering between
  *    them) race and give wrong results; order them on one stream.
  *  - Device-side status bits (bounded-wait expiry, packed-weight mismatch)
- *    are written to the internal array and are not reported by this entry
- *    point; QOQ_OK means the launch was enqueued.
+ *    go to the array's status word; QOQ_OK means the launch was enqueued.
+ *    Read the word with qoq_noalloc_status after a call and before the
+ *    next one (the next call clears it).
+ * Device ordinals of 64 and above: QOQ_ERR_UNSUPPORTED.
  */
 int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x,
                           const void *packed, const uint16_t *s_w, int M, int N, int K, int group,
                           uint16_t *O, qoq_stream_t stream);
+
+/*
+ * qoq_noalloc_status -- the device status word of the allocation-free GEMM's
+ * internal array on the current device, for callers of
+ * qoq_w4a8_gemm_noalloc (which cannot pass a workspace to
+ * qoq_workspace_status).  Synchronizes `stream`, copies the word to
+ * *host_status, clears it, and returns QOQ_OK, QOQ_ERR_TIMEOUT or
+ * QOQ_ERR_DEVICE by the bits found (1 = a bounded wait expired, 2 =
+ * packed-weight header mismatch or illegal codes).  Allocates nothing.  The
+ * paper has no counterpart of it.
+ */
+int qoq_noalloc_status(uint32_t *host_status, qoq_stream_t stream);
 
 /*
  * qoq_workspace_status -- synchronizes `stream`, copies the workspace status

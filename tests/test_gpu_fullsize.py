@@ -96,22 +96,28 @@ def _check_point(workload, name, M, group=128, check_quantizer=False):
             assert np.array_equal(d["s_g"].cpu().numpy(), wq["s_g"])
 
 
+# Every configuration point of the four full-size workloads.  Points are
+# ordered layer by layer so that each layer's oracle-quantized weights are
+# made once (the cache above holds the last two).
+DECODE_POINTS = [(name, M) for name in ("qkv", "o", "gate_up", "down") for M in synthetic.DECODE_MS]
+QWEN_POINTS = [(name, M) for name in ("gate_up", "down") for M in synthetic.QWEN_MS]
+
+
+@pytest.mark.parametrize("name,M", DECODE_POINTS)
+def test_llama_decode_full_size(name, M):
+    _check_point(1, name, M, check_quantizer=(M == synthetic.DECODE_MS[0]))
+
+
 @pytest.mark.parametrize("name", ["qkv", "o", "gate_up", "down"])
-def test_llama_decode_full_size(name):
-    for i, M in enumerate((1, 64, 256)):
-        _check_point(1, name, M, check_quantizer=(i == 0))
-
-
-@pytest.mark.parametrize("name", ["qkv", "down"])
 def test_llama_prefill_full_size(name):
-    _check_point(2, name, 4096)
+    _check_point(2, name, synthetic.PREFILL_M)
 
 
-@pytest.mark.parametrize("name,M", [("gate_up", 64), ("down", 1024)])
+@pytest.mark.parametrize("name,M", QWEN_POINTS)
 def test_qwen_full_size(name, M):
-    _check_point(3, name, M, check_quantizer=(name == "down"))
+    _check_point(3, name, M, check_quantizer=(M == synthetic.QWEN_MS[0]))
 
 
-def test_per_channel_gate_up_full_size():
-    for i, M in enumerate((1, 128, 4096)):
-        _check_point(4, "gate_up", M, group=0, check_quantizer=(i == 0))
+@pytest.mark.parametrize("M", synthetic.CHANNEL_MS)
+def test_per_channel_gate_up_full_size(M):
+    _check_point(4, "gate_up", M, group=0, check_quantizer=(M == synthetic.CHANNEL_MS[0]))

@@ -221,6 +221,87 @@ def test_channel_quantizer_invariants():
     assert (np.abs(rec - Wf)[inside] <= (0.5 + 1e-3) * np.broadcast_to(s, Wf.shape)[inside] + 1e-3 * s.max()).all()
 
 
+def _channel_rows_with_edge_cases(N, K, seed):
+    W = _rand_weights(N, K, seed=seed)
+    W[0] = 0                                   # all-zero row: the scale guard
+    W[1] = np.abs(W[1])                        # non-negative row: lo = 0, z = 0
+    W[2] = -np.abs(W[2])                       # non-positive row: hi = 0
+    W[3, :] = 0
+    W[3, 5] = np.float16(2.0 ** -20)           # a lone subnormal weight
+    return W
+
+
+def test_channel_scale_bits_vs_numpy_converter():
+    """s_W = fp16_rn(fp32(hi - lo) / 15), bit for bit, with numpy's IEEE fp32
+    arithmetic and its own binary16 converter (a library routine) -- the
+    per-channel counterpart of the step-1 scale check.  A truncated scale, an
+    fp16 (instead of fp32) difference or a missing zero guard fails here."""
+    W = _channel_rows_with_edge_cases(64, 768, seed=19)
+    r = oracle.quantize_weights_channel(W)
+    Wf = W.astype(np.float32)
+    lo = np.minimum(np.float32(0), Wf.min(axis=1))
+    hi = np.maximum(np.float32(0), Wf.max(axis=1))
+    s = ((hi - lo) / np.float32(15)).astype(np.float16)
+    s[s == 0] = np.float16(1.0)
+    assert np.array_equal(r["s_w"].view(np.uint16), s.view(np.uint16))
+    # zero and codes: IEEE fp32 quotients by the stored fp16 scale, numpy.rint (half-even)
+    sf = s.astype(np.float32)
+    z = np.clip(np.rint(-lo / sf), 0, 15).astype(np.int64)
+    q4 = np.clip(np.rint(Wf / sf[:, None]) + z[:, None], 0, 15)
+    assert np.array_equal(r["z"].astype(np.int64), z)
+    assert np.array_equal(r["q4"].astype(np.int64), q4.astype(np.int64))
+    assert r["s_w"].view(np.uint16)[0] == 0x3C00 and r["z"][0] == 0 and (r["q4"][0] == 0).all()
+    assert r["z"][1] == 0 and r["z"][2] == 15
+
+
+def test_channel_scale_difference_taken_in_fp32():
+    """A row whose fp16 difference hi - lo rounds to a different scale than the
+    fp32 difference: the oracle must follow the fp32 reading."""
+    found = None
+    cand = np.arange(0x3C00, 0x3C00 + 64, dtype=np.uint16).view(np.float16)      # hi in [1, 1.0625)
+    lows = -np.arange(0x0400, 0x1C00, 7, dtype=np.uint16).view(np.float16)      # lo in (-2^-6, -2^-14]
+    for hi in cand:
+        d16 = (np.float16(hi) - lows).astype(np.float16)                        # fp16 difference (RN)
+        d32 = np.float32(hi) - lows.astype(np.float32)                          # fp32 difference (RN)
+        s16 = (d16.astype(np.float32) / np.float32(15)).astype(np.float16)
+        s32 = (d32 / np.float32(15)).astype(np.float16)
+        diff = np.nonzero(s16.view(np.uint16) != s32.view(np.uint16))[0]
+        if diff.size:
+            found = (hi, lows[diff[0]], s32[diff[0]], s16[diff[0]])
+            break
+    assert found is not None
+    hi, lo, s32, s16 = found
+    W = np.zeros((1, 128), np.float16)
+    W[0, 0], W[0, 1] = hi, lo
+    r = oracle.quantize_weights_channel(W)
+    assert r["s_w"].view(np.uint16)[0] == s32.view(np.uint16)
+    assert r["s_w"].view(np.uint16)[0] != s16.view(np.uint16)
+
+
+def test_channel_constructed_ties_half_even():
+    """Exact ties of rne(-lo / s_W) and rne(W / s_W), with every value exact
+    in fp16 and s_W = 0.125 exactly ((hi - lo) / 15 = 1.875 / 15)."""
+    s = 0.125
+    r0 = np.zeros(128); r0[0], r0[1] = -2.5 * s, 1.875 - 2.5 * s     # z = rne(2.5) = 2 (half-away: 3)
+    r1 = np.zeros(128); r1[0], r1[1] = -3.5 * s, 1.875 - 3.5 * s     # z = rne(3.5) = 4
+    vals = np.array([0.5, 1.5, -0.5, -1.5, 2.5, 3.5, 4.5]) * s        # code ties
+    r0[2:9] = vals
+    r1[2:9] = vals
+    W = np.stack([r0, r1]).astype(np.float16)
+    assert np.array_equal(W.astype(np.float64), np.stack([r0, r1]))  # all exact in fp16
+    r = oracle.quantize_weights_channel(W)
+    assert list(r["s_w"].astype(np.float64)) == [s, s]
+    assert list(r["z"]) == [2, 4]
+    # rne: 0.5 -> 0, 1.5 -> 2, -0.5 -> 0, -1.5 -> -2, 2.5 -> 2, 3.5 -> 4, 4.5 -> 4; plus z
+    assert list(r["q4"][0, 2:9]) == [2, 4, 2, 0, 4, 6, 6]
+    assert list(r["q4"][1, 2:9]) == [4, 6, 4, 2, 6, 8, 8]
+    # the range ends: lo -> rne(-2.5) + 2 = 0, hi = 12.5 s -> 12 + 2 = 14
+    assert r["q4"][0, 0] == 0 and r["q4"][0, 1] == 14
+    # row 1: hi = 11.5 s -> rne 12, + z = 4 gives 16, clipped to 15
+    assert round(Fraction(23, 2)) == 12
+    assert r["q4"][1, 0] == 0 and r["q4"][1, 1] == 15
+
+
 # --------------------------------------------------------------- activations
 def test_quant_act_invariants():
     X = synthetic.activations(24, 768, 4, 4)

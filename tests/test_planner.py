@@ -84,3 +84,17 @@ def test_argument_errors():
     assert lib.qoq_gemm_plan(16, 256, 512, 64, SMS, None, byref(info)) == 2     # group
     opt = qoq.gemm_options(tokens_per_tile=48)
     assert lib.qoq_gemm_plan(16, 256, 512, 128, SMS, byref(opt), byref(info)) == 2
+
+
+def test_allocation_free_limit_depends_on_the_shape():
+    """The allocation-free entry point admits a shape when its scratch need
+    (the planned workspace) is at most 8 MiB: every Llama-3-8B layer up to
+    M = 64 (qkv and o also at 128), not Qwen1.5-72B down at M = 64."""
+    limit = 8 << 20
+    for M in (1, 8, 32, 64):
+        for NK in (QKV, O, GATE_UP, DOWN):
+            assert _plan(M, NK)["workspace_bytes"] <= limit
+    assert _plan(128, QKV)["workspace_bytes"] <= limit
+    assert _plan(128, O)["workspace_bytes"] <= limit
+    assert _plan(128, GATE_UP)["workspace_bytes"] > limit
+    assert _plan(64, (8192, 29568))["workspace_bytes"] > limit

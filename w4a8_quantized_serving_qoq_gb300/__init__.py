@@ -107,6 +107,7 @@ def load():
                                          ctypes.POINTER(qoq_gemm_options), P]),
                 "qoq_workspace_status": (I, [P, ctypes.POINTER(ctypes.c_uint32), P]),
                 "qoq_w4a8_gemm_noalloc": (I, [P, P, P, P, P, I, I, I, I, P, P]),
+                "qoq_noalloc_status": (I, [ctypes.POINTER(ctypes.c_uint32), P]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(lib, name)
@@ -387,6 +388,14 @@ def qoq_w4a8_gemm_noalloc(Qx, s_x, t_x, packed, s_w, N: int, K: int, group: int 
         _ptr(Qx), _ptr(s_x), _ptr(t_x), _ptr(packed), _ptr(s_w), M, N, K, group, _ptr(O),
         _stream(stream)))
     return O
+
+
+def qoq_noalloc_status(stream=None):
+    """(status code, raw status bits) of the allocation-free GEMM's internal
+    array on the current device; synchronizes the stream and clears the word."""
+    bits = ctypes.c_uint32(0)
+    st = load().qoq_noalloc_status(ctypes.byref(bits), _stream(stream))
+    return int(st), int(bits.value)
 
 
 def qoq_workspace_status(workspace, stream=None):

@@ -14,16 +14,24 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// QOQ_OK when the current device is one the library serves (its ordinal is
+// below qoq::kMaxDevices); checked before any planning or launch.
+int check_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QOQ_ERR_CUDA;
+    return (dev >= 0 && dev < qoq::kMaxDevices) ? QOQ_OK : QOQ_ERR_UNSUPPORTED;
+}
+
 int num_sms_current_device() {
     static std::mutex mu;
-    static int cache[64] = {};
+    static int cache[qoq::kMaxDevices] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= qoq::kMaxDevices) return 0;
     std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    if (cache[dev] > 0) return cache[dev];
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 64) cache[dev] = n;
+    cache[dev] = n;
     return n;
 }
 
@@ -71,6 +79,8 @@ int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const
     if ((s_x && !aligned(s_x, 2)) || (s_w && !aligned(s_w, 2)) || (O && !aligned(O, 16)) ||
         (t_x && !aligned(t_x, 4)) || (acc_out && !aligned(acc_out, 4)))
         return QOQ_ERR_MISALIGNED;
+    st = check_current_device();
+    if (st != QOQ_OK) return st;
     qoq::GemmPlan plan;
     if (!plan_for(M, N, K, group, opt, &plan)) return QOQ_ERR_CUDA;
     if (plan.total * (plan.ctas + 1ll) >= (1ll << 32)) return QOQ_ERR_UNSUPPORTED;

@@ -701,13 +701,14 @@ template <int BT>
 cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
     using C = Cfg<BT>;
     static std::mutex mu;
-    static bool configured[64] = {};
+    static bool configured[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (dev < 64 && !configured[dev]) {
+        if (!configured[dev]) {
             for (auto kern : {w4a8_gemm_kernel<BT, false>, w4a8_gemm_kernel<BT, true>}) {
                 e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));

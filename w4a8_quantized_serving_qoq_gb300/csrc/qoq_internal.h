@@ -8,6 +8,10 @@
 
 namespace qoq {
 
+// Device ordinals the library serves (per-device state is kept in arrays of
+// this size); the entry points return QOQ_ERR_UNSUPPORTED on a higher ordinal.
+constexpr int kMaxDevices = 64;
+
 // ------------------------------------------------------------------------
 // Packed weight format (written by the packer, read by the GEMM).
 // [header: 256 B]

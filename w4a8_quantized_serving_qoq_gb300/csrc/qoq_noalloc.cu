@@ -18,22 +18,24 @@
 
 namespace {
 
-// Fixed scratch shared by every call on a device: 8 MiB, enough for up to
-// 64 tokens per call on a GB300 (152 SMs).  Each GPU that loads the library
-// keeps this array until the process exits.
+// Fixed scratch shared by every call on a device: 8 MiB.  Whether a shape
+// fits depends on the shape, not on M alone: the call needs
+// qoq_gemm_workspace_bytes(M, N, K, group) <= 8 MiB (on a 152-SM GB300 every
+// Llama-3-8B linear layer up to M = 64 fits).  Each GPU that loads the
+// library keeps this array until the process exits.
 constexpr size_t kNoAllocScratchBytes = 8u << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-int g_sms[kMaxDevices] = {};
+void *g_scratch_ptr[qoq::kMaxDevices] = {};
+int g_sms[qoq::kMaxDevices] = {};
 
 // Once per device, with that device current: the device address of the
 // scratch array (the host-side symbol is not a device pointer) and the SM count.
 int setup_current_device(void **ptr, int *sms) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QOQ_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QOQ_ERR_CUDA;
+    if (dev < 0 || dev >= qoq::kMaxDevices) return QOQ_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_scratch_ptr[dev]) {
         void *p = nullptr;
@@ -93,4 +95,27 @@ extern "C" int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, cons
     a.timeout_ns = 2000000000ull;
     a.pdl = false;
     return qoq::launch_gemm(a, plan, s) == cudaSuccess ? QOQ_OK : QOQ_ERR_CUDA;
+}
+
+// Status word of the scratch array (its first 4 bytes), read like
+// qoq_workspace_status reads a caller's workspace.  Each
+// qoq_w4a8_gemm_noalloc call clears the word before it launches, so read it
+// after a call and before the next one on the device.
+extern "C" int qoq_noalloc_status(uint32_t *host_status, qoq_stream_t stream) {
+    if (!host_status) return QOQ_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    int sms = 0;
+    int st = setup_current_device(&scratch, &sms);
+    if (st != QOQ_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, scratch, sizeof(v), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, sizeof(v), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return QOQ_ERR_CUDA;
+    *host_status = v;
+    if (v & 1u) return QOQ_ERR_TIMEOUT;
+    if (v & 2u) return QOQ_ERR_DEVICE;
+    return QOQ_OK;
 }

@@ -65,11 +65,13 @@ def layer_seed(workload_id: int, layer: Layer) -> int:
     return 0 if workload_id == 0 else 1000 * workload_id + layer.layer_index
 
 
-def weights(N: int, K: int, seed: int, sigma: float = 0.02, outliers: int = 2) -> np.ndarray:
-    """fp16 [N][K] weights, seed stream 2*seed."""
+def weights(N: int, K: int, seed: int, sigma: float = 0.02, outliers: int = 2,
+            rows: int | None = None) -> np.ndarray:
+    """fp16 [N][K] weights, seed stream 2*seed; with `rows`, only the first
+    `rows` rows of that matrix (the values fill rows in order)."""
     rng = np.random.default_rng(2 * seed)
     cols = rng.choice(K, size=min(outliers, K), replace=False)
-    W = rng.standard_normal((N, K), dtype=np.float32)
+    W = rng.standard_normal((N if rows is None else min(rows, N), K), dtype=np.float32)
     W *= np.float32(sigma)
     W[:, cols] *= np.float32(10.0)
     return W.astype(np.float16)
