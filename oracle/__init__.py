@@ -60,6 +60,8 @@ def _load():
                 "oracle_gemm_i32_channel": (None, [P, P, P, P, i32, i32, i32, P]),
                 "oracle_gemm_i32_channel_at": (None, [P, P, P, P, i32, i32, i32, P, P, i32, P]),
                 "oracle_epilogue_f64": (None, [P, P, P, i32, i32, P]),
+                "oracle_rmsnorm_f64": (None, [P, P, ctypes.c_double, i32, i32, P]),
+                "oracle_silu_mul_f64": (None, [P, i32, i32, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -222,6 +224,42 @@ def epilogue_f64(acc, s_x, s_w) -> np.ndarray:
     O = np.zeros((M, N), np.float64)
     _load().oracle_epilogue_f64(_p(acc), _p(sx), _p(sw), M, N, _p(O))
     return O
+
+
+# --------------------------------------------------------------------------
+# The fp16 kernels in front of the GEMMs, into which the activation
+# quantization is fused (QServe summary, "QServe系统运行时"; QServe review
+# section 4, step 2)
+# --------------------------------------------------------------------------
+def rmsnorm_f64(X, gamma, eps: float) -> np.ndarray:
+    """Y = gamma * X / sqrt(mean(X^2) + eps) per row, in fp64 (X [M][K],
+    gamma [K] fp16)."""
+    X = _as_half_bits(X)
+    gamma = _as_half_bits(gamma)
+    M, K = X.shape
+    assert gamma.shape == (K,)
+    Y = np.zeros((M, K), np.float64)
+    _load().oracle_rmsnorm_f64(_p(X), _p(gamma), float(eps), M, K, _p(Y))
+    return Y
+
+
+def silu_mul_f64(H) -> np.ndarray:
+    """A = SiLU(G) * U, in fp64, for H = [G | U] of shape [M][2F] (fp16)."""
+    H = _as_half_bits(H)
+    M, F2 = H.shape
+    assert F2 % 2 == 0
+    A = np.zeros((M, F2 // 2), np.float64)
+    _load().oracle_silu_mul_f64(_p(H), M, F2 // 2, _p(A))
+    return A
+
+
+def fp16_within_one_ulp(Y16, Y_ref) -> np.ndarray:
+    """Per element: |Y16 - Y_ref| <= ulp16(|Y_ref|), the bound of an fp16
+    result rounded from an fp32 computation of Y_ref (relative error far below
+    2^-11) -- half an ulp for the final rounding plus the fp32 error."""
+    Y16 = np.asarray(Y16, dtype=np.float64)
+    Y_ref = np.asarray(Y_ref, dtype=np.float64)
+    return np.abs(Y16 - Y_ref) <= fp16_ulp(Y_ref)
 
 
 def fp16_ulp(x) -> np.ndarray:

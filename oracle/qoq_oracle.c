@@ -367,3 +367,51 @@ ORACLE_API void oracle_epilogue_f64(const int32_t *acc, const uint16_t *s_x,
         }
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* The FP16 kernels in front of the GEMMs, into which the QServe runtime     */
+/* fuses the per-token INT8 activation quantization ([QS-summary]           */
+/* "QServe系统运行时"; [QS-review] §4 ②: the norm before the QKV projection  */
+/* and the FFN's first layer, the activation kernel before the FFN's second  */
+/* layer).  Both are written here in fp64 from their definitions.           */
+/*                                                                           */
+/* RMS normalization.  The pages call the norm LayerNorm; the Llama-family  */
+/* blocks of the workloads use its RMS form (no mean subtraction, no bias):  */
+/*   Y[m,k] = gamma[k] * X[m,k] / sqrt(mean_k X[m,k]^2 + eps)                */
+/* X [M][K] and gamma [K] are fp16 bits; Y [M][K] fp64.                      */
+/* ------------------------------------------------------------------------- */
+ORACLE_API void oracle_rmsnorm_f64(const uint16_t *X, const uint16_t *gamma, double eps,
+                                   int M, int K, double *Y) {
+    for (int m = 0; m < M; m++) {
+        const uint16_t *row = X + (size_t)m * K;
+        double ss = 0.0;
+        for (int k = 0; k < K; k++) {
+            double v = (double)oracle_half_to_float(row[k]);
+            ss += v * v;
+        }
+        double denom = sqrt(ss / (double)K + eps);
+        for (int k = 0; k < K; k++) {
+            double v = (double)oracle_half_to_float(row[k]);
+            double gk = (double)oracle_half_to_float(gamma[k]);
+            Y[(size_t)m * K + k] = denom > 0.0 ? gk * v / denom : 0.0;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* SwiGLU activation of the FFN ("01 inference papers and experiments" book  */
+/* chapter, FFN/MLP module ⑤: down = SiLU(gate) ⊙ up · W_down):              */
+/*   A[m,f] = SiLU(G[m,f]) * U[m,f],  SiLU(g) = g / (1 + exp(-g))            */
+/* H [M][2F] is the gate_up projection's fp16 output with the gate in       */
+/* columns 0..F-1 and the up projection in columns F..2F-1; A [M][F] fp64.  */
+/* ------------------------------------------------------------------------- */
+ORACLE_API void oracle_silu_mul_f64(const uint16_t *H, int M, int F, double *A) {
+    for (int m = 0; m < M; m++) {
+        const uint16_t *row = H + (size_t)m * 2 * F;
+        for (int f = 0; f < F; f++) {
+            double g = (double)oracle_half_to_float(row[f]);
+            double u = (double)oracle_half_to_float(row[F + f]);
+            A[(size_t)m * F + f] = g / (1.0 + exp(-g)) * u;
+        }
+    }
+}

@@ -444,3 +444,68 @@ def test_tolerance_helper():
     assert ok.tolist() == [[True, True, False]]
     assert oracle.fp16_ulp(np.array([1.0]))[0] == 2.0 ** -10
     assert oracle.fp16_ulp(np.array([0.0]))[0] == 2.0 ** -24
+
+
+# ------------------------------------------- norm and activation in front of a GEMM --
+def test_rmsnorm_closed_forms():
+    K = 256
+    one = np.ones(K, np.float16)
+    # a constant row with eps = 0 normalizes to sign(c) everywhere
+    X = np.stack([np.full(K, 0.75), np.full(K, -3.0)]).astype(np.float16)
+    Y = oracle.rmsnorm_f64(X, one, 0.0)
+    assert np.allclose(Y[0], 1.0, rtol=0, atol=1e-15) and np.allclose(Y[1], -1.0, rtol=0, atol=1e-15)
+    # a lone nonzero a: a / sqrt(a^2 / K) = sign(a) sqrt(K); the zeros stay zero
+    X = np.zeros((1, K), np.float16)
+    X[0, 7] = -0.5
+    Y = oracle.rmsnorm_f64(X, one, 0.0)
+    assert Y[0, 7] == pytest.approx(-np.sqrt(K), rel=1e-15) and np.count_nonzero(Y) == 1
+    # eps enters under the root: c / sqrt(c^2 + eps); gamma scales each channel
+    g = (np.arange(K) % 5 + 1).astype(np.float16)
+    X = np.full((1, K), 0.5, np.float16)
+    Y = oracle.rmsnorm_f64(X, g, 1e-2)
+    assert np.allclose(Y[0], g.astype(np.float64) * 0.5 / np.sqrt(0.25 + 1e-2), rtol=1e-14, atol=0)
+    # an all-zero row stays zero (0 / sqrt(eps), and 0 / 0 read as 0 when eps = 0)
+    Z = np.zeros((2, K), np.float16)
+    assert not oracle.rmsnorm_f64(Z, one, 1e-6).any() and not oracle.rmsnorm_f64(Z, one, 0.0).any()
+
+
+def test_rmsnorm_vs_torch_cpu():
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    if not hasattr(F, "rms_norm"):
+        pytest.skip("torch without rms_norm")
+    X = synthetic.activations(6, 4096, 31, 4)
+    gamma = (1.0 + 0.1 * np.random.default_rng(3).standard_normal(4096)).astype(np.float16)
+    Y = oracle.rmsnorm_f64(X, gamma, 1e-5)
+    ref = F.rms_norm(torch.from_numpy(X.astype(np.float64)), (4096,),
+                     weight=torch.from_numpy(gamma.astype(np.float64)), eps=1e-5).numpy()
+    assert np.allclose(Y, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_silu_mul_closed_forms_and_library():
+    special = pytest.importorskip("scipy.special")
+    F = 512
+    rng = np.random.default_rng(12)
+    G = (rng.standard_normal((3, F)) * 4).astype(np.float16)
+    U = rng.standard_normal((3, F)).astype(np.float16)
+    G[0, :4] = [0.0, 30.0, -30.0, 1.0]
+    U[0, :4] = [5.0, 1.0, 1.0, 2.0]
+    A = oracle.silu_mul_f64(np.concatenate([G, U], axis=1))
+    g, u = G.astype(np.float64), U.astype(np.float64)
+    # the logistic function from scipy (a library routine): SiLU(g) = g * expit(g)
+    assert np.allclose(A, g * special.expit(g) * u, rtol=1e-14, atol=1e-300)
+    assert A[0, 0] == 0.0                                   # SiLU(0) = 0
+    assert A[0, 1] == pytest.approx(30.0, rel=1e-12)        # SiLU(g) -> g for large g
+    assert abs(A[0, 2]) < 1e-11                             # SiLU(g) -> 0 for very negative g
+    assert A[0, 3] == pytest.approx(2.0 / (1.0 + np.exp(-1.0)) * 1.0 * 1.0, rel=1e-15)
+    # SiLU(g) - SiLU(-g) = g exactly in real arithmetic (odd part of g * sigmoid(g))
+    ones = np.ones_like(G)
+    Ap = oracle.silu_mul_f64(np.concatenate([G, ones], axis=1))
+    Am = oracle.silu_mul_f64(np.concatenate([-G, ones], axis=1))
+    assert np.allclose(Ap - Am, g, rtol=1e-13, atol=1e-13)
+
+
+def test_fp16_one_ulp_helper():
+    ref = np.array([1.0, 1.0, 1.0, 0.0, 3e-8])
+    got = np.array([1.0 + 2 ** -10, 1.0 + 2 ** -9, 1.0 - 2 ** -11, 2 ** -24, 0.0])
+    assert oracle.fp16_within_one_ulp(got, ref).tolist() == [True, False, True, True, True]
