@@ -50,6 +50,8 @@ WORKLOAD = ("Llama-3-8B GEMMs g128, decode M in {1,8,32,64,128,256} + prefill M=
             "{qkv 6144x4096, o 4096x4096, gate_up 28672x4096, down 4096x14336}")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 BLOCKS = {
+    "fused_quant": (1, "Llama-3-8B: RMS norm + per-token INT8 quant (K=4096, the qkv / gate_up input) and "
+                       "SiLU-mul + quant (F=14336, the down input), M in {1,8,32,64,128,256,4096}"),
     "qwen72b": (3, "Qwen1.5-72B-shaped FFN GEMMs g128: {gate_up 59136x8192, down 8192x29568} x M in {64,1024}"),
     "per_channel": (4, "Llama-3-8B gate_up 28672x4096, per-channel W4A8 (zero folded via t_x), M = 1..4096"),
 }
@@ -77,7 +79,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-points", action="store_true", help="skip the per-point timings (and the blocks)")
-    ap.add_argument("--blocks", default="qwen72b,per_channel",
+    ap.add_argument("--blocks", default="fused_quant,qwen72b,per_channel",
                     help="comma list of extra workloads timed point by point ('' for none)")
     ap.add_argument("--layers", default="qkv,o,gate_up,down")
     ap.add_argument("--ms", default="1,8,32,64,128,256,4096",
@@ -601,7 +603,68 @@ def main(argv=None):
 
     # ---- further workloads, point by point ----
     block_out = {}
+
+    def fused_quant_block():
+        """The fused norm / activation + quantization kernels alone (graphs of
+        back-to-back launches, inputs > L2 rotated), against the HBM roof of
+        their bytes, and the unfused chain (torch's fp16 norm / SiLU-mul, then
+        qoq_quant_act_ex) for comparison."""
+        F_ = torch.nn.functional
+        rows = []
+        for M in [m for m in synthetic.DECODE_MS] + [synthetic.PREFILL_M]:
+            for op, K in (("rmsnorm_quant", 4096), ("silu_mul_quant", 14336)):
+                kind = qoq.qoq_gemm_path(M, 28672 if op == "rmsnorm_quant" else 4096, K, 128)
+                kin = K if op == "rmsnorm_quant" else 2 * K
+                nin = max(3, -(-2 * l2_bytes // (2 * M * kin)) + 1)
+                gen = torch.Generator(device=dev)
+                gen.manual_seed(M + K)
+                Xs = [torch.randn((M, kin), generator=gen, device=dev).to(torch.float16) for _ in range(min(nin, 64))]
+                gamma = (1 + 0.1 * torch.randn((K,), generator=gen, device=dev)).to(torch.float16)
+                Qx = torch.empty((M, K), dtype=torch.int8, device=dev)
+                sx = torch.empty((M,), dtype=torch.float16, device=dev)
+                act = torch.empty((qoq.qoq_act_operand_bytes(M, K, kind),), dtype=torch.uint8, device=dev)
+
+                def fused(r):
+                    if op == "rmsnorm_quant":
+                        qoq.qoq_rmsnorm_quant_act(Xs[r % len(Xs)], gamma, 1e-5, Qx, sx, None, act, kind=kind,
+                                                  with_t=False, flags=qoq.QOQ_LAUNCH_OVERLAP)
+                    else:
+                        qoq.qoq_silu_mul_quant_act(Xs[r % len(Xs)], Qx, sx, None, act, kind=kind, with_t=False,
+                                                   flags=qoq.QOQ_LAUNCH_OVERLAP)
+
+                Ybuf = torch.empty((M, K), dtype=torch.float16, device=dev)
+
+                def unfused(r):
+                    Xr = Xs[r % len(Xs)]
+                    if op == "rmsnorm_quant":
+                        torch.mul(F_.rms_norm(Xr, (K,), eps=1e-5), gamma, out=Ybuf)
+                    else:
+                        torch.mul(F_.silu(Xr[:, :K]), Xr[:, K:], out=Ybuf)
+                    qoq.qoq_quant_act_ex(Ybuf, Qx, sx, None, act, kind=kind, with_t=False)
+
+                fused(0)
+                unfused(0)
+                torch.cuda.synchronize()
+                reps = max(args.point_reps, len(Xs))
+                t_f = graph_us(fused, reps)
+                t_u = graph_us(unfused, reps)
+                nbytes = 2 * M * kin + (2 * K if op == "rmsnorm_quant" else 0) + M * K + act.numel() + 2 * M
+                rows.append({"op": op, "M": M, "K": K, "act_kind": kind, "us": round(t_f, 2),
+                             "unfused_us": round(t_u, 2), "bytes": nbytes,
+                             "GBs": round(nbytes / (t_f * 1e-6) / 1e9, 1),
+                             "hbm_frac": round(nbytes / (t_f * 1e-6) / bw, 3)})
+                del Xs
+        tb = sum(r["bytes"] for r in rows)
+        tt = sum(r["us"] for r in rows) * 1e-6
+        return {"workload": BLOCKS["fused_quant"][1], "bound": "hbm",
+                "bytes_weighted_hbm_frac": tb / tt / bw,
+                "fused_vs_unfused_time": sum(r["us"] for r in rows) / sum(r["unfused_us"] for r in rows),
+                "points": rows}
+
     for bname in blocks:
+        if bname == "fused_quant":
+            block_out[bname] = fused_quant_block()
+            continue
         wid, desc = BLOCKS[bname]
         bpts = [make_point(*p) for p in block_points(bname)]
         need = max(qoq.qoq_gemm_workspace_bytes(p["M"], p["layer"].N, p["layer"].K, p["group"]) for p in bpts)

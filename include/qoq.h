@@ -170,6 +170,46 @@ int qoq_quant_act_ex(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
                      int kind, void *act_operand, uint32_t flags, qoq_stream_t stream);
 
 /*
+ * qoq_rmsnorm_quant_act -- RMS normalization fused with the per-token INT8
+ * quantization of qoq_quant_act_ex: the norm in front of the QKV projection
+ * and the FFN's first layer, into which the QServe runtime fuses the
+ * activation quantization so that every GEMM receives INT8 activations
+ * ([QS-summary] "QServe系统运行时"; [QS-review] 4, step 2).  The pages call
+ * the norm LayerNorm; the Llama-family blocks use its RMS form, which this
+ * computes.  Per row m, in fp32:
+ *   r = 1 / sqrt(sum_k X[m,k]^2 / K + eps)   (0 when the root is 0)
+ *   y[m,k] = fp16_rn((X[m,k] * r) * gamma[k])
+ * and then exactly qoq_quant_act_ex on the fp16 row y: Qx, s_x, t_x and the
+ * activation operand of `kind` (act_operand may be NULL).  Y, if not NULL,
+ * receives y [M][K] (fp16): the rows the quantizer saw.
+ * X fp16 [M][K], gamma fp16 [K], Qx int8 [M][K], Y fp16 [M][K] (each 16-byte
+ * aligned), s_x fp16 [M], t_x int32 [M] or NULL.  eps >= 0 and finite
+ * (QOQ_ERR_INVALID_ARG otherwise).  Requirements: M, K > 0, K % 8 == 0
+ * (K % 128 == 0 with an activation operand).  flags: 0 or
+ * QOQ_LAUNCH_OVERLAP.
+ */
+int qoq_rmsnorm_quant_act(const uint16_t *X, const uint16_t *gamma, float eps, int M, int K, int8_t *Qx,
+                          uint16_t *s_x, int32_t *t_x, int kind, void *act_operand, uint16_t *Y, uint32_t flags,
+                          qoq_stream_t stream);
+
+/*
+ * qoq_silu_mul_quant_act -- the SwiGLU activation in front of the FFN's
+ * second layer (down = SiLU(gate) * up, "01 inference papers and
+ * experiments" book chapter, FFN/MLP module), fused with the per-token INT8
+ * quantization ([QS-summary] "QServe系统运行时": quantization fused into the
+ * activation kernel).  H [M][2F] fp16 is the gate_up projection's output,
+ * gate in columns 0..F-1, up in F..2F-1.  Per element, in fp32:
+ *   y[m,f] = fp16_rn((g / (1 + exp(-g))) * u),  g = H[m,f], u = H[m,F+f]
+ * (expf of the CUDA math library, IEEE division and product), then exactly
+ * qoq_quant_act_ex on the fp16 row y [F].  Y (optional) receives y [M][F].
+ * Inputs must be finite with |y| < 65504.  H, Qx, Y 16-byte aligned.
+ * Requirements: M, F > 0, F % 8 == 0 (F % 128 == 0 with an activation
+ * operand).  flags: 0 or QOQ_LAUNCH_OVERLAP.
+ */
+int qoq_silu_mul_quant_act(const uint16_t *H, int M, int F, int8_t *Qx, uint16_t *s_x, int32_t *t_x, int kind,
+                           void *act_operand, uint16_t *Y, uint32_t flags, qoq_stream_t stream);
+
+/*
  * Workspace bytes qoq_w4a8_gemm needs for this shape on the current device:
  * a 256-byte status word area, one arrival counter per persistent CTA and
  * one int32 partial-tile slot (tokens-per-tile x 128) per persistent CTA,

@@ -95,6 +95,8 @@ def load():
                 "qoq_quant_act": (I, [P, I, I, P, P, P, P]),
                 "qoq_act_operand_bytes": (S, [I, I, I]),
                 "qoq_quant_act_ex": (I, [P, I, I, P, P, P, I, P, ctypes.c_uint32, P]),
+                "qoq_rmsnorm_quant_act": (I, [P, P, ctypes.c_float, I, I, P, P, P, I, P, P, ctypes.c_uint32, P]),
+                "qoq_silu_mul_quant_act": (I, [P, I, I, P, P, P, I, P, P, ctypes.c_uint32, P]),
                 "qoq_gemm_workspace_bytes": (S, [I, I, I, I]),
                 "qoq_gemm_workspace_bytes_ex": (S, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
                 "qoq_gemm_path": (I, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
@@ -279,6 +281,61 @@ def qoq_quant_act_ex(X, Qx=None, s_x=None, t_x=None, act=None, kind: int = 2, wi
     _check("qoq_quant_act_ex", load().qoq_quant_act_ex(
         _ptr(X), M, K, _ptr(Qx), _ptr(s_x), _ptr(t_x), int(kind), _ptr(act), int(flags), _stream(stream)))
     return Qx, s_x, t_x, act
+
+
+def _quant_outputs(M, K, device, Qx, s_x, t_x, act, kind, with_t, with_act, Y, with_y):
+    torch = _torch()
+    if Qx is None:
+        Qx = torch.empty((M, K), dtype=torch.int8, device=device)
+    if s_x is None:
+        s_x = torch.empty((M,), dtype=torch.float16, device=device)
+    if t_x is None and with_t:
+        t_x = torch.empty((M,), dtype=torch.int32, device=device)
+    if act is None and with_act:
+        nbytes = qoq_act_operand_bytes(M, K, kind)
+        if nbytes == 0:
+            raise QoqError("qoq_act_operand_bytes", 2)
+        act = torch.empty((nbytes,), dtype=torch.uint8, device=device)
+    if Y is None and with_y:
+        Y = torch.empty((M, K), dtype=torch.float16, device=device)
+    _dev(Qx, torch.int8, "Qx")
+    _dev(s_x, torch.float16, "s_x")
+    _dev(t_x, torch.int32, "t_x")
+    _dev(act, torch.uint8, "act")
+    _dev(Y, torch.float16, "Y")
+    return Qx, s_x, t_x, act, Y
+
+
+def qoq_rmsnorm_quant_act(X, gamma, eps: float = 1e-5, Qx=None, s_x=None, t_x=None, act=None, kind: int = 2,
+                          with_t: bool = True, with_act: bool = True, Y=None, with_y: bool = False,
+                          flags: int = 0, stream=None):
+    """RMS norm of X [M][K] (gamma [K]) fused with the per-token INT8
+    quantization -> (Qx, s_x, t_x, act, Y); Y is the fp16 normalized rows
+    (only with with_y or a given Y)."""
+    torch = _torch()
+    _dev(X, torch.float16, "X")
+    _dev(gamma, torch.float16, "gamma")
+    M, K = X.shape
+    Qx, s_x, t_x, act, Y = _quant_outputs(M, K, X.device, Qx, s_x, t_x, act, kind, with_t, with_act, Y, with_y)
+    _check("qoq_rmsnorm_quant_act", load().qoq_rmsnorm_quant_act(
+        _ptr(X), _ptr(gamma), float(eps), M, K, _ptr(Qx), _ptr(s_x), _ptr(t_x), int(kind), _ptr(act), _ptr(Y),
+        int(flags), _stream(stream)))
+    return Qx, s_x, t_x, act, Y
+
+
+def qoq_silu_mul_quant_act(H, Qx=None, s_x=None, t_x=None, act=None, kind: int = 2, with_t: bool = True,
+                           with_act: bool = True, Y=None, with_y: bool = False, flags: int = 0, stream=None):
+    """SiLU(G) * U of H = [G | U] [M][2F] fused with the per-token INT8
+    quantization -> (Qx, s_x, t_x, act, Y) over F columns."""
+    torch = _torch()
+    _dev(H, torch.float16, "H")
+    M, F2 = H.shape
+    F = F2 // 2
+    Qx, s_x, t_x, act, Y = _quant_outputs(M, F, H.device, Qx, s_x, t_x, act, kind, with_t, with_act, Y, with_y)
+    _check("qoq_silu_mul_quant_act", load().qoq_silu_mul_quant_act(
+        _ptr(H), M, F, _ptr(Qx), _ptr(s_x), _ptr(t_x), int(kind), _ptr(act), _ptr(Y), int(flags),
+        _stream(stream)))
+    return Qx, s_x, t_x, act, Y
 
 
 def qoq_gemm_workspace_bytes(M: int, N: int, K: int, group: int = 128, options=None) -> int:

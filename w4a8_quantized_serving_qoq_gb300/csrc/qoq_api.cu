@@ -194,6 +194,38 @@ int qoq_quant_act_ex(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
                               (flags & QOQ_LAUNCH_OVERLAP) != 0, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int qoq_rmsnorm_quant_act(const uint16_t *X, const uint16_t *gamma, float eps, int M, int K, int8_t *Qx,
+                          uint16_t *s_x, int32_t *t_x, int kind, void *act_operand, uint16_t *Y, uint32_t flags,
+                          qoq_stream_t stream) {
+    if (M <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || eps > 3.0e38f) return QOQ_ERR_INVALID_ARG;  // rejects NaN and inf too
+    if (flags & ~QOQ_LAUNCH_OVERLAP) return QOQ_ERR_UNSUPPORTED;
+    if (act_operand && kind != 1 && kind != 2) return QOQ_ERR_INVALID_ARG;
+    if (K % 8 != 0 || (act_operand && K % 128 != 0)) return QOQ_ERR_UNSUPPORTED;
+    if (!X || !gamma || !Qx || !s_x) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(gamma, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) ||
+        (t_x && !aligned(t_x, 4)) || (act_operand && !aligned(act_operand, 16)) || (Y && !aligned(Y, 16)))
+        return QOQ_ERR_MISALIGNED;
+    return cuda_status(qoq::launch_rmsnorm_quant(X, gamma, eps, Y, M, K, Qx, s_x, t_x, act_operand ? kind : 0,
+                                                 act_operand, (flags & QOQ_LAUNCH_OVERLAP) != 0,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int qoq_silu_mul_quant_act(const uint16_t *H, int M, int F, int8_t *Qx, uint16_t *s_x, int32_t *t_x, int kind,
+                           void *act_operand, uint16_t *Y, uint32_t flags, qoq_stream_t stream) {
+    if (M <= 0 || F <= 0) return QOQ_ERR_INVALID_ARG;
+    if (flags & ~QOQ_LAUNCH_OVERLAP) return QOQ_ERR_UNSUPPORTED;
+    if (act_operand && kind != 1 && kind != 2) return QOQ_ERR_INVALID_ARG;
+    if (F % 8 != 0 || (act_operand && F % 128 != 0)) return QOQ_ERR_UNSUPPORTED;
+    if (!H || !Qx || !s_x) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(H, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) || (t_x && !aligned(t_x, 4)) ||
+        (act_operand && !aligned(act_operand, 16)) || (Y && !aligned(Y, 16)))
+        return QOQ_ERR_MISALIGNED;
+    return cuda_status(qoq::launch_silu_mul_quant(H, Y, M, F, Qx, s_x, t_x, act_operand ? kind : 0, act_operand,
+                                                  (flags & QOQ_LAUNCH_OVERLAP) != 0,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gemm_options *opt) {
     if (check_gemm_shape(M, N, K, group) != QOQ_OK || check_options(opt) != QOQ_OK) return 0;
     qoq::GemmPlan plan;

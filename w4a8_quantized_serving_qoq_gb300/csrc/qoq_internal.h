@@ -110,6 +110,14 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path =
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
                              int32_t *t_x, int act_kind, void *act_operand, bool pdl, cudaStream_t stream);
+// The same quantization of rows produced by the fp16 kernel in front of the
+// GEMM, fused into it: RMS norm of X [M][K] (gamma [K], eps), or SiLU(G) * U
+// of H = [G | U] [M][2F].  Y (optional) receives the fp16 rows quantized.
+cudaError_t launch_rmsnorm_quant(const uint16_t *X, const uint16_t *gamma, float eps, uint16_t *Y, int M, int K,
+                                 int8_t *Qx, uint16_t *s_x, int32_t *t_x, int act_kind, void *act_operand,
+                                 bool pdl, cudaStream_t stream);
+cudaError_t launch_silu_mul_quant(const uint16_t *H, uint16_t *Y, int M, int F, int8_t *Qx, uint16_t *s_x,
+                                  int32_t *t_x, int act_kind, void *act_operand, bool pdl, cudaStream_t stream);
 // Activation operand of the given kind from already quantized activations.
 cudaError_t launch_act_operand(const int8_t *Qx, int M, int K, int act_kind, void *act_operand,
                                cudaStream_t stream);

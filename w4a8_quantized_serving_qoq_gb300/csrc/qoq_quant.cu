@@ -110,48 +110,146 @@ __device__ __forceinline__ uint2 int8x4_to_f16x4(uint32_t w) {
 
 constexpr int kActCache = 4;  // 16-byte items per thread kept in registers between the passes
 
-// One CTA per token row.  s_x = fp16(max|x| / 127); Qx = clamp(rne(x / s_x), -127, 127);
-// an all-zero scale gives an all-zero row; t_x = row sum of Qx.  kAct
-// selects an activation operand written alongside: 0 none, 1 the fp16 copy
-// of Qx, 2 the fp8-path planes of u = Qx + 128 and the per-group sums t_g.
+// Where the fp16 row the quantizer sees comes from: the activations
+// themselves, or the output of the fp16 kernel in front of the GEMM, into
+// which the QServe runtime fuses the quantization ("QServe: W4A8KV4
+// Quantization and System Co-design for Efficient LLM Serving", section
+// "QServe系统运行时"): the norm before the QKV projection and the FFN's first
+// layer, the SwiGLU activation before the FFN's second layer.
+enum : int {
+    kSrcX = 0,        // X [M][K]
+    kSrcRmsNorm = 1,  // fp16(X * r * gamma), r = 1 / sqrt(mean_k X^2 + eps), X [M][K]
+    kSrcSiluMul = 2,  // fp16(SiLU(G) * U) of H = [G | U] [M][2K], SiLU(g) = g / (1 + e^-g)
+};
+
+struct RowSrc {
+    const uint16_t *X;      // X, or H for kSrcSiluMul
+    const uint16_t *gamma;  // [K] (kSrcRmsNorm)
+    float eps;              // (kSrcRmsNorm)
+    uint16_t *Y;            // optional [M][K]: the fp16 rows the quantizer saw
+};
+
+struct AddF { __device__ float operator()(float a, float b) const { return __fadd_rn(a, b); } };
+
+__device__ __forceinline__ float sumsq8(const uint4 v, float ss) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float a = h2f(static_cast<uint16_t>(w[j] & 0xffffu)), b = h2f(static_cast<uint16_t>(w[j] >> 16));
+        ss = __fmaf_rn(a, a, ss);
+        ss = __fmaf_rn(b, b, ss);
+    }
+    return ss;
+}
+
+// Eight normalized values: fp16((x * r) * gamma), each product rounded in fp32.
+__device__ __forceinline__ uint4 norm8(const uint4 x, const uint4 g, float r) {
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, gs[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = f2h_rn(__fmul_rn(__fmul_rn(h2f(static_cast<uint16_t>(xs[j] & 0xffffu)), r),
+                                             h2f(static_cast<uint16_t>(gs[j] & 0xffffu))));
+        const uint32_t hi = f2h_rn(__fmul_rn(__fmul_rn(h2f(static_cast<uint16_t>(xs[j] >> 16)), r),
+                                             h2f(static_cast<uint16_t>(gs[j] >> 16))));
+        o[j] = lo | (hi << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// fp16(SiLU(g) * u) in fp32: expf (the CUDA math library's), an IEEE
+// division and product; g -> -inf gives e^-g = inf and SiLU = -0.
+__device__ __forceinline__ float silu_mul1(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+__device__ __forceinline__ uint4 silu8(const uint4 g, const uint4 u) {
+    const uint32_t gs[4] = {g.x, g.y, g.z, g.w}, us[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = f2h_rn(silu_mul1(h2f(static_cast<uint16_t>(gs[j] & 0xffffu)),
+                                             h2f(static_cast<uint16_t>(us[j] & 0xffffu))));
+        const uint32_t hi = f2h_rn(silu_mul1(h2f(static_cast<uint16_t>(gs[j] >> 16)), h2f(static_cast<uint16_t>(us[j] >> 16))));
+        o[j] = lo | (hi << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// One CTA per token row.  The row is the fp16 row of the source (kSrc);
+// s_x = fp16(max|x| / 127); Qx = clamp(rne(x / s_x), -127, 127); an all-zero
+// scale gives an all-zero row; t_x = row sum of Qx.  kAct selects an
+// activation operand written alongside: 0 none, 1 the fp16 copy of Qx, 2 the
+// fp8-path planes of u = Qx + 128 and the per-group sums t_g (the last row's
+// CTA also zero-fills the padding columns M .. Mp-1 of t_g).
 // The trip count of every loop is uniform across the CTA (blockDim.x is a
 // multiple of 32), so the half-warp shuffles that sum one 128-k group (16
-// items of 8) always run with every lane present.
-template <int kAct>
-__global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, int8_t *__restrict__ Qx,
+// items of 8) always run with every lane present.  A source item is
+// recomputed from the same loads with the same rounded operations wherever
+// it is needed again, so every pass sees identical fp16 values.
+template <int kAct, int kSrc>
+__global__ void __launch_bounds__(kSrc == kSrcX ? 1024 : 512) quant_act_kernel(const RowSrc src, int M, int K, int8_t *__restrict__ Qx,
                                  uint16_t *__restrict__ s_x, int32_t *__restrict__ t_x,
                                  uint8_t *__restrict__ act) {
     __shared__ float shf[32];
     __shared__ int shi[32];
     // Under programmatic dependent launch: let the next kernel start
-    // launching, then wait for the previous one before reading X or writing.
-    // The row is prefetched into L2 first (the row is 16-byte aligned and a
-    // multiple of 16 bytes, K % 8 == 0): the wait covers the previous
-    // kernel's writes, and L2 holds the current data of every line.
+    // launching, then wait for the previous one before reading the source
+    // or writing.  The source row is prefetched into L2 first (16-byte
+    // aligned, a multiple of 16 bytes: K % 8 == 0): the wait covers the
+    // previous kernel's writes, and L2 holds the current data of every line.
     const size_t m = blockIdx.x;
-    const uint4 *row = reinterpret_cast<const uint4 *>(X + m * K);
+    const uint4 *row = reinterpret_cast<const uint4 *>(src.X + m * (kSrc == kSrcSiluMul ? 2 * static_cast<size_t>(K) : K));
+    const uint4 *urow = row + (K >> 3);  // up half of an [G | U] row
+    const uint4 *grow = reinterpret_cast<const uint4 *>(src.gamma);
     if (threadIdx.x == 0) {
         griddep_launch_dependents();
         prefetch_l2_bulk(row, static_cast<uint32_t>(K) * 2u);
+        if (kSrc == kSrcSiluMul) prefetch_l2_bulk(urow, static_cast<uint32_t>(K) * 2u);
     }
     griddep_wait();
     const int nv = K >> 3, bd = blockDim.x, tid = threadIdx.x;
     uint4 cache[kActCache];
+    float r = 0.f;
+    if constexpr (kSrc == kSrcRmsNorm) {
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < kActCache; ++j) {
+            const int i = tid + j * bd;
+            cache[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < nv) cache[j] = __ldg(row + i);
+            ss = sumsq8(cache[j], ss);
+        }
+        for (int i = tid + kActCache * bd; i < nv; i += bd) ss = sumsq8(__ldg(row + i), ss);
+        ss = block_reduce(ss, AddF(), shf, 0.f);
+        const float v = __fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), src.eps);
+        r = v > 0.f ? __frsqrt_rn(v) : 0.f;  // an all-zero row with eps = 0 stays zero
+    }
+    // fp16 item i (8 values) of the row the quantizer sees.
+    auto item = [&](int i) -> uint4 {
+        if constexpr (kSrc == kSrcRmsNorm) return norm8(__ldg(row + i), __ldg(grow + i), r);
+        else if constexpr (kSrc == kSrcSiluMul) return silu8(__ldg(row + i), __ldg(urow + i));
+        else return __ldg(row + i);
+    };
     float amax = 0.f;
 #pragma unroll
     for (int j = 0; j < kActCache; ++j) {
         const int i = tid + j * bd;
-        cache[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (i < nv) cache[j] = __ldg(row + i);
+        if constexpr (kSrc == kSrcRmsNorm) {
+            cache[j] = i < nv ? norm8(cache[j], __ldg(grow + i), r) : make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            cache[j] = i < nv ? item(i) : make_uint4(0u, 0u, 0u, 0u);
+        }
         amax = amax8(cache[j], amax);
     }
-    for (int i = tid + kActCache * bd; i < nv; i += bd) amax = amax8(__ldg(row + i), amax);
+    for (int i = tid + kActCache * bd; i < nv; i += bd) amax = amax8(item(i), amax);
     amax = block_reduce(amax, MaxOp(), shf, 0.f);
     const uint16_t sbits = f2h_rn(__fdiv_rn(amax, 127.0f));
     const float sf = h2f(sbits);
     const float inv = sf != 0.f ? __frcp_rn(sf) : 0.f;
 
     uint2 *qrow = reinterpret_cast<uint2 *>(Qx + m * K);
+    uint4 *yrow = (kSrc != kSrcX && src.Y) ? reinterpret_cast<uint4 *>(src.Y + m * K) : nullptr;
     uint2 *hrow = nullptr, *lrow = nullptr;
     uint4 *frow = nullptr;
     int32_t *tg = nullptr;
@@ -169,6 +267,7 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
         if (i < nv) {
             q = quant8(v, sf, inv, &part);
             qrow[i] = q;
+            if (yrow) yrow[i] = v;
         }
         tsum += part;
         if (kAct == 1 && i < nv) {
@@ -184,7 +283,12 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
             }
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if ((tid & 15) == 0 && i < nv) tg[static_cast<size_t>(i >> 4) * pitch + m] = part;
+            if ((tid & 15) == 0 && i < nv) {
+                int32_t *tcol = tg + static_cast<size_t>(i >> 4) * pitch;
+                tcol[m] = part;
+                if (m + 1 == static_cast<size_t>(M))
+                    for (int mm = M; mm < pitch; ++mm) tcol[mm] = 0;
+            }
         }
     };
 #pragma unroll
@@ -192,7 +296,7 @@ __global__ void quant_act_kernel(const uint16_t *__restrict__ X, int M, int K, i
         if (j * bd < nv) emit(tid + j * bd, cache[j]);
     for (int base = kActCache * bd; base < nv; base += bd) {
         const int i = base + tid;
-        emit(i, i < nv ? __ldg(row + i) : make_uint4(0u, 0u, 0u, 0u));
+        emit(i, i < nv ? item(i) : make_uint4(0u, 0u, 0u, 0u));
     }
     if (t_x) tsum = block_reduce(tsum, SumOp(), shi, 0);  // t_x is uniform across the CTA
     if (tid == 0) {
@@ -242,7 +346,12 @@ __global__ void act_operand_kernel(const int8_t *__restrict__ Qx, int M, int K, 
         }
 #pragma unroll
         for (int o = 4; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if ((threadIdx.x & 7) == 0 && i < nv) tg[static_cast<size_t>(i >> 3) * pitch + m] = part;
+        if ((threadIdx.x & 7) == 0 && i < nv) {
+            int32_t *tcol = tg + static_cast<size_t>(i >> 3) * pitch;
+            tcol[m] = part;
+            if (m + 1 == static_cast<size_t>(M))
+                for (int mm = M; mm < pitch; ++mm) tcol[mm] = 0;  // padding columns
+        }
     }
 }
 
@@ -319,23 +428,48 @@ __global__ void quantize_channel_kernel(const uint16_t *__restrict__ W, int K,
 
 }  // namespace
 
-cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
-                             int32_t *t_x, int act_kind, void *act_operand, bool pdl, cudaStream_t stream) {
+namespace {
+template <int kSrc>
+cudaError_t launch_quant_src(const RowSrc &src, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x,
+                             int act_kind, uint8_t *act, bool pdl, cudaStream_t stream) {
     // One CTA per row; about two 16-byte items per thread keeps the per-row
     // latency short (few rows) without idle warps; many rows: 256 threads.
     const int nv = K / 8;
     int threads = (nv / 2 + 31) / 32 * 32;
-    threads = threads < 128 ? 128 : (threads > 1024 ? 1024 : threads);
+    const int max_threads = kSrc == kSrcX ? 1024 : 512;  // the kernels' launch bounds
+    threads = threads < 128 ? 128 : (threads > max_threads ? max_threads : threads);
     if (M >= 296) threads = 256;
     const dim3 grid(M), block(threads);
-    uint8_t *act = static_cast<uint8_t *>(act_operand);
     if (!act) act_kind = 0;
     if (act_kind == 1)
-        return launch_kernel(quant_act_kernel<1>, grid, block, 0, stream, pdl, X, M, K, Qx, s_x, t_x, act);
+        return launch_kernel(quant_act_kernel<1, kSrc>, grid, block, 0, stream, pdl, src, M, K, Qx, s_x, t_x, act);
     if (act_kind == 2)
-        return launch_kernel(quant_act_kernel<2>, grid, block, 0, stream, pdl, X, M, K, Qx, s_x, t_x, act);
-    return launch_kernel(quant_act_kernel<0>, grid, block, 0, stream, pdl, X, M, K, Qx, s_x, t_x,
+        return launch_kernel(quant_act_kernel<2, kSrc>, grid, block, 0, stream, pdl, src, M, K, Qx, s_x, t_x, act);
+    return launch_kernel(quant_act_kernel<0, kSrc>, grid, block, 0, stream, pdl, src, M, K, Qx, s_x, t_x,
                          static_cast<uint8_t *>(nullptr));
+}
+}  // namespace
+
+cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
+                             int32_t *t_x, int act_kind, void *act_operand, bool pdl, cudaStream_t stream) {
+    const RowSrc src{X, nullptr, 0.f, nullptr};
+    return launch_quant_src<kSrcX>(src, M, K, Qx, s_x, t_x, act_kind, static_cast<uint8_t *>(act_operand), pdl,
+                                   stream);
+}
+
+cudaError_t launch_rmsnorm_quant(const uint16_t *X, const uint16_t *gamma, float eps, uint16_t *Y, int M, int K,
+                                 int8_t *Qx, uint16_t *s_x, int32_t *t_x, int act_kind, void *act_operand,
+                                 bool pdl, cudaStream_t stream) {
+    const RowSrc src{X, gamma, eps, Y};
+    return launch_quant_src<kSrcRmsNorm>(src, M, K, Qx, s_x, t_x, act_kind, static_cast<uint8_t *>(act_operand),
+                                         pdl, stream);
+}
+
+cudaError_t launch_silu_mul_quant(const uint16_t *H, uint16_t *Y, int M, int F, int8_t *Qx, uint16_t *s_x,
+                                  int32_t *t_x, int act_kind, void *act_operand, bool pdl, cudaStream_t stream) {
+    const RowSrc src{H, nullptr, 0.f, Y};
+    return launch_quant_src<kSrcSiluMul>(src, M, F, Qx, s_x, t_x, act_kind, static_cast<uint8_t *>(act_operand),
+                                         pdl, stream);
 }
 
 cudaError_t launch_act_operand(const int8_t *Qx, int M, int K, int act_kind, void *act_operand,
