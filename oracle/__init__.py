@@ -62,6 +62,8 @@ def _load():
                 "oracle_epilogue_f64": (None, [P, P, P, i32, i32, P]),
                 "oracle_rmsnorm_f64": (None, [P, P, ctypes.c_double, i32, i32, P]),
                 "oracle_silu_mul_f64": (None, [P, i32, i32, P]),
+                "oracle_kv4_quantize": (None, [P, i32, i32, P, P, P]),
+                "oracle_kv4_attention_f64": (None, [P, i32, i32, i32, P, P, P, P, P, P, ctypes.c_double, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -251,6 +253,39 @@ def silu_mul_f64(H) -> np.ndarray:
     A = np.zeros((M, F2 // 2), np.float64)
     _load().oracle_silu_mul_f64(_p(H), M, F2 // 2, _p(A))
     return A
+
+
+# --------------------------------------------------------------------------
+# KV4 cache quantization and decode attention (QServe summary, KV cache
+# management in "QServe系统运行时" and "QServe中的KV4注意力"; QServe review 3.2)
+# --------------------------------------------------------------------------
+def kv4_quantize(x):
+    """Per-vector asymmetric UINT4 with fp16 scale and zero: x fp16 [n][d] ->
+    (codes u8 [n][d], s fp16 [n], z fp16 [n]); x ~ (codes - z) * s."""
+    x = _as_half_bits(x)
+    n, d = x.shape
+    q = np.zeros((n, d), np.uint8)
+    s = np.zeros(n, np.uint16)
+    z = np.zeros(n, np.uint16)
+    _load().oracle_kv4_quantize(_p(x), n, d, _p(q), _p(s), _p(z))
+    return q, s.view(np.float16), z.view(np.float16)
+
+
+def kv4_attention_f64(Q, Kq, Ks, Kz, Vq, Vs, Vz, scale: float) -> np.ndarray:
+    """softmax(scale * Q Khat^T) Vhat for the G query heads of one KV head
+    and one sequence, in fp64: Q fp16 [G][d]; K/V codes [L][d], scales and
+    zeros fp16 [L] -> O [G][d]."""
+    Q = _as_half_bits(Q)
+    G, d = Q.shape
+    Kq = np.ascontiguousarray(Kq, dtype=np.uint8)
+    Vq = np.ascontiguousarray(Vq, dtype=np.uint8)
+    L = Kq.shape[0]
+    assert L >= 1 and Kq.shape == (L, d) and Vq.shape == (L, d)
+    Ks, Kz, Vs, Vz = (_as_half_bits(a) for a in (Ks, Kz, Vs, Vz))
+    O = np.zeros((G, d), np.float64)
+    _load().oracle_kv4_attention_f64(_p(Q), G, d, L, _p(Kq), _p(Ks), _p(Kz), _p(Vq), _p(Vs), _p(Vz),
+                                     float(scale), _p(O))
+    return O
 
 
 def fp16_within_one_ulp(Y16, Y_ref) -> np.ndarray:

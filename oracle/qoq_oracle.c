@@ -415,3 +415,92 @@ ORACLE_API void oracle_silu_mul_f64(const uint16_t *H, int M, int F, double *A) 
         }
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* KV4: per-head dynamic INT4 quantization of the KV cache ([QS-summary]    */
+/* "QServe系统运行时", KV cache management: paged cache, and right after the */
+/* quantized KV features of each page the per-head FP16 scale and zero,     */
+/* updated online; [QS-review] §3.2 "KV 缓存管理").  Each key or value      */
+/* vector of one token and one head (d values) gets eq. 1 of "整数量化"     */
+/* with an FP16 scale and an FP16 zero point:                                */
+/*   lo = min x, hi = max x                                                  */
+/*   s = fp16_rn((hi - lo) / 15)   (1.0 when that is 0)                      */
+/*   z = fp16_rn(rne(-lo / s))     (an integer, kept as FP16)                */
+/*   q = clamp(rne(x / s) + z, 0, 15)                                        */
+/* so that x is reconstructed as (q - z) * s.  Divisions are IEEE fp32,      */
+/* rne = round half to even.  x [n][d] fp16 bits; q [n][d] one code per      */
+/* byte; s, z [n] fp16 bits.                                                 */
+/* ------------------------------------------------------------------------- */
+ORACLE_API void oracle_kv4_quantize(const uint16_t *x, int n, int d, uint8_t *q,
+                                    uint16_t *s, uint16_t *z) {
+    for (int i = 0; i < n; i++) {
+        const uint16_t *v = x + (size_t)i * d;
+        float lo = oracle_half_to_float(v[0]), hi = lo;
+        for (int k = 1; k < d; k++) {
+            float f = oracle_half_to_float(v[k]);
+            if (f < lo) lo = f;
+            if (f > hi) hi = f;
+        }
+        uint16_t sh = oracle_float_to_half_rn((hi - lo) / 15.0f);
+        if ((sh & 0x7fff) == 0) sh = 0x3c00;
+        float sf = oracle_half_to_float(sh);
+        int64_t zi = oracle_rne_f32(-lo / sf);
+        uint16_t zh = oracle_float_to_half_rn((float)zi);
+        float zf = oracle_half_to_float(zh); /* an integer: rne result, kept as fp16 */
+        s[i] = sh;
+        z[i] = zh;
+        for (int k = 0; k < d; k++) {
+            int64_t c = oracle_rne_f32(oracle_half_to_float(v[k]) / sf) + (int64_t)zf;
+            q[(size_t)i * d + k] = (uint8_t)clamp64(c, 0, 15);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Decode attention over a KV4 cache, in fp64 ([QS-summary] "QServe中的KV4  */
+/* 注意力"; [QS-review] §4 step ④: the attention of the decode step reads   */
+/* the INT4 K/V, dequantizes, and computes softmax(q K^T) V).  One query    */
+/* token of one sequence; the G query heads of one KV head (grouped-query   */
+/* attention share the KV head); L cached tokens:                           */
+/*   Khat[t,k] = (Kq[t,k] - Kz[t]) * Ks[t],  Vhat likewise                  */
+/*   S[h,t] = scale * sum_k Q[h,k] * Khat[t,k]                              */
+/*   P[h,t] = exp(S[h,t] - max_t S[h,t]) / sum_t exp(...)                   */
+/*   O[h,k] = sum_t P[h,t] * Vhat[t,k]                                      */
+/* Q [G][d] fp16 bits; Kq, Vq [L][d] codes; Ks, Kz, Vs, Vz [L] fp16 bits;    */
+/* O [G][d] fp64.  L >= 1.                                                   */
+/* ------------------------------------------------------------------------- */
+ORACLE_API void oracle_kv4_attention_f64(const uint16_t *Q, int G, int d, int L,
+                                         const uint8_t *Kq, const uint16_t *Ks, const uint16_t *Kz,
+                                         const uint8_t *Vq, const uint16_t *Vs, const uint16_t *Vz,
+                                         double scale, double *O) {
+    double *S = (double *)malloc(sizeof(double) * (size_t)L);
+    if (!S) return;
+    for (int h = 0; h < G; h++) {
+        double mx = -INFINITY;
+        for (int t = 0; t < L; t++) {
+            double ks = (double)oracle_half_to_float(Ks[t]);
+            double kz = (double)oracle_half_to_float(Kz[t]);
+            double acc = 0.0;
+            for (int k = 0; k < d; k++) {
+                double kh = ((double)Kq[(size_t)t * d + k] - kz) * ks;
+                acc += (double)oracle_half_to_float(Q[(size_t)h * d + k]) * kh;
+            }
+            S[t] = scale * acc;
+            if (S[t] > mx) mx = S[t];
+        }
+        double den = 0.0;
+        for (int t = 0; t < L; t++) {
+            S[t] = exp(S[t] - mx);
+            den += S[t];
+        }
+        for (int k = 0; k < d; k++) O[(size_t)h * d + k] = 0.0;
+        for (int t = 0; t < L; t++) {
+            double p = S[t] / den;
+            double vs = (double)oracle_half_to_float(Vs[t]);
+            double vz = (double)oracle_half_to_float(Vz[t]);
+            for (int k = 0; k < d; k++)
+                O[(size_t)h * d + k] += p * ((double)Vq[(size_t)t * d + k] - vz) * vs;
+        }
+    }
+    free(S);
+}

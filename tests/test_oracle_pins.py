@@ -509,3 +509,93 @@ def test_fp16_one_ulp_helper():
     ref = np.array([1.0, 1.0, 1.0, 0.0, 3e-8])
     got = np.array([1.0 + 2 ** -10, 1.0 + 2 ** -9, 1.0 - 2 ** -11, 2 ** -24, 0.0])
     assert oracle.fp16_within_one_ulp(got, ref).tolist() == [True, False, True, True, True]
+
+
+# ------------------------------------------------------------------ KV4 cache --
+def _kv(n, d, seed, outliers=0):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((n, d)).astype(np.float32)
+    if outliers:
+        x[:, rng.choice(d, outliers, replace=False)] *= 10.0   # fixed outlier channels of a key head
+    return x.astype(np.float16)
+
+
+def test_kv4_quantize_vs_numpy_fp32():
+    """Scale, zero and codes bit for bit against numpy's IEEE fp32 arithmetic,
+    its binary16 converter and numpy.rint (half-even); includes a constant
+    vector (scale guard) and all-positive / all-negative vectors."""
+    x = _kv(40, 128, 5, outliers=3)
+    x[0] = np.float16(0.75)
+    x[1] = np.abs(x[1]) + np.float16(1.0)
+    x[2] = -np.abs(x[2]) - np.float16(2.0)
+    q, s, z = oracle.kv4_quantize(x)
+    xf = x.astype(np.float32)
+    lo, hi = xf.min(axis=1), xf.max(axis=1)
+    s_ref = ((hi - lo) / np.float32(15)).astype(np.float16)
+    s_ref[s_ref == 0] = np.float16(1.0)
+    sf = s_ref.astype(np.float32)
+    z_ref = np.rint(-lo / sf).astype(np.float16)
+    q_ref = np.clip(np.rint(xf / sf[:, None]) + z_ref.astype(np.float32)[:, None], 0, 15)
+    assert np.array_equal(s.view(np.uint16), s_ref.view(np.uint16))
+    assert np.array_equal(z.view(np.uint16), z_ref.view(np.uint16))
+    assert np.array_equal(q, q_ref.astype(np.uint8))
+    # all-positive vector: negative zero point; all-negative: zero point above 15
+    assert float(z[1]) < 0 and float(z[2]) > 15
+    # reconstruction error: half a level, or one level where the top code clips
+    rec = (q.astype(np.float64) - z.astype(np.float64)[:, None]) * s.astype(np.float64)[:, None]
+    assert (np.abs(rec - x.astype(np.float64)) <= 1.001 * s.astype(np.float64)[:, None]).all()
+    assert rec[0, 0] == 1.0 and (q[0] == 0).all()      # constant 0.75: s = 1, z = -1
+
+
+def test_kv4_quantize_constructed_ties():
+    """s = 1.875 / 15 = 0.125 exactly; rne(2.5) = 2 for the zero point and
+    half-even code ties (every value exact in fp16)."""
+    s = 0.125
+    v = np.zeros(128)
+    v[0], v[1] = -2.5 * s, 1.875 - 2.5 * s
+    v[2:8] = np.array([0.5, 1.5, -0.5, -1.5, 2.5, 3.5]) * s
+    v[8:] = 0.5 * s
+    x = v[None, :].astype(np.float16)
+    assert np.array_equal(x.astype(np.float64)[0], v)
+    q, sc, z = oracle.kv4_quantize(x)
+    assert float(sc[0]) == s and float(z[0]) == 2.0
+    assert list(q[0, :8]) == [0, 14, 2, 4, 2, 0, 4, 6]
+
+
+def _deq(q, s, z):
+    return (q.astype(np.float64) - z.astype(np.float64)[:, None]) * s.astype(np.float64)[:, None]
+
+
+def test_kv4_attention_closed_forms():
+    d = 128
+    Q = _kv(4, d, 6)
+    Kq, Ks, Kz = oracle.kv4_quantize(_kv(9, d, 7, outliers=2))
+    Vq, Vs, Vz = oracle.kv4_quantize(_kv(9, d, 8))
+    # one cached token: the output is that token's value for every head
+    O = oracle.kv4_attention_f64(Q, Kq[:1], Ks[:1], Kz[:1], Vq[:1], Vs[:1], Vz[:1], 0.088)
+    assert np.allclose(O, np.broadcast_to(_deq(Vq[:1], Vs[:1], Vz[:1]), (4, d)), rtol=0, atol=1e-15)
+    # identical keys: uniform attention, the mean of the values
+    Kr = np.repeat(Kq[:1], 9, axis=0)
+    O = oracle.kv4_attention_f64(Q, Kr, np.repeat(Ks[:1], 9), np.repeat(Kz[:1], 9), Vq, Vs, Vz, 0.088)
+    assert np.allclose(O, np.broadcast_to(_deq(Vq, Vs, Vz).mean(axis=0), (4, d)), rtol=1e-13, atol=1e-13)
+    # a key far ahead of the others takes all the weight
+    Q1 = np.zeros((1, d), np.float16)
+    Q1[0, :] = 1.0
+    Kq2 = np.zeros((3, d), np.uint8)
+    Kq2[1] = 15
+    one = np.ones(3, np.float16)
+    zero = np.zeros(3, np.float16)
+    O = oracle.kv4_attention_f64(Q1, Kq2, one, zero, Vq[:3], Vs[:3], Vz[:3], 1.0)
+    assert np.allclose(O[0], _deq(Vq[1:2], Vs[1:2], Vz[1:2])[0], rtol=0, atol=1e-12)
+
+
+def test_kv4_attention_vs_scipy_softmax():
+    special = pytest.importorskip("scipy.special")
+    d, L, G = 128, 77, 4
+    Q = _kv(G, d, 9)
+    Kq, Ks, Kz = oracle.kv4_quantize(_kv(L, d, 10, outliers=2))
+    Vq, Vs, Vz = oracle.kv4_quantize(_kv(L, d, 11))
+    scale = 1.0 / np.sqrt(d)
+    O = oracle.kv4_attention_f64(Q, Kq, Ks, Kz, Vq, Vs, Vz, scale)
+    P = special.softmax(scale * Q.astype(np.float64) @ _deq(Kq, Ks, Kz).T, axis=1)
+    assert np.allclose(O, P @ _deq(Vq, Vs, Vz), rtol=1e-12, atol=1e-12)
