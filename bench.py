@@ -52,6 +52,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 BLOCKS = {
     "fused_quant": (1, "Llama-3-8B: RMS norm + per-token INT8 quant (K=4096, the qkv / gate_up input) and "
                        "SiLU-mul + quant (F=14336, the down input), M in {1,8,32,64,128,256,4096}"),
+    "kv4_attention": (1, "Llama-3-8B decode attention over the KV4 cache (32 query / 8 KV heads, head dim 128): "
+                         "batch 64 x lengths 512..1536 and batch 8 x 8192"),
     "qwen72b": (3, "Qwen1.5-72B-shaped FFN GEMMs g128: {gate_up 59136x8192, down 8192x29568} x M in {64,1024}"),
     "per_channel": (4, "Llama-3-8B gate_up 28672x4096, per-channel W4A8 (zero folded via t_x), M = 1..4096"),
 }
@@ -79,7 +81,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-points", action="store_true", help="skip the per-point timings (and the blocks)")
-    ap.add_argument("--blocks", default="fused_quant,qwen72b,per_channel",
+    ap.add_argument("--blocks", default="fused_quant,kv4_attention,qwen72b,per_channel",
                     help="comma list of extra workloads timed point by point ('' for none)")
     ap.add_argument("--layers", default="qkv,o,gate_up,down")
     ap.add_argument("--ms", default="1,8,32,64,128,256,4096",
@@ -661,9 +663,69 @@ def main(argv=None):
                 "fused_vs_unfused_time": sum(r["us"] for r in rows) / sum(r["unfused_us"] for r in rows),
                 "points": rows}
 
+    def kv4_block():
+        """Decode attention over the KV4 cache alone (graphs of back-to-back
+        launches rotating over KV pools that together exceed twice the L2),
+        against the HBM roof of its bytes: the 4-bit K and V codes with their
+        fp16 scale and zero per token and head, Q and O."""
+        rows = []
+        hq, hkv, D = 32, 8, 128
+        for name, B, lo, hi in (("batch64_len512-1536", 64, 512, 1536), ("batch8_len8192", 8, 8192, 8192)):
+            rng = np.random.default_rng(B + lo)
+            lens = rng.integers(lo, hi + 1, B).astype(np.int32)
+            npg = (lens + 63) // 64
+            max_pages = int(npg.max())
+            num_pages = int(npg.sum())
+            page_b = qoq.qoq_kv4_page_bytes(hkv)
+            pool_bytes = num_pages * page_b
+            npools = max(3, -(-2 * l2_bytes // pool_bytes) + 1)
+            tab = np.full((B, max_pages), -1, np.int32)
+            k = 0
+            for b, n in enumerate(npg):
+                tab[b, :n] = np.arange(k, k + n)
+                k += n
+            table = torch.from_numpy(tab).to(dev)
+            seq = torch.from_numpy(np.concatenate([np.full(L, b, np.int32) for b, L in enumerate(lens)])).to(dev)
+            pos = torch.from_numpy(np.concatenate([np.arange(L, dtype=np.int32) for L in lens])).to(dev)
+            T = int(lens.sum())
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(B)
+            pools = []
+            for _ in range(npools):
+                Kt = torch.randn((T, hkv, D), generator=gen, device=dev)
+                Kt[:, :, :3] *= 10.0
+                Kt = Kt.to(torch.float16)
+                Vt = torch.randn((T, hkv, D), generator=gen, device=dev).to(torch.float16)
+                pool = torch.zeros((num_pages, page_b), dtype=torch.uint8, device=dev)
+                qoq.qoq_kv4_append(Kt, Vt, seq, pos, table, pool)
+                pools.append(pool)
+                del Kt, Vt
+            Q = torch.randn((B, hq, D), generator=gen, device=dev).to(torch.float16)
+            O = torch.empty_like(Q)
+            lens_d = torch.from_numpy(lens).to(dev)
+            wsk = qoq.new_workspace(qoq.qoq_kv4_attention_workspace_bytes(B, hq, hkv, max_pages), dev)
+
+            def attn(r):
+                qoq.qoq_kv4_decode_attention(Q, pools[r % len(pools)], table, lens_d, hkv, D ** -0.5, O=O, workspace=wsk)
+
+            attn(0)
+            torch.cuda.synchronize()
+            t = graph_us(attn, max(args.point_reps, npools))
+            nbytes = T * hkv * 2 * (64 + 4) + 2 * 2 * B * hq * D + 4 * B * (max_pages + 1)
+            rows.append({"config": name, "B": B, "tokens": T, "us": round(t, 2), "bytes": nbytes,
+                         "GBs": round(nbytes / (t * 1e-6) / 1e9, 1), "hbm_frac": round(nbytes / (t * 1e-6) / bw, 3),
+                         "status": qoq.qoq_workspace_status(wsk)[0]})
+            del pools
+        return {"workload": BLOCKS["kv4_attention"][1], "bound": "hbm",
+                "bytes_weighted_hbm_frac": sum(r["bytes"] for r in rows) / (sum(r["us"] for r in rows) * 1e-6) / bw,
+                "points": rows}
+
     for bname in blocks:
         if bname == "fused_quant":
             block_out[bname] = fused_quant_block()
+            continue
+        if bname == "kv4_attention":
+            block_out[bname] = kv4_block()
             continue
         wid, desc = BLOCKS[bname]
         bpts = [make_point(*p) for p in block_points(bname)]

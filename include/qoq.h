@@ -385,10 +385,90 @@ int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, const int32_t *
 int qoq_noalloc_status(uint32_t *host_status, qoq_stream_t stream);
 
 /*
+ * ---------------------------------------------------------------- KV4 ----
+ * The paged KV cache with per-head dynamic INT4 keys and values, and the
+ * decode attention that reads it ([QS-summary] "QServe系统运行时": paged KV
+ * cache, the per-head FP16 scale and zero point stored right after the
+ * quantized KV features inside each page and updated online; "QServe中的KV4
+ * 注意力"; [QS-review] 3.2 "KV 缓存管理" and 4, step 4).
+ *
+ * Quantization of one key or value vector (one token, one KV head, 128
+ * values; eq. 1 of [QS-summary] "整数量化" with FP16 scale and zero):
+ *   lo = min x, hi = max x; s = fp16((hi - lo) / 15) (1.0 when 0);
+ *   z = fp16(rne(-lo / s)) (an integer); q = clamp(rne(x / s) + z, 0, 15);
+ *   x ~ (q - z) * s.  Divisions IEEE fp32, rne = half to even.
+ *
+ * Page format: a page holds QOQ_KV4_PAGE_TOKENS = 64 token slots of one
+ * sequence for all KV heads, head dim QOQ_KV4_HEAD_DIM = 128, and takes
+ * qoq_kv4_page_bytes(H_kv) = H_kv * 8704 bytes: per KV head h, at offset
+ * 8704 h, one chunk
+ *   [K codes: 64 slots x 64 B][K meta: 64 slots x 4 B]
+ *   [V codes: 64 slots x 64 B][V meta: 64 slots x 4 B]
+ * A meta word holds s (fp16 bits, low half) and z (fp16 bits, high half).
+ * The 64 code bytes of a slot are sixteen little-endian 32-bit words, word i
+ * at byte 4 i; nibble j of a word (bits 4j .. 4j+3) holds one code:
+ *   K: word i = 4 r + jj; with a = j & 3, b = j >> 2 the nibble holds
+ *      dimension 32 jj + 16 (a >> 1) + 8 (a & 1) + 2 r + b;
+ *   V: word i = 2 g + w; the nibble holds dimension g + 8 (8 w + j).
+ * (The order in which the attention kernel's tensor-core fragments read the
+ * codes.)  A pool of pages is one buffer of num_pages pages; a sequence's
+ * page_table row lists its pages in token order: token position p of
+ * sequence b lives in page page_table[b][p / 64], slot p % 64.
+ */
+#define QOQ_KV4_PAGE_TOKENS 64
+#define QOQ_KV4_HEAD_DIM 128
+
+/* Bytes of one KV4 page for num_kv_heads heads (0 if num_kv_heads is not in 1..1024). */
+size_t qoq_kv4_page_bytes(int num_kv_heads);
+
+/*
+ * qoq_kv4_append -- quantize new key / value vectors into their cache slots
+ * (the online update of the pages).  K, V fp16 [num_tokens][num_kv_heads][128]
+ * (16-byte aligned); token t goes to sequence token_seq[t], position
+ * token_pos[t] (int32 [num_tokens]); page_table int32 [num_seqs][max_pages];
+ * pages: num_pages pages (16-byte aligned).  A token whose sequence,
+ * position or page index is out of range is skipped and bit 4 is ORed into
+ * *status (device uint32, may be NULL).  Two tokens of the same slot in one
+ * call race.  Requirements: all counts > 0, num_kv_heads <= 1024.
+ */
+int qoq_kv4_append(const uint16_t *K, const uint16_t *V, int num_tokens, int num_kv_heads, const int32_t *token_seq,
+                   const int32_t *token_pos, const int32_t *page_table, int num_seqs, int max_pages, void *pages,
+                   int num_pages, uint32_t *status, qoq_stream_t stream);
+
+/* Workspace bytes of qoq_kv4_decode_attention on the current device (0 for invalid arguments). */
+size_t qoq_kv4_attention_workspace_bytes(int B, int num_q_heads, int num_kv_heads, int max_pages);
+
+/*
+ * qoq_kv4_decode_attention -- one decode step of attention over the KV4
+ * cache, for B sequences with one query token each:
+ *   Khat_t = (q_t - z_t) s_t (per token and KV head), Vhat_t likewise;
+ *   O[b,h,:] = sum_t softmax_t(softmax_scale * Q[b,h,:] . Khat_t) Vhat_t
+ * over the seq_lens[b] cached tokens of sequence b, query head h reading KV
+ * head h / (num_q_heads / num_kv_heads) (grouped-query attention).
+ * Q, O fp16 [B][num_q_heads][128] (16-byte aligned); pages as written by
+ * qoq_kv4_append (num_pages in the pool); page_table int32 [B][max_pages];
+ * seq_lens int32 [B] in [0, 64 max_pages] (a sequence of length 0 gives a
+ * zero output); workspace >= qoq_kv4_attention_workspace_bytes, 16-byte
+ * aligned, zero-filled once before first use (its first word is the
+ * status word read by qoq_workspace_status: bit 4 = a length or page index
+ * out of range, whose tokens are then skipped or read as stale slots).
+ * Computed in fp32 with fp16 tensor-core operands (exact 4-bit codes and an
+ * fp16 hi + lo pair for each softmax weight times scale); the fp16 output is
+ * within 2e-3 * max_d |O[b,h,:]| + 1 fp16 ulp of the exact result.
+ * Requirements: num_q_heads a multiple of num_kv_heads with a ratio of 1, 2,
+ * 4 or 8; softmax_scale > 0 and finite; B, num_kv_heads <= 65535.
+ */
+int qoq_kv4_decode_attention(const uint16_t *Q, const void *pages, int num_pages, const int32_t *page_table,
+                             const int32_t *seq_lens, int B, int num_q_heads, int num_kv_heads, int max_pages,
+                             float softmax_scale, uint16_t *O, void *workspace, size_t ws_bytes,
+                             qoq_stream_t stream);
+
+/*
  * qoq_workspace_status -- synchronizes `stream`, copies the workspace status
  * word to *host_status, clears it on the device, and returns QOQ_OK,
  * QOQ_ERR_TIMEOUT or QOQ_ERR_DEVICE according to the bits found
- * (1 = a bounded wait expired, 2 = packed-weight header mismatch/illegal).
+ * (1 = a bounded wait expired, 2 = packed-weight header mismatch/illegal,
+ * 4 = a KV4 sequence length or page index out of range).
  */
 int qoq_workspace_status(void *workspace, uint32_t *host_status, qoq_stream_t stream);
 

@@ -97,6 +97,10 @@ def load():
                 "qoq_quant_act_ex": (I, [P, I, I, P, P, P, I, P, ctypes.c_uint32, P]),
                 "qoq_rmsnorm_quant_act": (I, [P, P, ctypes.c_float, I, I, P, P, P, I, P, P, ctypes.c_uint32, P]),
                 "qoq_silu_mul_quant_act": (I, [P, I, I, P, P, P, I, P, P, ctypes.c_uint32, P]),
+                "qoq_kv4_page_bytes": (S, [I]),
+                "qoq_kv4_append": (I, [P, P, I, I, P, P, P, I, I, P, I, P, P]),
+                "qoq_kv4_attention_workspace_bytes": (S, [I, I, I, I]),
+                "qoq_kv4_decode_attention": (I, [P, P, I, P, P, I, I, I, I, ctypes.c_float, P, P, S, P]),
                 "qoq_gemm_workspace_bytes": (S, [I, I, I, I]),
                 "qoq_gemm_workspace_bytes_ex": (S, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
                 "qoq_gemm_path": (I, [I, I, I, I, ctypes.POINTER(qoq_gemm_options)]),
@@ -444,6 +448,60 @@ def qoq_w4a8_gemm_noalloc(Qx, s_x, t_x, packed, s_w, N: int, K: int, group: int 
     _check("qoq_w4a8_gemm_noalloc", load().qoq_w4a8_gemm_noalloc(
         _ptr(Qx), _ptr(s_x), _ptr(t_x), _ptr(packed), _ptr(s_w), M, N, K, group, _ptr(O),
         _stream(stream)))
+    return O
+
+
+# ------------------------------------------------------------------- KV4 --
+QOQ_KV4_PAGE_TOKENS = 64
+QOQ_KV4_HEAD_DIM = 128
+
+
+def qoq_kv4_page_bytes(num_kv_heads: int) -> int:
+    return int(load().qoq_kv4_page_bytes(num_kv_heads))
+
+
+def qoq_kv4_append(K, V, token_seq, token_pos, page_table, pages, status=None, stream=None):
+    """Quantize K, V fp16 [T][H_kv][128] into their slots of the uint8 page
+    pool `pages` ([num_pages][page bytes]); token t -> (token_seq[t],
+    token_pos[t]) through page_table int32 [num_seqs][max_pages]."""
+    torch = _torch()
+    _dev(K, torch.float16, "K")
+    _dev(V, torch.float16, "V")
+    _dev(token_seq, torch.int32, "token_seq")
+    _dev(token_pos, torch.int32, "token_pos")
+    _dev(page_table, torch.int32, "page_table")
+    _dev(pages, torch.uint8, "pages")
+    _dev(status, torch.int32, "status")
+    T, H = K.shape[0], K.shape[1]
+    num_seqs, max_pages = page_table.shape
+    num_pages = pages.shape[0]
+    _check("qoq_kv4_append", load().qoq_kv4_append(
+        _ptr(K), _ptr(V), T, H, _ptr(token_seq), _ptr(token_pos), _ptr(page_table), num_seqs, max_pages,
+        _ptr(pages), num_pages, _ptr(status), _stream(stream)))
+
+
+def qoq_kv4_attention_workspace_bytes(B: int, num_q_heads: int, num_kv_heads: int, max_pages: int) -> int:
+    return int(load().qoq_kv4_attention_workspace_bytes(B, num_q_heads, num_kv_heads, max_pages))
+
+
+def qoq_kv4_decode_attention(Q, pages, page_table, seq_lens, num_kv_heads: int, softmax_scale: float, O=None,
+                             workspace=None, stream=None):
+    """Decode attention over the KV4 page pool: Q fp16 [B][H_q][128] -> O."""
+    torch = _torch()
+    _dev(Q, torch.float16, "Q")
+    _dev(pages, torch.uint8, "pages")
+    _dev(page_table, torch.int32, "page_table")
+    _dev(seq_lens, torch.int32, "seq_lens")
+    B, Hq = Q.shape[0], Q.shape[1]
+    max_pages = page_table.shape[1]
+    if O is None:
+        O = torch.empty_like(Q)
+    _dev(O, torch.float16, "O")
+    if workspace is None:
+        workspace = new_workspace(qoq_kv4_attention_workspace_bytes(B, Hq, num_kv_heads, max_pages), Q.device, stream)
+    _check("qoq_kv4_decode_attention", load().qoq_kv4_decode_attention(
+        _ptr(Q), _ptr(pages), pages.shape[0], _ptr(page_table), _ptr(seq_lens), B, Hq, num_kv_heads, max_pages,
+        float(softmax_scale), _ptr(O), _ptr(workspace), workspace.numel(), _stream(stream)))
     return O
 
 

@@ -293,6 +293,68 @@ int qoq_w4a8_gemm_ex(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x,
                        workspace, ws_bytes, opt, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t qoq_kv4_page_bytes(int num_kv_heads) {
+    if (num_kv_heads <= 0 || num_kv_heads > 1024) return 0;
+    return static_cast<size_t>(num_kv_heads) * qoq::kKv4HeadChunkBytes;
+}
+
+int qoq_kv4_append(const uint16_t *K, const uint16_t *V, int num_tokens, int num_kv_heads, const int32_t *token_seq,
+                   const int32_t *token_pos, const int32_t *page_table, int num_seqs, int max_pages, void *pages,
+                   int num_pages, uint32_t *status, qoq_stream_t stream) {
+    if (num_tokens <= 0 || num_kv_heads <= 0 || num_kv_heads > 1024 || num_seqs <= 0 || max_pages <= 0 ||
+        num_pages <= 0)
+        return QOQ_ERR_INVALID_ARG;
+    if (!K || !V || !token_seq || !token_pos || !page_table || !pages) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(K, 16) || !aligned(V, 16) || !aligned(pages, 16) || !aligned(token_seq, 4) ||
+        !aligned(token_pos, 4) || !aligned(page_table, 4) || (status && !aligned(status, 4)))
+        return QOQ_ERR_MISALIGNED;
+    int st = check_current_device();
+    if (st != QOQ_OK) return st;
+    return cuda_status(qoq::launch_kv4_append(K, V, num_tokens, num_kv_heads, token_seq, token_pos, page_table,
+                                              num_seqs, max_pages, num_pages, pages, status,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+int check_kv4_attention_shape(int B, int num_q_heads, int num_kv_heads, int max_pages) {
+    if (B <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_pages <= 0) return QOQ_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return QOQ_ERR_UNSUPPORTED;
+    const int G = num_q_heads / num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return QOQ_ERR_UNSUPPORTED;
+    if (num_kv_heads > 65535 || B > 65535) return QOQ_ERR_UNSUPPORTED;
+    return QOQ_OK;
+}
+}  // namespace
+
+size_t qoq_kv4_attention_workspace_bytes(int B, int num_q_heads, int num_kv_heads, int max_pages) {
+    if (check_kv4_attention_shape(B, num_q_heads, num_kv_heads, max_pages) != QOQ_OK) return 0;
+    const int sms = num_sms_current_device();
+    if (sms <= 0) return 0;
+    return qoq::plan_kv4_attention(B, num_q_heads, num_kv_heads, max_pages, sms).ws_bytes;
+}
+
+int qoq_kv4_decode_attention(const uint16_t *Q, const void *pages, int num_pages, const int32_t *page_table,
+                             const int32_t *seq_lens, int B, int num_q_heads, int num_kv_heads, int max_pages,
+                             float softmax_scale, uint16_t *O, void *workspace, size_t ws_bytes,
+                             qoq_stream_t stream) {
+    int st = check_kv4_attention_shape(B, num_q_heads, num_kv_heads, max_pages);
+    if (st != QOQ_OK) return st;
+    if (num_pages <= 0 || !(softmax_scale > 0.0f) || softmax_scale > 3.0e38f) return QOQ_ERR_INVALID_ARG;
+    if (!Q || !pages || !page_table || !seq_lens || !O || !workspace) return QOQ_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(O, 16) || !aligned(pages, 16) || !aligned(page_table, 4) ||
+        !aligned(seq_lens, 4) || !aligned(workspace, 16))
+        return QOQ_ERR_MISALIGNED;
+    st = check_current_device();
+    if (st != QOQ_OK) return st;
+    const int sms = num_sms_current_device();
+    if (sms <= 0) return QOQ_ERR_CUDA;
+    const qoq::Kv4Plan plan = qoq::plan_kv4_attention(B, num_q_heads, num_kv_heads, max_pages, sms);
+    if (ws_bytes < plan.ws_bytes) return QOQ_ERR_WORKSPACE;
+    return cuda_status(qoq::launch_kv4_attention(Q, pages, page_table, seq_lens, B, num_q_heads, num_kv_heads,
+                                                 max_pages, num_pages, softmax_scale, O, workspace, plan,
+                                                 kDefaultTimeoutNs, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int qoq_workspace_status(void *workspace, uint32_t *host_status, qoq_stream_t stream) {
     if (!workspace || !host_status) return QOQ_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return QOQ_ERR_MISALIGNED;
@@ -305,7 +367,7 @@ int qoq_workspace_status(void *workspace, uint32_t *host_status, qoq_stream_t st
     if (e != cudaSuccess) return QOQ_ERR_CUDA;
     *host_status = v;
     if (v & 1u) return QOQ_ERR_TIMEOUT;
-    if (v & 2u) return QOQ_ERR_DEVICE;
+    if (v & 6u) return QOQ_ERR_DEVICE;
     return QOQ_OK;
 }
 

@@ -128,6 +128,26 @@ cudaError_t launch_pack(const uint8_t *q4, const uint8_t *s_g, const uint8_t *z,
 cudaError_t launch_unpack(const void *packed, int N, int K, int group, uint8_t *q4, uint8_t *s_g,
                           uint8_t *z, cudaStream_t stream);
 
+// KV4 paged cache: 64 tokens per page, head dim 128; per KV head one chunk
+// of [K codes 64 x 64 B][K (s, z) 64 x 4 B][V codes 64 x 64 B][V (s, z) 64 x 4 B].
+constexpr int kKv4PageTokens = 64;
+constexpr uint32_t kKv4HeadChunkBytes = 2 * (kKv4PageTokens * 64 + kKv4PageTokens * 4);  // 8704
+
+struct Kv4Plan {
+    int splits;            // CTAs per (sequence, KV head), each over pages_per_split pages
+    int pages_per_split;
+    size_t partial_offset; // workspace offset of the split partials
+    size_t ws_bytes;
+};
+Kv4Plan plan_kv4_attention(int B, int hq, int hkv, int max_pages, int num_sms);
+cudaError_t launch_kv4_append(const uint16_t *K, const uint16_t *V, int n_tok, int hkv, const int32_t *tok_seq,
+                              const int32_t *tok_pos, const int32_t *page_table, int num_seqs, int max_pages,
+                              int num_pages, void *pages, uint32_t *status, cudaStream_t stream);
+cudaError_t launch_kv4_attention(const uint16_t *Q, const void *pages, const int32_t *page_table,
+                                 const int32_t *seq_lens, int B, int hq, int hkv, int max_pages, int num_pages,
+                                 float scale, uint16_t *O, void *ws, const Kv4Plan &plan, uint64_t timeout_ns,
+                                 cudaStream_t stream);
+
 struct GemmArgs {
     const int8_t *Qx;
     const uint16_t *s_x;
