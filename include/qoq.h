@@ -408,7 +408,7 @@ int qoq_noalloc_status(uint32_t *host_status, qoq_stream_t stream);
  * The 64 code bytes of a slot are sixteen little-endian 32-bit words, word i
  * at byte 4 i; nibble j of a word (bits 4j .. 4j+3) holds one code:
  *   K: word i = 4 r + jj; with a = j & 3, b = j >> 2 the nibble holds
- *      dimension 32 jj + 16 (a >> 1) + 8 (a & 1) + 2 r + b;
+ *      dimension 32 jj + 16 (a & 1) + 8 (a >> 1) + 2 r + b;
  *   V: word i = 2 g + w; the nibble holds dimension g + 8 (8 w + j).
  * (The order in which the attention kernel's tensor-core fragments read the
  * codes.)  A pool of pages is one buffer of num_pages pages; a sequence's

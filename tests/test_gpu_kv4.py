@@ -36,7 +36,7 @@ def _nibble_dims():
         for j in range(8):
             r, jj = divmod(i, 4)
             a, b = j & 3, j >> 2
-            kd[i, j] = 32 * jj + 16 * (a >> 1) + 8 * (a & 1) + 2 * r + b
+            kd[i, j] = 32 * jj + 16 * (a & 1) + 8 * (a >> 1) + 2 * r + b
             g, w = divmod(i, 2)
             vd[i, j] = g + 8 * (8 * w + j)
     return kd, vd

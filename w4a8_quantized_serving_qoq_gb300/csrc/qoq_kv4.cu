@@ -22,17 +22,20 @@
 //    shared-memory ring with one bulk TMA copy;
 //  * four consumer warps take one 16-token tile of every page each;
 //  * the raw 4-bit codes are the tensor-core operands, as exact fp16
-//    integers (one bit-or and one fp16x2 subtract per two codes); the scales
-//    and zeros are applied per token around the products:
+//    subnormals (one mask per two codes); the scales and zeros are applied
+//    per token around the products:
 //      q . Khat_t = s_t * (q . c_t - z_t * sum(q)),
 //      sum_t p_t Vhat_t = sum_t (p_t s_t) c_t - sum_t p_t s_t z_t,
 //    so no multiply per cached element;
-//  * QK^T and PV are warp-level mma.sync m16n8k16 (fp16 in, fp32 out): the
-//    G query heads that share a KV head (grouped-query attention) are the
-//    N = 8 columns of QK^T; for PV the weights p_t s_t enter as an fp16
-//    pair hi + lo (hi = fp16(x), lo = fp16(x - hi)) in spare columns, so the
-//    fp16 operand loses no accuracy against fp32;
-//  * online softmax in fp32 with exp2f per warp; the warps' states are
+//  * QK^T and PV are warp-level mma.sync m16n8k16 (fp16 in, fp32 out).  The
+//    scores are computed transposed, the G query heads that share a KV head
+//    (grouped-query attention) as rows, twice, so that the score fragment of
+//    a lane is already its B fragment for PV: the weights p_t s_t enter PV
+//    as an fp16 pair hi + lo (hi = fp16(x), lo = fp16(x - hi)), hi through
+//    the first copy of the rows and lo through the second, so the fp16
+//    operand loses no accuracy against fp32;
+//  * online softmax in fp32 per warp, rescaling the accumulators only when
+//    the running maximum grows by more than 2^8; the warps' states are
 //    merged in shared memory; with several splits per sequence the partial
 //    states go to the workspace and a second kernel merges them.
 #include <cuda.h>
@@ -66,10 +69,12 @@ __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? l
 
 // ---------------------------------------------------------------- append --
 // Dimension held by nibble s of word jj of the 16-byte K chunk r of a token:
-// a = s & 3, b = s >> 2, dim = 32 jj + 16 (a >> 1) + 8 (a & 1) + 2 r + b.
+// a = s & 3, b = s >> 2, dim = 32 jj + 16 (a & 1) + 8 (a >> 1) + 2 r + b.
+// (Nibbles 0/4 and 2/6 fall in the k-chunk 32 jj .. +15, nibbles 1/5 and 3/7
+// in 32 jj + 16 .. +31, so one mask per k-chunk gives uniform factors.)
 __device__ __forceinline__ int k_nibble_dim(int r, int jj, int s) {
     const int a = s & 3, b = s >> 2;
-    return 32 * jj + 16 * (a >> 1) + 8 * (a & 1) + 2 * r + b;
+    return 32 * jj + 16 * (a & 1) + 8 * (a >> 1) + 2 * r + b;
 }
 // Dimension held by nibble s of word w of the 8-byte V group g of a token:
 // dim = g + 8 (8 w + s).
@@ -165,25 +170,35 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two 4-bit codes (nibbles s and s + 4 of w, shifted down by 4s) as an
-// fp16x2 of their exact integer values: 0x6400 | c is the fp16 1024 + c.
-__device__ __forceinline__ uint32_t codes_f16x2(uint32_t w_shifted) {
-    uint32_t h = (w_shifted & 0x000F000Fu) | 0x64006400u;
-    const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&h), __halves2half2(__ushort_as_half(0x6400u),
-                                                                                    __ushort_as_half(0x6400u)));
-    return *reinterpret_cast<const uint32_t *>(&r);
+// 2^x for x <= 0 (the hardware approximation; relative error about 2^-22,
+// results below 2^-126 flush to zero, which a softmax weight can afford).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    return static_cast<uint32_t>(f2h_rn(lo)) | (static_cast<uint32_t>(f2h_rn(hi)) << 16);
+// An fp16 pair (hi, lo) with hi + lo = x to about 2^-22 relative.
+__device__ __forceinline__ void split_f16(float x, uint16_t &hi, uint16_t &lo) {
+    const __half h = __float2half_rn(x);
+    hi = __half_as_ushort(h);
+    lo = f2h_rn(__fsub_rn(x, __half2float(h)));
 }
 
-template <int NSV>  // PV n-tiles: ceil(2G / 8)
+// Four-bit codes enter the tensor core as fp16 subnormals: a nibble c in
+// bits 0..3 of a half is exactly c * 2^-24, in bits 4..7 exactly 16 c *
+// 2^-24 (at most 240 * 2^-24, still subnormal).  So a mask of a 32-bit word
+// yields two codes (one per half) with no conversion arithmetic; the factor
+// 2^-24 (or 2^-20) is taken out of the fp32 result.
+constexpr uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u;
+constexpr float kF1 = 16777216.0f;   // 2^24
+constexpr float kF16 = 1048576.0f;   // 2^20
+
+template <int NSV>  // PV n-tiles: 1 for G <= 4, 2 for G = 8
 __global__ void __launch_bounds__(kThreads) kv4_attention_kernel(const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-    float *pstage = reinterpret_cast<float *>(ring + kStages * kChunkBytes);    // [4 warps][16 tokens][8 heads]
-    uint64_t *full = reinterpret_cast<uint64_t *>(pstage + kConsumerWarps * 128);
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + kStages * kChunkBytes);
     uint64_t *empty = full + kStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
 
@@ -232,280 +247,244 @@ __global__ void __launch_bounds__(kThreads) kv4_attention_kernel(const AttnParam
             for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
                 mbar_wait(&full[i % kStages], (i / kStages) & 1, nullptr, p.status, p.timeout_ns);
         }
-    } else {
-        // ------------------------------------------------ consumer warps --
-        const int g4 = lane >> 2, r = lane & 3;
-        // Q^T fragments (k = dims, n = the G query heads of this KV head)
-        // and sum(q) per head, loaded once.
-        uint32_t qb[8][2];
-        float qsum_part = 0.f;
-        {
-            const bool valid = g4 < G;
-            const uint16_t *qrow = p.Q + (static_cast<size_t>(b) * p.hq + h * G + (valid ? g4 : 0)) * kHD;
+        return;
+    }
+
+    // ---------------------------------------------------- consumer warps --
+    // Fragment coordinates of m16n8k16: quad row g4 = lane / 4, column pair r.
+    const int g4 = lane >> 2, r = lane & 3;
+    // S^T = Q Khat^T with the query heads as rows: row rho < 2G holds head
+    // rho mod G (the second copy feeds the lo half of the PV weights), the
+    // other rows are zero.  This lane's score rows: g4 (and g4 + 8).
+    const bool row_ok = g4 < 2 * G;
+    const int my_head = row_ok ? g4 % G : 0;
+    uint32_t qa[8][4];
+    float qsum = 0.f;
+    {
+        const uint16_t *qr0 = p.Q + (static_cast<size_t>(b) * p.hq + h * G + my_head) * kHD;
+        const bool ok8 = g4 + 8 < 2 * G;
+        const uint16_t *qr8 = p.Q + (static_cast<size_t>(b) * p.hq + h * G + (ok8 ? (g4 + 8) % G : 0)) * kHD;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t lo = valid ? *reinterpret_cast<const uint32_t *>(qrow + 16 * j + 2 * r) : 0u;
-                const uint32_t hi = valid ? *reinterpret_cast<const uint32_t *>(qrow + 16 * j + 2 * r + 8) : 0u;
-                qb[j][0] = lo;
-                qb[j][1] = hi;
-                qsum_part += h2f(static_cast<uint16_t>(lo & 0xffffu)) + h2f(static_cast<uint16_t>(lo >> 16)) +
-                             h2f(static_cast<uint16_t>(hi & 0xffffu)) + h2f(static_cast<uint16_t>(hi >> 16));
-            }
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t x0 = row_ok ? *reinterpret_cast<const uint32_t *>(qr0 + 16 * j + 2 * r) : 0u;
+            const uint32_t x1 = row_ok ? *reinterpret_cast<const uint32_t *>(qr0 + 16 * j + 2 * r + 8) : 0u;
+            qa[j][0] = x0;
+            qa[j][1] = ok8 ? *reinterpret_cast<const uint32_t *>(qr8 + 16 * j + 2 * r) : 0u;
+            qa[j][2] = x1;
+            qa[j][3] = ok8 ? *reinterpret_cast<const uint32_t *>(qr8 + 16 * j + 2 * r + 8) : 0u;
+            qsum += h2f(static_cast<uint16_t>(x0 & 0xffffu)) + h2f(static_cast<uint16_t>(x0 >> 16)) +
+                    h2f(static_cast<uint16_t>(x1 & 0xffffu)) + h2f(static_cast<uint16_t>(x1 >> 16));
         }
-        qsum_part += __shfl_xor_sync(0xffffffffu, qsum_part, 1);
-        qsum_part += __shfl_xor_sync(0xffffffffu, qsum_part, 2);  // sum(q) of head g4, in every lane of its quad
-        // this lane's QK^T columns are heads 2r and 2r + 1
-        const float qs0 = __shfl_sync(0xffffffffu, qsum_part, 8 * r);
-        const float qs1 = __shfl_sync(0xffffffffu, qsum_part, 8 * r + 4);
-        const bool hv0 = 2 * r < G, hv1 = 2 * r + 1 < G;
+    }
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);  // sum(q) of this lane's head
 
-        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, c_run[2] = {0.f, 0.f};
-        float acc[NSV][8][4];
+    // Softmax state of this lane's head, over its own tokens; the maximum
+    // m_used is uniform over the quad.  The exponentials use m_used, which is
+    // raised only when a tile's maximum exceeds it by more than 2^8 (weights
+    // up to 256 are harmless in fp32 / fp16), so the PV accumulators are
+    // rescaled rarely.
+    constexpr float kSlack = 8.0f;
+    float m_used = -INFINITY, l_part = 0.f, c_part = 0.f;
+    float acc[NSV][8][4];
 #pragma unroll
-        for (int n = 0; n < NSV; ++n)
+    for (int n = 0; n < NSV; ++n)
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt)
+        for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[n][mt][i] = 0.f;
-        // PV columns of this lane: n-tile n, column 8n + 2r + e -> head of
-        // that column and whether the hi or the lo part enters it
-        float *pst = pstage + warp * 128;
+            for (int i = 0; i < 4; ++i) acc[n][mt][i] = 0.f;
 
-        for (int i = 0; i < n_my; ++i) {
-            const int s = i % kStages, use = i / kStages;
-            if (!mbar_wait_warp(&full[s], use & 1, abort_flag, p.status, p.timeout_ns)) break;
-            const uint8_t *ck = ring + s * kChunkBytes;
-            const int tile0 = warp * 16;                       // this warp's tile of the page
-            const int tok0 = (pg0 + i) * kPageTok + tile0;     // position of its first token
-            // ---- S = Q K^T for 16 tokens x 8 columns
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint4 k0 = *reinterpret_cast<const uint4 *>(ck + (tile0 + g4) * 64 + 16 * r);
-            const uint4 k1 = *reinterpret_cast<const uint4 *>(ck + (tile0 + g4 + 8) * 64 + 16 * r);
-            const uint32_t kw0[4] = {k0.x, k0.y, k0.z, k0.w}, kw1[4] = {k1.x, k1.y, k1.z, k1.w};
+    const int tile0 = warp * 16;  // this warp's 16 tokens of every page
+    for (int i = 0; i < n_my; ++i) {
+        const int s = i % kStages, use = i / kStages;
+        if (!mbar_wait_warp(&full[s], use & 1, abort_flag, p.status, p.timeout_ns)) break;
+        const uint8_t *ck = ring + s * kChunkBytes;
+        const int tok0 = (pg0 + i) * kPageTok + tile0;
+        // ---- S^T: rows = heads, columns = tokens tile0 + 8 nt + {2r, 2r+1}
+        // (n-tile nt); even k-chunks hold codes at factor 2^-24, odd ones at 2^-20
+        float se[2][4], so[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) se[nt][e] = so[nt][e] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint4 kv = *reinterpret_cast<const uint4 *>(ck + (tile0 + 8 * nt + g4) * 64 + 16 * r);
+            const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int a = 2 * half;
-                    const uint32_t af[4] = {codes_f16x2(kw0[jj] >> (4 * a)), codes_f16x2(kw1[jj] >> (4 * a)),
-                                            codes_f16x2(kw0[jj] >> (4 * (a + 1))), codes_f16x2(kw1[jj] >> (4 * (a + 1)))};
-                    mma16816(sc, af, qb[2 * jj + half][0], qb[2 * jj + half][1]);
-                }
+                const uint32_t w8 = kw[jj] >> 8;
+                mma16816(se[nt], qa[2 * jj], kw[jj] & kLo, w8 & kLo);
+                mma16816(so[nt], qa[2 * jj + 1], kw[jj] & kHi, w8 & kHi);
             }
-            const uint32_t km0 = *reinterpret_cast<const uint32_t *>(ck + kCodesBytes + 4 * (tile0 + g4));
-            const uint32_t km1 = *reinterpret_cast<const uint32_t *>(ck + kCodesBytes + 4 * (tile0 + g4 + 8));
-            const float ks0 = h2f(static_cast<uint16_t>(km0 & 0xffffu)), kz0 = h2f(static_cast<uint16_t>(km0 >> 16));
-            const float ks1 = h2f(static_cast<uint16_t>(km1 & 0xffffu)), kz1 = h2f(static_cast<uint16_t>(km1 >> 16));
-            const bool in0 = tok0 + g4 < L, in1 = tok0 + g4 + 8 < L;
-            // scores in log2 units: scale * log2(e) * s_t * (q.c - z_t sum q)
-            float x[4];
-            x[0] = in0 && hv0 ? __fmul_rn(__fmul_rn(__fsub_rn(sc[0], __fmul_rn(kz0, qs0)), ks0), p.scale_log2) : -INFINITY;
-            x[1] = in0 && hv1 ? __fmul_rn(__fmul_rn(__fsub_rn(sc[1], __fmul_rn(kz0, qs1)), ks0), p.scale_log2) : -INFINITY;
-            x[2] = in1 && hv0 ? __fmul_rn(__fmul_rn(__fsub_rn(sc[2], __fmul_rn(kz1, qs0)), ks1), p.scale_log2) : -INFINITY;
-            x[3] = in1 && hv1 ? __fmul_rn(__fmul_rn(__fsub_rn(sc[3], __fmul_rn(kz1, qs1)), ks1), p.scale_log2) : -INFINITY;
-            // ---- online softmax over the tile (heads 2r, 2r + 1)
-            float tmax[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+        }
+        // K scale and zero of the lane's four tokens 8 nt + 2r + e
+        const uint2 km0 = *reinterpret_cast<const uint2 *>(ck + kCodesBytes + 4 * (tile0 + 2 * r));
+        const uint2 km1 = *reinterpret_cast<const uint2 *>(ck + kCodesBytes + 4 * (tile0 + 8 + 2 * r));
+        const uint32_t kmw[4] = {km0.x, km0.y, km1.x, km1.y};
+        float x[4];
+        float tmax = -INFINITY;
 #pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                tmax[0] = fmaxf(tmax[0], __shfl_xor_sync(0xffffffffu, tmax[0], o));
-                tmax[1] = fmaxf(tmax[1], __shfl_xor_sync(0xffffffffu, tmax[1], o));
-            }
-            float alpha[2], mnew[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                mnew[e] = fmaxf(m_run[e], tmax[e]);
-                alpha[e] = mnew[e] == -INFINITY ? 1.f : exp2f(m_run[e] - mnew[e]);
-                m_run[e] = mnew[e];
-            }
-            float pr[4];
-            pr[0] = x[0] == -INFINITY ? 0.f : exp2f(x[0] - mnew[0]);
-            pr[1] = x[1] == -INFINITY ? 0.f : exp2f(x[1] - mnew[1]);
-            pr[2] = x[2] == -INFINITY ? 0.f : exp2f(x[2] - mnew[0]);
-            pr[3] = x[3] == -INFINITY ? 0.f : exp2f(x[3] - mnew[1]);
-            // V weights p_t * s_t and their zero-point correction p_t s_t z_t
-            const uint32_t vm0 = *reinterpret_cast<const uint32_t *>(ck + kVOff + kCodesBytes + 4 * (tile0 + g4));
-            const uint32_t vm1 = *reinterpret_cast<const uint32_t *>(ck + kVOff + kCodesBytes + 4 * (tile0 + g4 + 8));
-            const float vs0 = h2f(static_cast<uint16_t>(vm0 & 0xffffu)), vz0 = h2f(static_cast<uint16_t>(vm0 >> 16));
-            const float vs1 = h2f(static_cast<uint16_t>(vm1 & 0xffffu)), vz1 = h2f(static_cast<uint16_t>(vm1 >> 16));
-            // (masked tokens may sit in never-written slots: select, never multiply, their scales)
-            const float w[4] = {pr[0] != 0.f ? __fmul_rn(pr[0], vs0) : 0.f, pr[1] != 0.f ? __fmul_rn(pr[1], vs0) : 0.f,
-                                pr[2] != 0.f ? __fmul_rn(pr[2], vs1) : 0.f, pr[3] != 0.f ? __fmul_rn(pr[3], vs1) : 0.f};
-            const float cz[4] = {w[0] != 0.f ? __fmul_rn(w[0], vz0) : 0.f, w[1] != 0.f ? __fmul_rn(w[1], vz0) : 0.f,
-                                 w[2] != 0.f ? __fmul_rn(w[2], vz1) : 0.f, w[3] != 0.f ? __fmul_rn(w[3], vz1) : 0.f};
-            float lsum[2] = {pr[0] + pr[2], pr[1] + pr[3]};
-            float csum[2] = {cz[0] + cz[2], cz[1] + cz[3]};
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], o);
-                    csum[e] += __shfl_xor_sync(0xffffffffu, csum[e], o);
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                l_run[e] = __fmaf_rn(l_run[e], alpha[e], lsum[e]);
-                c_run[e] = __fmaf_rn(c_run[e], alpha[e], csum[e]);
-            }
-            // rescale the PV accumulators by their head's alpha: column
-            // 8n + 2r + e holds head hd = col (< G, hi part) or col - G (lo
-            // part); its softmax state is component hd & 1 of the lanes of quad
-            // column hd >> 1
-            float ascale[NSV][2];
-#pragma unroll
-            for (int n = 0; n < NSV; ++n) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int col = 8 * n + 2 * r + e;
-                    const int hd = col < G ? col : (col < 2 * G ? col - G : 0);
-                    const float a0 = __shfl_sync(0xffffffffu, alpha[0], (lane & ~3) | (hd >> 1));
-                    const float a1 = __shfl_sync(0xffffffffu, alpha[1], (lane & ~3) | (hd >> 1));
-                    ascale[n][e] = (hd & 1) ? a1 : a0;
-                }
-            }
+        for (int t = 0; t < 4; ++t) {
+            const int nt = t >> 1, e = t & 1;
+            const float dot = __fmaf_rn(se[nt][e], kF1, __fmul_rn(so[nt][e], kF16));  // q . c_t
+            const float ks = h2f(static_cast<uint16_t>(kmw[t] & 0xffffu)), kz = h2f(static_cast<uint16_t>(kmw[t] >> 16));
+            const bool in = row_ok && tok0 + 8 * nt + 2 * r + e < L;
+            x[t] = in ? __fmul_rn(__fmul_rn(__fsub_rn(dot, __fmul_rn(kz, qsum)), ks), p.scale_log2) : -INFINITY;
+            tmax = fmaxf(tmax, x[t]);
+        }
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+        const bool raise = tmax > m_used + kSlack || (m_used == -INFINITY && tmax != -INFINITY);
+        if (__any_sync(0xffffffffu, raise)) {
+            const float m_new = raise ? tmax : m_used;
+            const float alpha = (m_used == -INFINITY || !raise) ? (m_used == -INFINITY ? 0.f : 1.f) : ex2(m_used - m_new);
+            m_used = m_new;
+            l_part *= alpha;
+            c_part *= alpha;
+            // PV column c (of either n-tile) belongs to the head of score row c
+            const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * r);
+            const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * r + 4);
 #pragma unroll
             for (int n = 0; n < NSV; ++n)
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
-                    acc[n][mt][0] *= ascale[n][0];
-                    acc[n][mt][1] *= ascale[n][1];
-                    acc[n][mt][2] *= ascale[n][0];
-                    acc[n][mt][3] *= ascale[n][1];
+                    acc[n][mt][0] *= a0;
+                    acc[n][mt][1] *= a1;
+                    acc[n][mt][2] *= a0;
+                    acc[n][mt][3] *= a1;
                 }
-            // transpose the weights through shared memory into the B layout
-            // (k = tokens, n = columns): [token][head]
-            pst[g4 * 8 + 2 * r] = w[0];
-            pst[g4 * 8 + 2 * r + 1] = w[1];
-            pst[(g4 + 8) * 8 + 2 * r] = w[2];
-            pst[(g4 + 8) * 8 + 2 * r + 1] = w[3];
-            __syncwarp();
-            uint32_t pb[NSV][2];
+        }
+        // weights w_t = p_t * s_t of the V scale and the zero correction
+        const uint2 vm0 = *reinterpret_cast<const uint2 *>(ck + kVOff + kCodesBytes + 4 * (tile0 + 2 * r));
+        const uint2 vm1 = *reinterpret_cast<const uint2 *>(ck + kVOff + kCodesBytes + 4 * (tile0 + 8 + 2 * r));
+        const uint32_t vmw[4] = {vm0.x, vm0.y, vm1.x, vm1.y};
+        uint16_t whi[4], wlo[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            // masked tokens may sit in never-written slots: select, never multiply, their scales
+            const float pt = x[t] == -INFINITY ? 0.f : ex2(__fsub_rn(x[t], m_used));
+            const float vs = h2f(static_cast<uint16_t>(vmw[t] & 0xffffu)), vz = h2f(static_cast<uint16_t>(vmw[t] >> 16));
+            const float w = pt != 0.f ? __fmul_rn(pt, vs) : 0.f;
+            l_part += pt;
+            c_part = w != 0.f ? __fmaf_rn(w, vz, c_part) : c_part;
+            split_f16(w, whi[t], wlo[t]);
+        }
+        // PV B fragment, column g4 (n-tile n): hi part of head g4 for g4 < G,
+        // lo part for G <= g4 < 2G (G <= 4); for G = 8 n-tile 0 is hi, 1 is lo
+        uint32_t pb[NSV][2];
+#pragma unroll
+        for (int n = 0; n < NSV; ++n) {
+            const bool hi_part = NSV == 2 ? n == 0 : g4 < G;
+            const uint16_t *src = hi_part ? whi : wlo;
+            pb[n][0] = row_ok ? (static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 16)) : 0u;
+            pb[n][1] = row_ok ? (static_cast<uint32_t>(src[2]) | (static_cast<uint32_t>(src[3]) << 16)) : 0u;
+        }
+        // ---- O^T += Vc^T W: rows = dims g4 + 8 nt' of the V group g4, k = tokens
+        const uint8_t *cv = ck + kVOff + 8 * g4;
+        const uint2 va = *reinterpret_cast<const uint2 *>(cv + (tile0 + 2 * r) * 64);
+        const uint2 vb = *reinterpret_cast<const uint2 *>(cv + (tile0 + 2 * r + 1) * 64);
+        const uint2 vc = *reinterpret_cast<const uint2 *>(cv + (tile0 + 2 * r + 8) * 64);
+        const uint2 vd = *reinterpret_cast<const uint2 *>(cv + (tile0 + 2 * r + 9) * 64);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with the page slot
+        // pairs (token 2r | token 2r+1) and (2r+8 | 2r+9) of the nibbles nt = 8 w + s
+        uint32_t ya[4], yc[4];
+        ya[0] = __byte_perm(va.x, vb.x, 0x5410);
+        ya[1] = __byte_perm(va.x, vb.x, 0x7632);
+        ya[2] = __byte_perm(va.y, vb.y, 0x5410);
+        ya[3] = __byte_perm(va.y, vb.y, 0x7632);
+        yc[0] = __byte_perm(vc.x, vd.x, 0x5410);
+        yc[1] = __byte_perm(vc.x, vd.x, 0x7632);
+        yc[2] = __byte_perm(vc.y, vd.y, 0x5410);
+        yc[3] = __byte_perm(vc.y, vd.y, 0x7632);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // y = ya[q] holds nibbles nt = 4q .. 4q+3: even nt at factor 2^-24
+            // (mask kLo), odd nt at 2^-20 (mask kHi) -> m-tiles 2q and 2q+1
+            const uint32_t a8 = ya[q] >> 8, c8 = yc[q] >> 8;
+            const uint32_t af0[4] = {ya[q] & kLo, ya[q] & kHi, yc[q] & kLo, yc[q] & kHi};
+            const uint32_t af1[4] = {a8 & kLo, a8 & kHi, c8 & kLo, c8 & kHi};
 #pragma unroll
             for (int n = 0; n < NSV; ++n) {
-                const int col = 8 * n + g4;
-                const bool hi_part = col < G, lo_part = col >= G && col < 2 * G;
-                const int hd = hi_part ? col : (lo_part ? col - G : 0);
-                float v4[4] = {pst[(2 * r) * 8 + hd], pst[(2 * r + 1) * 8 + hd], pst[(2 * r + 8) * 8 + hd],
-                               pst[(2 * r + 9) * 8 + hd]};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float hv = __half2float(__float2half_rn(v4[e]));
-                    v4[e] = hi_part ? hv : (lo_part ? __fsub_rn(v4[e], hv) : 0.f);
-                }
-                pb[n][0] = pack_f16x2(v4[0], v4[1]);
-                pb[n][1] = pack_f16x2(v4[2], v4[3]);
-            }
-            __syncwarp();
-            // ---- O^T += Vc^T (dims x tokens) * W (tokens x columns)
-            const uint8_t *cv = ck + kVOff;
-            const uint2 va = *reinterpret_cast<const uint2 *>(cv + (tile0 + 2 * r) * 64 + 8 * g4);
-            const uint2 vb = *reinterpret_cast<const uint2 *>(cv + (tile0 + 2 * r + 1) * 64 + 8 * g4);
-            const uint2 vc = *reinterpret_cast<const uint2 *>(cv + (tile0 + 2 * r + 8) * 64 + 8 * g4);
-            const uint2 vd = *reinterpret_cast<const uint2 *>(cv + (tile0 + 2 * r + 9) * 64 + 8 * g4);
-            // fp16x2 of (token 2r, token 2r+1) and (token 2r+8, token 2r+9) for
-            // the 16 dims g4 + 8 nt, nt = 8 w + s
-            uint32_t pa[16], pc[16];
-#pragma unroll
-            for (int ww = 0; ww < 2; ++ww) {
-                const uint32_t xa = ww ? va.y : va.x, xb = ww ? vb.y : vb.x;
-                const uint32_t xc = ww ? vc.y : vc.x, xd = ww ? vd.y : vd.x;
-                const uint32_t lo_ab = __byte_perm(xa, xb, 0x5410), hi_ab = __byte_perm(xa, xb, 0x7632);
-                const uint32_t lo_cd = __byte_perm(xc, xd, 0x5410), hi_cd = __byte_perm(xc, xd, 0x7632);
-#pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4) {
-                    pa[8 * ww + s4] = codes_f16x2(lo_ab >> (4 * s4));
-                    pa[8 * ww + 4 + s4] = codes_f16x2(hi_ab >> (4 * s4));
-                    pc[8 * ww + s4] = codes_f16x2(lo_cd >> (4 * s4));
-                    pc[8 * ww + 4 + s4] = codes_f16x2(hi_cd >> (4 * s4));
-                }
-            }
-            // every warp is done with this page slot (the V codes are in registers)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                const uint32_t af[4] = {pa[2 * mt], pa[2 * mt + 1], pc[2 * mt], pc[2 * mt + 1]};
-#pragma unroll
-                for (int n = 0; n < NSV; ++n) mma16816(acc[n][mt], af, pb[n][0], pb[n][1]);
+                mma16816(acc[n][2 * q], af0, pb[n][0], pb[n][1]);
+                mma16816(acc[n][2 * q + 1], af1, pb[n][0], pb[n][1]);
             }
         }
+    }
 
-        // ---- merge the four warps' states in shared memory (the ring is free
-        // once every consumer passed its last page; the producer only waits
-        // for copies it issued, which have all landed by then)
-        named_bar_sync_kv(1, 32 * kConsumerWarps);
-        float *mrg = reinterpret_cast<float *>(ring);  // [warp][G][2 + 128 + 1]: m, l, O..., c
-        const int stride = 2 + kHD + 1;
-        // column values of this lane: n-tile n, col 8n + 2r + e, dims g4 + 16 mt (+ 8)
+    // ---- the lane's partial sums over its tokens, summed over the quad
+    l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
+    l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
+    c_part += __shfl_xor_sync(0xffffffffu, c_part, 1);
+    c_part += __shfl_xor_sync(0xffffffffu, c_part, 2);
+
+    // ---- merge the four warps' states in shared memory (the ring is free
+    // once every consumer passed its last page; the producer waits only for
+    // copies it issued, which have all landed by then)
+    named_bar_sync_kv(1, 32 * kConsumerWarps);
+    float *mrg = reinterpret_cast<float *>(ring);  // [warp][G][2 + 128 + 1]: m, l, O..., c
+    const int stride = 2 + kHD + 1;
+    // accumulator rows: m-tile mt covers nibbles nt = 2 mt (dims g4 + 16 mt,
+    // factor 2^-24) and nt = 2 mt + 1 (dims g4 + 8 + 16 mt, factor 2^-20);
+    // columns 8 n + 2r + e
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
 #pragma unroll
         for (int n = 0; n < NSV; ++n)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int col = 8 * n + 2 * r + e;
-                if (col < 2 * G) {
-                    const int hd = col < G ? col : col - G;
-                    float *dst = mrg + (warp * G + hd) * stride + 2;
-                    if (col < G) {
+                const int col = (NSV == 2 ? 0 : 0) + 2 * r + e;
+                const bool hi_col = NSV == 2 ? n == 0 : col < G;
+                const bool lo_col = NSV == 2 ? n == 1 : (col >= G && col < 2 * G);
+                if (pass == 0 ? !hi_col : !lo_col) continue;
+                const int hd = NSV == 2 ? col : (hi_col ? col : col - G);
+                if (hd >= G) continue;
+                float *dst = mrg + (warp * G + hd) * stride + 2;
 #pragma unroll
-                        for (int mt = 0; mt < 8; ++mt) {
-                            dst[g4 + 16 * mt] = acc[n][mt][e];
-                            dst[g4 + 8 + 16 * mt] = acc[n][mt][2 + e];
-                        }
+                for (int mt = 0; mt < 8; ++mt) {
+                    const float v0 = __fmul_rn(acc[n][mt][e], kF1), v1 = __fmul_rn(acc[n][mt][2 + e], kF16);
+                    if (pass == 0) {
+                        dst[g4 + 16 * mt] = v0;
+                        dst[g4 + 8 + 16 * mt] = v1;
+                    } else {
+                        dst[g4 + 16 * mt] += v0;
+                        dst[g4 + 8 + 16 * mt] += v1;
                     }
                 }
             }
         named_bar_sync_kv(1, 32 * kConsumerWarps);
-#pragma unroll
-        for (int n = 0; n < NSV; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int col = 8 * n + 2 * r + e;
-                if (col >= G && col < 2 * G) {
-                    float *dst = mrg + (warp * G + col - G) * stride + 2;
-#pragma unroll
-                    for (int mt = 0; mt < 8; ++mt) {
-                        dst[g4 + 16 * mt] += acc[n][mt][e];
-                        dst[g4 + 8 + 16 * mt] += acc[n][mt][2 + e];
-                    }
-                }
-            }
-        if (g4 == 0) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int hd = 2 * r + e;
-                if (hd < G) {
-                    float *dst = mrg + (warp * G + hd) * stride;
-                    dst[0] = m_run[e];
-                    dst[1] = l_run[e];
-                    dst[2 + kHD] = c_run[e];
-                }
-            }
+    }
+    if (r == 0 && g4 < G) {
+        float *dst = mrg + (warp * G + g4) * stride;
+        dst[0] = m_used;
+        dst[1] = l_part;
+        dst[2 + kHD] = c_part;
+    }
+    named_bar_sync_kv(1, 32 * kConsumerWarps);
+    // one consumer thread per (head, dim) pair of the output
+    for (int idx = threadIdx.x; idx < G * kHD; idx += 32 * kConsumerWarps) {
+        const int hd = idx / kHD, d = idx % kHD;
+        float M = -INFINITY;
+        for (int w2 = 0; w2 < kConsumerWarps; ++w2) M = fmaxf(M, mrg[(w2 * G + hd) * stride]);
+        float Ls = 0.f, Os = 0.f;
+        for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+            const float *src = mrg + (w2 * G + hd) * stride;
+            const float f = src[0] == -INFINITY ? 0.f : ex2(src[0] - M);
+            Ls = __fmaf_rn(f, src[1], Ls);
+            Os = __fmaf_rn(f, __fsub_rn(src[2 + d], src[2 + kHD]), Os);
         }
-        named_bar_sync_kv(1, 32 * kConsumerWarps);
-        // one consumer thread per (head, dim) pair of the output
-        for (int idx = threadIdx.x; idx < G * kHD; idx += 32 * kConsumerWarps) {
-            const int hd = idx / kHD, d = idx % kHD;
-            float M = -INFINITY;
-            for (int w2 = 0; w2 < kConsumerWarps; ++w2) M = fmaxf(M, mrg[(w2 * G + hd) * stride]);
-            float Ls = 0.f, Os = 0.f;
-            for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
-                const float *src = mrg + (w2 * G + hd) * stride;
-                const float f = src[0] == -INFINITY ? 0.f : exp2f(src[0] - M);
-                Ls = __fmaf_rn(f, src[1], Ls);
-                Os = __fmaf_rn(f, __fsub_rn(src[2 + d], src[2 + kHD]), Os);
+        const size_t hq_idx = static_cast<size_t>(b) * p.hq + h * G + hd;
+        if (p.splits == 1) {
+            p.O[hq_idx * kHD + d] = f2h_rn(Ls > 0.f ? __fdiv_rn(Os, Ls) : 0.f);
+        } else {
+            float *part = p.partial + ((static_cast<size_t>(b) * p.hkv + h) * p.splits + split) * G * (2 + kHD) +
+                          hd * (2 + kHD);
+            if (d == 0) {
+                part[0] = M;
+                part[1] = Ls;
             }
-            const size_t hq_idx = static_cast<size_t>(b) * p.hq + h * G + hd;
-            if (p.splits == 1) {
-                p.O[hq_idx * kHD + d] = f2h_rn(Ls > 0.f ? __fdiv_rn(Os, Ls) : 0.f);
-            } else {
-                float *part = p.partial + ((static_cast<size_t>(b) * p.hkv + h) * p.splits + split) * G * (2 + kHD) +
-                              hd * (2 + kHD);
-                if (d == 0) {
-                    part[0] = M;
-                    part[1] = Ls;
-                }
-                part[2 + d] = Os;
-            }
+            part[2 + d] = Os;
         }
     }
 }
@@ -529,7 +508,7 @@ __global__ void kv4_combine_kernel(const float *__restrict__ partial, int hq, in
     O[(static_cast<size_t>(b) * hq + qh) * kHD + d] = f2h_rn(Ls > 0.f ? __fdiv_rn(Os, Ls) : 0.f);
 }
 
-constexpr size_t kAttnSmem = 128 + kStages * kChunkBytes + kConsumerWarps * 128 * 4 + 2 * kStages * 8 + 16;
+constexpr size_t kAttnSmem = 128 + kStages * kChunkBytes + 2 * kStages * 8 + 16;
 
 template <int NSV>
 cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
