@@ -323,6 +323,49 @@ def test_fp16_path_with_quantizer_act_operand(M, N, K, group):
     assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
 
 
+GEMV_CASES = [(1, 256, 512), (2, 384, 1024), (3, 128, 384), (5, 256, 1152), (8, 128, 128), (7, 256, 2304),
+              (4, 128, 29568)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMV_CASES)
+@pytest.mark.parametrize("group", [128, 0])
+@pytest.mark.parametrize("csize", [1, 2, 4, 8])
+def test_cuda_core_path_bit_exact(M, N, K, group, csize):
+    """The dp4a path (M <= 8): every K split over a thread-block cluster
+    (1, 2, 4, 8 CTAs, including splits that leave a CTA or a warp group
+    without a block), group and per-channel weights, int32 bit-exact and the
+    fp16 output within tolerance."""
+    wq, Qx, sx, tx = _gemm_case(M, N, K, 6000 + M + K, group)
+    packed, sw = _device_weights(wq, group)
+    ref = _ref_acc(wq, Qx, tx, group)
+    assert qoq.qoq_gemm_path(M, N, K, group, qoq.gemm_options(kernel=3, num_ctas=csize)) == 3
+    acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    opt = qoq.gemm_options(kernel=3, num_ctas=csize, acc_out=acc)
+    ws = qoq.new_workspace(qoq.qoq_gemm_workspace_bytes(M, N, K, group, opt))
+    for _ in range(2):
+        acc.fill_(0)
+        qoq.qoq_w4a8_gemm_ex(_t(Qx), None, _t(tx), packed, None, N, K, group, workspace=ws, options=opt)
+        assert np.array_equal(_np(acc), ref)
+    O = qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), _t(tx), packed, sw, N, K, group, workspace=ws,
+                             options=qoq.gemm_options(kernel=3, num_ctas=csize))
+    O_ref = oracle.epilogue_f64(ref, sx, wq["s_w"])
+    assert oracle.o_within_tolerance(_np(O).astype(np.float64), O_ref).all()
+    assert qoq.qoq_workspace_status(ws)[0] == qoq.QOQ_OK
+
+
+def test_cuda_core_path_refuses_mismatched_weights():
+    M, N, K = 4, 256, 512
+    wq, Qx, sx, tx = _gemm_case(M, N, K, 5)
+    packed, sw = _device_weights(wq, 128)
+    ws = qoq.new_workspace(256)
+    O = torch.zeros((M, N - 128), dtype=torch.float16, device=DEV)
+    qoq.qoq_w4a8_gemm_ex(_t(Qx), _t(sx), None, packed, sw, N - 128, K, 128, O=O, workspace=ws,
+                         options=qoq.gemm_options(kernel=3))
+    st, bits = qoq.qoq_workspace_status(ws)
+    assert st == 7 and bits & 2
+    assert float(O.abs().max()) == 0.0
+
+
 def test_gemm_exact_at_chunk_extremes():
     """Largest-magnitude products over whole 1024-k chunks: the fp32
     accumulation per chunk must still be exact (sums up to 127*128*1024)."""
@@ -343,7 +386,7 @@ def test_gemm_exact_at_chunk_extremes():
     ref = oracle.gemm_i32_group(Qx, q4, s_g, z)
     assert abs(int(ref[0, 0])) == 127 * 120 * K
     for ctas in (1, 7, 0):
-        for kernel in (1, 2):
+        for kernel in (1, 2, 3):
             acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
             qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128,
                                  options=qoq.gemm_options(num_ctas=ctas, acc_out=acc, kernel=kernel))

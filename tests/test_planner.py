@@ -15,7 +15,7 @@ def _plan(M, NK, group=128, **opt):
     return qoq.qoq_gemm_plan(M, N, K, group, SMS, options)
 
 
-@pytest.mark.parametrize("M", [1, 8, 16, 32])
+@pytest.mark.parametrize("M", [16, 32])
 @pytest.mark.parametrize("NK", [QKV, O, GATE_UP, DOWN])
 def test_decode_sizes_take_the_fp8_path_and_leave_8_sms(M, NK):
     p = _plan(M, NK)
@@ -26,8 +26,34 @@ def test_decode_sizes_take_the_fp8_path_and_leave_8_sms(M, NK):
     assert p["k_stages"] == p["tiles"] * (NK[1] // 128)
 
 
-def test_per_channel_weights_always_take_the_fp16_path():
-    for M in (1, 32, 64, 256):
+@pytest.mark.parametrize("M,MT", [(1, 1), (2, 2), (3, 4), (5, 8), (8, 8)])
+@pytest.mark.parametrize("NK,csize", [(QKV, 8), (O, 8), (GATE_UP, 4), (DOWN, 8), ((59136, 8192), 1),
+                                      ((8192, 29568), 8)])
+def test_up_to_8_tokens_take_the_cuda_core_path(M, MT, NK, csize):
+    """M <= 8: the dp4a path, tokens rounded up to 1, 2, 4 or 8; the K split
+    (cluster size) is the largest of 8, 4, 2, 1 that keeps at most six CTAs
+    per SM with a block per K half; only the status word in the workspace."""
+    p = _plan(M, NK)
+    assert (p["path"], p["tokens_per_tile"]) == (3, MT)
+    assert p["num_ctas"] == (NK[0] // 128) * csize
+    assert p["workspace_bytes"] == 256
+    for group in (0, 128):
+        assert _plan(M, NK, group=group)["path"] == 3
+
+
+def test_cuda_core_path_options():
+    assert _plan(1, O, kernel=3, num_ctas=2)["num_ctas"] == 32 * 2     # forced cluster size
+    assert _plan(1, O, kernel=2)["path"] == 2                          # forced tensor-core path
+    assert _plan(8, O, tokens_per_tile=16)["path"] == 2                # a token tile forces the tensor cores
+    lib = qoq.load()
+    info = qoq.qoq_gemm_plan_info()
+    opt = qoq.gemm_options(kernel=3)
+    # more than 8 tokens cannot take the CUDA-core path
+    assert lib.qoq_gemm_plan(9, 4096, 4096, 128, SMS, qoq.ctypes.byref(opt), qoq.ctypes.byref(info)) == 2
+
+
+def test_per_channel_weights_take_the_fp16_path_above_8_tokens():
+    for M in (9, 32, 64, 256):
         assert _plan(M, GATE_UP, group=0)["path"] == 1
 
 
@@ -55,14 +81,14 @@ def test_options_override_the_plan():
     p = _plan(256, GATE_UP, kernel=2)
     assert (p["path"], p["tokens_per_tile"]) == (2, 32)
     assert _plan(256, GATE_UP, num_ctas=7)["num_ctas"] == 7
-    assert _plan(1, O, num_ctas=5000)["num_ctas"] == 32 * 32  # clamped to the k-stages
+    assert _plan(1, O, num_ctas=5000, kernel=2)["num_ctas"] == 32 * 32  # clamped to the k-stages
 
 
 def _aligned(x, a=256):
     return (x + a - 1) // a * a
 
 
-@pytest.mark.parametrize("M,NK", [(1, QKV), (64, QKV), (128, O), (256, GATE_UP), (8, DOWN)])
+@pytest.mark.parametrize("M,NK", [(16, QKV), (64, QKV), (128, O), (256, GATE_UP), (32, DOWN)])
 def test_workspace_layout(M, NK):
     """[256-byte status][CTA counters][CTAs x tile x 128 int32 slots][activation operand]."""
     N, K = NK
@@ -91,7 +117,7 @@ def test_allocation_free_limit_depends_on_the_shape():
     (the planned workspace) is at most 8 MiB: every Llama-3-8B layer up to
     M = 64 (qkv and o also at 128), not Qwen1.5-72B down at M = 64."""
     limit = 8 << 20
-    for M in (1, 8, 32, 64):
+    for M in (1, 8, 16, 32, 64):
         for NK in (QKV, O, GATE_UP, DOWN):
             assert _plan(M, NK)["workspace_bytes"] <= limit
     assert _plan(128, QKV)["workspace_bytes"] <= limit

@@ -273,7 +273,7 @@ def qoq_quant_act_ex(X, Qx=None, s_x=None, t_x=None, act=None, kind: int = 2, wi
         s_x = torch.empty((M,), dtype=torch.float16, device=X.device)
     if t_x is None and with_t:
         t_x = torch.empty((M,), dtype=torch.int32, device=X.device)
-    if act is None and with_act:
+    if act is None and with_act and kind != 3:  # kind 3: the CUDA-core GEMM reads Qx, no operand
         nbytes = qoq_act_operand_bytes(M, K, kind)
         if nbytes == 0:
             raise QoqError("qoq_quant_act_ex", 2)
@@ -295,7 +295,7 @@ def _quant_outputs(M, K, device, Qx, s_x, t_x, act, kind, with_t, with_act, Y, w
         s_x = torch.empty((M,), dtype=torch.float16, device=device)
     if t_x is None and with_t:
         t_x = torch.empty((M,), dtype=torch.int32, device=device)
-    if act is None and with_act:
+    if act is None and with_act and kind != 3:
         nbytes = qoq_act_operand_bytes(M, K, kind)
         if nbytes == 0:
             raise QoqError("qoq_act_operand_bytes", 2)
@@ -349,7 +349,8 @@ def qoq_gemm_workspace_bytes(M: int, N: int, K: int, group: int = 128, options=N
 
 
 def qoq_gemm_path(M: int, N: int, K: int, group: int = 128, options=None) -> int:
-    """1 = fp16-operand path, 2 = fp8-operand path (reads the activation operand)."""
+    """1 = fp16-operand path, 2 = fp8-operand path (each reads the activation
+    operand of its kind), 3 = CUDA-core path for M <= 8 (reads Qx itself)."""
     st = int(load().qoq_gemm_path(M, N, K, group, None if options is None else ctypes.byref(options)))
     if st < 0:
         raise QoqError("qoq_gemm_path", -st)

@@ -50,7 +50,7 @@ int check_options(const qoq_gemm_options *opt) {
     const int bt = opt->tokens_per_tile;
     if (bt != 0 && bt != 16 && bt != 32 && bt != 64 && bt != 128) return QOQ_ERR_UNSUPPORTED;
     if (opt->num_ctas < 0 || opt->num_ctas > 65536) return QOQ_ERR_UNSUPPORTED;
-    if (opt->kernel < 0 || opt->kernel > 2) return QOQ_ERR_UNSUPPORTED;
+    if (opt->kernel < 0 || opt->kernel > 3) return QOQ_ERR_UNSUPPORTED;
     if (opt->flags & ~QOQ_LAUNCH_OVERLAP) return QOQ_ERR_UNSUPPORTED;
     return QOQ_OK;
 }
@@ -62,6 +62,9 @@ bool plan_for(int M, int N, int K, int group, const qoq_gemm_options *opt, qoq::
                           opt ? opt->num_ctas : 0);
     return true;
 }
+
+// A plan the kernels can run (path 0: a forced path that does not take this shape).
+bool plan_valid(const qoq::GemmPlan &plan) { return plan.path >= 1 && plan.path <= 3; }
 
 int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const void *packed,
                 const uint16_t *s_w, int M, int N, int K, int group, uint16_t *O, int32_t *acc_out,
@@ -83,6 +86,7 @@ int gemm_common(const int8_t *Qx, const uint16_t *s_x, const int32_t *t_x, const
     if (st != QOQ_OK) return st;
     qoq::GemmPlan plan;
     if (!plan_for(M, N, K, group, opt, &plan)) return QOQ_ERR_CUDA;
+    if (!plan_valid(plan)) return QOQ_ERR_UNSUPPORTED;
     if (plan.total * (plan.ctas + 1ll) >= (1ll << 32)) return QOQ_ERR_UNSUPPORTED;
     if (ws_bytes < plan.ws_bytes) return QOQ_ERR_WORKSPACE;
     qoq::GemmArgs a;
@@ -175,7 +179,7 @@ int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, in
 }
 
 size_t qoq_act_operand_bytes(int M, int K, int kind) {
-    if (M <= 0 || K <= 0 || K % 128 != 0 || (kind != 1 && kind != 2)) return 0;
+    if (M <= 0 || K <= 0 || K % 128 != 0 || (kind != 1 && kind != 2)) return 0;  // kind 3 reads Qx: none
     return qoq::act_operand_bytes(M, K, kind);
 }
 
@@ -183,7 +187,8 @@ int qoq_quant_act_ex(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
                      int kind, void *act_operand, uint32_t flags, qoq_stream_t stream) {
     if (M <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
     if (flags & ~QOQ_LAUNCH_OVERLAP) return QOQ_ERR_UNSUPPORTED;
-    if (act_operand && kind != 1 && kind != 2) return QOQ_ERR_INVALID_ARG;
+    if (act_operand && kind != 1 && kind != 2 && kind != 3) return QOQ_ERR_INVALID_ARG;
+    if (kind == 3) act_operand = nullptr;  // the CUDA-core path reads Qx itself
     if (K % 8 != 0 || (act_operand && K % 128 != 0)) return QOQ_ERR_UNSUPPORTED;
     if (!X || !Qx || !s_x) return QOQ_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) || (t_x && !aligned(t_x, 4)) ||
@@ -200,7 +205,8 @@ int qoq_rmsnorm_quant_act(const uint16_t *X, const uint16_t *gamma, float eps, i
     if (M <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
     if (!(eps >= 0.0f) || eps > 3.0e38f) return QOQ_ERR_INVALID_ARG;  // rejects NaN and inf too
     if (flags & ~QOQ_LAUNCH_OVERLAP) return QOQ_ERR_UNSUPPORTED;
-    if (act_operand && kind != 1 && kind != 2) return QOQ_ERR_INVALID_ARG;
+    if (act_operand && kind != 1 && kind != 2 && kind != 3) return QOQ_ERR_INVALID_ARG;
+    if (kind == 3) act_operand = nullptr;  // the CUDA-core path reads Qx itself
     if (K % 8 != 0 || (act_operand && K % 128 != 0)) return QOQ_ERR_UNSUPPORTED;
     if (!X || !gamma || !Qx || !s_x) return QOQ_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(gamma, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) ||
@@ -215,7 +221,8 @@ int qoq_silu_mul_quant_act(const uint16_t *H, int M, int F, int8_t *Qx, uint16_t
                            void *act_operand, uint16_t *Y, uint32_t flags, qoq_stream_t stream) {
     if (M <= 0 || F <= 0) return QOQ_ERR_INVALID_ARG;
     if (flags & ~QOQ_LAUNCH_OVERLAP) return QOQ_ERR_UNSUPPORTED;
-    if (act_operand && kind != 1 && kind != 2) return QOQ_ERR_INVALID_ARG;
+    if (act_operand && kind != 1 && kind != 2 && kind != 3) return QOQ_ERR_INVALID_ARG;
+    if (kind == 3) act_operand = nullptr;  // the CUDA-core path reads Qx itself
     if (F % 8 != 0 || (act_operand && F % 128 != 0)) return QOQ_ERR_UNSUPPORTED;
     if (!H || !Qx || !s_x) return QOQ_ERR_INVALID_ARG;
     if (!aligned(H, 16) || !aligned(Qx, 16) || !aligned(s_x, 2) || (t_x && !aligned(t_x, 4)) ||
@@ -229,7 +236,7 @@ int qoq_silu_mul_quant_act(const uint16_t *H, int M, int F, int8_t *Qx, uint16_t
 size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gemm_options *opt) {
     if (check_gemm_shape(M, N, K, group) != QOQ_OK || check_options(opt) != QOQ_OK) return 0;
     qoq::GemmPlan plan;
-    if (!plan_for(M, N, K, group, opt, &plan)) return 0;
+    if (!plan_for(M, N, K, group, opt, &plan) || !plan_valid(plan)) return 0;
     return plan.ws_bytes;
 }
 
@@ -244,6 +251,7 @@ int qoq_gemm_path(int M, int N, int K, int group, const qoq_gemm_options *opt) {
     if (st != QOQ_OK) return -st;
     qoq::GemmPlan plan;
     if (!plan_for(M, N, K, group, opt, &plan)) return -QOQ_ERR_CUDA;
+    if (!plan_valid(plan)) return -QOQ_ERR_UNSUPPORTED;
     return plan.path;
 }
 
@@ -256,6 +264,7 @@ int qoq_gemm_plan(int M, int N, int K, int group, int num_sms, const qoq_gemm_op
     if (st != QOQ_OK) return st;
     const qoq::GemmPlan plan = qoq::plan_gemm(M, N, K, group, num_sms, opt ? opt->kernel : 0,
                                               opt ? opt->tokens_per_tile : 0, opt ? opt->num_ctas : 0);
+    if (!plan_valid(plan)) return QOQ_ERR_UNSUPPORTED;
     out->path = plan.path;
     out->tokens_per_tile = plan.BT;
     out->num_ctas = plan.ctas;

@@ -789,9 +789,59 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
 
 }  // namespace
 
+namespace {
+// Shared memory of a GEMV-path CTA: activations and their group sums for its
+// blocks, and two int32 reduction buffers (the launcher sizes it the same way).
+size_t gemv_smem_bytes(int MT, int G, int csize) {
+    const size_t nb = static_cast<size_t>((G + csize - 1) / csize);
+    return MT * nb * 128 + MT * nb * 4 + 2 * static_cast<size_t>(MT) * 128 * 4;
+}
+constexpr size_t kGemvSmemMax = 200u << 10;
+}  // namespace
+
 GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, int force_bt,
                    int force_ctas) {
     GemmPlan pl{};
+    const int G = K / kTileK, n_tiles = N / kTileN;
+    // Decode batches of at most 8 tokens: the CUDA-core GEMV path, whose
+    // launches carry no tensor-core setup, when its shared memory fits.
+    int mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
+    int csize = 1;
+    if (M <= 8 && num_sms > 0) {
+        // The largest cluster (K split) that keeps at most six 256-thread CTAs
+        // per SM and at least one 128-k block per K half of a CTA.
+        for (int c = 8; c >= 1; c >>= 1) {
+            if (static_cast<long long>(n_tiles) * c <= 6LL * num_sms && G >= 2 * c) {
+                csize = c;
+                break;
+            }
+        }
+        if (force_path == kPathGemv && force_ctas > 0) csize = force_ctas >= 8 ? 8 : (force_ctas >= 4 ? 4 : (force_ctas >= 2 ? 2 : 1));
+        while (csize < 8 && gemv_smem_bytes(mt, G, csize) > kGemvSmemMax) csize *= 2;
+    }
+    const bool gemv_ok = M <= 8 && (group == 0 || group == 128) && gemv_smem_bytes(mt, G, csize) <= kGemvSmemMax;
+    if (force_path == kPathGemv || (force_path == 0 && force_bt == 0 && gemv_ok)) {
+        if (!gemv_ok) {
+            // forced for a shape the path cannot take: report an empty plan
+            pl.path = 0;
+            return pl;
+        }
+        pl.path = kPathGemv;
+        pl.BT = mt;
+        pl.tok_tiles = 1;
+        pl.n_tiles = n_tiles;
+        pl.G = G;
+        pl.tiles = n_tiles;
+        pl.total = static_cast<long long>(n_tiles) * G;
+        pl.gv_csize = csize;
+        pl.ctas = n_tiles * csize;
+        pl.counters_offset = kWsStatusBytes;
+        pl.slots_offset = kWsStatusBytes;
+        pl.zero_bytes = kWsStatusBytes;
+        pl.act_offset = kWsStatusBytes;
+        pl.ws_bytes = kWsStatusBytes;
+        return pl;
+    }
     // The fp8 path (4 MMAs per 128-k group, per-group exact drain) wins for
     // decode batches; larger token tiles keep the fp16 path.
     int path = force_path;
@@ -843,6 +893,7 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
     }
     if (ctas > pl.total) ctas = pl.total;
     pl.ctas = static_cast<int>(ctas);
+    pl.gv_csize = 0;
     pl.counters_offset = kWsStatusBytes;
     pl.slots_offset = kWsStatusBytes + (static_cast<size_t>(pl.ctas) * 4 + 255) / 256 * 256;
     pl.zero_bytes = pl.slots_offset + static_cast<size_t>(pl.ctas) * bt * kTileN * 4;
@@ -852,6 +903,7 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
 }
 
 cudaError_t launch_gemm(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
+    if (plan.path == kPathGemv) return launch_gemv(a, plan, stream);
     if (plan.path == kPathF8) return launch_gemm_f8(a, plan, stream);
     switch (plan.BT) {
         case 16: return launch_bt<16>(a, plan, stream);

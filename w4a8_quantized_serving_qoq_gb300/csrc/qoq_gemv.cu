@@ -1,0 +1,315 @@
+// W4A8 GEMM for decode batches (M <= 8) on the CUDA cores: the GEMV regime,
+// where a launch streams the 4-bit weights once and does a handful of
+// multiply-adds per weight.
+//
+// Sources: "QServe: W4A8KV4 Quantization and System Co-design for Efficient
+// LLM Serving" (papercache summary), sections "逐组W4A8 GEMM中的快速反量化"
+// (dequantization in byte lanes, multiply then subtract, legal under the
+// protective range) and "逐通道W4A8 GEMM中的快速反量化" (eq. 13: the zero
+// folded out of the main loop through t_x); "QServe：把 W4A8KV4 的理论收益做
+// 成实测吞吐的量化—系统协同设计" (zenmind review) 3.2: for small m, slice the
+// reduction dimension and reduce the partial sums on chip.
+//
+// GB300 design:
+//  * one lane per weight row: a 128-row tile of the packed weights is read
+//    by four warps as 512-byte coalesced rows of 16-byte chunks (the packed
+//    block order), non-allocating in L1;
+//  * one 32-bit multiply-add per 4 weights gives (q4 - z) * s_g + 128 in each
+//    byte (no carries: the protective range keeps (q4 - z) s_g in
+//    [-127, 127]); dp4a.u32.s32 multiplies the four biased weights with four
+//    INT8 activations and accumulates in exact int32; the bias comes out as
+//    128 * (sum of the group's activations), computed once per CTA;
+//    per-channel weights need no dequantization at all (raw q4, then
+//    - z * t_x at the end);
+//  * the K dimension is split over the CTAs of a thread-block cluster (and
+//    over two warp groups in each CTA); the int32 partial sums are reduced in
+//    shared memory and across the cluster through distributed shared memory,
+//    each CTA finishing an equal share of the tile's rows, so no partial sum
+//    leaves the chip and no workspace round trip or split-tile tail follows;
+//  * under programmatic dependent launch the weights of the first blocks are
+//    loaded before the wait for the preceding kernel (weights are static).
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "qoq_device.cuh"
+#include "qoq_internal.h"
+
+namespace qoq {
+namespace {
+
+constexpr int kGvThreads = 256;  // 8 warps: rows 32 (w % 4) .. +31 of the tile, K half w / 4
+
+struct GemvParams {
+    const uint8_t *packed;
+    const int8_t *Qx;
+    const uint16_t *s_x;
+    const int32_t *t_x;
+    const uint16_t *s_w;
+    uint16_t *O;
+    int32_t *acc_out;
+    uint32_t *status;
+    int M, N, K, group, G;
+    int csize;     // CTAs per cluster: the K split
+    int nb_max;    // blocks (128 k) per CTA, at most
+};
+
+__device__ __forceinline__ float h2f_gv(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void *p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_dsmem_s32(const int *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// One packed 128 x 128 block as this lane (weight row r) sees it.
+struct BlockRegs {
+    uint4 c[4];     // k = 32 p .. 32 p + 31, p = 0..3
+    uint32_t meta;  // s_g | z << 8 | code sum << 16 (group mode)
+};
+
+__device__ __forceinline__ void load_block(BlockRegs &br, const uint8_t *blk, int r, bool group) {
+#pragma unroll
+    for (int p4 = 0; p4 < 4; ++p4) br.c[p4] = ld_stream_v4(blk + 16 * (p4 * 128 + r));
+    br.meta = group ? ld_stream_u32(blk + kCodeBytes + 4 * r) : 0u;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams p) {
+    extern __shared__ __align__(16) uint8_t gv_smem[];
+    const int nbm = p.nb_max;
+    uint32_t *xs = reinterpret_cast<uint32_t *>(gv_smem);                    // [MT][nbm * 32] words of Qx
+    int *gsum = reinterpret_cast<int *>(gv_smem + MT * nbm * 128);           // [MT][nbm]
+    int *red = gsum + MT * nbm;                                              // [MT][128]: K half 1
+    int *part = red + MT * 128;                                              // [MT][128]: this CTA's sums
+    __shared__ int hdr_ok;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = 32 * (warp & 3) + lane;  // weight row in the tile
+    const int half = warp >> 2;
+    const int tile = blockIdx.y;
+    const uint32_t crank = p.csize > 1 ? cluster_rank() : 0u;
+    const bool group = p.group != 0;
+    const uint32_t bb = block_bytes(p.group);
+    // blocks of this CTA, then of this warp's K half
+    const int kb0 = static_cast<int>(crank) * p.G / p.csize, kb1 = (static_cast<int>(crank) + 1) * p.G / p.csize;
+    const int nb = kb1 - kb0;
+    const int hmid = kb0 + nb / 2;
+    const int wb0 = half ? hmid : kb0, wb1 = half ? kb1 : hmid;
+    const uint8_t *tile_base = p.packed + kHeaderBytes + static_cast<size_t>(tile) * p.G * bb;
+
+    if (threadIdx.x == 0) {
+        griddep_launch_dependents();
+        const PackedHeader *h = reinterpret_cast<const PackedHeader *>(p.packed);
+        hdr_ok = (h->magic == kPackedMagic && h->version == kPackedVersion && h->N == p.N && h->K == p.K &&
+                  h->group == p.group && h->illegal == 0u) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!hdr_ok) {  // the same decision in every CTA of every cluster: none reaches a cluster barrier
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
+            griddep_wait();  // the status word may still be in use by the preceding kernel
+            atomicOr(p.status, kStatusBadPacked);
+        }
+        return;
+    }
+    // Weights are static: the first block streams in while the preceding kernel finishes.
+    BlockRegs cur;
+    if (wb0 < wb1) load_block(cur, tile_base + static_cast<size_t>(wb0) * bb, r, group);
+    griddep_wait();
+
+    // This CTA's activations [M][nb * 128] into shared memory (tokens >= M read as 0),
+    // and per (token, block) the sum of the 128 activations.
+    {
+        const int words = nb * 32;
+        for (int idx = threadIdx.x; idx < MT * words / 4; idx += kGvThreads) {
+            const int m = idx / (words / 4), q = idx % (words / 4);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (m < p.M) v = __ldg(reinterpret_cast<const uint4 *>(p.Qx + static_cast<size_t>(m) * p.K + kb0 * 128) + q);
+            reinterpret_cast<uint4 *>(xs + m * nbm * 32)[q] = v;
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < MT * nb; idx += kGvThreads) {
+            const int m = idx / nb, j = idx % nb;
+            const uint32_t *w = xs + m * nbm * 32 + j * 32;
+            int s = 0;
+#pragma unroll 8
+            for (int i = 0; i < 32; ++i) s = __dp4a(static_cast<int>(w[i]), 0x01010101, s);
+            gsum[m * nbm + j] = s;
+        }
+        __syncthreads();
+    }
+
+    int acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0;
+    for (int b = wb0; b < wb1; ++b) {
+        BlockRegs nxt;
+        if (b + 1 < wb1) load_block(nxt, tile_base + static_cast<size_t>(b + 1) * bb, r, group);
+        const int jb = b - kb0;  // block index inside the CTA's activation slice
+        const uint32_t s = group ? (cur.meta & 0xffu) : 1u;
+        const uint32_t z = group ? ((cur.meta >> 8) & 0xffu) : 0u;
+        // group mode: bytes (q - z) s + 128; per-channel: the raw codes q
+        const uint32_t cst = group ? static_cast<uint32_t>(128 - static_cast<int>(z * s)) * 0x01010101u : 0u;
+#pragma unroll
+        for (int p4 = 0; p4 < 4; ++p4) {
+            const uint32_t w4[4] = {cur.c[p4].x, cur.c[p4].y, cur.c[p4].z, cur.c[p4].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t ulo = (w4[j] & 0x0F0F0F0Fu) * s + cst;         // k = 32 p + 8 j + 0..3
+                const uint32_t uhi = ((w4[j] >> 4) & 0x0F0F0F0Fu) * s + cst;  // k = 32 p + 8 j + 4..7
+                const int wi = jb * 32 + 8 * p4 + 2 * j;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    if (m < p.M) {
+                        const uint2 x = *reinterpret_cast<const uint2 *>(xs + m * nbm * 32 + wi);
+                        acc[m] = dp4a_us(ulo, x.x, acc[m]);
+                        acc[m] = dp4a_us(uhi, x.y, acc[m]);
+                    }
+                }
+            }
+        }
+        if (group) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[m] -= 128 * gsum[m * nbm + jb];
+        }
+        if (b + 1 < wb1) cur = nxt;
+    }
+
+    // ---- K halves of the CTA, then the CTAs of the cluster
+    if (half) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) red[m * 128 + r] = acc[m];
+    }
+    __syncthreads();
+    if (!half) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) part[m * 128 + r] = acc[m] + red[m * 128 + r];
+    }
+    if (p.csize > 1) cluster_sync();  // every CTA's part[] complete and visible in the cluster
+    else __syncthreads();
+    // this CTA finishes rows [crank * 128 / csize, (crank + 1) * 128 / csize) of the tile
+    const int rows = 128 / p.csize, row0 = static_cast<int>(crank) * rows;
+    for (int idx = threadIdx.x; idx < MT * rows; idx += kGvThreads) {
+        const int m = idx / rows, rr = row0 + idx % rows;
+        if (m >= p.M) continue;
+        int tot = part[m * 128 + rr];
+        for (int q = 0; q < p.csize; ++q)
+            if (q != static_cast<int>(crank)) tot += ld_dsmem_s32(part + m * 128 + rr, static_cast<uint32_t>(q));
+        const int n = tile * 128 + rr;
+        if (!group) tot -= static_cast<int>(p.packed[packed_z_offset(p.N, p.K) + n]) * p.t_x[m];
+        const size_t idx_o = static_cast<size_t>(m) * p.N + n;
+        if (p.acc_out)
+            p.acc_out[idx_o] = tot;
+        else
+            p.O[idx_o] = __half_as_ushort(__float2half_rn(
+                __fmul_rn(__fmul_rn(static_cast<float>(tot), h2f_gv(p.s_x[m])), h2f_gv(p.s_w[n]))));
+    }
+    if (p.csize > 1) cluster_sync();  // peers' shared memory stays alive until every read is done
+}
+
+template <int MT>
+cudaError_t launch_gemv_mt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
+    const int nb_max = (plan.G + plan.gv_csize - 1) / plan.gv_csize;
+    const size_t smem = static_cast<size_t>(MT) * nb_max * 128 + static_cast<size_t>(MT) * nb_max * 4 +
+                        2 * static_cast<size_t>(MT) * 128 * 4;
+    static std::mutex mu;
+    static size_t configured[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (configured[dev] < smem) {
+            e = cudaFuncSetAttribute(w4a8_gemv_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+            configured[dev] = smem;
+        }
+    }
+    GemvParams p;
+    p.packed = static_cast<const uint8_t *>(a.packed);
+    p.Qx = a.Qx;
+    p.s_x = a.s_x;
+    p.t_x = a.t_x;
+    p.s_w = a.s_w;
+    p.O = a.O;
+    p.acc_out = a.acc_out;
+    p.status = static_cast<uint32_t *>(a.ws);
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.group = a.group;
+    p.G = plan.G;
+    p.csize = plan.gv_csize;
+    p.nb_max = nb_max;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.gv_csize, plan.n_tiles);
+    cfg.blockDim = dim3(kGvThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (plan.gv_csize > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(plan.gv_csize);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (a.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = na ? attr : nullptr;
+    cfg.numAttrs = static_cast<unsigned>(na);
+    return cudaLaunchKernelEx(&cfg, w4a8_gemv_kernel<MT>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
+    switch (plan.BT) {
+        case 1: return launch_gemv_mt<1>(a, plan, stream);
+        case 2: return launch_gemv_mt<2>(a, plan, stream);
+        case 4: return launch_gemv_mt<4>(a, plan, stream);
+        case 8: return launch_gemv_mt<8>(a, plan, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qoq

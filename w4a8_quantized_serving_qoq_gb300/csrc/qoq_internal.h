@@ -78,17 +78,19 @@ __host__ __device__ inline int act_tg_pitch(int M) { return (M + 3) & ~3; }
 __host__ __device__ inline size_t act_planes_bytes(int M, int K) { return 2 * static_cast<size_t>(M) * K; }
 __host__ __device__ inline size_t act_operand_bytes(int M, int K, int kind) {
     if (kind == 1) return 2 * static_cast<size_t>(M) * K;
+    if (kind == 3) return 0;  // the CUDA-core path reads Qx itself
     return act_planes_bytes(M, K) + static_cast<size_t>(K / kTileK) * act_tg_pitch(M) * 4;
 }
 
 enum GemmPath : int {
     kPathF16 = 1,          // weights dequantized to exact fp16, kind::f16 MMA
     kPathF8 = 2,           // raw 4-bit codes and split activations as exact e4m3, kind::f8f6f4 MMA
+    kPathGemv = 3,         // decode batches (M <= 8): CUDA-core dp4a, K split over a thread-block cluster
 };
 
 struct GemmPlan {
     int path;              // GemmPath
-    int BT;                // tokens per tile: 16, 32, 64 or 128
+    int BT;                // tokens per tile: 16, 32, 64 or 128 (GEMV path: tokens per launch, 1, 2, 4 or 8)
     int tok_tiles;         // ceil(M / BT)
     int n_tiles;           // N / 128
     int G;                 // K / 128 k-stages per tile
@@ -100,6 +102,7 @@ struct GemmPlan {
     size_t slots_offset;
     size_t act_offset;     // activation operand scratch (used when the caller passes none)
     size_t zero_bytes;     // leading workspace bytes that must be zero before a launch
+    int gv_csize;          // GEMV path: CTAs per cluster (K split), 1, 2, 4 or 8
 };
 
 // Kernel path, tile shape and persistent-CTA count for one GEMM.
@@ -166,6 +169,7 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream);
 cudaError_t launch_gemm_f8(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream);
+cudaError_t launch_gemv(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream);
 
 // Debug flag: the TMA producer withholds the second stage's load, so the
 // consumers' bounded waits expire (exercises the timeout path).

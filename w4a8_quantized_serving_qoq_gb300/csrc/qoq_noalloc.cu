@@ -70,6 +70,7 @@ extern "C" int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, cons
     int st = setup_current_device(&scratch, &sms);
     if (st != QOQ_OK) return st;
     const qoq::GemmPlan plan = qoq::plan_gemm(M, N, K, group, sms);
+    if (plan.path < 1 || plan.path > 3) return QOQ_ERR_UNSUPPORTED;
     if (plan.total * (plan.ctas + 1ll) >= (1ll << 32)) return QOQ_ERR_UNSUPPORTED;
     if (plan.ws_bytes > kNoAllocScratchBytes) return QOQ_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
