@@ -421,7 +421,7 @@ def test_end_to_end_tiny_workload():
 
 # ----------------------------------------------------------- error paths --
 def test_workspace_too_small_rejected():
-    M, N, K = 8, 256, 4096
+    M, N, K = 16, 256, 4096   # a tensor-core path (M <= 8 needs only the status area)
     need = qoq.qoq_gemm_workspace_bytes(M, N, K, 128)
     assert need > 256  # status area plus counters and partial-tile slots
     ws = qoq.new_workspace(256)
