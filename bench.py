@@ -83,6 +83,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-points", action="store_true", help="skip the per-point timings (and the blocks)")
     ap.add_argument("--blocks", default="fused_quant,kv4_attention,qwen72b,per_channel",
                     help="comma list of extra workloads timed point by point ('' for none)")
+    ap.add_argument("--tune", action="store_true",
+                    help="time the GEMM's candidate launch choices for every shape and token count of the "
+                         "workloads on this GPU, write the planner's dispatch table (csrc/qoq_dispatch_table.inc) "
+                         "and print a summary instead of the benchmark line")
     ap.add_argument("--layers", default="qkv,o,gate_up,down")
     ap.add_argument("--ms", default="1,8,32,64,128,256,4096",
                     help="token counts of the headline step (4096 = the prefill workload)")
@@ -347,6 +351,152 @@ def run_reference(args, points):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- dispatch table --
+DISPATCH_TABLE = os.path.join(ROOT, "w4a8_quantized_serving_qoq_gb300", "csrc", "qoq_dispatch_table.inc")
+
+
+def gemm_candidates(M, N, K, group, sms):
+    """(path, tokens_per_tile, ctas) launch choices timed by --tune; (0, 0, 0)
+    is the planner's current automatic choice.  ctas is the CTA count (paths
+    1 and 2) or the cluster size (path 3)."""
+    tiles = N // 128
+    cands = [(0, 0, 0)]
+    if M <= 8:
+        cands += [(3, 0, c) for c in (1, 2, 4, 8)]
+    if group == 128 and M <= 64:
+        for bt in (16, 32):
+            if bt == 16 and M > 32:
+                continue
+            t = -(-M // bt) * tiles
+            cands += [(2, bt, c) for c in sorted({sms, sms - 8} | ({t} if t <= sms else set()))]
+    cap = 128 if M > 64 else max(16, 1 << (max(M, 1) - 1).bit_length())
+    for bt in (16, 32, 64, 128):
+        if bt > cap or (M >= 256 and bt < 64):
+            continue
+        t = -(-M // bt) * tiles
+        cands += [(1, bt, c) for c in sorted({sms} | ({t} if t <= sms else set()))]
+    return cands
+
+
+def write_dispatch_table(entries, sms):
+    lines = ["// Measured launch choices of the W4A8 GEMM planner, written by",
+             "// `python bench.py --tune` on a GPU (the entries apply only to GPUs with the",
+             "// same SM count).  One entry per line:",
+             "//   {N, K, group, M, num_sms, path, tokens_per_tile, ctas (path 3: cluster size)},",
+             "// with the measured time of the choice and of the planner's rules."]
+    for e in sorted(entries, key=lambda e: (e["N"], e["K"], e["group"], e["M"])):
+        lines.append(f"{{{e['N']}, {e['K']}, {e['group']}, {e['M']}, {sms}, {e['path']}, {e['bt']}, {e['ctas']}}},"
+                     f"  // {e['us']:.2f} us (rules {e['rule_us']:.2f} us)")
+    with open(DISPATCH_TABLE, "w") as f:
+        f.write("\n".join(lines) + "\n")
+
+
+def run_tune(args):
+    """Times every candidate launch choice of every GEMM point of the four
+    full-size workloads (weights rotated past L2, graphs of back-to-back
+    launches as in the per-point timings), keeps the fastest per (N, K,
+    group, M) and writes the dispatch table the planner reads."""
+    import torch
+    import w4a8_quantized_serving_qoq_gb300 as qoq
+    from w4a8_quantized_serving_qoq_gb300 import synthetic
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    l2_bytes = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
+    stream = torch.cuda.current_stream()
+    points = []
+    for wid in (1, 2, 3, 4):
+        _, layers, Ms, _, _, _, _ = synthetic.WORKLOADS[wid]
+        points += [(wid, layer, M) for layer in layers for M in Ms]
+    seen, entries, report = set(), [], []
+    loaded = [None, None]
+    for wid, layer, M in points:
+        _, _, _, sigma, wo, xo, group = synthetic.WORKLOADS[wid]
+        key = (layer.N, layer.K, group, M)
+        if key in seen:
+            continue
+        seen.add(key)
+        s_ = synthetic.layer_seed(wid, layer)
+        if loaded[0] != (wid, layer.name):  # points come layer by layer: load each layer's weights once
+            loaded[1] = None
+            torch.cuda.empty_cache()
+            W = torch.from_numpy(synthetic.weights(layer.N, layer.K, s_, sigma, wo)).to(dev)
+            wq = qoq.qoq_quantize_weights(W, group)
+            packed = qoq.qoq_pack_weights(wq["q4"], wq["s_g"], wq["z"], group)
+            ncopy = max(3, -(-2 * l2_bytes // packed.numel()) + 1)
+            loaded[:] = [(wid, layer.name), ([packed] + [packed.clone() for _ in range(ncopy - 1)], wq["s_w"])]
+            del W, wq, packed
+        copies, s_w = loaded[1]
+        X = torch.from_numpy(synthetic.activations(M, layer.K, s_, xo)).to(dev)
+        acts = {}
+        Qx = sx = tx = None
+        for kind in (1, 2, 3):
+            if kind == 2 and group != 128:
+                continue
+            Qx, sx, tx, act = qoq.qoq_quant_act_ex(X, kind=kind, with_t=True)
+            acts[kind] = act
+        O = torch.empty((M, layer.N), dtype=torch.float16, device=dev)
+        ws = qoq.new_workspace(1 << 20, dev)
+        times = {}
+        for cand in gemm_candidates(M, layer.N, layer.K, group, sms):
+            path, bt, ctas = cand
+            try:
+                kind = qoq.qoq_gemm_path(M, layer.N, layer.K, group, qoq.gemm_options(kernel=path, tokens_per_tile=bt,
+                                                                                      num_ctas=ctas))
+            except qoq.QoqError:
+                continue
+            opt = qoq.gemm_options(kernel=path, tokens_per_tile=bt, num_ctas=ctas, act_operand=acts.get(kind),
+                                   flags=qoq.QOQ_LAUNCH_OVERLAP)
+            need = qoq.qoq_gemm_workspace_bytes(M, layer.N, layer.K, group, opt)
+            if need > ws.numel():
+                ws = qoq.new_workspace(need, dev)
+
+            def fn(r):
+                qoq.qoq_w4a8_gemm_ex(Qx, sx, tx, copies[r % len(copies)], s_w, layer.N, layer.K, group, O=O,
+                                     workspace=ws, options=opt)
+            fn(0)
+            torch.cuda.synchronize()
+            reps = max(8 if M * layer.N * layer.K >= 2 ** 36 else args.point_reps, len(copies))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for r in range(reps):
+                    fn(r)
+            for _ in range(2):
+                g.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3 / reps)
+            del g
+            times[cand] = statistics.median(ts)
+        status = qoq.qoq_workspace_status(ws)[0]
+        best = min(times, key=times.get)
+        rule_us = times[(0, 0, 0)]
+        if best == (0, 0, 0):  # record what the rules chose, so the table pins it
+            info = qoq.qoq_gemm_plan(M, layer.N, layer.K, group, sms)
+            best_entry = (info["path"], info["tokens_per_tile"] if info["path"] != 3 else 0,
+                          info["num_ctas"] // (layer.N // 128) if info["path"] == 3 else info["num_ctas"])
+        else:
+            best_entry = best
+        entries.append(dict(N=layer.N, K=layer.K, group=group, M=M, path=best_entry[0], bt=best_entry[1],
+                            ctas=best_entry[2], us=times[best], rule_us=rule_us))
+        report.append({"workload": wid, "layer": layer.name, "M": M, "best": list(best_entry),
+                       "best_us": round(times[best], 2), "rule_us": round(rule_us, 2), "status": status,
+                       "candidates": {f"{p}/{b}/{c}": round(t, 2) for (p, b, c), t in times.items()}})
+        print(json.dumps(report[-1]), file=sys.stderr, flush=True)
+        del copies, X, acts, O
+    write_dispatch_table(entries, sms)
+    print(json.dumps({"tuned": len(entries), "num_sms": sms, "table": DISPATCH_TABLE,
+                      "rules_us": sum(e["rule_us"] for e in entries), "table_us": sum(e["us"] for e in entries),
+                      "points": report}), flush=True)
+
+
 # ------------------------------------------------------------ GPU path --
 def main(argv=None):
     args = parse_args(argv)
@@ -355,6 +505,9 @@ def main(argv=None):
     points = headline_points(args.layers.split(","), Ms)
     if args.impl == "reference":
         run_reference(args, points)
+        return
+    if args.tune:
+        run_tune(args)
         return
 
     import torch

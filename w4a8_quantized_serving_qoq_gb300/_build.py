@@ -33,7 +33,8 @@ def sources() -> list[str]:
 
 
 def _inputs() -> list[str]:
-    return sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + [
+    return sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
+        glob.glob(os.path.join(CSRC, "*.inc")) + [
         os.path.join(ROOT, "include", "qoq.h"), os.path.abspath(__file__)]
 
 

@@ -790,6 +790,29 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
 }  // namespace
 
 namespace {
+// Measured launch choices: for a shape (N, K, group) tuned on a GPU with
+// num_sms SMs, the fastest (path, tokens per tile, CTA count or cluster
+// size) found at token count M, timed on that GPU against the other
+// candidates and the rules below (the ADAngel review's offline per-shape
+// policy table, looked up at run time).  An entry covers the token counts
+// above the next smaller tuned M of the same shape, up to its own M.
+struct DispatchEntry {
+    int N, K, group, M, num_sms, path, bt, ctas;
+};
+const DispatchEntry kDispatchTable[] = {
+#include "qoq_dispatch_table.inc"
+    {0, 0, 0, 0, 0, 0, 0, 0}  // end
+};
+
+const DispatchEntry *find_dispatch(int M, int N, int K, int group, int num_sms) {
+    const DispatchEntry *best = nullptr;
+    for (const DispatchEntry *e = kDispatchTable; e->N != 0; ++e) {
+        if (e->N != N || e->K != K || e->group != group || e->num_sms != num_sms || e->M < M) continue;
+        if (!best || e->M < best->M) best = e;
+    }
+    return best;
+}
+
 // Shared memory of a GEMV-path CTA: activations and their group sums for its
 // blocks, and two int32 reduction buffers (the launcher sizes it the same way).
 size_t gemv_smem_bytes(int MT, int G, int csize) {
@@ -801,6 +824,12 @@ constexpr size_t kGemvSmemMax = 200u << 10;
 
 GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, int force_bt,
                    int force_ctas) {
+    if (force_path == 0 && force_bt == 0 && force_ctas == 0) {
+        if (const DispatchEntry *e = find_dispatch(M, N, K, group, num_sms)) {
+            const GemmPlan t = plan_gemm(M, N, K, group, num_sms, e->path, e->bt, e->ctas);
+            if (t.path == e->path) return t;  // else the rules below
+        }
+    }
     GemmPlan pl{};
     const int G = K / kTileK, n_tiles = N / kTileN;
     // Decode batches of at most 8 tokens: the CUDA-core GEMV path, whose

@@ -131,6 +131,9 @@ __global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams 
     const int wb0 = half ? hmid : kb0, wb1 = half ? kb1 : hmid;
     const uint8_t *tile_base = p.packed + kHeaderBytes + static_cast<size_t>(tile) * p.G * bb;
 
+    // The header is checked before any weight is read (a call whose N or K
+    // disagrees with the buffer must not read past it).  The decision is the
+    // same in every CTA of every cluster, so none reaches a cluster barrier.
     if (threadIdx.x == 0) {
         griddep_launch_dependents();
         const PackedHeader *h = reinterpret_cast<const PackedHeader *>(p.packed);
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams 
                   h->group == p.group && h->illegal == 0u) ? 1 : 0;
     }
     __syncthreads();
-    if (!hdr_ok) {  // the same decision in every CTA of every cluster: none reaches a cluster barrier
+    if (!hdr_ok) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
             griddep_wait();  // the status word may still be in use by the preceding kernel
             atomicOr(p.status, kStatusBadPacked);
@@ -149,18 +152,17 @@ __global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams 
     BlockRegs cur;
     if (wb0 < wb1) load_block(cur, tile_base + static_cast<size_t>(wb0) * bb, r, group);
     griddep_wait();
-
-    // This CTA's activations [M][nb * 128] into shared memory (tokens >= M read as 0),
-    // and per (token, block) the sum of the 128 activations.
-    {
-        const int words = nb * 32;
-        for (int idx = threadIdx.x; idx < MT * words / 4; idx += kGvThreads) {
-            const int m = idx / (words / 4), q = idx % (words / 4);
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (m < p.M) v = __ldg(reinterpret_cast<const uint4 *>(p.Qx + static_cast<size_t>(m) * p.K + kb0 * 128) + q);
-            reinterpret_cast<uint4 *>(xs + m * nbm * 32)[q] = v;
-        }
-        __syncthreads();
+    // This CTA's activations [M][nb * 128] into shared memory (tokens >= M read as 0).
+    const int words = nb * 32;
+    for (int idx = threadIdx.x; idx < MT * words / 4; idx += kGvThreads) {
+        const int m = idx / (words / 4), q = idx % (words / 4);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (m < p.M) v = __ldg(reinterpret_cast<const uint4 *>(p.Qx + static_cast<size_t>(m) * p.K + kb0 * 128) + q);
+        reinterpret_cast<uint4 *>(xs + m * nbm * 32)[q] = v;
+    }
+    __syncthreads();
+    // per (token, block): the sum of its 128 activations (the bias of the biased weight bytes)
+    if (group) {
         for (int idx = threadIdx.x; idx < MT * nb; idx += kGvThreads) {
             const int m = idx / nb, j = idx % nb;
             const uint32_t *w = xs + m * nbm * 32 + j * 32;
