@@ -138,6 +138,17 @@ int qoq_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x, in
 #define QOQ_LAUNCH_OVERLAP 1u
 
 /*
+ * GEMM option flag (qoq_gemm_options.flags): QOQ_PLAN_RULES plans the launch
+ * by the planner's rules alone.  Without it an automatic plan (no kernel,
+ * tokens_per_tile or num_ctas forced) first looks the shape up in the
+ * library's measured dispatch table: launch choices timed per (N, K, group,
+ * M) on a GPU with the same SM count (the offline per-shape policy table of
+ * the ADAngel review, "离线 Oracle Policy Map 与在线查表"), an entry covering
+ * the token counts above the next smaller tuned M of its shape up to its own.
+ */
+#define QOQ_PLAN_RULES 2u
+
+/*
  * Bytes of an activation operand (0 for an invalid shape or kind; requires
  * K % 128 == 0).  An activation operand is the INT8 activation of
  * qoq_quant_act in the order and encoding one GEMM path's tensor cores
@@ -281,8 +292,8 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  *                     the same Qx (16-byte aligned), of the kind equal to
  *                     this GEMM's qoq_gemm_path; the GEMM reads it instead
  *                     of building it.  NULL = build it in the workspace.
- *   flags           : 0 or QOQ_LAUNCH_OVERLAP (see above; other bits:
- *                     QOQ_ERR_UNSUPPORTED).
+ *   flags           : 0, QOQ_LAUNCH_OVERLAP and / or QOQ_PLAN_RULES (see
+ *                     above; other bits: QOQ_ERR_UNSUPPORTED).
  */
 typedef struct {
     int tokens_per_tile;

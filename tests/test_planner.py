@@ -1,6 +1,9 @@
 """The GEMM launch planner (qoq_gemm_plan, host only): which tensor-core path,
 tile size and CTA count each Llama-3-8B decode shape gets on a 152-SM GB300,
 the option overrides, the workspace layout and argument errors."""
+import os
+import re
+
 import pytest
 
 import w4a8_quantized_serving_qoq_gb300 as qoq
@@ -10,9 +13,10 @@ QKV, O, GATE_UP, DOWN = (6144, 4096), (4096, 4096), (28672, 4096), (4096, 14336)
 
 
 def _plan(M, NK, group=128, **opt):
+    """The planner's rules (the measured dispatch table is pinned separately)."""
     N, K = NK
-    options = qoq.gemm_options(**opt) if opt else None
-    return qoq.qoq_gemm_plan(M, N, K, group, SMS, options)
+    opt["flags"] = opt.get("flags", 0) | qoq.QOQ_PLAN_RULES
+    return qoq.qoq_gemm_plan(M, N, K, group, SMS, qoq.gemm_options(**opt))
 
 
 @pytest.mark.parametrize("M", [16, 32])
@@ -124,3 +128,49 @@ def test_allocation_free_limit_depends_on_the_shape():
     assert _plan(128, O)["workspace_bytes"] <= limit
     assert _plan(128, GATE_UP)["workspace_bytes"] > limit
     assert _plan(64, (8192, 29568))["workspace_bytes"] > limit
+
+
+# ---------------------------------------------------------- dispatch table --
+TABLE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                     "w4a8_quantized_serving_qoq_gb300", "csrc", "qoq_dispatch_table.inc")
+
+
+def _table():
+    rows = []
+    for line in open(TABLE):
+        m = re.match(r"\{([-\d, ]+)\},", line.strip())
+        if m:
+            rows.append(tuple(int(v) for v in m.group(1).split(",")))
+    return rows
+
+
+def test_table_entries_are_what_an_automatic_plan_gets():
+    """Every measured entry {N, K, group, M, num_sms, path, tokens, ctas} is
+    the plan of that shape on a GPU with that SM count (cluster size for the
+    CUDA-core path), and of every M down to the next smaller tuned M."""
+    rows = _table()
+    for N, K, group, M, sms, path, bt, ctas in rows:
+        p = qoq.qoq_gemm_plan(M, N, K, group, sms)
+        assert p["path"] == path
+        if path == 3:
+            assert p["num_ctas"] == (N // 128) * ctas
+        else:
+            assert (p["tokens_per_tile"], p["num_ctas"]) == (bt, min(ctas, p["k_stages"]))
+        below = [r[3] for r in rows if r[:3] == (N, K, group) and r[4] == sms and r[3] < M]
+        lo = max(below) + 1 if below else 1
+        assert qoq.qoq_gemm_plan(lo, N, K, group, sms)["path"] == (path if lo <= 8 or path != 3 else p["path"])
+
+
+def test_table_applies_only_to_its_gpu_and_shapes():
+    rows = _table()
+    for N, K, group, M, sms, path, bt, ctas in rows[:5]:
+        other = qoq.qoq_gemm_plan(M, N, K, group, sms + 4)
+        rules = qoq.qoq_gemm_plan(M, N, K, group, sms + 4, qoq.gemm_options(flags=qoq.QOQ_PLAN_RULES))
+        assert other == rules
+    # a shape nobody tuned plans by the rules
+    p = qoq.qoq_gemm_plan(8, 1024, 1024, 128, 152)
+    assert p == qoq.qoq_gemm_plan(8, 1024, 1024, 128, 152, qoq.gemm_options(flags=qoq.QOQ_PLAN_RULES))
+    # beyond the largest tuned M of a shape: the rules
+    big = max((r for r in rows if r[:3] == (4096, 4096, 128)), key=lambda r: r[3])
+    p = qoq.qoq_gemm_plan(big[3] * 2, 4096, 4096, 128, big[4])
+    assert p == qoq.qoq_gemm_plan(big[3] * 2, 4096, 4096, 128, big[4], qoq.gemm_options(flags=qoq.QOQ_PLAN_RULES))

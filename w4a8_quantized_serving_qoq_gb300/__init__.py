@@ -21,6 +21,7 @@ _lib = None
 
 QOQ_OK = 0
 QOQ_LAUNCH_OVERLAP = 1  # programmatic dependent launch (include/qoq.h)
+QOQ_PLAN_RULES = 2      # plan by the rules alone, not the measured dispatch table
 STATUS_NAMES = {
     0: "QOQ_OK", 1: "QOQ_ERR_INVALID_ARG", 2: "QOQ_ERR_UNSUPPORTED", 3: "QOQ_ERR_MISALIGNED",
     4: "QOQ_ERR_WORKSPACE", 5: "QOQ_ERR_CUDA", 6: "QOQ_ERR_TIMEOUT", 7: "QOQ_ERR_DEVICE",
@@ -523,5 +524,5 @@ def qoq_workspace_status(workspace, stream=None):
 
 __all__ = [n for n in dir() if n.startswith("qoq_")] + [
     "QoqError", "build", "load", "library_path", "header_functions", "new_workspace", "gemm_options",
-    "QOQ_LAUNCH_OVERLAP",
+    "QOQ_LAUNCH_OVERLAP", "QOQ_PLAN_RULES",
 ]

@@ -779,6 +779,7 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     p.tok_tiles = plan.tok_tiles;
     p.total = plan.total;
     p.ctas = plan.ctas;
+    p.dp_tiles = plan.dp_tiles;
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
     dim3 grid(plan.ctas);
@@ -823,8 +824,8 @@ constexpr size_t kGemvSmemMax = 200u << 10;
 }  // namespace
 
 GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, int force_bt,
-                   int force_ctas) {
-    if (force_path == 0 && force_bt == 0 && force_ctas == 0) {
+                   int force_ctas, bool use_table) {
+    if (use_table && force_path == 0 && force_bt == 0 && force_ctas == 0) {
         if (const DispatchEntry *e = find_dispatch(M, N, K, group, num_sms)) {
             const GemmPlan t = plan_gemm(M, N, K, group, num_sms, e->path, e->bt, e->ctas);
             if (t.path == e->path) return t;  // else the rules below
@@ -923,6 +924,10 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
     if (ctas > pl.total) ctas = pl.total;
     pl.ctas = static_cast<int>(ctas);
     pl.gv_csize = 0;
+    // At least two waves of tiles: all but the last one to two waves go whole
+    // to the CTAs round-robin (concurrent CTAs share their weight and
+    // activation tiles in L2), the rest is balanced by stream-K.
+    pl.dp_tiles = pl.tiles >= 2 * ctas ? static_cast<int>((pl.tiles / ctas - 1) * ctas) : 0;
     pl.counters_offset = kWsStatusBytes;
     pl.slots_offset = kWsStatusBytes + (static_cast<size_t>(pl.ctas) * 4 + 255) / 256 * 256;
     pl.zero_bytes = pl.slots_offset + static_cast<size_t>(pl.ctas) * bt * kTileN * 4;

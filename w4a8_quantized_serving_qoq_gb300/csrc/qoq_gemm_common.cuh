@@ -28,6 +28,7 @@ struct GemmParams {
     int tok_tiles;
     long long total;        // tiles * G stages
     int ctas;
+    int dp_tiles;           // tiles [0, dp_tiles) go whole to CTAs round-robin; the rest is stream-K
     uint32_t debug_flags;
     uint64_t timeout_ns;
 };
@@ -53,22 +54,40 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Persistent stream-K schedule: the tiles x G k-stages of the GEMM are cut
-// into `ctas` contiguous, equal ranges; CTA c owns [c*T/P, (c+1)*T/P).  A
-// range crosses tile boundaries; each piece inside one tile is a segment.
-// Tiles are ordered token-tile fastest, so neighbouring work shares weights.
+// Persistent schedule, data-parallel then stream-K.  The first dp_tiles
+// tiles (a multiple of the CTA count, used when there are at least two waves
+// of tiles) go whole to the CTAs round-robin: CTA c takes tiles c, c + P,
+// c + 2P, ..., so the CTAs running at one time work on consecutive tiles,
+// which share weight and activation tiles in L2.  The remaining tiles x G
+// k-stages are cut into P contiguous, equal ranges; CTA c owns
+// [base + c R / P, base + (c + 1) R / P), base = dp_tiles G, R = the remaining
+// stages.  A range crosses tile boundaries; each piece inside one tile is a
+// segment.  Tiles are ordered token-tile fastest, so neighbouring work shares
+// weights.
 struct Segment {
     int tile, k0, k1;
 };
 
 struct SegmentWalker {
+    uint32_t dp_next, dp_end, dp_step;
     uint32_t w, w1, G;  // total stages < 2^31 (checked on the host)
     // ctas * total < 2^32 (checked on the host), so 32-bit arithmetic is exact.
     __device__ SegmentWalker(const GemmParams &p, int cta)
-        : w(static_cast<uint32_t>(cta) * static_cast<uint32_t>(p.total) / static_cast<uint32_t>(p.ctas)),
-          w1(static_cast<uint32_t>(cta + 1) * static_cast<uint32_t>(p.total) / static_cast<uint32_t>(p.ctas)),
-          G(static_cast<uint32_t>(p.G)) {}
+        : dp_next(static_cast<uint32_t>(cta)), dp_end(static_cast<uint32_t>(p.dp_tiles)),
+          dp_step(static_cast<uint32_t>(p.ctas)), G(static_cast<uint32_t>(p.G)) {
+        const uint32_t base = static_cast<uint32_t>(p.dp_tiles) * G;
+        const uint32_t R = static_cast<uint32_t>(p.total) - base;
+        w = base + static_cast<uint32_t>(cta) * R / static_cast<uint32_t>(p.ctas);
+        w1 = base + static_cast<uint32_t>(cta + 1) * R / static_cast<uint32_t>(p.ctas);
+    }
     __device__ bool next(Segment &s) {
+        if (dp_next < dp_end) {
+            s.tile = static_cast<int>(dp_next);
+            s.k0 = 0;
+            s.k1 = static_cast<int>(G);
+            dp_next += dp_step;
+            return true;
+        }
         if (w >= w1) return false;
         const uint32_t t = w / G;
         s.tile = static_cast<int>(t);
@@ -80,9 +99,12 @@ struct SegmentWalker {
     }
 };
 
-// CTA whose range holds global stage `s`.
+// CTA whose stream-K range holds global stage `s` (s in the stream-K part:
+// only split tiles ask, and every split tile lies there).
 __device__ __forceinline__ int cta_of_stage(uint32_t s, const GemmParams &p) {
-    return static_cast<int>(((s + 1) * static_cast<uint32_t>(p.ctas) - 1) / static_cast<uint32_t>(p.total));
+    const uint32_t base = static_cast<uint32_t>(p.dp_tiles) * static_cast<uint32_t>(p.G);
+    const uint32_t R = static_cast<uint32_t>(p.total) - base;
+    return static_cast<int>(((s - base + 1) * static_cast<uint32_t>(p.ctas) - 1) / R);
 }
 
 // Split-tile completion, decided by one thread: true when every other

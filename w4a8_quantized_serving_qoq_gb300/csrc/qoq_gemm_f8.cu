@@ -779,6 +779,7 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
     p.tok_tiles = plan.tok_tiles;
     p.total = plan.total;
     p.ctas = plan.ctas;
+    p.dp_tiles = plan.dp_tiles;
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
     if (a.acc_out)

@@ -21,11 +21,11 @@
 //    128 * (sum of the group's activations), computed once per CTA;
 //    per-channel weights need no dequantization at all (raw q4, then
 //    - z * t_x at the end);
-//  * the K dimension is split over the CTAs of a thread-block cluster (and
-//    over two warp groups in each CTA); the int32 partial sums are reduced in
-//    shared memory and across the cluster through distributed shared memory,
-//    each CTA finishing an equal share of the tile's rows, so no partial sum
-//    leaves the chip and no workspace round trip or split-tile tail follows;
+//  * the K dimension is split over the CTAs of a thread-block cluster and over
+//    two warp groups in each CTA; the int32 partial sums are reduced across
+//    the cluster through distributed shared memory, each CTA finishing an
+//    equal share of the tile's rows, so no partial sum leaves the chip and no
+//    workspace round trip or split-tile tail follows;
 //  * under programmatic dependent launch the weights of the first blocks are
 //    loaded before the wait for the preceding kernel (weights are static).
 #include <cuda.h>
@@ -113,8 +113,7 @@ __global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams 
     const int nbm = p.nb_max;
     uint32_t *xs = reinterpret_cast<uint32_t *>(gv_smem);                    // [MT][nbm * 32] words of Qx
     int *gsum = reinterpret_cast<int *>(gv_smem + MT * nbm * 128);           // [MT][nbm]
-    int *red = gsum + MT * nbm;                                              // [MT][128]: K half 1
-    int *part = red + MT * 128;                                              // [MT][128]: this CTA's sums
+    int *part = gsum + MT * nbm;                                             // [2 K halves][MT][128] sums
     __shared__ int hdr_ok;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -140,6 +139,7 @@ __global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams 
         hdr_ok = (h->magic == kPackedMagic && h->version == kPackedVersion && h->N == p.N && h->K == p.K &&
                   h->group == p.group && h->illegal == 0u) ? 1 : 0;
     }
+    for (int idx = threadIdx.x; idx < MT * nbm; idx += kGvThreads) gsum[idx] = 0;
     __syncthreads();
     if (!hdr_ok) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) {
@@ -152,27 +152,26 @@ __global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams 
     BlockRegs cur;
     if (wb0 < wb1) load_block(cur, tile_base + static_cast<size_t>(wb0) * bb, r, group);
     griddep_wait();
-    // This CTA's activations [M][nb * 128] into shared memory (tokens >= M read as 0).
+    // This CTA's activations [M][nb * 128] into shared memory (tokens >= M read as 0),
+    // and per (token, block) the sum of its 128 activations (the bias of the
+    // biased weight bytes), gathered with shared-memory atomics.
     const int words = nb * 32;
     for (int idx = threadIdx.x; idx < MT * words / 4; idx += kGvThreads) {
         const int m = idx / (words / 4), q = idx % (words / 4);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (m < p.M) v = __ldg(reinterpret_cast<const uint4 *>(p.Qx + static_cast<size_t>(m) * p.K + kb0 * 128) + q);
+        if (m < p.M) {
+            v = __ldg(reinterpret_cast<const uint4 *>(p.Qx + static_cast<size_t>(m) * p.K + kb0 * 128) + q);
+            if (group) {
+                const int t = __dp4a(static_cast<int>(v.x), 0x01010101,
+                                     __dp4a(static_cast<int>(v.y), 0x01010101,
+                                            __dp4a(static_cast<int>(v.z), 0x01010101,
+                                                   __dp4a(static_cast<int>(v.w), 0x01010101, 0))));
+                atomicAdd(gsum + m * nbm + q / 8, t);
+            }
+        }
         reinterpret_cast<uint4 *>(xs + m * nbm * 32)[q] = v;
     }
     __syncthreads();
-    // per (token, block): the sum of its 128 activations (the bias of the biased weight bytes)
-    if (group) {
-        for (int idx = threadIdx.x; idx < MT * nb; idx += kGvThreads) {
-            const int m = idx / nb, j = idx % nb;
-            const uint32_t *w = xs + m * nbm * 32 + j * 32;
-            int s = 0;
-#pragma unroll 8
-            for (int i = 0; i < 32; ++i) s = __dp4a(static_cast<int>(w[i]), 0x01010101, s);
-            gsum[m * nbm + j] = s;
-        }
-        __syncthreads();
-    }
 
     int acc[MT];
 #pragma unroll
@@ -210,26 +209,22 @@ __global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams 
         if (b + 1 < wb1) cur = nxt;
     }
 
-    // ---- K halves of the CTA, then the CTAs of the cluster
-    if (half) {
+    // ---- the two K halves of every CTA of the cluster publish their sums;
+    // each CTA then finishes an equal share of the tile's rows
 #pragma unroll
-        for (int m = 0; m < MT; ++m) red[m * 128 + r] = acc[m];
-    }
-    __syncthreads();
-    if (!half) {
-#pragma unroll
-        for (int m = 0; m < MT; ++m) part[m * 128 + r] = acc[m] + red[m * 128 + r];
-    }
+    for (int m = 0; m < MT; ++m) part[(half * MT + m) * 128 + r] = acc[m];
     if (p.csize > 1) cluster_sync();  // every CTA's part[] complete and visible in the cluster
     else __syncthreads();
-    // this CTA finishes rows [crank * 128 / csize, (crank + 1) * 128 / csize) of the tile
     const int rows = 128 / p.csize, row0 = static_cast<int>(crank) * rows;
     for (int idx = threadIdx.x; idx < MT * rows; idx += kGvThreads) {
         const int m = idx / rows, rr = row0 + idx % rows;
         if (m >= p.M) continue;
-        int tot = part[m * 128 + rr];
-        for (int q = 0; q < p.csize; ++q)
-            if (q != static_cast<int>(crank)) tot += ld_dsmem_s32(part + m * 128 + rr, static_cast<uint32_t>(q));
+        int tot = part[m * 128 + rr] + part[(MT + m) * 128 + rr];
+        for (int q = 0; q < p.csize; ++q) {
+            if (q == static_cast<int>(crank)) continue;
+            tot += ld_dsmem_s32(part + m * 128 + rr, static_cast<uint32_t>(q));
+            tot += ld_dsmem_s32(part + (MT + m) * 128 + rr, static_cast<uint32_t>(q));
+        }
         const int n = tile * 128 + rr;
         if (!group) tot -= static_cast<int>(p.packed[packed_z_offset(p.N, p.K) + n]) * p.t_x[m];
         const size_t idx_o = static_cast<size_t>(m) * p.N + n;
@@ -246,7 +241,7 @@ template <int MT>
 cudaError_t launch_gemv_mt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
     const int nb_max = (plan.G + plan.gv_csize - 1) / plan.gv_csize;
     const size_t smem = static_cast<size_t>(MT) * nb_max * 128 + static_cast<size_t>(MT) * nb_max * 4 +
-                        2 * static_cast<size_t>(MT) * 128 * 4;
+                        2 * static_cast<size_t>(MT) * 128 * 4;  // activations, group sums, two halves' sums
     static std::mutex mu;
     static size_t configured[kMaxDevices] = {};
     int dev = 0;

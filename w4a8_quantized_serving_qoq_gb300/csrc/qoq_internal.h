@@ -103,12 +103,14 @@ struct GemmPlan {
     size_t act_offset;     // activation operand scratch (used when the caller passes none)
     size_t zero_bytes;     // leading workspace bytes that must be zero before a launch
     int gv_csize;          // GEMV path: CTAs per cluster (K split), 1, 2, 4 or 8
+    int dp_tiles;          // tensor-core paths: tiles handed out whole, round-robin, before stream-K
 };
 
 // Kernel path, tile shape and persistent-CTA count for one GEMM.
 // force_path / force_bt / force_ctas (0 = automatic) pin the choice for tests.
+// use_table: consult the measured dispatch table before the rules.
 GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path = 0, int force_bt = 0,
-                   int force_ctas = 0);
+                   int force_ctas = 0, bool use_table = true);
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_quant_act(const uint16_t *X, int M, int K, int8_t *Qx, uint16_t *s_x,
