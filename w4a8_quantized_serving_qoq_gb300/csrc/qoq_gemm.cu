@@ -40,6 +40,7 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "qoq_gemm_common.cuh"
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool split = !(sg.k0 == 0 && sg.k1 == p.G);
                 const float sw = p.s_w ? h2f(p.s_w[n]) : 0.f;
                 const int zc = (p.group == 0) ? p.packed[packed_z_offset(p.N, p.K) + n] : 0;
-                const uint32_t tfirst = static_cast<uint32_t>(sg.tile) * static_cast<uint32_t>(p.G);
+                const uint32_t tfirst = static_cast<uint32_t>(sg.seq) * static_cast<uint32_t>(p.G);
                 const int slot_idx = split ? cta_of_stage(tfirst, p) : 0;
                 int32_t *slot = p.slots + static_cast<size_t>(slot_idx) * (BT * kTileN);
                 const int nch = (sg.k1 - sg.k0 + kChunkStages - 1) / kChunkStages;
@@ -780,6 +781,7 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     p.total = plan.total;
     p.ctas = plan.ctas;
     p.dp_tiles = plan.dp_tiles;
+    p.band = plan.band;
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
     dim3 grid(plan.ctas);
@@ -928,6 +930,15 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
     // to the CTAs round-robin (concurrent CTAs share their weight and
     // activation tiles in L2), the rest is balanced by stream-K.
     pl.dp_tiles = pl.tiles >= 2 * ctas ? static_cast<int>((pl.tiles / ctas - 1) * ctas) : 0;
+    // With several token tiles, the bands of the tile order hold about
+    // sqrt(P * BT / 32) weight tiles: a weight tile moves 64 bytes per k and an
+    // activation tile 2 BT, so this minimises the working set band * 64 +
+    // (P / band) * 2 BT bytes per k of the tiles the CTAs hold at one time.
+    pl.band = 0;
+    if (pl.tok_tiles > 1 && pl.dp_tiles > 0) {
+        int b = static_cast<int>(std::lround(std::sqrt(static_cast<double>(ctas) * bt / 32.0)));
+        pl.band = b < 1 ? 1 : (b > pl.n_tiles ? pl.n_tiles : b);
+    }
     pl.counters_offset = kWsStatusBytes;
     pl.slots_offset = kWsStatusBytes + (static_cast<size_t>(pl.ctas) * 4 + 255) / 256 * 256;
     pl.zero_bytes = pl.slots_offset + static_cast<size_t>(pl.ctas) * bt * kTileN * 4;

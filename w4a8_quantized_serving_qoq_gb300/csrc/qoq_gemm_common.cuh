@@ -28,7 +28,8 @@ struct GemmParams {
     int tok_tiles;
     long long total;        // tiles * G stages
     int ctas;
-    int dp_tiles;           // tiles [0, dp_tiles) go whole to CTAs round-robin; the rest is stream-K
+    int dp_tiles;           // work tiles [0, dp_tiles) go whole to CTAs round-robin; the rest is stream-K
+    int band;               // weight tiles per band of the tile order (0: token-tile fastest)
     uint32_t debug_flags;
     uint64_t timeout_ns;
 };
@@ -62,11 +63,28 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 // k-stages are cut into P contiguous, equal ranges; CTA c owns
 // [base + c R / P, base + (c + 1) R / P), base = dp_tiles G, R = the remaining
 // stages.  A range crosses tile boundaries; each piece inside one tile is a
-// segment.  Tiles are ordered token-tile fastest, so neighbouring work shares
-// weights.
+// segment.  Positions map to tiles through tile_at (the banded order).
 struct Segment {
-    int tile, k0, k1;
+    int seq;   // position in the work order (stage indices are seq * G + k)
+    int tile;  // the output tile: token tile tile % tok_tiles, weight tile tile / tok_tiles
+    int k0, k1;
 };
+
+// The tile at position j of the work order.  With band = 0 the order is
+// token-tile fastest (tile j).  Otherwise the weight tiles form bands of
+// `band` tiles; a band's tiles come weight-tile fastest, so P consecutive
+// positions (the tiles CTAs work on at one time) cover about band weight
+// tiles x P / band token tiles, a working set of band * (weight tile) +
+// (P / band) * (activation tile) that the planner keeps inside L2.
+__device__ __forceinline__ int tile_at(uint32_t j, const GemmParams &p) {
+    if (p.band <= 0) return static_cast<int>(j);
+    const uint32_t tt = static_cast<uint32_t>(p.tok_tiles), nt = static_cast<uint32_t>(p.N / kTileN);
+    const uint32_t bw = static_cast<uint32_t>(p.band), per_band = bw * tt;
+    const uint32_t b = j / per_band, r = j - b * per_band;
+    const uint32_t w = (b + 1) * bw <= nt ? bw : nt - b * bw;  // the last band may be narrower
+    const uint32_t tok = r / w, n = b * bw + (r - tok * w);
+    return static_cast<int>(n * tt + tok);
+}
 
 struct SegmentWalker {
     uint32_t dp_next, dp_end, dp_step;
@@ -74,7 +92,7 @@ struct SegmentWalker {
     // ctas * total < 2^32 (checked on the host), so 32-bit arithmetic is exact.
     __device__ SegmentWalker(const GemmParams &p, int cta)
         : dp_next(static_cast<uint32_t>(cta)), dp_end(static_cast<uint32_t>(p.dp_tiles)),
-          dp_step(static_cast<uint32_t>(p.ctas)), G(static_cast<uint32_t>(p.G)) {
+          dp_step(static_cast<uint32_t>(p.ctas)), G(static_cast<uint32_t>(p.G)), pp(&p) {
         const uint32_t base = static_cast<uint32_t>(p.dp_tiles) * G;
         const uint32_t R = static_cast<uint32_t>(p.total) - base;
         w = base + static_cast<uint32_t>(cta) * R / static_cast<uint32_t>(p.ctas);
@@ -82,7 +100,8 @@ struct SegmentWalker {
     }
     __device__ bool next(Segment &s) {
         if (dp_next < dp_end) {
-            s.tile = static_cast<int>(dp_next);
+            s.seq = static_cast<int>(dp_next);
+            s.tile = tile_at(dp_next, *pp);
             s.k0 = 0;
             s.k1 = static_cast<int>(G);
             dp_next += dp_step;
@@ -90,13 +109,15 @@ struct SegmentWalker {
         }
         if (w >= w1) return false;
         const uint32_t t = w / G;
-        s.tile = static_cast<int>(t);
+        s.seq = static_cast<int>(t);
+        s.tile = tile_at(t, *pp);
         s.k0 = static_cast<int>(w - t * G);
         const uint32_t end = w1 - t * G;
         s.k1 = static_cast<int>(end < G ? end : G);
         w = t * G + static_cast<uint32_t>(s.k1);
         return true;
     }
+    const GemmParams *pp;
 };
 
 // CTA whose stream-K range holds global stage `s` (s in the stream-K part:

@@ -352,10 +352,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         // drain's own decision happen, never both.
         if (lane == 0 && !(p.debug_flags & kDebugAlwaysPublish)) {
             SegmentWalker w(p, cta);
-            Segment sg, last{0, 0, 0};
+            Segment sg, last{0, 0, 0, 0};
             while (w.next(sg)) last = sg;
             const bool split = last.k1 > last.k0 && !(last.k0 == 0 && last.k1 == p.G);
-            const uint32_t tfirst = static_cast<uint32_t>(last.tile) * static_cast<uint32_t>(p.G);
+            const uint32_t tfirst = static_cast<uint32_t>(last.seq) * static_cast<uint32_t>(p.G);
             if (split && cta_of_stage(tfirst, p) == cta) {
                 griddep_wait();  // the workspace belongs to the preceding kernel until it completes
                 const uint32_t others = static_cast<uint32_t>(
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             const int m0 = tok_tile * BT, n = n_tile * kTileN + row;
             const bool split = !(sg.k0 == 0 && sg.k1 == p.G);
             const float sw = p.s_w ? h2f(p.s_w[n]) : 0.f;
-            const uint32_t tfirst = static_cast<uint32_t>(sg.tile) * static_cast<uint32_t>(p.G);
+            const uint32_t tfirst = static_cast<uint32_t>(sg.seq) * static_cast<uint32_t>(p.G);
             const int slot_idx = split ? cta_of_stage(tfirst, p) : 0;
             int32_t *slot = p.slots + static_cast<size_t>(slot_idx) * (BT * kTileN);
             named_bar_sync(2, kF8EpiThreads);
@@ -780,6 +780,7 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
     p.total = plan.total;
     p.ctas = plan.ctas;
     p.dp_tiles = plan.dp_tiles;
+    p.band = plan.band;
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
     if (a.acc_out)

@@ -104,6 +104,7 @@ struct GemmPlan {
     size_t zero_bytes;     // leading workspace bytes that must be zero before a launch
     int gv_csize;          // GEMV path: CTAs per cluster (K split), 1, 2, 4 or 8
     int dp_tiles;          // tensor-core paths: tiles handed out whole, round-robin, before stream-K
+    int band;              // weight tiles per band of the tile order (0: token-tile fastest)
 };
 
 // Kernel path, tile shape and persistent-CTA count for one GEMM.
