@@ -356,11 +356,12 @@ DISPATCH_TABLE = os.path.join(ROOT, "w4a8_quantized_serving_qoq_gb300", "csrc", 
 
 
 def gemm_candidates(M, N, K, group, sms):
-    """(path, tokens_per_tile, ctas) launch choices timed by --tune; (0, 0, 0)
-    is the planner's current automatic choice.  ctas is the CTA count (paths
-    1 and 2) or the cluster size (path 3)."""
+    """(path, tokens_per_tile, ctas, schedule) launch choices timed by --tune;
+    (0, 0, 0, 0) is the planner's current automatic choice.  ctas is the CTA
+    count (paths 1 and 2) or the cluster size (path 3); schedules 1..3 are
+    tried where there are at least two waves of tiles."""
     tiles = N // 128
-    cands = [(0, 0, 0)]
+    cands = [(0, 0, 0)]  # expanded to (path, bt, ctas, schedule) below
     if M <= 8:
         cands += [(3, 0, c) for c in (1, 2, 4, 8)]
     if group == 128 and M <= 64:
@@ -375,17 +376,25 @@ def gemm_candidates(M, N, K, group, sms):
             continue
         t = -(-M // bt) * tiles
         cands += [(1, bt, c) for c in sorted({sms} | ({t} if t <= sms else set()))]
-    return cands
+    out = []
+    for p_, b_, c_ in cands:
+        t = -(-M // max(b_, 1)) * tiles if b_ else 0
+        if p_ in (1, 2) and t >= 2 * c_:
+            out += [(p_, b_, c_, sch) for sch in (1, 2, 3)]
+        else:
+            out.append((p_, b_, c_, 0))
+    return out
 
 
 def write_dispatch_table(entries, sms):
     lines = ["// Measured launch choices of the W4A8 GEMM planner, written by",
              "// `python bench.py --tune` on a GPU (the entries apply only to GPUs with the",
              "// same SM count).  One entry per line:",
-             "//   {N, K, group, M, num_sms, path, tokens_per_tile, ctas (path 3: cluster size)},",
+             "//   {N, K, group, M, num_sms, path, tokens_per_tile, ctas (path 3: cluster size), schedule},",
              "// with the measured time of the choice and of the planner's rules."]
     for e in sorted(entries, key=lambda e: (e["N"], e["K"], e["group"], e["M"])):
-        lines.append(f"{{{e['N']}, {e['K']}, {e['group']}, {e['M']}, {sms}, {e['path']}, {e['bt']}, {e['ctas']}}},"
+        lines.append(f"{{{e['N']}, {e['K']}, {e['group']}, {e['M']}, {sms}, {e['path']}, {e['bt']}, {e['ctas']}, "
+                     f"{e['sched']}}},"
                      f"  // {e['us']:.2f} us (rules {e['rule_us']:.2f} us)")
     with open(DISPATCH_TABLE, "w") as f:
         f.write("\n".join(lines) + "\n")
@@ -440,14 +449,14 @@ def run_tune(args):
         ws = qoq.new_workspace(1 << 20, dev)
         times = {}
         for cand in gemm_candidates(M, layer.N, layer.K, group, sms):
-            path, bt, ctas = cand
+            path, bt, ctas, sched = cand
             try:
-                kind = qoq.qoq_gemm_path(M, layer.N, layer.K, group, qoq.gemm_options(kernel=path, tokens_per_tile=bt,
-                                                                                      num_ctas=ctas))
+                kind = qoq.qoq_gemm_path(M, layer.N, layer.K, group, qoq.gemm_options(
+                    kernel=path, tokens_per_tile=bt, num_ctas=ctas, schedule=sched))
             except qoq.QoqError:
                 continue
             opt = qoq.gemm_options(kernel=path, tokens_per_tile=bt, num_ctas=ctas, act_operand=acts.get(kind),
-                                   flags=qoq.QOQ_LAUNCH_OVERLAP)
+                                   flags=qoq.QOQ_LAUNCH_OVERLAP, schedule=sched)
             need = qoq.qoq_gemm_workspace_bytes(M, layer.N, layer.K, group, opt)
             if need > ws.numel():
                 ws = qoq.new_workspace(need, dev)
@@ -477,18 +486,18 @@ def run_tune(args):
             times[cand] = statistics.median(ts)
         status = qoq.qoq_workspace_status(ws)[0]
         best = min(times, key=times.get)
-        rule_us = times[(0, 0, 0)]
-        if best == (0, 0, 0):  # record what the rules chose, so the table pins it
+        rule_us = times[(0, 0, 0, 0)]
+        if best == (0, 0, 0, 0):  # record what the automatic plan chose, so the table pins it
             info = qoq.qoq_gemm_plan(M, layer.N, layer.K, group, sms)
             best_entry = (info["path"], info["tokens_per_tile"] if info["path"] != 3 else 0,
-                          info["num_ctas"] // (layer.N // 128) if info["path"] == 3 else info["num_ctas"])
+                          info["num_ctas"] // (layer.N // 128) if info["path"] == 3 else info["num_ctas"], 0)
         else:
             best_entry = best
         entries.append(dict(N=layer.N, K=layer.K, group=group, M=M, path=best_entry[0], bt=best_entry[1],
-                            ctas=best_entry[2], us=times[best], rule_us=rule_us))
+                            ctas=best_entry[2], sched=best_entry[3], us=times[best], rule_us=rule_us))
         report.append({"workload": wid, "layer": layer.name, "M": M, "best": list(best_entry),
                        "best_us": round(times[best], 2), "rule_us": round(rule_us, 2), "status": status,
-                       "candidates": {f"{p}/{b}/{c}": round(t, 2) for (p, b, c), t in times.items()}})
+                       "candidates": {"/".join(map(str, c)): round(t, 2) for c, t in times.items()}})
         print(json.dumps(report[-1]), file=sys.stderr, flush=True)
         del copies, X, acts, O
     write_dispatch_table(entries, sms)

@@ -294,6 +294,15 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  *                     of building it.  NULL = build it in the workspace.
  *   flags           : 0, QOQ_LAUNCH_OVERLAP and / or QOQ_PLAN_RULES (see
  *                     above; other bits: QOQ_ERR_UNSUPPORTED).
+ *   schedule        : order of the tensor-core paths' work, 0 = automatic;
+ *                     1 = stream-K only (each CTA one contiguous range of
+ *                     the tiles x K/128 k-stages, tiles token-tile fastest);
+ *                     2 = with two or more waves of tiles, all but the last
+ *                     one to two waves go whole to the CTAs round-robin
+ *                     (CTA c: tiles c, c + P, ...), token-tile fastest, the
+ *                     rest stream-K; 3 = as 2 with the tiles in bands of
+ *                     about sqrt(P * tokens_per_tile / 32) weight tiles,
+ *                     weight-tile fastest within a band.
  */
 typedef struct {
     int tokens_per_tile;
@@ -304,6 +313,7 @@ typedef struct {
     int kernel;
     const void *act_operand;
     uint32_t flags;
+    int schedule;
 } qoq_gemm_options;
 
 /* Workspace bytes for a GEMM run with the given options. */

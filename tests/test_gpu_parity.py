@@ -237,6 +237,28 @@ def test_gemm_tiles_and_stream_k_splits(bt, ctas, publish):
     assert qoq.qoq_workspace_status(ws)[0] == qoq.QOQ_OK
 
 
+@pytest.mark.parametrize("schedule", [1, 2, 3])
+@pytest.mark.parametrize("bt,ctas", [(32, 7), (64, 3), (128, 5), (16, 13), (32, 0)])
+@pytest.mark.parametrize("publish", [0, 2])
+def test_gemm_schedules_bit_exact(schedule, bt, ctas, publish):
+    """Stream-K only, data-parallel waves then stream-K, and the banded tile
+    order, over enough tiles for two or more waves: int32 bit-exact, the
+    workspace left zeroed, both split-tile completion routes."""
+    M, N, K = 300, 512, 1152
+    wq, Qx, sx, tx = _gemm_case(M, N, K, 78)
+    packed, sw = _device_weights(wq, 128)
+    ref = _ref_acc(wq, Qx, tx, 128)
+    acc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    opt = qoq.gemm_options(kernel=1, tokens_per_tile=bt, num_ctas=ctas, acc_out=acc, debug_flags=publish,
+                           schedule=schedule)
+    ws = qoq.new_workspace(qoq.qoq_gemm_workspace_bytes(M, N, K, 128, opt))
+    for _ in range(2):
+        acc.fill_(0)
+        qoq.qoq_w4a8_gemm_ex(_t(Qx), None, None, packed, None, N, K, 128, workspace=ws, options=opt)
+        assert np.array_equal(_np(acc), ref)
+    assert qoq.qoq_workspace_status(ws)[0] == qoq.QOQ_OK
+
+
 FP8_CASES = [(1, 256, 512), (3, 128, 384), (8, 384, 1024), (16, 256, 896), (17, 128, 640), (31, 256, 256),
              (32, 128, 1152),
              # several 32-token tiles (the planner's choice for M <= 64 when a

@@ -149,7 +149,7 @@ def test_table_entries_are_what_an_automatic_plan_gets():
     the plan of that shape on a GPU with that SM count (cluster size for the
     CUDA-core path), and of every M down to the next smaller tuned M."""
     rows = _table()
-    for N, K, group, M, sms, path, bt, ctas in rows:
+    for N, K, group, M, sms, path, bt, ctas, sched in rows:
         p = qoq.qoq_gemm_plan(M, N, K, group, sms)
         assert p["path"] == path
         if path == 3:
@@ -163,7 +163,7 @@ def test_table_entries_are_what_an_automatic_plan_gets():
 
 def test_table_applies_only_to_its_gpu_and_shapes():
     rows = _table()
-    for N, K, group, M, sms, path, bt, ctas in rows[:5]:
+    for N, K, group, M, sms, path, bt, ctas, sched in rows[:5]:
         other = qoq.qoq_gemm_plan(M, N, K, group, sms + 4)
         rules = qoq.qoq_gemm_plan(M, N, K, group, sms + 4, qoq.gemm_options(flags=qoq.QOQ_PLAN_RULES))
         assert other == rules

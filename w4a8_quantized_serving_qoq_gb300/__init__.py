@@ -44,6 +44,7 @@ class qoq_gemm_options(ctypes.Structure):
         ("kernel", ctypes.c_int),
         ("act_operand", ctypes.c_void_p),
         ("flags", ctypes.c_uint32),
+        ("schedule", ctypes.c_int),
     ]
 
 
@@ -411,10 +412,10 @@ def qoq_w4a8_gemm_i32(Qx, t_x, packed, N: int, K: int, group: int = 128, acc=Non
 
 
 def gemm_options(tokens_per_tile=0, num_ctas=0, timeout_ns=0, debug_flags=0, acc_out=None, kernel=0,
-                 act_operand=None, flags=0):
+                 act_operand=None, flags=0, schedule=0):
     return qoq_gemm_options(tokens_per_tile, num_ctas, timeout_ns, debug_flags,
                             None if acc_out is None else acc_out.data_ptr(), kernel,
-                            None if act_operand is None else act_operand.data_ptr(), flags)
+                            None if act_operand is None else act_operand.data_ptr(), flags, schedule)
 
 
 def qoq_w4a8_gemm_ex(Qx, s_x, t_x, packed, s_w, N: int, K: int, group: int = 128, O=None,

@@ -52,6 +52,7 @@ int check_options(const qoq_gemm_options *opt) {
     if (opt->num_ctas < 0 || opt->num_ctas > 65536) return QOQ_ERR_UNSUPPORTED;
     if (opt->kernel < 0 || opt->kernel > 3) return QOQ_ERR_UNSUPPORTED;
     if (opt->flags & ~(QOQ_LAUNCH_OVERLAP | QOQ_PLAN_RULES)) return QOQ_ERR_UNSUPPORTED;
+    if (opt->schedule < 0 || opt->schedule > 3) return QOQ_ERR_UNSUPPORTED;
     return QOQ_OK;
 }
 
@@ -59,7 +60,8 @@ bool plan_for(int M, int N, int K, int group, const qoq_gemm_options *opt, qoq::
     const int sms = num_sms_current_device();
     if (sms <= 0) return false;
     *out = qoq::plan_gemm(M, N, K, group, sms, opt ? opt->kernel : 0, opt ? opt->tokens_per_tile : 0,
-                          opt ? opt->num_ctas : 0, !(opt && (opt->flags & QOQ_PLAN_RULES)));
+                          opt ? opt->num_ctas : 0, !(opt && (opt->flags & QOQ_PLAN_RULES)),
+                          opt ? opt->schedule : 0);
     return true;
 }
 
@@ -264,7 +266,7 @@ int qoq_gemm_plan(int M, int N, int K, int group, int num_sms, const qoq_gemm_op
     if (st != QOQ_OK) return st;
     const qoq::GemmPlan plan = qoq::plan_gemm(M, N, K, group, num_sms, opt ? opt->kernel : 0,
                                               opt ? opt->tokens_per_tile : 0, opt ? opt->num_ctas : 0,
-                                              !(opt && (opt->flags & QOQ_PLAN_RULES)));
+                                              !(opt && (opt->flags & QOQ_PLAN_RULES)), opt ? opt->schedule : 0);
     if (!plan_valid(plan)) return QOQ_ERR_UNSUPPORTED;
     out->path = plan.path;
     out->tokens_per_tile = plan.BT;

@@ -800,11 +800,11 @@ namespace {
 // policy table, looked up at run time).  An entry covers the token counts
 // above the next smaller tuned M of the same shape, up to its own M.
 struct DispatchEntry {
-    int N, K, group, M, num_sms, path, bt, ctas;
+    int N, K, group, M, num_sms, path, bt, ctas, sched;
 };
 const DispatchEntry kDispatchTable[] = {
 #include "qoq_dispatch_table.inc"
-    {0, 0, 0, 0, 0, 0, 0, 0}  // end
+    {0, 0, 0, 0, 0, 0, 0, 0, 0}  // end
 };
 
 const DispatchEntry *find_dispatch(int M, int N, int K, int group, int num_sms) {
@@ -826,10 +826,10 @@ constexpr size_t kGemvSmemMax = 200u << 10;
 }  // namespace
 
 GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, int force_bt,
-                   int force_ctas, bool use_table) {
-    if (use_table && force_path == 0 && force_bt == 0 && force_ctas == 0) {
+                   int force_ctas, bool use_table, int force_sched) {
+    if (use_table && force_path == 0 && force_bt == 0 && force_ctas == 0 && force_sched == 0) {
         if (const DispatchEntry *e = find_dispatch(M, N, K, group, num_sms)) {
-            const GemmPlan t = plan_gemm(M, N, K, group, num_sms, e->path, e->bt, e->ctas);
+            const GemmPlan t = plan_gemm(M, N, K, group, num_sms, e->path, e->bt, e->ctas, false, e->sched);
             if (t.path == e->path) return t;  // else the rules below
         }
     }
@@ -866,6 +866,7 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
         pl.tiles = n_tiles;
         pl.total = static_cast<long long>(n_tiles) * G;
         pl.gv_csize = csize;
+        pl.sched = 0;
         pl.ctas = n_tiles * csize;
         pl.counters_offset = kWsStatusBytes;
         pl.slots_offset = kWsStatusBytes;
@@ -929,15 +930,22 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
     // At least two waves of tiles: all but the last one to two waves go whole
     // to the CTAs round-robin (concurrent CTAs share their weight and
     // activation tiles in L2), the rest is balanced by stream-K.
-    pl.dp_tiles = pl.tiles >= 2 * ctas ? static_cast<int>((pl.tiles / ctas - 1) * ctas) : 0;
-    // With several token tiles, the bands of the tile order hold about
-    // sqrt(P * BT / 32) weight tiles: a weight tile moves 64 bytes per k and an
-    // activation tile 2 BT, so this minimises the working set band * 64 +
-    // (P / band) * 2 BT bytes per k of the tiles the CTAs hold at one time.
+    // Schedule (measured per shape by the dispatch table; the rule: data-
+    // parallel waves for K up to 8192, where the DRAM traffic of the
+    // prefill shapes fell most, stream-K only for longer K).
+    int sched = force_sched > 0 ? force_sched : (K <= 8192 ? 2 : 1);
+    if (pl.tiles < 2 * ctas) sched = 1;  // fewer than two waves: stream-K only
+    pl.sched = sched;
+    pl.dp_tiles = sched >= 2 ? static_cast<int>((pl.tiles / ctas - 1) * ctas) : 0;
+    // Banded order: bands of about sqrt(P * BT / 32) weight tiles (a weight
+    // tile moves 64 bytes per k and an activation tile 2 BT, so this minimises
+    // the working set band * 64 + (P / band) * 2 BT bytes per k of the tiles
+    // the CTAs hold at one time), the bands made about equal.
     pl.band = 0;
-    if (pl.tok_tiles > 1 && pl.dp_tiles > 0) {
-        int b = static_cast<int>(std::lround(std::sqrt(static_cast<double>(ctas) * bt / 32.0)));
-        pl.band = b < 1 ? 1 : (b > pl.n_tiles ? pl.n_tiles : b);
+    if (sched == 3 && pl.tok_tiles > 1) {
+        const int b = static_cast<int>(std::lround(std::sqrt(static_cast<double>(ctas) * bt / 32.0)));
+        const int nb = (pl.n_tiles + (b < 1 ? 1 : b) - 1) / (b < 1 ? 1 : b);
+        pl.band = (pl.n_tiles + nb - 1) / nb;
     }
     pl.counters_offset = kWsStatusBytes;
     pl.slots_offset = kWsStatusBytes + (static_cast<size_t>(pl.ctas) * 4 + 255) / 256 * 256;
