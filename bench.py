@@ -57,7 +57,8 @@ BLOCKS = {
     "qwen72b": (3, "Qwen1.5-72B-shaped FFN GEMMs g128: {gate_up 59136x8192, down 8192x29568} x M in {64,1024}"),
     "per_channel": (4, "Llama-3-8B gate_up 28672x4096, per-channel W4A8 (zero folded via t_x), M = 1..4096"),
 }
-GEMM_SOURCES = ("qoq_gemm.cu", "qoq_gemm_f8.cu", "qoq_gemm_common.cuh", "qoq_device.cuh", "qoq_internal.h")
+GEMM_SOURCES = ("qoq_gemm.cu", "qoq_gemm_f8.cu", "qoq_gemv.cu", "qoq_gemm_common.cuh", "qoq_device.cuh",
+                "qoq_internal.h", "qoq_dispatch_table.inc")
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "w4a8_gemm_traffic_llama3_8b_step.md")
 
 
