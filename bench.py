@@ -88,6 +88,8 @@ def parse_args(argv=None):
                     help="time the GEMM's candidate launch choices for every shape and token count of the "
                          "workloads on this GPU, write the planner's dispatch table (csrc/qoq_dispatch_table.inc) "
                          "and print a summary instead of the benchmark line")
+    ap.add_argument("--block-ms", default="",
+                    help="comma list: time only these token counts in the qwen72b and per_channel blocks")
     ap.add_argument("--layers", default="qkv,o,gate_up,down")
     ap.add_argument("--ms", default="1,8,32,64,128,256,4096",
                     help="token counts of the headline step (4096 = the prefill workload)")
@@ -891,7 +893,8 @@ def main(argv=None):
             block_out[bname] = kv4_block()
             continue
         wid, desc = BLOCKS[bname]
-        bpts = [make_point(*p) for p in block_points(bname)]
+        keep = {int(m) for m in args.block_ms.split(",") if m}
+        bpts = [make_point(*p) for p in block_points(bname) if not keep or p[2] in keep]
         need = max(qoq.qoq_gemm_workspace_bytes(p["M"], p["layer"].N, p["layer"].K, p["group"]) for p in bpts)
         if need > ws.numel():
             ws = qoq.new_workspace(need, dev)
