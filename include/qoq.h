@@ -211,7 +211,8 @@ int qoq_rmsnorm_quant_act(const uint16_t *X, const uint16_t *gamma, float eps, i
  * activation kernel).  H [M][2F] fp16 is the gate_up projection's output,
  * gate in columns 0..F-1, up in F..2F-1.  Per element, in fp32:
  *   y[m,f] = fp16_rn((g / (1 + exp(-g))) * u),  g = H[m,f], u = H[m,F+f]
- * (expf of the CUDA math library, IEEE division and product), then exactly
+ * (the CUDA fast intrinsics __expf and __fdividef, then a product: y within
+ * 1.4e-5 relative of the exact value before its fp16 rounding), then exactly
  * qoq_quant_act_ex on the fp16 row y [F].  Y (optional) receives y [M][F].
  * Inputs must be finite with |y| < 65504.  H, Qx, Y 16-byte aligned.
  * Requirements: M, F > 0, F % 8 == 0 (F % 128 == 0 with an activation

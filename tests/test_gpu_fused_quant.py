@@ -47,7 +47,8 @@ def _gamma(K, seed):
     return (1.0 + 0.2 * np.random.default_rng(seed).standard_normal(K)).astype(np.float16)
 
 
-@pytest.mark.parametrize("M,K", [(1, 4096), (5, 1024), (16, 4096), (129, 256), (300, 14336), (3, 8), (2, 29568)])
+@pytest.mark.parametrize("M,K", [(1, 4096), (5, 1024), (16, 4096), (129, 256), (300, 14336), (3, 8), (2, 29568),
+                                 (2003, 384), (600, 4096), (297, 29568)])
 @pytest.mark.parametrize("kind", [0, 1, 2])
 def test_rmsnorm_quant_matches_oracle(M, K, kind):
     if kind and K % 128:
@@ -91,7 +92,8 @@ def _gate_up(M, F, seed):
     return np.concatenate([G, U], axis=1)
 
 
-@pytest.mark.parametrize("M,F", [(1, 14336), (7, 1024), (32, 128), (256, 14336), (300, 2048), (2, 8)])
+@pytest.mark.parametrize("M,F", [(1, 14336), (7, 1024), (32, 128), (256, 14336), (300, 2048), (2, 8),
+                                 (1999, 1024), (320, 14336), (300, 29568)])
 @pytest.mark.parametrize("kind", [0, 1, 2])
 def test_silu_mul_quant_matches_oracle(M, F, kind):
     if kind and F % 128:

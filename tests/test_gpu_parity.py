@@ -56,7 +56,8 @@ def _pack_spec(q4, s_g, z, group):
 
 
 # ------------------------------------------------------------ quantizers --
-@pytest.mark.parametrize("M,K", [(16, 512), (1, 4096), (5, 1024), (129, 256), (300, 14336)])
+@pytest.mark.parametrize("M,K", [(16, 512), (1, 4096), (5, 1024), (129, 256), (300, 14336), (2500, 256),
+                                 (1000, 4096)])
 def test_quant_act_bit_exact(M, K):
     X = synthetic.activations(M, K, 100 + M, 4)
     X[0, : min(K, 8)] = 0
@@ -83,7 +84,8 @@ def _act_operand_spec(Qx):
     return hi, lo, tg
 
 
-@pytest.mark.parametrize("M,K", [(1, 128), (3, 512), (16, 4096), (17, 1152), (300, 14336)])
+@pytest.mark.parametrize("M,K", [(1, 128), (3, 512), (16, 4096), (17, 1152), (300, 14336), (2501, 256),
+                                 (777, 4096)])
 @pytest.mark.parametrize("kind", [1, 2])
 def test_quant_act_ex_act_operand_bit_exact(M, K, kind):
     X = synthetic.activations(M, K, 300 + M, 4)
@@ -106,6 +108,7 @@ def test_quant_act_ex_act_operand_bit_exact(M, K, kind):
     assert np.array_equal(a[M * K: 2 * M * K].reshape(M, K), lo)
     got_tg = a[2 * M * K:].view(np.int32).reshape(K // 128, Mp)
     assert np.array_equal(got_tg[:, :M], tg[:, :M])
+    assert not got_tg[:, M:].any()  # padding columns zero-filled by the last row
 
 
 def test_quant_act_ties_half_even():

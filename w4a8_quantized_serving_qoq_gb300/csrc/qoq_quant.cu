@@ -13,6 +13,8 @@
 // to nearest-even (__fdiv_rn), then rounded half-to-even to an integer.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "qoq_internal.h"
 #include "qoq_device.cuh"
 
@@ -51,43 +53,71 @@ struct MaxOp { __device__ float operator()(float a, float b) const { return fmax
 struct MinOp { __device__ float operator()(float a, float b) const { return fminf(a, b); } };
 struct SumOp { __device__ int operator()(int a, int b) const { return a + b; } };
 
+// Round-to-nearest-even of t by one addition: for |t| < 2^22 the fp32 sum
+// t + 1.5 * 2^23 has unit spacing, so the addition rounds t to an integer
+// (ties to even), and the sum's bits are 0x4B400000 + rne(t): its low byte
+// is the two's-complement INT8 code.
+constexpr float kRneMagic = 12582912.0f;
+
 // Quantize eight fp16 values (one 16-byte load) with scale sf; returns the
-// eight INT8 codes as two words and adds them to *sum.
+// eight INT8 codes as two words, adds them to sum and, for kF16, also returns
+// them as fp16 (exact integers) in *f16.
 // rne(x / s) with the quotient rounded to fp32 first, as the definition
 // states, without a division per element: inv = RN(1/s) and t = RN(x * inv)
 // differ from x/s by at most 127.1 * 2^-23 < 1.6e-5, and RN(x/s) by at most
 // half an ulp of 127 (3.9e-6) more.  So t and RN(x/s) round to the same
-// integer unless t lies within 3e-5 of a half-integer; there the IEEE
-// division decides.  (|x / s| <= 127.1 because s is max|x| / 127 rounded to
-// fp16.)
-__device__ __forceinline__ int quant_one(float x, float sf, float inv) {
-    const float t = __fmul_rn(x, inv);
-    if (fabsf(__fsub_rn(__fsub_rn(t, floorf(t)), 0.5f)) < 3.0e-5f) return __float2int_rn(__fdiv_rn(x, sf));
-    return __float2int_rn(t);
-}
-
-__device__ __forceinline__ uint2 quant8(const uint4 v, float sf, float inv, int *sum) {
+// integer unless t lies within 3e-5 of a half-integer (|t - rne(t)| >
+// 0.49997); there the IEEE division decides.  Codes are clamped to
+// [-127, 127] (clamping t first gives the same codes: rne is monotone and
+// maps +-127 to themselves); s = 0 gives inv = 0 and zero codes.
+template <bool kF16>
+__device__ __forceinline__ uint2 quant8(const uint4 v, float sf, float inv, int &sum, uint4 *f16) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[2] = {0u, 0u};
+    float t[8], r[8];
+    bool tie = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const uint16_t hb = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu));
-        int q = 0;
-        if (sf != 0.f) q = clampi(quant_one(h2f(hb), sf, inv), -127, 127);
-        *sum += q;
-        out[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << ((j & 3) * 8);
+        t[j] = fminf(fmaxf(__fmul_rn(h2f(hb), inv), -127.0f), 127.0f);
+        r[j] = __fadd_rn(t[j], kRneMagic);
+        tie |= fabsf(__fsub_rn(t[j], __fsub_rn(r[j], kRneMagic))) > 0.49997f;
     }
-    return make_uint2(out[0], out[1]);
+    if (tie) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (fabsf(__fsub_rn(t[j], __fsub_rn(r[j], kRneMagic))) > 0.49997f) {
+                const uint16_t hb = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu));
+                const int q = clampi(__float2int_rn(__fdiv_rn(h2f(hb), sf)), -127, 127);
+                r[j] = __fadd_rn(static_cast<float>(q), kRneMagic);
+            }
+        }
+    }
+    uint32_t b[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) b[j] = __float_as_uint(r[j]);
+    const uint32_t q0 = __byte_perm(__byte_perm(b[0], b[1], 0x0040u), __byte_perm(b[2], b[3], 0x0040u), 0x5410u);
+    const uint32_t q1 = __byte_perm(__byte_perm(b[4], b[5], 0x0040u), __byte_perm(b[6], b[7], 0x0040u), 0x5410u);
+    sum = __dp4a(static_cast<int>(q0), 0x01010101, sum);
+    sum = __dp4a(static_cast<int>(q1), 0x01010101, sum);
+    if constexpr (kF16) {
+        uint32_t h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half2 p = __floats2half2_rn(__fsub_rn(r[2 * j], kRneMagic), __fsub_rn(r[2 * j + 1], kRneMagic));
+            h[j] = *reinterpret_cast<const uint32_t *>(&p);
+        }
+        *f16 = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    return make_uint2(q0, q1);
 }
 
+// Running max of |x| over eight fp16 values, taken on packed halves (the
+// maximum of fp16 values is exact in fp16).
 __device__ __forceinline__ float amax8(const uint4 v, float amax) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        amax = fmaxf(amax, fabsf(h2f(static_cast<uint16_t>(w[j] & 0xffffu))));
-        amax = fmaxf(amax, fabsf(h2f(static_cast<uint16_t>(w[j] >> 16))));
-    }
-    return amax;
+    const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu, v.w & 0x7fff7fffu};
+    const __half2 m = __hmax2(__hmax2(*reinterpret_cast<const __half2 *>(&w[0]), *reinterpret_cast<const __half2 *>(&w[1])),
+                              __hmax2(*reinterpret_cast<const __half2 *>(&w[2]), *reinterpret_cast<const __half2 *>(&w[3])));
+    return fmaxf(amax, fmaxf(__low2float(m), __high2float(m)));
 }
 
 // fp8-path operand bytes of eight INT8 codes (two words): u = Qx + 128
@@ -157,10 +187,14 @@ __device__ __forceinline__ uint4 norm8(const uint4 x, const uint4 g, float r) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// fp16(SiLU(g) * u) in fp32: expf (the CUDA math library's), an IEEE
-// division and product; g -> -inf gives e^-g = inf and SiLU = -0.
+// fp16(SiLU(g) * u) in fp32 with the fast intrinsics: __expf (relative
+// error below 1.3e-5 for |g| <= 90, i.e. wherever fp16 inputs give a
+// non-zero result), __fdividef (2 ulp) and a product, so y is within 1.4e-5
+// relative of the exact value before its fp16 rounding (2^-11 relative).
+// Large negative g: e^-g overflows to inf (or 1 + e^-g exceeds 2^126) and
+// SiLU(g) = -0, where the exact value rounds to zero in fp16 too.
 __device__ __forceinline__ float silu_mul1(float g, float u) {
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+    return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), u);
 }
 
 __device__ __forceinline__ uint4 silu8(const uint4 g, const uint4 u) {
@@ -174,6 +208,70 @@ __device__ __forceinline__ uint4 silu8(const uint4 g, const uint4 u) {
         o[j] = lo | (hi << 16);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The outputs of one token row m: the codes, the optional fp16 row the
+// quantizer saw, and the activation operand of kind kAct (0 none, 1 the fp16
+// copy of Qx, 2 the fp8-path planes of u = Qx + 128 and the per-group sums
+// t_g, whose padding columns M .. Mp-1 the last row also zero-fills).
+template <int kAct>
+struct RowOut {
+    uint2 *qrow;
+    uint4 *yrow;
+    uint4 *frow = nullptr;
+    uint2 *hrow = nullptr, *lrow = nullptr;
+    int32_t *tg = nullptr;
+    int pitch;
+    size_t m;
+    int M;
+    __device__ RowOut(int8_t *Qx, uint16_t *Y, uint8_t *act, size_t m_, int M_, int K)
+        : qrow(reinterpret_cast<uint2 *>(Qx + m_ * K)),
+          yrow(Y ? reinterpret_cast<uint4 *>(Y + m_ * K) : nullptr),
+          pitch(act_tg_pitch(M_)),
+          m(m_),
+          M(M_) {
+        if (kAct == 1) frow = reinterpret_cast<uint4 *>(act + 2 * m_ * K);
+        if (kAct == 2) {
+            hrow = reinterpret_cast<uint2 *>(act + m_ * K);
+            lrow = reinterpret_cast<uint2 *>(act + static_cast<size_t>(M_) * K + m_ * K);
+            tg = reinterpret_cast<int32_t *>(act + act_planes_bytes(M_, K));
+        }
+    }
+};
+
+// Quantizes and writes item i (8 values v) of the row, adding its codes to
+// tsum.  Lanes with i >= nv write nothing; for kind 2 every lane of the warp
+// must call it together (the 16 items of a 128-k group are summed by
+// half-warp shuffles, so i runs over consecutive items in each half-warp).
+template <int kAct>
+__device__ __forceinline__ void emit8(const RowOut<kAct> &o, int i, int nv, const uint4 v, float sf, float inv,
+                                      int &tsum) {
+    int part = 0;
+    uint2 q = make_uint2(0u, 0u);
+    if (i < nv) {
+        uint4 f16;
+        q = quant8<kAct == 1>(v, sf, inv, part, &f16);
+        o.qrow[i] = q;
+        if (o.yrow) o.yrow[i] = v;
+        if (kAct == 1) o.frow[i] = f16;
+    }
+    tsum += part;
+    if (kAct == 2) {
+        if (i < nv) {
+            uint2 hi, lo;
+            split_u(q, hi, lo);
+            o.hrow[i] = hi;
+            o.lrow[i] = lo;
+        }
+#pragma unroll
+        for (int s = 8; s > 0; s >>= 1) part += __shfl_xor_sync(0xffffffffu, part, s);
+        if ((threadIdx.x & 15) == 0 && i < nv) {
+            int32_t *tcol = o.tg + static_cast<size_t>(i >> 4) * o.pitch;
+            tcol[o.m] = part;
+            if (o.m + 1 == static_cast<size_t>(o.M))
+                for (int mm = o.M; mm < o.pitch; ++mm) tcol[mm] = 0;
+        }
+    }
 }
 
 // One CTA per token row.  The row is the fp16 row of the source (kSrc);
@@ -248,61 +346,104 @@ __global__ void __launch_bounds__(kSrc == kSrcX ? 1024 : 512) quant_act_kernel(c
     const float sf = h2f(sbits);
     const float inv = sf != 0.f ? __frcp_rn(sf) : 0.f;
 
-    uint2 *qrow = reinterpret_cast<uint2 *>(Qx + m * K);
-    uint4 *yrow = (kSrc != kSrcX && src.Y) ? reinterpret_cast<uint4 *>(src.Y + m * K) : nullptr;
-    uint2 *hrow = nullptr, *lrow = nullptr;
-    uint4 *frow = nullptr;
-    int32_t *tg = nullptr;
-    const int pitch = act_tg_pitch(M);
-    if (kAct == 1) frow = reinterpret_cast<uint4 *>(act + 2 * m * K);
-    if (kAct == 2) {
-        hrow = reinterpret_cast<uint2 *>(act + m * K);
-        lrow = reinterpret_cast<uint2 *>(act + static_cast<size_t>(M) * K + m * K);
-        tg = reinterpret_cast<int32_t *>(act + act_planes_bytes(M, K));
-    }
+    const RowOut<kAct> out(Qx, kSrc != kSrcX ? src.Y : nullptr, act, m, M, K);
     int tsum = 0;
-    auto emit = [&](int i, const uint4 v) {
-        int part = 0;
-        uint2 q = make_uint2(0u, 0u);
-        if (i < nv) {
-            q = quant8(v, sf, inv, &part);
-            qrow[i] = q;
-            if (yrow) yrow[i] = v;
-        }
-        tsum += part;
-        if (kAct == 1 && i < nv) {
-            const uint2 a = int8x4_to_f16x4(q.x), b = int8x4_to_f16x4(q.y);
-            frow[i] = make_uint4(a.x, a.y, b.x, b.y);
-        }
-        if (kAct == 2) {
-            if (i < nv) {
-                uint2 hi, lo;
-                split_u(q, hi, lo);
-                hrow[i] = hi;
-                lrow[i] = lo;
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if ((tid & 15) == 0 && i < nv) {
-                int32_t *tcol = tg + static_cast<size_t>(i >> 4) * pitch;
-                tcol[m] = part;
-                if (m + 1 == static_cast<size_t>(M))
-                    for (int mm = M; mm < pitch; ++mm) tcol[mm] = 0;
-            }
-        }
-    };
 #pragma unroll
     for (int j = 0; j < kActCache; ++j)
-        if (j * bd < nv) emit(tid + j * bd, cache[j]);
+        if (j * bd < nv) emit8(out, tid + j * bd, nv, cache[j], sf, inv, tsum);
     for (int base = kActCache * bd; base < nv; base += bd) {
         const int i = base + tid;
-        emit(i, i < nv ? item(i) : make_uint4(0u, 0u, 0u, 0u));
+        emit8(out, i, nv, i < nv ? item(i) : make_uint4(0u, 0u, 0u, 0u), sf, inv, tsum);
     }
     if (t_x) tsum = block_reduce(tsum, SumOp(), shi, 0);  // t_x is uniform across the CTA
     if (tid == 0) {
         s_x[m] = sbits;
         if (t_x) t_x[m] = tsum;
     }
+}
+
+// The same quantizer for many rows (bandwidth-bound sizes): persistent CTAs
+// take rows blockIdx.x, blockIdx.x + gridDim.x, ... and stream them through
+// a ring of kRing row buffers in shared memory with 16-byte asynchronous
+// copies, kRing - 1 rows ahead of the one being quantized, so each SM keeps
+// several rows in flight with few registers.  The row is then read from
+// shared memory only: the norm / activation values overwrite the source in
+// place after the pass that computes them (with the max), and the last pass
+// quantizes them.  gamma (kSrcRmsNorm) is staged once per CTA.  Arithmetic,
+// rounding and outputs are those of quant_act_kernel.  Every loop's trip
+// count is uniform across the CTA, as the group-sum shuffles require.
+template <int kAct, int kSrc, int kRing, int kT>
+__global__ void __launch_bounds__(kT) quant_rows_kernel(const RowSrc src, int M, int K, int8_t *__restrict__ Qx,
+                                                        uint16_t *__restrict__ s_x, int32_t *__restrict__ t_x,
+                                                        uint8_t *__restrict__ act) {
+    extern __shared__ uint4 rows_smem[];
+    __shared__ float shf[32];
+    __shared__ int shi[32];
+    const int nv = K >> 3;                                  // 16-byte items (8 values) of a row
+    const int items = kSrc == kSrcSiluMul ? 2 * nv : nv;    // source items per row ([G | U] for SiLU-mul)
+    const int tid = threadIdx.x;
+    // Rows of this CTA (the grid is at most M wide).
+    const int rows = (M - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1;
+    uint4 *gam = rows_smem;                                      // [nv] (kSrcRmsNorm)
+    uint4 *ring = rows_smem + (kSrc == kSrcRmsNorm ? nv : 0);   // kRing x [items]
+    const uint4 *srcv = reinterpret_cast<const uint4 *>(src.X);
+    if (tid == 0) griddep_launch_dependents();
+    griddep_wait();  // the source rows may be written by the preceding kernel
+    auto issue = [&](int t) {
+        if (t < rows) {
+            const size_t m = blockIdx.x + static_cast<size_t>(t) * gridDim.x;
+            const uint4 *row = srcv + m * items;
+            const uint32_t dst = smem_u32(ring + static_cast<size_t>(t % kRing) * items);
+            for (int i = tid; i < items; i += kT) cp_async16(dst + 16u * i, row + i);
+        }
+        cp_async_commit();  // possibly empty: every thread commits one group per row index
+    };
+    if constexpr (kSrc == kSrcRmsNorm) {
+        const uint4 *g = reinterpret_cast<const uint4 *>(src.gamma);
+        for (int i = tid; i < nv; i += kT) cp_async16(smem_u32(gam + i), g + i);  // joins row 0's group
+    }
+#pragma unroll
+    for (int t = 0; t < kRing - 1; ++t) issue(t);
+    for (int t = 0; t < rows; ++t) {
+        issue(t + kRing - 1);
+        cp_async_wait<kRing - 1>();  // this thread's copies of row t have landed
+        __syncthreads();             // ... and every other thread's
+        const size_t m = blockIdx.x + static_cast<size_t>(t) * gridDim.x;
+        uint4 *buf = ring + static_cast<size_t>(t % kRing) * items;
+        float r = 0.f;
+        if constexpr (kSrc == kSrcRmsNorm) {
+            float ss = 0.f;
+            for (int i = tid; i < nv; i += kT) ss = sumsq8(buf[i], ss);
+            ss = block_reduce(ss, AddF(), shf, 0.f);
+            const float v = __fadd_rn(__fdiv_rn(ss, static_cast<float>(K)), src.eps);
+            r = v > 0.f ? __frsqrt_rn(v) : 0.f;
+        }
+        float amax = 0.f;
+        for (int i = tid; i < nv; i += kT) {
+            uint4 y = buf[i];
+            if constexpr (kSrc == kSrcRmsNorm) y = norm8(y, gam[i], r);
+            if constexpr (kSrc == kSrcSiluMul) y = silu8(y, buf[nv + i]);
+            if constexpr (kSrc != kSrcX) buf[i] = y;  // this thread's own item, read back below
+            amax = amax8(y, amax);
+        }
+        amax = block_reduce(amax, MaxOp(), shf, 0.f);
+        const uint16_t sbits = f2h_rn(__fdiv_rn(amax, 127.0f));
+        const float sf = h2f(sbits);
+        const float inv = sf != 0.f ? __frcp_rn(sf) : 0.f;
+        const RowOut<kAct> out(Qx, kSrc != kSrcX ? src.Y : nullptr, act, m, M, K);
+        int tsum = 0;
+        for (int base = 0; base < nv; base += kT) {
+            const int i = base + tid;
+            emit8(out, i, nv, i < nv ? buf[i] : make_uint4(0u, 0u, 0u, 0u), sf, inv, tsum);
+        }
+        if (t_x) tsum = block_reduce(tsum, SumOp(), shi, 0);
+        if (tid == 0) {
+            s_x[m] = sbits;
+            if (t_x) t_x[m] = tsum;
+        }
+        __syncthreads();  // buffer t % kRing is refilled by the next iteration's copies
+    }
+    cp_async_wait<0>();
 }
 
 // fp16-path activation operand from INT8 activations: 8 codes per thread
@@ -429,9 +570,71 @@ __global__ void quantize_channel_kernel(const uint16_t *__restrict__ W, int K,
 }  // namespace
 
 namespace {
+// Launch of the row-streaming quantizer: 256 threads and kRing = 4 row
+// buffers for rows of up to 16 KB, else 512 threads and 2 buffers (enough
+// warps per SM for the arithmetic); as many CTAs as fit on the GPU (at most
+// M).  Returns false (nothing launched) when not even one CTA fits in shared
+// memory.
+template <int kAct, int kSrc, int kRing, int kT>
+bool launch_rows_ring(const RowSrc &src, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x, uint8_t *act,
+                      bool pdl, cudaStream_t stream, cudaError_t *err) {
+    auto kern = quant_rows_kernel<kAct, kSrc, kRing, kT>;
+    const size_t nv = static_cast<size_t>(K) / 8;
+    const size_t items = kSrc == kSrcSiluMul ? 2 * nv : nv;
+    const size_t smem = 16 * ((kSrc == kSrcRmsNorm ? nv : 0) + kRing * items);
+    constexpr size_t kMaxDyn = 232448 - 1024;  // the per-block opt-in limit less room for the static arrays
+    if (smem > kMaxDyn) return false;
+    static std::mutex mu;
+    static bool configured[kMaxDevices] = {};
+    static int sms[kMaxDevices] = {};
+    int dev = 0;
+    if ((*err = cudaGetDevice(&dev)) != cudaSuccess) return true;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return true;
+    }
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!configured[dev]) {
+            if ((*err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxDyn))) != cudaSuccess ||
+                (*err = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+                return true;
+            configured[dev] = true;
+        }
+    }
+    int per_sm = 0;
+    if ((*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kT, smem)) != cudaSuccess) return true;
+    if (per_sm < 1) return false;
+    const long long ctas = static_cast<long long>(sms[dev]) * per_sm;
+    const dim3 grid(static_cast<unsigned>(ctas < M ? ctas : M)), block(kT);
+    *err = launch_kernel(kern, grid, block, smem, stream, pdl, src, M, K, Qx, s_x, t_x, act);
+    return true;
+}
+
+template <int kAct, int kSrc>
+bool launch_rows(const RowSrc &src, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x, uint8_t *act,
+                 bool pdl, cudaStream_t stream, cudaError_t *err) {
+    const size_t row_bytes = static_cast<size_t>(K) * (kSrc == kSrcSiluMul ? 4 : 2);
+    if (row_bytes <= 16384)
+        return launch_rows_ring<kAct, kSrc, 4, 256>(src, M, K, Qx, s_x, t_x, act, pdl, stream, err);
+    return launch_rows_ring<kAct, kSrc, 2, 512>(src, M, K, Qx, s_x, t_x, act, pdl, stream, err);
+}
+
+// Rows at which the row-streaming kernel takes over (about two rows per SM).
+constexpr int kRowsKernelMinM = 296;
+
 template <int kSrc>
 cudaError_t launch_quant_src(const RowSrc &src, int M, int K, int8_t *Qx, uint16_t *s_x, int32_t *t_x,
                              int act_kind, uint8_t *act, bool pdl, cudaStream_t stream) {
+    if (!act) act_kind = 0;
+    if (M >= kRowsKernelMinM) {
+        cudaError_t e = cudaSuccess;
+        bool done;
+        if (act_kind == 1) done = launch_rows<1, kSrc>(src, M, K, Qx, s_x, t_x, act, pdl, stream, &e);
+        else if (act_kind == 2) done = launch_rows<2, kSrc>(src, M, K, Qx, s_x, t_x, act, pdl, stream, &e);
+        else done = launch_rows<0, kSrc>(src, M, K, Qx, s_x, t_x, nullptr, pdl, stream, &e);
+        if (done) return e;
+    }
     // One CTA per row; about two 16-byte items per thread keeps the per-row
     // latency short (few rows) without idle warps; many rows: 256 threads.
     const int nv = K / 8;
@@ -440,7 +643,6 @@ cudaError_t launch_quant_src(const RowSrc &src, int M, int K, int8_t *Qx, uint16
     threads = threads < 128 ? 128 : (threads > max_threads ? max_threads : threads);
     if (M >= 296) threads = 256;
     const dim3 grid(M), block(threads);
-    if (!act) act_kind = 0;
     if (act_kind == 1)
         return launch_kernel(quant_act_kernel<1, kSrc>, grid, block, 0, stream, pdl, src, M, K, Qx, s_x, t_x, act);
     if (act_kind == 2)
