@@ -28,12 +28,14 @@
 //      sum_t p_t Vhat_t = sum_t (p_t s_t) c_t - sum_t p_t s_t z_t,
 //    so no multiply per cached element;
 //  * QK^T and PV are warp-level mma.sync m16n8k16 (fp16 in, fp32 out).  The
-//    scores are computed transposed, the G query heads that share a KV head
-//    (grouped-query attention) as rows, twice, so that the score fragment of
-//    a lane is already its B fragment for PV: the weights p_t s_t enter PV
-//    as an fp16 pair hi + lo (hi = fp16(x), lo = fp16(x - hi)), hi through
-//    the first copy of the rows and lo through the second, so the fp16
-//    operand loses no accuracy against fp32;
+//    scores are computed as S^T with 16 tokens as rows (the K codes are the
+//    A operand) and the G query heads that share a KV head (grouped-query
+//    attention) as the 8 columns, each head twice for G <= 4; one movmatrix
+//    transpose per 8 x 8 half turns the weight tile into PV's B fragment.
+//    The weights p_t s_t enter PV as an fp16 pair hi + lo (hi = fp16(x), lo
+//    = fp16(x - hi)), hi through the first copy of the columns and lo
+//    through the second (G = 8: two PV n-tiles), so the fp16 operand loses
+//    no accuracy against fp32;
 //  * online softmax in fp32 per warp, rescaling the accumulators only when
 //    the running maximum grows by more than 2^8; the warps' states are
 //    merged in shared memory; with several splits per sequence the partial
@@ -170,19 +172,20 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8 x 8 matrix of 16-bit elements held as the warp's m8n8
+// fragments (lane l holds row l / 4, columns 2 (l % 4) and + 1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // 2^x for x <= 0 (the hardware approximation; relative error about 2^-22,
 // results below 2^-126 flush to zero, which a softmax weight can afford).
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// An fp16 pair (hi, lo) with hi + lo = x to about 2^-22 relative.
-__device__ __forceinline__ void split_f16(float x, uint16_t &hi, uint16_t &lo) {
-    const __half h = __float2half_rn(x);
-    hi = __half_as_ushort(h);
-    lo = f2h_rn(__fsub_rn(x, __half2float(h)));
 }
 
 // Four-bit codes enter the tensor core as fp16 subnormals: a nibble c in
@@ -195,7 +198,7 @@ constexpr float kF1 = 16777216.0f;   // 2^24
 constexpr float kF16 = 1048576.0f;   // 2^20
 
 template <int NSV>  // PV n-tiles: 1 for G <= 4, 2 for G = 8
-__global__ void __launch_bounds__(kThreads) kv4_attention_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kThreads, NSV == 1 ? 4 : 3) kv4_attention_kernel(const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     uint64_t *full = reinterpret_cast<uint64_t *>(ring + kStages * kChunkBytes);
@@ -253,39 +256,52 @@ __global__ void __launch_bounds__(kThreads) kv4_attention_kernel(const AttnParam
     // ---------------------------------------------------- consumer warps --
     // Fragment coordinates of m16n8k16: quad row g4 = lane / 4, column pair r.
     const int g4 = lane >> 2, r = lane & 3;
-    // S^T = Q Khat^T with the query heads as rows: row rho < 2G holds head
-    // rho mod G (the second copy feeds the lo half of the PV weights), the
-    // other rows are zero.  This lane's score rows: g4 (and g4 + 8).
-    const bool row_ok = g4 < 2 * G;
-    const int my_head = row_ok ? g4 % G : 0;
-    uint32_t qa[8][4];
+    // Columns of the score tile S^T [16 tokens][8]: for G <= 4, column c <
+    // 2G holds query head c mod G (the copy at c >= G feeds the lo half of
+    // the PV weights), the others are zero; for G = 8 column c is head c.
+    // B operand of QK^T (Q^T, k = dims, n = columns): this lane's column is
+    // g4; its two registers per 16-dim k-chunk j are dims 16 j + 2r (+1) and
+    // 16 j + 2r + 8 (+9).
+    const int ncols = NSV == 2 ? 8 : 2 * G;
+    uint32_t qb[8][2];
     float qsum = 0.f;
     {
-        const uint16_t *qr0 = p.Q + (static_cast<size_t>(b) * p.hq + h * G + my_head) * kHD;
-        const bool ok8 = g4 + 8 < 2 * G;
-        const uint16_t *qr8 = p.Q + (static_cast<size_t>(b) * p.hq + h * G + (ok8 ? (g4 + 8) % G : 0)) * kHD;
+        const bool ok = g4 < ncols;
+        const uint16_t *qr = p.Q + (static_cast<size_t>(b) * p.hq + h * G + (ok ? g4 % G : 0)) * kHD;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const uint32_t x0 = row_ok ? *reinterpret_cast<const uint32_t *>(qr0 + 16 * j + 2 * r) : 0u;
-            const uint32_t x1 = row_ok ? *reinterpret_cast<const uint32_t *>(qr0 + 16 * j + 2 * r + 8) : 0u;
-            qa[j][0] = x0;
-            qa[j][1] = ok8 ? *reinterpret_cast<const uint32_t *>(qr8 + 16 * j + 2 * r) : 0u;
-            qa[j][2] = x1;
-            qa[j][3] = ok8 ? *reinterpret_cast<const uint32_t *>(qr8 + 16 * j + 2 * r + 8) : 0u;
+            const uint32_t x0 = ok ? *reinterpret_cast<const uint32_t *>(qr + 16 * j + 2 * r) : 0u;
+            const uint32_t x1 = ok ? *reinterpret_cast<const uint32_t *>(qr + 16 * j + 2 * r + 8) : 0u;
+            qb[j][0] = x0;
+            qb[j][1] = x1;
             qsum += h2f(static_cast<uint16_t>(x0 & 0xffffu)) + h2f(static_cast<uint16_t>(x0 >> 16)) +
                     h2f(static_cast<uint16_t>(x1 & 0xffffu)) + h2f(static_cast<uint16_t>(x1 >> 16));
         }
     }
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
-    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);  // sum(q) of this lane's head
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);  // sum(q) of column g4's head
+    // This lane's score / PV columns: c = 2r + e, e = 0, 1.
+    bool col_ok[2], col_hi[2];
+    float qs[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int c = 2 * r + e;
+        col_ok[e] = c < ncols;
+        col_hi[e] = NSV == 2 || c < G;  // G = 8: both halves of every column (n-tiles 0 and 1)
+        qs[e] = __shfl_sync(0xffffffffu, qsum, 4 * c);
+    }
 
-    // Softmax state of this lane's head, over its own tokens; the maximum
-    // m_used is uniform over the quad.  The exponentials use m_used, which is
-    // raised only when a tile's maximum exceeds it by more than 2^8 (weights
-    // up to 256 are harmless in fp32 / fp16), so the PV accumulators are
-    // rescaled rarely.
+    // Softmax state of this lane's two columns, over its own tokens; the
+    // reference maximum m_ref is uniform over the eight lanes of a column.
+    // The exponentials use m_ref, which is raised only when a tile's maximum
+    // exceeds it by more than 2^8 (m_plus = m_ref + 8, or -inf before the
+    // column's first score; weights up to 256 are harmless in fp32 / fp16),
+    // so the PV accumulators are rescaled rarely.
     constexpr float kSlack = 8.0f;
-    float m_used = -INFINITY, l_part = 0.f, c_part = 0.f;
+    float m_ref[2] = {0.f, 0.f}, m_plus[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f}, c_part[2] = {0.f, 0.f};
+    // Bytes of the packed PV weight pair (G <= 4): for each of the lane's
+    // columns the hi half (from the first operand) or the lo half.
+    const uint32_t half_sel = (col_hi[0] ? 0x0010u : 0x0054u) | (col_hi[1] ? 0x3200u : 0x7600u);
     float acc[NSV][8][4];
 #pragma unroll
     for (int n = 0; n < NSV; ++n)
@@ -300,85 +316,109 @@ __global__ void __launch_bounds__(kThreads) kv4_attention_kernel(const AttnParam
         if (!mbar_wait_warp(&full[s], use & 1, abort_flag, p.status, p.timeout_ns)) break;
         const uint8_t *ck = ring + s * kChunkBytes;
         const int tok0 = (pg0 + i) * kPageTok + tile0;
-        // ---- S^T: rows = heads, columns = tokens tile0 + 8 nt + {2r, 2r+1}
-        // (n-tile nt); even k-chunks hold codes at factor 2^-24, odd ones at 2^-20
-        float se[2][4], so[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) se[nt][e] = so[nt][e] = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const uint4 kv = *reinterpret_cast<const uint4 *>(ck + (tile0 + 8 * nt + g4) * 64 + 16 * r);
-            const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+        // ---- S^T: rows = tokens tile0 + g4 (+8), columns as above.  A
+        // fragment of k-word jj: the 16-byte K chunk r of the two tokens;
+        // even k-chunks hold codes at factor 2^-24 (mask kLo), odd ones at
+        // 2^-20 (mask kHi).
+        float se[4] = {0.f, 0.f, 0.f, 0.f}, so[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const uint4 k0 = *reinterpret_cast<const uint4 *>(ck + (tile0 + g4) * 64 + 16 * r);
+            const uint4 k8 = *reinterpret_cast<const uint4 *>(ck + (tile0 + 8 + g4) * 64 + 16 * r);
+            const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w}, w8[4] = {k8.x, k8.y, k8.z, k8.w};
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
-                const uint32_t w8 = kw[jj] >> 8;
-                mma16816(se[nt], qa[2 * jj], kw[jj] & kLo, w8 & kLo);
-                mma16816(so[nt], qa[2 * jj + 1], kw[jj] & kHi, w8 & kHi);
+                const uint32_t s0 = w0[jj] >> 8, s8 = w8[jj] >> 8;
+                const uint32_t alo[4] = {w0[jj] & kLo, w8[jj] & kLo, s0 & kLo, s8 & kLo};
+                const uint32_t ahi[4] = {w0[jj] & kHi, w8[jj] & kHi, s0 & kHi, s8 & kHi};
+                mma16816(se, alo, qb[2 * jj][0], qb[2 * jj][1]);
+                mma16816(so, ahi, qb[2 * jj + 1][0], qb[2 * jj + 1][1]);
             }
         }
-        // K scale and zero of the lane's four tokens 8 nt + 2r + e
-        const uint2 km0 = *reinterpret_cast<const uint2 *>(ck + kCodesBytes + 4 * (tile0 + 2 * r));
-        const uint2 km1 = *reinterpret_cast<const uint2 *>(ck + kCodesBytes + 4 * (tile0 + 8 + 2 * r));
-        const uint32_t kmw[4] = {km0.x, km0.y, km1.x, km1.y};
+        // Per token (g4 and g4 + 8 of the tile): in range?  Score factors
+        // a = 2^24 ks scale and b = kz ks scale (so x = (se + so / 16) a -
+        // b sum(q)), and the V scale / zero, zeroed out of range (unwritten
+        // slots may hold any bits: select, never multiply, their values).
+        // Score value v is token g4 + 8 (v >> 1), column 2r + (v & 1).
+        float ka[2], kb[2], vsc[2], vzc[2];
+        bool tin[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint32_t km = *reinterpret_cast<const uint32_t *>(ck + kCodesBytes + 4 * (tile0 + 8 * t + g4));
+            const uint32_t vm = *reinterpret_cast<const uint32_t *>(ck + kVOff + kCodesBytes + 4 * (tile0 + 8 * t + g4));
+            tin[t] = tok0 + g4 + 8 * t < L;
+            const float kss = __fmul_rn(h2f(static_cast<uint16_t>(km & 0xffffu)), p.scale_log2);
+            ka[t] = __fmul_rn(kss, kF1);
+            kb[t] = __fmul_rn(h2f(static_cast<uint16_t>(km >> 16)), kss);
+            vsc[t] = tin[t] ? h2f(static_cast<uint16_t>(vm & 0xffffu)) : 0.f;
+            vzc[t] = tin[t] ? h2f(static_cast<uint16_t>(vm >> 16)) : 0.f;
+        }
         float x[4];
-        float tmax = -INFINITY;
+        bool raise = false;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int nt = t >> 1, e = t & 1;
-            const float dot = __fmaf_rn(se[nt][e], kF1, __fmul_rn(so[nt][e], kF16));  // q . c_t
-            const float ks = h2f(static_cast<uint16_t>(kmw[t] & 0xffffu)), kz = h2f(static_cast<uint16_t>(kmw[t] >> 16));
-            const bool in = row_ok && tok0 + 8 * nt + 2 * r + e < L;
-            x[t] = in ? __fmul_rn(__fmul_rn(__fsub_rn(dot, __fmul_rn(kz, qsum)), ks), p.scale_log2) : -INFINITY;
-            tmax = fmaxf(tmax, x[t]);
+        for (int v = 0; v < 4; ++v) {
+            const int t = v >> 1, e = v & 1;
+            const float xs = __fmaf_rn(__fmaf_rn(so[v], 0.0625f, se[v]), ka[t], -__fmul_rn(kb[t], qs[e]));
+            x[v] = tin[t] && col_ok[e] ? xs : -INFINITY;
+            raise |= x[v] > m_plus[e];  // m_plus = -inf until the column has a score
         }
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-        const bool raise = tmax > m_used + kSlack || (m_used == -INFINITY && tmax != -INFINITY);
         if (__any_sync(0xffffffffu, raise)) {
-            const float m_new = raise ? tmax : m_used;
-            const float alpha = (m_used == -INFINITY || !raise) ? (m_used == -INFINITY ? 0.f : 1.f) : ex2(m_used - m_new);
-            m_used = m_new;
-            l_part *= alpha;
-            c_part *= alpha;
-            // PV column c (of either n-tile) belongs to the head of score row c
-            const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * r);
-            const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * r + 4);
+            // column maxima of the tile over the eight lanes of each column
 #pragma unroll
-            for (int n = 0; n < NSV; ++n)
+            for (int e = 0; e < 2; ++e) {
+                float tmax = fmaxf(x[e], x[2 + e]);
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+                if (tmax > m_plus[e]) {
+                    const float alpha = m_plus[e] == -INFINITY ? 0.f : ex2(m_ref[e] - tmax);
+                    m_ref[e] = tmax;
+                    m_plus[e] = tmax + kSlack;
+                    l_part[e] *= alpha;
+                    c_part[e] *= alpha;
+                    // PV column 2r + e is this lane's column e in every n-tile
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    acc[n][mt][0] *= a0;
-                    acc[n][mt][1] *= a1;
-                    acc[n][mt][2] *= a0;
-                    acc[n][mt][3] *= a1;
+                    for (int n = 0; n < NSV; ++n)
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            acc[n][mt][e] *= alpha;
+                            acc[n][mt][2 + e] *= alpha;
+                        }
                 }
+            }
         }
-        // weights w_t = p_t * s_t of the V scale and the zero correction
-        const uint2 vm0 = *reinterpret_cast<const uint2 *>(ck + kVOff + kCodesBytes + 4 * (tile0 + 2 * r));
-        const uint2 vm1 = *reinterpret_cast<const uint2 *>(ck + kVOff + kCodesBytes + 4 * (tile0 + 8 + 2 * r));
-        const uint32_t vmw[4] = {vm0.x, vm0.y, vm1.x, vm1.y};
-        uint16_t whi[4], wlo[4];
+        // weights w = p_t * s_t of the V scale and the zero correction, as
+        // an fp16 pair hi + lo; the PV weight of column c is hi (c < G) or
+        // lo (a copy column) for G <= 4, both (n-tiles 0 and 1) for G = 8.
+        // p = 2^(x - m_ref) is 0 for masked scores (x = -inf, m_ref finite).
+        uint32_t pw[NSV][2];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            // masked tokens may sit in never-written slots: select, never multiply, their scales
-            const float pt = x[t] == -INFINITY ? 0.f : ex2(__fsub_rn(x[t], m_used));
-            const float vs = h2f(static_cast<uint16_t>(vmw[t] & 0xffffu)), vz = h2f(static_cast<uint16_t>(vmw[t] >> 16));
-            const float w = pt != 0.f ? __fmul_rn(pt, vs) : 0.f;
-            l_part += pt;
-            c_part = w != 0.f ? __fmaf_rn(w, vz, c_part) : c_part;
-            split_f16(w, whi[t], wlo[t]);
+        for (int t = 0; t < 2; ++t) {
+            float w[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float pt = ex2(__fsub_rn(x[2 * t + e], m_ref[e]));
+                w[e] = __fmul_rn(pt, vsc[t]);
+                l_part[e] += pt;
+                c_part[e] = __fmaf_rn(w[e], vzc[t], c_part[e]);
+            }
+            const __half2 hi = __floats2half2_rn(w[0], w[1]);
+            const float2 hf = __half22float2(hi);
+            const __half2 lo = __floats2half2_rn(__fsub_rn(w[0], hf.x), __fsub_rn(w[1], hf.y));
+            const uint32_t hw = *reinterpret_cast<const uint32_t *>(&hi), lw = *reinterpret_cast<const uint32_t *>(&lo);
+            if (NSV == 2) {
+                pw[0][t] = hw;
+                pw[NSV - 1][t] = lw;
+            } else {
+                pw[0][t] = __byte_perm(hw, lw, half_sel);
+            }
         }
-        // PV B fragment, column g4 (n-tile n): hi part of head g4 for g4 < G,
-        // lo part for G <= g4 < 2G (G <= 4); for G = 8 n-tile 0 is hi, 1 is lo
+        // PV B fragment (k = tokens, n = columns) by transposing the two
+        // 8 x 8 halves of the weight tile
         uint32_t pb[NSV][2];
 #pragma unroll
         for (int n = 0; n < NSV; ++n) {
-            const bool hi_part = NSV == 2 ? n == 0 : g4 < G;
-            const uint16_t *src = hi_part ? whi : wlo;
-            pb[n][0] = row_ok ? (static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 16)) : 0u;
-            pb[n][1] = row_ok ? (static_cast<uint32_t>(src[2]) | (static_cast<uint32_t>(src[3]) << 16)) : 0u;
+            pb[n][0] = movmatrix_trans(pw[n][0]);
+            pb[n][1] = movmatrix_trans(pw[n][1]);
         }
         // ---- O^T += Vc^T W: rows = dims g4 + 8 nt' of the V group g4, k = tokens
         const uint8_t *cv = ck + kVOff + 8 * g4;
@@ -413,11 +453,14 @@ __global__ void __launch_bounds__(kThreads) kv4_attention_kernel(const AttnParam
         }
     }
 
-    // ---- the lane's partial sums over its tokens, summed over the quad
-    l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
-    l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
-    c_part += __shfl_xor_sync(0xffffffffu, c_part, 1);
-    c_part += __shfl_xor_sync(0xffffffffu, c_part, 2);
+    // ---- the lane's partial sums over its tokens, summed over its column's lanes
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l_part[e] += __shfl_xor_sync(0xffffffffu, l_part[e], o);
+            c_part[e] += __shfl_xor_sync(0xffffffffu, c_part[e], o);
+        }
 
     // ---- merge the four warps' states in shared memory (the ring is free
     // once every consumer passed its last page; the producer waits only for
@@ -427,14 +470,14 @@ __global__ void __launch_bounds__(kThreads) kv4_attention_kernel(const AttnParam
     const int stride = 2 + kHD + 1;
     // accumulator rows: m-tile mt covers nibbles nt = 2 mt (dims g4 + 16 mt,
     // factor 2^-24) and nt = 2 mt + 1 (dims g4 + 8 + 16 mt, factor 2^-20);
-    // columns 8 n + 2r + e
+    // columns 2r + e
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
 #pragma unroll
         for (int n = 0; n < NSV; ++n)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int col = (NSV == 2 ? 0 : 0) + 2 * r + e;
+                const int col = 2 * r + e;
                 const bool hi_col = NSV == 2 ? n == 0 : col < G;
                 const bool lo_col = NSV == 2 ? n == 1 : (col >= G && col < 2 * G);
                 if (pass == 0 ? !hi_col : !lo_col) continue;
@@ -455,11 +498,17 @@ __global__ void __launch_bounds__(kThreads) kv4_attention_kernel(const AttnParam
             }
         named_bar_sync_kv(1, 32 * kConsumerWarps);
     }
-    if (r == 0 && g4 < G) {
-        float *dst = mrg + (warp * G + g4) * stride;
-        dst[0] = m_used;
-        dst[1] = l_part;
-        dst[2 + kHD] = c_part;
+    if (g4 == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int col = 2 * r + e;
+            if (col < G) {
+                float *dst = mrg + (warp * G + col) * stride;
+                dst[0] = m_plus[e] == -INFINITY ? -INFINITY : m_ref[e];  // -inf: no score in this warp
+                dst[1] = l_part[e];
+                dst[2 + kHD] = c_part[e];
+            }
+        }
     }
     named_bar_sync_kv(1, 32 * kConsumerWarps);
     // one consumer thread per (head, dim) pair of the output
@@ -524,6 +573,11 @@ cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
             e = cudaFuncSetAttribute(kv4_attention_kernel<NSV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kAttnSmem));
             if (e != cudaSuccess) return e;
+            // the whole unified L1 / shared memory as shared memory, so that
+            // four CTAs (4 x 35 KB) fit beside each other
+            e = cudaFuncSetAttribute(kv4_attention_kernel<NSV>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     static_cast<int>(cudaSharedmemCarveoutMaxShared));
+            if (e != cudaSuccess) return e;
             configured[dev] = true;
         }
     }
@@ -540,14 +594,19 @@ cudaError_t launch_attn(const AttnParams &p, cudaStream_t stream) {
 Kv4Plan plan_kv4_attention(int B, int hq, int hkv, int max_pages, int num_sms) {
     Kv4Plan pl{};
     const long long base = static_cast<long long>(B) * hkv;
-    // about four CTAs per SM over the whole grid, at least two pages per split
-    long long splits = (4LL * num_sms + base - 1) / base;
+    // As many splits as keep the whole grid resident at once (one wave: 4
+    // CTAs per SM, 3 for G = 8), at least two pages per split.  A second,
+    // partial wave costs more than the shorter splits save (measured: batch
+    // 64 x ~1K tokens 25.8 us in one wave against 31.2 us in 1.7 waves).
+    const int G0 = hkv > 0 ? hq / hkv : 0;
+    const long long cap = static_cast<long long>(G0 > 4 ? 3 : 4) * num_sms;
+    long long splits = cap / base;
     const long long max_splits = (max_pages + 1) / 2;
     if (splits > max_splits) splits = max_splits;
     if (splits < 1) splits = 1;
     pl.pages_per_split = static_cast<int>((max_pages + splits - 1) / splits);
     pl.splits = (max_pages + pl.pages_per_split - 1) / pl.pages_per_split;
-    const int G = hkv > 0 ? hq / hkv : 0;
+    const int G = G0;
     pl.partial_offset = kWsStatusBytes;
     pl.ws_bytes = kWsStatusBytes + (pl.splits > 1 ? static_cast<size_t>(base) * pl.splits * G * (2 + kHD) * 4 : 0);
     return pl;
