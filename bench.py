@@ -711,15 +711,20 @@ def main(argv=None):
 
         # Transfers overlap the compute, as in a serving loop: the inputs go
         # up on a copy-in stream and the outputs come down on a copy-out
-        # stream, in groups of consecutive points (up to about 2 MB of output
-        # each, so large outputs go down while later points compute): a
-        # group's compute waits for its inputs' event, its outputs are copied
-        # once its last GEMM is done, and the step ends when all outputs are
-        # on the host.  A step overwrites inputs and outputs only after the
-        # previous step's readers of them have finished.
+        # stream, in groups of points (up to about 2 MB of output each, so
+        # large outputs go down while later points compute): a group's
+        # compute waits for its inputs' event, its outputs are copied once its
+        # last GEMM is done, and the step ends when all outputs are on the
+        # host.  The points run largest output first (the same work as the
+        # device-timed step, in another order), so the long copies of the
+        # prefill outputs overlap the compute of the remaining points instead
+        # of trailing the step.  A step overwrites inputs and outputs only
+        # after the previous step's readers of them have finished.
         copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        order = sorted(range(len(pts)), key=lambda i: -pts[i]["O"].numel())
         groups, cur, cur_bytes = [], [], 0
-        for i, pt in enumerate(pts):
+        for i in order:
+            pt = pts[i]
             cur.append(i)
             cur_bytes += pt["O"].numel() * 2
             if cur_bytes >= 2 << 20:

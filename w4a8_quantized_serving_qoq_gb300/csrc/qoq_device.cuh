@@ -173,20 +173,6 @@ __device__ __forceinline__ void bulk_wait() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared (L2 only), tracked by the
-// issuing thread's commit groups; cp_async_wait<N> returns once at most N of
-// its groups are still in flight (a hardware wait on the thread's own copies).
-__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void *gmem_src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gmem_src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Bulk prefetch of global memory into L2 (address and size 16-byte
 // aligned).  L2 is the point of coherence, so a prefetch issued before a
 // dependency wait cannot make a later read return stale data.

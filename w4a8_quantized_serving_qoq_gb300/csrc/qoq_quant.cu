@@ -26,6 +26,20 @@ __device__ __forceinline__ uint16_t f2h_rn(float f) { return __half_as_ushort(__
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
+// 16-byte asynchronous copy global -> shared (L2 only), tracked by the
+// issuing thread's commit groups; cp_async_wait<N> returns once at most N of
+// its groups are still in flight (a hardware wait on the thread's own copies).
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Round-half-even of a / b for integers, b > 0.
 __device__ __forceinline__ int rne_div(int a, int b) {
     int q = a / b, r = a - q * b;
