@@ -715,13 +715,15 @@ def main(argv=None):
         # large outputs go down while later points compute): a group's
         # compute waits for its inputs' event, its outputs are copied once its
         # last GEMM is done, and the step ends when all outputs are on the
-        # host.  The points run largest output first (the same work as the
-        # device-timed step, in another order), so the long copies of the
-        # prefill outputs overlap the compute of the remaining points instead
-        # of trailing the step.  A step overwrites inputs and outputs only
-        # after the previous step's readers of them have finished.
+        # host.  The points run in another order than in the device-timed
+        # step (the same work): most output bytes per unit of compute first
+        # (K ascending; then more tokens first, smaller outputs first), so the
+        # device-to-host copies, which take about as long as the whole
+        # compute, start early and overlap it instead of trailing the step.
+        # A step overwrites inputs and outputs only after the previous step's
+        # readers of them have finished.
         copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        order = sorted(range(len(pts)), key=lambda i: -pts[i]["O"].numel())
+        order = sorted(range(len(pts)), key=lambda i: (pts[i]["layer"].K, -pts[i]["M"], pts[i]["O"].numel()))
         groups, cur, cur_bytes = [], [], 0
         for i in order:
             pt = pts[i]
