@@ -288,7 +288,12 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  *   kernel          : 0 = automatic, 1 = fp16-operand tensor-core path
  *                     (dequantized weights), 2 = fp8-operand path (4-bit
  *                     codes and split activations as exact e4m3, group 128
- *                     only, tokens_per_tile 16 or 32).
+ *                     only, tokens_per_tile 16 or 32), 3 = CUDA-core dp4a
+ *                     path (M <= 8; num_ctas = the K split, a thread-block
+ *                     cluster of 1, 2, 4 or 8 CTAs per 128-row tile; no
+ *                     activation operand).  Automatic: the measured dispatch
+ *                     table for the shape, else dp4a up to 4 tokens, fp8 up
+ *                     to 32 (g128), fp16 above.
  *   act_operand     : the activation operand written by qoq_quant_act_ex for
  *                     the same Qx (16-byte aligned), of the kind equal to
  *                     this GEMM's qoq_gemm_path; the GEMM reads it instead
@@ -321,10 +326,11 @@ typedef struct {
 size_t qoq_gemm_workspace_bytes_ex(int M, int N, int K, int group, const qoq_gemm_options *opt);
 
 /*
- * The tensor-core path a GEMM of this shape and options takes on the current
- * device: 1 = fp16-operand path, 2 = fp8-operand path, or minus a qoq_status
- * for invalid arguments.  It is also the kind of activation operand the GEMM
- * reads (qoq_quant_act_ex).
+ * The path a GEMM of this shape and options takes on the current device:
+ * 1 = fp16-operand path, 2 = fp8-operand path, 3 = CUDA-core dp4a path, or
+ * minus a qoq_status for invalid arguments.  For 1 and 2 it is also the kind
+ * of activation operand the GEMM reads (qoq_quant_act_ex); path 3 reads Qx
+ * itself.
  */
 int qoq_gemm_path(int M, int N, int K, int group, const qoq_gemm_options *opt);
 

@@ -30,11 +30,11 @@ def test_decode_sizes_take_the_fp8_path_and_leave_8_sms(M, NK):
     assert p["k_stages"] == p["tiles"] * (NK[1] // 128)
 
 
-@pytest.mark.parametrize("M,MT", [(1, 1), (2, 2), (3, 4), (5, 8), (8, 8)])
+@pytest.mark.parametrize("M,MT", [(1, 1), (2, 2), (3, 4), (4, 4)])
 @pytest.mark.parametrize("NK,csize", [(QKV, 8), (O, 8), (GATE_UP, 4), (DOWN, 8), ((59136, 8192), 1),
                                       ((8192, 29568), 8)])
-def test_up_to_8_tokens_take_the_cuda_core_path(M, MT, NK, csize):
-    """M <= 8: the dp4a path, tokens rounded up to 1, 2, 4 or 8; the K split
+def test_up_to_4_tokens_take_the_cuda_core_path(M, MT, NK, csize):
+    """M <= 4: the dp4a path, tokens rounded up to 1, 2 or 4; the K split
     (cluster size) is the largest of 8, 4, 2, 1 that keeps at most six CTAs
     per SM with a block per K half; only the status word in the workspace."""
     p = _plan(M, NK)
@@ -43,6 +43,18 @@ def test_up_to_8_tokens_take_the_cuda_core_path(M, MT, NK, csize):
     assert p["workspace_bytes"] == 256
     for group in (0, 128):
         assert _plan(M, NK, group=group)["path"] == 3
+
+
+@pytest.mark.parametrize("M", [5, 8])
+@pytest.mark.parametrize("NK", [QKV, GATE_UP, (59136, 8192)])
+def test_5_to_8_tokens_take_the_tensor_cores_unless_forced(M, NK):
+    """From 5 tokens the rules leave the dp4a path (its work per weight grows
+    with the tokens): fp8 for g128, fp16 for per-channel weights; forcing the
+    path still gives it, with 8-token tiles."""
+    assert _plan(M, NK)["path"] == 2
+    assert _plan(M, NK, group=0)["path"] == 1
+    p = _plan(M, NK, kernel=3)
+    assert (p["path"], p["tokens_per_tile"]) == (3, 8)
 
 
 def test_cuda_core_path_options():

@@ -835,8 +835,11 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
     }
     GemmPlan pl{};
     const int G = K / kTileK, n_tiles = N / kTileN;
-    // Decode batches of at most 8 tokens: the CUDA-core GEMV path, whose
-    // launches carry no tensor-core setup, when its shared memory fits.
+    // Decode batches of at most 4 tokens: the CUDA-core GEMV path, whose
+    // launches carry no tensor-core setup, when its shared memory fits (the
+    // path takes up to 8 tokens when forced; from 5 tokens its dp4a work per
+    // weight outweighs the tensor cores' setup: gate_up at 8 tokens 54.8 us
+    // against 19.7 on the fp8 path).
     int mt = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
     int csize = 1;
     if (M <= 8 && num_sms > 0) {
@@ -852,7 +855,7 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
         while (csize < 8 && gemv_smem_bytes(mt, G, csize) > kGemvSmemMax) csize *= 2;
     }
     const bool gemv_ok = M <= 8 && (group == 0 || group == 128) && gemv_smem_bytes(mt, G, csize) <= kGemvSmemMax;
-    if (force_path == kPathGemv || (force_path == 0 && force_bt == 0 && gemv_ok)) {
+    if (force_path == kPathGemv || (force_path == 0 && force_bt == 0 && gemv_ok && M <= 4)) {
         if (!gemv_ok) {
             // forced for a shape the path cannot take: report an empty plan
             pl.path = 0;

@@ -85,7 +85,7 @@ __host__ __device__ inline size_t act_operand_bytes(int M, int K, int kind) {
 enum GemmPath : int {
     kPathF16 = 1,          // weights dequantized to exact fp16, kind::f16 MMA
     kPathF8 = 2,           // raw 4-bit codes and split activations as exact e4m3, kind::f8f6f4 MMA
-    kPathGemv = 3,         // decode batches (M <= 8): CUDA-core dp4a, K split over a thread-block cluster
+    kPathGemv = 3,         // decode batches (M <= 4; up to 8 when forced): CUDA-core dp4a, K split over a cluster
 };
 
 struct GemmPlan {

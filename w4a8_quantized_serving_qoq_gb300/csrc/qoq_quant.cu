@@ -83,8 +83,10 @@ constexpr float kRneMagic = 12582912.0f;
 // integer unless t lies within 3e-5 of a half-integer (|t - rne(t)| >
 // 0.49997); there the IEEE division decides.  Codes are clamped to
 // [-127, 127] (clamping t first gives the same codes: rne is monotone and
-// maps +-127 to themselves); s = 0 gives inv = 0 and zero codes.
-template <bool kF16>
+// maps +-127 to themselves); s = 0 gives inv = 0 and zero codes.  The clamp
+// can only act when s is an fp16 subnormal (kClamp): a normal s is within
+// 2^-11 relative of max|x| / 127, so |t| < 127.07 and rne(t) is in range.
+template <bool kF16, bool kClamp>
 __device__ __forceinline__ uint2 quant8(const uint4 v, float sf, float inv, int &sum, uint4 *f16) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float t[8], r[8];
@@ -92,7 +94,8 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, float sf, float inv, int 
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const uint16_t hb = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu));
-        t[j] = fminf(fmaxf(__fmul_rn(h2f(hb), inv), -127.0f), 127.0f);
+        t[j] = __fmul_rn(h2f(hb), inv);
+        if (kClamp) t[j] = fminf(fmaxf(t[j], -127.0f), 127.0f);
         r[j] = __fadd_rn(t[j], kRneMagic);
         tie |= fabsf(__fsub_rn(t[j], __fsub_rn(r[j], kRneMagic))) > 0.49997f;
     }
@@ -257,14 +260,23 @@ struct RowOut {
 // tsum.  Lanes with i >= nv write nothing; for kind 2 every lane of the warp
 // must call it together (the 16 items of a 128-k group are summed by
 // half-warp shuffles, so i runs over consecutive items in each half-warp).
-template <int kAct>
+// kNoClampPath: rows with a normal scale take the quantizer without the
+// clamp (a second inlined copy).  Measured faster in the 256-thread
+// row-streaming kernel (rows up to 16 KB: quant 16.7 -> 15.8 us at M = 4096,
+// K = 4096) and slower in the 512-thread one (K = 14336: 48.8 -> 52.4 us);
+// the one-CTA-per-row kernel, register-capped at 1,024-thread rows, keeps
+// the single clamped copy too.
+template <int kAct, bool kNoClampPath>
 __device__ __forceinline__ void emit8(const RowOut<kAct> &o, int i, int nv, const uint4 v, float sf, float inv,
                                       int &tsum) {
     int part = 0;
     uint2 q = make_uint2(0u, 0u);
     if (i < nv) {
         uint4 f16;
-        q = quant8<kAct == 1>(v, sf, inv, part, &f16);
+        if (kNoClampPath && sf >= 6.103515625e-05f)  // 2^-14, the smallest normal fp16 (uniform across the row)
+            q = quant8<kAct == 1, false>(v, sf, inv, part, &f16);
+        else
+            q = quant8<kAct == 1, true>(v, sf, inv, part, &f16);
         o.qrow[i] = q;
         if (o.yrow) o.yrow[i] = v;
         if (kAct == 1) o.frow[i] = f16;
@@ -364,10 +376,10 @@ __global__ void __launch_bounds__(kSrc == kSrcX ? 1024 : 512) quant_act_kernel(c
     int tsum = 0;
 #pragma unroll
     for (int j = 0; j < kActCache; ++j)
-        if (j * bd < nv) emit8(out, tid + j * bd, nv, cache[j], sf, inv, tsum);
+        if (j * bd < nv) emit8<kAct, false>(out, tid + j * bd, nv, cache[j], sf, inv, tsum);
     for (int base = kActCache * bd; base < nv; base += bd) {
         const int i = base + tid;
-        emit8(out, i, nv, i < nv ? item(i) : make_uint4(0u, 0u, 0u, 0u), sf, inv, tsum);
+        emit8<kAct, false>(out, i, nv, i < nv ? item(i) : make_uint4(0u, 0u, 0u, 0u), sf, inv, tsum);
     }
     if (t_x) tsum = block_reduce(tsum, SumOp(), shi, 0);  // t_x is uniform across the CTA
     if (tid == 0) {
@@ -448,7 +460,7 @@ __global__ void __launch_bounds__(kT) quant_rows_kernel(const RowSrc src, int M,
         int tsum = 0;
         for (int base = 0; base < nv; base += kT) {
             const int i = base + tid;
-            emit8(out, i, nv, i < nv ? buf[i] : make_uint4(0u, 0u, 0u, 0u), sf, inv, tsum);
+            emit8<kAct, kT == 256>(out, i, nv, i < nv ? buf[i] : make_uint4(0u, 0u, 0u, 0u), sf, inv, tsum);
         }
         if (t_x) tsum = block_reduce(tsum, SumOp(), shi, 0);
         if (tid == 0) {
