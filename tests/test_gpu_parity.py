@@ -111,6 +111,33 @@ def test_quant_act_ex_act_operand_bit_exact(M, K, kind):
     assert not got_tg[:, M:].any()  # padding columns zero-filled by the last row
 
 
+@pytest.mark.parametrize("M,K", [(7, 1024), (400, 1024), (310, 14336)])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_quant_act_row_scales_from_subnormal_to_large(M, K, kind):
+    """Rows scaled from 1e-7 to 1e3: the fp16 scale s_x runs from zero and
+    subnormal values (where the clamp to +-127 acts: max|x| / s_x can exceed
+    127 when s_x is a rounded subnormal) to normal ones, and the codes of every
+    row (both quantizer kernels, M < 296 and M >= 296; both branches of the
+    row-streaming kernel) equal the oracle's bit for bit."""
+    rng = np.random.default_rng(4000 + M + K + kind)
+    X = rng.standard_normal((M, K))
+    scales = 10.0 ** rng.uniform(-7, 3, M)
+    scales[:4] = [1e-7, 3e-7, 1.2e-6, 6e-6]     # s_x zero, smallest subnormals
+    X = (X * scales[:, None]).astype(np.float16)
+    Qx_r, sx_r, tx_r = oracle.quant_act(X)
+    assert (sx_r.view(np.uint16)[:M] < 0x0400).any() and (sx_r.view(np.uint16) >= 0x0400).any()
+    if kind == 0:
+        Qx, sx, tx = qoq.qoq_quant_act(_t(X))
+    else:
+        Qx, sx, tx, act = qoq.qoq_quant_act_ex(_t(X), kind=kind)
+        if kind == 1:
+            assert np.array_equal(_np(act).view(np.float16).reshape(M, K).astype(np.float64),
+                                  Qx_r.astype(np.float64))
+    assert np.array_equal(_np(Qx), Qx_r)
+    assert np.array_equal(_np(sx).view(np.uint16), sx_r.view(np.uint16))
+    assert np.array_equal(_np(tx), tx_r)
+
+
 def test_quant_act_ties_half_even():
     row = np.zeros(128, np.float32)
     row[0] = 127 * 0.125

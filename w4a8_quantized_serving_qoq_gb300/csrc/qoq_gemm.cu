@@ -21,7 +21,8 @@
 //    with byte-lane SIMD: one 32-bit multiply-add per 4 weights yields
 //    (q4 - z) * s_g + 128 in each byte (legal because the protective range
 //    keeps every product in [-128, 127]), then byte -> fp16 by exponent
-//    splicing and one fp16x2 subtract, stored to TMEM as the A operand;
+//    splicing and one fp16x2 subtract, stored to TMEM as the A operand
+//    (per-channel weights: the raw codes as fp16 subnormals, see kPC);
 //  * two threads issue tcgen05.mma on alternate stages (kind::f16, fp32
 //    accumulation in TMEM).  Operands are integers with |product| <= 127 *
 //    128, so an fp32 sum over 1024 k (8 stages) stays below 2^24 and is exact
@@ -134,7 +135,13 @@ __device__ __forceinline__ void biased_bytes_to_f16x4(uint32_t u, uint32_t &lo, 
 
 // kAccOut: the int32 test output (GemmParams::acc_out) instead of fp16 O.  A
 // separate instantiation, so that the fp16 kernel carries no code for it.
-template <int BT, bool kAccOut>
+// kPC: per-channel weights (group == 0).  Their raw codes q in [0, 15] enter
+// the MMA as fp16 subnormals (the byte q in the low bits of a half is exactly
+// q * 2^-24, so a byte permute with zero bytes is the whole conversion); a
+// chunk's sums, at most 1024 * 15 * 127 * 2^-24, stay exact in fp32, and the
+// drain scales them back by 2^24.  (The g128 codes carry the bias 128 of the
+// byte-lane dequantization, which would limit an exact chunk to 512 k.)
+template <int BT, bool kAccOut, bool kPC>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_gemm_kernel(const __grid_constant__ CUtensorMap qx_map, const __grid_constant__ CUtensorMap o_map,
                      const GemmParams p) {
@@ -420,8 +427,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (j + 1 < NB) tmem_st16(cbase + static_cast<uint32_t>(16 * j + 16), zero16);
     #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            acc[16 * j + i] += __float2int_rn(__uint_as_float(f0[i]));
-                            if (j + 1 < NB) acc[16 * j + 16 + i] += __float2int_rn(__uint_as_float(f1[i]));
+                            if constexpr (kPC) {  // 2^24 undoes the subnormal codes
+                                acc[16 * j + i] += __float2int_rn(__fmul_rn(__uint_as_float(f0[i]), 16777216.0f));
+                                if (j + 1 < NB)
+                                    acc[16 * j + 16 + i] += __float2int_rn(__fmul_rn(__uint_as_float(f1[i]), 16777216.0f));
+                            } else {
+                                acc[16 * j + i] += __float2int_rn(__uint_as_float(f0[i]));
+                                if (j + 1 < NB) acc[16 * j + 16 + i] += __float2int_rn(__uint_as_float(f1[i]));
+                            }
                         }
                     }
                     tmem_wait_st();
@@ -631,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // operand slot, so only the TMEM store follows the MMAs that
                 // free the slot.
                 uint32_t s = 1, zz = 0;
-                if (p.group) {
+                if (!kPC) {
                     uint16_t meta;
                     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(meta) : "r"(wraw + kCodeBytes + 4 * wr));
                     s = meta & 0xffu;
@@ -649,11 +662,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 4; ++j) {
                             const uint32_t lo = w4[j] & 0x0F0F0F0Fu;
                             const uint32_t hi = (w4[j] >> 4) & 0x0F0F0F0Fu;
-                            const uint32_t ulo = lo * s + cst;  // bytes: (q - z) * s + 128
-                            const uint32_t uhi = hi * s + cst;
                             uint32_t *f = a_frag[h] + 16 * i + 4 * j;
-                            biased_bytes_to_f16x4(ulo, f[0], f[1]);
-                            biased_bytes_to_f16x4(uhi, f[2], f[3]);
+                            if (kPC) {
+                                // raw codes as fp16 subnormals q * 2^-24
+                                f[0] = __byte_perm(lo, 0u, 0x4140u);
+                                f[1] = __byte_perm(lo, 0u, 0x4342u);
+                                f[2] = __byte_perm(hi, 0u, 0x4140u);
+                                f[3] = __byte_perm(hi, 0u, 0x4342u);
+                            } else {
+                                const uint32_t ulo = lo * s + cst;  // bytes: (q - z) * s + 128
+                                const uint32_t uhi = hi * s + cst;
+                                biased_bytes_to_f16x4(ulo, f[0], f[1]);
+                                biased_bytes_to_f16x4(uhi, f[2], f[3]);
+                            }
                         }
                     }
                 }
@@ -710,7 +731,8 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!configured[dev]) {
-            for (auto kern : {w4a8_gemm_kernel<BT, false>, w4a8_gemm_kernel<BT, true>}) {
+            for (auto kern : {w4a8_gemm_kernel<BT, false, false>, w4a8_gemm_kernel<BT, true, false>,
+                              w4a8_gemm_kernel<BT, false, true>, w4a8_gemm_kernel<BT, true, true>}) {
                 e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));
                 if (e != cudaSuccess) return e;
@@ -786,8 +808,14 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     p.timeout_ns = a.timeout_ns;
     dim3 grid(plan.ctas);
     if (a.acc_out)
-        return launch_kernel(w4a8_gemm_kernel<BT, true>, grid, dim3(kThreads), C::kSmemBytes, stream, a.pdl, map, o_map, p);
-    return launch_kernel(w4a8_gemm_kernel<BT, false>, grid, dim3(kThreads), C::kSmemBytes, stream, a.pdl, map, o_map, p);
+        return p.group ? launch_kernel(w4a8_gemm_kernel<BT, true, false>, grid, dim3(kThreads), C::kSmemBytes, stream,
+                                       a.pdl, map, o_map, p)
+                       : launch_kernel(w4a8_gemm_kernel<BT, true, true>, grid, dim3(kThreads), C::kSmemBytes, stream,
+                                       a.pdl, map, o_map, p);
+    return p.group ? launch_kernel(w4a8_gemm_kernel<BT, false, false>, grid, dim3(kThreads), C::kSmemBytes, stream,
+                                   a.pdl, map, o_map, p)
+                   : launch_kernel(w4a8_gemm_kernel<BT, false, true>, grid, dim3(kThreads), C::kSmemBytes, stream,
+                                   a.pdl, map, o_map, p);
 }
 
 }  // namespace
