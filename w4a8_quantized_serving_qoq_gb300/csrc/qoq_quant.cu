@@ -86,26 +86,72 @@ constexpr float kRneMagic = 12582912.0f;
 // maps +-127 to themselves); s = 0 gives inv = 0 and zero codes.  The clamp
 // can only act when s is an fp16 subnormal (kClamp): a normal s is within
 // 2^-11 relative of max|x| / 127, so |t| < 127.07 and rne(t) is in range.
+// Paired fp32 arithmetic (sm_100 and later): one instruction rounds two
+// independent fp32 operations exactly as two scalar ones would.
+__device__ __forceinline__ uint64_t f32x2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 template <bool kF16, bool kClamp>
 __device__ __forceinline__ uint2 quant8(const uint4 v, float sf, float inv, int &sum, uint4 *f16) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float t[8], r[8];
+    float t[8], r[8], qf[8];  // x / s, t + magic (the code in its low byte), rne(t)
     bool tie = false;
+    if constexpr (!kClamp) {
+        // the same roundings as the scalar form below, two values per instruction
+        const uint64_t inv2 = f32x2_pack(inv, inv), mg2 = f32x2_pack(kRneMagic, kRneMagic);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint16_t hb = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu));
-        t[j] = __fmul_rn(h2f(hb), inv);
-        if (kClamp) t[j] = fminf(fmaxf(t[j], -127.0f), 127.0f);
-        r[j] = __fadd_rn(t[j], kRneMagic);
-        tie |= fabsf(__fsub_rn(t[j], __fsub_rn(r[j], kRneMagic))) > 0.49997f;
+        for (int j = 0; j < 4; ++j) {
+            const uint64_t T = f32x2_mul(f32x2_pack(h2f(static_cast<uint16_t>(w[j] & 0xffffu)),
+                                                    h2f(static_cast<uint16_t>(w[j] >> 16))),
+                                         inv2);
+            const uint64_t R = f32x2_add(T, mg2);
+            const uint64_t Q = f32x2_sub(R, mg2);
+            float d0, d1;
+            f32x2_unpack(f32x2_sub(T, Q), d0, d1);
+            f32x2_unpack(T, t[2 * j], t[2 * j + 1]);
+            f32x2_unpack(R, r[2 * j], r[2 * j + 1]);
+            f32x2_unpack(Q, qf[2 * j], qf[2 * j + 1]);
+            tie |= fabsf(d0) > 0.49997f || fabsf(d1) > 0.49997f;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint16_t hb = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu));
+            t[j] = fminf(fmaxf(__fmul_rn(h2f(hb), inv), -127.0f), 127.0f);
+            r[j] = __fadd_rn(t[j], kRneMagic);
+            qf[j] = __fsub_rn(r[j], kRneMagic);
+            tie |= fabsf(__fsub_rn(t[j], qf[j])) > 0.49997f;
+        }
     }
     if (tie) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            if (fabsf(__fsub_rn(t[j], __fsub_rn(r[j], kRneMagic))) > 0.49997f) {
+            if (fabsf(__fsub_rn(t[j], qf[j])) > 0.49997f) {
                 const uint16_t hb = static_cast<uint16_t>((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu));
                 const int q = clampi(__float2int_rn(__fdiv_rn(h2f(hb), sf)), -127, 127);
-                r[j] = __fadd_rn(static_cast<float>(q), kRneMagic);
+                qf[j] = static_cast<float>(q);
+                r[j] = __fadd_rn(qf[j], kRneMagic);
             }
         }
     }
@@ -120,7 +166,7 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, float sf, float inv, int 
         uint32_t h[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const __half2 p = __floats2half2_rn(__fsub_rn(r[2 * j], kRneMagic), __fsub_rn(r[2 * j + 1], kRneMagic));
+            const __half2 p = __floats2half2_rn(qf[2 * j], qf[2 * j + 1]);
             h[j] = *reinterpret_cast<const uint32_t *>(&p);
         }
         *f16 = make_uint4(h[0], h[1], h[2], h[3]);
@@ -189,17 +235,20 @@ __device__ __forceinline__ float sumsq8(const uint4 v, float ss) {
     return ss;
 }
 
-// Eight normalized values: fp16((x * r) * gamma), each product rounded in fp32.
+// Eight normalized values: fp16((x * r) * gamma), each product rounded in
+// fp32 (paired fp32 multiplies, the same roundings as scalar ones).
 __device__ __forceinline__ uint4 norm8(const uint4 x, const uint4 g, float r) {
     const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, gs[4] = {g.x, g.y, g.z, g.w};
+    const uint64_t r2 = f32x2_pack(r, r);
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = f2h_rn(__fmul_rn(__fmul_rn(h2f(static_cast<uint16_t>(xs[j] & 0xffffu)), r),
-                                             h2f(static_cast<uint16_t>(gs[j] & 0xffffu))));
-        const uint32_t hi = f2h_rn(__fmul_rn(__fmul_rn(h2f(static_cast<uint16_t>(xs[j] >> 16)), r),
-                                             h2f(static_cast<uint16_t>(gs[j] >> 16))));
-        o[j] = lo | (hi << 16);
+        const uint64_t X = f32x2_pack(h2f(static_cast<uint16_t>(xs[j] & 0xffffu)), h2f(static_cast<uint16_t>(xs[j] >> 16)));
+        const uint64_t G = f32x2_pack(h2f(static_cast<uint16_t>(gs[j] & 0xffffu)), h2f(static_cast<uint16_t>(gs[j] >> 16)));
+        float lo, hi;
+        f32x2_unpack(f32x2_mul(f32x2_mul(X, r2), G), lo, hi);
+        const __half2 p = __floats2half2_rn(lo, hi);
+        o[j] = *reinterpret_cast<const uint32_t *>(&p);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
