@@ -714,14 +714,17 @@ def main(argv=None):
         # stream, in groups of points (up to about 2 MB of output each, so
         # large outputs go down while later points compute): a group's
         # compute waits for its inputs' event, its outputs are copied once its
-        # last GEMM is done, and the step ends when all outputs are on the
-        # host.  The points run in another order than in the device-timed
-        # step (the same work): most output bytes per unit of compute first
-        # (K ascending; then more tokens first, smaller outputs first), so the
-        # device-to-host copies, which take about as long as the whole
-        # compute, start early and overlap it instead of trailing the step.
-        # A step overwrites inputs and outputs only after the previous step's
-        # readers of them have finished.
+        # last GEMM is done.  Device inputs and outputs are double-buffered
+        # across steps, so step n + 1's inputs go up while step n computes
+        # and its outputs come down; a buffer set is rewritten only after
+        # step n - 1's readers of it (its compute for the inputs, its
+        # device-to-host copies for the outputs) have finished, and the timed
+        # region ends when the last step's outputs are on the host.  The
+        # points run in another order than in the device-timed step (the same
+        # work): most output bytes per unit of compute first (K ascending;
+        # then more tokens first, smaller outputs first), so the
+        # device-to-host copies, which take about as long as the compute,
+        # start early in the step.
         copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         order = sorted(range(len(pts)), key=lambda i: (pts[i]["layer"].K, -pts[i]["M"], pts[i]["O"].numel()))
         groups, cur, cur_bytes = [], [], 0
@@ -734,46 +737,60 @@ def main(argv=None):
                 cur, cur_bytes = [], 0
         if cur:
             groups.append(cur)
-        ev_in = [torch.cuda.Event() for _ in groups]
-        ev_done = [torch.cuda.Event() for _ in groups]
+        bufs = [[(p["X"], p["O"]) for p in pts], [(torch.empty_like(p["X"]), torch.empty_like(p["O"])) for p in pts]]
+        ev_in = [[torch.cuda.Event() for _ in groups] for _ in range(2)]
+        ev_done = [[torch.cuda.Event() for _ in groups] for _ in range(2)]
+        ev_comp_end = [torch.cuda.Event() for _ in range(2)]
+        ev_out_end = [torch.cuda.Event() for _ in range(2)]
+        for e in ev_comp_end + ev_out_end:
+            e.record(stream)
 
-        def e2e_step():
-            copy_in.wait_stream(stream)
+        def e2e_step(n):
+            bs = n % 2
+            copy_in.wait_event(ev_comp_end[bs])  # step n - 2 has read these inputs
             with torch.cuda.stream(copy_in):
                 for gi, grp in enumerate(groups):
                     for i in grp:
-                        pts[i]["X"].copy_(hostX[i], non_blocking=True)
-                    ev_in[gi].record(copy_in)
-            stream.wait_stream(copy_out)
+                        bufs[bs][i][0].copy_(hostX[i], non_blocking=True)
+                    ev_in[bs][gi].record(copy_in)
+            stream.wait_event(ev_out_end[bs])  # step n - 2's outputs are on the host
             for gi, grp in enumerate(groups):
-                stream.wait_event(ev_in[gi])
+                stream.wait_event(ev_in[bs][gi])
                 for i in grp:
+                    pts[i]["X"], pts[i]["O"] = bufs[bs][i]
                     run_point(pts[i], i)
-                ev_done[gi].record(stream)
-                copy_out.wait_event(ev_done[gi])
+                ev_done[bs][gi].record(stream)
+                copy_out.wait_event(ev_done[bs][gi])
                 with torch.cuda.stream(copy_out):
                     for i in grp:
-                        hostO[i].copy_(pts[i]["O"], non_blocking=True)
-            stream.wait_stream(copy_out)
+                        hostO[i].copy_(bufs[bs][i][1], non_blocking=True)
+            ev_comp_end[bs].record(stream)
+            ev_out_end[bs].record(copy_out)
 
-        for _ in range(2):
-            e2e_step()
+        for n in range(2):
+            e2e_step(n)
+        stream.wait_stream(copy_out)
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        copy_in.wait_stream(stream)
+        copy_out.wait_stream(stream)
+        for n in range(e2e_steps):
+            e2e_step(n)
+        stream.wait_stream(copy_out)
         b.record(stream)
         torch.cuda.synchronize()
+        for i, p in enumerate(pts):
+            p["X"], p["O"] = bufs[0][i]
         if dist:
             dist.barrier()
         e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, dist, dev)
         e2e = {"value": whole_job_tops(ops_step, world, e2e_ms), "unit": "TOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "path": "Python binding -> C ABI per call (no CUDA graph), pinned host buffers, host<->device copies on two side streams overlapping the compute"}
-        del hostX, hostO
+               "path": "Python binding -> C ABI per call (no CUDA graph), pinned host buffers, host<->device copies on two side streams overlapping the compute, device inputs and outputs double-buffered across steps"}
+        del hostX, hostO, bufs
 
     # ---- further workloads, point by point ----
     block_out = {}
