@@ -690,6 +690,7 @@ def main(argv=None):
                 "group": pt["group"], "path": pt["plan"]["path"], "tokens_per_tile": pt["plan"]["tokens_per_tile"],
                 "ctas": pt["plan"]["num_ctas"], "gemm_us": round(t_g, 2), "quant_us": round(t_q, 2),
                 "TOPS": round(nops / (t_g * 1e-6) / 1e12, 2), "GBs": round(nbytes / (t_g * 1e-6) / 1e9, 1),
+                "GBs_full": round(roofline.w4a8_bytes_full(M, layer.N, layer.K, pt["group"]) / (t_g * 1e-6) / 1e9, 1),
                 "bound": roofline.bound(M, layer.N, layer.K, bw, p16),
                 "roof_frac": round(troof / (t_g * 1e-6), 3),
             })

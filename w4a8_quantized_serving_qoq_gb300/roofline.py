@@ -21,7 +21,9 @@ def w4a8_bytes(M: int, N: int, K: int) -> int:
 
 
 def w4a8_bytes_full(M: int, N: int, K: int, group: int = 128) -> int:
-    """Adds group metadata (2 B per 128 weights here), s_w, s_x and the fp16 output."""
+    """The stricter traffic: B plus the group metadata (the UINT8 scale and
+    the zero, one byte each, per 128 weights; per-channel: one zero byte per
+    row), s_w, s_x and the fp16 output."""
     meta = (N * (K // group) * 2) if group else N
     return w4a8_bytes(M, N, K) + meta + 2 * N + 2 * M + 2 * M * N
 
