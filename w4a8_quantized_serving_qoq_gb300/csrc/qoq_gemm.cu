@@ -121,6 +121,17 @@ __device__ __forceinline__ void write_block_i32(const GemmParams &p, uint32_t bu
     }
 }
 
+// D[tmem] += A[tmem] * B[smem desc]^T (kind::f16, accumulating), the B
+// descriptor passed as its two 32-bit words.
+__device__ __forceinline__ void mma_f16_tmem_a_acc(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                   uint32_t idesc) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 bd;\n setp.ne.b32 p, 1, 0;\n mov.b64 bd, {%2, %3};\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc)
+        : "memory");
+}
+
 // Four INT8 / biased bytes -> two fp16x2 words holding the signed values.
 // Input byte b is v + 128 (v in [-128, 127]); 0x64XX is the fp16 1024 + XX.
 __device__ __forceinline__ void biased_bytes_to_f16x4(uint32_t u, uint32_t &lo, uint32_t &hi) {
@@ -332,10 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t d_tmem = tmem + C::kChunk0 + static_cast<uint32_t>((cur & 1) * BT);
                             const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u;
                             const uint32_t b_slot = smem_u32(b_base + (st % RB) * C::kBBytes);
+                            // The slot's descriptor once; each k step adds its byte offset / 16
+                            // to the address field (bits 0-13, no carry: shared-memory
+                            // addresses stay below 2^18), a 32-bit add on the low word.
+                            const uint64_t bd0 = desc_kmajor_sw128(b_slot);
+                            const uint32_t bd_lo = static_cast<uint32_t>(bd0), bd_hi = static_cast<uint32_t>(bd0 >> 32);
     #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t bd = desc_kmajor_sw128(b_slot + (kk >> 2) * C::kBAtom + (kk & 3) * 32);
-                                mma_f16_tmem_a(d_tmem, a_tmem + 8u * kk, bd, idesc, 1u);
+                                const uint32_t off = ((kk >> 2) * C::kBAtom + (kk & 3) * 32) >> 4;
+                                mma_f16_tmem_a_acc(d_tmem, a_tmem + 8u * kk, bd_lo + off, bd_hi, idesc);
                             }
                             mma_commit(&op_empty[os]);
                             mma_commit(&b_empty[st % RB]);
