@@ -97,12 +97,23 @@ struct F8Cfg {
     static_assert((kAuxStages * kAuxStageBytes) % 8 == 0, "barrier alignment");
 };
 
-__device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f8f6f4, the B descriptor
+// passed as its two 32-bit words: _first overwrites D, _acc accumulates.
+__device__ __forceinline__ void mma_f8_tmem_a_first(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                    uint32_t idesc) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "{\n .reg .pred p;\n .reg .b64 bd;\n setp.ne.b32 p, 0, 0;\n mov.b64 bd, {%2, %3};\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], bd, %4, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f8_tmem_a_acc(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                  uint32_t idesc) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 bd;\n setp.ne.b32 p, 1, 0;\n mov.b64 bd, {%2, %3};\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], bd, %4, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc)
         : "memory");
 }
 
@@ -325,11 +336,13 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     for (int g = 0; g < ng; ++g) {
                         const uint32_t d_tmem = tmem + static_cast<uint32_t>((2 * ds + g) * C::kNmma);
                         const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u + 32u * g;
-                        const uint32_t bg = b_base + g * C::kPlaneGroupBytes;
+                        // the group's descriptor once; each k step adds 32 bytes / 16 to the
+                        // address field (low word, no carry below 2^18)
+                        const uint64_t bd0 = desc_kmajor_sw128(b_base + g * C::kPlaneGroupBytes);
+                        const uint32_t lo = static_cast<uint32_t>(bd0), hi = static_cast<uint32_t>(bd0 >> 32);
+                        mma_f8_tmem_a_first(d_tmem, a_tmem, lo, hi, idesc);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_f8_tmem_a(d_tmem, a_tmem + 8u * kk, desc_kmajor_sw128(bg + 32u * kk), idesc,
-                                          kk ? 1u : 0u);
+                        for (int kk = 1; kk < 4; ++kk) mma_f8_tmem_a_acc(d_tmem, a_tmem + 8u * kk, lo + 2u * kk, hi, idesc);
                     }
                     mma_commit(&raw_empty[rs]);
                     mma_commit(&d_full[ds]);
