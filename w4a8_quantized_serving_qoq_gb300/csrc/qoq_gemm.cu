@@ -317,36 +317,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool stop = false;
                 while (!stop && walk.next(sg)) {
                     const int len = sg.k1 - sg.k0;
-                    int cur = 0;
-                    bool own_in_chunk = false;
-                    for (int i = 0; i < len; ++i, ++st) {
-                        const bool first = (i % kChunkStages) == 0;
-                        const bool last = (i % kChunkStages) == kChunkStages - 1 || i == len - 1;
-                        if (first) {
-                            cur = gc++;
-                            own_in_chunk = false;
+                    // chunk by chunk (chunks start at multiples of kChunkStages
+                    // of the segment); this thread's stages of a chunk are those
+                    // of its parity, two apart
+                    for (int i0 = 0; i0 < len && !stop; i0 += kChunkStages) {
+                        const int cur = gc++;
+                        const int i1 = min(len, i0 + kChunkStages);
+                        const int ib = i0 + (((st + i0) & 1) != par ? 1 : 0);
+                        if (ib < i1 && !mbar_wait(&chunk_empty[cur & 1], (cur >> 1) & 1, abort_flag, p.status, tmo)) {
+                            stop = true;
+                            break;
                         }
-                        if ((st & 1) == par) {
-                            if (!own_in_chunk) {
-                                own_in_chunk = true;
-                                if (!mbar_wait(&chunk_empty[cur & 1], (cur >> 1) & 1, abort_flag, p.status, tmo)) {
-                                    stop = true;
-                                    break;
-                                }
-                            }
-                            const int os = st % OPS, ouse = st / OPS;
+                        const uint32_t d_tmem = tmem + C::kChunk0 + static_cast<uint32_t>((cur & 1) * BT);
+                        for (int i = ib; i < i1; i += 2) {
+                            const int s = st + i;
+                            const int os = s % OPS, ouse = s / OPS, bs = s % RB;
                             if (!mbar_wait(&op_full[os], ouse & 1, abort_flag, p.status, tmo)) {
                                 stop = true;
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t d_tmem = tmem + C::kChunk0 + static_cast<uint32_t>((cur & 1) * BT);
                             const uint32_t a_tmem = tmem + C::kA0 + static_cast<uint32_t>(os) * 64u;
-                            const uint32_t b_slot = smem_u32(b_base + (st % RB) * C::kBBytes);
                             // The slot's descriptor once; each k step adds its byte offset / 16
                             // to the address field (bits 0-13, no carry: shared-memory
                             // addresses stay below 2^18), a 32-bit add on the low word.
-                            const uint64_t bd0 = desc_kmajor_sw128(b_slot);
+                            const uint64_t bd0 = desc_kmajor_sw128(smem_u32(b_base + bs * C::kBBytes));
                             const uint32_t bd_lo = static_cast<uint32_t>(bd0), bd_hi = static_cast<uint32_t>(bd0 >> 32);
     #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
@@ -354,10 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 mma_f16_tmem_a_acc(d_tmem, a_tmem + 8u * kk, bd_lo + off, bd_hi, idesc);
                             }
                             mma_commit(&op_empty[os]);
-                            mma_commit(&b_empty[st % RB]);
+                            mma_commit(&b_empty[bs]);
                         }
-                        if (last) mma_commit(&chunk_full[cur & 1]);
+                        if (!stop) mma_commit(&chunk_full[cur & 1]);
                     }
+                    st += len;
                 }
                 // All of this thread's MMAs must finish before TMEM is released.
                 mma_commit(mma_done);
