@@ -7,7 +7,8 @@
   oracle's own quantized keys and values, per (sequence, query head) row:
   |O - O_ref| <= 2e-3 * max_d |O_ref| + ulp16(|O_ref|), for grouped-query
   ratios 1, 2, 4 and 8, ragged lengths (page tails), split sequences, empty
-  sequences, and the Llama-3-8B decode workload (batch 64, lengths 512-1536).
+  sequences, many short sequences, a single token, repeated calls on one
+  workspace, and the Llama-3-8B decode workload (batch 64, lengths 512-1536).
 """
 import numpy as np
 import pytest
@@ -221,3 +222,43 @@ def test_attention_reports_bad_page_indices():
     qoq.qoq_kv4_decode_attention(_t(Q), pages, _t(table), _t(c["lens"]), hkv, 0.088, workspace=ws)
     st, bits = qoq.qoq_workspace_status(ws)
     assert st == 7 and bits & 4
+
+
+def test_attention_many_short_sequences():
+    """700 sequences of 1 to 3 pages (more (sequence, KV head) pairs than
+    resident CTAs), one of them empty."""
+    lens = list(np.random.default_rng(70).integers(1, 193, 700))
+    lens[5] = 0
+    hkv, hq = 2, 8
+    c = make_cache(lens, hkv, 71)
+    got, _ = _check(c, hkv, hq, 72)
+    assert not got.reshape(len(lens), hq, D)[5].any()
+
+
+def test_attention_single_token():
+    hkv, hq = 1, 4
+    c = make_cache([1], hkv, 73)
+    _check(c, hkv, hq, 74)
+
+
+def test_attention_repeated_calls_reuse_the_workspace():
+    """The same workspace gives the same outputs call after call, across
+    shapes (split and unsplit sequences)."""
+    hkv, hq = 8, 32
+    c = make_cache([2000, 7, 900], hkv, 75)
+    B = 3
+    Q = np.random.default_rng(76).standard_normal((B, hq, D)).astype(np.float16)
+    pages = device_pages(c, hkv)
+    ws = qoq.new_workspace(qoq.qoq_kv4_attention_workspace_bytes(B, hq, hkv, c["max_pages"]))
+    ref = _reference(c, Q, hkv, 0.05).reshape(B * hq, D)
+    for _ in range(3):
+        O = qoq.qoq_kv4_decode_attention(_t(Q), pages, _t(c["table"]), _t(c["lens"]), hkv, 0.05, workspace=ws)
+        got = O.cpu().numpy().astype(np.float64).reshape(B * hq, D)
+        assert oracle.o_within_tolerance(got, ref).all()
+    c1 = make_cache([100], hkv, 77)
+    Q1 = np.random.default_rng(78).standard_normal((1, hq, D)).astype(np.float16)
+    O1 = qoq.qoq_kv4_decode_attention(_t(Q1), device_pages(c1, hkv), _t(c1["table"]), _t(c1["lens"]), hkv, 0.05,
+                                      workspace=ws)
+    assert oracle.o_within_tolerance(O1.cpu().numpy().astype(np.float64).reshape(hq, D),
+                                     _reference(c1, Q1, hkv, 0.05).reshape(hq, D)).all()
+    assert qoq.qoq_workspace_status(ws)[0] == 0
