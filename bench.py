@@ -362,7 +362,7 @@ DISPATCH_TABLE = os.path.join(ROOT, "w4a8_quantized_serving_qoq_gb300", "csrc", 
 def gemm_candidates(M, N, K, group, sms):
     """(path, tokens_per_tile, ctas, schedule) launch choices timed by --tune;
     (0, 0, 0, 0) is the planner's current automatic choice.  ctas is the CTA
-    count (paths 1 and 2) or the cluster size (path 3); schedules 1..3 are
+    count (paths 1 and 2) or the cluster size (path 3); schedules 1..4 are
     tried where there are at least two waves of tiles."""
     tiles = N // 128
     cands = [(0, 0, 0)]  # expanded to (path, bt, ctas, schedule) below
@@ -384,7 +384,7 @@ def gemm_candidates(M, N, K, group, sms):
     for p_, b_, c_ in cands:
         t = -(-M // max(b_, 1)) * tiles if b_ else 0
         if p_ in (1, 2) and t >= 2 * c_:
-            out += [(p_, b_, c_, sch) for sch in (1, 2, 3)]
+            out += [(p_, b_, c_, sch) for sch in (1, 2, 3, 4)]
         else:
             out.append((p_, b_, c_, 0))
     return out

@@ -308,7 +308,9 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  *                     (CTA c: tiles c, c + P, ...), token-tile fastest, the
  *                     rest stream-K; 3 = as 2 with the tiles in bands of
  *                     about sqrt(P * tokens_per_tile / 32) weight tiles,
- *                     weight-tile fastest within a band.
+ *                     weight-tile fastest within a band; 4 = as 2 with the
+ *                     tiles weight-tile fastest (every weight tile of one
+ *                     token tile, then the next token tile).
  */
 typedef struct {
     int tokens_per_tile;

@@ -267,12 +267,13 @@ def test_gemm_tiles_and_stream_k_splits(bt, ctas, publish):
     assert qoq.qoq_workspace_status(ws)[0] == qoq.QOQ_OK
 
 
-@pytest.mark.parametrize("schedule", [1, 2, 3])
+@pytest.mark.parametrize("schedule", [1, 2, 3, 4])
 @pytest.mark.parametrize("bt,ctas", [(32, 7), (64, 3), (128, 5), (16, 13), (32, 0)])
 @pytest.mark.parametrize("publish", [0, 2])
 def test_gemm_schedules_bit_exact(schedule, bt, ctas, publish):
-    """Stream-K only, data-parallel waves then stream-K, and the banded tile
-    order, over enough tiles for two or more waves: int32 bit-exact, the
+    """Stream-K only, data-parallel waves then stream-K, the banded tile
+    order and the weight-tile-fastest order, over enough tiles for two or
+    more waves: int32 bit-exact, the
     workspace left zeroed, both split-tile completion routes."""
     M, N, K = 300, 512, 1152
     wq, Qx, sx, tx = _gemm_case(M, N, K, 78)

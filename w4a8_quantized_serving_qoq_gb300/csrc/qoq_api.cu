@@ -52,7 +52,7 @@ int check_options(const qoq_gemm_options *opt) {
     if (opt->num_ctas < 0 || opt->num_ctas > 65536) return QOQ_ERR_UNSUPPORTED;
     if (opt->kernel < 0 || opt->kernel > 3) return QOQ_ERR_UNSUPPORTED;
     if (opt->flags & ~(QOQ_LAUNCH_OVERLAP | QOQ_PLAN_RULES)) return QOQ_ERR_UNSUPPORTED;
-    if (opt->schedule < 0 || opt->schedule > 3) return QOQ_ERR_UNSUPPORTED;
+    if (opt->schedule < 0 || opt->schedule > 4) return QOQ_ERR_UNSUPPORTED;
     return QOQ_OK;
 }
 

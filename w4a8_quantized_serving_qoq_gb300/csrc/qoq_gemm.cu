@@ -980,11 +980,12 @@ GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path, 
     if (pl.tiles < 2 * ctas) sched = 1;  // fewer than two waves: stream-K only
     pl.sched = sched;
     pl.dp_tiles = sched >= 2 ? static_cast<int>((pl.tiles / ctas - 1) * ctas) : 0;
-    // Banded order: bands of about sqrt(P * BT / 32) weight tiles (a weight
+    // Banded order (schedule 3): bands of about sqrt(P * BT / 32) weight tiles (a weight
     // tile moves 64 bytes per k and an activation tile 2 BT, so this minimises
     // the working set band * 64 + (P / band) * 2 BT bytes per k of the tiles
     // the CTAs hold at one time), the bands made about equal.
     pl.band = 0;
+    if (sched == 4) pl.band = pl.n_tiles;  // one band: weight-tile fastest
     if (sched == 3 && pl.tok_tiles > 1) {
         const int b = static_cast<int>(std::lround(std::sqrt(static_cast<double>(ctas) * bt / 32.0)));
         const int nb = (pl.n_tiles + (b < 1 ? 1 : b) - 1) / (b < 1 ? 1 : b);

@@ -105,14 +105,15 @@ struct GemmPlan {
     int gv_csize;          // GEMV path: CTAs per cluster (K split), 1, 2, 4 or 8
     int dp_tiles;          // tensor-core paths: tiles handed out whole, round-robin, before stream-K
     int band;              // weight tiles per band of the tile order (0: token-tile fastest)
-    int sched;             // the schedule chosen: 1, 2 or 3 (as force_sched); 0 on the GEMV path
+    int sched;             // the schedule chosen: 1 to 4 (as force_sched); 0 on the GEMV path
 };
 
 // Kernel path, tile shape and persistent-CTA count for one GEMM.
 // force_path / force_bt / force_ctas (0 = automatic) pin the choice for tests.
 // use_table: consult the measured dispatch table before the rules.
 // force_sched: 0 automatic, 1 stream-K only, 2 data-parallel waves then
-// stream-K (tiles token-tile fastest), 3 as 2 with banded tile order.
+// stream-K (tiles token-tile fastest), 3 as 2 with banded tile order, 4 as 2
+// with the tiles weight-tile fastest.
 GemmPlan plan_gemm(int M, int N, int K, int group, int num_sms, int force_path = 0, int force_bt = 0,
                    int force_ctas = 0, bool use_table = true, int force_sched = 0);
 
