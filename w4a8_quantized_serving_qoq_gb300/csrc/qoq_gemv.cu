@@ -23,9 +23,10 @@
 //    - z * t_x at the end);
 //  * the K dimension is split over the CTAs of a thread-block cluster and over
 //    two warp groups in each CTA; the int32 partial sums are reduced across
-//    the cluster through distributed shared memory, each CTA finishing an
-//    equal share of the tile's rows, so no partial sum leaves the chip and no
-//    workspace round trip or split-tile tail follows;
+//    the cluster through distributed shared memory: each CTA adds its sums
+//    into the CTA that finishes their rows (every CTA finishes an equal share
+//    of the tile's rows), so no partial sum leaves the chip and no workspace
+//    round trip or split-tile tail follows;
 //  * under programmatic dependent launch the weights of the first blocks are
 //    loaded before the wait for the preceding kernel (weights are static).
 #include <cuda.h>
@@ -83,16 +84,20 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// The two halves of a cluster barrier, so that work can run between them.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ int ld_dsmem_s32(const int *local, uint32_t rank) {
+// *local (the same offset in CTA `rank` of the cluster) += v, in that CTA's
+// shared memory.
+__device__ __forceinline__ void red_dsmem_add_s32(int *local, uint32_t rank, int v) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    int v;
-    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
-    return v;
+    asm volatile("red.shared::cluster.add.s32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
 
 // One packed 128 x 128 block as this lane (weight row r) sees it.
@@ -108,12 +113,12 @@ __device__ __forceinline__ void load_block(BlockRegs &br, const uint8_t *blk, in
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kGvThreads, MT <= 4 ? 3 : 2) w4a8_gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(16) uint8_t gv_smem[];
     const int nbm = p.nb_max;
     uint32_t *xs = reinterpret_cast<uint32_t *>(gv_smem);                    // [MT][nbm * 32] words of Qx
     int *gsum = reinterpret_cast<int *>(gv_smem + MT * nbm * 128);           // [MT][nbm]
-    int *part = gsum + MT * nbm;                                             // [2 K halves][MT][128] sums
+    int *part = gsum + MT * nbm;  // [2 K halves][MT][128] sums; with a cluster [MT][128 / csize] totals
     __shared__ int hdr_ok;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -147,6 +152,14 @@ __global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams 
             atomicOr(p.status, kStatusBadPacked);
         }
         return;
+    }
+    const int rows = 128 / p.csize, row0 = static_cast<int>(crank) * rows;  // the tile rows this CTA finishes
+    if (p.csize > 1) {
+        // Every CTA of the cluster adds its sums of this CTA's rows into this
+        // CTA's totals: zero them, and let the peers know (the barrier's
+        // wait comes only before the adds).
+        for (int idx = threadIdx.x; idx < MT * rows; idx += kGvThreads) part[idx] = 0;
+        cluster_arrive();
     }
     // Weights are static: the first two blocks stream in while the preceding
     // kernel finishes.  The loop keeps two blocks in flight ahead of the one
@@ -213,32 +226,39 @@ __global__ void __launch_bounds__(kGvThreads) w4a8_gemv_kernel(const GemvParams 
         nx1 = nx2;
     }
 
-    // ---- the two K halves of every CTA of the cluster publish their sums;
-    // each CTA then finishes an equal share of the tile's rows
+    // ---- reduction of the K split.  With a cluster, each thread adds its
+    // sums into the totals of the CTA that finishes its row (a shared-memory
+    // reduction in that CTA, through distributed shared memory), so after one
+    // barrier every CTA holds the complete sums of its share of the rows.
+    // Without one, the two K halves meet in this CTA's shared memory.
+    if (p.csize > 1) {
+        cluster_wait();  // every CTA of the cluster has zeroed its totals
+        const uint32_t owner = static_cast<uint32_t>(r / rows);
+        const int rr = r % rows;
 #pragma unroll
-    for (int m = 0; m < MT; ++m) part[(half * MT + m) * 128 + r] = acc[m];
-    if (p.csize > 1) cluster_sync();  // every CTA's part[] complete and visible in the cluster
-    else __syncthreads();
-    const int rows = 128 / p.csize, row0 = static_cast<int>(crank) * rows;
+        for (int m = 0; m < MT; ++m)
+            if (m < p.M) red_dsmem_add_s32(part + m * rows + rr, owner, acc[m]);
+        cluster_arrive();
+        cluster_wait();  // every addition into this CTA's totals has landed
+    } else {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) part[(half * MT + m) * 128 + r] = acc[m];
+        __syncthreads();
+    }
     for (int idx = threadIdx.x; idx < MT * rows; idx += kGvThreads) {
-        const int m = idx / rows, rr = row0 + idx % rows;
+        const int m = idx / rows, rl = idx % rows, rr = row0 + rl;
         if (m >= p.M) continue;
-        int tot = part[m * 128 + rr] + part[(MT + m) * 128 + rr];
-        for (int q = 0; q < p.csize; ++q) {
-            if (q == static_cast<int>(crank)) continue;
-            tot += ld_dsmem_s32(part + m * 128 + rr, static_cast<uint32_t>(q));
-            tot += ld_dsmem_s32(part + (MT + m) * 128 + rr, static_cast<uint32_t>(q));
-        }
+        const int tot = p.csize > 1 ? part[m * rows + rl] : part[m * 128 + rr] + part[(MT + m) * 128 + rr];
         const int n = tile * 128 + rr;
-        if (!group) tot -= static_cast<int>(p.packed[packed_z_offset(p.N, p.K) + n]) * p.t_x[m];
+        int res = tot;
+        if (!group) res -= static_cast<int>(p.packed[packed_z_offset(p.N, p.K) + n]) * p.t_x[m];
         const size_t idx_o = static_cast<size_t>(m) * p.N + n;
         if (p.acc_out)
-            p.acc_out[idx_o] = tot;
+            p.acc_out[idx_o] = res;
         else
             p.O[idx_o] = __half_as_ushort(__float2half_rn(
-                __fmul_rn(__fmul_rn(static_cast<float>(tot), h2f_gv(p.s_x[m])), h2f_gv(p.s_w[n]))));
+                __fmul_rn(__fmul_rn(static_cast<float>(res), h2f_gv(p.s_x[m])), h2f_gv(p.s_w[n]))));
     }
-    if (p.csize > 1) cluster_sync();  // peers' shared memory stays alive until every read is done
 }
 
 template <int MT>
