@@ -622,8 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(1, kEpiThreads);  // also: is_last is rewritten by the next split segment
                 if (*abort_flag != 0) break;
             }
-            // Bulk copies read shared memory until they complete: wait before exit.
-            if (et == 0) bulk_wait<0>();
+            // Bulk copies read shared memory until they have read it: wait for that
+            // before exit (their global writes complete on their own, and are
+            // visible to every later grid, a dependent one's dependency wait included).
+            if (et == 0) bulk_wait_read<0>();
             (void)ok;
         }
     } else if (run) {

@@ -694,8 +694,10 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             named_bar_sync(1, kF8EpiThreads);
             if (*abort_flag != 0) break;
         }
-        // Bulk copies read shared memory until they complete: wait before exit.
-        if (et == 0) bulk_wait<0>();
+        // Bulk copies read shared memory until they have read it: wait for that
+        // before exit (their global writes complete on their own, and are
+        // visible to every later grid, a dependent one's dependency wait included).
+        if (et == 0) bulk_wait_read<0>();
     }
 
     tc_fence_before();
