@@ -373,13 +373,15 @@ def gemm_candidates(M, N, K, group, sms):
             if bt == 16 and M > 32:
                 continue
             t = -(-M // bt) * tiles
-            cands += [(2, bt, c) for c in sorted({sms, sms - 8} | ({t} if t <= sms else set()))]
+            # whole-tile multiples below a wave too: fewer CTAs with longer
+            # ranges can beat every SM at these latency-bound sizes
+            cands += [(2, bt, c) for c in sorted({sms, sms - 8} | {t * f for f in (1, 2, 3, 4) if t * f <= sms})]
     cap = 128 if M > 64 else max(16, 1 << (max(M, 1) - 1).bit_length())
     for bt in (16, 32, 64, 128):
         if bt > cap or (M >= 256 and bt < 64):
             continue
         t = -(-M // bt) * tiles
-        cands += [(1, bt, c) for c in sorted({sms} | ({t} if t <= sms else set()))]
+        cands += [(1, bt, c) for c in sorted({sms} | {t * f for f in (1, 2, 3, 4) if t * f <= sms})]
     out = []
     for p_, b_, c_ in cands:
         t = -(-M // max(b_, 1)) * tiles if b_ else 0
