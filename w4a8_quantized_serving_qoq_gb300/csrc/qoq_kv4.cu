@@ -61,6 +61,7 @@ constexpr int kStages = 4;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr uint32_t kStatusBadIndex = 4u;  // a sequence length or page index out of range
+constexpr int kRankMaxB = 256;            // batches up to this size run longest sequence first
 
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 __device__ __forceinline__ uint16_t f2h_rn(float f) { return __half_as_ushort(__float2half_rn(f)); }
@@ -206,7 +207,30 @@ __global__ void __launch_bounds__(kThreads, NSV == 1 ? 4 : 3) kv4_attention_kern
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, h = blockIdx.y;
+    int b = blockIdx.z;
+    if (p.splits == 1 && p.B <= kRankMaxB) {
+        // Launch order longest sequence first: the CTAs are handed to the SMs
+        // in launch order, so each SM's share mixes long and short sequences
+        // (and the SMs that get one CTA more get short ones).  Block z takes
+        // the sequence of rank z in (length descending, index ascending).
+        __shared__ int s_len[kRankMaxB];
+        __shared__ int s_b;
+        for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+            const int Li = p.seq_lens[i];
+            s_len[i] = Li < 0 ? 0 : (Li > p.max_pages * kPageTok ? p.max_pages * kPageTok : Li);
+        }
+        if (threadIdx.x == 0) s_b = b;
+        __syncthreads();
+        for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+            const int Li = s_len[i];
+            int rank = 0;
+            for (int o = 0; o < p.B; ++o) rank += (s_len[o] > Li || (s_len[o] == Li && o < i)) ? 1 : 0;
+            if (rank == static_cast<int>(blockIdx.z)) s_b = i;
+        }
+        __syncthreads();
+        b = s_b;
+    }
     const int G = p.G;
     int L = p.seq_lens[b];
     if (L < 0 || L > p.max_pages * kPageTok) {
