@@ -112,8 +112,14 @@ __device__ __forceinline__ void load_block(BlockRegs &br, const uint8_t *blk, in
     br.meta = group ? ld_stream_u32(blk + kCodeBytes + 4 * r) : 0u;
 }
 
-template <int MT>
-__global__ void __launch_bounds__(kGvThreads, MT <= 4 ? 3 : 2) w4a8_gemv_kernel(const GemvParams p) {
+// kAhead: weight blocks in flight ahead of the one being multiplied (2; or
+// 1 for a single token when each warp has at most two blocks: they are all
+// requested before the dependency wait either way, and the fewer registers
+// let four CTAs share an SM, so the CTAs of a launch fit beside the
+// running one and start early).
+template <int MT, int kAhead>
+__global__ void __launch_bounds__(kGvThreads, (MT == 1 && kAhead == 1) ? 4 : (MT <= 4 ? 3 : 2))
+    w4a8_gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(16) uint8_t gv_smem[];
     const int nbm = p.nb_max;
     uint32_t *xs = reinterpret_cast<uint32_t *>(gv_smem);                    // [MT][nbm * 32] words of Qx
@@ -168,6 +174,7 @@ __global__ void __launch_bounds__(kGvThreads, MT <= 4 ? 3 : 2) w4a8_gemv_kernel(
     BlockRegs cur{}, nx1{}, nx2{};
     if (wb0 < wb1) load_block(cur, tile_base + static_cast<size_t>(wb0) * bb, r, group);
     if (wb0 + 1 < wb1) load_block(nx1, tile_base + static_cast<size_t>(wb0 + 1) * bb, r, group);
+    static_assert(kAhead == 1 || kAhead == 2, "blocks ahead");
     griddep_wait();
     // This CTA's activations [M][nb * 128] into shared memory (tokens >= M read as 0),
     // and per (token, block) the sum of its 128 activations (the bias of the
@@ -194,7 +201,8 @@ __global__ void __launch_bounds__(kGvThreads, MT <= 4 ? 3 : 2) w4a8_gemv_kernel(
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0;
     for (int b = wb0; b < wb1; ++b) {
-        if (b + 2 < wb1) load_block(nx2, tile_base + static_cast<size_t>(b + 2) * bb, r, group);
+        if constexpr (kAhead == 2)
+            if (b + 2 < wb1) load_block(nx2, tile_base + static_cast<size_t>(b + 2) * bb, r, group);
         const int jb = b - kb0;  // block index inside the CTA's activation slice
         const uint32_t s = group ? (cur.meta & 0xffu) : 1u;
         const uint32_t z = group ? ((cur.meta >> 8) & 0xffu) : 0u;
@@ -223,7 +231,11 @@ __global__ void __launch_bounds__(kGvThreads, MT <= 4 ? 3 : 2) w4a8_gemv_kernel(
             for (int m = 0; m < MT; ++m) acc[m] -= 128 * gsum[m * nbm + jb];
         }
         cur = nx1;
-        nx1 = nx2;
+        if constexpr (kAhead == 2) {
+            nx1 = nx2;
+        } else {
+            if (b + 2 < wb1) load_block(nx1, tile_base + static_cast<size_t>(b + 2) * bb, r, group);
+        }
     }
 
     // ---- reduction of the K split.  With a cluster, each thread adds its
@@ -261,7 +273,7 @@ __global__ void __launch_bounds__(kGvThreads, MT <= 4 ? 3 : 2) w4a8_gemv_kernel(
     }
 }
 
-template <int MT>
+template <int MT, int kAhead>
 cudaError_t launch_gemv_mt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
     const int nb_max = (plan.G + plan.gv_csize - 1) / plan.gv_csize;
     const size_t smem = static_cast<size_t>(MT) * nb_max * 128 + static_cast<size_t>(MT) * nb_max * 4 +
@@ -275,7 +287,7 @@ cudaError_t launch_gemv_mt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t
     {
         std::lock_guard<std::mutex> lock(mu);
         if (configured[dev] < smem) {
-            e = cudaFuncSetAttribute(w4a8_gemv_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(w4a8_gemv_kernel<MT, kAhead>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem));
             if (e != cudaSuccess) return e;
             configured[dev] = smem;
@@ -318,17 +330,21 @@ cudaError_t launch_gemv_mt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t
     }
     cfg.attrs = na ? attr : nullptr;
     cfg.numAttrs = static_cast<unsigned>(na);
-    return cudaLaunchKernelEx(&cfg, w4a8_gemv_kernel<MT>, p);
+    return cudaLaunchKernelEx(&cfg, w4a8_gemv_kernel<MT, kAhead>, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stream) {
     switch (plan.BT) {
-        case 1: return launch_gemv_mt<1>(a, plan, stream);
-        case 2: return launch_gemv_mt<2>(a, plan, stream);
-        case 4: return launch_gemv_mt<4>(a, plan, stream);
-        case 8: return launch_gemv_mt<8>(a, plan, stream);
+        case 1: {
+            // at most two blocks per warp (its K half of the CTA's blocks): one ahead suffices
+            const int nb_max = (plan.G + plan.gv_csize - 1) / plan.gv_csize;
+            return (nb_max + 1) / 2 <= 2 ? launch_gemv_mt<1, 1>(a, plan, stream) : launch_gemv_mt<1, 2>(a, plan, stream);
+        }
+        case 2: return launch_gemv_mt<2, 2>(a, plan, stream);
+        case 4: return launch_gemv_mt<4, 2>(a, plan, stream);
+        case 8: return launch_gemv_mt<8, 2>(a, plan, stream);
         default: return cudaErrorInvalidValue;
     }
 }
