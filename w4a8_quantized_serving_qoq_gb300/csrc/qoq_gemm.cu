@@ -468,30 +468,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                             write_block_i32(p, ibuf, m0 + 16 * j, n, zc, tile_sx + 16 * j, tile_tx + 16 * j, sw, ok);
                         }
                     } else {
-                        // fp16 outputs: blocks of 16 tokens x 128 rows staged, then
-                        // one tensor store each (rows past M are clipped by the copy).
+                        // fp16 outputs: blocks of 16 tokens x 128 rows (4 KB each)
+                        // staged four at a time across both staging buffers, then
+                        // one tensor store per block (rows past M are clipped by
+                        // the copy): two barriers per four blocks.
+                        constexpr int kRound = 4;
     #pragma unroll
-                        for (int j = 0; j < NB; ++j) {
-                            if (et == 0) bulk_wait_read<1>();  // the buffer's previous copy has read it
+                        for (int j0 = 0; j0 < NB; j0 += kRound) {
+                            if (et == 0) bulk_wait_read<0>();  // earlier copies have read the staging buffers
                             named_bar_sync(3, kEpiThreads);
-                            const uint32_t buf = smem_u32(stg_base) + (stg_use & 1) * C::kStgBytes;
-                            uint32_t sxv[16], txv[16];
-                            ld_shared_x16(smem_u32(tile_sx + 16 * j), sxv);
-                            ld_shared_x16(smem_u32(tile_tx + 16 * j), txv);
-                            uint16_t o[16];
     #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                o[i] = out_fp16(acc[16 * j + i], zc, static_cast<int>(txv[i]), __uint_as_float(sxv[i]), sw);
+                            for (int jj = 0; jj < kRound; ++jj) {
+                                const int j = j0 + jj;
+                                if (j >= NB) break;
+                                const uint32_t buf = smem_u32(stg_base) + static_cast<uint32_t>(jj) * (C::kStgBytes / 2);
+                                uint32_t sxv[16], txv[16];
+                                ld_shared_x16(smem_u32(tile_sx + 16 * j), sxv);
+                                ld_shared_x16(smem_u32(tile_tx + 16 * j), txv);
+                                uint16_t o[16];
     #pragma unroll
-                            for (int i = 0; i < 16; ++i) st_shared_u16(buf + 2u * (i * kTileN + et), o[i]);
+                                for (int i = 0; i < 16; ++i)
+                                    o[i] = out_fp16(acc[16 * j + i], zc, static_cast<int>(txv[i]), __uint_as_float(sxv[i]), sw);
+    #pragma unroll
+                                for (int i = 0; i < 16; ++i) st_shared_u16(buf + 2u * (i * kTileN + et), o[i]);
+                            }
                             fence_proxy_async_smem();
                             named_bar_sync(3, kEpiThreads);
                             if (et == 0 && *abort_flag == 0) {
-                                tma_store_2d(&o_map, stg_base + (stg_use & 1) * C::kStgBytes, n_tile * kTileN, m0 + 16 * j);
+    #pragma unroll
+                                for (int jj = 0; jj < kRound; ++jj) {
+                                    if (j0 + jj >= NB) break;
+                                    tma_store_2d(&o_map, stg_base + jj * (C::kStgBytes / 2), n_tile * kTileN, m0 + 16 * (j0 + jj));
+                                }
                                 bulk_commit();
                             }
-                            ++stg_use;
                         }
+                        // The other users of the staging buffers take them in turn
+                        // with one copy allowed in flight: leave none.
+                        if (et == 0) bulk_wait_read<0>();
                     }
                 } else {
                     // Split tile: if every other contributor has already published
