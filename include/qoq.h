@@ -57,6 +57,21 @@ const char *qoq_status_string(int status);
 int qoq_version(void);
 
 /*
+ * qoq_bounds_checked -- 1 when this library is the bounds-check build
+ * (compiled with QOQ_DEBUG_BOUNDS; the Python binding loads it when the
+ * environment sets QOQ_DEBUG=1), else 0.  In that build every GEMM kernel
+ * (all three paths) tests, before the access, each weight-block copy, each
+ * split-tile slot and arrival-counter access and each output element it
+ * writes by plain stores, and the KV4 attention each output and split
+ * partial it writes, against the extent of its buffer; an access outside it
+ * is skipped and sets bit 8 of the status word (qoq_workspace_status and
+ * qoq_noalloc_status then return QOQ_ERR_DEVICE).  Results are otherwise
+ * those of the release build.  A debugging aid with no counterpart in the
+ * paper.
+ */
+int qoq_bounds_checked(void);
+
+/*
  * qoq_quantize_weights -- progressive group quantization of fp16 weights on
  * the device ([QS-summary] "渐进式组量化" eq. 4/5 and "保护性量化范围";
  * [QS-review] 3.1).  One-time, load-time operation.
@@ -409,7 +424,9 @@ int qoq_w4a8_gemm_noalloc(const int8_t *Qx, const uint16_t *s_x, const int32_t *
  * qoq_workspace_status).  Synchronizes `stream`, copies the word to
  * *host_status, clears it, and returns QOQ_OK, QOQ_ERR_TIMEOUT or
  * QOQ_ERR_DEVICE by the bits found (1 = a bounded wait expired, 2 =
- * packed-weight header mismatch or illegal codes).  Allocates nothing.  The
+ * packed-weight header mismatch or illegal codes, 8 = bounds-check build
+ * only: an access outside its buffer was skipped; 8 takes precedence over 1).
+ * Allocates nothing.  The
  * paper has no counterpart of it.
  */
 int qoq_noalloc_status(uint32_t *host_status, qoq_stream_t stream);
@@ -498,7 +515,9 @@ int qoq_kv4_decode_attention(const uint16_t *Q, const void *pages, int num_pages
  * word to *host_status, clears it on the device, and returns QOQ_OK,
  * QOQ_ERR_TIMEOUT or QOQ_ERR_DEVICE according to the bits found
  * (1 = a bounded wait expired, 2 = packed-weight header mismatch/illegal,
- * 4 = a KV4 sequence length or page index out of range).
+ * 4 = a KV4 sequence length or page index out of range, 8 = bounds-check
+ * build only: an access outside its buffer was skipped; 8 takes precedence
+ * over 1, whose expired wait it causes).
  */
 int qoq_workspace_status(void *workspace, uint32_t *host_status, qoq_stream_t stream);
 

@@ -19,6 +19,27 @@ def test_exports_every_header_function(lib):
         assert hasattr(lib, n), n
 
 
+def test_loaded_library_matches_request(lib):
+    """QOQ_DEBUG=1 loads the bounds-check build; otherwise the release one."""
+    assert qoq.qoq_bounds_checked() == qoq.debug_build_requested()
+    assert qoq.library_path().endswith("libqoq_debug.so" if qoq.debug_build_requested() else "libqoq.so")
+
+
+def test_bounds_check_build_exports_every_header_function():
+    """The bounds-check library is built beside the release one, exports the
+    same C ABI and says which build it is."""
+    from w4a8_quantized_serving_qoq_gb300 import _build
+    _build.build(debug=True)
+    dbg = ctypes.CDLL(_build.LIB_DEBUG)
+    for n in qoq.header_functions():
+        assert hasattr(dbg, n), n
+    dbg.qoq_bounds_checked.restype = ctypes.c_int
+    assert dbg.qoq_bounds_checked() == 1
+    rel = ctypes.CDLL(_build.LIB)
+    rel.qoq_bounds_checked.restype = ctypes.c_int
+    assert rel.qoq_bounds_checked() == 0
+
+
 def test_status_strings(lib):
     for code, name in qoq.STATUS_NAMES.items():
         assert qoq.qoq_status_string(code) == name

@@ -5,7 +5,9 @@ A thin ctypes binding over ``libqoq.so`` (C ABI declared in
 argument marshalling only: torch tensors provide device memory and the
 current CUDA stream; every step of the computation runs in the library's
 CUDA kernels.  There is no CPU fallback: if the library is missing or fails
-to load, every call raises.
+to load, every call raises.  With QOQ_DEBUG=1 in the environment at the first
+call, the bounds-check build ``libqoq_debug.so`` is loaded instead (see
+qoq_bounds_checked in ``include/qoq.h``).
 """
 from __future__ import annotations
 
@@ -48,12 +50,17 @@ class qoq_gemm_options(ctypes.Structure):
     ]
 
 
+def debug_build_requested() -> bool:
+    """True when QOQ_DEBUG=1 asks for the bounds-check library."""
+    return os.environ.get("QOQ_DEBUG", "") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.library(debug_build_requested())
 
 
 def build(force: bool = False) -> str:
-    """Compile libqoq.so for sm_103a (in-tree)."""
+    """Compile libqoq.so and libqoq_debug.so for sm_103a (in-tree)."""
     return _build.build(force=force)
 
 
@@ -83,13 +90,15 @@ def load():
         return lib
     with _lock:
         if _lib is None:
-            if not _build.up_to_date():
-                _build.build()
-            lib = ctypes.CDLL(_build.LIB)
+            dbg = debug_build_requested()
+            if not _build.up_to_date(dbg):
+                _build.build(debug=dbg)
+            lib = ctypes.CDLL(_build.library(dbg))
             P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
             sigs = {
                 "qoq_status_string": (ctypes.c_char_p, [I]),
                 "qoq_version": (I, []),
+                "qoq_bounds_checked": (I, []),
                 "qoq_quantize_weights": (I, [P, I, I, I, P, P, P, P, P]),
                 "qoq_packed_weight_bytes": (S, [I, I, I]),
                 "qoq_pack_weights": (I, [P, P, P, I, I, I, P, P]),
@@ -190,6 +199,11 @@ def qoq_status_string(status: int) -> str:
 
 def qoq_version() -> int:
     return int(load().qoq_version())
+
+
+def qoq_bounds_checked() -> bool:
+    """True when the loaded library is the bounds-check build."""
+    return bool(load().qoq_bounds_checked())
 
 
 def qoq_quantize_weights(W, group: int = 128, stream=None):
@@ -524,6 +538,7 @@ def qoq_workspace_status(workspace, stream=None):
 
 
 __all__ = [n for n in dir() if n.startswith("qoq_")] + [
-    "QoqError", "build", "load", "library_path", "header_functions", "new_workspace", "gemm_options",
+    "QoqError", "build", "load", "library_path", "debug_build_requested", "header_functions", "new_workspace",
+    "gemm_options",
     "QOQ_LAUNCH_OVERLAP", "QOQ_PLAN_RULES",
 ]

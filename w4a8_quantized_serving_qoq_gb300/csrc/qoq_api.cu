@@ -131,6 +131,14 @@ const char *qoq_status_string(int status) {
 
 int qoq_version(void) { return static_cast<int>(qoq::kPackedVersion); }
 
+int qoq_bounds_checked(void) {
+#ifdef QOQ_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 int qoq_quantize_weights(const uint16_t *W, int N, int K, int group, uint8_t *q4, uint8_t *s_g,
                          uint8_t *z, uint16_t *s_w, qoq_stream_t stream) {
     if (N <= 0 || K <= 0) return QOQ_ERR_INVALID_ARG;
@@ -378,6 +386,7 @@ int qoq_workspace_status(void *workspace, uint32_t *host_status, qoq_stream_t st
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return QOQ_ERR_CUDA;
     *host_status = v;
+    if (v & 8u) return QOQ_ERR_DEVICE;  // bounds-check build: a skipped access, the cause of any expired wait
     if (v & 1u) return QOQ_ERR_TIMEOUT;
     if (v & 6u) return QOQ_ERR_DEVICE;
     return QOQ_OK;

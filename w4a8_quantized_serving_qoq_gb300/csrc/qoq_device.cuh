@@ -13,7 +13,33 @@ namespace qoq {
 enum : uint32_t {
     kStatusTimeout = 1u,       // a bounded wait gave up
     kStatusBadPacked = 2u,     // packed-weight header mismatch or illegal codes
+    kStatusBounds = 8u,        // bounds-check build: an access outside its buffer was skipped
 };
+
+// Bounds-check build (compiled with QOQ_DEBUG_BOUNDS).  Before a global
+// access whose address a kernel computes itself, and that no tensor map
+// clips, the kernel asks in_bounds whether [off, off + n) lies inside
+// [0, extent) (all three in the access's own units).  When it does not, the
+// check ORs kStatusBounds into *status (if not null) and returns false, and
+// the caller skips the access (and, where other roles wait on it, raises the
+// CTA's abort flag).  In the release build the answer is the constant true
+// and the test compiles away.
+#ifdef QOQ_DEBUG_BOUNDS
+constexpr bool kBoundsBuild = true;
+#else
+constexpr bool kBoundsBuild = false;
+#endif
+
+__device__ __forceinline__ bool in_bounds(unsigned long long off, unsigned long long n, unsigned long long extent,
+                                          uint32_t *status) {
+    if constexpr (!kBoundsBuild) {
+        return true;
+    } else {
+        const bool ok = off <= extent && n <= extent - off;
+        if (!ok && status != nullptr) atomicOr(status, kStatusBounds);
+        return ok;
+    }
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

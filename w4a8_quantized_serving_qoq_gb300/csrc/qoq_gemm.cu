@@ -263,6 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             stop = true;
                             break;
                         }
+                        if (!weights_in_bounds(p, kHeaderBytes + (static_cast<unsigned long long>(n_tile) * p.G + k) * bb,
+                                               bb)) {
+                            *abort_flag = 1;
+                            stop = true;
+                            break;
+                        }
                         mbar_arrive_expect_tx(&w_full[slot], bb);
                         tma_load_1d(w_base + slot * kWRawBytes, wblk + static_cast<size_t>(k) * bb, bb, &w_full[slot]);
                         issued = st + 1;
@@ -514,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     named_bar_sync(3, kEpiThreads);
                     if (et == 0) {
                         int f = 0;
+                        if (!slot_in_bounds<BT>(p, slot_idx)) *abort_flag = 1;
                         if (*abort_flag == 0 && !(p.debug_flags & kDebugAlwaysPublish))
                             f = finish_directly(p, cta, slot_idx, tfirst, abort_flag) ? 1 : 0;
                         *fin_flag = f;
@@ -834,6 +841,7 @@ cudaError_t launch_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t stre
     p.band = plan.band;
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
+    set_extents(p, plan, a.N, a.K, a.group);
     dim3 grid(plan.ctas);
     if (a.acc_out)
         return p.group ? launch_kernel(w4a8_gemm_kernel<BT, true, false>, grid, dim3(kThreads), C::kSmemBytes, stream,

@@ -32,7 +32,46 @@ struct GemmParams {
     int band;               // weight tiles per band of the tile order (0: token-tile fastest)
     uint32_t debug_flags;
     uint64_t timeout_ns;
+#ifdef QOQ_DEBUG_BOUNDS
+    // Buffer extents (bounds-check build only: the release kernels keep the
+    // smaller parameter block): bytes of the packed weights, int32 words of
+    // the slot array, arrival counters.
+    unsigned long long packed_bytes, slot_words, n_counters;
+#endif
 };
+
+// The extents above from the workspace layout of a plan (slot array and
+// counters as the plan laid them out, not as the kernel would compute them).
+inline void set_extents(GemmParams &p, const GemmPlan &plan, int N, int K, int group) {
+#ifdef QOQ_DEBUG_BOUNDS
+    p.packed_bytes = packed_bytes(N, K, group);
+    p.n_counters = (plan.slots_offset - plan.counters_offset) / 4;
+    p.slot_words = plan.zero_bytes > plan.slots_offset ? (plan.zero_bytes - plan.slots_offset) / 4 : 0;
+#else
+    (void)p, (void)plan, (void)N, (void)K, (void)group;
+#endif
+}
+
+// Bounds-check build: bytes [off, off + n) of the packed weights.
+__device__ __forceinline__ bool weights_in_bounds(const GemmParams &p, unsigned long long off, unsigned long long n) {
+#ifdef QOQ_DEBUG_BOUNDS
+    return in_bounds(off, n, p.packed_bytes, p.status);
+#else
+    return true;
+#endif
+}
+
+// Bounds-check build: one split tile's slot (all its rows) and its arrival
+// counter.  A failure is recorded by in_bounds; the caller raises the abort.
+template <int BT>
+__device__ __forceinline__ bool slot_in_bounds(const GemmParams &p, int slot_idx) {
+#ifdef QOQ_DEBUG_BOUNDS
+    return in_bounds(static_cast<unsigned long long>(slot_idx) * (BT * kTileN), BT * kTileN, p.slot_words, p.status) &&
+           in_bounds(static_cast<unsigned long long>(slot_idx), 1, p.n_counters, p.status);
+#else
+    return true;
+#endif
+}
 
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
@@ -159,6 +198,7 @@ __device__ __forceinline__ bool finish_directly(const GemmParams &p, int cta, in
 __device__ __forceinline__ void write_out(const GemmParams &p, int m, int n, int acc, int zc, int tx,
                                           float sx, float sw) {
     const size_t idx = static_cast<size_t>(m) * p.N + n;
+    if (!in_bounds(idx, 1, static_cast<unsigned long long>(p.M) * p.N, p.status)) return;
     acc -= zc * tx;
     if (p.acc_out)
         p.acc_out[idx] = acc;

@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             // writes.  Each stage's barrier is armed for all its bytes; the
             // activation operand copies follow after the wait.
             const bool withhold = (p.debug_flags & kDebugWithholdStage) != 0;
-            const int pre_max = withhold ? 1 : R;
+            int pre_max = withhold ? 1 : R;
             int pre = 0;
             {
                 SegmentWalker w0(p, cta);
@@ -255,6 +255,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                     const uint8_t *wrow = p.packed + kHeaderBytes + static_cast<size_t>(n_tile) * p.G * kBlockBytesG;
                     for (int k = s0.k0; k < s0.k1 && pre < pre_max; k += kGroupsPerStage, ++pre) {
                         const int ng = min(kGroupsPerStage, s0.k1 - k);
+                        if (!weights_in_bounds(p, kHeaderBytes + (static_cast<unsigned long long>(n_tile) * p.G + k) * kBlockBytesG,
+                                               static_cast<unsigned long long>(ng) * kBlockBytesG)) {
+                            *abort_flag = 1;
+                            pre_max = pre;  // the main loop stops at this stage
+                            break;
+                        }
                         uint8_t *dst = raw_base + pre * C::kRawSlotBytes;
                         mbar_arrive_expect_tx(&raw_full[pre], ng * kBlockBytesG);
                         tma_load_1d(dst + C::kWOff, wrow + static_cast<size_t>(k) * kBlockBytesG, ng * kBlockBytesG,
@@ -279,6 +285,13 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                         break;
                     }
                     if (withhold && st == 1) {
+                        stop = true;
+                        break;
+                    }
+                    if (st >= pre &&
+                        !weights_in_bounds(p, kHeaderBytes + (static_cast<unsigned long long>(n_tile) * p.G + k) * kBlockBytesG,
+                                           static_cast<unsigned long long>(ng) * kBlockBytesG)) {
+                        *abort_flag = 1;
                         stop = true;
                         break;
                     }
@@ -369,7 +382,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             while (w.next(sg)) last = sg;
             const bool split = last.k1 > last.k0 && !(last.k0 == 0 && last.k1 == p.G);
             const uint32_t tfirst = static_cast<uint32_t>(last.seq) * static_cast<uint32_t>(p.G);
-            if (split && cta_of_stage(tfirst, p) == cta) {
+            if (split && cta_of_stage(tfirst, p) == cta && slot_in_bounds<BT>(p, cta)) {
                 griddep_wait();  // the workspace belongs to the preceding kernel until it completes
                 const uint32_t others = static_cast<uint32_t>(
                     cta_of_stage(tfirst + static_cast<uint32_t>(p.G) - 1u, p) - cta);
@@ -603,6 +616,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 named_bar_sync(3, kF8EpiThreads);
                 if (et == 0) {
                     int f = 0;
+                    if (!slot_in_bounds<BT>(p, slot_idx)) *abort_flag = 1;
                     if (*abort_flag == 0 && !(p.debug_flags & kDebugAlwaysPublish)) {
                         // The tile's first k-stage is in this range only for the
                         // range's last segment.  If the prefetch warp already
@@ -798,6 +812,7 @@ cudaError_t launch_f8_bt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t s
     p.band = plan.band;
     p.debug_flags = a.debug_flags;
     p.timeout_ns = a.timeout_ns;
+    set_extents(p, plan, a.N, a.K, a.group);
     if (a.acc_out)
         return launch_kernel(w4a8_gemm_f8_kernel<BT, true>, dim3(plan.ctas), dim3(kF8Threads), C::kSmemBytes, stream,
                              a.pdl, plane_map, tg_map, o_map, p);

@@ -54,6 +54,9 @@ struct GemvParams {
     int M, N, K, group, G;
     int csize;     // CTAs per cluster: the K split
     int nb_max;    // blocks (128 k) per CTA, at most
+#ifdef QOQ_DEBUG_BOUNDS
+    unsigned long long packed_bytes;  // extent of the packed weights (bounds-check build only)
+#endif
 };
 
 __device__ __forceinline__ float h2f_gv(uint16_t b) { return __half2float(__ushort_as_half(b)); }
@@ -138,7 +141,8 @@ __global__ void __launch_bounds__(kGvThreads, (MT == 1 && kAhead == 1) ? 4 : (MT
     const int kb0 = static_cast<int>(crank) * p.G / p.csize, kb1 = (static_cast<int>(crank) + 1) * p.G / p.csize;
     const int nb = kb1 - kb0;
     const int hmid = kb0 + nb / 2;
-    const int wb0 = half ? hmid : kb0, wb1 = half ? kb1 : hmid;
+    const int wb0 = half ? hmid : kb0;
+    int wb1 = half ? kb1 : hmid;
     const uint8_t *tile_base = p.packed + kHeaderBytes + static_cast<size_t>(tile) * p.G * bb;
 
     // The header is checked before any weight is read (a call whose N or K
@@ -159,6 +163,13 @@ __global__ void __launch_bounds__(kGvThreads, (MT == 1 && kAhead == 1) ? 4 : (MT
         }
         return;
     }
+    // Bounds-check build: a weight range outside the buffer is skipped (the
+    // CTA still takes every cluster barrier, with zero sums).
+#ifdef QOQ_DEBUG_BOUNDS
+    if (!in_bounds(kHeaderBytes + (static_cast<unsigned long long>(tile) * p.G + wb0) * bb,
+                   static_cast<unsigned long long>(wb1 - wb0) * bb, p.packed_bytes, p.status))
+        wb1 = wb0;
+#endif
     const int rows = 128 / p.csize, row0 = static_cast<int>(crank) * rows;  // the tile rows this CTA finishes
     if (p.csize > 1) {
         // Every CTA of the cluster adds its sums of this CTA's rows into this
@@ -265,6 +276,7 @@ __global__ void __launch_bounds__(kGvThreads, (MT == 1 && kAhead == 1) ? 4 : (MT
         int res = tot;
         if (!group) res -= static_cast<int>(p.packed[packed_z_offset(p.N, p.K) + n]) * p.t_x[m];
         const size_t idx_o = static_cast<size_t>(m) * p.N + n;
+        if (!in_bounds(idx_o, 1, static_cast<unsigned long long>(p.M) * p.N, p.status)) continue;
         if (p.acc_out)
             p.acc_out[idx_o] = res;
         else
@@ -309,6 +321,9 @@ cudaError_t launch_gemv_mt(const GemmArgs &a, const GemmPlan &plan, cudaStream_t
     p.G = plan.G;
     p.csize = plan.gv_csize;
     p.nb_max = nb_max;
+#ifdef QOQ_DEBUG_BOUNDS
+    p.packed_bytes = packed_bytes(a.N, a.K, a.group);
+#endif
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.gv_csize, plan.n_tiles);
     cfg.blockDim = dim3(kGvThreads);

@@ -549,10 +549,15 @@ __global__ void __launch_bounds__(kThreads, NSV == 1 ? 4 : 3) kv4_attention_kern
         }
         const size_t hq_idx = static_cast<size_t>(b) * p.hq + h * G + hd;
         if (p.splits == 1) {
+            if (!in_bounds(hq_idx * kHD + d, 1, static_cast<unsigned long long>(p.B) * p.hq * kHD, p.status)) continue;
             p.O[hq_idx * kHD + d] = f2h_rn(Ls > 0.f ? __fdiv_rn(Os, Ls) : 0.f);
         } else {
-            float *part = p.partial + ((static_cast<size_t>(b) * p.hkv + h) * p.splits + split) * G * (2 + kHD) +
-                          hd * (2 + kHD);
+            const size_t part_off =
+                ((static_cast<size_t>(b) * p.hkv + h) * p.splits + split) * G * (2 + kHD) + hd * (2 + kHD);
+            if (!in_bounds(part_off, 2 + kHD,
+                           static_cast<unsigned long long>(p.B) * p.hkv * p.splits * G * (2 + kHD), p.status))
+                continue;
+            float *part = p.partial + part_off;
             if (d == 0) {
                 part[0] = M;
                 part[1] = Ls;

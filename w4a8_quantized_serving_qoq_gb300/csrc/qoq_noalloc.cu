@@ -116,6 +116,7 @@ extern "C" int qoq_noalloc_status(uint32_t *host_status, qoq_stream_t stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return QOQ_ERR_CUDA;
     *host_status = v;
+    if (v & 8u) return QOQ_ERR_DEVICE;  // bounds-check build: a skipped access, the cause of any expired wait
     if (v & 1u) return QOQ_ERR_TIMEOUT;
     if (v & 2u) return QOQ_ERR_DEVICE;
     return QOQ_OK;
