@@ -553,12 +553,16 @@ def main(argv=None):
     if args.impl == "reference":
         run_reference(args, points)
         return
+    import w4a8_quantized_serving_qoq_gb300 as qoq
+    if qoq.debug_build_requested():
+        # The bounds-check library tests its accesses: its times are not the product's.
+        raise SystemExit("bench.py times the release library: unset QOQ_DEBUG (QOQ_DEBUG=1 selects the "
+                         "bounds-check build)")
     if args.tune:
         run_tune(args)
         return
 
     import torch
-    import w4a8_quantized_serving_qoq_gb300 as qoq
     from w4a8_quantized_serving_qoq_gb300 import roofline
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -30,3 +30,14 @@ def test_reference_arm_prints_one_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == "TOPS"
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_gpu_arm_refuses_the_bounds_check_build():
+    """QOQ_DEBUG=1 selects the bounds-check library, whose times are not the
+    product's: the GPU arm exits with an error before timing anything."""
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    env["QOQ_DEBUG"] = "1"
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "1", "--warmup", "0"],
+                         env=env, capture_output=True, text=True, timeout=300)
+    assert out.returncode != 0
+    assert "QOQ_DEBUG" in out.stderr and not out.stdout.strip()
