@@ -305,7 +305,9 @@ int qoq_w4a8_gemm_i32(const int8_t *Qx, const int32_t *t_x, const void *packed, 
  *                     codes and split activations as exact e4m3, group 128
  *                     only, tokens_per_tile 16 or 32), 3 = CUDA-core dp4a
  *                     path (M <= 8; num_ctas = the K split, a thread-block
- *                     cluster of 1, 2, 4 or 8 CTAs per 128-row tile; no
+ *                     cluster of 1, 2, 4 or 8 CTAs per 128-row tile, raised
+ *                     to the next of those sizes while one CTA's slice of
+ *                     the activations would not fit in shared memory; no
  *                     activation operand).  Automatic: the measured dispatch
  *                     table for the shape, else dp4a up to 4 tokens, fp8 up
  *                     to 32 (g128), fp16 above.
